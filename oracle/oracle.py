@@ -1,0 +1,260 @@
+"""ctypes wrapper around the plain C oracle (``moe_oracle.c``).
+
+TEST INFRASTRUCTURE.  Only the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` import this module.  It shares
+nothing with the CUDA library: it builds and loads its own ``libmoe_oracle.so``
+from ``moe_oracle.c`` and never imports the product package.
+
+Arrays are numpy arrays.  16-bit floating point tensors travel as their raw
+bits: ``np.float16`` arrays or ``np.uint16`` bit arrays together with a dtype
+name (``"f16"``, ``"bf16"``); fp32 tensors as ``np.float32``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB = os.path.join(_HERE, "libmoe_oracle.so")
+
+DTYPE_CODES = {"f16": 0, "bf16": 1, "f32": 2}
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``libmoe_oracle.so`` next to its source (gcc, strict fp)."""
+    with _lock:
+        stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+        if force or stale:
+            tmp = _LIB + f".tmp{os.getpid()}"
+            cmd = ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                   "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB)
+    P = ctypes.c_void_p
+    I64 = ctypes.c_int64
+    I = ctypes.c_int
+    sig = {
+        "oracle_decode": (None, [P, I, I64, P]),
+        "oracle_encode": (None, [P, I, I64, P]),
+        "oracle_resolve_threads": (I, [I]),
+        "oracle_gate_logits": (I, [P, P, P, I64, I64, I64, I, P, I]),
+        "oracle_topk_softmax": (I, [P, I64, I64, I64, P, P]),
+        "oracle_num_m_blocks": (I64, [I64, I64, I64, I64]),
+        "oracle_build_dispatch": (I, [P, P, I64, I64, I64, I64, P, P, P, P, I64, P, P, P]),
+        "oracle_gather_rows": (I, [P, P, I64, I64, I64, I, P]),
+        "oracle_grouped_gate_up_silu": (I, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I64, I, P, I]),
+        "oracle_grouped_down": (I, [P, P, P, P, P, P, I64, I64, P, I64, I64, I64, I64, I, P, I]),
+        "oracle_reduce_fused": (I, [P, I64, P, P, I64, I64, I64, I, I, P, P, I]),
+        "oracle_moe_tokens_dense": (I, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I64, I, P, I]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _bits(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Contiguous storage array for ``dtype`` (uint16 bits for f16/bf16)."""
+    if dtype == "f32":
+        return np.ascontiguousarray(a, dtype=np.float32)
+    if a.dtype == np.float16:
+        if dtype != "f16":
+            raise ValueError("np.float16 array passed as bf16")
+        return np.ascontiguousarray(a).view(np.uint16)
+    if a.dtype in (np.uint16, np.int16):
+        return np.ascontiguousarray(a).view(np.uint16)
+    raise TypeError(f"expected 16-bit storage for {dtype}, got {a.dtype}")
+
+
+def _empty(shape, dtype: str) -> np.ndarray:
+    return np.empty(shape, dtype=np.float32 if dtype == "f32" else np.uint16)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle {what}: invalid arguments (rc={rc})")
+
+
+def threads(n: int = 0) -> int:
+    return _load().oracle_resolve_threads(n)
+
+
+def decode(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Storage values -> fp32 (exact widening)."""
+    src = _bits(a, dtype)
+    out = np.empty(src.shape, dtype=np.float32)
+    _load().oracle_decode(_ptr(src), DTYPE_CODES[dtype], src.size, _ptr(out))
+    return out
+
+
+def encode(a: np.ndarray, dtype: str) -> np.ndarray:
+    """fp32 -> storage bits, round-to-nearest-even."""
+    src = np.ascontiguousarray(a, dtype=np.float32)
+    out = _empty(src.shape, dtype)
+    _load().oracle_encode(_ptr(src), DTYPE_CODES[dtype], src.size, _ptr(out))
+    return out
+
+
+def gate_logits(x, wg, bias, dtype: str, nthreads: int = 0) -> np.ndarray:
+    xb, wb = _bits(x, dtype), _bits(wg, dtype)
+    T, d_h = xb.shape
+    E = wb.shape[0]
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    out = np.empty((T, E), dtype=np.float32)
+    _check(_load().oracle_gate_logits(_ptr(xb), _ptr(wb), _ptr(b), T, d_h, E,
+                                      DTYPE_CODES[dtype], _ptr(out), nthreads), "gate_logits")
+    return out
+
+
+def topk_softmax(logits: np.ndarray, k: int):
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = lg.shape
+    idx = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float32)
+    _check(_load().oracle_topk_softmax(_ptr(lg), T, E, k, _ptr(idx), _ptr(w)), "topk_softmax")
+    return idx, w
+
+
+def gate_topk(x, wg, bias, k: int, dtype: str, nthreads: int = 0):
+    return topk_softmax(gate_logits(x, wg, bias, dtype, nthreads), k)
+
+
+def num_m_blocks(T: int, k: int, E: int, block_m: int = 128) -> int:
+    return int(_load().oracle_num_m_blocks(T, k, E, block_m))
+
+
+def build_dispatch(topk_idx: np.ndarray, topk_w, E: int, block_m: int = 128) -> dict:
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, k = idx.shape
+    w = None if topk_w is None else np.ascontiguousarray(topk_w, dtype=np.float32)
+    mb = num_m_blocks(T, k, E, block_m)
+    out = {
+        "group_sizes": np.empty(E, np.int32),
+        "group_offsets": np.empty(E, np.int32),
+        "group_padded_offsets": np.empty(E, np.int32),
+        "group_idx_for_bx": np.empty(mb, np.int32),
+        "sorted_token_idx": np.empty(T * k, np.int32),
+        "sorted_row_weight": np.empty(T * k, np.float32),
+        "token_topk_to_pos": np.empty((T, k), np.int32),
+    }
+    _check(_load().oracle_build_dispatch(
+        _ptr(idx), _ptr(w), T, k, E, block_m, _ptr(out["group_sizes"]), _ptr(out["group_offsets"]),
+        _ptr(out["group_padded_offsets"]), _ptr(out["group_idx_for_bx"]), mb,
+        _ptr(out["sorted_token_idx"]), _ptr(out["sorted_row_weight"]),
+        _ptr(out["token_topk_to_pos"])), "build_dispatch")
+    return out
+
+
+def gather_rows(x, sorted_token_idx, dtype: str) -> np.ndarray:
+    xb = _bits(x, dtype)
+    T, d_h = xb.shape
+    st = np.ascontiguousarray(sorted_token_idx, dtype=np.int32)
+    out = _empty((st.size, d_h), dtype)
+    _check(_load().oracle_gather_rows(_ptr(xb), _ptr(st), st.size, T, d_h,
+                                      DTYPE_CODES[dtype], _ptr(out)), "gather_rows")
+    return out
+
+
+def _tables(t: dict):
+    return [np.ascontiguousarray(t[n], dtype=np.int32) for n in
+            ("group_sizes", "group_offsets", "group_padded_offsets", "group_idx_for_bx")]
+
+
+def grouped_gate_up_silu(a, w_gate, w_up, tables: dict, dtype: str, block_m: int = 128,
+                         nthreads: int = 0) -> np.ndarray:
+    ab, wg, wu = _bits(a, dtype), _bits(w_gate, dtype), _bits(w_up, dtype)
+    n_rows, d_h = ab.shape
+    E, d_e, _ = wg.shape
+    s, o, p, g = _tables(tables)
+    h = _empty((n_rows, d_e), dtype)
+    _check(_load().oracle_grouped_gate_up_silu(
+        _ptr(ab), _ptr(wg), _ptr(wu), _ptr(s), _ptr(o), _ptr(p), _ptr(g), g.size, block_m,
+        n_rows, d_h, d_e, E, DTYPE_CODES[dtype], _ptr(h), nthreads), "grouped_gate_up_silu")
+    return h
+
+
+def grouped_down(h, w_down, tables: dict, dtype: str, row_weights=None, block_m: int = 128,
+                 nthreads: int = 0) -> np.ndarray:
+    hb, wd = _bits(h, dtype), _bits(w_down, dtype)
+    n_rows, d_e = hb.shape
+    E, d_h, _ = wd.shape
+    s, o, p, g = _tables(tables)
+    rw = None if row_weights is None else np.ascontiguousarray(row_weights, dtype=np.float32)
+    y = _empty((n_rows, d_h), dtype)
+    _check(_load().oracle_grouped_down(
+        _ptr(hb), _ptr(wd), _ptr(s), _ptr(o), _ptr(p), _ptr(g), g.size, block_m, _ptr(rw),
+        n_rows, d_h, d_e, E, DTYPE_CODES[dtype], _ptr(y), nthreads), "grouped_down")
+    return y
+
+
+def reduce_fused(x, token_topk_to_pos, topk_weights, in_dtype: str, out_dtype: str,
+                 nthreads: int = 0):
+    """Returns (out, err_flag)."""
+    pos = np.ascontiguousarray(token_topk_to_pos, dtype=np.int32)
+    T, K = pos.shape
+    xb = _bits(x, in_dtype)
+    n_rows, H = xb.shape
+    w = None if topk_weights is None else np.ascontiguousarray(topk_weights, dtype=np.float32)
+    out = _empty((T, H), out_dtype)
+    err = np.zeros(1, np.int32)
+    _check(_load().oracle_reduce_fused(_ptr(xb), n_rows, _ptr(pos), _ptr(w), T, K, H,
+                                       DTYPE_CODES[in_dtype], DTYPE_CODES[out_dtype], _ptr(out),
+                                       _ptr(err), nthreads), "reduce_fused")
+    return out, int(err[0])
+
+
+def moe_tokens_dense(x, w_gate, w_up, w_down, topk_idx, topk_w, tokens, dtype: str,
+                     nthreads: int = 0) -> np.ndarray:
+    """Brute-force forward of the listed tokens, no dispatch tables involved."""
+    xb = _bits(x, dtype)
+    wg, wu, wd = _bits(w_gate, dtype), _bits(w_up, dtype), _bits(w_down, dtype)
+    T, d_h = xb.shape
+    E, d_e, _ = wg.shape
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    w = np.ascontiguousarray(topk_w, dtype=np.float32)
+    k = idx.shape[1]
+    tok = np.ascontiguousarray(tokens, dtype=np.int32)
+    out = _empty((tok.size, d_h), dtype)
+    _check(_load().oracle_moe_tokens_dense(
+        _ptr(xb), _ptr(wg), _ptr(wu), _ptr(wd), _ptr(idx), _ptr(w), _ptr(tok), tok.size, T, d_h,
+        d_e, E, k, DTYPE_CODES[dtype], _ptr(out), nthreads), "moe_tokens_dense")
+    return out
+
+
+def moe_forward(x, wg, bias, w_gate, w_up, w_down, k: int, dtype: str, block_m: int = 128,
+                nthreads: int = 0) -> dict:
+    """The whole path through the dispatch tables: gate, top-k, tables, gather,
+    stage 1, stage 2 and the fp32 combine.  Returns every intermediate."""
+    E = _bits(wg, dtype).shape[0]
+    logits = gate_logits(x, wg, bias, dtype, nthreads)
+    idx, w = topk_softmax(logits, k)
+    tab = build_dispatch(idx, w, E, block_m)
+    a = gather_rows(x, tab["sorted_token_idx"], dtype)
+    h = grouped_gate_up_silu(a, w_gate, w_up, tab, dtype, block_m, nthreads)
+    y = grouped_down(h, w_down, tab, dtype, None, block_m, nthreads)
+    out, err = reduce_fused(y, tab["token_topk_to_pos"], w, dtype, dtype, nthreads)
+    res = dict(tab)
+    res.update(logits=logits, topk_idx=idx, topk_w=w, a=a, h=h, y=y, out=out, err=err)
+    return res
