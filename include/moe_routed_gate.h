@@ -1,0 +1,212 @@
+/*
+ * moe_routed_gate.h -- C-ABI of the GB300 (sm_103a) routed-expert MoE forward.
+ *
+ * The forward of one DeepSeek-style MoE layer's routed experts:
+ *   gate logits -> softmax / top-k -> counting-sort dispatch (four tables plus
+ *   the sorted token-index and row-weight arrays, every expert padded to
+ *   block_m = 128 rows) -> grouped gate/up GEMM with SiLU(gate)*up fused ->
+ *   grouped down GEMM -> moe_reduce_fused combine.
+ * Sources: the CSDN article "tilelang baseline" of the tilelang-metax MoE
+ * contest operator (sections "forward", "stage 1 gate+up", "stage 2 down"),
+ * the TileLang tutorial ch.18 skeletons.py (moe_routed_kernel: the dispatch
+ * contract) and TileOPs-Metax PR #55 (moe_reduce_fused, sections 1-3).
+ *
+ * Conventions for every entry point:
+ *   - Pointers are caller-owned DEVICE memory unless stated otherwise; the
+ *     library never allocates device memory.  Inputs are read only; outputs
+ *     are fully overwritten (rows/elements the operation defines).
+ *   - Tensors are dense, row-major, and 16-byte aligned.  Stacked expert
+ *     weights use the nn.Linear (out x in) layout of the pages:
+ *     W_gate, W_up [E, d_expert, d_hidden]; W_down [E, d_hidden, d_expert].
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous: no host synchronisation and no
+ *     device-to-host copy happens inside any call.
+ *   - Arguments are validated on the host before anything is launched; a bad
+ *     argument returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *     MOE_ERR_WORKSPACE and launches nothing.  A launch failure returns
+ *     MOE_ERR_CUDA.  Conditions only the device can see (a combine position
+ *     out of range, a pipeline wait that timed out) are written as a non-zero
+ *     code into the optional `err_flag` word, which the caller reads after
+ *     synchronising; kernels never trap.
+ *   - Sizes are int64_t element counts; T = tokens, k = top-k, E = experts,
+ *     Tk = T*k token-expert pairs, d_h = d_hidden, d_e = d_expert.
+ */
+#ifndef MOE_ROUTED_GATE_H
+#define MOE_ROUTED_GATE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* identical to cudaStream_t */
+
+typedef enum { MOE_F16 = 0, MOE_BF16 = 1, MOE_F32 = 2 } moe_dtype_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1, /* null pointer, bad size, k > E, misaligned, ... */
+    MOE_ERR_UNSUPPORTED = 2, /* a dtype or shape combination this build does not run */
+    MOE_ERR_WORKSPACE = 3,   /* workspace smaller than the *_workspace_bytes answer */
+    MOE_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+    MOE_ERR_DEVICE_FLAG = 5, /* (err_flag value) a combine position was out of range */
+    MOE_ERR_TIMEOUT = 6      /* (err_flag value) a device pipeline wait gave up */
+} moe_status_t;
+
+/* Block height of the dispatch padding and of the grouped GEMM tiles. */
+#define MOE_BLOCK_M 128
+
+/* Human-readable name of a status code.  Never NULL. */
+MOE_API const char *moe_status_string(int status);
+
+/* Number of M blocks of the padded token space: ceil(T*k / block_m) + E
+ * (CSDN "forward": M = ceil(B*S*top_k / block_token) + n_routed_experts;
+ * skeletons.py moe_routed_kernel: m_blocks).  Returns -1 on bad arguments. */
+MOE_API int64_t moe_num_m_blocks(int64_t T, int64_t k, int64_t E, int64_t block_m);
+
+/* Workspace sizes in bytes (0 means none is needed; -1 cast to size_t on bad args). */
+MOE_API size_t moe_gate_topk_workspace_bytes(int64_t T, int64_t E);
+MOE_API size_t moe_build_dispatch_workspace_bytes(int64_t T, int64_t k, int64_t E);
+MOE_API size_t moe_forward_workspace_bytes(int64_t T, int64_t d_h, int64_t d_e, int64_t E, int64_t k,
+                                   moe_dtype_t dtype);
+
+/*
+ * Gate and routing (CSDN "forward", step 1: expert_indices, expert_scores =
+ * gating_network(x); the gate body is not printed on the pages).
+ *   logits[t,e] = sum_j x[t,j] * w_g[e,j] (+ bias[e]) in fp32.  The sum order is
+ *   fixed: lane L = (j/8) mod 32 accumulates its 8-element chunks in ascending
+ *   j with fmaf, then the 32 partials are combined by the xor butterfly
+ *   s = 16, 8, 4, 2, 1; this makes the routing reproducible bit for bit.
+ *   topk_idx[t, 0..k-1]: the k largest logits, descending, ties to the lower id.
+ *   topk_w[t, j] = softmax over all E logits at topk_idx[t, j] (no renormalisation).
+ * x [T, d_h] and w_g [E, d_h] in `dtype` (f16 or bf16); bias [E] fp32 or NULL.
+ * Requires d_h % 256 == 0, 1 <= k <= min(E, 32), E <= 1024.
+ * ws: moe_gate_topk_workspace_bytes(T, E) bytes of scratch (the fp32 logits).
+ */
+MOE_API moe_status_t moe_gate_topk(const void *x, const void *w_g, const float *bias, int64_t T,
+                           int64_t d_h, int64_t E, int64_t k, moe_dtype_t dtype,
+                           int32_t *topk_idx, float *topk_w, void *ws, size_t ws_bytes,
+                           moe_stream_t stream);
+
+/*
+ * Counting-sort dispatch (CSDN "forward", steps 2-5; skeletons.py docstring:
+ * the kernel takes four tables and looks up per block which rows it owns).
+ *   group_sizes[e]          = #pairs routed to e            (bincount, minlength E)
+ *   group_offsets[e]        = exclusive prefix sum of group_sizes
+ *   group_padded_offsets[e] = padded start: po[0] = 0,
+ *                             po[i] = po[i-1] + ceil((c[i-1] + 1) / block_m) * block_m
+ *   group_idx_for_bx[bx]    = last e with bx*block_m >= po[e], bx < moe_num_m_blocks
+ *   The pairs f = t*k + j are sorted by expert, stably (ascending f inside an
+ *   expert): row r = group_offsets[e] + rank; sorted_token_idx[r] = t,
+ *   sorted_row_weight[r] = topk_w[f] (1 when topk_w is NULL),
+ *   token_topk_to_pos[f] = r.
+ * topk_idx [T,k] int32 with values in [0, E) (others give undefined tables);
+ * outputs sized [E], [E], [E], [M_blk], [Tk], [Tk], [Tk].  block_m must be 128.
+ * ws: moe_build_dispatch_workspace_bytes(T, k, E) bytes of scratch.
+ */
+MOE_API moe_status_t moe_build_dispatch(const int32_t *topk_idx, const float *topk_w, int64_t T,
+                                int64_t k, int64_t E, int64_t block_m, int32_t *group_sizes,
+                                int32_t *group_offsets, int32_t *group_padded_offsets,
+                                int32_t *group_idx_for_bx, int32_t *sorted_token_idx,
+                                float *sorted_row_weight, int32_t *token_topk_to_pos, void *ws,
+                                size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Row gather (CSDN "forward", step 3: stacked_expert_tokens[r] = x_flat[token of r]).
+ *   a_out[r, :] = x[sorted_token_idx[r], :] for r < n_rows.  x [T, d_h].
+ * sorted_token_idx values must lie in [0, T).  d_h * elem_size % 16 == 0.
+ */
+MOE_API moe_status_t moe_gather_rows(const void *x, const int32_t *sorted_token_idx, int64_t n_rows,
+                             int64_t T, int64_t d_h, moe_dtype_t dtype, void *a_out,
+                             moe_stream_t stream);
+
+/*
+ * Grouped gate/up GEMM with fused SiLU (CSDN "tilelang kernel stage 1 gate+up";
+ * skeletons.py moe_routed_kernel first kernel).  For each M block bx:
+ *   g = group_idx_for_bx[bx]; m_start = bx*128 - group_padded_offsets[g] + group_offsets[g];
+ *   rows = clamp(group_sizes[g] - (bx*128 - group_padded_offsets[g]), 0, 128);
+ *   h[m_start + i, :] = silu(A_i W_gate[g]^T) * (A_i W_up[g]^T), i < rows,
+ * fp32 accumulation on the tensor cores, rounded once to `dtype`.
+ * a [n_rows, d_h]; w_gate, w_up [E, d_e, d_h]; h [n_rows, d_e]; tables as produced
+ * by moe_build_dispatch for (T, k) with T*k == n_rows.  dtype f16 or bf16;
+ * d_h % 64 == 0, d_e % 64 == 0.  Rows of h outside the tables' rows are not written.
+ * err_flag: optional device int32, set to MOE_ERR_TIMEOUT if a pipeline wait gives up.
+ */
+MOE_API moe_status_t moe_grouped_gate_up_silu(const void *a, const void *w_gate, const void *w_up,
+                                      const int32_t *group_sizes, const int32_t *group_offsets,
+                                      const int32_t *group_padded_offsets,
+                                      const int32_t *group_idx_for_bx, int64_t m_blocks,
+                                      int64_t n_rows, int64_t d_h, int64_t d_e, int64_t E,
+                                      moe_dtype_t dtype, void *h, int32_t *err_flag,
+                                      moe_stream_t stream);
+
+/*
+ * Grouped down GEMM (CSDN "tilelang kernel stage 2 down"; skeletons.py second
+ * kernel).  Same block lookup; y[m_start + i, :] = (h_i W_down[g]^T) * rw_i,
+ * rw_i = row_weights[m_start + i] when row_weights is non-NULL, else 1 (the
+ * forward applies the routing weight once, in the combine).  fp32 accumulation,
+ * rounded once to `dtype`.  h [n_rows, d_e]; w_down [E, d_h, d_e]; y [n_rows, d_h].
+ * d_h % 256 == 0, d_e % 64 == 0.
+ */
+MOE_API moe_status_t moe_grouped_down(const void *h, const void *w_down, const int32_t *group_sizes,
+                              const int32_t *group_offsets, const int32_t *group_padded_offsets,
+                              const int32_t *group_idx_for_bx, int64_t m_blocks,
+                              const float *row_weights, int64_t n_rows, int64_t d_h,
+                              int64_t d_e, int64_t E, moe_dtype_t dtype, void *y,
+                              int32_t *err_flag, moe_stream_t stream);
+
+/*
+ * moe_reduce_fused (TileOPs-Metax PR #55, section 1): for every token t and
+ * hidden element h,
+ *   out[t, h] = cast( sum over k ascending with 0 <= pos[t,k] < n_rows of
+ *                     w[t,k] * x[pos[t,k], h] )
+ * accumulated in fp32 as acc = acc + (w * x) starting from +0, cast once.
+ * pos = token_topk_to_pos [T, K] int32, -1 marks a padding slot (skipped);
+ * w = topk_weights [T, K] fp32, or NULL for unit weights.  x [n_rows, H].
+ * Requires H % 256 == 0 (the page's check).  Dtypes: in == out (f16, bf16,
+ * f32), or f32 in with f16/bf16 out.  A pos < -1 or >= n_rows is skipped and
+ * sets *err_flag = MOE_ERR_DEVICE_FLAG when err_flag is non-NULL.
+ */
+MOE_API moe_status_t moe_reduce_fused(const void *x, int64_t n_rows, const int32_t *token_topk_to_pos,
+                              const float *topk_weights, int64_t T, int64_t K, int64_t H,
+                              moe_dtype_t in_dtype, moe_dtype_t out_dtype, void *out,
+                              int32_t *err_flag, moe_stream_t stream);
+
+/*
+ * The whole routed forward, stream ordered, no host round trip:
+ *   moe_gate_topk -> moe_build_dispatch -> moe_gather_rows ->
+ *   moe_grouped_gate_up_silu -> moe_grouped_down -> moe_reduce_fused.
+ * x [T, d_h]; w_g [E, d_h]; bias [E] fp32 or NULL; w_gate/w_up [E, d_e, d_h];
+ * w_down [E, d_h, d_e]; out [T, d_h]; all in `dtype` (f16 or bf16).
+ * ws: moe_forward_workspace_bytes(...) bytes, 256-byte aligned; it holds every
+ * intermediate (routing, tables, gathered rows, h, y) and is not read before
+ * being written, so it needs no clearing.  err_flag: optional device int32.
+ */
+MOE_API moe_status_t moe_forward(const void *x, const void *w_g, const float *bias, const void *w_gate,
+                         const void *w_up, const void *w_down, int64_t T, int64_t d_h,
+                         int64_t d_e, int64_t E, int64_t k, moe_dtype_t dtype, void *ws,
+                         size_t ws_bytes, void *out, int32_t *err_flag, moe_stream_t stream);
+
+/*
+ * Offsets (bytes from the workspace start) of moe_forward's intermediates, for
+ * inspection after a call: index 0 logits, 1 topk_idx, 2 topk_w, 3 group_sizes,
+ * 4 group_offsets, 5 group_padded_offsets, 6 group_idx_for_bx,
+ * 7 sorted_token_idx, 8 sorted_row_weight, 9 token_topk_to_pos, 10 dispatch
+ * scratch, 11 gathered rows A, 12 h, 13 y.  Returns -1 for a bad index.
+ */
+MOE_API int64_t moe_forward_workspace_offset(int64_t T, int64_t d_h, int64_t d_e, int64_t E, int64_t k,
+                                     moe_dtype_t dtype, int index);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTED_GATE_H */

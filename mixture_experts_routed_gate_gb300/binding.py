@@ -1,0 +1,332 @@
+"""Thin Python binding of ``libmoe_routed_gb300.so`` (argument marshalling only).
+
+Every function here has the name of the C-ABI entry point it calls, takes
+CUDA tensors, checks their dtype/shape/contiguity, and passes raw pointers and
+``torch.cuda.current_stream()`` to the library.  All computation happens in
+the library's kernels; there is no fallback: if the library is missing or a
+call fails, a ``MoEError`` is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+_DT = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
+_DT_NAME = {0: "f16", 1: "bf16", 2: "f32"}
+_lib = None
+
+BLOCK_M = 128
+WS_NAMES = ["logits", "topk_idx", "topk_w", "group_sizes", "group_offsets",
+            "group_padded_offsets", "group_idx_for_bx", "sorted_token_idx", "sorted_row_weight",
+            "token_topk_to_pos", "dispatch_scratch", "a", "h", "y"]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        msg = lib().moe_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{what}: {msg}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load the CUDA library (build it first with ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build the CUDA library first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(path)
+    P, I64, SZ, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+    sigs = {
+        "moe_status_string": (ctypes.c_char_p, [I]),
+        "moe_num_m_blocks": (I64, [I64, I64, I64, I64]),
+        "moe_gate_topk_workspace_bytes": (SZ, [I64, I64]),
+        "moe_build_dispatch_workspace_bytes": (SZ, [I64, I64, I64]),
+        "moe_forward_workspace_bytes": (SZ, [I64, I64, I64, I64, I64, I]),
+        "moe_forward_workspace_offset": (I64, [I64, I64, I64, I64, I64, I, I]),
+        "moe_gate_topk": (I, [P, P, P, I64, I64, I64, I64, I, P, P, P, SZ, P]),
+        "moe_build_dispatch": (I, [P, P, I64, I64, I64, I64, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_gather_rows": (I, [P, P, I64, I64, I64, I, P, P]),
+        "moe_grouped_gate_up_silu": (I, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, P, P]),
+        "moe_grouped_down": (I, [P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I, P, P, P]),
+        "moe_reduce_fused": (I, [P, I64, P, P, I64, I64, I64, I, I, P, P, P]),
+        "moe_forward": (I, [P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, SZ, P, P, P]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def exported_symbols():
+    return ["moe_status_string", "moe_num_m_blocks", "moe_gate_topk_workspace_bytes",
+            "moe_build_dispatch_workspace_bytes", "moe_forward_workspace_bytes",
+            "moe_forward_workspace_offset", "moe_gate_topk", "moe_build_dispatch",
+            "moe_gather_rows", "moe_grouped_gate_up_silu", "moe_grouped_down",
+            "moe_reduce_fused", "moe_forward"]
+
+
+# --------------------------------------------------------------------------- helpers
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(dev):
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _cuda(t, name, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return t
+
+
+def _dtype_code(t, name):
+    if t.dtype not in _DT:
+        raise TypeError(f"{name}: unsupported dtype {t.dtype}")
+    return _DT[t.dtype]
+
+
+def _check(status, what):
+    if status != 0:
+        raise MoEError(status, what)
+
+
+def num_m_blocks(T: int, k: int, E: int, block_m: int = BLOCK_M) -> int:
+    return int(lib().moe_num_m_blocks(T, k, E, block_m))
+
+
+moe_num_m_blocks = num_m_blocks
+
+
+# --------------------------------------------------------------------------- entry points
+
+def moe_gate_topk(x, w_g, bias, k: int, topk_idx=None, topk_w=None, ws=None):
+    """Routing: returns (topk_idx [T,k] int32, topk_w [T,k] fp32)."""
+    _cuda(x, "x", ndim=2)
+    _cuda(w_g, "w_g", dtype=x.dtype, ndim=2)
+    T, d_h = x.shape
+    E = w_g.shape[0]
+    if w_g.shape[1] != d_h:
+        raise ValueError("w_g must be [E, d_hidden]")
+    if bias is not None:
+        _cuda(bias, "bias", dtype=torch.float32, ndim=1)
+        if bias.numel() != E:
+            raise ValueError("bias must be [E]")
+    dev = x.device
+    if topk_idx is None:
+        topk_idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    _cuda(topk_idx, "topk_idx", dtype=torch.int32)
+    _cuda(topk_w, "topk_w", dtype=torch.float32)
+    need = lib().moe_gate_topk_workspace_bytes(T, E)
+    if ws is None:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().moe_gate_topk(_ptr(x), _ptr(w_g), _ptr(bias), T, d_h, E, k,
+                                   _dtype_code(x, "x"), _ptr(topk_idx), _ptr(topk_w), _ptr(ws),
+                                   ws.numel() * ws.element_size(), _stream(dev)), "moe_gate_topk")
+    return topk_idx, topk_w
+
+
+def moe_build_dispatch(topk_idx, topk_w, E: int, block_m: int = BLOCK_M, out=None, ws=None):
+    """Dispatch tables: returns a dict of device tensors (names as in the C-ABI)."""
+    _cuda(topk_idx, "topk_idx", dtype=torch.int32, ndim=2)
+    T, k = topk_idx.shape
+    if topk_w is not None:
+        _cuda(topk_w, "topk_w", dtype=torch.float32)
+        if topk_w.shape != topk_idx.shape:
+            raise ValueError("topk_w must match topk_idx")
+    dev = topk_idx.device
+    mb = num_m_blocks(T, k, E, block_m)
+    if out is None:
+        i32 = dict(dtype=torch.int32, device=dev)
+        out = dict(group_sizes=torch.empty(E, **i32), group_offsets=torch.empty(E, **i32),
+                   group_padded_offsets=torch.empty(E, **i32),
+                   group_idx_for_bx=torch.empty(max(mb, 0), **i32),
+                   sorted_token_idx=torch.empty(T * k, **i32),
+                   sorted_row_weight=torch.empty(T * k, dtype=torch.float32, device=dev),
+                   token_topk_to_pos=torch.empty((T, k), **i32))
+    need = lib().moe_build_dispatch_workspace_bytes(T, k, E)
+    if ws is None:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().moe_build_dispatch(
+            _ptr(topk_idx), _ptr(topk_w), T, k, E, block_m, _ptr(out["group_sizes"]),
+            _ptr(out["group_offsets"]), _ptr(out["group_padded_offsets"]),
+            _ptr(out["group_idx_for_bx"]), _ptr(out["sorted_token_idx"]),
+            _ptr(out["sorted_row_weight"]), _ptr(out["token_topk_to_pos"]), _ptr(ws),
+            ws.numel() * ws.element_size(), _stream(dev)), "moe_build_dispatch")
+    return out
+
+
+def moe_gather_rows(x, sorted_token_idx, out=None):
+    _cuda(x, "x", ndim=2)
+    _cuda(sorted_token_idx, "sorted_token_idx", dtype=torch.int32)
+    T, d_h = x.shape
+    n = sorted_token_idx.numel()
+    if out is None:
+        out = torch.empty((n, d_h), dtype=x.dtype, device=x.device)
+    _cuda(out, "out", dtype=x.dtype)
+    with torch.cuda.device(x.device):
+        _check(lib().moe_gather_rows(_ptr(x), _ptr(sorted_token_idx), n, T, d_h,
+                                     _dtype_code(x, "x"), _ptr(out), _stream(x.device)),
+               "moe_gather_rows")
+    return out
+
+
+def _tables(t):
+    names = ("group_sizes", "group_offsets", "group_padded_offsets", "group_idx_for_bx")
+    for n in names:
+        _cuda(t[n], n, dtype=torch.int32)
+    return [t[n] for n in names]
+
+
+def moe_grouped_gate_up_silu(a, w_gate, w_up, tables, h=None, err=None):
+    _cuda(a, "a", ndim=2)
+    _cuda(w_gate, "w_gate", dtype=a.dtype, ndim=3)
+    _cuda(w_up, "w_up", dtype=a.dtype, ndim=3)
+    n_rows, d_h = a.shape
+    E, d_e, d_h2 = w_gate.shape
+    if d_h2 != d_h or w_up.shape != w_gate.shape:
+        raise ValueError("w_gate / w_up must be [E, d_expert, d_hidden]")
+    s, o, p, g = _tables(tables)
+    if h is None:
+        h = torch.empty((n_rows, d_e), dtype=a.dtype, device=a.device)
+    _cuda(h, "h", dtype=a.dtype)
+    if err is not None:
+        _cuda(err, "err", dtype=torch.int32)
+    with torch.cuda.device(a.device):
+        _check(lib().moe_grouped_gate_up_silu(
+            _ptr(a), _ptr(w_gate), _ptr(w_up), _ptr(s), _ptr(o), _ptr(p), _ptr(g), g.numel(),
+            n_rows, d_h, d_e, E, _dtype_code(a, "a"), _ptr(h), _ptr(err), _stream(a.device)),
+            "moe_grouped_gate_up_silu")
+    return h
+
+
+def moe_grouped_down(h, w_down, tables, row_weights=None, y=None, err=None):
+    _cuda(h, "h", ndim=2)
+    _cuda(w_down, "w_down", dtype=h.dtype, ndim=3)
+    n_rows, d_e = h.shape
+    E, d_h, d_e2 = w_down.shape
+    if d_e2 != d_e:
+        raise ValueError("w_down must be [E, d_hidden, d_expert]")
+    s, o, p, g = _tables(tables)
+    if row_weights is not None:
+        _cuda(row_weights, "row_weights", dtype=torch.float32)
+    if y is None:
+        y = torch.empty((n_rows, d_h), dtype=h.dtype, device=h.device)
+    _cuda(y, "y", dtype=h.dtype)
+    if err is not None:
+        _cuda(err, "err", dtype=torch.int32)
+    with torch.cuda.device(h.device):
+        _check(lib().moe_grouped_down(
+            _ptr(h), _ptr(w_down), _ptr(s), _ptr(o), _ptr(p), _ptr(g), g.numel(),
+            _ptr(row_weights), n_rows, d_h, d_e, E, _dtype_code(h, "h"), _ptr(y), _ptr(err),
+            _stream(h.device)), "moe_grouped_down")
+    return y
+
+
+def moe_reduce_fused(x, token_topk_to_pos, topk_weights=None, out_dtype=None, out=None, err=None):
+    """out[t] = cast(sum_k w[t,k] * x[pos[t,k]]) over pos >= 0, fp32 accumulation."""
+    _cuda(x, "x", ndim=2)
+    _cuda(token_topk_to_pos, "token_topk_to_pos", dtype=torch.int32, ndim=2)
+    if topk_weights is not None:
+        if topk_weights.dtype != torch.float32:
+            raise TypeError(f"topk_weights must be torch.float32, got {topk_weights.dtype}")
+        _cuda(topk_weights, "topk_weights", dtype=torch.float32, ndim=2)
+        if topk_weights.shape != token_topk_to_pos.shape:
+            raise ValueError("topk_weights and token_topk_to_pos shapes differ")
+    n_rows, H = x.shape
+    T, K = token_topk_to_pos.shape
+    out_dtype = x.dtype if out_dtype is None else out_dtype
+    if out is None:
+        out = torch.empty((T, H), dtype=out_dtype, device=x.device)
+    _cuda(out, "out", dtype=out_dtype)
+    if err is not None:
+        _cuda(err, "err", dtype=torch.int32)
+    with torch.cuda.device(x.device):
+        _check(lib().moe_reduce_fused(_ptr(x), n_rows, _ptr(token_topk_to_pos), _ptr(topk_weights),
+                                      T, K, H, _dtype_code(x, "x"), _dtype_code(out, "out"),
+                                      _ptr(out), _ptr(err), _stream(x.device)),
+               "moe_reduce_fused")
+    return out
+
+
+def forward_workspace_bytes(T, d_h, d_e, E, k, dtype) -> int:
+    return int(lib().moe_forward_workspace_bytes(T, d_h, d_e, E, k, _DT[dtype]))
+
+
+def forward_workspace_views(ws, T, d_h, d_e, E, k, dtype) -> dict:
+    """Typed views of moe_forward's intermediates inside its workspace."""
+    L = lib()
+    code = _DT[dtype]
+    Tk = T * k
+    mb = num_m_blocks(T, k, E)
+    shapes = {"logits": ((T, E), torch.float32), "topk_idx": ((T, k), torch.int32),
+              "topk_w": ((T, k), torch.float32), "group_sizes": ((E,), torch.int32),
+              "group_offsets": ((E,), torch.int32), "group_padded_offsets": ((E,), torch.int32),
+              "group_idx_for_bx": ((mb,), torch.int32), "sorted_token_idx": ((Tk,), torch.int32),
+              "sorted_row_weight": ((Tk,), torch.float32),
+              "token_topk_to_pos": ((T, k), torch.int32), "a": ((Tk, d_h), dtype),
+              "h": ((Tk, d_e), dtype), "y": ((Tk, d_h), dtype)}
+    out = {}
+    for i, name in enumerate(WS_NAMES):
+        if name not in shapes:
+            continue
+        shape, dt = shapes[name]
+        off = int(L.moe_forward_workspace_offset(T, d_h, d_e, E, k, code, i))
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.empty((), dtype=dt).element_size()
+        out[name] = ws[off:off + nbytes].view(dt).view(shape)
+    return out
+
+
+def moe_forward(x, w_g, bias, w_gate, w_up, w_down, k: int, ws=None, out=None, err=None):
+    """The whole routed forward; returns out [T, d_hidden]."""
+    _cuda(x, "x", ndim=2)
+    for n, t in (("w_g", w_g), ("w_gate", w_gate), ("w_up", w_up), ("w_down", w_down)):
+        _cuda(t, n, dtype=x.dtype)
+    if bias is not None:
+        _cuda(bias, "bias", dtype=torch.float32, ndim=1)
+    T, d_h = x.shape
+    E, d_e, _ = w_gate.shape
+    need = forward_workspace_bytes(T, d_h, d_e, E, k, x.dtype)
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _cuda(ws, "ws", dtype=torch.uint8)
+    if out is None:
+        out = torch.empty((T, d_h), dtype=x.dtype, device=x.device)
+    _cuda(out, "out", dtype=x.dtype)
+    if err is not None:
+        _cuda(err, "err", dtype=torch.int32)
+    with torch.cuda.device(x.device):
+        _check(lib().moe_forward(_ptr(x), _ptr(w_g), _ptr(bias), _ptr(w_gate), _ptr(w_up),
+                                 _ptr(w_down), T, d_h, d_e, E, k, _dtype_code(x, "x"), _ptr(ws),
+                                 ws.numel(), _ptr(out), _ptr(err), _stream(x.device)),
+               "moe_forward")
+    return out

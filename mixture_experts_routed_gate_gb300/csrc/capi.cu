@@ -1,0 +1,292 @@
+// capi.cu -- the exported C-ABI: host-side argument checks, workspace layout,
+// and the stream-ordered composition of the forward.  See the public header
+// for the contract of every entry point.
+#include <cuda_runtime.h>
+
+#include "../../include/moe_routed_gate.h"
+#include "internal.h"
+
+namespace moe {
+
+int device_sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
+}  // namespace moe
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_half_type(moe_dtype_t d) { return d == MOE_F16 || d == MOE_BF16; }
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int64_t m_blocks_of(int64_t T, int64_t k, int64_t E, int64_t block_m) {
+    if (T < 0 || k <= 0 || E <= 0 || block_m <= 0) return -1;
+    return (T * k + block_m - 1) / block_m + E;
+}
+
+struct FwdLayout {
+    size_t off[14];
+    size_t total;
+};
+
+bool fwd_layout(int64_t T, int64_t d_h, int64_t d_e, int64_t E, int64_t k, moe_dtype_t dtype,
+                FwdLayout *L) {
+    if (T < 0 || d_h <= 0 || d_e <= 0 || E <= 0 || k <= 0 || !is_half_type(dtype)) return false;
+    const size_t es = 2;
+    const size_t Tk = static_cast<size_t>(T * k);
+    const size_t mb = static_cast<size_t>(m_blocks_of(T, k, E, MOE_BLOCK_M));
+    const size_t sz[14] = {
+        static_cast<size_t>(T) * E * 4,  // 0 logits
+        Tk * 4,                          // 1 topk_idx
+        Tk * 4,                          // 2 topk_w
+        static_cast<size_t>(E) * 4,      // 3 group_sizes
+        static_cast<size_t>(E) * 4,      // 4 group_offsets
+        static_cast<size_t>(E) * 4,      // 5 group_padded_offsets
+        mb * 4,                          // 6 group_idx_for_bx
+        Tk * 4,                          // 7 sorted_token_idx
+        Tk * 4,                          // 8 sorted_row_weight
+        Tk * 4,                          // 9 token_topk_to_pos
+        moe::dispatch_scratch_bytes(static_cast<int64_t>(Tk), E),  // 10 dispatch scratch
+        Tk * d_h * es,                   // 11 A (gathered rows)
+        Tk * d_e * es,                   // 12 h
+        Tk * d_h * es,                   // 13 y
+    };
+    size_t cur = 0;
+    for (int i = 0; i < 14; ++i) {
+        L->off[i] = cur;
+        cur += align_up(sz[i] > 0 ? sz[i] : 1);
+    }
+    L->total = cur;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: unsupported dtype or shape";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace too small";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
+        case MOE_ERR_DEVICE_FLAG: return "MOE_ERR_DEVICE_FLAG: out-of-range position seen on the device";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a device pipeline wait timed out";
+        default: return "unknown moe status";
+    }
+}
+
+int64_t moe_num_m_blocks(int64_t T, int64_t k, int64_t E, int64_t block_m) {
+    return m_blocks_of(T, k, E, block_m);
+}
+
+size_t moe_gate_topk_workspace_bytes(int64_t T, int64_t E) {
+    if (T < 0 || E <= 0) return static_cast<size_t>(-1);
+    return static_cast<size_t>(T) * static_cast<size_t>(E) * 4;
+}
+
+size_t moe_build_dispatch_workspace_bytes(int64_t T, int64_t k, int64_t E) {
+    if (T < 0 || k <= 0 || E <= 0) return static_cast<size_t>(-1);
+    return moe::dispatch_scratch_bytes(T * k, E);
+}
+
+size_t moe_forward_workspace_bytes(int64_t T, int64_t d_h, int64_t d_e, int64_t E, int64_t k,
+                                   moe_dtype_t dtype) {
+    FwdLayout L;
+    if (!fwd_layout(T, d_h, d_e, E, k, dtype, &L)) return static_cast<size_t>(-1);
+    return L.total;
+}
+
+int64_t moe_forward_workspace_offset(int64_t T, int64_t d_h, int64_t d_e, int64_t E, int64_t k,
+                                     moe_dtype_t dtype, int index) {
+    FwdLayout L;
+    if (index < 0 || index >= 14 || !fwd_layout(T, d_h, d_e, E, k, dtype, &L)) return -1;
+    return static_cast<int64_t>(L.off[index]);
+}
+
+moe_status_t moe_gate_topk(const void *x, const void *w_g, const float *bias, int64_t T,
+                           int64_t d_h, int64_t E, int64_t k, moe_dtype_t dtype,
+                           int32_t *topk_idx, float *topk_w, void *ws, size_t ws_bytes,
+                           moe_stream_t stream) {
+    if (T < 0 || d_h <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+    if (d_h % 256 != 0 || k > E || k > 32 || E > 1024) return MOE_ERR_INVALID_ARG;
+    if (!is_half_type(dtype)) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!x || !w_g || !topk_idx || !topk_w || !ws) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_g) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_gate_topk_workspace_bytes(T, E)) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    float *logits = static_cast<float *>(ws);
+    cudaError_t e = moe::launch_gate_logits(x, w_g, bias, T, d_h, E, dtype, logits, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_status(moe::launch_topk_softmax(logits, T, E, k, topk_idx, topk_w, s));
+}
+
+moe_status_t moe_build_dispatch(const int32_t *topk_idx, const float *topk_w, int64_t T,
+                                int64_t k, int64_t E, int64_t block_m, int32_t *group_sizes,
+                                int32_t *group_offsets, int32_t *group_padded_offsets,
+                                int32_t *group_idx_for_bx, int32_t *sorted_token_idx,
+                                float *sorted_row_weight, int32_t *token_topk_to_pos, void *ws,
+                                size_t ws_bytes, moe_stream_t stream) {
+    if (T < 0 || k <= 0 || E <= 0 || E > 1024 || block_m != MOE_BLOCK_M) return MOE_ERR_INVALID_ARG;
+    if (T * k > (int64_t(1) << 30)) return MOE_ERR_UNSUPPORTED;
+    if (!group_sizes || !group_offsets || !group_padded_offsets || !group_idx_for_bx)
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !sorted_token_idx || !sorted_row_weight || !token_topk_to_pos))
+        return MOE_ERR_INVALID_ARG;
+    const size_t need = moe_build_dispatch_workspace_bytes(T, k, E);
+    if (T > 0 && (ws_bytes < need || !ws)) return MOE_ERR_WORKSPACE;
+    return cuda_status(moe::launch_dispatch(
+        topk_idx, topk_w, T, k, E, block_m, group_sizes, group_offsets, group_padded_offsets,
+        group_idx_for_bx, m_blocks_of(T, k, E, block_m), sorted_token_idx, sorted_row_weight,
+        token_topk_to_pos, ws, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_gather_rows(const void *x, const int32_t *sorted_token_idx, int64_t n_rows,
+                             int64_t T, int64_t d_h, moe_dtype_t dtype, void *a_out,
+                             moe_stream_t stream) {
+    if (n_rows < 0 || T < 0 || d_h <= 0) return MOE_ERR_INVALID_ARG;
+    const int es = dtype == MOE_F32 ? 4 : 2;
+    if (dtype != MOE_F16 && dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
+    if ((d_h * es) % 16 != 0) return MOE_ERR_INVALID_ARG;
+    if (n_rows == 0) return MOE_OK;
+    if (!x || !sorted_token_idx || !a_out || !aligned16(x) || !aligned16(a_out))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_status(moe::launch_gather_rows(x, sorted_token_idx, n_rows, d_h, es, a_out,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static moe_status_t check_gemm_tables(const int32_t *s, const int32_t *o, const int32_t *p,
+                                      const int32_t *g, int64_t m_blocks, int64_t n_rows, int64_t E) {
+    if (!s || !o || !p || !g) return MOE_ERR_INVALID_ARG;
+    if (m_blocks <= 0 || n_rows <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+    if (m_blocks > (n_rows + MOE_BLOCK_M - 1) / MOE_BLOCK_M + E) return MOE_ERR_INVALID_ARG;
+    if (n_rows > (int64_t(1) << 31) - 256) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status_t moe_grouped_gate_up_silu(const void *a, const void *w_gate, const void *w_up,
+                                      const int32_t *group_sizes, const int32_t *group_offsets,
+                                      const int32_t *group_padded_offsets,
+                                      const int32_t *group_idx_for_bx, int64_t m_blocks,
+                                      int64_t n_rows, int64_t d_h, int64_t d_e, int64_t E,
+                                      moe_dtype_t dtype, void *h, int32_t *err_flag,
+                                      moe_stream_t stream) {
+    if (!is_half_type(dtype)) return MOE_ERR_UNSUPPORTED;
+    if (d_h <= 0 || d_e <= 0 || d_h % 64 != 0 || d_e % 64 != 0) return MOE_ERR_INVALID_ARG;
+    if (n_rows == 0) return MOE_OK;
+    moe_status_t st = check_gemm_tables(group_sizes, group_offsets, group_padded_offsets,
+                                        group_idx_for_bx, m_blocks, n_rows, E);
+    if (st != MOE_OK) return st;
+    if (!a || !w_gate || !w_up || !h) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(h))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_status(moe::launch_grouped_gemm(
+        true, dtype, a, w_gate, w_up, group_sizes, group_offsets, group_padded_offsets,
+        group_idx_for_bx, m_blocks, nullptr, n_rows, d_h, d_e, E, h, err_flag,
+        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_grouped_down(const void *h, const void *w_down, const int32_t *group_sizes,
+                              const int32_t *group_offsets, const int32_t *group_padded_offsets,
+                              const int32_t *group_idx_for_bx, int64_t m_blocks,
+                              const float *row_weights, int64_t n_rows, int64_t d_h,
+                              int64_t d_e, int64_t E, moe_dtype_t dtype, void *y,
+                              int32_t *err_flag, moe_stream_t stream) {
+    if (!is_half_type(dtype)) return MOE_ERR_UNSUPPORTED;
+    if (d_h <= 0 || d_e <= 0 || d_h % 64 != 0 || d_e % 64 != 0) return MOE_ERR_INVALID_ARG;
+    if (n_rows == 0) return MOE_OK;
+    moe_status_t st = check_gemm_tables(group_sizes, group_offsets, group_padded_offsets,
+                                        group_idx_for_bx, m_blocks, n_rows, E);
+    if (st != MOE_OK) return st;
+    if (!h || !w_down || !y) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(h) || !aligned16(w_down) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(moe::launch_grouped_gemm(
+        false, dtype, h, w_down, nullptr, group_sizes, group_offsets, group_padded_offsets,
+        group_idx_for_bx, m_blocks, row_weights, n_rows, d_e, d_h, E, y, err_flag,
+        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_reduce_fused(const void *x, int64_t n_rows, const int32_t *token_topk_to_pos,
+                              const float *topk_weights, int64_t T, int64_t K, int64_t H,
+                              moe_dtype_t in_dtype, moe_dtype_t out_dtype, void *out,
+                              int32_t *err_flag, moe_stream_t stream) {
+    if (T < 0 || K <= 0 || H <= 0 || n_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (H % 256 != 0) return MOE_ERR_INVALID_ARG;
+    const bool pair_ok = (in_dtype == out_dtype &&
+                          (in_dtype == MOE_F16 || in_dtype == MOE_BF16 || in_dtype == MOE_F32)) ||
+                         (in_dtype == MOE_F32 && (out_dtype == MOE_F16 || out_dtype == MOE_BF16));
+    if (!pair_ok) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!out || !token_topk_to_pos || (n_rows > 0 && !x)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(out) || (x && !aligned16(x))) return MOE_ERR_INVALID_ARG;
+    return cuda_status(moe::launch_reduce_fused(x, n_rows, token_topk_to_pos, topk_weights, T, K,
+                                                H, in_dtype, out_dtype, out, err_flag,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_forward(const void *x, const void *w_g, const float *bias, const void *w_gate,
+                         const void *w_up, const void *w_down, int64_t T, int64_t d_h,
+                         int64_t d_e, int64_t E, int64_t k, moe_dtype_t dtype, void *ws,
+                         size_t ws_bytes, void *out, int32_t *err_flag, moe_stream_t stream) {
+    if (!is_half_type(dtype)) return MOE_ERR_UNSUPPORTED;
+    if (T < 0 || d_h <= 0 || d_e <= 0 || E <= 0 || k <= 0 || k > E || k > 32 || E > 1024)
+        return MOE_ERR_INVALID_ARG;
+    if (d_h % 256 != 0 || d_e % 64 != 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !w_g || !w_gate || !w_up || !w_down || !out || !ws) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;
+    FwdLayout L;
+    if (!fwd_layout(T, d_h, d_e, E, k, dtype, &L)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    char *w = static_cast<char *>(ws);
+    float *logits = reinterpret_cast<float *>(w + L.off[0]);
+    int32_t *topk_idx = reinterpret_cast<int32_t *>(w + L.off[1]);
+    float *topk_w = reinterpret_cast<float *>(w + L.off[2]);
+    int32_t *sizes = reinterpret_cast<int32_t *>(w + L.off[3]);
+    int32_t *offsets = reinterpret_cast<int32_t *>(w + L.off[4]);
+    int32_t *padded = reinterpret_cast<int32_t *>(w + L.off[5]);
+    int32_t *gidx = reinterpret_cast<int32_t *>(w + L.off[6]);
+    int32_t *stok = reinterpret_cast<int32_t *>(w + L.off[7]);
+    float *sw = reinterpret_cast<float *>(w + L.off[8]);
+    int32_t *pos = reinterpret_cast<int32_t *>(w + L.off[9]);
+    void *scratch = w + L.off[10];
+    void *A = w + L.off[11];
+    void *hbuf = w + L.off[12];
+    void *ybuf = w + L.off[13];
+    const int64_t Tk = T * k;
+    const int64_t mb = m_blocks_of(T, k, E, MOE_BLOCK_M);
+    moe_status_t st;
+    st = moe_gate_topk(x, w_g, bias, T, d_h, E, k, dtype, topk_idx, topk_w, logits,
+                       static_cast<size_t>(T) * E * 4, stream);
+    if (st != MOE_OK) return st;
+    st = moe_build_dispatch(topk_idx, topk_w, T, k, E, MOE_BLOCK_M, sizes, offsets, padded, gidx,
+                            stok, sw, pos, scratch, moe::dispatch_scratch_bytes(Tk, E), stream);
+    if (st != MOE_OK) return st;
+    st = moe_gather_rows(x, stok, Tk, T, d_h, dtype, A, stream);
+    if (st != MOE_OK) return st;
+    st = moe_grouped_gate_up_silu(A, w_gate, w_up, sizes, offsets, padded, gidx, mb, Tk, d_h, d_e,
+                                  E, dtype, hbuf, err_flag, stream);
+    if (st != MOE_OK) return st;
+    st = moe_grouped_down(hbuf, w_down, sizes, offsets, padded, gidx, mb, nullptr, Tk, d_h, d_e, E,
+                          dtype, ybuf, err_flag, stream);
+    if (st != MOE_OK) return st;
+    return moe_reduce_fused(ybuf, Tk, pos, topk_w, T, k, d_h, dtype, dtype, out, err_flag, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,204 @@
+// dispatch.cu -- the counting-sort dispatch of the routed MoE forward.
+//
+// CSDN "forward", steps 2-5 (argsort by expert, bincount, cumsum, the
+// per-expert gather loop, group_sizes / group_offset / group_padded_offsets /
+// group_idx_for_bx) done on the device with no host round trip:
+//   1. dispatch_hist_kernel: each CTA counts the experts of its chunk of
+//      CHUNK consecutive pairs (f = t*k + j) into hist[chunk][e].
+//   2. dispatch_scan_kernel (one CTA, one thread per expert): per-expert
+//      running sum over chunks -> chunk bases and group_sizes; block scans ->
+//      group_offsets and the padded offsets; a binary search per M block ->
+//      group_idx_for_bx.  Chunk bases are made absolute in place.
+//   3. dispatch_scatter_kernel: each warp owns a contiguous run of pairs;
+//      warp-level counts in shared memory give every warp its start per
+//      expert; the warp then walks its pairs 32 at a time in ascending f and
+//      ranks equal experts with __match_any_sync, so the order inside an
+//      expert is ascending f (a stable sort) with no atomics-order effects.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int DS_WARPS = 8;
+constexpr int DS_THREADS = DS_WARPS * 32;
+constexpr int PAIRS_PER_WARP = 256;
+constexpr int CHUNK = DS_WARPS * PAIRS_PER_WARP;  // 2048 pairs per CTA
+constexpr int SCAN_THREADS = 1024;                // E <= 1024
+
+__global__ void __launch_bounds__(DS_THREADS)
+    dispatch_hist_kernel(const int32_t *__restrict__ idx, int64_t n_pairs, int E,
+                         int32_t *__restrict__ hist) {
+    extern __shared__ int32_t counts[];
+    for (int e = threadIdx.x; e < E; e += DS_THREADS) counts[e] = 0;
+    __syncthreads();
+    const int64_t f0 = static_cast<int64_t>(blockIdx.x) * CHUNK;
+    for (int i = threadIdx.x; i < CHUNK; i += DS_THREADS) {
+        const int64_t f = f0 + i;
+        if (f < n_pairs) {
+            const int e = __ldg(idx + f);
+            if (e >= 0 && e < E) atomicAdd(&counts[e], 1);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += DS_THREADS)
+        hist[static_cast<int64_t>(blockIdx.x) * E + e] = counts[e];
+}
+
+// Exclusive scan of one value per thread over the whole block (<= 1024 threads).
+__device__ int block_exclusive_scan(int v, int *warp_sums) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, s);
+        if (lane >= s) incl += o;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = (blockDim.x + 31) >> 5;
+        int ws = lane < nw ? warp_sums[lane] : 0;
+        int wi = ws;
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, wi, s);
+            if (lane >= s) wi += o;
+        }
+        warp_sums[lane] = wi - ws;  // exclusive prefix of warp totals
+    }
+    __syncthreads();
+    const int out = warp_sums[warp] + incl - v;
+    __syncthreads();  // warp_sums is reused by the next call
+    return out;
+}
+
+__global__ void __launch_bounds__(SCAN_THREADS)
+    dispatch_scan_kernel(int32_t *__restrict__ hist, int n_chunks, int E, int block_m,
+                         int32_t *__restrict__ sizes, int32_t *__restrict__ offsets,
+                         int32_t *__restrict__ padded, int32_t *__restrict__ gidx,
+                         int m_blocks) {
+    __shared__ int warp_sums[32];
+    __shared__ int po_s[SCAN_THREADS];
+    const int e = threadIdx.x;
+    int count = 0;
+    if (e < E) {
+        for (int c = 0; c < n_chunks; ++c) {
+            int32_t *h = hist + static_cast<int64_t>(c) * E + e;
+            const int v = *h;
+            *h = count;  // chunk base relative to the expert's start
+            count += v;
+        }
+        sizes[e] = count;
+    }
+    const int off = block_exclusive_scan(e < E ? count : 0, warp_sums);
+    // padded size of expert e: ceil((count + 1) / block_m) * block_m
+    const int psize = e < E ? ((count + block_m) / block_m) * block_m : 0;
+    const int poff = block_exclusive_scan(psize, warp_sums);
+    if (e < E) {
+        offsets[e] = off;
+        padded[e] = poff;
+        po_s[e] = poff;
+        for (int c = 0; c < n_chunks; ++c) hist[static_cast<int64_t>(c) * E + e] += off;
+    }
+    __syncthreads();
+    // group_idx_for_bx[bx] = last e with bx * block_m >= po[e] (po[0] = 0, increasing)
+    for (int bx = threadIdx.x; bx < m_blocks; bx += SCAN_THREADS) {
+        const long long start = static_cast<long long>(bx) * block_m;
+        int lo = 0, hi = E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (static_cast<long long>(po_s[mid]) <= start) lo = mid;
+            else hi = mid - 1;
+        }
+        gidx[bx] = lo;
+    }
+}
+
+__global__ void __launch_bounds__(DS_THREADS)
+    dispatch_scatter_kernel(const int32_t *__restrict__ idx, const float *__restrict__ w,
+                            int64_t n_pairs, int k, int E, const int32_t *__restrict__ bases,
+                            int32_t *__restrict__ sorted_tok, float *__restrict__ sorted_w,
+                            int32_t *__restrict__ pos) {
+    extern __shared__ int32_t wcount[];  // [DS_WARPS][E]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < DS_WARPS * E; i += DS_THREADS) wcount[i] = 0;
+    __syncthreads();
+    const int64_t wf0 = static_cast<int64_t>(blockIdx.x) * CHUNK + static_cast<int64_t>(warp) * PAIRS_PER_WARP;
+    int32_t *mine = wcount + warp * E;
+    // pass 1: per-warp expert counts
+    for (int r = 0; r < PAIRS_PER_WARP; r += 32) {
+        const int64_t f = wf0 + r + lane;
+        const int e = f < n_pairs ? __ldg(idx + f) : -1;
+        if (e >= 0 && e < E) atomicAdd(&mine[e], 1);
+    }
+    __syncthreads();
+    // warp starts per expert: chunk base + counts of the earlier warps
+    for (int e = threadIdx.x; e < E; e += DS_THREADS) {
+        int run = __ldg(bases + static_cast<int64_t>(blockIdx.x) * E + e);
+        for (int wv = 0; wv < DS_WARPS; ++wv) {
+            const int c = wcount[wv * E + e];
+            wcount[wv * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    // pass 2: stable ranks inside the warp, 32 pairs at a time in ascending f
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int r = 0; r < PAIRS_PER_WARP; r += 32) {
+        const int64_t f = wf0 + r + lane;
+        int e = f < n_pairs ? __ldg(idx + f) : -1;
+        if (e >= E) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        int row = 0;
+        if (e >= 0) row = mine[e] + __popc(peers & lt_mask);
+        __syncwarp();
+        if (e >= 0 && (peers & lt_mask) == 0) mine[e] += __popc(peers);  // lowest peer updates
+        __syncwarp();
+        if (e >= 0) {
+            sorted_tok[row] = static_cast<int32_t>(f / k);
+            sorted_w[row] = w ? __ldg(w + f) : 1.0f;
+            pos[f] = row;
+        }
+    }
+}
+
+}  // namespace
+
+size_t dispatch_scratch_bytes(int64_t n_pairs, int64_t E) {
+    const int64_t n_chunks = n_pairs > 0 ? (n_pairs + CHUNK - 1) / CHUNK : 1;
+    return static_cast<size_t>(n_chunks * E * 4);
+}
+
+cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_t T, int64_t k,
+                            int64_t E, int64_t block_m, int32_t *sizes, int32_t *offsets, int32_t *padded,
+                            int32_t *gidx, int64_t m_blocks, int32_t *sorted_token_idx,
+                            float *sorted_row_weight, int32_t *pos, void *scratch,
+                            cudaStream_t stream) {
+    const int64_t n_pairs = T * k;
+    const int64_t n_chunks = n_pairs > 0 ? (n_pairs + CHUNK - 1) / CHUNK : 0;
+    int32_t *hist = static_cast<int32_t *>(scratch);
+    if (n_chunks > 0) {
+        dispatch_hist_kernel<<<static_cast<unsigned>(n_chunks), DS_THREADS, E * 4, stream>>>(
+            topk_idx, n_pairs, static_cast<int>(E), hist);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    dispatch_scan_kernel<<<1, SCAN_THREADS, 0, stream>>>(
+        hist, static_cast<int>(n_chunks), static_cast<int>(E), static_cast<int>(block_m), sizes, offsets, padded,
+        gidx, static_cast<int>(m_blocks));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || n_chunks == 0) return e;
+    const size_t smem = static_cast<size_t>(DS_WARPS) * E * 4;
+    if (smem > 48 * 1024) {
+        e = cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    dispatch_scatter_kernel<<<static_cast<unsigned>(n_chunks), DS_THREADS, smem, stream>>>(
+        topk_idx, topk_w, n_pairs, static_cast<int>(k), static_cast<int>(E), hist,
+        sorted_token_idx, sorted_row_weight, pos);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

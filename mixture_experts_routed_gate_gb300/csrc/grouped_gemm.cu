@@ -1,0 +1,403 @@
+// grouped_gemm.cu -- the two grouped expert GEMMs of the routed MoE forward on
+// the 5th-generation tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+// Stage 1 (CSDN "tilelang kernel stage 1 gate+up"; skeletons.py moe_routed_kernel):
+//   h[rows of block bx] = silu(A W_gate[g]^T) * (A W_up[g]^T)
+// Stage 2 (CSDN "tilelang kernel stage 2 down"):
+//   y[rows of block bx] = (h W_down[g]^T) (* row weight)
+// with the block -> (expert g, first row m_start, valid rows) lookup of the
+// pages' dispatch contract.
+//
+// Design (one persistent CTA per SM, 192 threads):
+//   warp 0      TMA producer: per 64-wide K step loads the 128-row A tile and the
+//               256-row B tile (stage 1: 128 W_gate rows + 128 W_up rows of the
+//               same output columns; stage 2: 256 W_down rows) into a 4-deep
+//               shared-memory ring, 128-byte swizzled.
+//   warp 1      MMA issuer: one thread issues tcgen05.mma M=128 N=256 K=16 into
+//               a TMEM accumulator (2 x 256 columns, double buffered so the
+//               epilogue of tile i overlaps the main loop of tile i+1).
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (thread = row), stage 1
+//               fuses silu(gate)*up, stage 2 the optional row weight; round to
+//               the activation dtype and store only the block's valid rows.
+// Tiles are (M block, N tile) pairs in M-block-major order, dealt round-robin
+// to the CTAs; blocks with no valid rows (the padding blocks the tables
+// create) are skipped by every role.  Every wait is bounded (see
+// mbar_wait_bounded): on a timeout the kernel records kErrTimeout, drains the
+// copies and MMAs it issued, frees TMEM and returns.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // 64 x 2 B = 128 B: one swizzle span per row
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int NUM_THREADS = 192;
+constexpr int MMA_N = 256;
+constexpr int ACC_COLS = 256;
+constexpr int TMEM_COLS = 512;
+constexpr int A_BYTES = BM * BK * 2;         // 16 KB
+constexpr int B_BYTES = MMA_N * BK * 2;      // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES;
+
+struct GemmParams {
+    const int32_t *sizes;
+    const int32_t *offsets;
+    const int32_t *padded;
+    const int32_t *gidx;
+    const float *row_weights;
+    void *out;
+    int m_blocks;
+    int n_tiles;
+    int k_blocks;
+    int N;  // output columns
+    int *err;
+};
+
+struct TileInfo {
+    int g, m_start, rows, n0;
+};
+
+__device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int tile, int out_n) {
+    const int bx = tile / p.n_tiles;
+    const int nt = tile - bx * p.n_tiles;
+    TileInfo t;
+    t.g = __ldg(p.gidx + bx);
+    const int rel = bx * BM - __ldg(p.padded + t.g);
+    int rows = __ldg(p.sizes + t.g) - rel;
+    t.rows = rows < 0 ? 0 : (rows > BM ? BM : rows);
+    t.m_start = rel + __ldg(p.offsets + t.g);
+    t.n0 = nt * out_n;
+    return t;
+}
+
+// A wait used only while winding down after an abort: bounded, ignores the
+// abort flag (the point is to let in-flight hardware work land).
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    unsigned long long start = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - start > kWaitTimeoutNs) return;
+    }
+}
+
+template <int DT, bool GATE_UP>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB0,
+                        const __grid_constant__ CUtensorMap tmB1, const GemmParams p) {
+    constexpr int OUT_N = GATE_UP ? 128 : 256;  // output columns per tile
+    constexpr uint32_t IDESC = idesc_f16(DT == kBF16, BM, MMA_N);
+    using OutT = typename Elem<DT>::T;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);  // one arrival per epilogue warp
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB0);
+        if (GATE_UP) tma_prefetch_desc(&tmB1);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = p.m_blocks * p.n_tiles;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+                const TileInfo ti = tile_info(p, tile, OUT_N);
+                if (ti.rows == 0) continue;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_bar(stage);
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    const uint32_t a_dst = smem_u32(sA + stage * A_BYTES);
+                    const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
+                    tma_load_2d(a_dst, &tmA, fb, kb * BK, ti.m_start);
+                    if (GATE_UP) {
+                        tma_load_3d(b_dst, &tmB0, fb, kb * BK, ti.n0, ti.g);
+                        tma_load_3d(b_dst + B_BYTES / 2, &tmB1, fb, kb * BK, ti.n0, ti.g);
+                    } else {
+                        tma_load_3d(b_dst, &tmB0, fb, kb * BK, ti.n0, ti.g);
+                    }
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let every copy still in flight land before shared memory goes away
+                for (long j = 1; j <= STAGES && j <= issued; ++j) {
+                    const long i = issued - j;
+                    mbar_wait_drain(full_bar(static_cast<int>(i % STAGES)),
+                                    static_cast<uint32_t>((i / STAGES) & 1));
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------- MMA issuer --------------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool ok = true;
+            uint32_t last_bar = 0, last_parity = 0;
+            bool committed = false;
+            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+                const TileInfo ti = tile_info(p, tile, OUT_N);
+                if (ti.rows == 0) continue;
+                const int acc = local & 1;
+                const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
+                if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a_desc = smem_desc_sw128(smem_u32(sA + stage * A_BYTES));
+                    const uint64_t b_desc = smem_desc_sw128(smem_u32(sB + stage * B_BYTES));
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                        // +32 bytes per K=16 step inside the 128-byte swizzled row
+                        tc_mma_f16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, IDESC,
+                                   (kb | k) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(empty_bar(stage));  // frees the smem stage when these MMAs finish
+                    last_bar = empty_bar(stage);
+                    last_parity = phase;
+                    committed = true;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(tfull_bar(acc));  // accumulator ready for the epilogue
+                ++local;
+            }
+            if (!ok && committed) mbar_wait_drain(last_bar, last_parity);
+        }
+    } else {
+        // --------------------------------- epilogue ---------------------------------
+        const int q = warp & 3;  // TMEM lane quarter this warp may read
+        const int row = q * 32 + lane;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            const TileInfo ti = tile_info(p, tile, OUT_N);
+            if (ti.rows == 0) continue;
+            const int acc = local & 1;
+            const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
+            // one lane waits, the warp reconverges before the .sync.aligned TMEM loads
+            int ready = 1;
+            if (lane == 0) ready = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.err) ? 1 : 0;
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            if (!ready) break;
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * ACC_COLS);
+            const bool valid = row < ti.rows;
+            OutT *out_row = reinterpret_cast<OutT *>(p.out) +
+                            static_cast<int64_t>(ti.m_start + (valid ? row : 0)) * p.N;
+            float rw = 1.0f;
+            if (!GATE_UP && p.row_weights != nullptr && valid) rw = __ldg(p.row_weights + ti.m_start + row);
+#pragma unroll 1
+            for (int c = 0; c < OUT_N / 16; ++c) {
+                const int col = ti.n0 + c * 16;
+                uint32_t packed[8];
+                if (GATE_UP) {
+                    uint32_t g[16], u[16];
+                    tmem_ld16(t_row + c * 16, g);
+                    tmem_ld16(t_row + 128 + c * 16, u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float v[2];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const float gv = __uint_as_float(g[2 * i + h]);
+                            const float uv = __uint_as_float(u[2 * i + h]);
+                            const float s = gv * __frcp_rn(1.0f + __expf(-gv));
+                            v[h] = s * uv;
+                        }
+                        packed[i] = pack2<DT>(v[0], v[1]);
+                    }
+                } else {
+                    uint32_t r[16];
+                    tmem_ld16(t_row + c * 16, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        packed[i] = pack2<DT>(__uint_as_float(r[2 * i]) * rw,
+                                              __uint_as_float(r[2 * i + 1]) * rw);
+                }
+                if (valid && col < p.N) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(out_row + col);
+                    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            ++local;
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// Row-major [rows, K] 16-bit matrix, box = 64 K-elements x box_rows rows.
+bool make_map_2d(CUtensorMap *m, int dtype, const void *ptr, uint64_t K, uint64_t rows,
+                 uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {K, rows};
+    cuuint64_t strides[1] = {K * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Stacked [E, rows, K] 16-bit weights, box = 64 K-elements x box_rows rows x 1 expert.
+bool make_map_3d(CUtensorMap *m, int dtype, const void *ptr, uint64_t K, uint64_t rows,
+                 uint64_t E, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {K, rows, E};
+    cuuint64_t strides[2] = {K * 2, rows * K * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    3, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int DT, bool GATE_UP>
+cudaError_t launch_typed(const CUtensorMap &ta, const CUtensorMap &tb0, const CUtensorMap &tb1,
+                         const GemmParams &p, int grid, cudaStream_t stream) {
+    auto kern = grouped_gemm_kernel<DT, GATE_UP>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb0, tb1, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(bool gate_up, int dtype, const void *a, const void *w0,
+                                const void *w1, const int32_t *sizes, const int32_t *offsets,
+                                const int32_t *padded, const int32_t *gidx, int64_t m_blocks,
+                                const float *row_weights, int64_t n_rows, int64_t K, int64_t N,
+                                int64_t E, void *out, int32_t *err, cudaStream_t stream) {
+    if (n_rows <= 0 || m_blocks <= 0) return cudaSuccess;
+    const int out_n = gate_up ? 128 : 256;
+    CUtensorMap ta, tb0, tb1;
+    if (!make_map_2d(&ta, dtype, a, static_cast<uint64_t>(K), static_cast<uint64_t>(n_rows), BM))
+        return cudaErrorInvalidValue;
+    if (!make_map_3d(&tb0, dtype, w0, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                     static_cast<uint64_t>(E), gate_up ? 128u : 256u))
+        return cudaErrorInvalidValue;
+    if (gate_up) {
+        if (!make_map_3d(&tb1, dtype, w1, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                         static_cast<uint64_t>(E), 128u))
+            return cudaErrorInvalidValue;
+    } else {
+        tb1 = tb0;
+    }
+    GemmParams p;
+    p.sizes = sizes;
+    p.offsets = offsets;
+    p.padded = padded;
+    p.gidx = gidx;
+    p.row_weights = row_weights;
+    p.out = out;
+    p.m_blocks = static_cast<int>(m_blocks);
+    p.n_tiles = static_cast<int>((N + out_n - 1) / out_n);
+    p.k_blocks = static_cast<int>((K + BK - 1) / BK);
+    p.N = static_cast<int>(N);
+    p.err = err;
+    const int64_t total = m_blocks * p.n_tiles;
+    const int grid = static_cast<int>(total < device_sm_count() ? total : device_sm_count());
+    if (dtype == kBF16)
+        return gate_up ? launch_typed<kBF16, true>(ta, tb0, tb1, p, grid, stream)
+                       : launch_typed<kBF16, false>(ta, tb0, tb1, p, grid, stream);
+    return gate_up ? launch_typed<kF16, true>(ta, tb0, tb1, p, grid, stream)
+                   : launch_typed<kF16, false>(ta, tb0, tb1, p, grid, stream);
+}
+
+}  // namespace moe

@@ -1,0 +1,42 @@
+// internal.h -- host-side launchers of the kernels (C++ linkage, not exported).
+// The C-ABI layer validates every argument before calling these.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+int device_sm_count();
+
+// gate_topk.cu
+cudaError_t launch_gate_logits(const void *x, const void *wg, const float *bias, int64_t T,
+                               int64_t d_h, int64_t E, int dtype, float *logits,
+                               cudaStream_t stream);
+cudaError_t launch_topk_softmax(const float *logits, int64_t T, int64_t E, int64_t k,
+                                int32_t *topk_idx, float *topk_w, cudaStream_t stream);
+
+// dispatch.cu
+size_t dispatch_scratch_bytes(int64_t n_pairs, int64_t E);
+cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_t T, int64_t k,
+                            int64_t E, int64_t block_m, int32_t *sizes, int32_t *offsets, int32_t *padded,
+                            int32_t *gidx, int64_t m_blocks, int32_t *sorted_token_idx,
+                            float *sorted_row_weight, int32_t *pos, void *scratch,
+                            cudaStream_t stream);
+
+// rows.cu
+cudaError_t launch_gather_rows(const void *x, const int32_t *sorted_token_idx, int64_t n_rows,
+                               int64_t d_h, int elem_bytes, void *a_out, cudaStream_t stream);
+cudaError_t launch_reduce_fused(const void *x, int64_t n_rows, const int32_t *pos,
+                                const float *w, int64_t T, int64_t K, int64_t H, int in_dtype,
+                                int out_dtype, void *out, int32_t *err, cudaStream_t stream);
+
+// grouped_gemm.cu
+cudaError_t launch_grouped_gemm(bool gate_up, int dtype, const void *a, const void *w0,
+                                const void *w1, const int32_t *sizes, const int32_t *offsets,
+                                const int32_t *padded, const int32_t *gidx, int64_t m_blocks,
+                                const float *row_weights, int64_t n_rows, int64_t K, int64_t N,
+                                int64_t E, void *out, int32_t *err, cudaStream_t stream);
+
+}  // namespace moe

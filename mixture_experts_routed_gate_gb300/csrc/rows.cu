@@ -1,0 +1,206 @@
+// rows.cu -- the two row-moving steps of the routed MoE forward: the gather of
+// token rows into expert order and the moe_reduce_fused combine.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+// ---------------------------------------------------------------------------
+// gather: a_out[r, :] = x[sorted_token_idx[r], :]  (CSDN "forward", step 3)
+// One warp per row, 16-byte vectors, 4 in flight per lane.
+// ---------------------------------------------------------------------------
+constexpr int GA_WARPS = 8;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__global__ void __launch_bounds__(GA_WARPS * 32)
+    gather_rows_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ idx,
+                       int64_t n_rows, int nvec, uint4 *__restrict__ out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * GA_WARPS + warp;
+    if (r >= n_rows) return;
+    const uint4 *src = x + static_cast<int64_t>(__ldg(idx + r)) * nvec;
+    uint4 *dst = out + r * nvec;
+    int v = lane;
+    for (; v + 96 < nvec; v += 128) {
+        const uint4 a = ld_stream(src + v), b = ld_stream(src + v + 32);
+        const uint4 c = ld_stream(src + v + 64), d = ld_stream(src + v + 96);
+        dst[v] = a;
+        dst[v + 32] = b;
+        dst[v + 64] = c;
+        dst[v + 96] = d;
+    }
+    for (; v < nvec; v += 32) dst[v] = ld_stream(src + v);
+}
+
+// ---------------------------------------------------------------------------
+// moe_reduce_fused (TileOPs-Metax PR #55, section 1): one thread per 8
+// consecutive hidden elements of one token.  The K slot rows are gathered
+// with all loads of a group of 8 slots issued before any is consumed (the
+// multi-slot look-ahead), then accumulated in ascending slot order in fp32 as
+// acc = acc + (w * x), each product and sum rounded separately, padding
+// slots (pos < 0) skipped, and the result cast once.  With that fixed order
+// and rounding the result is the same bit pattern as the plain definition.
+// ---------------------------------------------------------------------------
+constexpr int RD_THREADS = 128;
+constexpr int RD_LOOKAHEAD = 8;
+
+template <typename TIn> struct Vec8;
+template <> struct Vec8<__half> { uint4 v; };
+template <> struct Vec8<__nv_bfloat16> { uint4 v; };
+template <> struct Vec8<float> { uint4 a, b; };
+
+template <typename TIn>
+__device__ __forceinline__ Vec8<TIn> load8(const TIn *p);
+template <>
+__device__ __forceinline__ Vec8<__half> load8<__half>(const __half *p) {
+    return Vec8<__half>{ld_stream(reinterpret_cast<const uint4 *>(p))};
+}
+template <>
+__device__ __forceinline__ Vec8<__nv_bfloat16> load8<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    return Vec8<__nv_bfloat16>{ld_stream(reinterpret_cast<const uint4 *>(p))};
+}
+template <>
+__device__ __forceinline__ Vec8<float> load8<float>(const float *p) {
+    const uint4 *q = reinterpret_cast<const uint4 *>(p);
+    return Vec8<float>{ld_stream(q), ld_stream(q + 1)};
+}
+
+__device__ __forceinline__ void unpack8(const Vec8<__nv_bfloat16> &v, float (&f)[8]) {
+    const uint32_t w[4] = {v.v.x, v.v.y, v.v.z, v.v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 p = unpack2<kBF16>(w[i]);
+        f[2 * i] = p.x;
+        f[2 * i + 1] = p.y;
+    }
+}
+__device__ __forceinline__ void unpack8(const Vec8<__half> &v, float (&f)[8]) {
+    const uint32_t w[4] = {v.v.x, v.v.y, v.v.z, v.v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 p = unpack2<kF16>(w[i]);
+        f[2 * i] = p.x;
+        f[2 * i + 1] = p.y;
+    }
+}
+__device__ __forceinline__ void unpack8(const Vec8<float> &v, float (&f)[8]) {
+    const uint32_t w[8] = {v.a.x, v.a.y, v.a.z, v.a.w, v.b.x, v.b.y, v.b.z, v.b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(w[i]);
+}
+
+template <typename TOut>
+__device__ __forceinline__ void store8(TOut *p, const float (&f)[8]);
+template <>
+__device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16 *p, const float (&f)[8]) {
+    *reinterpret_cast<uint4 *>(p) = make_uint4(pack2<kBF16>(f[0], f[1]), pack2<kBF16>(f[2], f[3]),
+                                               pack2<kBF16>(f[4], f[5]), pack2<kBF16>(f[6], f[7]));
+}
+template <>
+__device__ __forceinline__ void store8<__half>(__half *p, const float (&f)[8]) {
+    *reinterpret_cast<uint4 *>(p) = make_uint4(pack2<kF16>(f[0], f[1]), pack2<kF16>(f[2], f[3]),
+                                               pack2<kF16>(f[4], f[5]), pack2<kF16>(f[6], f[7]));
+}
+template <>
+__device__ __forceinline__ void store8<float>(float *p, const float (&f)[8]) {
+    float4 *q = reinterpret_cast<float4 *>(p);
+    q[0] = make_float4(f[0], f[1], f[2], f[3]);
+    q[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+template <typename TIn, typename TOut>
+__global__ void __launch_bounds__(RD_THREADS)
+    reduce_fused_kernel(const TIn *__restrict__ x, int64_t n_rows,
+                        const int32_t *__restrict__ pos, const float *__restrict__ w, int64_t T,
+                        int K, int H, TOut *__restrict__ out, int32_t *__restrict__ err) {
+    const int vpr = H >> 3;  // 8-element vectors per row
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * RD_THREADS + threadIdx.x;
+    const int64_t t = gid / vpr;
+    if (t >= T) return;
+    const int h0 = static_cast<int>(gid - t * vpr) * 8;
+    const int32_t *prow = pos + t * K;
+    const float *wrow = w ? w + t * K : nullptr;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    bool bad = false;
+    for (int k0 = 0; k0 < K; k0 += RD_LOOKAHEAD) {
+        Vec8<TIn> buf[RD_LOOKAHEAD];
+        bool use[RD_LOOKAHEAD];
+        float wk[RD_LOOKAHEAD];
+#pragma unroll
+        for (int j = 0; j < RD_LOOKAHEAD; ++j) {
+            use[j] = false;
+            wk[j] = 1.0f;
+            if (k0 + j < K) {
+                const int p = __ldg(prow + k0 + j);
+                use[j] = p >= 0 && p < n_rows;
+                bad |= (p < -1) || (p >= n_rows);
+                if (wrow) wk[j] = __ldg(wrow + k0 + j);
+                if (use[j]) buf[j] = load8<TIn>(x + static_cast<int64_t>(p) * H + h0);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < RD_LOOKAHEAD; ++j) {
+            if (use[j]) {
+                float f[8];
+                unpack8(buf[j], f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wk[j], f[i]));
+            }
+        }
+    }
+    store8<TOut>(out + t * H + h0, acc);
+    if (bad && err) atomicExch(err, kErrDeviceFlag);
+}
+
+template <typename TIn, typename TOut>
+cudaError_t launch_reduce_typed(const void *x, int64_t n_rows, const int32_t *pos, const float *w,
+                                int64_t T, int64_t K, int64_t H, void *out, int32_t *err,
+                                cudaStream_t stream) {
+    const int64_t threads = T * (H / 8);
+    const int64_t blocks = (threads + RD_THREADS - 1) / RD_THREADS;
+    reduce_fused_kernel<TIn, TOut><<<static_cast<unsigned>(blocks), RD_THREADS, 0, stream>>>(
+        static_cast<const TIn *>(x), n_rows, pos, w, T, static_cast<int>(K), static_cast<int>(H),
+        static_cast<TOut *>(out), err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gather_rows(const void *x, const int32_t *sorted_token_idx, int64_t n_rows,
+                               int64_t d_h, int elem_bytes, void *a_out, cudaStream_t stream) {
+    if (n_rows <= 0) return cudaSuccess;
+    const int nvec = static_cast<int>(d_h * elem_bytes / 16);
+    const int64_t blocks = (n_rows + GA_WARPS - 1) / GA_WARPS;
+    gather_rows_kernel<<<static_cast<unsigned>(blocks), GA_WARPS * 32, 0, stream>>>(
+        static_cast<const uint4 *>(x), sorted_token_idx, n_rows, nvec, static_cast<uint4 *>(a_out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_fused(const void *x, int64_t n_rows, const int32_t *pos,
+                                const float *w, int64_t T, int64_t K, int64_t H, int in_dtype,
+                                int out_dtype, void *out, int32_t *err, cudaStream_t stream) {
+    if (T <= 0) return cudaSuccess;
+    if (in_dtype == kBF16 && out_dtype == kBF16)
+        return launch_reduce_typed<__nv_bfloat16, __nv_bfloat16>(x, n_rows, pos, w, T, K, H, out, err, stream);
+    if (in_dtype == kF16 && out_dtype == kF16)
+        return launch_reduce_typed<__half, __half>(x, n_rows, pos, w, T, K, H, out, err, stream);
+    if (in_dtype == kF32 && out_dtype == kF32)
+        return launch_reduce_typed<float, float>(x, n_rows, pos, w, T, K, H, out, err, stream);
+    if (in_dtype == kF32 && out_dtype == kBF16)
+        return launch_reduce_typed<float, __nv_bfloat16>(x, n_rows, pos, w, T, K, H, out, err, stream);
+    if (in_dtype == kF32 && out_dtype == kF16)
+        return launch_reduce_typed<float, __half>(x, n_rows, pos, w, T, K, H, out, err, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -109,9 +109,17 @@ static uint16_t float_to_bf16(float f)
     return (uint16_t)upper;  /* carry into the exponent gives inf correctly */
 }
 
+/* Every binary16 pattern widened once (the table is half_to_float itself). */
+static float g_half_table[65536];
+static pthread_once_t g_half_once = PTHREAD_ONCE_INIT;
+static void fill_half_table(void)
+{
+    for (uint32_t b = 0; b < 65536u; ++b) g_half_table[b] = half_to_float((uint16_t)b);
+}
+
 static float load_elem(const void *p, int64_t i, int dtype)
 {
-    if (dtype == OR_F16) return half_to_float(((const uint16_t *)p)[i]);
+    if (dtype == OR_F16) return g_half_table[((const uint16_t *)p)[i]];
     if (dtype == OR_BF16) return bf16_to_float(((const uint16_t *)p)[i]);
     return ((const float *)p)[i];
 }
@@ -125,13 +133,17 @@ static void store_elem(void *p, int64_t i, int dtype, float v)
 
 static int dtype_ok(int d) { return d == OR_F16 || d == OR_BF16 || d == OR_F32; }
 
+static void oracle_init(void) { pthread_once(&g_half_once, fill_half_table); }
+
 void oracle_decode(const void *src, int dtype, int64_t n, float *dst)
 {
+    oracle_init();
     for (int64_t i = 0; i < n; ++i) dst[i] = load_elem(src, i, dtype);
 }
 
 void oracle_encode(const float *src, int dtype, int64_t n, void *dst)
 {
+    oracle_init();
     for (int64_t i = 0; i < n; ++i) store_elem(dst, i, dtype, src[i]);
 }
 
@@ -236,6 +248,7 @@ static void gate_rows(int64_t lo, int64_t hi, void *vctx)
 int oracle_gate_logits(const void *x, const void *wg, const float *bias, int64_t T,
                        int64_t d_h, int64_t E, int dtype, float *logits, int nthreads)
 {
+    oracle_init();
     if (!x || !wg || !logits || T < 0 || E <= 0 || d_h <= 0 || d_h % 256 != 0 ||
         !dtype_ok(dtype))
         return OR_EINVAL;
@@ -386,6 +399,7 @@ int oracle_build_dispatch(const int32_t *topk_idx, const float *topk_w, int64_t 
 int oracle_gather_rows(const void *x, const int32_t *sorted_token_idx, int64_t n_rows,
                        int64_t T, int64_t d_h, int dtype, void *a_out)
 {
+    oracle_init();
     if (!x || !sorted_token_idx || !a_out || n_rows < 0 || d_h <= 0 || !dtype_ok(dtype))
         return OR_EINVAL;
     size_t es = dtype == OR_F32 ? 4 : 2;
@@ -404,6 +418,38 @@ int oracle_gather_rows(const void *x, const int32_t *sorted_token_idx, int64_t n
 
 /* SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z)), exact math in double. */
 static double silu_d(double z) { return z / (1.0 + exp(-z)); }
+
+/* Stage 1 for one row: h[rh, :] = rt(silu(A[ra] W_gate[g]^T) * (A[ra] W_up[g]^T)). */
+static void stage1_row(const void *a, int64_t ra, const void *w_gate, const void *w_up, int64_t g,
+                       int64_t d_h, int64_t d_e, int dtype, void *h, int64_t rh)
+{
+    for (int64_t n = 0; n < d_e; ++n) {
+        const int64_t wrow = (g * d_e + n) * d_h;
+        float gate = 0.0f, up = 0.0f;
+        for (int64_t j = 0; j < d_h; ++j) {
+            float av = load_elem(a, ra * d_h + j, dtype);
+            gate = gate + av * load_elem(w_gate, wrow + j, dtype);
+            up = up + av * load_elem(w_up, wrow + j, dtype);
+        }
+        float s = (float)silu_d((double)gate);
+        float hv = s * up;
+        store_elem(h, rh * d_e + n, dtype, hv);
+    }
+}
+
+/* Stage 2 for one row: y[ry, :] = rt((h[rh] W_down[g]^T) * rw). */
+static void stage2_row(const void *h, int64_t rh, const void *w_down, int64_t g, int64_t d_h,
+                       int64_t d_e, int dtype, const float *rw, void *y, int64_t ry)
+{
+    for (int64_t o = 0; o < d_h; ++o) {
+        const int64_t wrow = (g * d_h + o) * d_e;
+        float acc = 0.0f;
+        for (int64_t j = 0; j < d_e; ++j)
+            acc = acc + load_elem(h, rh * d_e + j, dtype) * load_elem(w_down, wrow + j, dtype);
+        if (rw) acc = acc * (*rw);
+        store_elem(y, ry * d_h + o, dtype, acc);
+    }
+}
 
 typedef struct {
     const void *a, *w1, *w2; /* stage 1: a, w_gate, w_up; stage 2: h, w_down */
@@ -441,34 +487,62 @@ static void gemm_blocks(int64_t lo, int64_t hi, void *vctx)
         if (rows < 0) rows = 0;
         for (int64_t i = 0; i < rows; ++i) {
             int64_t r = m_start + i;
-            if (c->stage == 1) {
-                const int64_t K = c->d_h;
-                for (int64_t n = 0; n < c->d_e; ++n) {
-                    const int64_t wrow = (g * c->d_e + n) * K;
-                    float gate = 0.0f, up = 0.0f;
-                    for (int64_t j = 0; j < K; ++j) {
-                        float a = load_elem(c->a, r * K + j, c->dtype);
-                        gate = gate + a * load_elem(c->w1, wrow + j, c->dtype);
-                        up = up + a * load_elem(c->w2, wrow + j, c->dtype);
-                    }
-                    float s = (float)silu_d((double)gate);
-                    float h = s * up;
-                    store_elem(c->out, r * c->d_e + n, c->dtype, h);
-                }
-            } else {
-                const int64_t K = c->d_e;
-                for (int64_t o = 0; o < c->d_h; ++o) {
-                    const int64_t wrow = (g * c->d_h + o) * K;
-                    float acc = 0.0f;
-                    for (int64_t j = 0; j < K; ++j)
-                        acc = acc + load_elem(c->a, r * K + j, c->dtype) *
-                                        load_elem(c->w1, wrow + j, c->dtype);
-                    if (c->row_weights) acc = acc * c->row_weights[r];
-                    store_elem(c->out, r * c->d_h + o, c->dtype, acc);
-                }
-            }
+            if (c->stage == 1)
+                stage1_row(c->a, r, c->w1, c->w2, g, c->d_h, c->d_e, c->dtype, c->out, r);
+            else
+                stage2_row(c->a, r, c->w1, g, c->d_h, c->d_e, c->dtype,
+                           c->row_weights ? c->row_weights + r : NULL, c->out, r);
         }
     }
+}
+
+/* Per-row forms of the two stages for sampled checks of large problems: row i
+ * of the inputs belongs to expert row_expert[i]; same arithmetic as above. */
+typedef struct {
+    const void *in, *w1, *w2; const int32_t *row_expert; const float *rw;
+    int64_t d_h, d_e; int dtype; void *out; int stage;
+} rows_ctx;
+
+static void rows_range(int64_t lo, int64_t hi, void *vctx)
+{
+    rows_ctx *c = (rows_ctx *)vctx;
+    for (int64_t i = lo; i < hi; ++i) {
+        if (c->stage == 1)
+            stage1_row(c->in, i, c->w1, c->w2, c->row_expert[i], c->d_h, c->d_e, c->dtype, c->out, i);
+        else
+            stage2_row(c->in, i, c->w1, c->row_expert[i], c->d_h, c->d_e, c->dtype,
+                       c->rw ? c->rw + i : NULL, c->out, i);
+    }
+}
+
+int oracle_rows_gate_up_silu(const void *a_rows, const int32_t *row_expert, int64_t n,
+                             const void *w_gate, const void *w_up, int64_t d_h, int64_t d_e,
+                             int64_t E, int dtype, void *h_rows, int nthreads)
+{
+    oracle_init();
+    if (!a_rows || !row_expert || !w_gate || !w_up || !h_rows || n < 0 || d_h <= 0 ||
+        d_e <= 0 || !dtype_ok(dtype))
+        return OR_EINVAL;
+    for (int64_t i = 0; i < n; ++i)
+        if (row_expert[i] < 0 || row_expert[i] >= E) return OR_EINVAL;
+    rows_ctx c = {a_rows, w_gate, w_up, row_expert, NULL, d_h, d_e, dtype, h_rows, 1};
+    parallel_for(n, nthreads, rows_range, &c);
+    return OR_OK;
+}
+
+int oracle_rows_down(const void *h_rows, const int32_t *row_expert, int64_t n, const void *w_down,
+                     const float *row_weights, int64_t d_h, int64_t d_e, int64_t E, int dtype,
+                     void *y_rows, int nthreads)
+{
+    oracle_init();
+    if (!h_rows || !row_expert || !w_down || !y_rows || n < 0 || d_h <= 0 || d_e <= 0 ||
+        !dtype_ok(dtype))
+        return OR_EINVAL;
+    for (int64_t i = 0; i < n; ++i)
+        if (row_expert[i] < 0 || row_expert[i] >= E) return OR_EINVAL;
+    rows_ctx c = {h_rows, w_down, NULL, row_expert, row_weights, d_h, d_e, dtype, y_rows, 2};
+    parallel_for(n, nthreads, rows_range, &c);
+    return OR_OK;
 }
 
 static int check_tables(const int32_t *sizes, const int32_t *offsets, const int32_t *padded,
@@ -495,6 +569,7 @@ int oracle_grouped_gate_up_silu(const void *a, const void *w_gate, const void *w
                                 int64_t block_m, int64_t n_rows, int64_t d_h, int64_t d_e,
                                 int64_t E, int dtype, void *h, int nthreads)
 {
+    oracle_init();
     if (!a || !w_gate || !w_up || !h || d_h <= 0 || d_e <= 0 || !dtype_ok(dtype) ||
         !check_tables(group_sizes, group_offsets, group_padded_offsets, group_idx_for_bx,
                       m_blocks, n_rows, E, block_m))
@@ -511,6 +586,7 @@ int oracle_grouped_down(const void *h, const void *w_down, const int32_t *group_
                         const float *row_weights, int64_t n_rows, int64_t d_h, int64_t d_e,
                         int64_t E, int dtype, void *y, int nthreads)
 {
+    oracle_init();
     if (!h || !w_down || !y || d_h <= 0 || d_e <= 0 || !dtype_ok(dtype) ||
         !check_tables(group_sizes, group_offsets, group_padded_offsets, group_idx_for_bx,
                       m_blocks, n_rows, E, block_m))
@@ -565,6 +641,7 @@ int oracle_reduce_fused(const void *x, int64_t n_rows, const int32_t *token_topk
                         int in_dtype, int out_dtype, void *out, int32_t *err_flag,
                         int nthreads)
 {
+    oracle_init();
     if (!out || !token_topk_to_pos || T < 0 || K <= 0 || H <= 0 || n_rows < 0 ||
         (!x && n_rows > 0) || !dtype_ok(in_dtype) || !dtype_ok(out_dtype))
         return OR_EINVAL;
@@ -639,6 +716,7 @@ int oracle_moe_tokens_dense(const void *x, const void *w_gate, const void *w_up,
                             int64_t d_e, int64_t E, int64_t k, int dtype, void *out,
                             int nthreads)
 {
+    oracle_init();
     if (!x || !w_gate || !w_up || !w_down || !topk_idx || !topk_w || !tokens || !out ||
         d_h <= 0 || d_e <= 0 || E <= 0 || k <= 0 || !dtype_ok(dtype))
         return OR_EINVAL;

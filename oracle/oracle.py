@@ -62,6 +62,8 @@ def _load():
         "oracle_grouped_down": (I, [P, P, P, P, P, P, I64, I64, P, I64, I64, I64, I64, I, P, I]),
         "oracle_reduce_fused": (I, [P, I64, P, P, I64, I64, I64, I, I, P, P, I]),
         "oracle_moe_tokens_dense": (I, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I64, I, P, I]),
+        "oracle_rows_gate_up_silu": (I, [P, P, I64, P, P, I64, I64, I64, I, P, I]),
+        "oracle_rows_down": (I, [P, P, I64, P, P, I64, I64, I64, I, P, I]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -206,6 +208,31 @@ def grouped_down(h, w_down, tables: dict, dtype: str, row_weights=None, block_m:
     _check(_load().oracle_grouped_down(
         _ptr(hb), _ptr(wd), _ptr(s), _ptr(o), _ptr(p), _ptr(g), g.size, block_m, _ptr(rw),
         n_rows, d_h, d_e, E, DTYPE_CODES[dtype], _ptr(y), nthreads), "grouped_down")
+    return y
+
+
+def rows_gate_up_silu(a_rows, row_expert, w_gate, w_up, dtype: str, nthreads: int = 0):
+    """Stage 1 for a list of rows; row i uses expert row_expert[i]."""
+    ab, wg, wu = _bits(a_rows, dtype), _bits(w_gate, dtype), _bits(w_up, dtype)
+    n, d_h = ab.shape
+    E, d_e, _ = wg.shape
+    re = np.ascontiguousarray(row_expert, dtype=np.int32)
+    h = _empty((n, d_e), dtype)
+    _check(_load().oracle_rows_gate_up_silu(_ptr(ab), _ptr(re), n, _ptr(wg), _ptr(wu), d_h, d_e, E,
+                                            DTYPE_CODES[dtype], _ptr(h), nthreads), "rows_gate_up_silu")
+    return h
+
+
+def rows_down(h_rows, row_expert, w_down, dtype: str, row_weights=None, nthreads: int = 0):
+    """Stage 2 for a list of rows; row i uses expert row_expert[i]."""
+    hb, wd = _bits(h_rows, dtype), _bits(w_down, dtype)
+    n, d_e = hb.shape
+    E, d_h, _ = wd.shape
+    re = np.ascontiguousarray(row_expert, dtype=np.int32)
+    rw = None if row_weights is None else np.ascontiguousarray(row_weights, dtype=np.float32)
+    y = _empty((n, d_h), dtype)
+    _check(_load().oracle_rows_down(_ptr(hb), _ptr(re), n, _ptr(wd), _ptr(rw), d_h, d_e, E,
+                                    DTYPE_CODES[dtype], _ptr(y), nthreads), "rows_down")
     return y
 
 

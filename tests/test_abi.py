@@ -1,0 +1,105 @@
+"""The C-ABI library loads and exports every entry point the public header
+declares; host-side sizing and argument checks work without a GPU (none of
+these calls reaches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_routed_gate_gb300 import _build, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_routed_gate.h")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return binding.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MOE_API[^;(]*?\b(moe_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for required in ("moe_gate_topk", "moe_build_dispatch", "moe_grouped_gate_up_silu",
+                     "moe_grouped_down", "moe_reduce_fused", "moe_forward"):
+        assert required in names
+    assert sorted(binding.exported_symbols()) == names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_sizing_helpers(lib, oracle):
+    for T, k, E in [(64, 2, 8), (64, 6, 64), (4096, 8, 256), (0, 2, 8), (1, 1, 1)]:
+        assert lib.moe_num_m_blocks(T, k, E, 128) == oracle.num_m_blocks(T, k, E, 128)
+    assert lib.moe_num_m_blocks(4096, 8, 256, 128) == 512
+    assert lib.moe_num_m_blocks(-1, 2, 8, 128) == -1
+    assert lib.moe_gate_topk_workspace_bytes(64, 8) == 64 * 8 * 4
+    ws = lib.moe_forward_workspace_bytes(4096, 7168, 2048, 256, 8, 1)
+    # the gathered rows, h and y dominate: Tk*(2*d_h + d_e)*2 bytes
+    assert ws >= 32768 * (2 * 7168 + 2048) * 2
+    assert ws % 256 == 0
+    offs = [lib.moe_forward_workspace_offset(4096, 7168, 2048, 256, 8, 1, i) for i in range(14)]
+    assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    assert lib.moe_forward_workspace_offset(4096, 7168, 2048, 256, 8, 1, 14) == -1
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert lib.moe_status_string(s).startswith(b"MOE_")
+    assert lib.moe_status_string(99) == b"unknown moe status"
+
+
+def test_argument_errors_without_launch(lib):
+    """The pages' error cases (hidden % 256 != 0 for the combine) and others are
+    rejected on the host, before any CUDA call."""
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    # reduce: H % 256 != 0
+    assert lib.moe_reduce_fused(fake, 8, fake, None, 4, 2, 200, 1, 1, fake, None, None) == MOE_ERR_INVALID_ARG
+    # reduce: unsupported dtype pair (bf16 in, f32 out)
+    assert lib.moe_reduce_fused(fake, 8, fake, None, 4, 2, 256, 1, 2, fake, None, None) == MOE_ERR_UNSUPPORTED
+    # reduce: null output
+    assert lib.moe_reduce_fused(fake, 8, fake, None, 4, 2, 256, 1, 1, None, None, None) == MOE_ERR_INVALID_ARG
+    # gate: d_hidden % 256 != 0, k > E, f32 activations
+    assert lib.moe_gate_topk(fake, fake, None, 4, 200, 8, 2, 1, fake, fake, fake, 1 << 20, None) == MOE_ERR_INVALID_ARG
+    assert lib.moe_gate_topk(fake, fake, None, 4, 256, 8, 9, 1, fake, fake, fake, 1 << 20, None) == MOE_ERR_INVALID_ARG
+    assert lib.moe_gate_topk(fake, fake, None, 4, 256, 8, 2, 2, fake, fake, fake, 1 << 20, None) == MOE_ERR_UNSUPPORTED
+    # gate: workspace too small
+    assert lib.moe_gate_topk(fake, fake, None, 4, 256, 8, 2, 1, fake, fake, fake, 16, None) == MOE_ERR_WORKSPACE
+    # dispatch: block_m other than 128, workspace too small
+    assert lib.moe_build_dispatch(fake, None, 4, 2, 8, 64, fake, fake, fake, fake, fake, fake, fake,
+                                  fake, 1 << 20, None) == MOE_ERR_INVALID_ARG
+    assert lib.moe_build_dispatch(fake, None, 4, 2, 8, 128, fake, fake, fake, fake, fake, fake, fake,
+                                  fake, 0, None) == MOE_ERR_WORKSPACE
+    # grouped GEMMs: misaligned d_expert, m_blocks larger than the table space
+    assert lib.moe_grouped_gate_up_silu(fake, fake, fake, fake, fake, fake, fake, 3, 8, 256, 100, 8, 1,
+                                        fake, None, None) == MOE_ERR_INVALID_ARG
+    assert lib.moe_grouped_down(fake, fake, fake, fake, fake, fake, 99, None, 8, 256, 128, 8, 1,
+                                fake, None, None) == MOE_ERR_INVALID_ARG
+    # forward: workspace too small, misaligned workspace
+    assert lib.moe_forward(fake, fake, None, fake, fake, fake, 64, 256, 128, 8, 2, 0, P(0x100000), 16,
+                           fake, None, None) == MOE_ERR_WORKSPACE
+    assert lib.moe_forward(fake, fake, None, fake, fake, fake, 64, 256, 128, 8, 2, 0, P(0x100010),
+                           1 << 30, fake, None, None) == MOE_ERR_INVALID_ARG
+    # empty problems are valid no-ops
+    assert lib.moe_reduce_fused(fake, 0, fake, None, 0, 2, 256, 1, 1, fake, None, None) == MOE_OK
+    assert lib.moe_gather_rows(fake, fake, 0, 4, 256, 1, fake, None) == MOE_OK
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(_build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.lib()

@@ -1,0 +1,137 @@
+"""The whole routed forward (moe_forward) vs the oracle on the three MoE
+workloads.  The small workloads are compared on every output; the prefill
+workload (T=4096, d_hidden 7168, d_expert 2048, 256 experts, top-8, bf16) at
+full size and in the benchmark's launch configuration on its routing and
+tables (all, bit for bit) and on sampled h / y rows and output tokens that
+the oracle computes one by one."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import MOE_TOL, assert_bits_equal, assert_close, bits, require_cuda
+from mixture_experts_routed_gate_gb300 import binding, workloads
+
+pytestmark = pytest.mark.gpu
+
+TABLES = ("group_sizes", "group_offsets", "group_padded_offsets", "group_idx_for_bx",
+          "sorted_token_idx", "token_topk_to_pos")
+
+
+def _run_forward(d, cfg, T=None):
+    dev = d["x"].device
+    T = d["x"].shape[0] if T is None else T
+    ws = torch.empty(binding.forward_workspace_bytes(T, cfg.d_hidden, cfg.d_expert, cfg.n_experts,
+                                                     cfg.top_k, d["x"].dtype), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = binding.moe_forward(d["x"], d["wg"], d["bias"], d["w_gate"], d["w_up"], d["w_down"],
+                              cfg.top_k, ws=ws, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, int(err.item())
+    views = binding.forward_workspace_views(ws, T, cfg.d_hidden, cfg.d_expert, cfg.n_experts,
+                                            cfg.top_k, d["x"].dtype)
+    return out, views
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_forward_small_workloads(oracle, name):
+    dev = require_cuda()
+    cfg = workloads.MOE_CONFIGS[name]
+    d = workloads.make_moe_inputs(cfg, device=dev)
+    out, views = _run_forward(d, cfg)
+    nb = {n: (bits(v) if v is not None else None) for n, v in d.items()}
+    ref = oracle.moe_forward(nb["x"], nb["wg"], nb["bias"], nb["w_gate"], nb["w_up"], nb["w_down"],
+                             cfg.top_k, cfg.dtype)
+    assert_bits_equal(views["topk_idx"].cpu().numpy(), ref["topk_idx"], "topk_idx")
+    for n in TABLES:
+        assert_bits_equal(views[n].cpu().numpy().reshape(ref[n].shape), ref[n], n)
+    rtol, atol = MOE_TOL[cfg.dtype]
+    assert np.allclose(views["topk_w"].cpu().numpy(), ref["topk_w"], rtol=1e-5, atol=1e-7)
+    assert_close(bits(views["h"]), ref["h"], cfg.dtype, rtol, atol, "h")
+    assert_close(bits(views["y"]), ref["y"], cfg.dtype, rtol, atol, "y")
+    assert_close(bits(out), ref["out"], cfg.dtype, rtol, atol, "out")
+
+
+def test_forward_repeat_is_stateless():
+    """Two calls on the same input give the same bits (nothing carries over
+    from call to call)."""
+    dev = require_cuda()
+    cfg = workloads.MOE_CONFIGS["tiny"]
+    d = workloads.make_moe_inputs(cfg, device=dev)
+    o1, _ = _run_forward(d, cfg)
+    o1 = o1.clone()
+    o2, _ = _run_forward(d, cfg)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+@pytest.mark.parametrize("T", [1, 5, 200])
+def test_forward_token_counts(oracle, T):
+    dev = require_cuda()
+    cfg = workloads.MOE_CONFIGS["tiny"]
+    d = workloads.make_moe_inputs(cfg, device=dev, T=T)
+    out, views = _run_forward(d, cfg)
+    nb = {n: (bits(v) if v is not None else None) for n, v in d.items()}
+    ref = oracle.moe_forward(nb["x"], nb["wg"], nb["bias"], nb["w_gate"], nb["w_up"], nb["w_down"],
+                             cfg.top_k, cfg.dtype)
+    for n in TABLES:
+        assert_bits_equal(views[n].cpu().numpy().reshape(ref[n].shape), ref[n], n)
+    assert_close(bits(out), ref["out"], cfg.dtype, *MOE_TOL[cfg.dtype], "out")
+
+
+def _compact(w, experts):
+    """The listed experts' slices of a stacked weight, on the host."""
+    idx = torch.as_tensor(experts, dtype=torch.long, device=w.device)
+    return bits(w.index_select(0, idx))
+
+
+@pytest.mark.slow
+def test_forward_prefill_full_size(oracle):
+    dev = require_cuda()
+    cfg = workloads.MOE_CONFIGS["prefill"]
+    d = workloads.make_moe_inputs(cfg, device=dev)
+    out, views = _run_forward(d, cfg)
+    k = cfg.top_k
+    # routing: all tokens, bit for bit (logits too)
+    ref_logits = oracle.gate_logits(bits(d["x"]), bits(d["wg"]), d["bias"].cpu().numpy(), cfg.dtype)
+    assert_bits_equal(views["logits"].cpu().numpy().view(np.uint32), ref_logits.view(np.uint32), "logits")
+    ref_idx, ref_w = oracle.topk_softmax(ref_logits, k)
+    assert_bits_equal(views["topk_idx"].cpu().numpy(), ref_idx, "topk_idx")
+    assert np.allclose(views["topk_w"].cpu().numpy(), ref_w, rtol=1e-5, atol=1e-7)
+    tab = oracle.build_dispatch(ref_idx, ref_w, cfg.n_experts, 128)
+    for n in TABLES:
+        assert_bits_equal(views[n].cpu().numpy().reshape(tab[n].shape), tab[n], n)
+    sizes = tab["group_sizes"]
+    assert sizes.max() > 1000 and (sizes == 0).any(), "the Zipf bias should skew the loads"
+
+    # sampled rows of h and y: first and last rows, both ends of the largest
+    # expert and of its ragged last block, and rows of small experts
+    offs = tab["group_offsets"]
+    big = int(np.argmax(sizes))
+    small = [int(e) for e in np.argsort(sizes) if 0 < sizes[e] < 8][:2]
+    rows = {0, int(sizes.sum()) - 1, int(offs[big]), int(offs[big] + sizes[big] - 1),
+            int(offs[big] + (sizes[big] // 128) * 128 - 1), int(offs[big] + 127), int(offs[big] + 128)}
+    for e in small:
+        rows |= {int(offs[e]), int(offs[e] + sizes[e] - 1)}
+    rows = np.array(sorted(r for r in rows if 0 <= r < sizes.sum()), dtype=np.int64)
+    row_expert = np.searchsorted(np.cumsum(sizes), rows, side="right").astype(np.int32)
+    experts = np.unique(row_expert)
+    remap = {int(e): i for i, e in enumerate(experts)}
+    re = np.array([remap[int(e)] for e in row_expert], np.int32)
+    x_h = bits(d["x"])
+    a_rows = x_h[tab["sorted_token_idx"][rows]]
+    h_ref = oracle.rows_gate_up_silu(a_rows, re, _compact(d["w_gate"], experts),
+                                     _compact(d["w_up"], experts), cfg.dtype)
+    y_ref = oracle.rows_down(h_ref, re, _compact(d["w_down"], experts), cfg.dtype)
+    rtol, atol = MOE_TOL[cfg.dtype]
+    rows_t = torch.from_numpy(rows).to(dev)
+    assert_close(bits(views["h"].index_select(0, rows_t)), h_ref, cfg.dtype, rtol, atol, "sampled h rows")
+    assert_close(bits(views["y"].index_select(0, rows_t)), y_ref, cfg.dtype, rtol, atol, "sampled y rows")
+
+    # sampled output tokens, computed by the dense per-token brute force
+    tokens = np.array([0, 1, 1234, 2047, 4095], dtype=np.int32)
+    used = np.unique(ref_idx[tokens])
+    remap = {int(e): i for i, e in enumerate(used)}
+    idx_c = np.vectorize(lambda e: remap.get(int(e), 0))(ref_idx).astype(np.int32)
+    want = oracle.moe_tokens_dense(x_h, _compact(d["w_gate"], used), _compact(d["w_up"], used),
+                                   _compact(d["w_down"], used), idx_c, ref_w, tokens, cfg.dtype)
+    got = bits(out.index_select(0, torch.from_numpy(tokens.astype(np.int64)).to(dev)))
+    assert_close(got, want, cfg.dtype, rtol, atol, "sampled output tokens")

@@ -1,0 +1,131 @@
+"""The two grouped GEMM stages (tcgen05 kernels) vs the oracle's block walk.
+
+Tables and gathered rows come from the oracle and are copied to the device,
+so both sides see the same inputs.  Random inputs are compared within the
+MoE tolerances; integer-valued inputs make every fp32 sum exact and are
+compared bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import MOE_TOL, assert_bits_equal, assert_close, bits, require_cuda
+from mixture_experts_routed_gate_gb300 import binding, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _tables_to(dev, tab):
+    return {n: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for n, v in tab.items()}
+
+
+def _routing(rng, T, k, E, skew=False):
+    if skew:
+        p = 1.0 / np.arange(1, E + 1) ** 1.1
+        p /= p.sum()
+        return np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    return np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+
+
+def _from_bits(a, dtype, dev):
+    return workloads.from_numpy_bits(a, dtype).to(dev)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("T,k,E,d_h,d_e,skew", [(300, 4, 6, 512, 256, False),
+                                                (200, 8, 32, 256, 192, True),
+                                                (1, 1, 4, 256, 64, False)])
+def test_grouped_gemms_vs_oracle(oracle, dtype, T, k, E, d_h, d_e, skew):
+    """Several 128-row blocks per expert with ragged tails, empty experts,
+    several N tiles, a partial last N tile (d_e = 192), and a single row."""
+    dev = require_cuda()
+    rng = np.random.default_rng(T + E + d_e)
+    idx = _routing(rng, T, k, E, skew)
+    tab = oracle.build_dispatch(idx, None, E, 128)
+    td = workloads.torch_dtype(dtype)
+    x = torch.randn((T, d_h), generator=torch.Generator().manual_seed(1)).to(td)
+    w_gate = (torch.randn((E, d_e, d_h), generator=torch.Generator().manual_seed(2)) / d_h ** 0.5).to(td)
+    w_up = (torch.randn((E, d_e, d_h), generator=torch.Generator().manual_seed(3)) / d_h ** 0.5).to(td)
+    w_down = (torch.randn((E, d_h, d_e), generator=torch.Generator().manual_seed(4)) / d_e ** 0.5).to(td)
+    a = oracle.gather_rows(bits(x), tab["sorted_token_idx"], dtype)
+    h_ref = oracle.grouped_gate_up_silu(a, bits(w_gate), bits(w_up), tab, dtype)
+    y_ref = oracle.grouped_down(h_ref, bits(w_down), tab, dtype)
+    rw = rng.random(T * k).astype(np.float32)
+    yw_ref = oracle.grouped_down(h_ref, bits(w_down), tab, dtype, row_weights=rw)
+
+    tabd = _tables_to(dev, tab)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    a_d = _from_bits(a, dtype, dev)
+    h = binding.moe_grouped_gate_up_silu(a_d, w_gate.to(dev), w_up.to(dev), tabd, err=err)
+    h_in = _from_bits(h_ref, dtype, dev)  # stage 2 from the oracle's h: isolates stage 2
+    y = binding.moe_grouped_down(h_in, w_down.to(dev), tabd, err=err)
+    yw = binding.moe_grouped_down(h_in, w_down.to(dev), tabd, row_weights=torch.from_numpy(rw).to(dev), err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rtol, atol = MOE_TOL[dtype]
+    assert_close(bits(h), h_ref, dtype, rtol, atol, "h")
+    assert_close(bits(y), y_ref, dtype, rtol, atol, "y")
+    assert_close(bits(yw), yw_ref, dtype, rtol, atol, "y with row weights")
+
+
+def test_grouped_gemms_integer_inputs_bit_exact(oracle):
+    """fp16, small integers, gate logits >= 40 (silu(g) = g in fp32): every
+    sum is exact, so h = rt(G*U) and y = rt(h W_down^T) match bit for bit."""
+    dev = require_cuda()
+    rng = np.random.default_rng(11)
+    T, k, E, d_h, d_e = 260, 2, 3, 256, 128
+    idx = _routing(rng, T, k, E)
+    tab = oracle.build_dispatch(idx, None, E, 128)
+    x = rng.integers(0, 3, (T, d_h)).astype(np.float16)
+    x[:, 0] = 1
+    wg = rng.integers(0, 2, (E, d_e, d_h)).astype(np.float16)
+    wg[:, :, 0] = 40
+    wu = rng.integers(-1, 2, (E, d_e, d_h)).astype(np.float16)
+    wd = rng.integers(-1, 2, (E, d_h, d_e)).astype(np.float16)
+    a = oracle.gather_rows(x.view(np.uint16), tab["sorted_token_idx"], "f16")
+    h_ref = oracle.grouped_gate_up_silu(a, wg.view(np.uint16), wu.view(np.uint16), tab, "f16")
+    # exact small-integer h for stage 2 so that y stays exact in fp16 (|y| < 2048)
+    h_int = rng.integers(-2, 3, (T * k, d_e)).astype(np.float16).view(np.uint16)
+    y_ref = oracle.grouped_down(h_int, wd.view(np.uint16), tab, "f16")
+    tabd = _tables_to(dev, tab)
+    h = binding.moe_grouped_gate_up_silu(_from_bits(a, "f16", dev), torch.from_numpy(wg).to(dev),
+                                         torch.from_numpy(wu).to(dev), tabd)
+    y = binding.moe_grouped_down(_from_bits(h_int, "f16", dev), torch.from_numpy(wd).to(dev), tabd)
+    torch.cuda.synchronize()
+    assert_bits_equal(bits(h), h_ref, "integer h")
+    assert_bits_equal(bits(y), y_ref, "integer y")
+
+
+def test_grouped_gemms_zero_weights():
+    dev = require_cuda()
+    from oracle import oracle
+    rng = np.random.default_rng(12)
+    T, k, E, d_h, d_e = 150, 2, 4, 256, 128
+    tab = _tables_to(dev, oracle.build_dispatch(_routing(rng, T, k, E), None, E, 128))
+    a = torch.randn((T * k, d_h), device=dev).to(torch.bfloat16)
+    wg = torch.randn((E, d_e, d_h), device=dev).to(torch.bfloat16)
+    zero_u = torch.zeros((E, d_e, d_h), device=dev, dtype=torch.bfloat16)
+    h = binding.moe_grouped_gate_up_silu(a, wg, zero_u, tab)
+    assert torch.count_nonzero(h.float()) == 0
+    y = binding.moe_grouped_down(torch.randn((T * k, d_e), device=dev).to(torch.bfloat16),
+                                 torch.zeros((E, d_h, d_e), device=dev, dtype=torch.bfloat16), tab)
+    assert torch.count_nonzero(y.float()) == 0
+
+
+def test_grouped_gemm_rows_outside_the_tables_untouched(oracle):
+    """Stage 1 writes only the rows the tables own: with a table built for fewer
+    pairs than the buffer holds, the rows past the end keep their canary."""
+    dev = require_cuda()
+    rng = np.random.default_rng(13)
+    T, k, E, d_h, d_e = 100, 2, 5, 256, 128
+    tab = oracle.build_dispatch(_routing(rng, T, k, E), None, E, 128)
+    n = T * k
+    a = torch.randn((n + 40, d_h), device=dev).to(torch.float16)
+    h = torch.full((n + 40, d_e), 7.0, device=dev, dtype=torch.float16)
+    wg = torch.randn((E, d_e, d_h), device=dev).to(torch.float16) * 0.05
+    wu = torch.randn((E, d_e, d_h), device=dev).to(torch.float16) * 0.05
+    tabd = _tables_to(dev, tab)
+    # the kernel sees n_rows = n: pass views of the first n rows
+    binding.moe_grouped_gate_up_silu(a[:n], wg, wu, tabd, h=h[:n])
+    torch.cuda.synchronize()
+    assert (h[n:].float() == 7.0).all()
+    assert not (h[:n].float() == 7.0).all(dim=1).any()
