@@ -120,6 +120,33 @@ MOE_API moe_status_t moe_build_dispatch(const int32_t *topk_idx, const float *to
                                 size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_build_dispatch without a workspace argument.  This entry point has no
+ * counterpart on the pages; it exists for callers that cannot allocate
+ * device memory: code running while a CUDA graph is being captured (where
+ * cudaMalloc is not allowed) and engines whose device memory is planned up
+ * front by another runtime, so that nothing may be allocated per call.
+ * It computes exactly what moe_build_dispatch computes, with the scratch
+ * histograms in a fixed 1 MiB array inside the library (every GPU that loads
+ * the library holds it until the process exits); it allocates nothing.
+ *   - Limit: ceil(T*k / 2048) * E <= 262144 counters (for E = 256 that is up
+ *     to 2,097,152 token-expert pairs); larger problems return
+ *     MOE_ERR_WORKSPACE without launching.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (other
+ *     streams, other threads) race and give undefined tables.  Nothing needs
+ *     clearing between calls: the first kernel writes every counter it reads.
+ * Arguments, outputs and errors otherwise as moe_build_dispatch.
+ */
+MOE_API moe_status_t moe_build_dispatch_noalloc(const int32_t *topk_idx, const float *topk_w,
+                                        int64_t T, int64_t k, int64_t E, int64_t block_m,
+                                        int32_t *group_sizes, int32_t *group_offsets,
+                                        int32_t *group_padded_offsets,
+                                        int32_t *group_idx_for_bx, int32_t *sorted_token_idx,
+                                        float *sorted_row_weight, int32_t *token_topk_to_pos,
+                                        moe_stream_t stream);
+
+/*
  * Row gather (CSDN "forward", step 3: stacked_expert_tokens[r] = x_flat[token of r]).
  *   a_out[r, :] = x[sorted_token_idx[r], :] for r < n_rows.  x [T, d_h].
  * sorted_token_idx values must lie in [0, T).  d_h * elem_size % 16 == 0.

@@ -56,6 +56,7 @@ def lib():
         "moe_forward_workspace_offset": (I64, [I64, I64, I64, I64, I64, I, I]),
         "moe_gate_topk": (I, [P, P, P, I64, I64, I64, I64, I, P, P, P, SZ, P]),
         "moe_build_dispatch": (I, [P, P, I64, I64, I64, I64, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_build_dispatch_noalloc": (I, [P, P, I64, I64, I64, I64, P, P, P, P, P, P, P, P]),
         "moe_gather_rows": (I, [P, P, I64, I64, I64, I, P, P]),
         "moe_grouped_gate_up_silu": (I, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, P, P]),
         "moe_grouped_down": (I, [P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I, P, P, P]),
@@ -74,6 +75,7 @@ def exported_symbols():
     return ["moe_status_string", "moe_num_m_blocks", "moe_gate_topk_workspace_bytes",
             "moe_build_dispatch_workspace_bytes", "moe_forward_workspace_bytes",
             "moe_forward_workspace_offset", "moe_gate_topk", "moe_build_dispatch",
+            "moe_build_dispatch_noalloc",
             "moe_gather_rows", "moe_grouped_gate_up_silu", "moe_grouped_down",
             "moe_reduce_fused", "moe_forward"]
 
@@ -179,6 +181,41 @@ def moe_build_dispatch(topk_idx, topk_w, E: int, block_m: int = BLOCK_M, out=Non
             _ptr(out["group_idx_for_bx"]), _ptr(out["sorted_token_idx"]),
             _ptr(out["sorted_row_weight"]), _ptr(out["token_topk_to_pos"]), _ptr(ws),
             ws.numel() * ws.element_size(), _stream(dev)), "moe_build_dispatch")
+    return out
+
+
+def _dispatch_outputs(T, k, E, block_m, dev):
+    i32 = dict(dtype=torch.int32, device=dev)
+    mb = num_m_blocks(T, k, E, block_m)
+    return dict(group_sizes=torch.empty(E, **i32), group_offsets=torch.empty(E, **i32),
+                group_padded_offsets=torch.empty(E, **i32),
+                group_idx_for_bx=torch.empty(max(mb, 0), **i32),
+                sorted_token_idx=torch.empty(T * k, **i32),
+                sorted_row_weight=torch.empty(T * k, dtype=torch.float32, device=dev),
+                token_topk_to_pos=torch.empty((T, k), **i32))
+
+
+def moe_build_dispatch_noalloc(topk_idx, topk_w, E: int, block_m: int = BLOCK_M, out=None):
+    """moe_build_dispatch with the library's fixed scratch array instead of a
+    workspace (for callers that may not allocate device memory).  The output
+    tables are still the caller's: pass preallocated ones in ``out`` to make
+    the call itself allocation-free."""
+    _cuda(topk_idx, "topk_idx", dtype=torch.int32, ndim=2)
+    T, k = topk_idx.shape
+    if topk_w is not None:
+        _cuda(topk_w, "topk_w", dtype=torch.float32)
+        if topk_w.shape != topk_idx.shape:
+            raise ValueError("topk_w must match topk_idx")
+    dev = topk_idx.device
+    if out is None:
+        out = _dispatch_outputs(T, k, E, block_m, dev)
+    with torch.cuda.device(dev):
+        _check(lib().moe_build_dispatch_noalloc(
+            _ptr(topk_idx), _ptr(topk_w), T, k, E, block_m, _ptr(out["group_sizes"]),
+            _ptr(out["group_offsets"]), _ptr(out["group_padded_offsets"]),
+            _ptr(out["group_idx_for_bx"]), _ptr(out["sorted_token_idx"]),
+            _ptr(out["sorted_row_weight"]), _ptr(out["token_topk_to_pos"]), _stream(dev)),
+            "moe_build_dispatch_noalloc")
     return out
 
 

@@ -14,6 +14,9 @@
 //      expert; the warp then walks its pairs 32 at a time in ascending f and
 //      ranks equal experts with __match_any_sync, so the order inside an
 //      expert is ascending f (a stable sort) with no atomics-order effects.
+#include <mutex>
+
+#include "../../include/moe_routed_gate.h"
 #include "common.cuh"
 #include "internal.h"
 
@@ -202,3 +205,61 @@ cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Dispatch with no caller-provided scratch (moe_build_dispatch_noalloc).
+//
+// For callers that may not allocate device memory at all: code running while
+// a CUDA graph is being captured (cudaMalloc is not a capturable operation),
+// and engines whose device memory is planned once up front by another runtime
+// so that no call may allocate, or fail for lack of memory, in the middle of
+// a step.  Their per-chunk expert histograms live in this fixed array instead
+// of a workspace.  Every GPU that loads the library keeps the array until the
+// process exits.
+// ---------------------------------------------------------------------------
+static constexpr int64_t kStaticScratchInts = 262144;  // 1 MiB of int32 counters
+static __device__ __align__(256) int32_t g_dispatch_static_scratch[kStaticScratchInts];
+
+static std::mutex g_static_scratch_mu;
+static void *g_static_scratch_addr[64];  // device address per device id, looked up once
+
+extern "C" MOE_API moe_status_t moe_build_dispatch_noalloc(
+    const int32_t *topk_idx, const float *topk_w, int64_t T, int64_t k, int64_t E,
+    int64_t block_m, int32_t *group_sizes, int32_t *group_offsets,
+    int32_t *group_padded_offsets, int32_t *group_idx_for_bx, int32_t *sorted_token_idx,
+    float *sorted_row_weight, int32_t *token_topk_to_pos, moe_stream_t stream) {
+    if (T < 0 || k <= 0 || E <= 0 || E > 1024 || block_m != MOE_BLOCK_M) return MOE_ERR_INVALID_ARG;
+    if (T * k > (int64_t(1) << 30)) return MOE_ERR_UNSUPPORTED;
+    if (!group_sizes || !group_offsets || !group_padded_offsets || !group_idx_for_bx)
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !sorted_token_idx || !sorted_row_weight || !token_topk_to_pos))
+        return MOE_ERR_INVALID_ARG;
+    // the histograms need ceil(T*k / 2048) * E counters
+    if (moe::dispatch_scratch_bytes(T * k, E) > sizeof(g_dispatch_static_scratch))
+        return MOE_ERR_WORKSPACE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+        if (g_static_scratch_addr[dev] == nullptr) {
+            // host code only sees a stand-in symbol: ask the runtime for the
+            // array's address on the current device
+            void *addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_dispatch_static_scratch) != cudaSuccess || !addr)
+                return MOE_ERR_CUDA;
+            g_static_scratch_addr[dev] = addr;
+        }
+        scratch = g_static_scratch_addr[dev];
+    }
+    // The histogram kernel writes every counter the later kernels read, so the
+    // array needs no clearing between calls.
+    const int64_t m_blocks = (T * k + block_m - 1) / block_m + E;
+    cudaError_t e = moe::launch_dispatch(topk_idx, topk_w, T, k, E, block_m, group_sizes,
+                                         group_offsets, group_padded_offsets, group_idx_for_bx,
+                                         m_blocks, sorted_token_idx, sorted_row_weight,
+                                         token_topk_to_pos, scratch,
+                                         reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
