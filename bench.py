@@ -6,14 +6,16 @@
 One step = one pass of the whole routed forward (gate + top-k, dispatch
 tables, row gather, grouped gate/up GEMM with SiLU, grouped down GEMM,
 moe_reduce_fused) over one batch of synthetic tokens resident in HBM, through
-the library's C-ABI.  L2 is flushed (a 256 MB write) before every timed step,
-outside the timed events.  Each step's device time is taken with CUDA events
-on the launching stream; events between the entry points give each kernel's
-own duration inside the same timed region.
+the library's C-ABI; the six entry-point calls of a step are captured once
+into a CUDA graph (one per pooled token batch) and replayed.  Before every
+timed step L2 is evicted (a 256 MB write, then a 256 MB read of another
+buffer), outside the timed events.  Event record nodes between the entry
+points inside the graph give each step's and each kernel's device time.
 
 Prints ONE JSON line (rank 0).  ``value`` = tokens processed by all ranks /
-max-over-ranks time.  ``e2e`` = the same metric through ``moe_forward`` with
-host (pinned) input and output buffers, the copies inside the timed region.
+max-over-ranks time.  ``e2e`` = the same metric through the public
+``binding.ForwardGraph`` with pinned host input and output buffers, the
+host-to-device and device-to-host copies inside the timed region.
 ``--impl reference`` times the CPU oracle on the host cores instead.
 """
 from __future__ import annotations
@@ -39,7 +41,15 @@ from mixture_experts_routed_gate_gb300 import _build, roofline, workloads  # noq
 METRIC = "routed-MoE tokens/s and TFLOP/s (% roofline); reduce_fused GB/s vs HBM peak"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNELS_PER_STEP = 9  # gate logits, top-k, hist, scan, scatter, gather, gate/up, down, reduce
+
+
+def kernels_per_step(cfg) -> int:
+    """Kernels of one forward: gate (+ a top-k kernel when E > 64), dispatch
+    (one kernel up to 16384 pairs and 256 experts, else three), gather, the two
+    GEMM stages and the combine."""
+    gate = 1 if cfg.n_experts <= 64 else 2
+    dispatch = 1 if cfg.T * cfg.top_k <= 16384 and cfg.n_experts <= 256 else 3
+    return gate + dispatch + 4
 STAGES = ["gate_topk", "dispatch", "gather", "gate_up_silu", "down", "reduce"]
 
 
@@ -113,9 +123,8 @@ class ClockSampler:
 class NativeStep:
     """Pre-marshalled C-ABI calls of one forward step (no per-call Python checks)."""
 
-    def __init__(self, cfg, d, dev, x_pool):
+    def __init__(self, cfg, d, dev):
         from mixture_experts_routed_gate_gb300 import binding
-        self.b = binding
         L = binding.lib()
         self.L = L
         self.cfg = cfg
@@ -129,44 +138,67 @@ class NativeStep:
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.out = torch.empty((T, d_h), dtype=dt, device=dev)
         self.d = d
-        self.x_pool = x_pool
         self.mb = binding.num_m_blocks(T, k, E)
         off = lambda i: int(L.moe_forward_workspace_offset(T, d_h, d_e, E, k, self.code, i))
         self.scratch_ptr = self.ws.data_ptr() + off(10)
         self.scratch_bytes = int(L.moe_build_dispatch_workspace_bytes(T, k, E))
-        self.stream = torch.cuda.current_stream(dev)
-        self.sp = ctypes.c_void_p(self.stream.cuda_stream)
-        self.dev = dev
 
-    def p(self, t):
-        return ctypes.c_void_p(t.data_ptr()) if t is not None else None
-
-    def calls(self, x):
-        """The six entry points of one forward, in order."""
-        cfg, v, d, L, p = self.cfg, self.v, self.d, self.L, self.p
+    def calls(self, x, stream_ptr):
+        """(function, argument tuple) of the six entry points of one forward."""
+        cfg, v, d, L = self.cfg, self.v, self.d, self.L
+        p = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
         T, k, E, d_h, d_e = self.T, self.k, self.E, cfg.d_hidden, cfg.d_expert
         Tk = T * k
-        sp = self.sp
+        sp = ctypes.c_void_p(stream_ptr)
         tables = (p(v["group_sizes"]), p(v["group_offsets"]), p(v["group_padded_offsets"]),
                   p(v["group_idx_for_bx"]))
         return [
-            lambda: L.moe_gate_topk(p(x), p(d["wg"]), p(d["bias"]), T, d_h, E, k, self.code,
-                                    p(v["topk_idx"]), p(v["topk_w"]), p(v["logits"]),
-                                    T * E * 4, sp),
-            lambda: L.moe_build_dispatch(p(v["topk_idx"]), p(v["topk_w"]), T, k, E, 128, *tables,
-                                         p(v["sorted_token_idx"]), p(v["sorted_row_weight"]),
-                                         p(v["token_topk_to_pos"]),
-                                         ctypes.c_void_p(self.scratch_ptr), self.scratch_bytes, sp),
-            lambda: L.moe_gather_rows(p(x), p(v["sorted_token_idx"]), Tk, T, d_h, self.code,
-                                      p(v["a"]), sp),
-            lambda: L.moe_grouped_gate_up_silu(p(v["a"]), p(d["w_gate"]), p(d["w_up"]), *tables,
-                                               self.mb, Tk, d_h, d_e, E, self.code, p(v["h"]),
-                                               p(self.err), sp),
-            lambda: L.moe_grouped_down(p(v["h"]), p(d["w_down"]), *tables, self.mb, None, Tk, d_h,
-                                       d_e, E, self.code, p(v["y"]), p(self.err), sp),
-            lambda: L.moe_reduce_fused(p(v["y"]), Tk, p(v["token_topk_to_pos"]), p(v["topk_w"]), T,
-                                       k, d_h, self.code, self.code, p(self.out), p(self.err), sp),
+            (L.moe_gate_topk, (p(x), p(d["wg"]), p(d["bias"]), T, d_h, E, k, self.code,
+                               p(v["topk_idx"]), p(v["topk_w"]), p(v["logits"]), T * E * 4, sp)),
+            (L.moe_build_dispatch, (p(v["topk_idx"]), p(v["topk_w"]), T, k, E, 128, *tables,
+                                    p(v["sorted_token_idx"]), p(v["sorted_row_weight"]),
+                                    p(v["token_topk_to_pos"]), ctypes.c_void_p(self.scratch_ptr),
+                                    self.scratch_bytes, sp)),
+            (L.moe_gather_rows, (p(x), p(v["sorted_token_idx"]), Tk, T, d_h, self.code, p(v["a"]), sp)),
+            (L.moe_grouped_gate_up_silu, (p(v["a"]), p(d["w_gate"]), p(d["w_up"]), *tables, self.mb,
+                                          Tk, d_h, d_e, E, self.code, p(v["h"]), p(self.err), sp)),
+            (L.moe_grouped_down, (p(v["h"]), p(d["w_down"]), *tables, self.mb, None, Tk, d_h, d_e, E,
+                                  self.code, p(v["y"]), p(self.err), sp)),
+            (L.moe_reduce_fused, (p(v["y"]), Tk, p(v["token_topk_to_pos"]), p(v["topk_w"]), T, k, d_h,
+                                  self.code, self.code, p(self.out), p(self.err), sp)),
         ]
+
+
+def run_calls(calls, evs=None, stream=None):
+    from mixture_experts_routed_gate_gb300 import binding
+    if evs is not None:
+        evs[0].record(stream)
+    for j, (fn, args) in enumerate(calls):
+        st = fn(*args)
+        if st != 0:
+            raise RuntimeError(f"{STAGES[j]}: {binding.lib().moe_status_string(st).decode()}")
+        if evs is not None:
+            evs[j + 1].record(stream)
+
+
+class L2Flush:
+    """Evict L2 between timed steps: write a 256 MB buffer (evicts everything),
+    then read a second 256 MB buffer so that L2 ends up holding clean lines of
+    unrelated data (no write-backs leak into the next timed step)."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.sink = torch.empty((), dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.w.fill_(7)
+        torch.amax(self.r, dim=0, out=self.sink)
+
+
+def timing_events(n):
+    """Events that record inside a captured graph (external record nodes)."""
+    return [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)]
 
 
 def run_native(args, cfg, rank, world, dev):
@@ -177,56 +209,98 @@ def run_native(args, cfg, rank, world, dev):
     d = workloads.make_moe_inputs(cfg, device=dev, seed=cfg.seed)
     n_pool = 4
     x_pool = [d["x"]] + [workloads.make_tokens(cfg, cfg.T, device=dev, seed=i) for i in range(1, n_pool)]
-    step = NativeStep(cfg, d, dev, x_pool)
-    call_lists = [step.calls(x) for x in x_pool]
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = step.stream
+    step = NativeStep(cfg, d, dev)
+    stream = torch.cuda.Stream(dev)
+    flush = L2Flush(dev)
+    calls = [step.calls(x, stream.cuda_stream) for x in x_pool]
 
-    def one_step(i, evs=None):
-        calls = call_lists[i % n_pool]
-        if evs is not None:
-            evs[0].record(stream)
-        for j, c in enumerate(calls):
-            st = c()
-            if st != 0:
-                raise RuntimeError(f"{STAGES[j]}: {binding.lib().moe_status_string(st).decode()}")
-            if evs is not None:
-                evs[j + 1].record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            flush()
+            run_calls(calls[i % n_pool])
+        stream.synchronize()
+        if int(step.err.item()) != 0:
+            raise RuntimeError(f"device error flag {int(step.err.item())} after warm-up")
+        # routing statistics of each pooled batch (for the algorithmic byte counts)
+        act_experts, sizes_pool = [], []
+        for i in range(n_pool):
+            run_calls(calls[i])
+            stream.synchronize()
+            sz = step.v["group_sizes"].cpu().numpy().copy()
+            sizes_pool.append(sz)
+            act_experts.append(int((sz > 0).sum()))
 
-    for i in range(args.warmup):
-        flush.zero_()
-        one_step(i)
-    torch.cuda.synchronize()
-    if int(step.err.item()) != 0:
-        raise RuntimeError(f"device error flag {int(step.err.item())} after warm-up")
+        # Two CUDA graphs per pooled batch: the plain forward (timed for the
+        # step value) and the same forward with event record nodes between
+        # the entry points (timed for the per-kernel breakdown).
+        graphs, igraphs, gevents = [], [], []
+        mode = "cuda_graph"
+        try:
+            for i in range(n_pool):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    run_calls(calls[i])
+                graphs.append(g)
+                evs = timing_events(len(STAGES) + 1)
+                gi = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gi, stream=stream):
+                    run_calls(calls[i], evs, stream)
+                igraphs.append(gi)
+                gevents.append(evs)
+            for i in range(n_pool):
+                graphs[i].replay()
+                igraphs[i].replay()
+            stream.synchronize()
+        except Exception as exc:  # capture not available: time eager launches instead
+            mode = f"eager ({type(exc).__name__})"
+            graphs, igraphs = [], []
 
-    # routing statistics of each pooled batch (for the algorithmic byte counts)
-    act_experts, sizes_pool = [], []
-    for i in range(n_pool):
-        one_step(i)
-        torch.cuda.synchronize()
-        sz = step.v["group_sizes"].cpu().numpy().copy()
-        sizes_pool.append(sz)
-        act_experts.append(int((sz > 0).sum()))
+        # eager timing (the host launches every kernel), for the record
+        eager_ms = []
+        evs_e = [torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+        for i in range(min(args.steps, 50)):
+            flush()
+            run_calls(calls[i % n_pool], evs_e, stream)
+            evs_e[-1].synchronize()
+            eager_ms.append(evs_e[0].elapsed_time(evs_e[-1]))
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
-              for _ in range(args.steps)]
-    sampler = ClockSampler(dev.index if dev.index is not None else 0)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.15)
-    for i in range(args.steps):
-        flush.zero_()
-        one_step(i, events[i])
-    torch.cuda.synchronize()
-    clocks = sampler.stop()
-    if world > 1:
-        torch.distributed.barrier()
-    per_stage = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(len(STAGES))]
-                          for i in range(args.steps)])  # ms
-    step_ms = per_stage.sum(axis=1)
+        sampler = ClockSampler(dev.index if dev.index is not None else 0)
+        if world > 1:
+            torch.distributed.barrier()
+        stream.synchronize()
+        sampler.start()
+        time.sleep(0.15)
+        # timed region: K steps, events around each step (the step value)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush()
+            starts[i].record(stream)
+            if graphs:
+                graphs[i % n_pool].replay()
+            else:
+                run_calls(calls[i % n_pool])
+            ends[i].record(stream)
+        stream.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        step_ms = np.array([s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)])
+        # the same K steps with events between the kernels (per-kernel times)
+        per_stage = np.zeros((args.steps, len(STAGES)))
+        for i in range(args.steps):
+            flush()
+            if igraphs:
+                igraphs[i % n_pool].replay()
+                evs = gevents[i % n_pool]
+            else:
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+                run_calls(calls[i % n_pool], evs, stream)
+            evs[-1].synchronize()
+            per_stage[i] = [evs[j].elapsed_time(evs[j + 1]) for j in range(len(STAGES))]
+        stream.synchronize()
+        clocks = sampler.stop()
+        if world > 1:
+            torch.distributed.barrier()
     total_ms = float(step_ms.sum())
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
@@ -238,54 +312,47 @@ def run_native(args, cfg, rank, world, dev):
     e2e = measure_e2e(args, cfg, d, dev, flush, world)
     aux = measure_reduce_aux(dev, flush) if rank == 0 else None
     return dict(per_stage=per_stage, total_ms=total_ms, act_experts=act_experts,
-                sizes_pool=sizes_pool, clocks=clocks, e2e=e2e, aux=aux)
+                sizes_pool=sizes_pool, clocks=clocks, e2e=e2e, aux=aux, mode=mode,
+                eager_ms=float(np.median(eager_ms)), wall_s=t_wall)
 
 
 def measure_e2e(args, cfg, d, dev, flush, world):
-    """moe_forward through the public binding with pinned host buffers: H2D of
-    the step's tokens, the forward, D2H of the output, all inside the events."""
+    """The public API end to end: binding.ForwardGraph with pinned host input
+    and output buffers; each step copies the tokens host -> device, runs the
+    forward and copies the output device -> host, all inside the events."""
     from mixture_experts_routed_gate_gb300 import binding
     T, d_h = cfg.T, cfg.d_hidden
-    dt = d["x"].dtype
     n_pool = 4
-    host_x = [workloads.make_tokens(cfg, T, device="cpu", seed=100 + i).pin_memory() for i in range(n_pool)]
-    host_out = torch.empty((T, d_h), dtype=dt).pin_memory()
-    x_dev = torch.empty((T, d_h), dtype=dt, device=dev)
-    ws = torch.empty(binding.forward_workspace_bytes(T, d_h, cfg.d_expert, cfg.n_experts, cfg.top_k, dt),
-                     dtype=torch.uint8, device=dev)
-    out = torch.empty((T, d_h), dtype=dt, device=dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def step(i):
-        x_dev.copy_(host_x[i % n_pool], non_blocking=True)
-        binding.moe_forward(x_dev, d["wg"], d["bias"], d["w_gate"], d["w_up"], d["w_down"], cfg.top_k,
-                            ws=ws, out=out, err=err)
-        host_out.copy_(out, non_blocking=True)
-
-    for i in range(max(args.warmup, 3)):
-        flush.zero_()
-        step(i)
-    torch.cuda.synchronize()
+    host_x = [workloads.make_tokens(cfg, T, device="cpu", seed=100 + i) for i in range(n_pool)]
+    fg = binding.ForwardGraph(d["wg"], d["bias"], d["w_gate"], d["w_up"], d["w_down"], cfg.top_k, T,
+                              host_io=True)
+    stream = fg.stream
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.zero_()
-        starts[i].record(stream)
-        step(i)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            flush()
+            fg.x_host.copy_(host_x[i % n_pool])
+            fg.replay()
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        total_ms = 0.0
+        for i in range(args.steps):
+            fg.x_host.copy_(host_x[i % n_pool])  # host side: the caller's tokens into pinned memory
+            flush()
+            starts[i].record(stream)
+            fg.replay()
+            ends[i].record(stream)
+            ends[i].synchronize()
+            total_ms += starts[i].elapsed_time(ends[i])
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error flag {int(err.item())} in the e2e region")
-    es = x_dev.element_size()
+    if int(fg.err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(fg.err.item())} in the e2e region")
+    es = fg.x.element_size()
     return dict(total_ms=total_ms, h2d=T * d_h * es, d2h=T * d_h * es)
 
 
@@ -301,7 +368,7 @@ def measure_reduce_aux(dev, flush, reps: int = 20):
             binding.moe_reduce_fused(r["x"], r["pos"], r["w"], out=out)
         ts = []
         for _ in range(reps):
-            flush.zero_()
+            flush()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record()
             binding.moe_reduce_fused(r["x"], r["pos"], r["w"], out=out)
@@ -314,6 +381,80 @@ def measure_reduce_aux(dev, flush, reps: int = 20):
         res[name] = {"us": round(ms * 1e3, 2), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
                      "bytes": nbytes, "bytes_pages_formula": roofline.reduce_bytes_pages(c.T, c.K, c.H, 2)}
     return res
+
+
+# ----------------------------------------------------------------------------- one stage alone
+
+def run_only(args):
+    """Time one stage of the forward alone on a (possibly reduced) workload;
+    used to profile a single kernel with ncu on a small case.  Prints one JSON
+    line with the stage's median event time; not the benchmark line."""
+    import dataclasses
+    from mixture_experts_routed_gate_gb300 import binding
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = L2Flush(dev)
+    stream = torch.cuda.Stream(dev)
+    info = {}
+    if args.only.startswith("reduce"):
+        c = workloads.REDUCE_CONFIGS[args.only]
+        r = workloads.make_reduce_inputs(c.T, c.K, c.H, c.dtype, c.seed, device=dev)
+        out = torch.empty((c.T, c.H), dtype=torch.bfloat16, device=dev)
+        def fn():
+            binding.moe_reduce_fused(r["x"], r["pos"], r["w"], out=out)
+        n_valid = int((r["pos"] >= 0).sum().item())
+        info = {"workload": f"{c.name}: T={c.T} K={c.K} H={c.H} bf16",
+                "bytes": roofline.reduce_bytes(n_valid, c.T, c.K, c.H, 2, 2)}
+    elif args.only == "gate_topk":
+        base = workloads.MOE_CONFIGS[args.workload]
+        T = args.tokens or base.T
+        cfg = dataclasses.replace(base, batch=1, seq=T, n_experts=args.experts or base.n_experts)
+        d = workloads.make_moe_inputs(cfg, device=dev, with_experts=False)
+        E, k = cfg.n_experts, cfg.top_k
+        idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+        w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        ws = torch.empty(T * E * 4, dtype=torch.uint8, device=dev)
+        def fn():
+            binding.moe_gate_topk(d["x"], d["wg"], d["bias"], k, topk_idx=idx, topk_w=w, ws=ws)
+        info = {"workload": describe(cfg), "flops": roofline.gate_flops(T, cfg.d_hidden, E)}
+    else:
+        base = workloads.MOE_CONFIGS[args.workload]
+        T = args.tokens or base.T
+        cfg = dataclasses.replace(base, batch=1, seq=T, n_experts=args.experts or base.n_experts)
+        d = workloads.make_moe_inputs(cfg, device=dev)
+        step = NativeStep(cfg, d, dev)
+        calls = step.calls(d["x"], stream.cuda_stream)
+        with torch.cuda.stream(stream):
+            run_calls(calls)  # produce every intermediate once
+        stream.synchronize()
+        j = STAGES.index(args.only)
+        fnc, fargs = calls[j]
+        def fn():
+            st = fnc(*fargs)
+            if st != 0:
+                raise RuntimeError(binding.lib().moe_status_string(st).decode())
+        sizes = step.v["group_sizes"].cpu().numpy()
+        info = {"workload": describe(cfg), "active_experts": int((sizes > 0).sum()),
+                "max_rows": int(sizes.max())}
+    ts = []
+    with torch.cuda.stream(stream):
+        for i in range(3 + args.steps):
+            flush()
+            s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_.record(stream)
+            fn()
+            e_.record(stream)
+            e_.synchronize()
+            if i >= 3:
+                ts.append(s_.elapsed_time(e_))
+    line = {"mode": "only", "stage": args.only, "steps": args.steps,
+            "us_median": round(statistics.median(ts) * 1e3, 2), **info}
+    if "bytes" in info:
+        line["gbs"] = round(info["bytes"] / (statistics.median(ts) * 1e-3) / 1e9, 1)
+    if "flops" in info:
+        line["tflops"] = round(info["flops"] / (statistics.median(ts) * 1e-3) / 1e12, 2)
+    print(json.dumps(line))
 
 
 # ----------------------------------------------------------------------------- oracle arm
@@ -374,7 +515,16 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=list(workloads.MOE_CONFIGS), default="decode")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time")
+    ap.add_argument("--only", default=None,
+                    choices=STAGES + ["reduce-512", "reduce-4096"],
+                    help="time one stage alone (profiling aid; not the benchmark line)")
+    ap.add_argument("--experts", type=int, default=None, help="with --only: expert count override")
+    ap.add_argument("--tokens", type=int, default=None, help="with --only: token count override")
     args = ap.parse_args()
+    if args.only:
+        args.steps = args.steps or 5
+        run_only(args)
+        return
     cfg = workloads.MOE_CONFIGS[args.workload]
     if args.steps is None:
         args.steps = {"decode": 2000, "tiny": 2000, "prefill": 60}[cfg.name] if args.impl == "native" else 3
@@ -390,7 +540,7 @@ def main():
             "data": "synthetic: seeded N(0,1) tokens, N(0,1/fan_in) random-init expert and gate weights",
             "config": {"workload": describe(cfg), "T": cfg.T, "d_hidden": cfg.d_hidden,
                        "d_expert": cfg.d_expert, "n_experts": cfg.n_experts, "top_k": cfg.top_k,
-                       "l2": "flushed before every timed step (256 MB write)",
+                       "l2": "evicted before every timed step: 256 MB write, then a 256 MB read of another buffer",
                        "parallelism": f"replicas x{args.gpus}"}}
 
     if args.impl == "reference":
@@ -461,6 +611,7 @@ def main():
         "tflops": round(flops_step * args.steps / (res["total_ms"] / 1e3) / 1e12, 3),
         "step_roofline_frac": round(step_roof_ms / ms_step, 4),
         "kernels_us": {s: round(float(per_stage[:, i].mean()) * 1e3, 2) for i, s in enumerate(STAGES)},
+        "kernels_note": "per-kernel times from replays of the same graphs with event nodes between the kernels",
         "active_experts": e_act,
         "roofline": rl,
         "reduce_fused_bf16_x8_7168": res["aux"],
@@ -468,7 +619,9 @@ def main():
                          "kind": "oracle", "sample": cpu["sample"]},
         "e2e": {"value": round(T * args.steps * world / (e2e["total_ms"] / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": kernels_per_step(cfg) * args.steps,
+        "launch_mode": res["mode"],
+        "eager_ms_per_step": round(res["eager_ms"], 5),
         "clocks": res["clocks"],
     })
     print(json.dumps(line))

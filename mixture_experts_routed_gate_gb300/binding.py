@@ -367,3 +367,43 @@ def moe_forward(x, w_g, bias, w_gate, w_up, w_down, k: int, ws=None, out=None, e
                                  ws.numel(), _ptr(out), _ptr(err), _stream(x.device)),
                "moe_forward")
     return out
+
+
+class ForwardGraph:
+    """``moe_forward`` captured once into a CUDA graph for a fixed token count,
+    with static device buffers (and, with ``host_io``, pinned host buffers whose
+    host-to-device and device-to-host copies are part of the graph).
+
+    Fill ``x`` (or ``x_host``), call :meth:`replay`, and read ``out`` (or
+    ``out_host`` after synchronising).  One replay is one launch from the host,
+    which removes the per-kernel launch cost of a small decode step."""
+
+    def __init__(self, w_g, bias, w_gate, w_up, w_down, k: int, T: int, host_io: bool = False):
+        dev = w_gate.device
+        dt = w_gate.dtype
+        E, d_e, d_h = w_gate.shape
+        self.params = (w_g, bias, w_gate, w_up, w_down, k)
+        self.x = torch.zeros((T, d_h), dtype=dt, device=dev)
+        self.out = torch.empty((T, d_h), dtype=dt, device=dev)
+        self.ws = torch.empty(forward_workspace_bytes(T, d_h, d_e, E, k, dt), dtype=torch.uint8, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.x_host = torch.zeros((T, d_h), dtype=dt).pin_memory() if host_io else None
+        self.out_host = torch.empty((T, d_h), dtype=dt).pin_memory() if host_io else None
+        self.stream = torch.cuda.Stream(dev)
+        with torch.cuda.stream(self.stream):
+            self._body()  # first call on the device outside capture (one-time set-up)
+        self.stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self._body()
+
+    def _body(self):
+        w_g, bias, w_gate, w_up, w_down, k = self.params
+        if self.x_host is not None:
+            self.x.copy_(self.x_host, non_blocking=True)
+        moe_forward(self.x, w_g, bias, w_gate, w_up, w_down, k, ws=self.ws, out=self.out, err=self.err)
+        if self.out_host is not None:
+            self.out_host.copy_(self.out, non_blocking=True)
+
+    def replay(self):
+        self.graph.replay()

@@ -132,9 +132,8 @@ moe_status_t moe_gate_topk(const void *x, const void *w_g, const float *bias, in
     if (ws_bytes < moe_gate_topk_workspace_bytes(T, E)) return MOE_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     float *logits = static_cast<float *>(ws);
-    cudaError_t e = moe::launch_gate_logits(x, w_g, bias, T, d_h, E, dtype, logits, s);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    return cuda_status(moe::launch_topk_softmax(logits, T, E, k, topk_idx, topk_w, s));
+    return cuda_status(moe::launch_gate_topk(x, w_g, bias, T, d_h, E, k, dtype, logits, topk_idx,
+                                             topk_w, s));
 }
 
 moe_status_t moe_build_dispatch(const int32_t *topk_idx, const float *topk_w, int64_t T,

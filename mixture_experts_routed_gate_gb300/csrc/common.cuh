@@ -148,6 +148,27 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *desc, uint
         : "memory");
 }
 
+// L2 eviction-priority policies for TMA loads (createpolicy, whole footprint).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *desc, uint32_t bar, int c0,
+                                                 int c1, int c2, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
 // ----------------------------------------------------------------------------
 // tcgen05: tensor memory, MMA, commit, loads
 // ----------------------------------------------------------------------------

@@ -14,6 +14,8 @@
 //      expert; the warp then walks its pairs 32 at a time in ascending f and
 //      ranks equal experts with __match_any_sync, so the order inside an
 //      expert is ascending f (a stable sort) with no atomics-order effects.
+// Problems of at most 16384 pairs and 256 experts run all of it in a single
+// CTA (dispatch_small_kernel): one launch instead of three.
 #include <mutex>
 
 #include "../../include/moe_routed_gate.h"
@@ -166,6 +168,100 @@ __global__ void __launch_bounds__(DS_THREADS)
     }
 }
 
+// Whole dispatch in one CTA for small problems (at most SMALL_MAX_PAIRS pairs
+// and SMALL_MAX_E experts): the pairs stay in registers (warp w owns a
+// contiguous run of 32*R pairs), per-warp counts in shared memory, one block
+// scan, the block lookup, then the stable scatter from the same registers.
+constexpr int SMALL_THREADS = 1024;
+constexpr int SMALL_WARPS = SMALL_THREADS / 32;
+constexpr int SMALL_MAX_ROUNDS = 16;
+constexpr int SMALL_MAX_PAIRS = SMALL_WARPS * 32 * SMALL_MAX_ROUNDS;  // 16384
+constexpr int SMALL_MAX_E = 256;
+
+__global__ void __launch_bounds__(SMALL_THREADS)
+    dispatch_small_kernel(const int32_t *__restrict__ idx, const float *__restrict__ w,
+                          int n_pairs, int k, int E, int block_m, int32_t *__restrict__ sizes,
+                          int32_t *__restrict__ offsets, int32_t *__restrict__ padded,
+                          int32_t *__restrict__ gidx, int m_blocks,
+                          int32_t *__restrict__ sorted_tok, float *__restrict__ sorted_w,
+                          int32_t *__restrict__ pos) {
+    __shared__ int32_t wcount[SMALL_WARPS * SMALL_MAX_E];
+    __shared__ int po_s[SMALL_MAX_E];
+    __shared__ int warp_sums[32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rounds = (n_pairs + SMALL_THREADS - 1) / SMALL_THREADS;  // <= SMALL_MAX_ROUNDS
+    const int wf0 = warp * rounds * 32;
+    for (int i = threadIdx.x; i < SMALL_WARPS * E; i += SMALL_THREADS) wcount[i] = 0;
+    int ev[SMALL_MAX_ROUNDS];
+#pragma unroll
+    for (int r = 0; r < SMALL_MAX_ROUNDS; ++r) {
+        const int f = wf0 + r * 32 + lane;
+        int e = -1;
+        if (r < rounds && f < n_pairs) e = __ldg(idx + f);
+        ev[r] = (e >= 0 && e < E) ? e : -1;
+    }
+    __syncthreads();
+    const unsigned lt_mask = (1u << lane) - 1u;
+    int32_t *mine = wcount + warp * E;
+#pragma unroll
+    for (int r = 0; r < SMALL_MAX_ROUNDS; ++r) {
+        if (r < rounds) {
+            const unsigned peers = __match_any_sync(0xffffffffu, ev[r]);
+            if (ev[r] >= 0 && (peers & lt_mask) == 0) mine[ev[r]] += __popc(peers);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    const int e = threadIdx.x;
+    int count = 0;
+    if (e < E) {
+        for (int wv = 0; wv < SMALL_WARPS; ++wv) {
+            const int c = wcount[wv * E + e];
+            wcount[wv * E + e] = count;
+            count += c;
+        }
+    }
+    const int off = block_exclusive_scan(e < E ? count : 0, warp_sums);
+    const int psize = e < E ? ((count + block_m) / block_m) * block_m : 0;
+    const int poff = block_exclusive_scan(psize, warp_sums);
+    if (e < E) {
+        sizes[e] = count;
+        offsets[e] = off;
+        padded[e] = poff;
+        po_s[e] = poff;
+        for (int wv = 0; wv < SMALL_WARPS; ++wv) wcount[wv * E + e] += off;
+    }
+    __syncthreads();
+    for (int bx = threadIdx.x; bx < m_blocks; bx += SMALL_THREADS) {
+        const long long start = static_cast<long long>(bx) * block_m;
+        int lo = 0, hi = E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (static_cast<long long>(po_s[mid]) <= start) lo = mid;
+            else hi = mid - 1;
+        }
+        gidx[bx] = lo;
+    }
+#pragma unroll
+    for (int r = 0; r < SMALL_MAX_ROUNDS; ++r) {
+        if (r < rounds) {
+            const int f = wf0 + r * 32 + lane;
+            const int ee = ev[r];
+            const unsigned peers = __match_any_sync(0xffffffffu, ee);
+            int row = 0;
+            if (ee >= 0) row = mine[ee] + __popc(peers & lt_mask);
+            __syncwarp();
+            if (ee >= 0 && (peers & lt_mask) == 0) mine[ee] += __popc(peers);
+            __syncwarp();
+            if (ee >= 0) {
+                sorted_tok[row] = f / k;
+                sorted_w[row] = w ? __ldg(w + f) : 1.0f;
+                pos[f] = row;
+            }
+        }
+    }
+}
+
 }  // namespace
 
 size_t dispatch_scratch_bytes(int64_t n_pairs, int64_t E) {
@@ -179,6 +275,13 @@ cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_
                             float *sorted_row_weight, int32_t *pos, void *scratch,
                             cudaStream_t stream) {
     const int64_t n_pairs = T * k;
+    if (n_pairs <= SMALL_MAX_PAIRS && E <= SMALL_MAX_E) {
+        dispatch_small_kernel<<<1, SMALL_THREADS, 0, stream>>>(
+            topk_idx, topk_w, static_cast<int>(n_pairs), static_cast<int>(k), static_cast<int>(E),
+            static_cast<int>(block_m), sizes, offsets, padded, gidx, static_cast<int>(m_blocks),
+            sorted_token_idx, sorted_row_weight, pos);
+        return cudaGetLastError();
+    }
     const int64_t n_chunks = n_pairs > 0 ? (n_pairs + CHUNK - 1) / CHUNK : 0;
     int32_t *hist = static_cast<int32_t *>(scratch);
     if (n_chunks > 0) {
@@ -193,10 +296,14 @@ cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || n_chunks == 0) return e;
     const size_t smem = static_cast<size_t>(DS_WARPS) * E * 4;
-    if (smem > 48 * 1024) {
+    static size_t attr_bytes[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (smem > 48 * 1024 && (dev < 0 || dev >= 64 || attr_bytes[dev] < smem)) {
         e = cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
         if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_bytes[dev] = smem;
     }
     dispatch_scatter_kernel<<<static_cast<unsigned>(n_chunks), DS_THREADS, smem, stream>>>(
         topk_idx, topk_w, n_pairs, static_cast<int>(k), static_cast<int>(E), hist,

@@ -9,23 +9,27 @@
 // the d_hidden axis is cut into 8-element chunks; chunk c is summed by warp
 // lane (c mod 32) in ascending index with fmaf, then the 32 lane partials are
 // combined by the xor butterfly s = 16, 8, 4, 2, 1.  The kernel is the
-// natural warp-split-K dot product: a warp owns an 8-token x 8-expert tile,
-// each lane keeps one partial per (token, expert) pair, and 256-element
-// slices of x and W_g are staged through shared memory with cp.async.
+// natural warp-split-K dot product: a warp owns a (4 or 8)-token x 8-expert tile,
+// each lane keeps one partial per (token, expert) pair and reads its 16-byte
+// chunk of every row from shared memory (conflict free); 256-element slices
+// of x and W_g stream through a 4-stage cp.async ring.
+//
+// Three shapes of the same kernel:
+//   * E <= 64: one CTA holds 4 tokens x all experts and also selects the
+//     top-k from its logits in shared memory (one launch for the gate);
+//   * many tokens: CTA = 16 tokens x 32 experts (16 warps of 4 x 8 pairs), then
+//     topk_softmax_kernel;
+//   * few tokens: CTA = one warp of 4 tokens x 8 experts (more CTAs in
+//     flight), then topk_softmax_kernel.
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
 namespace {
 
-constexpr int GT_TOK = 16;        // tokens per CTA
-constexpr int GT_EXP = 32;        // experts per CTA
-constexpr int WT_TOK = 8;         // tokens per warp
-constexpr int WT_EXP = 8;         // experts per warp
-constexpr int GT_WARPS = (GT_TOK / WT_TOK) * (GT_EXP / WT_EXP);  // 8
-constexpr int GT_THREADS = GT_WARPS * 32;
-constexpr int SLICE = 256;        // elements per lane round: 32 lanes x 8
-constexpr int ROW_BYTES = SLICE * 2;  // 512 B of one row per slice
+constexpr int SLICE = 256;                // elements per lane round: 32 lanes x 8
+constexpr int ROW_BYTES = SLICE * 2;      // 512 B of one row per slice
+constexpr int GATE_STAGES = 4;
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool pred) {
     const int n = pred ? 16 : 0;  // zero-fill rows past the end
@@ -38,121 +42,16 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int DT>
-__global__ void __launch_bounds__(GT_THREADS)
-    gate_logits_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ wg,
-                       const float *__restrict__ bias, int T, int d_h, int E,
-                       float *__restrict__ logits) {
-    // [2 buffers][GT_TOK + GT_EXP rows][512 B]
-    __shared__ __align__(16) uint8_t tiles[2][GT_TOK + GT_EXP][ROW_BYTES];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t0 = blockIdx.x * GT_TOK, e0 = blockIdx.y * GT_EXP;
-    const int wt = (warp / (GT_EXP / WT_EXP)) * WT_TOK;  // warp's token offset in the tile
-    const int we = (warp % (GT_EXP / WT_EXP)) * WT_EXP;  // warp's expert offset
-    const int n_slices = d_h / SLICE;
-
-    // one slice = (GT_TOK + GT_EXP) rows x 32 chunks of 16 B = 1536 chunks
-    auto load_slice = [&](int s, int buf) {
-        for (int c = threadIdx.x; c < (GT_TOK + GT_EXP) * 32; c += GT_THREADS) {
-            const int r = c >> 5, ch = c & 31;
-            const bool is_tok = r < GT_TOK;
-            const int gr = is_tok ? t0 + r : e0 + (r - GT_TOK);
-            const bool ok = is_tok ? gr < T : gr < E;
-            const uint16_t *base = is_tok ? x : wg;
-            const uint16_t *src = base + static_cast<int64_t>(ok ? gr : 0) * d_h + s * SLICE + ch * 8;
-            cp_async16(smem_u32(&tiles[buf][r][ch * 16]), src, ok);
-        }
-        cp_async_commit();
-    };
-
-    float acc[WT_TOK][WT_EXP];
-#pragma unroll
-    for (int i = 0; i < WT_TOK; ++i)
-#pragma unroll
-        for (int j = 0; j < WT_EXP; ++j) acc[i][j] = 0.0f;
-
-    load_slice(0, 0);
-    for (int s = 0; s < n_slices; ++s) {
-        const int buf = s & 1;
-        if (s + 1 < n_slices) {
-            load_slice(s + 1, buf ^ 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        // lane owns chunk `lane` of this slice: elements [8*lane, 8*lane + 8)
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {  // 4 words = 8 elements, ascending
-            float2 xv[WT_TOK], wv[WT_EXP];
-#pragma unroll
-            for (int i = 0; i < WT_TOK; ++i)
-                xv[i] = unpack2<DT>(*reinterpret_cast<const uint32_t *>(&tiles[buf][wt + i][lane * 16 + w * 4]));
-#pragma unroll
-            for (int j = 0; j < WT_EXP; ++j)
-                wv[j] = unpack2<DT>(*reinterpret_cast<const uint32_t *>(&tiles[buf][GT_TOK + we + j][lane * 16 + w * 4]));
-#pragma unroll
-            for (int i = 0; i < WT_TOK; ++i)
-#pragma unroll
-                for (int j = 0; j < WT_EXP; ++j) {
-                    acc[i][j] = fmaf(xv[i].x, wv[j].x, acc[i][j]);
-                    acc[i][j] = fmaf(xv[i].y, wv[j].y, acc[i][j]);
-                }
-        }
-        __syncthreads();
-    }
-
-    // xor butterfly s = 16, 8, 4, 2, 1; every lane ends with the full sum
-#pragma unroll
-    for (int i = 0; i < WT_TOK; ++i)
-#pragma unroll
-        for (int j = 0; j < WT_EXP; ++j) {
-            float v = acc[i][j];
-#pragma unroll
-            for (int sh = 16; sh >= 1; sh >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, sh);
-            acc[i][j] = v;
-        }
-    // lane L writes pairs L and L + 32 of the warp's 64
-#pragma unroll
-    for (int i = 0; i < WT_TOK; ++i)
-#pragma unroll
-        for (int j = 0; j < WT_EXP; ++j) {
-            const int pair = i * WT_EXP + j;
-            if ((pair & 31) == lane) {
-                const int t = t0 + wt + i, e = e0 + we + j;
-                if (t < T && e < E) {
-                    float l = acc[i][j];
-                    if (bias) l = l + bias[e];
-                    logits[static_cast<int64_t>(t) * E + e] = l;
-                }
-            }
-        }
-}
-
-// One warp per token.  Each lane holds E/32 logits (expert e at lane e % 32,
-// slot e / 32).  k rounds of a warp argmax by (logit desc, id asc); softmax
-// over all E in fp32 with the max subtracted.
-constexpr int TK_WARPS = 8;
-
+// Warp argmax by (logit desc, id asc) over k rounds, then the softmax weights.
+// Lane holds v[s] = logit of expert s*32 + lane (or -inf past E).
 template <int SLOTS>
-__global__ void __launch_bounds__(TK_WARPS * 32)
-    topk_softmax_kernel(const float *__restrict__ logits, int T, int E, int k,
-                        int32_t *__restrict__ topk_idx, float *__restrict__ topk_w) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * TK_WARPS + warp;
-    if (t >= T) return;
-    const float *row = logits + static_cast<int64_t>(t) * E;
-    float v[SLOTS];
+__device__ __forceinline__ void warp_topk_softmax(float (&v)[SLOTS], int E, int k, int32_t *idx_out,
+                                                  float *w_out, int lane) {
     bool taken[SLOTS];
 #pragma unroll
-    for (int s = 0; s < SLOTS; ++s) {
-        const int e = s * 32 + lane;
-        v[s] = e < E ? row[e] : -INFINITY;
-        taken[s] = e >= E;
-    }
-    float top_logit = 0.0f;
-    float sel_logit[32];
-    int sel_id[32];
+    for (int s = 0; s < SLOTS; ++s) taken[s] = s * 32 + lane >= E;
+    float top_logit = 0.0f, my_logit = 0.0f;
+    int my_id = 0;
     for (int j = 0; j < k; ++j) {
         float best = -INFINITY;
         int best_id = 0x7fffffff;
@@ -176,9 +75,11 @@ __global__ void __launch_bounds__(TK_WARPS * 32)
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s)
             if (s * 32 + lane == best_id) taken[s] = true;
-        sel_logit[j] = best;
-        sel_id[j] = best_id;
         if (j == 0) top_logit = best;
+        if (j == lane) {
+            my_logit = best;
+            my_id = best_id;
+        }
     }
     float sum = 0.0f;
 #pragma unroll
@@ -187,38 +88,198 @@ __global__ void __launch_bounds__(TK_WARPS * 32)
 #pragma unroll
     for (int sh = 16; sh >= 1; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
     if (lane < k) {
-        float l = 0.0f;
-        int id = 0;
-        for (int j = 0; j < k; ++j)
-            if (j == lane) {
-                l = sel_logit[j];
-                id = sel_id[j];
-            }
-        topk_idx[static_cast<int64_t>(t) * k + lane] = id;
-        topk_w[static_cast<int64_t>(t) * k + lane] = expf(l - top_logit) / sum;
+        idx_out[lane] = my_id;
+        w_out[lane] = expf(my_logit - top_logit) / sum;
     }
 }
 
-}  // namespace
+template <int DT, int TPW, int WT, int WE, bool FUSE_TOPK>
+__global__ void __launch_bounds__(WT *WE * 32)
+    gate_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ wg,
+                const float *__restrict__ bias, int T, int d_h, int E, int k,
+                float *__restrict__ logits, int32_t *__restrict__ topk_idx,
+                float *__restrict__ topk_w) {
+    constexpr int TOK = WT * TPW, EXP = WE * 8, ROWS = TOK + EXP;
+    constexpr int THREADS = WT * WE * 32;
+    constexpr int STAGE_BYTES = ROWS * ROW_BYTES;
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * TOK, e0 = blockIdx.y * EXP;
+    const int wt = (warp / WE) * TPW;  // warp's first token in the tile
+    const int we = (warp % WE) * 8;  // warp's first expert in the tile
+    const int n_slices = d_h / SLICE;
 
-cudaError_t launch_gate_logits(const void *x, const void *wg, const float *bias, int64_t T,
-                               int64_t d_h, int64_t E, int dtype, float *logits,
-                               cudaStream_t stream) {
-    if (T <= 0) return cudaSuccess;
-    dim3 grid(static_cast<unsigned>((T + GT_TOK - 1) / GT_TOK),
-              static_cast<unsigned>((E + GT_EXP - 1) / GT_EXP));
-    const auto *xp = static_cast<const uint16_t *>(x);
-    const auto *wp = static_cast<const uint16_t *>(wg);
-    if (dtype == kBF16)
-        gate_logits_kernel<kBF16><<<grid, GT_THREADS, 0, stream>>>(xp, wp, bias, (int)T, (int)d_h, (int)E, logits);
-    else
-        gate_logits_kernel<kF16><<<grid, GT_THREADS, 0, stream>>>(xp, wp, bias, (int)T, (int)d_h, (int)E, logits);
+    auto load_slice = [&](int s) {
+        uint8_t *stage = smem + (s % GATE_STAGES) * STAGE_BYTES;
+        for (int c = threadIdx.x; c < ROWS * 32; c += THREADS) {
+            const int r = c >> 5, ch = c & 31;
+            const bool is_tok = r < TOK;
+            const int gr = is_tok ? t0 + r : e0 + (r - TOK);
+            const bool ok = is_tok ? gr < T : gr < E;
+            const uint16_t *src = (is_tok ? x : wg) + static_cast<int64_t>(ok ? gr : 0) * d_h +
+                                  s * SLICE + ch * 8;
+            cp_async16(smem_u32(stage + r * ROW_BYTES + ch * 16), src, ok);
+        }
+    };
+
+    float acc[TPW][8];
+#pragma unroll
+    for (int i = 0; i < TPW; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+#pragma unroll
+    for (int s = 0; s < GATE_STAGES - 1; ++s) {
+        if (s < n_slices) load_slice(s);
+        cp_async_commit();
+    }
+    for (int s = 0; s < n_slices; ++s) {
+        cp_async_wait<GATE_STAGES - 2>();
+        __syncthreads();
+        const uint8_t *stage = smem + (s % GATE_STAGES) * STAGE_BYTES;
+        // lane owns chunk `lane` of the slice: elements 8*lane .. 8*lane+7, ascending
+        uint4 xv[TPW], wv[8];
+#pragma unroll
+        for (int i = 0; i < TPW; ++i)
+            xv[i] = *reinterpret_cast<const uint4 *>(stage + (wt + i) * ROW_BYTES + lane * 16);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            wv[j] = *reinterpret_cast<const uint4 *>(stage + (TOK + we + j) * ROW_BYTES + lane * 16);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float2 xf[TPW], wf[8];
+#pragma unroll
+            for (int i = 0; i < TPW; ++i) {
+                const uint32_t word = q == 0 ? xv[i].x : q == 1 ? xv[i].y : q == 2 ? xv[i].z : xv[i].w;
+                xf[i] = unpack2<DT>(word);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t word = q == 0 ? wv[j].x : q == 1 ? wv[j].y : q == 2 ? wv[j].z : wv[j].w;
+                wf[j] = unpack2<DT>(word);
+            }
+            // element 2q of every pair, then element 2q+1: the two updates of
+            // one accumulator are TPW*8 independent FMAs apart
+#pragma unroll
+            for (int i = 0; i < TPW; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xf[i].x, wf[j].x, acc[i][j]);
+#pragma unroll
+            for (int i = 0; i < TPW; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xf[i].y, wf[j].y, acc[i][j]);
+        }
+        // refill the stage consumed one iteration ago (every thread is past it)
+        if (s + GATE_STAGES - 1 < n_slices) load_slice(s + GATE_STAGES - 1);
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
+
+    // xor butterfly s = 16, 8, 4, 2, 1; every lane ends with the full sum
+#pragma unroll
+    for (int i = 0; i < TPW; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float v = acc[i][j];
+#pragma unroll
+            for (int sh = 16; sh >= 1; sh >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, sh);
+            acc[i][j] = v;
+        }
+
+    if constexpr (!FUSE_TOPK) {
+        // lane L writes pairs L (and L + 32) of the warp's TPW*8
+#pragma unroll
+        for (int i = 0; i < TPW; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (((i * 8 + j) & 31) == lane) {
+                    const int t = t0 + wt + i, e = e0 + we + j;
+                    if (t < T && e < E) {
+                        float l = acc[i][j];
+                        if (bias) l = l + bias[e];
+                        logits[static_cast<int64_t>(t) * E + e] = l;
+                    }
+                }
+            }
+    } else {
+        // one CTA holds every expert of its TOK tokens: logits to shared
+        // memory, then warp w selects the top-k of token t0 + w
+        static_assert(!FUSE_TOPK || (WT == 1 && EXP == 64 && TPW <= WE), "fused shape");
+        __syncthreads();  // the ring is no longer read
+        float *lsm = reinterpret_cast<float *>(smem);  // [TOK][EXP]
+#pragma unroll
+        for (int i = 0; i < TPW; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (((i * 8 + j) & 31) == lane) {
+                    const int t = t0 + wt + i, e = e0 + we + j;
+                    float l = acc[i][j];
+                    if (e < E && bias) l = l + bias[e];
+                    lsm[(wt + i) * EXP + we + j] = l;
+                    if (t < T && e < E) logits[static_cast<int64_t>(t) * E + e] = l;
+                }
+            }
+        __syncthreads();
+        const int t = t0 + warp;
+        if (warp < TOK && t < T) {
+            float v[2];
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                const int e = s * 32 + lane;
+                v[s] = e < E ? lsm[warp * EXP + e] : -INFINITY;
+            }
+            warp_topk_softmax<2>(v, E, k, topk_idx + static_cast<int64_t>(t) * k,
+                                 topk_w + static_cast<int64_t>(t) * k, lane);
+        }
+    }
+}
+
+// One warp per token over logits in global memory.
+constexpr int TK_WARPS = 8;
+
+template <int SLOTS>
+__global__ void __launch_bounds__(TK_WARPS * 32)
+    topk_softmax_kernel(const float *__restrict__ logits, int T, int E, int k,
+                        int32_t *__restrict__ topk_idx, float *__restrict__ topk_w) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * TK_WARPS + warp;
+    if (t >= T) return;
+    const float *row = logits + static_cast<int64_t>(t) * E;
+    float v[SLOTS];
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+        const int e = s * 32 + lane;
+        v[s] = e < E ? row[e] : -INFINITY;
+    }
+    warp_topk_softmax<SLOTS>(v, E, k, topk_idx + static_cast<int64_t>(t) * k,
+                             topk_w + static_cast<int64_t>(t) * k, lane);
+}
+
+template <int DT, int TPW, int WT, int WE, bool FUSE>
+cudaError_t launch_gate_shape(const void *x, const void *wg, const float *bias, int64_t T,
+                              int64_t d_h, int64_t E, int64_t k, float *logits, int32_t *idx,
+                              float *w, cudaStream_t stream) {
+    constexpr int TOK = WT * TPW, EXP = WE * 8;
+    const size_t smem = static_cast<size_t>(GATE_STAGES) * (TOK + EXP) * ROW_BYTES;
+    auto kern = gate_kernel<DT, TPW, WT, WE, FUSE>;
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (smem > 48 * 1024 && (dev < 0 || dev >= 64 || !attr_done[dev])) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    dim3 grid(static_cast<unsigned>((T + TOK - 1) / TOK), static_cast<unsigned>((E + EXP - 1) / EXP));
+    kern<<<grid, WT * WE * 32, smem, stream>>>(static_cast<const uint16_t *>(x),
+                                               static_cast<const uint16_t *>(wg), bias, (int)T,
+                                               (int)d_h, (int)E, (int)k, logits, idx, w);
     return cudaGetLastError();
 }
 
-cudaError_t launch_topk_softmax(const float *logits, int64_t T, int64_t E, int64_t k,
-                                int32_t *topk_idx, float *topk_w, cudaStream_t stream) {
-    if (T <= 0) return cudaSuccess;
+cudaError_t launch_topk(const float *logits, int64_t T, int64_t E, int64_t k, int32_t *topk_idx,
+                        float *topk_w, cudaStream_t stream) {
     const unsigned grid = static_cast<unsigned>((T + TK_WARPS - 1) / TK_WARPS);
     const int slots = static_cast<int>((E + 31) / 32);
 #define MOE_TOPK_CASE(S)                                                                        \
@@ -227,7 +288,6 @@ cudaError_t launch_topk_softmax(const float *logits, int64_t T, int64_t E, int64
                                                                     topk_idx, topk_w);          \
         return cudaGetLastError();                                                              \
     }
-    MOE_TOPK_CASE(1)
     MOE_TOPK_CASE(2)
     MOE_TOPK_CASE(4)
     MOE_TOPK_CASE(8)
@@ -235,6 +295,33 @@ cudaError_t launch_topk_softmax(const float *logits, int64_t T, int64_t E, int64
     MOE_TOPK_CASE(32)
 #undef MOE_TOPK_CASE
     return cudaErrorInvalidValue;
+}
+
+template <int DT>
+cudaError_t launch_gate_typed(const void *x, const void *wg, const float *bias, int64_t T,
+                              int64_t d_h, int64_t E, int64_t k, float *logits, int32_t *idx,
+                              float *w, cudaStream_t stream) {
+    // E <= 64: 4 tokens x 64 experts per CTA (8 warps of 4 x 8 pairs), top-k fused
+    if (E <= 64)
+        return launch_gate_shape<DT, 4, 1, 8, true>(x, wg, bias, T, d_h, E, k, logits, idx, w, stream);
+    cudaError_t e;
+    if (T >= 512)  // 16 tokens x 32 experts per CTA: 16 warps of 4 x 8 pairs
+        e = launch_gate_shape<DT, 4, 4, 4, false>(x, wg, bias, T, d_h, E, k, logits, idx, w, stream);
+    else           // one warp of 4 x 8 pairs per CTA
+        e = launch_gate_shape<DT, 4, 1, 1, false>(x, wg, bias, T, d_h, E, k, logits, idx, w, stream);
+    if (e != cudaSuccess) return e;
+    return launch_topk(logits, T, E, k, idx, w, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_gate_topk(const void *x, const void *wg, const float *bias, int64_t T,
+                             int64_t d_h, int64_t E, int64_t k, int dtype, float *logits,
+                             int32_t *topk_idx, float *topk_w, cudaStream_t stream) {
+    if (T <= 0) return cudaSuccess;
+    if (dtype == kBF16)
+        return launch_gate_typed<kBF16>(x, wg, bias, T, d_h, E, k, logits, topk_idx, topk_w, stream);
+    return launch_gate_typed<kF16>(x, wg, bias, T, d_h, E, k, logits, topk_idx, topk_w, stream);
 }
 
 }  // namespace moe

@@ -19,9 +19,10 @@
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (thread = row), stage 1
 //               fuses silu(gate)*up, stage 2 the optional row weight; round to
 //               the activation dtype and store only the block's valid rows.
-// Tiles are (M block, N tile) pairs in M-block-major order, dealt round-robin
-// to the CTAs; blocks with no valid rows (the padding blocks the tables
-// create) are skipped by every role.  Every wait is bounded (see
+// Tiles are (M block, N tile) pairs; the blocks are ordered by the schedule
+// below (full and partial blocks interleaved; blocks with no valid rows, the
+// padding blocks the tables create, left out) and dealt round-robin to the
+// CTAs.  Every wait is bounded (see
 // mbar_wait_bounded): on a timeout the kernel records kErrTimeout, drains the
 // copies and MMAs it issued, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -44,7 +45,9 @@ constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int B_BYTES = MMA_N * BK * 2;      // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES;
+constexpr int MAX_SCHED = 4096;  // M blocks the in-kernel schedule can order
+constexpr int SCHED_BYTES = MAX_SCHED * 4 + MAX_SCHED + 64;
+constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES + SCHED_BYTES;
 
 struct GemmParams {
     const int32_t *sizes;
@@ -64,17 +67,68 @@ struct TileInfo {
     int g, m_start, rows, n0;
 };
 
-__device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int tile, int out_n) {
-    const int bx = tile / p.n_tiles;
-    const int nt = tile - bx * p.n_tiles;
+// Valid rows of M block bx (the pages' actual_rows) and its first row.
+__device__ __forceinline__ int block_rows(const GemmParams &p, int bx, int *g_out, int *m_start) {
+    const int g = __ldg(p.gidx + bx);
+    const int rel = bx * BM - __ldg(p.padded + g);
+    int rows = __ldg(p.sizes + g) - rel;
+    rows = rows < 0 ? 0 : (rows > BM ? BM : rows);
+    if (g_out) *g_out = g;
+    if (m_start) *m_start = rel + __ldg(p.offsets + g);
+    return rows;
+}
+
+// The tile schedule.  Non-empty M blocks are split into full blocks (128
+// valid rows: the tensor pipe is the limit) and partial blocks (mostly
+// padding: streaming the expert's weights is the limit), each list in block
+// order, and the two lists are interleaved evenly; the N tiles of one block
+// stay adjacent.  Dealt round-robin to the persistent CTAs, every window of
+// consecutive tiles then mixes both kinds, so the tensor pipe and HBM are
+// busy at the same time, while the blocks of one large expert still run
+// close together and share its weights through L2.
+struct Schedule {
+    const int *list;  // [n_full full blocks][n_partial partial blocks]; null = natural order
+    int n_full, n_blocks;
+};
+
+__device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const Schedule &sc, int tile,
+                                              int out_n) {
+    const int bp = tile / p.n_tiles;
+    const int nt = tile - bp * p.n_tiles;
+    int bx = bp;
+    if (sc.list) {
+        const int hb = static_cast<int>(static_cast<int64_t>(bp) * sc.n_full / sc.n_blocks);
+        const int hn = static_cast<int>(static_cast<int64_t>(bp + 1) * sc.n_full / sc.n_blocks);
+        bx = hn > hb ? sc.list[hb] : sc.list[sc.n_full + (bp - hb)];
+    }
     TileInfo t;
-    t.g = __ldg(p.gidx + bx);
-    const int rel = bx * BM - __ldg(p.padded + t.g);
-    int rows = __ldg(p.sizes + t.g) - rel;
-    t.rows = rows < 0 ? 0 : (rows > BM ? BM : rows);
-    t.m_start = rel + __ldg(p.offsets + t.g);
+    t.rows = block_rows(p, bx, &t.g, &t.m_start);
     t.n0 = nt * out_n;
     return t;
+}
+
+// Exclusive scan of one int per thread across the CTA; returns the total.
+template <int NT>
+__device__ __forceinline__ int cta_exclusive_scan(int v, int *scratch, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    int base = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+        const int x = scratch[w];
+        if (w < warp) base += x;
+        tot += x;
+    }
+    __syncthreads();
+    *total = tot;
+    return base + incl - v;
 }
 
 // A wait used only while winding down after an abort: bounded, ignores the
@@ -103,6 +157,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *sched = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(bars) + BAR_BYTES);
+    uint8_t *sched_cls = reinterpret_cast<uint8_t *>(sched + MAX_SCHED);
+    int *sched_scratch = reinterpret_cast<int *>(sched_cls + MAX_SCHED);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -131,21 +188,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish();
     }
+    // ----- schedule: classify the M blocks, list full and partial ones -----
+    Schedule sc{nullptr, 0, p.m_blocks};
+    if (p.m_blocks <= MAX_SCHED) {
+        for (int bx = threadIdx.x; bx < p.m_blocks; bx += NUM_THREADS) {
+            const int r = block_rows(p, bx, nullptr, nullptr);
+            sched_cls[bx] = r == 0 ? 0 : (r == BM ? 2 : 1);
+        }
+        __syncthreads();
+        const int chunk = (p.m_blocks + NUM_THREADS - 1) / NUM_THREADS;
+        const int lo = threadIdx.x * chunk;
+        const int hi = min(p.m_blocks, lo + chunk);
+        int nf = 0, np = 0;
+        for (int bx = lo; bx < hi; ++bx) {
+            nf += sched_cls[bx] == 2;
+            np += sched_cls[bx] == 1;
+        }
+        int tot_f, tot_p;
+        int bf = cta_exclusive_scan<NUM_THREADS>(nf, sched_scratch, &tot_f);
+        int bpart = cta_exclusive_scan<NUM_THREADS>(np, sched_scratch, &tot_p);
+        for (int bx = lo; bx < hi; ++bx) {
+            if (sched_cls[bx] == 2) sched[bf++] = bx;
+            else if (sched_cls[bx] == 1) sched[tot_f + bpart++] = bx;
+        }
+        sc.list = sched;
+        sc.n_full = tot_f;
+        sc.n_blocks = tot_f + tot_p;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = p.m_blocks * p.n_tiles;
+    const int total = sc.n_blocks * p.n_tiles;
 
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
+            const uint64_t pol_first = l2_policy_evict_first();
+            const uint64_t pol_last = l2_policy_evict_last();
             int stage = 0;
             uint32_t phase = 0;
             long issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-                const TileInfo ti = tile_info(p, tile, OUT_N);
+                const TileInfo ti = tile_info(p, sc, tile, OUT_N);
                 if (ti.rows == 0) continue;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
@@ -157,11 +243,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t a_dst = smem_u32(sA + stage * A_BYTES);
                     const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
                     tma_load_2d(a_dst, &tmA, fb, kb * BK, ti.m_start);
+                    // weights of a partial block are read by this block only:
+                    // let them leave L2 first, ahead of reused data
+                    const uint64_t pol = ti.rows < BM ? pol_first : pol_last;
                     if (GATE_UP) {
-                        tma_load_3d(b_dst, &tmB0, fb, kb * BK, ti.n0, ti.g);
-                        tma_load_3d(b_dst + B_BYTES / 2, &tmB1, fb, kb * BK, ti.n0, ti.g);
+                        tma_load_3d_hint(b_dst, &tmB0, fb, kb * BK, ti.n0, ti.g, pol);
+                        tma_load_3d_hint(b_dst + B_BYTES / 2, &tmB1, fb, kb * BK, ti.n0, ti.g, pol);
                     } else {
-                        tma_load_3d(b_dst, &tmB0, fb, kb * BK, ti.n0, ti.g);
+                        tma_load_3d_hint(b_dst, &tmB0, fb, kb * BK, ti.n0, ti.g, pol);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -189,7 +278,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t last_bar = 0, last_parity = 0;
             bool committed = false;
             for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-                const TileInfo ti = tile_info(p, tile, OUT_N);
+                const TileInfo ti = tile_info(p, sc, tile, OUT_N);
                 if (ti.rows == 0) continue;
                 const int acc = local & 1;
                 const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
@@ -234,7 +323,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row = q * 32 + lane;
         int local = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            const TileInfo ti = tile_info(p, tile, OUT_N);
+            const TileInfo ti = tile_info(p, sc, tile, OUT_N);
             if (ti.rows == 0) continue;
             const int acc = local & 1;
             const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
@@ -351,8 +440,16 @@ template <int DT, bool GATE_UP>
 cudaError_t launch_typed(const CUtensorMap &ta, const CUtensorMap &tb0, const CUtensorMap &tb1,
                          const GemmParams &p, int grid, cudaStream_t stream) {
     auto kern = grouped_gemm_kernel<DT, GATE_UP>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
+    // the shared-memory opt-in is set once per device (cheap launches, and no
+    // attribute call while a graph is being captured after the first use)
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
     kern<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb0, tb1, p);
     return cudaGetLastError();
 }

@@ -10,12 +10,10 @@ namespace moe {
 
 int device_sm_count();
 
-// gate_topk.cu
-cudaError_t launch_gate_logits(const void *x, const void *wg, const float *bias, int64_t T,
-                               int64_t d_h, int64_t E, int dtype, float *logits,
-                               cudaStream_t stream);
-cudaError_t launch_topk_softmax(const float *logits, int64_t T, int64_t E, int64_t k,
-                                int32_t *topk_idx, float *topk_w, cudaStream_t stream);
+// gate_topk.cu: logits (written to `logits`, [T, E] fp32), top-k ids and weights
+cudaError_t launch_gate_topk(const void *x, const void *wg, const float *bias, int64_t T,
+                             int64_t d_h, int64_t E, int64_t k, int dtype, float *logits,
+                             int32_t *topk_idx, float *topk_w, cudaStream_t stream);
 
 // dispatch.cu
 size_t dispatch_scratch_bytes(int64_t n_pairs, int64_t E);

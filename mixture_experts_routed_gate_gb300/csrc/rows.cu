@@ -162,10 +162,221 @@ __global__ void __launch_bounds__(RD_THREADS)
     if (bad && err) atomicExch(err, kErrDeviceFlag);
 }
 
+// ---------------------------------------------------------------------------
+// Persistent combine fed by bulk copies (TileOPs-Metax PR #55 section 1 "H
+// tiling" and "look-ahead", done with the copy engine): a work item is one
+// token and one H tile of HT elements.  Warp 0 is the producer: lane j reads
+// pos[t, j] and w[t, j]; each valid slot row's H tile is fetched with one
+// cp.async.bulk into a stage of a shared-memory ring (all K slots of an item
+// land on the stage's mbarrier); the slot weights and the valid mask go into
+// the stage header.  Warps 1..4 consume: thread i accumulates 8 hidden
+// elements over the valid slots in ascending order (acc = acc + w*x, the same
+// roundings as the plain definition) and stores them once.  The producer runs
+// RD_STAGES items ahead, so the position lookups and the row fetches of later
+// items overlap the arithmetic of earlier ones.
+// ---------------------------------------------------------------------------
+constexpr int RB_CONSUMER_WARPS = 4;
+constexpr int RB_THREADS = 32 * (1 + RB_CONSUMER_WARPS);
+constexpr int RB_MAX_K = 32;
+constexpr int RB_HEADER = 256;  // weights[32] + mask, padded
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void rb_wait_drain(uint32_t bar, uint32_t parity) {
+    const unsigned long long start = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - start > kWaitTimeoutNs) return;
+}
+
+template <typename TIn>
+__device__ __forceinline__ void load8_smem(const uint8_t *p, float (&f)[8]);
+template <>
+__device__ __forceinline__ void load8_smem<__nv_bfloat16>(const uint8_t *p, float (&f)[8]) {
+    unpack8(Vec8<__nv_bfloat16>{*reinterpret_cast<const uint4 *>(p)}, f);
+}
+template <>
+__device__ __forceinline__ void load8_smem<__half>(const uint8_t *p, float (&f)[8]) {
+    unpack8(Vec8<__half>{*reinterpret_cast<const uint4 *>(p)}, f);
+}
+template <>
+__device__ __forceinline__ void load8_smem<float>(const uint8_t *p, float (&f)[8]) {
+    const uint4 *q = reinterpret_cast<const uint4 *>(p);
+    unpack8(Vec8<float>{q[0], q[1]}, f);
+}
+
+template <typename TIn, typename TOut>
+__global__ void __launch_bounds__(RB_THREADS)
+    reduce_bulk_kernel(const TIn *__restrict__ x, int64_t n_rows, const int32_t *__restrict__ pos,
+                       const float *__restrict__ w, int T, int K, int H, int HT, int stages,
+                       TOut *__restrict__ out, int32_t *__restrict__ err) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row_bytes = HT * static_cast<int>(sizeof(TIn));
+    const int stage_bytes = RB_HEADER + K * row_bytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + stages * stage_bytes);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * stages);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (stages + s); };
+    const int tiles = H / HT;
+    const int64_t n_items = static_cast<int64_t>(T) * tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), RB_CONSUMER_WARPS);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ------------------------------- producer -------------------------------
+        int stage = 0;
+        uint32_t phase = 0;
+        long issued = 0;
+        bool ok = true;
+        int64_t item = blockIdx.x;
+        int p_next = -1;
+        float w_next = 1.0f;
+        if (item < n_items && lane < K) {
+            const int64_t t = item / tiles;
+            p_next = __ldg(pos + t * K + lane);
+            if (w) w_next = __ldg(w + t * K + lane);
+        }
+        for (; item < n_items; item += gridDim.x) {
+            const int p = p_next;
+            const float wv = w_next;
+            const int64_t t = item / tiles;
+            const int ht = static_cast<int>(item - t * tiles);
+            // prefetch the next item's positions and weights
+            const int64_t nxt = item + gridDim.x;
+            if (nxt < n_items && lane < K) {
+                const int64_t tn = nxt / tiles;
+                p_next = __ldg(pos + tn * K + lane);
+                w_next = w ? __ldg(w + tn * K + lane) : 1.0f;
+            }
+            const bool valid = lane < K && p >= 0 && p < n_rows;
+            const bool bad = lane < K && (p < -1 || p >= n_rows);
+            const unsigned mask = __ballot_sync(0xffffffffu, valid);
+            if (__any_sync(0xffffffffu, bad) && lane == 0 && err) atomicExch(err, kErrDeviceFlag);
+            int go = 1;
+            if (lane == 0) go = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, err) ? 1 : 0;
+            go = __shfl_sync(0xffffffffu, go, 0);
+            if (!go) {
+                ok = false;
+                break;
+            }
+            uint8_t *st = smem + stage * stage_bytes;
+            if (lane < K) reinterpret_cast<float *>(st)[lane] = wv;
+            if (lane == 0) {
+                reinterpret_cast<unsigned *>(st)[RB_MAX_K] = mask;
+                mbar_arrive_expect_tx(full_bar(stage), static_cast<uint32_t>(__popc(mask) * row_bytes));
+            }
+            __syncwarp();
+            if (valid)
+                bulk_g2s(smem_u32(st + RB_HEADER + lane * row_bytes),
+                         x + static_cast<int64_t>(p) * H + static_cast<int64_t>(ht) * HT,
+                         static_cast<uint32_t>(row_bytes), full_bar(stage));
+            ++issued;
+            if (++stage == stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok && lane == 0) {
+            for (long j = 1; j <= stages && j <= issued; ++j) {
+                const long i = issued - j;
+                rb_wait_drain(full_bar(static_cast<int>(i % stages)), static_cast<uint32_t>((i / stages) & 1));
+            }
+        }
+    } else {
+        // ------------------------------- consumers ------------------------------
+        const int ct = threadIdx.x - 32;  // 0 .. 127
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+            const int64_t t = item / tiles;
+            const int ht = static_cast<int>(item - t * tiles);
+            int go = 1;
+            if (lane == 0) go = mbar_wait_bounded(full_bar(stage), phase, abort_flag, err) ? 1 : 0;
+            go = __shfl_sync(0xffffffffu, go, 0);
+            if (!go) break;
+            const uint8_t *st = smem + stage * stage_bytes;
+            const unsigned mask = reinterpret_cast<const unsigned *>(st)[RB_MAX_K];
+            for (int v = ct; v < HT / 8; v += 32 * RB_CONSUMER_WARPS) {
+                float acc[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+                for (int k = 0; k < K; ++k) {
+                    if ((mask >> k) & 1u) {
+                        const float wk = reinterpret_cast<const float *>(st)[k];
+                        float f[8];
+                        load8_smem<TIn>(st + RB_HEADER + k * row_bytes + v * 8 * static_cast<int>(sizeof(TIn)), f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wk, f[i]));
+                    }
+                }
+                store8<TOut>(out + t * H + static_cast<int64_t>(ht) * HT + v * 8, acc);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(stage));
+            if (++stage == stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
+template <typename TIn, typename TOut>
+cudaError_t launch_reduce_bulk(const void *x, int64_t n_rows, const int32_t *pos, const float *w,
+                               int64_t T, int64_t K, int64_t H, void *out, int32_t *err,
+                               cudaStream_t stream) {
+    // H tile: the largest of 1024 / 512 / 256 that divides H with a slot row <= 2 KB
+    int HT = 256;
+    for (int cand : {1024, 512}) {
+        if (H % cand == 0 && cand * static_cast<int>(sizeof(TIn)) <= 2048) {
+            HT = cand;
+            break;
+        }
+    }
+    const int stage_bytes = RB_HEADER + static_cast<int>(K) * HT * static_cast<int>(sizeof(TIn));
+    int stages = (64 * 1024) / stage_bytes;
+    stages = stages < 2 ? 2 : (stages > 6 ? 6 : stages);
+    const size_t smem = static_cast<size_t>(stages) * stage_bytes + 16 * stages + 16;
+    auto kern = reduce_bulk_kernel<TIn, TOut>;
+    static size_t attr_bytes[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (smem > 48 * 1024 && (dev < 0 || dev >= 64 || attr_bytes[dev] < smem)) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_bytes[dev] = smem;
+    }
+    const int per_sm = static_cast<int>((200 * 1024) / smem) < 1 ? 1 : static_cast<int>((200 * 1024) / smem);
+    const int64_t n_items = T * (H / HT);
+    int64_t grid = static_cast<int64_t>(device_sm_count()) * (per_sm > 4 ? 4 : per_sm);
+    if (grid > n_items) grid = n_items;
+    kern<<<static_cast<unsigned>(grid), RB_THREADS, smem, stream>>>(
+        static_cast<const TIn *>(x), n_rows, pos, w, static_cast<int>(T), static_cast<int>(K),
+        static_cast<int>(H), HT, stages, static_cast<TOut *>(out), err);
+    return cudaGetLastError();
+}
+
 template <typename TIn, typename TOut>
 cudaError_t launch_reduce_typed(const void *x, int64_t n_rows, const int32_t *pos, const float *w,
                                 int64_t T, int64_t K, int64_t H, void *out, int32_t *err,
                                 cudaStream_t stream) {
+    if (K <= RB_MAX_K)
+        return launch_reduce_bulk<TIn, TOut>(x, n_rows, pos, w, T, K, H, out, err, stream);
     const int64_t threads = T * (H / 8);
     const int64_t blocks = (threads + RD_THREADS - 1) / RD_THREADS;
     reduce_fused_kernel<TIn, TOut><<<static_cast<unsigned>(blocks), RD_THREADS, 0, stream>>>(

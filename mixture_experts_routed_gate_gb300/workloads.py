@@ -110,21 +110,24 @@ def _stacked_normal(E: int, rows: int, cols: int, std: float, dtype: str,
 
 
 def make_moe_inputs(cfg: MoEConfig, device="cpu", seed: int | None = None,
-                    T: int | None = None) -> dict:
+                    T: int | None = None, with_experts: bool = True) -> dict:
     """x [T,d_h]; wg [E,d_h]; bias [E] fp32 or None; w_gate, w_up [E,d_e,d_h];
-    w_down [E,d_h,d_e].  ``T`` overrides the token count (same weights)."""
+    w_down [E,d_h,d_e].  ``T`` overrides the token count (same weights);
+    ``with_experts=False`` skips the expert weights (gate-only use)."""
     seed = cfg.seed if seed is None else seed
     T = cfg.T if T is None else T
     d_h, d_e, E, dt = cfg.d_hidden, cfg.d_expert, cfg.n_experts, cfg.dtype
     gen = _gen(device, seed)
     wg = _normal((E, d_h), 1.0 / math.sqrt(d_h), dt, gen, device)
-    w_gate = _stacked_normal(E, d_e, d_h, 1.0 / math.sqrt(d_h), dt, gen, device)
-    w_up = _stacked_normal(E, d_e, d_h, 1.0 / math.sqrt(d_h), dt, gen, device)
-    w_down = _stacked_normal(E, d_h, d_e, 1.0 / math.sqrt(d_e), dt, gen, device)
     bias = None
     if cfg.zipf_bias:
         rank = torch.randperm(E, generator=gen, device=device).to(torch.float64) + 1.0
         bias = (-1.1 * torch.log(rank)).to(torch.float32)
+    w_gate = w_up = w_down = None
+    if with_experts:
+        w_gate = _stacked_normal(E, d_e, d_h, 1.0 / math.sqrt(d_h), dt, gen, device)
+        w_up = _stacked_normal(E, d_e, d_h, 1.0 / math.sqrt(d_h), dt, gen, device)
+        w_down = _stacked_normal(E, d_h, d_e, 1.0 / math.sqrt(d_e), dt, gen, device)
     xgen = _gen(device, seed * 1000003 + T)
     x = _normal((T, d_h), 1.0, dt, xgen, device)
     return dict(x=x, wg=wg, bias=bias, w_gate=w_gate, w_up=w_up, w_down=w_down)

@@ -77,6 +77,31 @@ def test_forward_token_counts(oracle, T):
     assert_close(bits(out), ref["out"], cfg.dtype, *MOE_TOL[cfg.dtype], "out")
 
 
+@pytest.mark.parametrize("host_io", [False, True])
+def test_forward_graph_replay_matches_eager(host_io):
+    """moe_forward captured into a CUDA graph (binding.ForwardGraph) and
+    replayed on new tokens gives the same bits as eager calls."""
+    dev = require_cuda()
+    cfg = workloads.MOE_CONFIGS["decode"]
+    d = workloads.make_moe_inputs(cfg, device=dev)
+    fg = binding.ForwardGraph(d["wg"], d["bias"], d["w_gate"], d["w_up"], d["w_down"], cfg.top_k,
+                              cfg.T, host_io=host_io)
+    for seed in (1, 2):
+        x = workloads.make_tokens(cfg, cfg.T, device=dev, seed=seed)
+        if host_io:
+            fg.x_host.copy_(x.cpu())
+        else:
+            fg.x.copy_(x)
+        torch.cuda.synchronize()
+        fg.replay()
+        torch.cuda.synchronize()
+        got = fg.out_host if host_io else fg.out
+        want = binding.moe_forward(x, d["wg"], d["bias"], d["w_gate"], d["w_up"], d["w_down"], cfg.top_k)
+        torch.cuda.synchronize()
+        assert torch.equal(got.cpu().view(torch.int16), want.cpu().view(torch.int16))
+        assert int(fg.err.item()) == 0
+
+
 def _compact(w, experts):
     """The listed experts' slices of a stacked weight, on the host."""
     idx = torch.as_tensor(experts, dtype=torch.long, device=w.device)

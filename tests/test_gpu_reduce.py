@@ -63,6 +63,18 @@ def test_reduce_f32_in_half_out(oracle, out_dtype):
     assert_bits_equal(bits(out), want, "f32 -> half combine")
 
 
+@pytest.mark.parametrize("K", [32, 40])
+def test_reduce_many_slots(oracle, K):
+    """K = 32 is the widest the bulk-copy kernel takes; K = 40 goes through the
+    per-thread kernel."""
+    dev = require_cuda()
+    d = workloads.make_reduce_inputs(16, K, 512, "bf16", 8, device=dev)
+    out = _run(d, "bf16")
+    torch.cuda.synchronize()
+    want, _ = _ref(oracle, d, "bf16")
+    assert_bits_equal(bits(out), want, f"K={K}")
+
+
 def test_reduce_k1_identity_and_all_padding():
     dev = require_cuda()
     T, H = 33, 512

@@ -88,18 +88,21 @@ def test_gate_ties_go_to_lower_id(oracle):
 @pytest.mark.parametrize("T,k,E,skew", [(64, 2, 8, False), (64, 6, 64, False),
                                         (3000, 8, 256, True), (1, 4, 4, False),
                                         (500, 1, 1, False), (4096, 8, 256, True),
-                                        (1024, 1, 8, False)])
+                                        (1024, 1, 8, False), (2048, 8, 256, True),
+                                        (2049, 8, 256, True), (40, 4, 300, False),
+                                        (0, 2, 8, False)])
 def test_dispatch_tables_bit_exact(oracle, T, k, E, skew):
     dev = require_cuda()
     rng = np.random.default_rng(T * 7 + E)
     if skew:
         p = 1.0 / np.arange(1, E + 1) ** 1.1
         p /= p.sum()
-        idx = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+        idx = np.array([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)], np.int32)
     else:
-        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        idx = np.array([rng.permutation(E)[:k] for _ in range(T)], np.int32)
     if T == 1024 and k == 1:
         idx[:] = np.repeat(np.arange(8), 128).reshape(T, 1)  # every count a multiple of 128
+    idx = idx.reshape(T, k)
     w = rng.random((T, k)).astype(np.float32)
     tab = binding.moe_build_dispatch(torch.from_numpy(idx).to(dev), torch.from_numpy(w).to(dev), E)
     torch.cuda.synchronize()
