@@ -357,29 +357,48 @@ def measure_e2e(args, cfg, d, dev, flush, world):
 
 
 def measure_reduce_aux(dev, flush, reps: int = 20):
-    """moe_reduce_fused alone on the bf16 T x 8 x 7168 workloads (GB/s)."""
+    """moe_reduce_fused alone on the bf16 T x 8 x 7168 workloads (GB/s), and
+    its scaled variants at T = 512 (x_sf; e4m3 output; sf + e4m3 output)."""
     from mixture_experts_routed_gate_gb300 import binding
-    res = {}
-    for name in ("reduce-512", "reduce-4096"):
-        c = workloads.REDUCE_CONFIGS[name]
-        r = workloads.make_reduce_inputs(c.T, c.K, c.H, c.dtype, c.seed, device=dev)
-        out = torch.empty((c.T, c.H), dtype=torch.bfloat16, device=dev)
+
+    def time_it(fn):
         for _ in range(3):
-            binding.moe_reduce_fused(r["x"], r["pos"], r["w"], out=out)
+            fn()
         ts = []
         for _ in range(reps):
             flush()
-            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s.record()
-            binding.moe_reduce_fused(r["x"], r["pos"], r["w"], out=out)
-            e.record()
-            e.synchronize()
-            ts.append(s.elapsed_time(e))
+            s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_.record()
+            fn()
+            e_.record()
+            e_.synchronize()
+            ts.append(s_.elapsed_time(e_))
+        return statistics.median(ts)
+
+    res = {}
+    for name in ("reduce-512", "reduce-4096"):
+        c = workloads.REDUCE_CONFIGS[name]
+        r = workloads.make_reduce_inputs(c.T, c.K, c.H, c.dtype, c.seed, device=dev, scales=True)
+        out = torch.empty((c.T, c.H), dtype=torch.bfloat16, device=dev)
         n_valid = int((r["pos"] >= 0).sum().item())
         nbytes = roofline.reduce_bytes(n_valid, c.T, c.K, c.H, 2, 2)
-        ms = statistics.median(ts)
+        ms = time_it(lambda: binding.moe_reduce_fused(r["x"], r["pos"], r["w"], out=out))
         res[name] = {"us": round(ms * 1e3, 2), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
                      "bytes": nbytes, "bytes_pages_formula": roofline.reduce_bytes_pages(c.T, c.K, c.H, 2)}
+        if name != "reduce-512":
+            continue
+        out8 = torch.empty((c.T, c.H), dtype=torch.float8_e4m3fn, device=dev)
+        variants = {
+            "with_x_sf": (lambda: binding.moe_reduce_fused_scaled(r["x"], r["pos"], r["w"], x_sf=r["x_sf"], out=out),
+                          nbytes + n_valid * 4),
+            "fp8_out": (lambda: binding.moe_reduce_fused_scaled(r["x"], r["pos"], r["w"], out=out8),
+                        nbytes - c.T * c.H),
+            "quantized": (lambda: binding.moe_reduce_fused_scaled(r["x"], r["pos"], r["w"], sf=r["sf"], out=out8),
+                          nbytes - c.T * c.H + c.T * 4),
+        }
+        for vname, (fn, vb) in variants.items():
+            ms = time_it(fn)
+            res[f"{name}-{vname}"] = {"us": round(ms * 1e3, 2), "gbs": round(vb / (ms * 1e-3) / 1e9, 1), "bytes": vb}
     return res
 
 

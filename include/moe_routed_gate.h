@@ -49,7 +49,8 @@ extern "C" {
 
 typedef struct CUstream_st *moe_stream_t; /* identical to cudaStream_t */
 
-typedef enum { MOE_F16 = 0, MOE_BF16 = 1, MOE_F32 = 2 } moe_dtype_t;
+/* MOE_E4M3 (float8 e4m3fn) is an output type of moe_reduce_fused_scaled only. */
+typedef enum { MOE_F16 = 0, MOE_BF16 = 1, MOE_F32 = 2, MOE_E4M3 = 3 } moe_dtype_t;
 
 typedef enum {
     MOE_OK = 0,
@@ -206,6 +207,26 @@ MOE_API moe_status_t moe_reduce_fused(const void *x, int64_t n_rows, const int32
                               const float *topk_weights, int64_t T, int64_t K, int64_t H,
                               moe_dtype_t in_dtype, moe_dtype_t out_dtype, void *out,
                               int32_t *err_flag, moe_stream_t stream);
+
+/*
+ * moe_reduce_fused with the scaling and output switches of TileOPs-Metax
+ * PR #55's op variants (WithXsf, Fp8, Quantized; section 1 "variants inlined
+ * into one kernel", commit "correct roofline FLOPs for the scaling variants"):
+ *   s[t,k]   = w[t,k] * x_sf[pos[t,k]]     x_sf: one fp32 scale per row of x
+ *                                            (per routed slot), or NULL = 1
+ *   acc[t,h] = sum over k ascending, valid pos, of s[t,k] * x[pos[t,k], h]
+ *   out[t,h] = cast(acc[t,h] * sf[t])        sf: one fp32 scale per token, or NULL
+ * with the same fp32 order and roundings as moe_reduce_fused (each product
+ * and sum rounded; sf applied after the sum).  out_dtype may be MOE_E4M3:
+ * float8 e4m3fn, round to nearest even, finite values saturated to +-448.
+ * x_sf has n_rows entries, sf has T.  Other arguments and errors as
+ * moe_reduce_fused.
+ */
+MOE_API moe_status_t moe_reduce_fused_scaled(const void *x, int64_t n_rows,
+                                     const int32_t *token_topk_to_pos, const float *topk_weights,
+                                     const float *x_sf, const float *sf, int64_t T, int64_t K,
+                                     int64_t H, moe_dtype_t in_dtype, moe_dtype_t out_dtype,
+                                     void *out, int32_t *err_flag, moe_stream_t stream);
 
 /*
  * The whole routed forward, stream ordered, no host round trip:

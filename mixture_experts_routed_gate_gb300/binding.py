@@ -15,8 +15,8 @@ import torch
 
 from . import _build
 
-_DT = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
-_DT_NAME = {0: "f16", 1: "bf16", 2: "f32"}
+_DT = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2, torch.float8_e4m3fn: 3}
+_DT_NAME = {0: "f16", 1: "bf16", 2: "f32", 3: "e4m3"}
 _lib = None
 
 BLOCK_M = 128
@@ -61,6 +61,7 @@ def lib():
         "moe_grouped_gate_up_silu": (I, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, P, P]),
         "moe_grouped_down": (I, [P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I, P, P, P]),
         "moe_reduce_fused": (I, [P, I64, P, P, I64, I64, I64, I, I, P, P, P]),
+        "moe_reduce_fused_scaled": (I, [P, I64, P, P, P, P, I64, I64, I64, I, I, P, P, P]),
         "moe_forward": (I, [P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, SZ, P, P, P]),
     }
     for name, (res, args) in sigs.items():
@@ -77,7 +78,7 @@ def exported_symbols():
             "moe_forward_workspace_offset", "moe_gate_topk", "moe_build_dispatch",
             "moe_build_dispatch_noalloc",
             "moe_gather_rows", "moe_grouped_gate_up_silu", "moe_grouped_down",
-            "moe_reduce_fused", "moe_forward"]
+            "moe_reduce_fused", "moe_reduce_fused_scaled", "moe_forward"]
 
 
 # --------------------------------------------------------------------------- helpers
@@ -298,7 +299,8 @@ def moe_reduce_fused(x, token_topk_to_pos, topk_weights=None, out_dtype=None, ou
             raise ValueError("topk_weights and token_topk_to_pos shapes differ")
     n_rows, H = x.shape
     T, K = token_topk_to_pos.shape
-    out_dtype = x.dtype if out_dtype is None else out_dtype
+    if out_dtype is None:
+        out_dtype = x.dtype if out is None else out.dtype
     if out is None:
         out = torch.empty((T, H), dtype=out_dtype, device=x.device)
     _cuda(out, "out", dtype=out_dtype)
@@ -309,6 +311,43 @@ def moe_reduce_fused(x, token_topk_to_pos, topk_weights=None, out_dtype=None, ou
                                       T, K, H, _dtype_code(x, "x"), _dtype_code(out, "out"),
                                       _ptr(out), _ptr(err), _stream(x.device)),
                "moe_reduce_fused")
+    return out
+
+
+def moe_reduce_fused_scaled(x, token_topk_to_pos, topk_weights=None, x_sf=None, sf=None,
+                            out_dtype=None, out=None, err=None):
+    """The combine with an optional per-row scale x_sf [n_rows], an optional
+    per-token scale sf [T] and an optional float8 e4m3fn output."""
+    _cuda(x, "x", ndim=2)
+    _cuda(token_topk_to_pos, "token_topk_to_pos", dtype=torch.int32, ndim=2)
+    n_rows, H = x.shape
+    T, K = token_topk_to_pos.shape
+    if topk_weights is not None:
+        if topk_weights.dtype != torch.float32:
+            raise TypeError(f"topk_weights must be torch.float32, got {topk_weights.dtype}")
+        _cuda(topk_weights, "topk_weights", dtype=torch.float32, ndim=2)
+        if topk_weights.shape != token_topk_to_pos.shape:
+            raise ValueError("topk_weights and token_topk_to_pos shapes differ")
+    if x_sf is not None:
+        _cuda(x_sf, "x_sf", dtype=torch.float32, ndim=1)
+        if x_sf.numel() != n_rows:
+            raise ValueError("x_sf must have one entry per row of x")
+    if sf is not None:
+        _cuda(sf, "sf", dtype=torch.float32, ndim=1)
+        if sf.numel() != T:
+            raise ValueError("sf must have one entry per token")
+    if out_dtype is None:
+        out_dtype = x.dtype if out is None else out.dtype
+    if out is None:
+        out = torch.empty((T, H), dtype=out_dtype, device=x.device)
+    _cuda(out, "out", dtype=out_dtype)
+    if err is not None:
+        _cuda(err, "err", dtype=torch.int32)
+    with torch.cuda.device(x.device):
+        _check(lib().moe_reduce_fused_scaled(
+            _ptr(x), n_rows, _ptr(token_topk_to_pos), _ptr(topk_weights), _ptr(x_sf), _ptr(sf), T, K,
+            H, _dtype_code(x, "x"), _dtype_code(out, "out"), _ptr(out), _ptr(err), _stream(x.device)),
+            "moe_reduce_fused_scaled")
     return out
 
 

@@ -221,22 +221,45 @@ moe_status_t moe_grouped_down(const void *h, const void *w_down, const int32_t *
         reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static bool reduce_pair_ok(moe_dtype_t in, moe_dtype_t out, bool allow_fp8) {
+    const bool in_ok = in == MOE_F16 || in == MOE_BF16 || in == MOE_F32;
+    if (!in_ok) return false;
+    if (out == in) return true;
+    if (in == MOE_F32 && (out == MOE_F16 || out == MOE_BF16)) return true;
+    return allow_fp8 && out == MOE_E4M3;
+}
+
+static moe_status_t reduce_common(const void *x, int64_t n_rows, const int32_t *pos,
+                                  const float *w, const float *x_sf, const float *sf, int64_t T,
+                                  int64_t K, int64_t H, moe_dtype_t in_dtype,
+                                  moe_dtype_t out_dtype, void *out, int32_t *err_flag,
+                                  moe_stream_t stream, bool allow_fp8) {
+    if (T < 0 || K <= 0 || H <= 0 || n_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (H % 256 != 0) return MOE_ERR_INVALID_ARG;
+    if (!reduce_pair_ok(in_dtype, out_dtype, allow_fp8)) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!out || !pos || (n_rows > 0 && !x)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(out) || (x && !aligned16(x))) return MOE_ERR_INVALID_ARG;
+    return cuda_status(moe::launch_reduce_fused(x, n_rows, pos, w, x_sf, sf, T, K, H, in_dtype,
+                                                out_dtype, out, err_flag,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_reduce_fused(const void *x, int64_t n_rows, const int32_t *token_topk_to_pos,
                               const float *topk_weights, int64_t T, int64_t K, int64_t H,
                               moe_dtype_t in_dtype, moe_dtype_t out_dtype, void *out,
                               int32_t *err_flag, moe_stream_t stream) {
-    if (T < 0 || K <= 0 || H <= 0 || n_rows < 0) return MOE_ERR_INVALID_ARG;
-    if (H % 256 != 0) return MOE_ERR_INVALID_ARG;
-    const bool pair_ok = (in_dtype == out_dtype &&
-                          (in_dtype == MOE_F16 || in_dtype == MOE_BF16 || in_dtype == MOE_F32)) ||
-                         (in_dtype == MOE_F32 && (out_dtype == MOE_F16 || out_dtype == MOE_BF16));
-    if (!pair_ok) return MOE_ERR_UNSUPPORTED;
-    if (T == 0) return MOE_OK;
-    if (!out || !token_topk_to_pos || (n_rows > 0 && !x)) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(out) || (x && !aligned16(x))) return MOE_ERR_INVALID_ARG;
-    return cuda_status(moe::launch_reduce_fused(x, n_rows, token_topk_to_pos, topk_weights, T, K,
-                                                H, in_dtype, out_dtype, out, err_flag,
-                                                reinterpret_cast<cudaStream_t>(stream)));
+    return reduce_common(x, n_rows, token_topk_to_pos, topk_weights, nullptr, nullptr, T, K, H,
+                         in_dtype, out_dtype, out, err_flag, stream, false);
+}
+
+moe_status_t moe_reduce_fused_scaled(const void *x, int64_t n_rows,
+                                     const int32_t *token_topk_to_pos, const float *topk_weights,
+                                     const float *x_sf, const float *sf, int64_t T, int64_t K,
+                                     int64_t H, moe_dtype_t in_dtype, moe_dtype_t out_dtype,
+                                     void *out, int32_t *err_flag, moe_stream_t stream) {
+    return reduce_common(x, n_rows, token_topk_to_pos, topk_weights, x_sf, sf, T, K, H, in_dtype,
+                         out_dtype, out, err_flag, stream, true);
 }
 
 moe_status_t moe_forward(const void *x, const void *w_g, const float *bias, const void *w_gate,

@@ -10,7 +10,7 @@
 
 namespace moe {
 
-enum DType : int { kF16 = 0, kBF16 = 1, kF32 = 2 };
+enum DType : int { kF16 = 0, kBF16 = 1, kF32 = 2, kE4M3 = 3 };
 
 // Device error codes written into the caller's err_flag word (same values as
 // moe_status_t in the public header).

@@ -27,8 +27,9 @@ cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_
 cudaError_t launch_gather_rows(const void *x, const int32_t *sorted_token_idx, int64_t n_rows,
                                int64_t d_h, int elem_bytes, void *a_out, cudaStream_t stream);
 cudaError_t launch_reduce_fused(const void *x, int64_t n_rows, const int32_t *pos,
-                                const float *w, int64_t T, int64_t K, int64_t H, int in_dtype,
-                                int out_dtype, void *out, int32_t *err, cudaStream_t stream);
+                                const float *w, const float *x_sf, const float *sf, int64_t T,
+                                int64_t K, int64_t H, int in_dtype, int out_dtype, void *out,
+                                int32_t *err, cudaStream_t stream);
 
 // grouped_gemm.cu
 cudaError_t launch_grouped_gemm(bool gate_up, int dtype, const void *a, const void *w0,

@@ -1,5 +1,7 @@
 // rows.cu -- the two row-moving steps of the routed MoE forward: the gather of
 // token rows into expert order and the moe_reduce_fused combine.
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -116,10 +118,21 @@ __device__ __forceinline__ void store8<float>(float *p, const float (&f)[8]) {
     q[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
 
+// float8 e4m3fn output: round to nearest even, saturate to the finite range
+template <>
+__device__ __forceinline__ void store8<__nv_fp8_e4m3>(__nv_fp8_e4m3 *p, const float (&f)[8]) {
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        q[i] = __nv_cvt_float2_to_fp8x2(make_float2(f[2 * i], f[2 * i + 1]), __NV_SATFINITE, __NV_E4M3);
+    *reinterpret_cast<uint2 *>(p) = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+}
+
 template <typename TIn, typename TOut>
 __global__ void __launch_bounds__(RD_THREADS)
     reduce_fused_kernel(const TIn *__restrict__ x, int64_t n_rows,
-                        const int32_t *__restrict__ pos, const float *__restrict__ w, int64_t T,
+                        const int32_t *__restrict__ pos, const float *__restrict__ w,
+                        const float *__restrict__ x_sf, const float *__restrict__ sf, int64_t T,
                         int K, int H, TOut *__restrict__ out, int32_t *__restrict__ err) {
     const int vpr = H >> 3;  // 8-element vectors per row
     const int64_t gid = static_cast<int64_t>(blockIdx.x) * RD_THREADS + threadIdx.x;
@@ -145,6 +158,7 @@ __global__ void __launch_bounds__(RD_THREADS)
                 use[j] = p >= 0 && p < n_rows;
                 bad |= (p < -1) || (p >= n_rows);
                 if (wrow) wk[j] = __ldg(wrow + k0 + j);
+                if (use[j] && x_sf) wk[j] = __fmul_rn(wk[j], __ldg(x_sf + p));
                 if (use[j]) buf[j] = load8<TIn>(x + static_cast<int64_t>(p) * H + h0);
             }
         }
@@ -157,6 +171,11 @@ __global__ void __launch_bounds__(RD_THREADS)
                 for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wk[j], f[i]));
             }
         }
+    }
+    if (sf) {
+        const float sv = __ldg(sf + t);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = __fmul_rn(acc[i], sv);
     }
     store8<TOut>(out + t * H + h0, acc);
     if (bad && err) atomicExch(err, kErrDeviceFlag);
@@ -172,8 +191,7 @@ __global__ void __launch_bounds__(RD_THREADS)
 // the stage header.  Warps 1..4 consume: thread i accumulates 8 hidden
 // elements over the valid slots in ascending order (acc = acc + w*x, the same
 // roundings as the plain definition) and stores them once.  The producer runs
-// RD_STAGES items ahead, so the position lookups and the row fetches of later
-// items overlap the arithmetic of earlier ones.
+// up to `stages` items ahead of the consumers.
 // ---------------------------------------------------------------------------
 constexpr int RB_CONSUMER_WARPS = 4;
 constexpr int RB_THREADS = 32 * (1 + RB_CONSUMER_WARPS);
@@ -212,7 +230,8 @@ __device__ __forceinline__ void load8_smem<float>(const uint8_t *p, float (&f)[8
 template <typename TIn, typename TOut>
 __global__ void __launch_bounds__(RB_THREADS)
     reduce_bulk_kernel(const TIn *__restrict__ x, int64_t n_rows, const int32_t *__restrict__ pos,
-                       const float *__restrict__ w, int T, int K, int H, int HT, int stages,
+                       const float *__restrict__ w, const float *__restrict__ x_sf,
+                       const float *__restrict__ sf, int T, int K, int H, int HT, int stages,
                        TOut *__restrict__ out, int32_t *__restrict__ err) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -236,35 +255,50 @@ __global__ void __launch_bounds__(RB_THREADS)
     }
     __syncthreads();
 
+    // Items are dealt round-robin (neighbouring CTAs read neighbouring H tiles
+    // of the same rows, which keeps DRAM pages open).  The producer holds the
+    // positions and weights of a group of 32/K items in its lanes (lane l has
+    // slot l % K of item l / K) and loads the next group while issuing the
+    // current one, so the position lookups stay off the critical path.
     if (warp == 0) {
         // ------------------------------- producer -------------------------------
+        const int G = 32 / K;  // items per group
+        const int my_q = lane / K, my_k = lane - (lane / K) * K;
+        const bool slot_lane = lane < G * K;
+        auto load_group = [&](int64_t first, int &pv, float &wv) {
+            pv = -1;
+            wv = 1.0f;
+            const int64_t item = blockIdx.x + (first + my_q) * static_cast<int64_t>(gridDim.x);
+            if (slot_lane && item < n_items) {
+                const int64_t t = item / tiles;
+                pv = __ldg(pos + t * K + my_k);
+                if (w) wv = __ldg(w + t * K + my_k);
+            }
+        };
         int stage = 0;
         uint32_t phase = 0;
         long issued = 0;
         bool ok = true;
-        int64_t item = blockIdx.x;
-        int p_next = -1;
-        float w_next = 1.0f;
-        if (item < n_items && lane < K) {
-            const int64_t t = item / tiles;
-            p_next = __ldg(pos + t * K + lane);
-            if (w) w_next = __ldg(w + t * K + lane);
-        }
-        for (; item < n_items; item += gridDim.x) {
-            const int p = p_next;
-            const float wv = w_next;
+        int p_cur, p_nxt;
+        float w_cur, w_nxt;
+        load_group(0, p_cur, w_cur);
+        load_group(G, p_nxt, w_nxt);
+        for (int64_t sidx = 0;; ++sidx) {
+            const int64_t item = blockIdx.x + sidx * static_cast<int64_t>(gridDim.x);
+            if (item >= n_items) break;
+            const int q = static_cast<int>(sidx % G);
+            if (q == 0 && sidx > 0) {
+                p_cur = p_nxt;
+                w_cur = w_nxt;
+                load_group(sidx + G, p_nxt, w_nxt);
+            }
             const int64_t t = item / tiles;
             const int ht = static_cast<int>(item - t * tiles);
-            // prefetch the next item's positions and weights
-            const int64_t nxt = item + gridDim.x;
-            if (nxt < n_items && lane < K) {
-                const int64_t tn = nxt / tiles;
-                p_next = __ldg(pos + tn * K + lane);
-                w_next = w ? __ldg(w + tn * K + lane) : 1.0f;
-            }
-            const bool valid = lane < K && p >= 0 && p < n_rows;
-            const bool bad = lane < K && (p < -1 || p >= n_rows);
-            const unsigned mask = __ballot_sync(0xffffffffu, valid);
+            const bool mine = slot_lane && my_q == q;
+            const bool valid = mine && p_cur >= 0 && p_cur < n_rows;
+            const bool bad = mine && (p_cur < -1 || p_cur >= n_rows);
+            const unsigned mask = (__ballot_sync(0xffffffffu, valid) >> (q * K)) &
+                                  (K == 32 ? 0xffffffffu : ((1u << K) - 1u));
             if (__any_sync(0xffffffffu, bad) && lane == 0 && err) atomicExch(err, kErrDeviceFlag);
             int go = 1;
             if (lane == 0) go = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, err) ? 1 : 0;
@@ -274,15 +308,15 @@ __global__ void __launch_bounds__(RB_THREADS)
                 break;
             }
             uint8_t *st = smem + stage * stage_bytes;
-            if (lane < K) reinterpret_cast<float *>(st)[lane] = wv;
+            if (mine) reinterpret_cast<float *>(st)[my_k] = (valid && x_sf) ? __fmul_rn(w_cur, __ldg(x_sf + p_cur)) : w_cur;
             if (lane == 0) {
                 reinterpret_cast<unsigned *>(st)[RB_MAX_K] = mask;
                 mbar_arrive_expect_tx(full_bar(stage), static_cast<uint32_t>(__popc(mask) * row_bytes));
             }
             __syncwarp();
             if (valid)
-                bulk_g2s(smem_u32(st + RB_HEADER + lane * row_bytes),
-                         x + static_cast<int64_t>(p) * H + static_cast<int64_t>(ht) * HT,
+                bulk_g2s(smem_u32(st + RB_HEADER + my_k * row_bytes),
+                         x + static_cast<int64_t>(p_cur) * H + static_cast<int64_t>(ht) * HT,
                          static_cast<uint32_t>(row_bytes), full_bar(stage));
             ++issued;
             if (++stage == stages) {
@@ -323,6 +357,11 @@ __global__ void __launch_bounds__(RB_THREADS)
                         for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wk, f[i]));
                     }
                 }
+                if (sf) {
+                    const float sv = __ldg(sf + t);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = __fmul_rn(acc[i], sv);
+                }
                 store8<TOut>(out + t * H + static_cast<int64_t>(ht) * HT + v * 8, acc);
             }
             __syncwarp();
@@ -337,8 +376,8 @@ __global__ void __launch_bounds__(RB_THREADS)
 
 template <typename TIn, typename TOut>
 cudaError_t launch_reduce_bulk(const void *x, int64_t n_rows, const int32_t *pos, const float *w,
-                               int64_t T, int64_t K, int64_t H, void *out, int32_t *err,
-                               cudaStream_t stream) {
+                               const float *x_sf, const float *sf, int64_t T, int64_t K, int64_t H,
+                               void *out, int32_t *err, cudaStream_t stream) {
     // H tile: the largest of 1024 / 512 / 256 that divides H with a slot row <= 2 KB
     int HT = 256;
     for (int cand : {1024, 512}) {
@@ -347,8 +386,10 @@ cudaError_t launch_reduce_bulk(const void *x, int64_t n_rows, const int32_t *pos
             break;
         }
     }
+    // about 64 KB of ring per CTA, three CTAs per SM (measured best among
+    // 1-2 KB tiles, 2-6 stages and 2-8 CTAs per SM at 512 and 4096 tokens)
     const int stage_bytes = RB_HEADER + static_cast<int>(K) * HT * static_cast<int>(sizeof(TIn));
-    int stages = (64 * 1024) / stage_bytes;
+    int stages = (68 * 1024) / stage_bytes;
     stages = stages < 2 ? 2 : (stages > 6 ? 6 : stages);
     const size_t smem = static_cast<size_t>(stages) * stage_bytes + 16 * stages + 16;
     auto kern = reduce_bulk_kernel<TIn, TOut>;
@@ -363,26 +404,39 @@ cudaError_t launch_reduce_bulk(const void *x, int64_t n_rows, const int32_t *pos
     }
     const int per_sm = static_cast<int>((200 * 1024) / smem) < 1 ? 1 : static_cast<int>((200 * 1024) / smem);
     const int64_t n_items = T * (H / HT);
-    int64_t grid = static_cast<int64_t>(device_sm_count()) * (per_sm > 4 ? 4 : per_sm);
+    int64_t grid = static_cast<int64_t>(device_sm_count()) * (per_sm > 3 ? 3 : per_sm);
     if (grid > n_items) grid = n_items;
     kern<<<static_cast<unsigned>(grid), RB_THREADS, smem, stream>>>(
-        static_cast<const TIn *>(x), n_rows, pos, w, static_cast<int>(T), static_cast<int>(K),
-        static_cast<int>(H), HT, stages, static_cast<TOut *>(out), err);
+        static_cast<const TIn *>(x), n_rows, pos, w, x_sf, sf, static_cast<int>(T),
+        static_cast<int>(K), static_cast<int>(H), HT, stages, static_cast<TOut *>(out), err);
     return cudaGetLastError();
 }
 
 template <typename TIn, typename TOut>
 cudaError_t launch_reduce_typed(const void *x, int64_t n_rows, const int32_t *pos, const float *w,
-                                int64_t T, int64_t K, int64_t H, void *out, int32_t *err,
-                                cudaStream_t stream) {
+                                const float *x_sf, const float *sf, int64_t T, int64_t K,
+                                int64_t H, void *out, int32_t *err, cudaStream_t stream) {
     if (K <= RB_MAX_K)
-        return launch_reduce_bulk<TIn, TOut>(x, n_rows, pos, w, T, K, H, out, err, stream);
+        return launch_reduce_bulk<TIn, TOut>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream);
     const int64_t threads = T * (H / 8);
     const int64_t blocks = (threads + RD_THREADS - 1) / RD_THREADS;
     reduce_fused_kernel<TIn, TOut><<<static_cast<unsigned>(blocks), RD_THREADS, 0, stream>>>(
-        static_cast<const TIn *>(x), n_rows, pos, w, T, static_cast<int>(K), static_cast<int>(H),
-        static_cast<TOut *>(out), err);
+        static_cast<const TIn *>(x), n_rows, pos, w, x_sf, sf, T, static_cast<int>(K),
+        static_cast<int>(H), static_cast<TOut *>(out), err);
     return cudaGetLastError();
+}
+
+template <typename TIn>
+cudaError_t launch_reduce_in(const void *x, int64_t n_rows, const int32_t *pos, const float *w,
+                             const float *x_sf, const float *sf, int64_t T, int64_t K, int64_t H,
+                             int out_dtype, void *out, int32_t *err, cudaStream_t stream) {
+    switch (out_dtype) {
+        case kF16: return launch_reduce_typed<TIn, __half>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream);
+        case kBF16: return launch_reduce_typed<TIn, __nv_bfloat16>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream);
+        case kF32: return launch_reduce_typed<TIn, float>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream);
+        case kE4M3: return launch_reduce_typed<TIn, __nv_fp8_e4m3>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
@@ -398,20 +452,16 @@ cudaError_t launch_gather_rows(const void *x, const int32_t *sorted_token_idx, i
 }
 
 cudaError_t launch_reduce_fused(const void *x, int64_t n_rows, const int32_t *pos,
-                                const float *w, int64_t T, int64_t K, int64_t H, int in_dtype,
-                                int out_dtype, void *out, int32_t *err, cudaStream_t stream) {
+                                const float *w, const float *x_sf, const float *sf, int64_t T,
+                                int64_t K, int64_t H, int in_dtype, int out_dtype, void *out,
+                                int32_t *err, cudaStream_t stream) {
     if (T <= 0) return cudaSuccess;
-    if (in_dtype == kBF16 && out_dtype == kBF16)
-        return launch_reduce_typed<__nv_bfloat16, __nv_bfloat16>(x, n_rows, pos, w, T, K, H, out, err, stream);
-    if (in_dtype == kF16 && out_dtype == kF16)
-        return launch_reduce_typed<__half, __half>(x, n_rows, pos, w, T, K, H, out, err, stream);
-    if (in_dtype == kF32 && out_dtype == kF32)
-        return launch_reduce_typed<float, float>(x, n_rows, pos, w, T, K, H, out, err, stream);
-    if (in_dtype == kF32 && out_dtype == kBF16)
-        return launch_reduce_typed<float, __nv_bfloat16>(x, n_rows, pos, w, T, K, H, out, err, stream);
-    if (in_dtype == kF32 && out_dtype == kF16)
-        return launch_reduce_typed<float, __half>(x, n_rows, pos, w, T, K, H, out, err, stream);
-    return cudaErrorInvalidValue;
+    switch (in_dtype) {
+        case kF16: return launch_reduce_in<__half>(x, n_rows, pos, w, x_sf, sf, T, K, H, out_dtype, out, err, stream);
+        case kBF16: return launch_reduce_in<__nv_bfloat16>(x, n_rows, pos, w, x_sf, sf, T, K, H, out_dtype, out, err, stream);
+        case kF32: return launch_reduce_in<float>(x, n_rows, pos, w, x_sf, sf, T, K, H, out_dtype, out, err, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace moe

@@ -27,7 +27,8 @@ import torch
 
 BLOCK_M = 128
 
-_TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+_TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
+                 "e4m3": torch.float8_e4m3fn}
 
 
 def torch_dtype(name: str) -> torch.dtype:
@@ -140,8 +141,9 @@ def make_tokens(cfg: MoEConfig, T: int, device="cpu", seed: int = 0) -> torch.Te
 
 
 def make_reduce_inputs(T: int, K: int, H: int, dtype: str, seed: int, device="cpu",
-                       weighted: bool = True, pad_fraction: float = 0.1) -> dict:
-    """x [T*K, H]; token_topk_to_pos [T,K] int32 (-1 = padding); topk_weights [T,K] fp32 or None."""
+                       weighted: bool = True, pad_fraction: float = 0.1, scales: bool = False) -> dict:
+    """x [T*K, H]; token_topk_to_pos [T,K] int32 (-1 = padding); topk_weights [T,K] fp32 or None.
+    With ``scales``: x_sf [T*K] fp32 and sf [T] fp32, both log-uniform in [1/4, 4]."""
     gen = _gen(device, seed * 7 + T * 131 + K * 17 + H)
     n = T * K
     x = _normal((n, H), 1.0, dtype, gen, device)
@@ -154,7 +156,12 @@ def make_reduce_inputs(T: int, K: int, H: int, dtype: str, seed: int, device="cp
     if weighted:
         logits = torch.randn((T, K), generator=gen, device=device, dtype=torch.float32)
         w = torch.softmax(logits, dim=1)
-    return dict(x=x, pos=pos, w=w)
+    out = dict(x=x, pos=pos, w=w)
+    if scales:
+        u = torch.rand((n + T,), generator=gen, device=device, dtype=torch.float32)
+        s = torch.exp2(u * 4.0 - 2.0)
+        out.update(x_sf=s[:n].contiguous(), sf=s[n:].contiguous())
+    return out
 
 
 def to_numpy_bits(t: torch.Tensor):
@@ -162,6 +169,8 @@ def to_numpy_bits(t: torch.Tensor):
     t = t.detach().to("cpu").contiguous()
     if t.dtype in (torch.float16, torch.bfloat16):
         return t.view(torch.int16).numpy().view("uint16")
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).numpy()
     return t.numpy()
 
 

@@ -42,6 +42,7 @@
 #define OR_F16 0
 #define OR_BF16 1
 #define OR_F32 2
+#define OR_E4M3 3
 
 #define OR_OK 0
 #define OR_EINVAL 1
@@ -117,10 +118,42 @@ static void fill_half_table(void)
     for (uint32_t b = 0; b < 65536u; ++b) g_half_table[b] = half_to_float((uint16_t)b);
 }
 
+/* float8 e4m3fn: 1 sign, 4 exponent (bias 7), 3 fraction bits; no infinity;
+ * S.1111.111 is NaN; largest finite 448, smallest subnormal 2^-9. */
+static float e4m3_to_float(uint8_t b)
+{
+    uint32_t sign = (b >> 7) & 1u, exp = (b >> 3) & 0xfu, frac = b & 7u;
+    double mag;
+    if (exp == 0xf && frac == 7) return bits_f32((sign << 31) | 0x7fc00000u);
+    if (exp == 0) mag = ldexp((double)frac, -9);
+    else mag = ldexp((double)(8u | frac), (int)exp - 10);
+    return (float)(sign ? -mag : mag);
+}
+
+/* Round to e4m3fn, nearest-even, saturating finite values to +-448; NaN -> NaN. */
+static uint8_t float_to_e4m3_sat(float f)
+{
+    uint8_t sign = (uint8_t)((f32_bits(f) >> 24) & 0x80u);
+    if (isnan(f)) return (uint8_t)(sign | 0x7fu);
+    double a = fabs((double)f);
+    if (a >= 464.0) return (uint8_t)(sign | 0x7eu);     /* 448: rounds past the top */
+    if (a < ldexp(1.0, -6)) {                            /* subnormal: units of 2^-9 */
+        double r = nearbyint(a * ldexp(1.0, 9));
+        return (uint8_t)(sign | (uint8_t)r);            /* r == 8 is the min normal */
+    }
+    int e;
+    double m = frexp(a, &e);                             /* a = m * 2^e, m in [0.5, 1) */
+    double sgn = nearbyint(ldexp(m, 4));                 /* 4 significant bits: [8, 16] */
+    if (sgn >= 16.0) { sgn = 8.0; e += 1; }
+    int biased = e + 6;
+    return (uint8_t)(sign | (uint8_t)(biased << 3) | (uint8_t)((unsigned)sgn - 8u));
+}
+
 static float load_elem(const void *p, int64_t i, int dtype)
 {
     if (dtype == OR_F16) return g_half_table[((const uint16_t *)p)[i]];
     if (dtype == OR_BF16) return bf16_to_float(((const uint16_t *)p)[i]);
+    if (dtype == OR_E4M3) return e4m3_to_float(((const uint8_t *)p)[i]);
     return ((const float *)p)[i];
 }
 
@@ -128,10 +161,12 @@ static void store_elem(void *p, int64_t i, int dtype, float v)
 {
     if (dtype == OR_F16) ((uint16_t *)p)[i] = float_to_half(v);
     else if (dtype == OR_BF16) ((uint16_t *)p)[i] = float_to_bf16(v);
+    else if (dtype == OR_E4M3) ((uint8_t *)p)[i] = float_to_e4m3_sat(v);
     else ((float *)p)[i] = v;
 }
 
 static int dtype_ok(int d) { return d == OR_F16 || d == OR_BF16 || d == OR_F32; }
+static int out_dtype_ok(int d) { return dtype_ok(d) || d == OR_E4M3; }
 
 static void oracle_init(void) { pthread_once(&g_half_once, fill_half_table); }
 
@@ -610,6 +645,7 @@ int oracle_grouped_down(const void *h, const void *w_down, const int32_t *group_
  */
 typedef struct {
     const void *x; int64_t n_rows; const int32_t *pos; const float *w;
+    const float *x_sf, *sf;
     int64_t K, H; int in_dtype, out_dtype; void *out; int bad;
 } reduce_ctx;
 
@@ -626,14 +662,44 @@ static void reduce_rows(int64_t lo, int64_t hi, void *vctx)
                 continue;
             }
             float w = c->w ? c->w[t * c->K + k] : 1.0f;
+            if (c->x_sf) w = w * c->x_sf[p];          /* one multiply per routed slot */
             for (int64_t hh = 0; hh < c->H; ++hh) {
                 float prod = w * load_elem(c->x, p * c->H + hh, c->in_dtype);
                 acc[hh] = acc[hh] + prod;
             }
         }
-        for (int64_t hh = 0; hh < c->H; ++hh) store_elem(c->out, t * c->H + hh, c->out_dtype, acc[hh]);
+        float s = c->sf ? c->sf[t] : 1.0f;
+        for (int64_t hh = 0; hh < c->H; ++hh) {
+            float v = c->sf ? acc[hh] * s : acc[hh];  /* one multiply per output element */
+            store_elem(c->out, t * c->H + hh, c->out_dtype, v);
+        }
     }
     free(acc);
+}
+
+/*
+ * [PR55 section 1, variants]: the same combine with the compile-time switches
+ * of the page's four ops: x_sf (WithXsf), a scale per expanded row of x, is
+ * folded into the slot weight (w * x_sf[pos], one multiply per routed slot);
+ * sf (Quantized), read here as one scale per token, multiplies every output
+ * element of that token after the sum (one multiply per output element);
+ * the output may be float8 e4m3fn (Fp8 / Quantized), rounded to nearest even
+ * and saturated to +-448.
+ */
+int oracle_reduce_fused_scaled(const void *x, int64_t n_rows, const int32_t *token_topk_to_pos,
+                               const float *topk_weights, const float *x_sf, const float *sf,
+                               int64_t T, int64_t K, int64_t H, int in_dtype, int out_dtype,
+                               void *out, int32_t *err_flag, int nthreads)
+{
+    oracle_init();
+    if (!out || !token_topk_to_pos || T < 0 || K <= 0 || H <= 0 || n_rows < 0 ||
+        (!x && n_rows > 0) || !dtype_ok(in_dtype) || !out_dtype_ok(out_dtype))
+        return OR_EINVAL;
+    reduce_ctx c = {x, n_rows, token_topk_to_pos, topk_weights, x_sf, sf, K, H, in_dtype,
+                    out_dtype, out, 0};
+    parallel_for(T, nthreads, reduce_rows, &c);
+    if (err_flag) *err_flag = c.bad;
+    return OR_OK;
 }
 
 int oracle_reduce_fused(const void *x, int64_t n_rows, const int32_t *token_topk_to_pos,
@@ -641,14 +707,9 @@ int oracle_reduce_fused(const void *x, int64_t n_rows, const int32_t *token_topk
                         int in_dtype, int out_dtype, void *out, int32_t *err_flag,
                         int nthreads)
 {
-    oracle_init();
-    if (!out || !token_topk_to_pos || T < 0 || K <= 0 || H <= 0 || n_rows < 0 ||
-        (!x && n_rows > 0) || !dtype_ok(in_dtype) || !dtype_ok(out_dtype))
-        return OR_EINVAL;
-    reduce_ctx c = {x, n_rows, token_topk_to_pos, topk_weights, K, H, in_dtype, out_dtype, out, 0};
-    parallel_for(T, nthreads, reduce_rows, &c);
-    if (err_flag) *err_flag = c.bad;
-    return OR_OK;
+    if (!dtype_ok(out_dtype)) return OR_EINVAL;
+    return oracle_reduce_fused_scaled(x, n_rows, token_topk_to_pos, topk_weights, NULL, NULL, T,
+                                      K, H, in_dtype, out_dtype, out, err_flag, nthreads);
 }
 
 /* ------------------------------------------------------------------------- */

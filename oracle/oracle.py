@@ -22,7 +22,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.c")
 _LIB = os.path.join(_HERE, "libmoe_oracle.so")
 
-DTYPE_CODES = {"f16": 0, "bf16": 1, "f32": 2}
+DTYPE_CODES = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3}
 _lock = threading.Lock()
 _lib = None
 
@@ -61,6 +61,7 @@ def _load():
         "oracle_grouped_gate_up_silu": (I, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I64, I, P, I]),
         "oracle_grouped_down": (I, [P, P, P, P, P, P, I64, I64, P, I64, I64, I64, I64, I, P, I]),
         "oracle_reduce_fused": (I, [P, I64, P, P, I64, I64, I64, I, I, P, P, I]),
+        "oracle_reduce_fused_scaled": (I, [P, I64, P, P, P, P, I64, I64, I64, I, I, P, P, I]),
         "oracle_moe_tokens_dense": (I, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I64, I, P, I]),
         "oracle_rows_gate_up_silu": (I, [P, P, I64, P, P, I64, I64, I64, I, P, I]),
         "oracle_rows_down": (I, [P, P, I64, P, P, I64, I64, I64, I, P, I]),
@@ -81,6 +82,8 @@ def _bits(a: np.ndarray, dtype: str) -> np.ndarray:
     """Contiguous storage array for ``dtype`` (uint16 bits for f16/bf16)."""
     if dtype == "f32":
         return np.ascontiguousarray(a, dtype=np.float32)
+    if dtype == "e4m3":
+        return np.ascontiguousarray(a).view(np.uint8)
     if a.dtype == np.float16:
         if dtype != "f16":
             raise ValueError("np.float16 array passed as bf16")
@@ -91,6 +94,8 @@ def _bits(a: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def _empty(shape, dtype: str) -> np.ndarray:
+    if dtype == "e4m3":
+        return np.empty(shape, dtype=np.uint8)
     return np.empty(shape, dtype=np.float32 if dtype == "f32" else np.uint16)
 
 
@@ -249,6 +254,25 @@ def reduce_fused(x, token_topk_to_pos, topk_weights, in_dtype: str, out_dtype: s
     _check(_load().oracle_reduce_fused(_ptr(xb), n_rows, _ptr(pos), _ptr(w), T, K, H,
                                        DTYPE_CODES[in_dtype], DTYPE_CODES[out_dtype], _ptr(out),
                                        _ptr(err), nthreads), "reduce_fused")
+    return out, int(err[0])
+
+
+def reduce_fused_scaled(x, token_topk_to_pos, topk_weights, x_sf, sf, in_dtype: str,
+                        out_dtype: str, nthreads: int = 0):
+    """The combine with the optional per-row x_sf and per-token sf scales and
+    e4m3 output.  Returns (out, err_flag)."""
+    pos = np.ascontiguousarray(token_topk_to_pos, dtype=np.int32)
+    T, K = pos.shape
+    xb = _bits(x, in_dtype)
+    n_rows, H = xb.shape
+    f32 = lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.float32)
+    w, xs, s = f32(topk_weights), f32(x_sf), f32(sf)
+    out = _empty((T, H), out_dtype)
+    err = np.zeros(1, np.int32)
+    _check(_load().oracle_reduce_fused_scaled(_ptr(xb), n_rows, _ptr(pos), _ptr(w), _ptr(xs),
+                                              _ptr(s), T, K, H, DTYPE_CODES[in_dtype],
+                                              DTYPE_CODES[out_dtype], _ptr(out), _ptr(err),
+                                              nthreads), "reduce_fused_scaled")
     return out, int(err[0])
 
 

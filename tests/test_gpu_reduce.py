@@ -135,3 +135,38 @@ def test_reduce_empty_batch():
     pos = torch.zeros((0, 8), dtype=torch.int32, device=dev)
     out = binding.moe_reduce_fused(x, pos, None)
     assert out.shape == (0, 256)
+
+
+def _variant_cases():
+    cases = []
+    for (T, K, H) in [(4, 2, 256), (32, 8, 3072), (512, 8, 7168)]:
+        for in_dt in ("f16", "bf16", "f32"):
+            if H == 7168 and in_dt != "bf16":
+                continue
+            for out_dt in (in_dt, "e4m3"):
+                for xs in (False, True):
+                    for sf in (False, True):
+                        cases.append((T, K, H, in_dt, out_dt, xs, sf))
+    return cases
+
+
+@pytest.mark.parametrize("T,K,H,in_dt,out_dt,use_xsf,use_sf", _variant_cases(),
+                         ids=lambda v: str(v))
+def test_reduce_scaled_variants_bit_exact(oracle, T, K, H, in_dt, out_dt, use_xsf, use_sf):
+    """The WithXsf / Fp8 / Quantized switches (TileOPs-Metax PR #55): per-row
+    x_sf, per-token sf, e4m3 output; bit for bit against the oracle (the
+    e4m3 rounding included), and within the page's fp8 tolerance 0.1."""
+    dev = require_cuda()
+    d = workloads.make_reduce_inputs(T, K, H, in_dt, 6, device=dev, scales=True)
+    xs = d["x_sf"] if use_xsf else None
+    sf = d["sf"] if use_sf else None
+    out = binding.moe_reduce_fused_scaled(d["x"], d["pos"], d["w"], x_sf=xs, sf=sf,
+                                          out_dtype=workloads.torch_dtype(out_dt))
+    torch.cuda.synchronize()
+    want, err = oracle.reduce_fused_scaled(bits(d["x"]), d["pos"].cpu().numpy(), d["w"].cpu().numpy(),
+                                           None if xs is None else xs.cpu().numpy(),
+                                           None if sf is None else sf.cpu().numpy(), in_dt, out_dt)
+    assert err == 0
+    assert_bits_equal(bits(out), want, "scaled combine")
+    if out_dt == "e4m3":
+        assert_close(bits(out), want, "e4m3", 0.1, 0.1, "fp8 combine")

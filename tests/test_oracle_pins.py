@@ -487,3 +487,72 @@ def test_dense_brute_force_equals_table_path(oracle, dtype):
                                     res["topk_idx"], res["topk_w"], tokens, dtype)
     assert np.array_equal(dense, res["out"])
     assert res["err"] == 0
+
+
+# --------------------------------------------------------------------------- #
+# combine variants: x_sf / sf scales and float8 e4m3fn output
+# --------------------------------------------------------------------------- #
+
+def test_decode_all_e4m3_patterns(oracle):
+    bits = np.arange(256, dtype=np.uint8)
+    got = oracle.decode(bits, "e4m3")
+    ref = torch.from_numpy(bits).view(torch.float8_e4m3fn).float().numpy()
+    nan = np.isnan(ref)
+    assert nan.sum() == 2  # S.1111.111
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_encode_e4m3_matches_torch_in_range_and_saturates(oracle):
+    rng = np.random.default_rng(20)
+    v = np.concatenate([rng.standard_normal(20000) * s for s in (1e-3, 0.1, 1, 30, 200)]).astype(np.float32)
+    grid = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    grid = np.sort(grid[np.isfinite(grid)])
+    mids = ((grid[1:].astype(np.float64) + grid[:-1]) / 2).astype(np.float32)  # exact ties
+    v = np.concatenate([v, grid, mids, np.nextafter(mids, np.float32(1e9)), np.nextafter(mids, np.float32(-1e9))])
+    v = v[np.abs(v) < 464]
+    got = oracle.encode(v, "e4m3")
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref)
+    # past the largest finite value the saturating reading gives +-448 (0x7e / 0xfe)
+    big = np.array([464.0, 500.0, 1e30, -464.0, -1e30], np.float32)
+    assert list(oracle.encode(big, "e4m3")) == [0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
+    assert oracle.encode(np.array([np.nan], np.float32), "e4m3")[0] & 0x7F == 0x7F
+
+
+def test_scaled_combine_reduces_to_plain_and_closed_forms(oracle):
+    d = workloads.make_reduce_inputs(24, 8, 512, "bf16", seed=21)
+    x = workloads.to_numpy_bits(d["x"])
+    pos, w = d["pos"].numpy(), d["w"].numpy()
+    base, _ = oracle.reduce_fused(x, pos, w, "bf16", "bf16")
+    ones_r, ones_t = np.ones(x.shape[0], np.float32), np.ones(24, np.float32)
+    for xs, sf in ((None, None), (ones_r, None), (None, ones_t), (ones_r, ones_t)):
+        got, _ = oracle.reduce_fused_scaled(x, pos, w, xs, sf, "bf16", "bf16")
+        assert np.array_equal(got, base)
+    # integer rows, power-of-two weights and scales: every product and sum exact
+    rng = np.random.default_rng(22)
+    T, K, H = 12, 4, 256
+    xi = rng.integers(-6, 7, (T * K, H)).astype(np.float32)
+    pos = rng.permutation(T * K).astype(np.int32).reshape(T, K)
+    pos[0, 1] = -1
+    wi = rng.choice([0.5, 1.0, 2.0], (T, K)).astype(np.float32)
+    xs = rng.choice([0.25, 1.0, 4.0], T * K).astype(np.float32)
+    sf = rng.choice([0.5, 2.0], T).astype(np.float32)
+    got, _ = oracle.reduce_fused_scaled(xi, pos, wi, xs, sf, "f32", "f32")
+    ref = np.zeros((T, H))
+    for t in range(T):
+        for k in range(K):
+            if pos[t, k] >= 0:
+                ref[t] += wi[t, k] * xs[pos[t, k]] * xi[pos[t, k]]
+        ref[t] *= sf[t]
+    assert np.array_equal(got, ref.astype(np.float32))
+
+
+def test_e4m3_output_is_the_rounded_fp32_result(oracle):
+    """With fp32 in, the e4m3 output equals rounding the fp32 output once."""
+    d = workloads.make_reduce_inputs(16, 8, 256, "f32", seed=23)
+    x, pos, w = d["x"].numpy(), d["pos"].numpy(), d["w"].numpy()
+    sf = np.full(16, 8.0, np.float32)
+    f32, _ = oracle.reduce_fused_scaled(x, pos, w, None, sf, "f32", "f32")
+    f8, _ = oracle.reduce_fused_scaled(x, pos, w, None, sf, "f32", "e4m3")
+    assert np.array_equal(f8, oracle.encode(f32, "e4m3"))
