@@ -273,6 +273,7 @@ moe_status_t moe_forward(const void *x, const void *w_g, const float *bias, cons
     if (T == 0) return MOE_OK;
     if (!x || !w_g || !w_gate || !w_up || !w_down || !out || !ws) return MOE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_g)) return MOE_ERR_INVALID_ARG;
     FwdLayout L;
     if (!fwd_layout(T, d_h, d_e, E, k, dtype, &L)) return MOE_ERR_INVALID_ARG;
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;

@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(DS_THREADS)
                          int32_t *__restrict__ hist) {
     extern __shared__ int32_t counts[];
     for (int e = threadIdx.x; e < E; e += DS_THREADS) counts[e] = 0;
+    griddep_wait();
+    griddep_launch_dependents();
     __syncthreads();
     const int64_t f0 = static_cast<int64_t>(blockIdx.x) * CHUNK;
     for (int i = threadIdx.x; i < CHUNK; i += DS_THREADS) {
@@ -87,6 +89,8 @@ __global__ void __launch_bounds__(SCAN_THREADS)
     __shared__ int po_s[SCAN_THREADS];
     const int e = threadIdx.x;
     int count = 0;
+    griddep_wait();
+    griddep_launch_dependents();
     if (e < E) {
         for (int c = 0; c < n_chunks; ++c) {
             int32_t *h = hist + static_cast<int64_t>(c) * E + e;
@@ -128,6 +132,8 @@ __global__ void __launch_bounds__(DS_THREADS)
     extern __shared__ int32_t wcount[];  // [DS_WARPS][E]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < DS_WARPS * E; i += DS_THREADS) wcount[i] = 0;
+    griddep_wait();
+    griddep_launch_dependents();
     __syncthreads();
     const int64_t wf0 = static_cast<int64_t>(blockIdx.x) * CHUNK + static_cast<int64_t>(warp) * PAIRS_PER_WARP;
     int32_t *mine = wcount + warp * E;
@@ -172,12 +178,11 @@ __global__ void __launch_bounds__(DS_THREADS)
 // and SMALL_MAX_E experts): the pairs stay in registers (warp w owns a
 // contiguous run of 32*R pairs), per-warp counts in shared memory, one block
 // scan, the block lookup, then the stable scatter from the same registers.
-constexpr int SMALL_THREADS = 1024;
-constexpr int SMALL_WARPS = SMALL_THREADS / 32;
 constexpr int SMALL_MAX_ROUNDS = 16;
-constexpr int SMALL_MAX_PAIRS = SMALL_WARPS * 32 * SMALL_MAX_ROUNDS;  // 16384
+constexpr int SMALL_MAX_PAIRS = 1024 * SMALL_MAX_ROUNDS;  // 16384
 constexpr int SMALL_MAX_E = 256;
 
+template <int SMALL_THREADS>
 __global__ void __launch_bounds__(SMALL_THREADS)
     dispatch_small_kernel(const int32_t *__restrict__ idx, const float *__restrict__ w,
                           int n_pairs, int k, int E, int block_m, int32_t *__restrict__ sizes,
@@ -185,6 +190,8 @@ __global__ void __launch_bounds__(SMALL_THREADS)
                           int32_t *__restrict__ gidx, int m_blocks,
                           int32_t *__restrict__ sorted_tok, float *__restrict__ sorted_w,
                           int32_t *__restrict__ pos) {
+    constexpr int SMALL_WARPS = SMALL_THREADS / 32;
+    static_assert(SMALL_THREADS >= SMALL_MAX_E, "one thread per expert");
     __shared__ int32_t wcount[SMALL_WARPS * SMALL_MAX_E];
     __shared__ int po_s[SMALL_MAX_E];
     __shared__ int warp_sums[32];
@@ -192,6 +199,8 @@ __global__ void __launch_bounds__(SMALL_THREADS)
     const int rounds = (n_pairs + SMALL_THREADS - 1) / SMALL_THREADS;  // <= SMALL_MAX_ROUNDS
     const int wf0 = warp * rounds * 32;
     for (int i = threadIdx.x; i < SMALL_WARPS * E; i += SMALL_THREADS) wcount[i] = 0;
+    griddep_wait();
+    griddep_launch_dependents();
     int ev[SMALL_MAX_ROUNDS];
 #pragma unroll
     for (int r = 0; r < SMALL_MAX_ROUNDS; ++r) {
@@ -276,24 +285,27 @@ cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_
                             cudaStream_t stream) {
     const int64_t n_pairs = T * k;
     if (n_pairs <= SMALL_MAX_PAIRS && E <= SMALL_MAX_E) {
-        dispatch_small_kernel<<<1, SMALL_THREADS, 0, stream>>>(
-            topk_idx, topk_w, static_cast<int>(n_pairs), static_cast<int>(k), static_cast<int>(E),
-            static_cast<int>(block_m), sizes, offsets, padded, gidx, static_cast<int>(m_blocks),
-            sorted_token_idx, sorted_row_weight, pos);
-        return cudaGetLastError();
+        // fewer threads (shorter per-expert walks and scans) for few pairs
+        auto kern = n_pairs <= 256 * SMALL_MAX_ROUNDS ? dispatch_small_kernel<256>
+                                                      : dispatch_small_kernel<1024>;
+        const int threads = n_pairs <= 256 * SMALL_MAX_ROUNDS ? 256 : 1024;
+        return launch_pdl(kern, dim3(1), dim3(threads), 0, stream, topk_idx, topk_w,
+                          static_cast<int>(n_pairs), static_cast<int>(k), static_cast<int>(E),
+                          static_cast<int>(block_m), sizes, offsets, padded, gidx,
+                          static_cast<int>(m_blocks), sorted_token_idx, sorted_row_weight, pos);
     }
     const int64_t n_chunks = n_pairs > 0 ? (n_pairs + CHUNK - 1) / CHUNK : 0;
     int32_t *hist = static_cast<int32_t *>(scratch);
     if (n_chunks > 0) {
-        dispatch_hist_kernel<<<static_cast<unsigned>(n_chunks), DS_THREADS, E * 4, stream>>>(
-            topk_idx, n_pairs, static_cast<int>(E), hist);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(dispatch_hist_kernel, dim3(static_cast<unsigned>(n_chunks)),
+                                   dim3(DS_THREADS), static_cast<size_t>(E * 4), stream, topk_idx,
+                                   n_pairs, static_cast<int>(E), hist);
         if (e != cudaSuccess) return e;
     }
-    dispatch_scan_kernel<<<1, SCAN_THREADS, 0, stream>>>(
-        hist, static_cast<int>(n_chunks), static_cast<int>(E), static_cast<int>(block_m), sizes, offsets, padded,
-        gidx, static_cast<int>(m_blocks));
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(SCAN_THREADS), 0, stream, hist,
+                               static_cast<int>(n_chunks), static_cast<int>(E),
+                               static_cast<int>(block_m), sizes, offsets, padded, gidx,
+                               static_cast<int>(m_blocks));
     if (e != cudaSuccess || n_chunks == 0) return e;
     const size_t smem = static_cast<size_t>(DS_WARPS) * E * 4;
     static size_t attr_bytes[64] = {0};
@@ -305,10 +317,10 @@ cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_bytes[dev] = smem;
     }
-    dispatch_scatter_kernel<<<static_cast<unsigned>(n_chunks), DS_THREADS, smem, stream>>>(
-        topk_idx, topk_w, n_pairs, static_cast<int>(k), static_cast<int>(E), hist,
-        sorted_token_idx, sorted_row_weight, pos);
-    return cudaGetLastError();
+    return launch_pdl(dispatch_scatter_kernel, dim3(static_cast<unsigned>(n_chunks)), dim3(DS_THREADS),
+                      smem, stream, topk_idx, topk_w, n_pairs, static_cast<int>(k),
+                      static_cast<int>(E), static_cast<const int32_t *>(hist), sorted_token_idx,
+                      sorted_row_weight, pos);
 }
 
 }  // namespace moe

@@ -15,8 +15,9 @@
 // of x and W_g stream through a 4-stage cp.async ring.
 //
 // Three shapes of the same kernel:
-//   * E <= 64: one CTA holds 4 tokens x all experts and also selects the
-//     top-k from its logits in shared memory (one launch for the gate);
+//   * E <= 64: one CTA holds 1 token (small batches) or 4 tokens x all
+//     experts and also selects the top-k from its logits in shared memory
+//     (one launch for the gate);
 //   * many tokens: CTA = 16 tokens x 32 experts (16 warps of 4 x 8 pairs), then
 //     topk_softmax_kernel;
 //   * few tokens: CTA = one warp of 4 tokens x 8 experts (more CTAs in
@@ -127,6 +128,9 @@ __global__ void __launch_bounds__(WT *WE * 32)
     for (int i = 0; i < TPW; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+    griddep_wait();  // x (and W_g) may come from the previous kernel
+    griddep_launch_dependents();
 
 #pragma unroll
     for (int s = 0; s < GATE_STAGES - 1; ++s) {
@@ -243,6 +247,8 @@ __global__ void __launch_bounds__(TK_WARPS * 32)
                         int32_t *__restrict__ topk_idx, float *__restrict__ topk_w) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * TK_WARPS + warp;
+    griddep_wait();
+    griddep_launch_dependents();
     if (t >= T) return;
     const float *row = logits + static_cast<int64_t>(t) * E;
     float v[SLOTS];
@@ -272,10 +278,9 @@ cudaError_t launch_gate_shape(const void *x, const void *wg, const float *bias, 
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
     dim3 grid(static_cast<unsigned>((T + TOK - 1) / TOK), static_cast<unsigned>((E + EXP - 1) / EXP));
-    kern<<<grid, WT * WE * 32, smem, stream>>>(static_cast<const uint16_t *>(x),
-                                               static_cast<const uint16_t *>(wg), bias, (int)T,
-                                               (int)d_h, (int)E, (int)k, logits, idx, w);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(WT * WE * 32), smem, stream, static_cast<const uint16_t *>(x),
+                      static_cast<const uint16_t *>(wg), bias, (int)T, (int)d_h, (int)E, (int)k,
+                      logits, idx, w);
 }
 
 cudaError_t launch_topk(const float *logits, int64_t T, int64_t E, int64_t k, int32_t *topk_idx,
@@ -283,11 +288,9 @@ cudaError_t launch_topk(const float *logits, int64_t T, int64_t E, int64_t k, in
     const unsigned grid = static_cast<unsigned>((T + TK_WARPS - 1) / TK_WARPS);
     const int slots = static_cast<int>((E + 31) / 32);
 #define MOE_TOPK_CASE(S)                                                                        \
-    if (slots <= S) {                                                                           \
-        topk_softmax_kernel<S><<<grid, TK_WARPS * 32, 0, stream>>>(logits, (int)T, (int)E, (int)k, \
-                                                                    topk_idx, topk_w);          \
-        return cudaGetLastError();                                                              \
-    }
+    if (slots <= S)                                                                             \
+        return launch_pdl(topk_softmax_kernel<S>, dim3(grid), dim3(TK_WARPS * 32), 0, stream,    \
+                          logits, (int)T, (int)E, (int)k, topk_idx, topk_w);
     MOE_TOPK_CASE(2)
     MOE_TOPK_CASE(4)
     MOE_TOPK_CASE(8)
@@ -301,9 +304,14 @@ template <int DT>
 cudaError_t launch_gate_typed(const void *x, const void *wg, const float *bias, int64_t T,
                               int64_t d_h, int64_t E, int64_t k, float *logits, int32_t *idx,
                               float *w, cudaStream_t stream) {
-    // E <= 64: 4 tokens x 64 experts per CTA (8 warps of 4 x 8 pairs), top-k fused
-    if (E <= 64)
+    // E <= 64: one CTA holds all experts of its tokens (8 warps x 8 experts)
+    // and selects their top-k; one token per CTA while that still fills the
+    // GPU with few CTAs, else 4 tokens per CTA
+    if (E <= 64) {
+        if (T <= 4 * device_sm_count())
+            return launch_gate_shape<DT, 1, 1, 8, true>(x, wg, bias, T, d_h, E, k, logits, idx, w, stream);
         return launch_gate_shape<DT, 4, 1, 8, true>(x, wg, bias, T, d_h, E, k, logits, idx, w, stream);
+    }
     cudaError_t e;
     if (T >= 512)  // 16 tokens x 32 experts per CTA: 16 warps of 4 x 8 pairs
         e = launch_gate_shape<DT, 4, 4, 4, false>(x, wg, bias, T, d_h, E, k, logits, idx, w, stream);

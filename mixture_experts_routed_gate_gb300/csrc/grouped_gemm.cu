@@ -188,6 +188,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish();
     }
+    // everything above is independent of the previous kernel; the tables and
+    // rows below are not
+    griddep_wait();
+    griddep_launch_dependents();
     // ----- schedule: classify the M blocks, list full and partial ones -----
     Schedule sc{nullptr, 0, p.m_blocks};
     if (p.m_blocks <= MAX_SCHED) {
@@ -450,8 +454,7 @@ cudaError_t launch_typed(const CUtensorMap &ta, const CUtensorMap &tb0, const CU
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
-    kern<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb0, tb1, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, ta, tb0, tb1, p);
 }
 
 }  // namespace

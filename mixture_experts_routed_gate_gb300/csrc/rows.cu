@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(GA_WARPS * 32)
                        int64_t n_rows, int nvec, uint4 *__restrict__ out) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t r = static_cast<int64_t>(blockIdx.x) * GA_WARPS + warp;
+    griddep_wait();
+    griddep_launch_dependents();
     if (r >= n_rows) return;
     const uint4 *src = x + static_cast<int64_t>(__ldg(idx + r)) * nvec;
     uint4 *dst = out + r * nvec;
@@ -137,6 +139,8 @@ __global__ void __launch_bounds__(RD_THREADS)
     const int vpr = H >> 3;  // 8-element vectors per row
     const int64_t gid = static_cast<int64_t>(blockIdx.x) * RD_THREADS + threadIdx.x;
     const int64_t t = gid / vpr;
+    griddep_wait();
+    griddep_launch_dependents();
     if (t >= T) return;
     const int h0 = static_cast<int>(gid - t * vpr) * 8;
     const int32_t *prow = pos + t * K;
@@ -254,6 +258,8 @@ __global__ void __launch_bounds__(RB_THREADS)
         fence_mbar_init();
     }
     __syncthreads();
+    griddep_wait();  // x, positions and weights may come from the previous kernel
+    griddep_launch_dependents();
 
     // Items are dealt round-robin (neighbouring CTAs read neighbouring H tiles
     // of the same rows, which keeps DRAM pages open).  The producer holds the
@@ -406,10 +412,10 @@ cudaError_t launch_reduce_bulk(const void *x, int64_t n_rows, const int32_t *pos
     const int64_t n_items = T * (H / HT);
     int64_t grid = static_cast<int64_t>(device_sm_count()) * (per_sm > 3 ? 3 : per_sm);
     if (grid > n_items) grid = n_items;
-    kern<<<static_cast<unsigned>(grid), RB_THREADS, smem, stream>>>(
-        static_cast<const TIn *>(x), n_rows, pos, w, x_sf, sf, static_cast<int>(T),
-        static_cast<int>(K), static_cast<int>(H), HT, stages, static_cast<TOut *>(out), err);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(RB_THREADS), smem, stream,
+                      static_cast<const TIn *>(x), n_rows, pos, w, x_sf, sf, static_cast<int>(T),
+                      static_cast<int>(K), static_cast<int>(H), HT, stages,
+                      static_cast<TOut *>(out), err);
 }
 
 template <typename TIn, typename TOut>
@@ -420,10 +426,10 @@ cudaError_t launch_reduce_typed(const void *x, int64_t n_rows, const int32_t *po
         return launch_reduce_bulk<TIn, TOut>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream);
     const int64_t threads = T * (H / 8);
     const int64_t blocks = (threads + RD_THREADS - 1) / RD_THREADS;
-    reduce_fused_kernel<TIn, TOut><<<static_cast<unsigned>(blocks), RD_THREADS, 0, stream>>>(
-        static_cast<const TIn *>(x), n_rows, pos, w, x_sf, sf, T, static_cast<int>(K),
-        static_cast<int>(H), static_cast<TOut *>(out), err);
-    return cudaGetLastError();
+    return launch_pdl(reduce_fused_kernel<TIn, TOut>, dim3(static_cast<unsigned>(blocks)),
+                      dim3(RD_THREADS), 0, stream, static_cast<const TIn *>(x), n_rows, pos, w,
+                      x_sf, sf, T, static_cast<int>(K), static_cast<int>(H),
+                      static_cast<TOut *>(out), err);
 }
 
 template <typename TIn>
@@ -446,9 +452,9 @@ cudaError_t launch_gather_rows(const void *x, const int32_t *sorted_token_idx, i
     if (n_rows <= 0) return cudaSuccess;
     const int nvec = static_cast<int>(d_h * elem_bytes / 16);
     const int64_t blocks = (n_rows + GA_WARPS - 1) / GA_WARPS;
-    gather_rows_kernel<<<static_cast<unsigned>(blocks), GA_WARPS * 32, 0, stream>>>(
-        static_cast<const uint4 *>(x), sorted_token_idx, n_rows, nvec, static_cast<uint4 *>(a_out));
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(GA_WARPS * 32), 0,
+                      stream, static_cast<const uint4 *>(x), sorted_token_idx, n_rows, nvec,
+                      static_cast<uint4 *>(a_out));
 }
 
 cudaError_t launch_reduce_fused(const void *x, int64_t n_rows, const int32_t *pos,
