@@ -118,6 +118,23 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(total_ms: float, world: int, device=None) -> float:
+    """The slowest rank's timed-region length (every rank calls this)."""
+    if world <= 1:
+        return total_ms
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: int, world: int, total_ms: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time (weak scaling: each rank runs its own replica)."""
+    return units_per_rank * world / (total_ms / 1e3)
+
+
 # ----------------------------------------------------------------------------- native arm
 
 class NativeStep:
@@ -313,11 +330,7 @@ def run_native(args, cfg, rank, world, dev):
         clocks = sampler.stop()
         if world > 1:
             torch.distributed.barrier()
-    total_ms = float(step_ms.sum())
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(step_ms.sum()), world, dev)
     if int(step.err.item()) != 0:
         raise RuntimeError(f"device error flag {int(step.err.item())} in the timed region")
 
@@ -358,10 +371,7 @@ def measure_e2e(args, cfg, d, dev, flush, world):
             ends[i].record(stream)
             ends[i].synchronize()
             total_ms += starts[i].elapsed_time(ends[i])
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     if int(fg.err.item()) != 0:
         raise RuntimeError(f"device error flag {int(fg.err.item())} in the e2e region")
     es = fg.x.element_size()
@@ -609,8 +619,7 @@ def main():
     Tk = T * k
     per_stage = res["per_stage"]
     ms_step = res["total_ms"] / args.steps
-    tokens_total = T * args.steps * world
-    value = tokens_total / (res["total_ms"] / 1e3)
+    value = aggregate_throughput(T * args.steps, world, res["total_ms"])
     e_act = float(np.mean(res["act_experts"]))
     es = 2
     flops_step = roofline.moe_forward_flops(T, k, d_h, d_e, E)
@@ -648,7 +657,7 @@ def main():
         "reduce_fused_bf16_x8_7168": res["aux"],
         "cpu_baseline": {"value": round(cpu["value"], 2), "unit": "tokens/s", "cores": threads,
                          "kind": "oracle", "sample": cpu["sample"]},
-        "e2e": {"value": round(T * args.steps * world / (e2e["total_ms"] / 1e3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(aggregate_throughput(T * args.steps, world, e2e["total_ms"]), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": kernels_per_step(cfg) * args.steps,
         "launch_mode": res["mode"],
