@@ -12,7 +12,8 @@
 // natural warp-split-K dot product: a warp owns a (4 or 8)-token x 8-expert tile,
 // each lane keeps one partial per (token, expert) pair and reads its 16-byte
 // chunk of every row from shared memory (conflict free); 256-element slices
-// of x and W_g stream through a 4-stage cp.async ring.
+// of x and W_g arrive by TMA (one box of token rows and one of expert rows per
+// slice) in a 4-stage ring.
 //
 // Three shapes of the same kernel:
 //   * E <= 64: one CTA holds 1 token (small batches) or 4 tokens x all
@@ -31,17 +32,6 @@ namespace {
 constexpr int SLICE = 256;                // elements per lane round: 32 lanes x 8
 constexpr int ROW_BYTES = SLICE * 2;      // 512 B of one row per slice
 constexpr int GATE_STAGES = 4;
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool pred) {
-    const int n = pred ? 16 : 0;  // zero-fill rows past the end
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 // Warp argmax by (logit desc, id asc) over k rounds, then the softmax weights.
 // Lane holds v[s] = logit of expert s*32 + lane (or -inf past E).
@@ -96,32 +86,39 @@ __device__ __forceinline__ void warp_topk_softmax(float (&v)[SLOTS], int E, int 
 
 template <int DT, int TPW, int WT, int WE, bool FUSE_TOPK>
 __global__ void __launch_bounds__(WT *WE * 32)
-    gate_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ wg,
+    gate_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                 const float *__restrict__ bias, int T, int d_h, int E, int k,
                 float *__restrict__ logits, int32_t *__restrict__ topk_idx,
                 float *__restrict__ topk_w) {
     constexpr int TOK = WT * TPW, EXP = WE * 8, ROWS = TOK + EXP;
-    constexpr int THREADS = WT * WE * 32;
     constexpr int STAGE_BYTES = ROWS * ROW_BYTES;
-    extern __shared__ __align__(16) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * TOK, e0 = blockIdx.y * EXP;
     const int wt = (warp / WE) * TPW;  // warp's first token in the tile
     const int we = (warp % WE) * 8;  // warp's first expert in the tile
     const int n_slices = d_h / SLICE;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + GATE_STAGES * STAGE_BYTES);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(full + GATE_STAGES);
 
+    // one slice = a 256-column box of the CTA's token rows and expert rows,
+    // two TMA copies landing on the stage's mbarrier (rows past T / E read 0)
     auto load_slice = [&](int s) {
-        uint8_t *stage = smem + (s % GATE_STAGES) * STAGE_BYTES;
-        for (int c = threadIdx.x; c < ROWS * 32; c += THREADS) {
-            const int r = c >> 5, ch = c & 31;
-            const bool is_tok = r < TOK;
-            const int gr = is_tok ? t0 + r : e0 + (r - TOK);
-            const bool ok = is_tok ? gr < T : gr < E;
-            const uint16_t *src = (is_tok ? x : wg) + static_cast<int64_t>(ok ? gr : 0) * d_h +
-                                  s * SLICE + ch * 8;
-            cp_async16(smem_u32(stage + r * ROW_BYTES + ch * 16), src, ok);
-        }
+        const int st = s % GATE_STAGES;
+        uint8_t *stage = smem + st * STAGE_BYTES;
+        const uint32_t bar = smem_u32(full + st);
+        mbar_arrive_expect_tx(bar, STAGE_BYTES);
+        tma_load_2d(smem_u32(stage), &tm_x, bar, s * SLICE, t0);
+        tma_load_2d(smem_u32(stage + TOK * ROW_BYTES), &tm_w, bar, s * SLICE, e0);
     };
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < GATE_STAGES; ++i) mbar_init(smem_u32(full + i), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_w);
+    }
+    __syncthreads();
 
     float acc[TPW][8];
 #pragma unroll
@@ -132,14 +129,14 @@ __global__ void __launch_bounds__(WT *WE * 32)
     griddep_wait();  // x (and W_g) may come from the previous kernel
     griddep_launch_dependents();
 
-#pragma unroll
-    for (int s = 0; s < GATE_STAGES - 1; ++s) {
-        if (s < n_slices) load_slice(s);
-        cp_async_commit();
-    }
+    if (threadIdx.x == 0)
+        for (int s = 0; s < GATE_STAGES && s < n_slices; ++s) load_slice(s);
+    int done = 0;  // slices consumed
     for (int s = 0; s < n_slices; ++s) {
-        cp_async_wait<GATE_STAGES - 2>();
-        __syncthreads();
+        // every thread waits for the stage (bounded; a lost copy ends the loop)
+        if (!mbar_wait_bounded(smem_u32(full + s % GATE_STAGES),
+                               static_cast<uint32_t>((s / GATE_STAGES) & 1), abort_flag, nullptr))
+            break;
         const uint8_t *stage = smem + (s % GATE_STAGES) * STAGE_BYTES;
         // lane owns chunk `lane` of the slice: elements 8*lane .. 8*lane+7, ascending
         uint4 xv[TPW], wv[8];
@@ -173,11 +170,18 @@ __global__ void __launch_bounds__(WT *WE * 32)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xf[i].y, wf[j].y, acc[i][j]);
         }
-        // refill the stage consumed one iteration ago (every thread is past it)
-        if (s + GATE_STAGES - 1 < n_slices) load_slice(s + GATE_STAGES - 1);
-        cp_async_commit();
+        __syncthreads();  // every warp is done with this stage: refill it
+        if (threadIdx.x == 0 && s + GATE_STAGES < n_slices && !*abort_flag) load_slice(s + GATE_STAGES);
+        done = s + 1;
     }
-    cp_async_wait<0>();
+    if (threadIdx.x == 0) {
+        // after a timeout, let the copies still in flight land before exit
+        for (int s = done; s < n_slices && s < done + GATE_STAGES; ++s) {
+            const unsigned long long t_start = global_timer_ns();
+            while (!mbar_try_wait(smem_u32(full + s % GATE_STAGES), static_cast<uint32_t>((s / GATE_STAGES) & 1)))
+                if (global_timer_ns() - t_start > kWaitTimeoutNs) break;
+        }
+    }
 
     // xor butterfly s = 16, 8, 4, 2, 1; every lane ends with the full sum
 #pragma unroll
@@ -266,7 +270,11 @@ cudaError_t launch_gate_shape(const void *x, const void *wg, const float *bias, 
                               int64_t d_h, int64_t E, int64_t k, float *logits, int32_t *idx,
                               float *w, cudaStream_t stream) {
     constexpr int TOK = WT * TPW, EXP = WE * 8;
-    const size_t smem = static_cast<size_t>(GATE_STAGES) * (TOK + EXP) * ROW_BYTES;
+    const size_t smem = static_cast<size_t>(GATE_STAGES) * (TOK + EXP) * ROW_BYTES + 8 * GATE_STAGES + 16;
+    CUtensorMap tm_x, tm_w;
+    if (!encode_tma_2d_plain(&tm_x, x, static_cast<uint64_t>(d_h), static_cast<uint64_t>(T), SLICE, TOK) ||
+        !encode_tma_2d_plain(&tm_w, wg, static_cast<uint64_t>(d_h), static_cast<uint64_t>(E), SLICE, EXP))
+        return cudaErrorInvalidValue;
     auto kern = gate_kernel<DT, TPW, WT, WE, FUSE>;
     static bool attr_done[64] = {false};
     int dev = 0;
@@ -278,9 +286,8 @@ cudaError_t launch_gate_shape(const void *x, const void *wg, const float *bias, 
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
     dim3 grid(static_cast<unsigned>((T + TOK - 1) / TOK), static_cast<unsigned>((E + EXP - 1) / EXP));
-    return launch_pdl(kern, grid, dim3(WT * WE * 32), smem, stream, static_cast<const uint16_t *>(x),
-                      static_cast<const uint16_t *>(wg), bias, (int)T, (int)d_h, (int)E, (int)k,
-                      logits, idx, w);
+    return launch_pdl(kern, grid, dim3(WT * WE * 32), smem, stream, tm_x, tm_w, bias, (int)T,
+                      (int)d_h, (int)E, (int)k, logits, idx, w);
 }
 
 cudaError_t launch_topk(const float *logits, int64_t T, int64_t E, int64_t k, int32_t *topk_idx,

@@ -408,6 +408,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+}  // namespace
+
+// Row-major [rows, inner] 16-bit matrix, box = box_inner x box_rows, no swizzle.
+bool encode_tma_2d_plain(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows,
+                         uint32_t box_inner, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(ptr), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+namespace {
+
 // Row-major [rows, K] 16-bit matrix, box = 64 K-elements x box_rows rows.
 bool make_map_2d(CUtensorMap *m, int dtype, const void *ptr, uint64_t K, uint64_t rows,
                  uint32_t box_rows) {

@@ -6,9 +6,16 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <cuda.h>
+
 namespace moe {
 
 int device_sm_count();
+
+// grouped_gemm.cu: tensor map of a row-major [rows, inner] 16-bit matrix,
+// box = box_inner x box_rows elements, no swizzle.  False if encoding fails.
+bool encode_tma_2d_plain(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows,
+                         uint32_t box_inner, uint32_t box_rows);
 
 // gate_topk.cu: logits (written to `logits`, [T, E] fp32), top-k ids and weights
 cudaError_t launch_gate_topk(const void *x, const void *wg, const float *bias, int64_t T,
