@@ -189,6 +189,15 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     return p;
 }
 
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *desc, uint32_t bar, int c0,
+                                                 int c1, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *desc, uint32_t bar, int c0,
                                                  int c1, int c2, uint64_t policy) {
     asm volatile(

@@ -15,7 +15,10 @@
 //               shared-memory ring, 128-byte swizzled.
 //   warp 1      MMA issuer: one thread issues tcgen05.mma M=128 N=256 K=16 into
 //               a TMEM accumulator (2 x 256 columns, double buffered so the
-//               epilogue of tile i overlaps the main loop of tile i+1).
+//               epilogue of tile i overlaps the main loop of tile i+1).  Blocks
+//               with at most 64 valid rows are computed swapped: two M=128
+//               MMAs with the weight halves as A and the block's rows as B
+//               (N = rows rounded up to 16), a fraction of the tensor work.
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (thread = row), stage 1
 //               fuses silu(gate)*up, stage 2 the optional row weight; round to
 //               the activation dtype and store only the block's valid rows.
@@ -45,8 +48,13 @@ constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int B_BYTES = MMA_N * BK * 2;      // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int BAR_BYTES = 256;
-constexpr int MAX_SCHED = 4096;  // M blocks the in-kernel schedule can order
-constexpr int SCHED_BYTES = MAX_SCHED * 4 + MAX_SCHED + 64;
+// Blocks with at most this many valid rows run "swapped": the weight tile is
+// the M=128 operand and the block's rows the N operand (N = rows rounded up
+// to 16), so a mostly-padding block costs N/128 of a full MMA.
+constexpr int SWAP_MAX_ROWS = 64;
+constexpr int MAX_SCHED = 2048;  // M blocks the in-kernel schedule can order
+// block list, expert per full block, run start / length (int16), class, scratch
+constexpr int SCHED_BYTES = MAX_SCHED * 4 + MAX_SCHED * 4 + 2 * MAX_SCHED * 2 + MAX_SCHED + 64;
 constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES + SCHED_BYTES;
 
 struct GemmParams {
@@ -65,6 +73,7 @@ struct GemmParams {
 
 struct TileInfo {
     int g, m_start, rows, n0;
+    bool big;  // part of a large expert's stripe-major run
 };
 
 // Valid rows of M block bx (the pages' actual_rows) and its first row.
@@ -78,32 +87,52 @@ __device__ __forceinline__ int block_rows(const GemmParams &p, int bx, int *g_ou
     return rows;
 }
 
-// The tile schedule.  Non-empty M blocks are split into full blocks (128
-// valid rows: the tensor pipe is the limit) and partial blocks (mostly
-// padding: streaming the expert's weights is the limit), each list in block
-// order, and the two lists are interleaved evenly; the N tiles of one block
-// stay adjacent.  Dealt round-robin to the persistent CTAs, every window of
-// consecutive tiles then mixes both kinds, so the tensor pipe and HBM are
-// busy at the same time, while the blocks of one large expert still run
-// close together and share its weights through L2.
+// The tile schedule.  Non-empty M blocks are split by expert size: blocks of
+// experts with at least 128 rows (their full blocks are tensor-bound) and
+// the single block of each smaller expert (mostly padding: streaming the
+// expert's weights is the limit).  Small experts' tiles go block by block.
+// Large experts' tiles go expert by expert, and inside an expert N-stripe
+// first: every block of the expert on weight stripe n before stripe n+1, so
+// a stripe is fetched from HBM once while the expert's activation rows are
+// re-read from L2.  The two tile sequences are interleaved evenly,
+// so every window of tiles dealt round-robin to the persistent CTAs mixes
+// both kinds and the tensor pipe and HBM are busy at the same time.
 struct Schedule {
-    const int *list;  // [n_full full blocks][n_partial partial blocks]; null = natural order
+    const int *list;       // [n_full full blocks][n_partial partial blocks]; null = natural order
+    const int16_t *run_start;  // per full block: index of its expert's first full block in list
+    const int16_t *run_len;    // per full block: number of full blocks of its expert
     int n_full, n_blocks;
 };
 
 __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const Schedule &sc, int tile,
                                               int out_n) {
-    const int bp = tile / p.n_tiles;
-    const int nt = tile - bp * p.n_tiles;
-    int bx = bp;
+    int bx, nt;
+    bool tile_is_big = false;
     if (sc.list) {
-        const int hb = static_cast<int>(static_cast<int64_t>(bp) * sc.n_full / sc.n_blocks);
-        const int hn = static_cast<int>(static_cast<int64_t>(bp + 1) * sc.n_full / sc.n_blocks);
-        bx = hn > hb ? sc.list[hb] : sc.list[sc.n_full + (bp - hb)];
+        const int64_t n_full_t = static_cast<int64_t>(sc.n_full) * p.n_tiles;
+        const int64_t n_all_t = static_cast<int64_t>(sc.n_blocks) * p.n_tiles;
+        const int64_t hb = tile * n_full_t / n_all_t;         // full tiles before position tile
+        const int64_t hn = (tile + 1) * n_full_t / n_all_t;
+        if (hn > hb) {
+            tile_is_big = true;
+            const int fb = static_cast<int>(hb / p.n_tiles);  // full block whose run holds it
+            const int rs = sc.run_start[fb], rl = sc.run_len[fb];
+            const int64_t o = hb - static_cast<int64_t>(rs) * p.n_tiles;
+            nt = static_cast<int>(o / rl);
+            bx = sc.list[rs + static_cast<int>(o - static_cast<int64_t>(nt) * rl)];
+        } else {
+            const int64_t lt = tile - hb;                     // partial tile index
+            bx = sc.list[sc.n_full + static_cast<int>(lt / p.n_tiles)];
+            nt = static_cast<int>(lt % p.n_tiles);
+        }
+    } else {
+        bx = tile / p.n_tiles;
+        nt = tile - bx * p.n_tiles;
     }
     TileInfo t;
     t.rows = block_rows(p, bx, &t.g, &t.m_start);
     t.n0 = nt * out_n;
+    t.big = sc.list != nullptr && tile_is_big;
     return t;
 }
 
@@ -158,8 +187,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *sched = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(bars) + BAR_BYTES);
-    uint8_t *sched_cls = reinterpret_cast<uint8_t *>(sched + MAX_SCHED);
-    int *sched_scratch = reinterpret_cast<int *>(sched_cls + MAX_SCHED);
+    int *sched_g = sched + MAX_SCHED;
+    int16_t *sched_rs = reinterpret_cast<int16_t *>(sched_g + MAX_SCHED);
+    int16_t *sched_rl = sched_rs + MAX_SCHED;
+    uint8_t *sched_cls = reinterpret_cast<uint8_t *>(sched_rl + MAX_SCHED);
+    int *sched_scratch = reinterpret_cast<int *>(sched_cls + MAX_SCHED + (4 - MAX_SCHED % 4) % 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -193,11 +225,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     griddep_wait();
     griddep_launch_dependents();
     // ----- schedule: classify the M blocks, list full and partial ones -----
-    Schedule sc{nullptr, 0, p.m_blocks};
+    Schedule sc{nullptr, nullptr, nullptr, 0, p.m_blocks};
     if (p.m_blocks <= MAX_SCHED) {
         for (int bx = threadIdx.x; bx < p.m_blocks; bx += NUM_THREADS) {
-            const int r = block_rows(p, bx, nullptr, nullptr);
-            sched_cls[bx] = r == 0 ? 0 : (r == BM ? 2 : 1);
+            int g;
+            const int r = block_rows(p, bx, &g, nullptr);
+            // every block of an expert with at least one full block joins that
+            // expert's run (its tail too: one sweep over the expert's weights)
+            sched_cls[bx] = r == 0 ? 0 : (__ldg(p.sizes + g) >= BM ? 2 : 1);
         }
         __syncthreads();
         const int chunk = (p.m_blocks + NUM_THREADS - 1) / NUM_THREADS;
@@ -215,7 +250,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (sched_cls[bx] == 2) sched[bf++] = bx;
             else if (sched_cls[bx] == 1) sched[tot_f + bpart++] = bx;
         }
+        __syncthreads();
+        // runs of full blocks of one expert (consecutive in the list, block
+        // order = expert order): each full block learns its run's start/length
+        for (int i = threadIdx.x; i < tot_f; i += NUM_THREADS) sched_g[i] = __ldg(p.gidx + sched[i]);
+        __syncthreads();
+        for (int i = threadIdx.x; i < tot_f; i += NUM_THREADS) {
+            const int g = sched_g[i];
+            int lo_i = i, hi_i = i;
+            while (lo_i > 0 && sched_g[lo_i - 1] == g) --lo_i;
+            while (hi_i + 1 < tot_f && sched_g[hi_i + 1] == g) ++hi_i;
+            sched_rs[i] = static_cast<int16_t>(lo_i);
+            sched_rl[i] = static_cast<int16_t>(hi_i - lo_i + 1);
+        }
         sc.list = sched;
+        sc.run_start = sched_rs;
+        sc.run_len = sched_rl;
         sc.n_full = tot_f;
         sc.n_blocks = tot_f + tot_p;
     }
@@ -246,15 +296,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);
                     const uint32_t a_dst = smem_u32(sA + stage * A_BYTES);
                     const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
-                    tma_load_2d(a_dst, &tmA, fb, kb * BK, ti.m_start);
-                    // weights of a partial block are read by this block only:
-                    // let them leave L2 first, ahead of reused data
-                    const uint64_t pol = ti.rows < BM ? pol_first : pol_last;
+                    // a large expert's rows and weight stripes are reused by the
+                    // tiles of its run: keep them; a small expert's weights are
+                    // read by one block only: let them leave L2 first
+                    if (ti.big) tma_load_2d_hint(a_dst, &tmA, fb, kb * BK, ti.m_start, pol_last);
+                    else tma_load_2d(a_dst, &tmA, fb, kb * BK, ti.m_start);
+                    const uint64_t polb = ti.big ? pol_last : pol_first;
                     if (GATE_UP) {
-                        tma_load_3d_hint(b_dst, &tmB0, fb, kb * BK, ti.n0, ti.g, pol);
-                        tma_load_3d_hint(b_dst + B_BYTES / 2, &tmB1, fb, kb * BK, ti.n0, ti.g, pol);
+                        tma_load_3d_hint(b_dst, &tmB0, fb, kb * BK, ti.n0, ti.g, polb);
+                        tma_load_3d_hint(b_dst + B_BYTES / 2, &tmB1, fb, kb * BK, ti.n0, ti.g, polb);
                     } else {
-                        tma_load_3d_hint(b_dst, &tmB0, fb, kb * BK, ti.n0, ti.g, pol);
+                        tma_load_3d_hint(b_dst, &tmB0, fb, kb * BK, ti.n0, ti.g, polb);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -292,6 +344,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
+                const bool swap = ti.rows <= SWAP_MAX_ROWS;
+                const int np = (ti.rows + 15) & ~15;
+                const uint32_t idesc_sw = idesc_f16(DT == kBF16, BM, static_cast<uint32_t>(np));
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.err)) {
                         ok = false;
@@ -300,11 +355,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tc_fence_after();
                     const uint64_t a_desc = smem_desc_sw128(smem_u32(sA + stage * A_BYTES));
                     const uint64_t b_desc = smem_desc_sw128(smem_u32(sB + stage * B_BYTES));
+                    if (swap) {
+                        // D[feature][row]: first 128 weight rows into columns [0, np),
+                        // the other 128 into [np, 2np)
+                        const uint64_t b2_desc = smem_desc_sw128(smem_u32(sB + stage * B_BYTES + B_BYTES / 2));
 #pragma unroll
-                    for (int k = 0; k < BK / UMMA_K; ++k) {
-                        // +32 bytes per K=16 step inside the 128-byte swizzled row
-                        tc_mma_f16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, IDESC,
-                                   (kb | k) != 0 ? 1u : 0u);
+                        for (int k = 0; k < BK / UMMA_K; ++k) {
+                            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+                            tc_mma_f16(d_tmem, b_desc + 2u * k, a_desc + 2u * k, idesc_sw, accum);
+                            tc_mma_f16(d_tmem + static_cast<uint32_t>(np), b2_desc + 2u * k,
+                                       a_desc + 2u * k, idesc_sw, accum);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k) {
+                            // +32 bytes per K=16 step inside the 128-byte swizzled row
+                            tc_mma_f16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, IDESC,
+                                       (kb | k) != 0 ? 1u : 0u);
+                        }
                     }
                     tc_commit(empty_bar(stage));  // frees the smem stage when these MMAs finish
                     last_bar = empty_bar(stage);
@@ -339,6 +407,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * ACC_COLS);
+            if (ti.rows <= SWAP_MAX_ROWS) {
+                // swapped tile: this thread holds output feature `row` (and, for
+                // stage 2, feature 128 + row) for every row j of the block
+                const int np = (ti.rows + 15) & ~15;
+                OutT *out = reinterpret_cast<OutT *>(p.out);
+                const int f0 = ti.n0 + row;
+                const int f1 = GATE_UP ? -1 : ti.n0 + 128 + row;
+#pragma unroll 1
+                for (int j0 = 0; j0 < np; j0 += 16) {
+                    uint32_t a[16], b[16];
+                    tmem_ld16(t_row + j0, a);
+                    tmem_ld16(t_row + np + j0, b);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int j = j0 + jj;
+                        if (j < ti.rows) {
+                            const int64_t r = static_cast<int64_t>(ti.m_start + j) * p.N;
+                            if (GATE_UP) {
+                                const float gv = __uint_as_float(a[jj]);
+                                const float s = gv * __frcp_rn(1.0f + __expf(-gv));
+                                if (f0 < p.N) out[r + f0] = from_f32<OutT>(s * __uint_as_float(b[jj]));
+                            } else {
+                                const float rwj = p.row_weights ? __ldg(p.row_weights + ti.m_start + j) : 1.0f;
+                                if (f0 < p.N) out[r + f0] = from_f32<OutT>(__uint_as_float(a[jj]) * rwj);
+                                if (f1 < p.N) out[r + f1] = from_f32<OutT>(__uint_as_float(b[jj]) * rwj);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(acc));
+                ++local;
+                continue;
+            }
             const bool valid = row < ti.rows;
             OutT *out_row = reinterpret_cast<OutT *>(p.out) +
                             static_cast<int64_t>(ti.m_start + (valid ? row : 0)) * p.N;
