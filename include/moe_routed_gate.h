@@ -192,6 +192,28 @@ MOE_API moe_status_t moe_grouped_down(const void *h, const void *w_down, const i
                               int32_t *err_flag, moe_stream_t stream);
 
 /*
+ * Both expert GEMMs in one persistent launch (CSDN "tilelang kernel stage 2
+ * down": the article names fusing the two stages as an optimisation point).
+ * Results equal moe_grouped_gate_up_silu(a -> h) followed by
+ * moe_grouped_down(h -> y, row_weights): h [n_rows, d_e] is still written (it
+ * is stage 2's operand, read back mostly from L2) and y [n_rows, d_h].
+ * Inside the kernel a stage-2 tile starts once all stage-1 tiles of its M
+ * block are stored; the block's counter lives in `ready`, caller-owned device
+ * memory of m_blocks int32 that this call zeroes (stream ordered) before the
+ * launch.  The waits are bounded: after about 2 s *err_flag is set to
+ * MOE_ERR_TIMEOUT and the kernel returns (this needs all CTAs of the grid,
+ * one per SM, resident at once; a GPU shared with a partitioning runtime can
+ * break that).  Other arguments, layouts and errors as the two calls.
+ */
+MOE_API moe_status_t moe_grouped_mlp(const void *a, const void *w_gate, const void *w_up,
+                             const void *w_down, const int32_t *group_sizes,
+                             const int32_t *group_offsets, const int32_t *group_padded_offsets,
+                             const int32_t *group_idx_for_bx, int64_t m_blocks,
+                             const float *row_weights, int64_t n_rows, int64_t d_h, int64_t d_e,
+                             int64_t E, moe_dtype_t dtype, void *h, void *y, int32_t *ready,
+                             int32_t *err_flag, moe_stream_t stream);
+
+/*
  * moe_reduce_fused (TileOPs-Metax PR #55, section 1): for every token t and
  * hidden element h,
  *   out[t, h] = cast( sum over k ascending with 0 <= pos[t,k] < n_rows of
@@ -231,7 +253,7 @@ MOE_API moe_status_t moe_reduce_fused_scaled(const void *x, int64_t n_rows,
 /*
  * The whole routed forward, stream ordered, no host round trip:
  *   moe_gate_topk -> moe_build_dispatch -> moe_gather_rows ->
- *   moe_grouped_gate_up_silu -> moe_grouped_down -> moe_reduce_fused.
+ *   moe_grouped_mlp (stage 1 + stage 2 in one launch) -> moe_reduce_fused.
  * x [T, d_h]; w_g [E, d_h]; bias [E] fp32 or NULL; w_gate/w_up [E, d_e, d_h];
  * w_down [E, d_h, d_e]; out [T, d_h]; all in `dtype` (f16 or bf16).
  * ws: moe_forward_workspace_bytes(...) bytes, 256-byte aligned; it holds every
@@ -248,7 +270,8 @@ MOE_API moe_status_t moe_forward(const void *x, const void *w_g, const float *bi
  * inspection after a call: index 0 logits, 1 topk_idx, 2 topk_w, 3 group_sizes,
  * 4 group_offsets, 5 group_padded_offsets, 6 group_idx_for_bx,
  * 7 sorted_token_idx, 8 sorted_row_weight, 9 token_topk_to_pos, 10 dispatch
- * scratch, 11 gathered rows A, 12 h, 13 y.  Returns -1 for a bad index.
+ * scratch, 11 gathered rows A, 12 h, 13 y, 14 the per-block counters of
+ * moe_grouped_mlp.  Returns -1 for a bad index.
  */
 MOE_API int64_t moe_forward_workspace_offset(int64_t T, int64_t d_h, int64_t d_e, int64_t E, int64_t k,
                                      moe_dtype_t dtype, int index);

@@ -22,7 +22,7 @@ _lib = None
 BLOCK_M = 128
 WS_NAMES = ["logits", "topk_idx", "topk_w", "group_sizes", "group_offsets",
             "group_padded_offsets", "group_idx_for_bx", "sorted_token_idx", "sorted_row_weight",
-            "token_topk_to_pos", "dispatch_scratch", "a", "h", "y"]
+            "token_topk_to_pos", "dispatch_scratch", "a", "h", "y", "mlp_ready"]
 
 
 class MoEError(RuntimeError):
@@ -60,6 +60,7 @@ def lib():
         "moe_gather_rows": (I, [P, P, I64, I64, I64, I, P, P]),
         "moe_grouped_gate_up_silu": (I, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, P, P]),
         "moe_grouped_down": (I, [P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I, P, P, P]),
+        "moe_grouped_mlp": (I, [P, P, P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I, P, P, P, P, P]),
         "moe_reduce_fused": (I, [P, I64, P, P, I64, I64, I64, I, I, P, P, P]),
         "moe_reduce_fused_scaled": (I, [P, I64, P, P, P, P, I64, I64, I64, I, I, P, P, P]),
         "moe_forward": (I, [P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, SZ, P, P, P]),
@@ -78,7 +79,7 @@ def exported_symbols():
             "moe_forward_workspace_offset", "moe_gate_topk", "moe_build_dispatch",
             "moe_build_dispatch_noalloc",
             "moe_gather_rows", "moe_grouped_gate_up_silu", "moe_grouped_down",
-            "moe_reduce_fused", "moe_reduce_fused_scaled", "moe_forward"]
+            "moe_grouped_mlp", "moe_reduce_fused", "moe_reduce_fused_scaled", "moe_forward"]
 
 
 # --------------------------------------------------------------------------- helpers
@@ -287,6 +288,42 @@ def moe_grouped_down(h, w_down, tables, row_weights=None, y=None, err=None):
     return y
 
 
+def moe_grouped_mlp(a, w_gate, w_up, w_down, tables, row_weights=None, h=None, y=None,
+                    ready=None, err=None):
+    """Stage 1 and stage 2 in one launch; returns (h, y)."""
+    _cuda(a, "a", ndim=2)
+    for n, t in (("w_gate", w_gate), ("w_up", w_up), ("w_down", w_down)):
+        _cuda(t, n, dtype=a.dtype, ndim=3)
+    n_rows, d_h = a.shape
+    E, d_e, d_h2 = w_gate.shape
+    if d_h2 != d_h or w_up.shape != w_gate.shape:
+        raise ValueError("w_gate / w_up must be [E, d_expert, d_hidden]")
+    if tuple(w_down.shape) != (E, d_h, d_e):
+        raise ValueError("w_down must be [E, d_hidden, d_expert]")
+    s, o, p, g = _tables(tables)
+    if row_weights is not None:
+        _cuda(row_weights, "row_weights", dtype=torch.float32)
+    if h is None:
+        h = torch.empty((n_rows, d_e), dtype=a.dtype, device=a.device)
+    if y is None:
+        y = torch.empty((n_rows, d_h), dtype=a.dtype, device=a.device)
+    if ready is None:
+        ready = torch.empty(max(g.numel(), 1), dtype=torch.int32, device=a.device)
+    _cuda(h, "h", dtype=a.dtype)
+    _cuda(y, "y", dtype=a.dtype)
+    _cuda(ready, "ready", dtype=torch.int32)
+    if ready.numel() < g.numel():
+        raise ValueError("ready needs one int32 per M block")
+    if err is not None:
+        _cuda(err, "err", dtype=torch.int32)
+    with torch.cuda.device(a.device):
+        _check(lib().moe_grouped_mlp(
+            _ptr(a), _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(s), _ptr(o), _ptr(p), _ptr(g),
+            g.numel(), _ptr(row_weights), n_rows, d_h, d_e, E, _dtype_code(a, "a"), _ptr(h),
+            _ptr(y), _ptr(ready), _ptr(err), _stream(a.device)), "moe_grouped_mlp")
+    return h, y
+
+
 def moe_reduce_fused(x, token_topk_to_pos, topk_weights=None, out_dtype=None, out=None, err=None):
     """out[t] = cast(sum_k w[t,k] * x[pos[t,k]]) over pos >= 0, fp32 accumulation."""
     _cuda(x, "x", ndim=2)
@@ -367,7 +404,7 @@ def forward_workspace_views(ws, T, d_h, d_e, E, k, dtype) -> dict:
               "group_idx_for_bx": ((mb,), torch.int32), "sorted_token_idx": ((Tk,), torch.int32),
               "sorted_row_weight": ((Tk,), torch.float32),
               "token_topk_to_pos": ((T, k), torch.int32), "a": ((Tk, d_h), dtype),
-              "h": ((Tk, d_e), dtype), "y": ((Tk, d_h), dtype)}
+              "h": ((Tk, d_e), dtype), "y": ((Tk, d_h), dtype), "mlp_ready": ((mb,), torch.int32)}
     out = {}
     for i, name in enumerate(WS_NAMES):
         if name not in shapes:

@@ -38,8 +38,10 @@ int64_t m_blocks_of(int64_t T, int64_t k, int64_t E, int64_t block_m) {
     return (T * k + block_m - 1) / block_m + E;
 }
 
+constexpr int kFwdSections = 15;
+
 struct FwdLayout {
-    size_t off[14];
+    size_t off[kFwdSections];
     size_t total;
 };
 
@@ -49,7 +51,7 @@ bool fwd_layout(int64_t T, int64_t d_h, int64_t d_e, int64_t E, int64_t k, moe_d
     const size_t es = 2;
     const size_t Tk = static_cast<size_t>(T * k);
     const size_t mb = static_cast<size_t>(m_blocks_of(T, k, E, MOE_BLOCK_M));
-    const size_t sz[14] = {
+    const size_t sz[kFwdSections] = {
         static_cast<size_t>(T) * E * 4,  // 0 logits
         Tk * 4,                          // 1 topk_idx
         Tk * 4,                          // 2 topk_w
@@ -64,9 +66,10 @@ bool fwd_layout(int64_t T, int64_t d_h, int64_t d_e, int64_t E, int64_t k, moe_d
         Tk * d_h * es,                   // 11 A (gathered rows)
         Tk * d_e * es,                   // 12 h
         Tk * d_h * es,                   // 13 y
+        mb * 4,                          // 14 per-block counters of the expert MLP
     };
     size_t cur = 0;
-    for (int i = 0; i < 14; ++i) {
+    for (int i = 0; i < kFwdSections; ++i) {
         L->off[i] = cur;
         cur += align_up(sz[i] > 0 ? sz[i] : 1);
     }
@@ -115,7 +118,7 @@ size_t moe_forward_workspace_bytes(int64_t T, int64_t d_h, int64_t d_e, int64_t 
 int64_t moe_forward_workspace_offset(int64_t T, int64_t d_h, int64_t d_e, int64_t E, int64_t k,
                                      moe_dtype_t dtype, int index) {
     FwdLayout L;
-    if (index < 0 || index >= 14 || !fwd_layout(T, d_h, d_e, E, k, dtype, &L)) return -1;
+    if (index < 0 || index >= kFwdSections || !fwd_layout(T, d_h, d_e, E, k, dtype, &L)) return -1;
     return static_cast<int64_t>(L.off[index]);
 }
 
@@ -136,12 +139,12 @@ moe_status_t moe_gate_topk(const void *x, const void *w_g, const float *bias, in
                                              topk_w, s));
 }
 
-moe_status_t moe_build_dispatch(const int32_t *topk_idx, const float *topk_w, int64_t T,
-                                int64_t k, int64_t E, int64_t block_m, int32_t *group_sizes,
-                                int32_t *group_offsets, int32_t *group_padded_offsets,
-                                int32_t *group_idx_for_bx, int32_t *sorted_token_idx,
-                                float *sorted_row_weight, int32_t *token_topk_to_pos, void *ws,
-                                size_t ws_bytes, moe_stream_t stream) {
+static moe_status_t build_dispatch(const int32_t *topk_idx, const float *topk_w, int64_t T,
+                                   int64_t k, int64_t E, int64_t block_m, int32_t *group_sizes,
+                                   int32_t *group_offsets, int32_t *group_padded_offsets,
+                                   int32_t *group_idx_for_bx, int32_t *sorted_token_idx,
+                                   float *sorted_row_weight, int32_t *token_topk_to_pos, void *ws,
+                                   size_t ws_bytes, int32_t *ready, moe_stream_t stream) {
     if (T < 0 || k <= 0 || E <= 0 || E > 1024 || block_m != MOE_BLOCK_M) return MOE_ERR_INVALID_ARG;
     if (T * k > (int64_t(1) << 30)) return MOE_ERR_UNSUPPORTED;
     if (!group_sizes || !group_offsets || !group_padded_offsets || !group_idx_for_bx)
@@ -153,7 +156,18 @@ moe_status_t moe_build_dispatch(const int32_t *topk_idx, const float *topk_w, in
     return cuda_status(moe::launch_dispatch(
         topk_idx, topk_w, T, k, E, block_m, group_sizes, group_offsets, group_padded_offsets,
         group_idx_for_bx, m_blocks_of(T, k, E, block_m), sorted_token_idx, sorted_row_weight,
-        token_topk_to_pos, ws, reinterpret_cast<cudaStream_t>(stream)));
+        token_topk_to_pos, ws, ready, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_build_dispatch(const int32_t *topk_idx, const float *topk_w, int64_t T,
+                                int64_t k, int64_t E, int64_t block_m, int32_t *group_sizes,
+                                int32_t *group_offsets, int32_t *group_padded_offsets,
+                                int32_t *group_idx_for_bx, int32_t *sorted_token_idx,
+                                float *sorted_row_weight, int32_t *token_topk_to_pos, void *ws,
+                                size_t ws_bytes, moe_stream_t stream) {
+    return build_dispatch(topk_idx, topk_w, T, k, E, block_m, group_sizes, group_offsets,
+                          group_padded_offsets, group_idx_for_bx, sorted_token_idx,
+                          sorted_row_weight, token_topk_to_pos, ws, ws_bytes, nullptr, stream);
 }
 
 moe_status_t moe_gather_rows(const void *x, const int32_t *sorted_token_idx, int64_t n_rows,
@@ -219,6 +233,48 @@ moe_status_t moe_grouped_down(const void *h, const void *w_down, const int32_t *
         false, dtype, h, w_down, nullptr, group_sizes, group_offsets, group_padded_offsets,
         group_idx_for_bx, m_blocks, row_weights, n_rows, d_e, d_h, E, y, err_flag,
         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// zero_ready: clear the counters on the stream first (the forward has its
+// dispatch kernel clear them instead, keeping the kernels back to back).
+static moe_status_t grouped_mlp(const void *a, const void *w_gate, const void *w_up,
+                                const void *w_down, const int32_t *group_sizes,
+                                const int32_t *group_offsets, const int32_t *group_padded_offsets,
+                                const int32_t *group_idx_for_bx, int64_t m_blocks,
+                                const float *row_weights, int64_t n_rows, int64_t d_h, int64_t d_e,
+                                int64_t E, moe_dtype_t dtype, void *h, void *y, int32_t *ready,
+                                int32_t *err_flag, moe_stream_t stream, bool zero_ready) {
+    if (!is_half_type(dtype)) return MOE_ERR_UNSUPPORTED;
+    if (d_h <= 0 || d_e <= 0 || d_h % 64 != 0 || d_e % 64 != 0) return MOE_ERR_INVALID_ARG;
+    if (n_rows == 0) return MOE_OK;
+    moe_status_t st = check_gemm_tables(group_sizes, group_offsets, group_padded_offsets,
+                                        group_idx_for_bx, m_blocks, n_rows, E);
+    if (st != MOE_OK) return st;
+    if (!a || !w_gate || !w_up || !w_down || !h || !y || !ready) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+        !aligned16(h) || !aligned16(y))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (zero_ready) {
+        cudaError_t e = cudaMemsetAsync(ready, 0, static_cast<size_t>(m_blocks) * 4, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return cuda_status(moe::launch_grouped_mlp(dtype, a, w_gate, w_up, w_down, group_sizes,
+                                               group_offsets, group_padded_offsets, group_idx_for_bx,
+                                               m_blocks, row_weights, n_rows, d_h, d_e, E, h, y,
+                                               ready, err_flag, s));
+}
+
+moe_status_t moe_grouped_mlp(const void *a, const void *w_gate, const void *w_up,
+                             const void *w_down, const int32_t *group_sizes,
+                             const int32_t *group_offsets, const int32_t *group_padded_offsets,
+                             const int32_t *group_idx_for_bx, int64_t m_blocks,
+                             const float *row_weights, int64_t n_rows, int64_t d_h, int64_t d_e,
+                             int64_t E, moe_dtype_t dtype, void *h, void *y, int32_t *ready,
+                             int32_t *err_flag, moe_stream_t stream) {
+    return grouped_mlp(a, w_gate, w_up, w_down, group_sizes, group_offsets, group_padded_offsets,
+                       group_idx_for_bx, m_blocks, row_weights, n_rows, d_h, d_e, E, dtype, h, y,
+                       ready, err_flag, stream, true);
 }
 
 static bool reduce_pair_ok(moe_dtype_t in, moe_dtype_t out, bool allow_fp8) {
@@ -292,22 +348,21 @@ moe_status_t moe_forward(const void *x, const void *w_g, const float *bias, cons
     void *A = w + L.off[11];
     void *hbuf = w + L.off[12];
     void *ybuf = w + L.off[13];
+    int32_t *ready = reinterpret_cast<int32_t *>(w + L.off[14]);
     const int64_t Tk = T * k;
     const int64_t mb = m_blocks_of(T, k, E, MOE_BLOCK_M);
     moe_status_t st;
     st = moe_gate_topk(x, w_g, bias, T, d_h, E, k, dtype, topk_idx, topk_w, logits,
                        static_cast<size_t>(T) * E * 4, stream);
     if (st != MOE_OK) return st;
-    st = moe_build_dispatch(topk_idx, topk_w, T, k, E, MOE_BLOCK_M, sizes, offsets, padded, gidx,
-                            stok, sw, pos, scratch, moe::dispatch_scratch_bytes(Tk, E), stream);
+    // the dispatch also clears the expert MLP's per-block counters
+    st = build_dispatch(topk_idx, topk_w, T, k, E, MOE_BLOCK_M, sizes, offsets, padded, gidx, stok,
+                        sw, pos, scratch, moe::dispatch_scratch_bytes(Tk, E), ready, stream);
     if (st != MOE_OK) return st;
     st = moe_gather_rows(x, stok, Tk, T, d_h, dtype, A, stream);
     if (st != MOE_OK) return st;
-    st = moe_grouped_gate_up_silu(A, w_gate, w_up, sizes, offsets, padded, gidx, mb, Tk, d_h, d_e,
-                                  E, dtype, hbuf, err_flag, stream);
-    if (st != MOE_OK) return st;
-    st = moe_grouped_down(hbuf, w_down, sizes, offsets, padded, gidx, mb, nullptr, Tk, d_h, d_e, E,
-                          dtype, ybuf, err_flag, stream);
+    st = grouped_mlp(A, w_gate, w_up, w_down, sizes, offsets, padded, gidx, mb, nullptr, Tk, d_h,
+                     d_e, E, dtype, hbuf, ybuf, ready, err_flag, stream, false);
     if (st != MOE_OK) return st;
     return moe_reduce_fused(ybuf, Tk, pos, topk_w, T, k, d_h, dtype, dtype, out, err_flag, stream);
 }

@@ -153,6 +153,42 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // ----------------------------------------------------------------------------
+// Counters between CTAs of one persistent grid.  The writer's plain stores
+// are published with a gpu-scope release add; the reader acquires the count
+// and then orders its later TMA (async proxy) reads after what it acquired.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void counter_publish(int *ctr) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(ctr) : "memory");
+}
+
+__device__ __forceinline__ int counter_load_acquire(const int *ctr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    return v;
+}
+
+// Waits until *ctr >= target; false (after recording kErrTimeout and raising
+// the abort flag) when the wait runs out or the CTA already aborted.
+__device__ __forceinline__ bool counter_wait_bounded(const int *ctr, int target,
+                                                     volatile int *abort_flag, int *err_flag) {
+    if (counter_load_acquire(ctr) < target) {
+        const unsigned long long start = global_timer_ns();
+        for (;;) {
+            __nanosleep(100);
+            if (counter_load_acquire(ctr) >= target) break;
+            if (*abort_flag) return false;
+            if (global_timer_ns() - start > kWaitTimeoutNs) {
+                *abort_flag = 1;
+                if (err_flag) atomicExch(err_flag, kErrTimeout);
+                return false;
+            }
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
+// ----------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), global -> shared, completion on an mbarrier
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const void *desc) {

@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(SCAN_THREADS)
     dispatch_scan_kernel(int32_t *__restrict__ hist, int n_chunks, int E, int block_m,
                          int32_t *__restrict__ sizes, int32_t *__restrict__ offsets,
                          int32_t *__restrict__ padded, int32_t *__restrict__ gidx,
-                         int m_blocks) {
+                         int m_blocks, int32_t *__restrict__ ready) {
     __shared__ int warp_sums[32];
     __shared__ int po_s[SCAN_THREADS];
     const int e = threadIdx.x;
@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(SCAN_THREADS)
             else hi = mid - 1;
         }
         gidx[bx] = lo;
+        if (ready) ready[bx] = 0;
     }
 }
 
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(SMALL_THREADS)
                           int32_t *__restrict__ offsets, int32_t *__restrict__ padded,
                           int32_t *__restrict__ gidx, int m_blocks,
                           int32_t *__restrict__ sorted_tok, float *__restrict__ sorted_w,
-                          int32_t *__restrict__ pos) {
+                          int32_t *__restrict__ pos, int32_t *__restrict__ ready) {
     constexpr int SMALL_WARPS = SMALL_THREADS / 32;
     static_assert(SMALL_THREADS >= SMALL_MAX_E, "one thread per expert");
     __shared__ int32_t wcount[SMALL_WARPS * SMALL_MAX_E];
@@ -250,6 +251,7 @@ __global__ void __launch_bounds__(SMALL_THREADS)
             else hi = mid - 1;
         }
         gidx[bx] = lo;
+        if (ready) ready[bx] = 0;
     }
 #pragma unroll
     for (int r = 0; r < SMALL_MAX_ROUNDS; ++r) {
@@ -282,7 +284,7 @@ cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_
                             int64_t E, int64_t block_m, int32_t *sizes, int32_t *offsets, int32_t *padded,
                             int32_t *gidx, int64_t m_blocks, int32_t *sorted_token_idx,
                             float *sorted_row_weight, int32_t *pos, void *scratch,
-                            cudaStream_t stream) {
+                            int32_t *ready, cudaStream_t stream) {
     const int64_t n_pairs = T * k;
     if (n_pairs <= SMALL_MAX_PAIRS && E <= SMALL_MAX_E) {
         // fewer threads (shorter per-expert walks and scans) for few pairs
@@ -292,7 +294,7 @@ cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_
         return launch_pdl(kern, dim3(1), dim3(threads), 0, stream, topk_idx, topk_w,
                           static_cast<int>(n_pairs), static_cast<int>(k), static_cast<int>(E),
                           static_cast<int>(block_m), sizes, offsets, padded, gidx,
-                          static_cast<int>(m_blocks), sorted_token_idx, sorted_row_weight, pos);
+                          static_cast<int>(m_blocks), sorted_token_idx, sorted_row_weight, pos, ready);
     }
     const int64_t n_chunks = n_pairs > 0 ? (n_pairs + CHUNK - 1) / CHUNK : 0;
     int32_t *hist = static_cast<int32_t *>(scratch);
@@ -305,7 +307,7 @@ cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_
     cudaError_t e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(SCAN_THREADS), 0, stream, hist,
                                static_cast<int>(n_chunks), static_cast<int>(E),
                                static_cast<int>(block_m), sizes, offsets, padded, gidx,
-                               static_cast<int>(m_blocks));
+                               static_cast<int>(m_blocks), ready);
     if (e != cudaSuccess || n_chunks == 0) return e;
     const size_t smem = static_cast<size_t>(DS_WARPS) * E * 4;
     static size_t attr_bytes[64] = {0};
@@ -378,7 +380,7 @@ extern "C" MOE_API moe_status_t moe_build_dispatch_noalloc(
     cudaError_t e = moe::launch_dispatch(topk_idx, topk_w, T, k, E, block_m, group_sizes,
                                          group_offsets, group_padded_offsets, group_idx_for_bx,
                                          m_blocks, sorted_token_idx, sorted_row_weight,
-                                         token_topk_to_pos, scratch,
+                                         token_topk_to_pos, scratch, nullptr,
                                          reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

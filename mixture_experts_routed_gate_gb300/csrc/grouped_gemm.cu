@@ -25,7 +25,17 @@
 // Tiles are (M block, N tile) pairs; the blocks are ordered by the schedule
 // below (full and partial blocks interleaved; blocks with no valid rows, the
 // padding blocks the tables create, left out) and dealt round-robin to the
-// CTAs.  Every wait is bounded (see
+// CTAs.
+//
+// The expert MLP mode runs both stages in one launch: the stage-1 tiles come
+// first in the tile order, then the stage-2 tiles in the same block order.
+// Each epilogue warp that stores part of a block's h publishes it on a
+// per-block counter; the producer starts a stage-2 tile once its block's
+// counter is complete.  A CTA's stage-1 tiles all precede its stage-2 tiles
+// and every CTA of the grid is resident (one per SM), so every wait ends.
+// Both stages then share one wave tail and no launch gap separates them.
+//
+// Every wait is bounded (see
 // mbar_wait_bounded): on a timeout the kernel records kErrTimeout, drains the
 // copies and MMAs it issued, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -57,24 +67,33 @@ constexpr int MAX_SCHED = 2048;  // M blocks the in-kernel schedule can order
 constexpr int SCHED_BYTES = MAX_SCHED * 4 + MAX_SCHED * 4 + 2 * MAX_SCHED * 2 + MAX_SCHED + 64;
 constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES + SCHED_BYTES;
 
+enum { MODE_GATE_UP = 0, MODE_DOWN = 1, MODE_MLP = 2 };
+
+struct PhaseParams {
+    void *out;     // h (stage 1) or y (stage 2), row-major [rows, N]
+    int n_tiles;   // output tiles per M block
+    int k_blocks;  // 64-wide K steps
+    int N;         // output columns
+};
+
 struct GemmParams {
     const int32_t *sizes;
     const int32_t *offsets;
     const int32_t *padded;
     const int32_t *gidx;
     const float *row_weights;
-    void *out;
+    int *ready;  // MODE_MLP: per M block, stage-1 epilogue warp-tiles stored
+    PhaseParams ph[2];  // [0] stage 1 (gate/up), [1] stage 2 (down)
     int m_blocks;
-    int n_tiles;
-    int k_blocks;
-    int N;  // output columns
     int *err;
 };
 
 struct TileInfo {
-    int g, m_start, rows, n0;
+    int g, m_start, rows, n0, bx, phase;
     bool big;  // part of a large expert's stripe-major run
 };
+
+constexpr int EPI_WARPS = 4;
 
 // Valid rows of M block bx (the pages' actual_rows) and its first row.
 __device__ __forceinline__ int block_rows(const GemmParams &p, int bx, int *g_out, int *m_start) {
@@ -105,34 +124,63 @@ struct Schedule {
 };
 
 __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const Schedule &sc, int tile,
-                                              int out_n) {
+                                              int n_tiles, int out_n) {
     int bx, nt;
     bool tile_is_big = false;
     if (sc.list) {
-        const int64_t n_full_t = static_cast<int64_t>(sc.n_full) * p.n_tiles;
-        const int64_t n_all_t = static_cast<int64_t>(sc.n_blocks) * p.n_tiles;
+        const int64_t n_full_t = static_cast<int64_t>(sc.n_full) * n_tiles;
+        const int64_t n_all_t = static_cast<int64_t>(sc.n_blocks) * n_tiles;
         const int64_t hb = tile * n_full_t / n_all_t;         // full tiles before position tile
         const int64_t hn = (tile + 1) * n_full_t / n_all_t;
         if (hn > hb) {
             tile_is_big = true;
-            const int fb = static_cast<int>(hb / p.n_tiles);  // full block whose run holds it
+            const int fb = static_cast<int>(hb / n_tiles);  // full block whose run holds it
             const int rs = sc.run_start[fb], rl = sc.run_len[fb];
-            const int64_t o = hb - static_cast<int64_t>(rs) * p.n_tiles;
+            const int64_t o = hb - static_cast<int64_t>(rs) * n_tiles;
             nt = static_cast<int>(o / rl);
             bx = sc.list[rs + static_cast<int>(o - static_cast<int64_t>(nt) * rl)];
         } else {
             const int64_t lt = tile - hb;                     // partial tile index
-            bx = sc.list[sc.n_full + static_cast<int>(lt / p.n_tiles)];
-            nt = static_cast<int>(lt % p.n_tiles);
+            bx = sc.list[sc.n_full + static_cast<int>(lt / n_tiles)];
+            nt = static_cast<int>(lt % n_tiles);
         }
     } else {
-        bx = tile / p.n_tiles;
-        nt = tile - bx * p.n_tiles;
+        bx = tile / n_tiles;
+        nt = tile - bx * n_tiles;
     }
     TileInfo t;
     t.rows = block_rows(p, bx, &t.g, &t.m_start);
     t.n0 = nt * out_n;
+    t.bx = bx;
+    t.phase = 0;
     t.big = sc.list != nullptr && tile_is_big;
+    return t;
+}
+
+// The parameters of stage `phase` (field by field: indexing the kernel
+// parameter array with a run-time index would copy it to local memory).
+__device__ __forceinline__ PhaseParams phase_params_of(const GemmParams &p, int phase) {
+    PhaseParams r;
+    r.out = phase == 0 ? p.ph[0].out : p.ph[1].out;
+    r.n_tiles = phase == 0 ? p.ph[0].n_tiles : p.ph[1].n_tiles;
+    r.k_blocks = phase == 0 ? p.ph[0].k_blocks : p.ph[1].k_blocks;
+    r.N = phase == 0 ? p.ph[0].N : p.ph[1].N;
+    return r;
+}
+
+// Tile `tile` of the launch: its stage and its place in that stage's order.
+// n0_tiles = stage-1 tiles of the launch (MODE_MLP only).
+template <int MODE>
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, const Schedule &sc, int tile,
+                                                int n0_tiles) {
+    int phase = MODE == MODE_DOWN ? 1 : 0;
+    if (MODE == MODE_MLP && tile >= n0_tiles) {
+        phase = 1;
+        tile -= n0_tiles;
+    }
+    TileInfo t = tile_info(p, sc, tile, phase == 0 ? p.ph[0].n_tiles : p.ph[1].n_tiles,
+                           phase == 0 ? 128 : 256);
+    t.phase = phase;
     return t;
 }
 
@@ -169,12 +217,26 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
     }
 }
 
-template <int DT, bool GATE_UP>
+// An epilogue warp has stored its part of a stage-1 tile: make the stores
+// visible at gpu scope (and to the async proxy that TMA reads through), then
+// count the warp-tile on the block's counter.
+__device__ __forceinline__ void publish_h(int *ctr, int lane) {
+    __threadfence();
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) counter_publish(ctr);
+}
+
+// Stage 1 reads rows A through tmA0 and W_gate / W_up through tmB0 / tmB1;
+// stage 2 reads h through tmA1 and W_down through tmB2.
+template <int DT, int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmB0,
-                        const __grid_constant__ CUtensorMap tmB1, const GemmParams p) {
-    constexpr int OUT_N = GATE_UP ? 128 : 256;  // output columns per tile
+                        const __grid_constant__ CUtensorMap tmB1,
+                        const __grid_constant__ CUtensorMap tmA1,
+                        const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
+    constexpr bool HAS0 = MODE != MODE_DOWN, HAS1 = MODE != MODE_GATE_UP;
     constexpr uint32_t IDESC = idesc_f16(DT == kBF16, BM, MMA_N);
     using OutT = typename Elem<DT>::T;
 
@@ -212,9 +274,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB0);
-        if (GATE_UP) tma_prefetch_desc(&tmB1);
+        if (HAS0) {
+            tma_prefetch_desc(&tmA0);
+            tma_prefetch_desc(&tmB0);
+            tma_prefetch_desc(&tmB1);
+        }
+        if (HAS1) {
+            tma_prefetch_desc(&tmA1);
+            tma_prefetch_desc(&tmB2);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -273,7 +341,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = sc.n_blocks * p.n_tiles;
+    const int n0_tiles = HAS0 ? sc.n_blocks * p.ph[0].n_tiles : 0;
+    const int total = n0_tiles + (HAS1 ? sc.n_blocks * p.ph[1].n_tiles : 0);
 
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
@@ -285,9 +354,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             long issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-                const TileInfo ti = tile_info(p, sc, tile, OUT_N);
+                const TileInfo ti = decode_tile<MODE>(p, sc, tile, n0_tiles);
                 if (ti.rows == 0) continue;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                // a stage-2 tile reads h rows of its block: wait until every
+                // stage-1 epilogue warp-tile of the block has stored them
+                if (MODE == MODE_MLP && ti.phase == 1 &&
+                    !counter_wait_bounded(p.ready + ti.bx, EPI_WARPS * p.ph[0].n_tiles, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                const int kblocks = phase_params_of(p, ti.phase).k_blocks;
+                for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
                         ok = false;
                         break;
@@ -299,14 +376,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // a large expert's rows and weight stripes are reused by the
                     // tiles of its run: keep them; a small expert's weights are
                     // read by one block only: let them leave L2 first
-                    if (ti.big) tma_load_2d_hint(a_dst, &tmA, fb, kb * BK, ti.m_start, pol_last);
-                    else tma_load_2d(a_dst, &tmA, fb, kb * BK, ti.m_start);
+                    const CUtensorMap *ta = HAS0 && ti.phase == 0 ? &tmA0 : &tmA1;
+                    if (ti.big) tma_load_2d_hint(a_dst, ta, fb, kb * BK, ti.m_start, pol_last);
+                    else tma_load_2d(a_dst, ta, fb, kb * BK, ti.m_start);
                     const uint64_t polb = ti.big ? pol_last : pol_first;
-                    if (GATE_UP) {
+                    if (HAS0 && ti.phase == 0) {
                         tma_load_3d_hint(b_dst, &tmB0, fb, kb * BK, ti.n0, ti.g, polb);
                         tma_load_3d_hint(b_dst + B_BYTES / 2, &tmB1, fb, kb * BK, ti.n0, ti.g, polb);
                     } else {
-                        tma_load_3d_hint(b_dst, &tmB0, fb, kb * BK, ti.n0, ti.g, polb);
+                        tma_load_3d_hint(b_dst, &tmB2, fb, kb * BK, ti.n0, ti.g, polb);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -334,8 +412,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t last_bar = 0, last_parity = 0;
             bool committed = false;
             for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-                const TileInfo ti = tile_info(p, sc, tile, OUT_N);
+                const TileInfo ti = decode_tile<MODE>(p, sc, tile, n0_tiles);
                 if (ti.rows == 0) continue;
+                const int kblocks = phase_params_of(p, ti.phase).k_blocks;
                 const int acc = local & 1;
                 const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
                 if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) {
@@ -347,7 +426,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const bool swap = ti.rows <= SWAP_MAX_ROWS;
                 const int np = (ti.rows + 15) & ~15;
                 const uint32_t idesc_sw = idesc_f16(DT == kBF16, BM, static_cast<uint32_t>(np));
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.err)) {
                         ok = false;
                         break;
@@ -395,8 +474,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row = q * 32 + lane;
         int local = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            const TileInfo ti = tile_info(p, sc, tile, OUT_N);
+            const TileInfo ti = decode_tile<MODE>(p, sc, tile, n0_tiles);
             if (ti.rows == 0) continue;
+            const bool gu = HAS0 && ti.phase == 0;  // stage 1: silu(gate) * up
+            const int out_cols = gu ? 128 : 256;
+            const PhaseParams php = phase_params_of(p, ti.phase);
+            const int N = php.N;
+            OutT *const out_base = reinterpret_cast<OutT *>(php.out);
             const int acc = local & 1;
             const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
             // one lane waits, the warp reconverges before the .sync.aligned TMEM loads
@@ -411,9 +495,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // swapped tile: this thread holds output feature `row` (and, for
                 // stage 2, feature 128 + row) for every row j of the block
                 const int np = (ti.rows + 15) & ~15;
-                OutT *out = reinterpret_cast<OutT *>(p.out);
+                OutT *out = out_base;
                 const int f0 = ti.n0 + row;
-                const int f1 = GATE_UP ? -1 : ti.n0 + 128 + row;
+                const int f1 = gu ? -1 : ti.n0 + 128 + row;
 #pragma unroll 1
                 for (int j0 = 0; j0 < np; j0 += 16) {
                     uint32_t a[16], b[16];
@@ -424,15 +508,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int jj = 0; jj < 16; ++jj) {
                         const int j = j0 + jj;
                         if (j < ti.rows) {
-                            const int64_t r = static_cast<int64_t>(ti.m_start + j) * p.N;
-                            if (GATE_UP) {
+                            const int64_t r = static_cast<int64_t>(ti.m_start + j) * N;
+                            if (gu) {
                                 const float gv = __uint_as_float(a[jj]);
                                 const float s = gv * __frcp_rn(1.0f + __expf(-gv));
-                                if (f0 < p.N) out[r + f0] = from_f32<OutT>(s * __uint_as_float(b[jj]));
+                                if (f0 < N) out[r + f0] = from_f32<OutT>(s * __uint_as_float(b[jj]));
                             } else {
                                 const float rwj = p.row_weights ? __ldg(p.row_weights + ti.m_start + j) : 1.0f;
-                                if (f0 < p.N) out[r + f0] = from_f32<OutT>(__uint_as_float(a[jj]) * rwj);
-                                if (f1 < p.N) out[r + f1] = from_f32<OutT>(__uint_as_float(b[jj]) * rwj);
+                                if (f0 < N) out[r + f0] = from_f32<OutT>(__uint_as_float(a[jj]) * rwj);
+                                if (f1 < N) out[r + f1] = from_f32<OutT>(__uint_as_float(b[jj]) * rwj);
                             }
                         }
                     }
@@ -440,19 +524,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty_bar(acc));
+                if (MODE == MODE_MLP && gu) publish_h(p.ready + ti.bx, lane);
                 ++local;
                 continue;
             }
             const bool valid = row < ti.rows;
-            OutT *out_row = reinterpret_cast<OutT *>(p.out) +
-                            static_cast<int64_t>(ti.m_start + (valid ? row : 0)) * p.N;
+            OutT *out_row = out_base + static_cast<int64_t>(ti.m_start + (valid ? row : 0)) * N;
             float rw = 1.0f;
-            if (!GATE_UP && p.row_weights != nullptr && valid) rw = __ldg(p.row_weights + ti.m_start + row);
+            if (!gu && p.row_weights != nullptr && valid) rw = __ldg(p.row_weights + ti.m_start + row);
 #pragma unroll 1
-            for (int c = 0; c < OUT_N / 16; ++c) {
+            for (int c = 0; c < out_cols / 16; ++c) {
                 const int col = ti.n0 + c * 16;
                 uint32_t packed[8];
-                if (GATE_UP) {
+                if (gu) {
                     uint32_t g[16], u[16];
                     tmem_ld16(t_row + c * 16, g);
                     tmem_ld16(t_row + 128 + c * 16, u);
@@ -478,7 +562,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         packed[i] = pack2<DT>(__uint_as_float(r[2 * i]) * rw,
                                               __uint_as_float(r[2 * i + 1]) * rw);
                 }
-                if (valid && col < p.N) {
+                if (valid && col < N) {
                     uint4 *dst = reinterpret_cast<uint4 *>(out_row + col);
                     dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
                     dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
@@ -487,6 +571,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (MODE == MODE_MLP && gu) publish_h(p.ready + ti.bx, lane);
             ++local;
         }
     }
@@ -563,10 +648,9 @@ bool make_map_3d(CUtensorMap *m, int dtype, const void *ptr, uint64_t K, uint64_
     return r == CUDA_SUCCESS;
 }
 
-template <int DT, bool GATE_UP>
-cudaError_t launch_typed(const CUtensorMap &ta, const CUtensorMap &tb0, const CUtensorMap &tb1,
-                         const GemmParams &p, int grid, cudaStream_t stream) {
-    auto kern = grouped_gemm_kernel<DT, GATE_UP>;
+template <int DT, int MODE>
+cudaError_t launch_typed(const CUtensorMap *maps, const GemmParams &p, int grid, cudaStream_t stream) {
+    auto kern = grouped_gemm_kernel<DT, MODE>;
     // the shared-memory opt-in is set once per device (cheap launches, and no
     // attribute call while a graph is being captured after the first use)
     static bool attr_done[64] = {false};
@@ -577,7 +661,57 @@ cudaError_t launch_typed(const CUtensorMap &ta, const CUtensorMap &tb0, const CU
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
-    return launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, ta, tb0, tb1, p);
+    return launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, maps[0], maps[1],
+                      maps[2], maps[3], maps[4], p);
+}
+
+template <int MODE>
+cudaError_t launch_mode(int dtype, const CUtensorMap *maps, const GemmParams &p, int64_t tiles,
+                        cudaStream_t stream) {
+    const int grid = static_cast<int>(tiles < device_sm_count() ? tiles : device_sm_count());
+    if (dtype == kBF16) return launch_typed<kBF16, MODE>(maps, p, grid, stream);
+    return launch_typed<kF16, MODE>(maps, p, grid, stream);
+}
+
+GemmParams base_params(const int32_t *sizes, const int32_t *offsets, const int32_t *padded,
+                       const int32_t *gidx, int64_t m_blocks, const float *row_weights, int32_t *err) {
+    GemmParams p{};
+    p.sizes = sizes;
+    p.offsets = offsets;
+    p.padded = padded;
+    p.gidx = gidx;
+    p.row_weights = row_weights;
+    p.ready = nullptr;
+    p.m_blocks = static_cast<int>(m_blocks);
+    p.err = err;
+    return p;
+}
+
+PhaseParams phase_params(void *out, int64_t K, int64_t N, int out_n) {
+    PhaseParams ph;
+    ph.out = out;
+    ph.n_tiles = static_cast<int>((N + out_n - 1) / out_n);
+    ph.k_blocks = static_cast<int>((K + BK - 1) / BK);
+    ph.N = static_cast<int>(N);
+    return ph;
+}
+
+// Stage-1 maps into maps[0..2]: rows [n_rows, d_h], W_gate / W_up [E, d_e, d_h].
+bool stage1_maps(CUtensorMap *maps, int dtype, const void *a, const void *w_gate, const void *w_up,
+                 int64_t n_rows, int64_t d_h, int64_t d_e, int64_t E) {
+    return make_map_2d(&maps[0], dtype, a, static_cast<uint64_t>(d_h), static_cast<uint64_t>(n_rows), BM) &&
+           make_map_3d(&maps[1], dtype, w_gate, static_cast<uint64_t>(d_h), static_cast<uint64_t>(d_e),
+                       static_cast<uint64_t>(E), 128u) &&
+           make_map_3d(&maps[2], dtype, w_up, static_cast<uint64_t>(d_h), static_cast<uint64_t>(d_e),
+                       static_cast<uint64_t>(E), 128u);
+}
+
+// Stage-2 maps into maps[3..4]: h [n_rows, d_e], W_down [E, d_h, d_e].
+bool stage2_maps(CUtensorMap *maps, int dtype, const void *h, const void *w_down, int64_t n_rows,
+                 int64_t d_h, int64_t d_e, int64_t E) {
+    return make_map_2d(&maps[3], dtype, h, static_cast<uint64_t>(d_e), static_cast<uint64_t>(n_rows), BM) &&
+           make_map_3d(&maps[4], dtype, w_down, static_cast<uint64_t>(d_e), static_cast<uint64_t>(d_h),
+                       static_cast<uint64_t>(E), 256u);
 }
 
 }  // namespace
@@ -588,39 +722,43 @@ cudaError_t launch_grouped_gemm(bool gate_up, int dtype, const void *a, const vo
                                 const float *row_weights, int64_t n_rows, int64_t K, int64_t N,
                                 int64_t E, void *out, int32_t *err, cudaStream_t stream) {
     if (n_rows <= 0 || m_blocks <= 0) return cudaSuccess;
-    const int out_n = gate_up ? 128 : 256;
-    CUtensorMap ta, tb0, tb1;
-    if (!make_map_2d(&ta, dtype, a, static_cast<uint64_t>(K), static_cast<uint64_t>(n_rows), BM))
-        return cudaErrorInvalidValue;
-    if (!make_map_3d(&tb0, dtype, w0, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
-                     static_cast<uint64_t>(E), gate_up ? 128u : 256u))
-        return cudaErrorInvalidValue;
+    CUtensorMap maps[5];
+    GemmParams p = base_params(sizes, offsets, padded, gidx, m_blocks, row_weights, err);
     if (gate_up) {
-        if (!make_map_3d(&tb1, dtype, w1, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
-                         static_cast<uint64_t>(E), 128u))
-            return cudaErrorInvalidValue;
-    } else {
-        tb1 = tb0;
+        // stage 1: K = d_h, N = d_e
+        if (!stage1_maps(maps, dtype, a, w0, w1, n_rows, K, N, E)) return cudaErrorInvalidValue;
+        maps[3] = maps[0];
+        maps[4] = maps[1];
+        p.ph[0] = phase_params(out, K, N, 128);
+        p.ph[1] = p.ph[0];
+        return launch_mode<MODE_GATE_UP>(dtype, maps, p, m_blocks * p.ph[0].n_tiles, stream);
     }
-    GemmParams p;
-    p.sizes = sizes;
-    p.offsets = offsets;
-    p.padded = padded;
-    p.gidx = gidx;
-    p.row_weights = row_weights;
-    p.out = out;
-    p.m_blocks = static_cast<int>(m_blocks);
-    p.n_tiles = static_cast<int>((N + out_n - 1) / out_n);
-    p.k_blocks = static_cast<int>((K + BK - 1) / BK);
-    p.N = static_cast<int>(N);
-    p.err = err;
-    const int64_t total = m_blocks * p.n_tiles;
-    const int grid = static_cast<int>(total < device_sm_count() ? total : device_sm_count());
-    if (dtype == kBF16)
-        return gate_up ? launch_typed<kBF16, true>(ta, tb0, tb1, p, grid, stream)
-                       : launch_typed<kBF16, false>(ta, tb0, tb1, p, grid, stream);
-    return gate_up ? launch_typed<kF16, true>(ta, tb0, tb1, p, grid, stream)
-                   : launch_typed<kF16, false>(ta, tb0, tb1, p, grid, stream);
+    // stage 2: K = d_e, N = d_h
+    if (!stage2_maps(maps, dtype, a, w0, n_rows, N, K, E)) return cudaErrorInvalidValue;
+    maps[0] = maps[3];
+    maps[1] = maps[4];
+    maps[2] = maps[4];
+    p.ph[1] = phase_params(out, K, N, 256);
+    p.ph[0] = p.ph[1];
+    return launch_mode<MODE_DOWN>(dtype, maps, p, m_blocks * p.ph[1].n_tiles, stream);
+}
+
+cudaError_t launch_grouped_mlp(int dtype, const void *a, const void *w_gate, const void *w_up,
+                               const void *w_down, const int32_t *sizes, const int32_t *offsets,
+                               const int32_t *padded, const int32_t *gidx, int64_t m_blocks,
+                               const float *row_weights, int64_t n_rows, int64_t d_h, int64_t d_e,
+                               int64_t E, void *h, void *y, int32_t *ready, int32_t *err,
+                               cudaStream_t stream) {
+    if (n_rows <= 0 || m_blocks <= 0) return cudaSuccess;
+    CUtensorMap maps[5];
+    if (!stage1_maps(maps, dtype, a, w_gate, w_up, n_rows, d_h, d_e, E) ||
+        !stage2_maps(maps, dtype, h, w_down, n_rows, d_h, d_e, E))
+        return cudaErrorInvalidValue;
+    GemmParams p = base_params(sizes, offsets, padded, gidx, m_blocks, row_weights, err);
+    p.ready = ready;
+    p.ph[0] = phase_params(h, d_h, d_e, 128);
+    p.ph[1] = phase_params(y, d_e, d_h, 256);
+    return launch_mode<MODE_MLP>(dtype, maps, p, m_blocks * (p.ph[0].n_tiles + p.ph[1].n_tiles), stream);
 }
 
 }  // namespace moe

@@ -28,7 +28,7 @@ cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_
                             int64_t E, int64_t block_m, int32_t *sizes, int32_t *offsets, int32_t *padded,
                             int32_t *gidx, int64_t m_blocks, int32_t *sorted_token_idx,
                             float *sorted_row_weight, int32_t *pos, void *scratch,
-                            cudaStream_t stream);
+                            int32_t *ready, cudaStream_t stream);
 
 // rows.cu
 cudaError_t launch_gather_rows(const void *x, const int32_t *sorted_token_idx, int64_t n_rows,
@@ -44,5 +44,13 @@ cudaError_t launch_grouped_gemm(bool gate_up, int dtype, const void *a, const vo
                                 const int32_t *padded, const int32_t *gidx, int64_t m_blocks,
                                 const float *row_weights, int64_t n_rows, int64_t K, int64_t N,
                                 int64_t E, void *out, int32_t *err, cudaStream_t stream);
+// Stage 1 and stage 2 in one persistent launch; `ready` (m_blocks int32) must
+// be zero when the kernel starts.
+cudaError_t launch_grouped_mlp(int dtype, const void *a, const void *w_gate, const void *w_up,
+                               const void *w_down, const int32_t *sizes, const int32_t *offsets,
+                               const int32_t *padded, const int32_t *gidx, int64_t m_blocks,
+                               const float *row_weights, int64_t n_rows, int64_t d_h, int64_t d_e,
+                               int64_t E, void *h, void *y, int32_t *ready, int32_t *err,
+                               cudaStream_t stream);
 
 }  // namespace moe

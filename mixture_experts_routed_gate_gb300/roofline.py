@@ -44,6 +44,16 @@ def down_bytes(n_rows: int, d_h: int, d_e: int, active_experts: int, e: int) -> 
     return active_experts * d_h * d_e * e + n_rows * d_e * e + n_rows * d_h * e
 
 
+def expert_mlp_bytes(n_rows: int, d_h: int, d_e: int, active_experts: int, e: int) -> int:
+    """Both stages in one launch: the three weight matrices of every active
+    expert, the gathered rows read, h written and read back, y written."""
+    return gate_up_bytes(n_rows, d_h, d_e, active_experts, e) + down_bytes(n_rows, d_h, d_e, active_experts, e)
+
+
+def expert_mlp_flops(n_rows: int, d_h: int, d_e: int) -> int:
+    return gate_up_flops(n_rows, d_h, d_e) + down_flops(n_rows, d_h, d_e)
+
+
 def gate_flops(T: int, d_h: int, E: int) -> int:
     return 2 * T * E * d_h
 

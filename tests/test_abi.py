@@ -50,9 +50,11 @@ def test_sizing_helpers(lib, oracle):
     # the gathered rows, h and y dominate: Tk*(2*d_h + d_e)*2 bytes
     assert ws >= 32768 * (2 * 7168 + 2048) * 2
     assert ws % 256 == 0
-    offs = [lib.moe_forward_workspace_offset(4096, 7168, 2048, 256, 8, 1, i) for i in range(14)]
+    offs = [lib.moe_forward_workspace_offset(4096, 7168, 2048, 256, 8, 1, i) for i in range(15)]
     assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
-    assert lib.moe_forward_workspace_offset(4096, 7168, 2048, 256, 8, 1, 14) == -1
+    # the last section holds one int32 counter per M block
+    assert ws - offs[14] >= 512 * 4
+    assert lib.moe_forward_workspace_offset(4096, 7168, 2048, 256, 8, 1, 15) == -1
 
 
 def test_status_strings(lib):
@@ -88,6 +90,11 @@ def test_argument_errors_without_launch(lib):
                                         fake, None, None) == MOE_ERR_INVALID_ARG
     assert lib.moe_grouped_down(fake, fake, fake, fake, fake, fake, 99, None, 8, 256, 128, 8, 1,
                                 fake, None, None) == MOE_ERR_INVALID_ARG
+    # expert MLP in one launch: no counter buffer, misaligned d_expert
+    assert lib.moe_grouped_mlp(fake, fake, fake, fake, fake, fake, fake, fake, 3, None, 8, 256, 128, 8, 1,
+                               fake, fake, None, None, None) == MOE_ERR_INVALID_ARG
+    assert lib.moe_grouped_mlp(fake, fake, fake, fake, fake, fake, fake, fake, 3, None, 8, 256, 100, 8, 1,
+                               fake, fake, fake, None, None) == MOE_ERR_INVALID_ARG
     # forward: workspace too small, misaligned workspace
     assert lib.moe_forward(fake, fake, None, fake, fake, fake, 64, 256, 128, 8, 2, 0, P(0x100000), 16,
                            fake, None, None) == MOE_ERR_WORKSPACE

@@ -129,3 +129,99 @@ def test_grouped_gemm_rows_outside_the_tables_untouched(oracle):
     torch.cuda.synchronize()
     assert (h[n:].float() == 7.0).all()
     assert not (h[:n].float() == 7.0).all(dim=1).any()
+
+
+def _mlp_inputs(dtype, T, k, E, d_h, d_e, skew, seed, dev):
+    rng = np.random.default_rng(seed)
+    idx = _routing(rng, T, k, E, skew)
+    td = workloads.torch_dtype(dtype)
+    x = torch.randn((T, d_h), generator=torch.Generator().manual_seed(seed + 1)).to(td)
+    w_gate = (torch.randn((E, d_e, d_h), generator=torch.Generator().manual_seed(seed + 2)) / d_h ** 0.5).to(td)
+    w_up = (torch.randn((E, d_e, d_h), generator=torch.Generator().manual_seed(seed + 3)) / d_h ** 0.5).to(td)
+    w_down = (torch.randn((E, d_h, d_e), generator=torch.Generator().manual_seed(seed + 4)) / d_e ** 0.5).to(td)
+    return idx, x, w_gate.to(dev), w_up.to(dev), w_down.to(dev), rng
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("T,k,E,d_h,d_e,skew", [(300, 4, 6, 512, 256, False),
+                                                (200, 8, 32, 256, 192, True),
+                                                (1, 1, 4, 256, 64, False),
+                                                (1024, 2, 4, 512, 256, False),
+                                                (64, 6, 64, 512, 256, False)])
+def test_grouped_mlp_equals_two_stages(oracle, dtype, T, k, E, d_h, d_e, skew):
+    """Both stages in one launch give bit for bit the h and y of the two
+    separate launches (same tiles, same MMA order), and agree with the oracle.
+    Covers large experts (stripe-major runs, 512 rows each), mostly-padding
+    blocks (swapped MMA), a partial last N tile and a single row."""
+    dev = require_cuda()
+    idx, x, wg, wu, wd, rng = _mlp_inputs(dtype, T, k, E, d_h, d_e, skew, T + E, dev)
+    tab = oracle.build_dispatch(idx, None, E, 128)
+    a = oracle.gather_rows(bits(x), tab["sorted_token_idx"], dtype)
+    tabd = _tables_to(dev, tab)
+    a_d = _from_bits(a, dtype, dev)
+    rw = torch.from_numpy(rng.random(T * k).astype(np.float32)).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    h2 = binding.moe_grouped_gate_up_silu(a_d, wg, wu, tabd, err=err)
+    y2 = binding.moe_grouped_down(h2, wd, tabd, err=err)
+    yw2 = binding.moe_grouped_down(h2, wd, tabd, row_weights=rw, err=err)
+    h1, y1 = binding.moe_grouped_mlp(a_d, wg, wu, wd, tabd, err=err)
+    _, yw1 = binding.moe_grouped_mlp(a_d, wg, wu, wd, tabd, row_weights=rw, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_bits_equal(bits(h1), bits(h2), "fused h")
+    assert_bits_equal(bits(y1), bits(y2), "fused y")
+    assert_bits_equal(bits(yw1), bits(yw2), "fused y with row weights")
+    h_ref = oracle.grouped_gate_up_silu(a, bits(wg.cpu()), bits(wu.cpu()), tab, dtype)
+    y_ref = oracle.grouped_down(bits(h1), bits(wd.cpu()), tab, dtype)
+    rtol, atol = MOE_TOL[dtype]
+    assert_close(bits(h1), h_ref, dtype, rtol, atol, "fused h vs oracle")
+    assert_close(bits(y1), y_ref, dtype, rtol, atol, "fused y vs oracle (from the kernel's h)")
+
+
+def test_grouped_mlp_repeated_calls_share_counters(oracle):
+    """The per-block counters are cleared by every call: ten calls on one
+    counter buffer give the same bits and no error."""
+    dev = require_cuda()
+    idx, x, wg, wu, wd, _ = _mlp_inputs("bf16", 300, 4, 6, 512, 256, False, 21, dev)
+    tab = oracle.build_dispatch(idx, None, 6, 128)
+    tabd = _tables_to(dev, tab)
+    a_d = _from_bits(oracle.gather_rows(bits(x), tab["sorted_token_idx"], "bf16"), "bf16", dev)
+    ready = torch.full((tabd["group_idx_for_bx"].numel(),), 12345, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    _, y0 = binding.moe_grouped_mlp(a_d, wg, wu, wd, tabd, ready=ready, err=err)
+    ys = [binding.moe_grouped_mlp(a_d, wg, wu, wd, tabd, ready=ready, err=err)[1] for _ in range(10)]
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for y in ys:
+        assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+
+
+def test_grouped_mlp_beyond_the_schedule_table(oracle):
+    """More M blocks than the in-kernel schedule orders (2048): tiles run in
+    natural block order, padding blocks skipped; sampled rows vs the oracle
+    and the fused launch bit-equal to the two separate ones."""
+    dev = require_cuda()
+    T, k, E, d_h, d_e = 16640, 8, 1024, 256, 64  # 1040 + 1024 = 2064 M blocks
+    idx, x, wg, wu, wd, rng = _mlp_inputs("f16", T, k, E, d_h, d_e, False, 31, dev)
+    tab = oracle.build_dispatch(idx, None, E, 128)
+    assert len(tab["group_idx_for_bx"]) > 2048
+    tabd = _tables_to(dev, tab)
+    a = oracle.gather_rows(bits(x), tab["sorted_token_idx"], "f16")
+    a_d = _from_bits(a, "f16", dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    h2 = binding.moe_grouped_gate_up_silu(a_d, wg, wu, tabd, err=err)
+    y2 = binding.moe_grouped_down(h2, wd, tabd, err=err)
+    h1, y1 = binding.moe_grouped_mlp(a_d, wg, wu, wd, tabd, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_bits_equal(bits(h1), bits(h2), "fused h")
+    assert_bits_equal(bits(y1), bits(y2), "fused y")
+    sizes, offs = tab["group_sizes"], tab["group_offsets"]
+    row_expert = np.repeat(np.arange(E, dtype=np.int32), sizes)
+    rows = rng.choice(T * k, size=96, replace=False)
+    h_ref = oracle.rows_gate_up_silu(a[rows], row_expert[rows], bits(wg.cpu()), bits(wu.cpu()), "f16")
+    y_ref = oracle.rows_down(bits(h1)[rows], row_expert[rows], bits(wd.cpu()), "f16")
+    rtol, atol = MOE_TOL["f16"]
+    assert_close(bits(h1)[rows], h_ref, "f16", rtol, atol, "sampled h")
+    assert_close(bits(y1)[rows], y_ref, "f16", rtol, atol, "sampled y")
+    assert offs[-1] + sizes[-1] == T * k
