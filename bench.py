@@ -391,8 +391,10 @@ def measure_e2e(args, cfg, d, dev, flush, world):
 
 
 def measure_reduce_aux(dev, flush, reps: int = 20):
-    """moe_reduce_fused alone on the bf16 T x 8 x 7168 workloads (GB/s), and
-    its scaled variants at T = 512 (x_sf; e4m3 output; sf + e4m3 output)."""
+    """moe_reduce_fused alone on the bf16 T x 8 x 7168 workloads (GB/s): one
+    launch per timed region after an L2 eviction (the pages' protocol), and
+    launches back to back on rotating cold inputs; the scaled variants at
+    T = 512 (x_sf; e4m3 output; sf + e4m3 output)."""
     from mixture_experts_routed_gate_gb300 import binding
 
     def time_it(fn):
@@ -409,6 +411,32 @@ def measure_reduce_aux(dev, flush, reps: int = 20):
             ts.append(s_.elapsed_time(e_))
         return statistics.median(ts)
 
+    def streamed(c, n_sets, launches):
+        """Launches back to back in one CUDA graph, each on the next of n_sets
+        input sets (together several times the L2), so every launch reads cold
+        rows; per-launch time = replay time / launches."""
+        sets = [workloads.make_reduce_inputs(c.T, c.K, c.H, c.dtype, c.seed + i, device=dev)
+                for i in range(n_sets)]
+        outs = [torch.empty((c.T, c.H), dtype=torch.bfloat16, device=dev) for _ in range(n_sets)]
+        nb = sum(roofline.reduce_bytes(int((r["pos"] >= 0).sum().item()), c.T, c.K, c.H, 2, 2)
+                 for r in sets) / n_sets
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for i in range(n_sets):  # first use outside the capture (attributes, lazy init)
+                binding.moe_reduce_fused(sets[i]["x"], sets[i]["pos"], sets[i]["w"], out=outs[i])
+            side.synchronize()
+            with torch.cuda.graph(g, stream=side):
+                for j in range(launches):
+                    r = sets[j % n_sets]
+                    binding.moe_reduce_fused(r["x"], r["pos"], r["w"], out=outs[j % n_sets])
+        torch.cuda.current_stream(dev).wait_stream(side)
+        ms = time_it(g.replay) / launches
+        del g, sets, outs
+        return {"streamed_us": round(ms * 1e3, 2), "streamed_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
+                "streamed_sets": n_sets, "streamed_launches": launches}
+
     res = {}
     for name in ("reduce-512", "reduce-4096"):
         c = workloads.REDUCE_CONFIGS[name]
@@ -419,6 +447,7 @@ def measure_reduce_aux(dev, flush, reps: int = 20):
         ms = time_it(lambda: binding.moe_reduce_fused(r["x"], r["pos"], r["w"], out=out))
         res[name] = {"us": round(ms * 1e3, 2), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
                      "bytes": nbytes, "bytes_pages_formula": roofline.reduce_bytes_pages(c.T, c.K, c.H, 2)}
+        res[name].update(streamed(c, 8, 32) if c.T <= 512 else streamed(c, 2, 8))
         if name != "reduce-512":
             continue
         out8 = torch.empty((c.T, c.H), dtype=torch.float8_e4m3fn, device=dev)

@@ -31,13 +31,82 @@ namespace {
 
 constexpr int SLICE = 256;                // elements per lane round: 32 lanes x 8
 constexpr int ROW_BYTES = SLICE * 2;      // 512 B of one row per slice
-constexpr int GATE_STAGES = 4;
+// Ring depth: the small-batch shapes keep up to 8 slices (about 200 KB) in
+// flight, since their time is the latency of the first slices; the 16-warp
+// many-token shape keeps 4 (two CTAs per SM).
+__host__ __device__ constexpr int gate_stages(int rows, bool many_tokens) {
+    return many_tokens ? 4 : ((200 * 1024) / (rows * ROW_BYTES) > 8 ? 8 : (200 * 1024) / (rows * ROW_BYTES));
+}
 
-// Warp argmax by (logit desc, id asc) over k rounds, then the softmax weights.
+// Top-k by (logit desc, id asc) and the softmax weights of TOK tokens whose
+// 64 logits per token (E <= 64 valid) sit in shared memory, lsm[TOK][64],
+// with every thread of the CTA taking part (the single-token latency case).
+// Q = NT / (TOK * 64) threads rank one value, each against 64 / Q of the
+// token's values (4-wide shared loads, a short loop), and their counts are
+// added by shuffles; the value of rank r < k is selection slot r.  The
+// softmax denominator is summed by the token's warp as in warp_topk_rounds
+// (per lane: its expert, then expert + 32; then the xor butterfly), so the
+// weights are the same bits either way.  Scratch after lsm: ranks and the
+// top logit per token.
+template <int TOK, int NT>
+__device__ __forceinline__ void cta_topk_softmax(float *lsm, int t0, int T, int E, int k,
+                                                 int32_t *__restrict__ topk_idx,
+                                                 float *__restrict__ topk_w) {
+    constexpr int EXP = 64, Q = NT / (TOK * EXP), PER = EXP / Q;
+    static_assert(Q >= 1 && Q * TOK * EXP == NT && PER % 4 == 0, "ranking shape");
+    int *rank_s = reinterpret_cast<int *>(lsm + TOK * EXP);
+    float *top_s = reinterpret_cast<float *>(rank_s + TOK * EXP);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int vi = tid / Q, part = tid - vi * Q;
+    const int tt = vi / EXP, e = vi - tt * EXP;
+    const float mine = lsm[vi];
+    const float4 *row4 = reinterpret_cast<const float4 *>(lsm + tt * EXP + part * PER);
+    int r = 0;
+#pragma unroll 1
+    for (int q = 0; q < PER / 4; ++q) {
+        const float4 o = row4[q];
+        const int o0 = part * PER + q * 4;
+        r += (o0 < E && (o.x > mine || (o.x == mine && o0 < e))) ? 1 : 0;
+        r += (o0 + 1 < E && (o.y > mine || (o.y == mine && o0 + 1 < e))) ? 1 : 0;
+        r += (o0 + 2 < E && (o.z > mine || (o.z == mine && o0 + 2 < e))) ? 1 : 0;
+        r += (o0 + 3 < E && (o.w > mine || (o.w == mine && o0 + 3 < e))) ? 1 : 0;
+    }
+#pragma unroll
+    for (int sh = 1; sh < Q; sh <<= 1) r += __shfl_xor_sync(0xffffffffu, r, sh);
+    if (part == 0) {
+        rank_s[vi] = r;
+        if (e < E && r == 0) top_s[tt] = mine;
+    }
+    __syncthreads();
+    const int t = t0 + warp;
+    if (warp < TOK && t < T) {
+        const float top = top_s[warp];
+        const float v0 = lsm[warp * EXP + lane], v1 = lsm[warp * EXP + 32 + lane];
+        float sum = 0.0f;
+        if (lane < E) sum += expf(v0 - top);
+        if (32 + lane < E) sum += expf(v1 - top);
+#pragma unroll
+        for (int sh = 16; sh >= 1; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
+        const int r0 = rank_s[warp * EXP + lane], r1 = rank_s[warp * EXP + 32 + lane];
+        int32_t *idx_out = topk_idx + static_cast<int64_t>(t) * k;
+        float *w_out = topk_w + static_cast<int64_t>(t) * k;
+        if (lane < E && r0 < k) {
+            idx_out[r0] = lane;
+            w_out[r0] = expf(v0 - top) / sum;
+        }
+        if (32 + lane < E && r1 < k) {
+            idx_out[r1] = 32 + lane;
+            w_out[r1] = expf(v1 - top) / sum;
+        }
+    }
+}
+
+// Warp argmax by (logit desc, id asc) over k rounds, then the softmax weights
+// (for many experts: k rounds cost less than ranking every value).
 // Lane holds v[s] = logit of expert s*32 + lane (or -inf past E).
 template <int SLOTS>
-__device__ __forceinline__ void warp_topk_softmax(float (&v)[SLOTS], int E, int k, int32_t *idx_out,
-                                                  float *w_out, int lane) {
+__device__ __forceinline__ void warp_topk_rounds(float (&v)[SLOTS], int E, int k, int32_t *idx_out,
+                                                 float *w_out, int lane) {
     bool taken[SLOTS];
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) taken[s] = s * 32 + lane >= E;
@@ -92,6 +161,7 @@ __global__ void __launch_bounds__(WT *WE * 32)
                 float *__restrict__ topk_w) {
     constexpr int TOK = WT * TPW, EXP = WE * 8, ROWS = TOK + EXP;
     constexpr int STAGE_BYTES = ROWS * ROW_BYTES;
+    constexpr int GATE_STAGES = gate_stages(ROWS, WT * WE > 8);
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * TOK, e0 = blockIdx.y * EXP;
@@ -194,51 +264,36 @@ __global__ void __launch_bounds__(WT *WE * 32)
             acc[i][j] = v;
         }
 
+    // every lane now holds all TPW*8 sums; lane L keeps pair L (TPW*8 <= 32)
+    // and writes it: one select chain and one store, compact one-shot code
+    static_assert(TPW * 8 <= 32, "one pair per lane");
+    float mine = 0.0f;
+#pragma unroll
+    for (int i = 0; i < TPW; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mine = (i * 8 + j == lane) ? acc[i][j] : mine;
+    const int my_i = lane >> 3, my_j = lane & 7;
+    const int my_t = t0 + wt + my_i, my_e = e0 + we + my_j;
     if constexpr (!FUSE_TOPK) {
-        // lane L writes pairs L (and L + 32) of the warp's TPW*8
-#pragma unroll
-        for (int i = 0; i < TPW; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (((i * 8 + j) & 31) == lane) {
-                    const int t = t0 + wt + i, e = e0 + we + j;
-                    if (t < T && e < E) {
-                        float l = acc[i][j];
-                        if (bias) l = l + bias[e];
-                        logits[static_cast<int64_t>(t) * E + e] = l;
-                    }
-                }
-            }
+        if (lane < TPW * 8 && my_t < T && my_e < E) {
+            float l = mine;
+            if (bias) l = l + bias[my_e];
+            logits[static_cast<int64_t>(my_t) * E + my_e] = l;
+        }
     } else {
         // one CTA holds every expert of its TOK tokens: logits to shared
         // memory, then warp w selects the top-k of token t0 + w
         static_assert(!FUSE_TOPK || (WT == 1 && EXP == 64 && TPW <= WE), "fused shape");
         __syncthreads();  // the ring is no longer read
         float *lsm = reinterpret_cast<float *>(smem);  // [TOK][EXP]
-#pragma unroll
-        for (int i = 0; i < TPW; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (((i * 8 + j) & 31) == lane) {
-                    const int t = t0 + wt + i, e = e0 + we + j;
-                    float l = acc[i][j];
-                    if (e < E && bias) l = l + bias[e];
-                    lsm[(wt + i) * EXP + we + j] = l;
-                    if (t < T && e < E) logits[static_cast<int64_t>(t) * E + e] = l;
-                }
-            }
-        __syncthreads();
-        const int t = t0 + warp;
-        if (warp < TOK && t < T) {
-            float v[2];
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
-                const int e = s * 32 + lane;
-                v[s] = e < E ? lsm[warp * EXP + e] : -INFINITY;
-            }
-            warp_topk_softmax<2>(v, E, k, topk_idx + static_cast<int64_t>(t) * k,
-                                 topk_w + static_cast<int64_t>(t) * k, lane);
+        if (lane < TPW * 8) {
+            float l = mine;
+            if (my_e < E && bias) l = l + bias[my_e];
+            lsm[(wt + my_i) * EXP + we + my_j] = l;
+            if (my_t < T && my_e < E) logits[static_cast<int64_t>(my_t) * E + my_e] = l;
         }
+        __syncthreads();
+        cta_topk_softmax<TOK, WT * WE * 32>(lsm, t0, T, E, k, topk_idx, topk_w);
     }
 }
 
@@ -261,7 +316,7 @@ __global__ void __launch_bounds__(TK_WARPS * 32)
         const int e = s * 32 + lane;
         v[s] = e < E ? row[e] : -INFINITY;
     }
-    warp_topk_softmax<SLOTS>(v, E, k, topk_idx + static_cast<int64_t>(t) * k,
+    warp_topk_rounds<SLOTS>(v, E, k, topk_idx + static_cast<int64_t>(t) * k,
                              topk_w + static_cast<int64_t>(t) * k, lane);
 }
 
@@ -270,6 +325,7 @@ cudaError_t launch_gate_shape(const void *x, const void *wg, const float *bias, 
                               int64_t d_h, int64_t E, int64_t k, float *logits, int32_t *idx,
                               float *w, cudaStream_t stream) {
     constexpr int TOK = WT * TPW, EXP = WE * 8;
+    constexpr int GATE_STAGES = gate_stages(TOK + EXP, WT * WE > 8);
     const size_t smem = static_cast<size_t>(GATE_STAGES) * (TOK + EXP) * ROW_BYTES + 8 * GATE_STAGES + 16;
     CUtensorMap tm_x, tm_w;
     if (!encode_tma_2d_plain(&tm_x, x, static_cast<uint64_t>(d_h), static_cast<uint64_t>(T), SLICE, TOK) ||

@@ -62,9 +62,10 @@ constexpr int BAR_BYTES = 256;
 // the M=128 operand and the block's rows the N operand (N = rows rounded up
 // to 16), so a mostly-padding block costs N/128 of a full MMA.
 constexpr int SWAP_MAX_ROWS = 64;
-constexpr int MAX_SCHED = 2048;  // M blocks the in-kernel schedule can order
-// block list, expert per full block, run start / length (int16), class, scratch
-constexpr int SCHED_BYTES = MAX_SCHED * 4 + MAX_SCHED * 4 + 2 * MAX_SCHED * 2 + MAX_SCHED + 64;
+constexpr int MAX_SCHED = 1024;  // M blocks the in-kernel schedule can order
+// block list; per block: expert, first row, valid rows, class; per listed
+// full block: run start / length (int16); scan scratch
+constexpr int SCHED_BYTES = MAX_SCHED * 4 * 3 + 2 * MAX_SCHED * 2 + 2 * MAX_SCHED + 64;
 constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES + SCHED_BYTES;
 
 enum { MODE_GATE_UP = 0, MODE_DOWN = 1, MODE_MLP = 2 };
@@ -120,6 +121,9 @@ struct Schedule {
     const int *list;       // [n_full full blocks][n_partial partial blocks]; null = natural order
     const int16_t *run_start;  // per full block: index of its expert's first full block in list
     const int16_t *run_len;    // per full block: number of full blocks of its expert
+    const int *blk_g;          // per M block: expert, first row, valid rows (from the tables)
+    const int *blk_m;
+    const uint8_t *blk_rows;
     int n_full, n_blocks;
 };
 
@@ -149,7 +153,13 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const Schedul
         nt = tile - bx * n_tiles;
     }
     TileInfo t;
-    t.rows = block_rows(p, bx, &t.g, &t.m_start);
+    if (sc.list) {
+        t.g = sc.blk_g[bx];
+        t.m_start = sc.blk_m[bx];
+        t.rows = sc.blk_rows[bx];
+    } else {
+        t.rows = block_rows(p, bx, &t.g, &t.m_start);
+    }
     t.n0 = nt * out_n;
     t.bx = bx;
     t.phase = 0;
@@ -249,11 +259,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *sched = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(bars) + BAR_BYTES);
-    int *sched_g = sched + MAX_SCHED;
-    int16_t *sched_rs = reinterpret_cast<int16_t *>(sched_g + MAX_SCHED);
+    int *blk_g = sched + MAX_SCHED;
+    int *blk_m = blk_g + MAX_SCHED;
+    int16_t *sched_rs = reinterpret_cast<int16_t *>(blk_m + MAX_SCHED);
     int16_t *sched_rl = sched_rs + MAX_SCHED;
     uint8_t *sched_cls = reinterpret_cast<uint8_t *>(sched_rl + MAX_SCHED);
-    int *sched_scratch = reinterpret_cast<int *>(sched_cls + MAX_SCHED + (4 - MAX_SCHED % 4) % 4);
+    uint8_t *blk_rows = sched_cls + MAX_SCHED;
+    int *sched_scratch = reinterpret_cast<int *>(blk_rows + MAX_SCHED);
+    static_assert(MAX_SCHED % 4 == 0, "scratch alignment");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -293,11 +306,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     griddep_wait();
     griddep_launch_dependents();
     // ----- schedule: classify the M blocks, list full and partial ones -----
-    Schedule sc{nullptr, nullptr, nullptr, 0, p.m_blocks};
+    Schedule sc{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0, p.m_blocks};
     if (p.m_blocks <= MAX_SCHED) {
         for (int bx = threadIdx.x; bx < p.m_blocks; bx += NUM_THREADS) {
-            int g;
-            const int r = block_rows(p, bx, &g, nullptr);
+            int g, m0;
+            const int r = block_rows(p, bx, &g, &m0);
+            blk_g[bx] = g;
+            blk_m[bx] = m0;
+            blk_rows[bx] = static_cast<uint8_t>(r);
             // every block of an expert with at least one full block joins that
             // expert's run (its tail too: one sweep over the expert's weights)
             sched_cls[bx] = r == 0 ? 0 : (__ldg(p.sizes + g) >= BM ? 2 : 1);
@@ -321,19 +337,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncthreads();
         // runs of full blocks of one expert (consecutive in the list, block
         // order = expert order): each full block learns its run's start/length
-        for (int i = threadIdx.x; i < tot_f; i += NUM_THREADS) sched_g[i] = __ldg(p.gidx + sched[i]);
-        __syncthreads();
         for (int i = threadIdx.x; i < tot_f; i += NUM_THREADS) {
-            const int g = sched_g[i];
+            const int g = blk_g[sched[i]];
             int lo_i = i, hi_i = i;
-            while (lo_i > 0 && sched_g[lo_i - 1] == g) --lo_i;
-            while (hi_i + 1 < tot_f && sched_g[hi_i + 1] == g) ++hi_i;
+            while (lo_i > 0 && blk_g[sched[lo_i - 1]] == g) --lo_i;
+            while (hi_i + 1 < tot_f && blk_g[sched[hi_i + 1]] == g) ++hi_i;
             sched_rs[i] = static_cast<int16_t>(lo_i);
             sched_rl[i] = static_cast<int16_t>(hi_i - lo_i + 1);
         }
         sc.list = sched;
         sc.run_start = sched_rs;
         sc.run_len = sched_rl;
+        sc.blk_g = blk_g;
+        sc.blk_m = blk_m;
+        sc.blk_rows = blk_rows;
         sc.n_full = tot_f;
         sc.n_blocks = tot_f + tot_p;
     }
