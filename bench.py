@@ -45,18 +45,26 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 def kernels_per_step(cfg) -> int:
     """Kernels of one forward: gate (+ a top-k kernel when E > 64), dispatch
-    (one kernel up to 16384 pairs and 256 experts, else three), gather, the
-    expert MLP (both GEMM stages in one launch) and the combine."""
+    (one kernel up to 16384 pairs and 256 experts, else three), gather (none
+    when T <= 64: the expert MLP gathers its rows itself), the expert MLP
+    (both GEMM stages in one launch) and the combine."""
     gate = 1 if cfg.n_experts <= 64 else 2
     dispatch = 1 if cfg.T * cfg.top_k <= 16384 and cfg.n_experts <= 256 else 3
-    return gate + dispatch + 3
+    gather = 0 if cfg.T <= 64 else 1
+    return gate + dispatch + gather + 2
 
 
-# the entry points of one forward, in order (moe_forward makes the same calls)
-STAGES = ["gate_topk", "dispatch", "gather", "expert_mlp", "reduce"]
+def forward_stages(T: int) -> list:
+    """The entry points of one forward, in order (moe_forward makes the same
+    calls; for T <= 64 the expert MLP gathers its rows and there is no gather)."""
+    if T <= 64:
+        return ["gate_topk", "dispatch", "expert_mlp", "reduce"]
+    return ["gate_topk", "dispatch", "gather", "expert_mlp", "reduce"]
+
+
 # stages `--only` can time alone: the forward's, plus the two GEMM stages as
 # separate launches
-ONLY_STAGES = STAGES + ["gate_up_silu", "down"]
+ONLY_STAGES = ["gate_topk", "dispatch", "gather", "expert_mlp", "reduce", "gate_up_silu", "down"]
 
 
 def describe(cfg) -> str:
@@ -153,6 +161,7 @@ class NativeStep:
         self.cfg = cfg
         T, d_h, d_e, E, k = cfg.T, cfg.d_hidden, cfg.d_expert, cfg.n_experts, cfg.top_k
         self.T, self.k, self.E = T, k, E
+        self.stages = forward_stages(T)
         dt = d["x"].dtype
         self.code = {torch.float16: 0, torch.bfloat16: 1}[dt]
         self.ws = torch.empty(binding.forward_workspace_bytes(T, d_h, d_e, E, k, dt),
@@ -175,9 +184,10 @@ class NativeStep:
                                 self.code, p(self.ws), self.ws.numel(), p(self.out), p(self.err),
                                 ctypes.c_void_p(stream_ptr)))
 
-    def calls(self, x, stream_ptr, names=STAGES):
+    def calls(self, x, stream_ptr, names=None):
         """(function, argument tuple) of the named entry points (default: the
-        five calls of one forward, in order)."""
+        calls of one forward, in order)."""
+        names = self.stages if names is None else names
         cfg, v, d, L = self.cfg, self.v, self.d, self.L
         p = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
         T, k, E, d_h, d_e = self.T, self.k, self.E, cfg.d_hidden, cfg.d_expert
@@ -194,9 +204,13 @@ class NativeStep:
                                     p(v["token_topk_to_pos"]), ctypes.c_void_p(self.scratch_ptr),
                                     self.scratch_bytes, sp)),
             "gather": (L.moe_gather_rows, (p(x), p(v["sorted_token_idx"]), Tk, T, d_h, self.code, p(v["a"]), sp)),
-            "expert_mlp": (L.moe_grouped_mlp, (p(v["a"]), p(d["w_gate"]), p(d["w_up"]), p(d["w_down"]),
-                                               *tables, self.mb, None, Tk, d_h, d_e, E, self.code,
-                                               p(v["h"]), p(v["y"]), ready, p(self.err), sp)),
+            # the gathering form for T <= 64 (rows from x), as moe_forward does
+            "expert_mlp": (L.moe_grouped_mlp, (None if T <= 64 else p(v["a"]), p(d["w_gate"]), p(d["w_up"]),
+                                               p(d["w_down"]), *tables, self.mb, None, Tk, d_h, d_e, E,
+                                               self.code, p(v["h"]), p(v["y"]), ready,
+                                               p(x) if T <= 64 else None,
+                                               p(v["sorted_token_idx"]) if T <= 64 else None,
+                                               T if T <= 64 else 0, p(self.err), sp)),
             "gate_up_silu": (L.moe_grouped_gate_up_silu, (p(v["a"]), p(d["w_gate"]), p(d["w_up"]), *tables, self.mb,
                                           Tk, d_h, d_e, E, self.code, p(v["h"]), p(self.err), sp)),
             "down": (L.moe_grouped_down, (p(v["h"]), p(d["w_down"]), *tables, self.mb, None, Tk, d_h, d_e, E,
@@ -282,7 +296,7 @@ def run_native(args, cfg, rank, world, dev):
                 with torch.cuda.graph(g, stream=stream):
                     run_calls(fwd_calls[i])
                 graphs.append(g)
-                evs = timing_events(len(STAGES) + 1)
+                evs = timing_events(len(step.stages) + 1)
                 gi = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(gi, stream=stream):
                     run_calls(calls[i], evs, stream)
@@ -298,7 +312,7 @@ def run_native(args, cfg, rank, world, dev):
 
         # eager timing (the host launches every kernel), for the record
         eager_ms = []
-        evs_e = [torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+        evs_e = [torch.cuda.Event(enable_timing=True) for _ in range(len(step.stages) + 1)]
         for i in range(min(args.steps, 50)):
             flush()
             run_calls(calls[i % n_pool], evs_e, stream)
@@ -327,17 +341,17 @@ def run_native(args, cfg, rank, world, dev):
         t_wall = time.perf_counter() - t_wall
         step_ms = np.array([s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)])
         # the same K steps with events between the kernels (per-kernel times)
-        per_stage = np.zeros((args.steps, len(STAGES)))
+        per_stage = np.zeros((args.steps, len(step.stages)))
         for i in range(args.steps):
             flush()
             if igraphs:
                 igraphs[i % n_pool].replay()
                 evs = gevents[i % n_pool]
             else:
-                evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(step.stages) + 1)]
                 run_calls(calls[i % n_pool], evs, stream)
             evs[-1].synchronize()
-            per_stage[i] = [evs[j].elapsed_time(evs[j + 1]) for j in range(len(STAGES))]
+            per_stage[i] = [evs[j].elapsed_time(evs[j + 1]) for j in range(len(step.stages))]
         stream.synchronize()
         clocks = sampler.stop()
         if world > 1:
@@ -348,7 +362,7 @@ def run_native(args, cfg, rank, world, dev):
 
     e2e = measure_e2e(args, cfg, d, dev, flush, world)
     aux = measure_reduce_aux(dev, flush) if rank == 0 else None
-    return dict(per_stage=per_stage, total_ms=total_ms, act_experts=act_experts,
+    return dict(per_stage=per_stage, stages=list(step.stages), total_ms=total_ms, act_experts=act_experts,
                 sizes_pool=sizes_pool, clocks=clocks, e2e=e2e, aux=aux, mode=mode,
                 eager_ms=float(np.median(eager_ms)), wall_s=t_wall)
 
@@ -664,7 +678,8 @@ def main():
     es = 2
     flops_step = roofline.moe_forward_flops(T, k, d_h, d_e, E)
     # dominant kernel: the expert MLP (both grouped GEMM stages in one launch)
-    gu_ms = float(per_stage[:, STAGES.index("expert_mlp")].mean())
+    stages = res["stages"]
+    gu_ms = float(per_stage[:, stages.index("expert_mlp")].mean())
     gu_bytes = roofline.expert_mlp_bytes(Tk, d_h, d_e, round(e_act), es)
     gu_flops = roofline.expert_mlp_flops(Tk, d_h, d_e)
     t_bytes = gu_bytes / (peaks["hbm_gbs"] * 1e9)
@@ -690,7 +705,7 @@ def main():
         "value": round(value, 1), "ms_per_step": round(ms_step, 5),
         "tflops": round(flops_step * args.steps / (res["total_ms"] / 1e3) / 1e12, 3),
         "step_roofline_frac": round(step_roof_ms / ms_step, 4),
-        "kernels_us": {s: round(float(per_stage[:, i].mean()) * 1e3, 2) for i, s in enumerate(STAGES)},
+        "kernels_us": {s: round(float(per_stage[:, i].mean()) * 1e3, 2) for i, s in enumerate(stages)},
         "kernels_note": "per-kernel times from replays of the same graphs with event nodes between the kernels",
         "active_experts": e_act,
         "roofline": rl,

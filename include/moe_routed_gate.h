@@ -198,9 +198,16 @@ MOE_API moe_status_t moe_grouped_down(const void *h, const void *w_down, const i
  * moe_grouped_down(h -> y, row_weights): h [n_rows, d_e] is still written (it
  * is stage 2's operand, read back mostly from L2) and y [n_rows, d_h].
  * Inside the kernel a stage-2 tile starts once all stage-1 tiles of its M
- * block are stored; the block's counter lives in `ready`, caller-owned device
- * memory of m_blocks int32 that this call zeroes (stream ordered) before the
- * launch.  The waits are bounded: after about 2 s *err_flag is set to
+ * block are stored, and each CTA takes its next tile from a shared counter.
+ * `ready` is caller-owned device memory of m_blocks + 1 int32 (the per-block
+ * counters, then the tile counter) that this call zeroes (stream ordered)
+ * before the launch.
+ * Gathering form: with sorted_token_idx non-NULL, stage 1 reads its rows from
+ * the tokens x [T, d_h] by those indices (the gather of the CSDN "forward",
+ * step 3, done by four-row TMA gathers in the kernel) and `a` is not read; this needs
+ * 1 <= T <= 64 (every expert then holds at most 64 rows).  Otherwise x and T
+ * are ignored and may be NULL / 0.
+ * The waits are bounded: after about 2 s *err_flag is set to
  * MOE_ERR_TIMEOUT and the kernel returns (this needs all CTAs of the grid,
  * one per SM, resident at once; a GPU shared with a partitioning runtime can
  * break that).  Other arguments, layouts and errors as the two calls.
@@ -211,6 +218,7 @@ MOE_API moe_status_t moe_grouped_mlp(const void *a, const void *w_gate, const vo
                              const int32_t *group_idx_for_bx, int64_t m_blocks,
                              const float *row_weights, int64_t n_rows, int64_t d_h, int64_t d_e,
                              int64_t E, moe_dtype_t dtype, void *h, void *y, int32_t *ready,
+                             const void *x, const int32_t *sorted_token_idx, int64_t T,
                              int32_t *err_flag, moe_stream_t stream);
 
 /*
@@ -253,7 +261,9 @@ MOE_API moe_status_t moe_reduce_fused_scaled(const void *x, int64_t n_rows,
 /*
  * The whole routed forward, stream ordered, no host round trip:
  *   moe_gate_topk -> moe_build_dispatch -> moe_gather_rows ->
- *   moe_grouped_mlp (stage 1 + stage 2 in one launch) -> moe_reduce_fused.
+ *   moe_grouped_mlp (stage 1 + stage 2 in one launch) -> moe_reduce_fused;
+ * for T <= 64 the gather is done inside moe_grouped_mlp (its gathering form)
+ * and the gathered-rows section of the workspace is left unwritten.
  * x [T, d_h]; w_g [E, d_h]; bias [E] fp32 or NULL; w_gate/w_up [E, d_e, d_h];
  * w_down [E, d_h, d_e]; out [T, d_h]; all in `dtype` (f16 or bf16).
  * ws: moe_forward_workspace_bytes(...) bytes, 256-byte aligned; it holds every

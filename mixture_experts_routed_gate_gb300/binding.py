@@ -60,7 +60,7 @@ def lib():
         "moe_gather_rows": (I, [P, P, I64, I64, I64, I, P, P]),
         "moe_grouped_gate_up_silu": (I, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, P, P]),
         "moe_grouped_down": (I, [P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I, P, P, P]),
-        "moe_grouped_mlp": (I, [P, P, P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I, P, P, P, P, P]),
+        "moe_grouped_mlp": (I, [P, P, P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I, P, P, P, P, P, I64, P, P]),
         "moe_reduce_fused": (I, [P, I64, P, P, I64, I64, I64, I, I, P, P, P]),
         "moe_reduce_fused_scaled": (I, [P, I64, P, P, P, P, I64, I64, I64, I, I, P, P, P]),
         "moe_forward": (I, [P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, SZ, P, P, P]),
@@ -289,12 +289,21 @@ def moe_grouped_down(h, w_down, tables, row_weights=None, y=None, err=None):
 
 
 def moe_grouped_mlp(a, w_gate, w_up, w_down, tables, row_weights=None, h=None, y=None,
-                    ready=None, err=None):
-    """Stage 1 and stage 2 in one launch; returns (h, y)."""
-    _cuda(a, "a", ndim=2)
+                    ready=None, err=None, x=None, sorted_token_idx=None):
+    """Stage 1 and stage 2 in one launch; returns (h, y).  With x and
+    sorted_token_idx (and a=None), stage 1 gathers its rows from the tokens x
+    (needs at most 64 tokens)."""
+    gathering = sorted_token_idx is not None
+    if gathering:
+        _cuda(x, "x", ndim=2)
+        _cuda(sorted_token_idx, "sorted_token_idx", dtype=torch.int32)
+        src, n_rows, d_h = x, sorted_token_idx.numel(), x.shape[1]
+    else:
+        _cuda(a, "a", ndim=2)
+        src = a
+        n_rows, d_h = a.shape
     for n, t in (("w_gate", w_gate), ("w_up", w_up), ("w_down", w_down)):
-        _cuda(t, n, dtype=a.dtype, ndim=3)
-    n_rows, d_h = a.shape
+        _cuda(t, n, dtype=src.dtype, ndim=3)
     E, d_e, d_h2 = w_gate.shape
     if d_h2 != d_h or w_up.shape != w_gate.shape:
         raise ValueError("w_gate / w_up must be [E, d_expert, d_hidden]")
@@ -304,23 +313,25 @@ def moe_grouped_mlp(a, w_gate, w_up, w_down, tables, row_weights=None, h=None, y
     if row_weights is not None:
         _cuda(row_weights, "row_weights", dtype=torch.float32)
     if h is None:
-        h = torch.empty((n_rows, d_e), dtype=a.dtype, device=a.device)
+        h = torch.empty((n_rows, d_e), dtype=src.dtype, device=src.device)
     if y is None:
-        y = torch.empty((n_rows, d_h), dtype=a.dtype, device=a.device)
+        y = torch.empty((n_rows, d_h), dtype=src.dtype, device=src.device)
     if ready is None:
-        ready = torch.empty(max(g.numel(), 1), dtype=torch.int32, device=a.device)
-    _cuda(h, "h", dtype=a.dtype)
-    _cuda(y, "y", dtype=a.dtype)
+        ready = torch.empty(g.numel() + 1, dtype=torch.int32, device=src.device)
+    _cuda(h, "h", dtype=src.dtype)
+    _cuda(y, "y", dtype=src.dtype)
     _cuda(ready, "ready", dtype=torch.int32)
-    if ready.numel() < g.numel():
-        raise ValueError("ready needs one int32 per M block")
+    if ready.numel() < g.numel() + 1:
+        raise ValueError("ready needs one int32 per M block plus one")
     if err is not None:
         _cuda(err, "err", dtype=torch.int32)
-    with torch.cuda.device(a.device):
+    with torch.cuda.device(src.device):
         _check(lib().moe_grouped_mlp(
-            _ptr(a), _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(s), _ptr(o), _ptr(p), _ptr(g),
-            g.numel(), _ptr(row_weights), n_rows, d_h, d_e, E, _dtype_code(a, "a"), _ptr(h),
-            _ptr(y), _ptr(ready), _ptr(err), _stream(a.device)), "moe_grouped_mlp")
+            _ptr(a) if not gathering else None, _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(s), _ptr(o),
+            _ptr(p), _ptr(g), g.numel(), _ptr(row_weights), n_rows, d_h, d_e, E, _dtype_code(src, "x"),
+            _ptr(h), _ptr(y), _ptr(ready), _ptr(x) if gathering else None,
+            _ptr(sorted_token_idx), x.shape[0] if gathering else 0, _ptr(err), _stream(src.device)),
+            "moe_grouped_mlp")
     return h, y
 
 
@@ -404,7 +415,7 @@ def forward_workspace_views(ws, T, d_h, d_e, E, k, dtype) -> dict:
               "group_idx_for_bx": ((mb,), torch.int32), "sorted_token_idx": ((Tk,), torch.int32),
               "sorted_row_weight": ((Tk,), torch.float32),
               "token_topk_to_pos": ((T, k), torch.int32), "a": ((Tk, d_h), dtype),
-              "h": ((Tk, d_e), dtype), "y": ((Tk, d_h), dtype), "mlp_ready": ((mb,), torch.int32)}
+              "h": ((Tk, d_e), dtype), "y": ((Tk, d_h), dtype), "mlp_ready": ((mb + 1,), torch.int32)}
     out = {}
     for i, name in enumerate(WS_NAMES):
         if name not in shapes:

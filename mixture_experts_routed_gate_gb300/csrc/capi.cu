@@ -66,7 +66,7 @@ bool fwd_layout(int64_t T, int64_t d_h, int64_t d_e, int64_t E, int64_t k, moe_d
         Tk * d_h * es,                   // 11 A (gathered rows)
         Tk * d_e * es,                   // 12 h
         Tk * d_h * es,                   // 13 y
-        mb * 4,                          // 14 per-block counters of the expert MLP
+        (mb + 1) * 4,                    // 14 per-block counters + tile counter of the expert MLP
     };
     size_t cur = 0;
     for (int i = 0; i < kFwdSections; ++i) {
@@ -237,32 +237,39 @@ moe_status_t moe_grouped_down(const void *h, const void *w_down, const int32_t *
 
 // zero_ready: clear the counters on the stream first (the forward has its
 // dispatch kernel clear them instead, keeping the kernels back to back).
+// gather_idx: stage 1 gathers token rows of x [T, d_h] by these indices
+// instead of reading `a` (the forward, when T <= 64: no block then holds more
+// than 64 rows, the most the gathering path takes).
 static moe_status_t grouped_mlp(const void *a, const void *w_gate, const void *w_up,
                                 const void *w_down, const int32_t *group_sizes,
                                 const int32_t *group_offsets, const int32_t *group_padded_offsets,
                                 const int32_t *group_idx_for_bx, int64_t m_blocks,
                                 const float *row_weights, int64_t n_rows, int64_t d_h, int64_t d_e,
                                 int64_t E, moe_dtype_t dtype, void *h, void *y, int32_t *ready,
-                                int32_t *err_flag, moe_stream_t stream, bool zero_ready) {
+                                int32_t *err_flag, moe_stream_t stream, bool zero_ready,
+                                const void *x = nullptr, const int32_t *gather_idx = nullptr,
+                                int64_t T = 0) {
     if (!is_half_type(dtype)) return MOE_ERR_UNSUPPORTED;
     if (d_h <= 0 || d_e <= 0 || d_h % 64 != 0 || d_e % 64 != 0) return MOE_ERR_INVALID_ARG;
     if (n_rows == 0) return MOE_OK;
     moe_status_t st = check_gemm_tables(group_sizes, group_offsets, group_padded_offsets,
                                         group_idx_for_bx, m_blocks, n_rows, E);
     if (st != MOE_OK) return st;
-    if (!a || !w_gate || !w_up || !w_down || !h || !y || !ready) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(a) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+    const void *rows_in = gather_idx ? x : a;
+    if (!rows_in || !w_gate || !w_up || !w_down || !h || !y || !ready) return MOE_ERR_INVALID_ARG;
+    if (gather_idx && (T <= 0 || T > 64)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(rows_in) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
         !aligned16(h) || !aligned16(y))
         return MOE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (zero_ready) {
-        cudaError_t e = cudaMemsetAsync(ready, 0, static_cast<size_t>(m_blocks) * 4, s);
+        cudaError_t e = cudaMemsetAsync(ready, 0, static_cast<size_t>(m_blocks + 1) * 4, s);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     return cuda_status(moe::launch_grouped_mlp(dtype, a, w_gate, w_up, w_down, group_sizes,
                                                group_offsets, group_padded_offsets, group_idx_for_bx,
                                                m_blocks, row_weights, n_rows, d_h, d_e, E, h, y,
-                                               ready, err_flag, s));
+                                               ready, err_flag, s, x, gather_idx, T));
 }
 
 moe_status_t moe_grouped_mlp(const void *a, const void *w_gate, const void *w_up,
@@ -271,10 +278,11 @@ moe_status_t moe_grouped_mlp(const void *a, const void *w_gate, const void *w_up
                              const int32_t *group_idx_for_bx, int64_t m_blocks,
                              const float *row_weights, int64_t n_rows, int64_t d_h, int64_t d_e,
                              int64_t E, moe_dtype_t dtype, void *h, void *y, int32_t *ready,
+                             const void *x, const int32_t *sorted_token_idx, int64_t T,
                              int32_t *err_flag, moe_stream_t stream) {
     return grouped_mlp(a, w_gate, w_up, w_down, group_sizes, group_offsets, group_padded_offsets,
                        group_idx_for_bx, m_blocks, row_weights, n_rows, d_h, d_e, E, dtype, h, y,
-                       ready, err_flag, stream, true);
+                       ready, err_flag, stream, true, x, sorted_token_idx, T);
 }
 
 static bool reduce_pair_ok(moe_dtype_t in, moe_dtype_t out, bool allow_fp8) {
@@ -359,10 +367,16 @@ moe_status_t moe_forward(const void *x, const void *w_g, const float *bias, cons
     st = build_dispatch(topk_idx, topk_w, T, k, E, MOE_BLOCK_M, sizes, offsets, padded, gidx, stok,
                         sw, pos, scratch, moe::dispatch_scratch_bytes(Tk, E), ready, stream);
     if (st != MOE_OK) return st;
-    st = moe_gather_rows(x, stok, Tk, T, d_h, dtype, A, stream);
-    if (st != MOE_OK) return st;
-    st = grouped_mlp(A, w_gate, w_up, w_down, sizes, offsets, padded, gidx, mb, nullptr, Tk, d_h,
-                     d_e, E, dtype, hbuf, ybuf, ready, err_flag, stream, false);
+    if (T <= 64) {
+        // every expert holds at most T <= 64 rows: stage 1 gathers them from x
+        st = grouped_mlp(nullptr, w_gate, w_up, w_down, sizes, offsets, padded, gidx, mb, nullptr, Tk,
+                         d_h, d_e, E, dtype, hbuf, ybuf, ready, err_flag, stream, false, x, stok, T);
+    } else {
+        st = moe_gather_rows(x, stok, Tk, T, d_h, dtype, A, stream);
+        if (st != MOE_OK) return st;
+        st = grouped_mlp(A, w_gate, w_up, w_down, sizes, offsets, padded, gidx, mb, nullptr, Tk, d_h,
+                         d_e, E, dtype, hbuf, ybuf, ready, err_flag, stream, false);
+    }
     if (st != MOE_OK) return st;
     return moe_reduce_fused(ybuf, Tk, pos, topk_w, T, k, d_h, dtype, dtype, out, err_flag, stream);
 }

@@ -204,6 +204,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *desc, uint
         : "memory");
 }
 
+// Four rows r0..r3 (any order, any rows of the tensor) of one column box:
+// the tensor map's box is one row high; the rows land one after another at
+// dst, each swizzled by its shared-memory address like a tiled load.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *desc, uint32_t bar, int c0,
+                                            int r0, int r1, int r2, int r3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *desc, uint32_t bar, int c0,
                                             int c1, int c2) {
     asm volatile(

@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(SCAN_THREADS)
         gidx[bx] = lo;
         if (ready) ready[bx] = 0;
     }
+    if (ready && threadIdx.x == 0) ready[m_blocks] = 0;  // the expert MLP's tile counter
 }
 
 __global__ void __launch_bounds__(DS_THREADS)
@@ -253,6 +254,7 @@ __global__ void __launch_bounds__(SMALL_THREADS)
         gidx[bx] = lo;
         if (ready) ready[bx] = 0;
     }
+    if (ready && threadIdx.x == 0) ready[m_blocks] = 0;  // the expert MLP's tile counter
 #pragma unroll
     for (int r = 0; r < SMALL_MAX_ROUNDS; ++r) {
         if (r < rounds) {

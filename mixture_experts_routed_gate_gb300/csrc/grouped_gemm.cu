@@ -58,6 +58,9 @@ constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int B_BYTES = MMA_N * BK * 2;      // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int BAR_BYTES = 256;
+// Tile ids handed from the producer to the MMA and epilogue warps when tiles
+// are taken from a global counter (expert MLP mode).
+constexpr int TRING = 4;
 // Blocks with at most this many valid rows run "swapped": the weight tile is
 // the M=128 operand and the block's rows the N operand (N = rows rounded up
 // to 16), so a mostly-padding block costs N/128 of a full MMA.
@@ -84,6 +87,11 @@ struct GemmParams {
     const int32_t *gidx;
     const float *row_weights;
     int *ready;  // MODE_MLP: per M block, stage-1 epilogue warp-tiles stored
+    int *tile_counter;  // MODE_MLP: next tile to take (null: fixed round-robin)
+    // MODE_MLP with every block at most SWAP_MAX_ROWS rows: stage 1 gathers its
+    // rows straight from the tokens x (through tmX) by these indices (null:
+    // stage 1 reads the gathered rows through tmA0)
+    const int32_t *gather_idx;
     PhaseParams ph[2];  // [0] stage 1 (gate/up), [1] stage 2 (down)
     int m_blocks;
     int *err;
@@ -237,15 +245,17 @@ __device__ __forceinline__ void publish_h(int *ctr, int lane) {
     if (lane == 0) counter_publish(ctr);
 }
 
-// Stage 1 reads rows A through tmA0 and W_gate / W_up through tmB0 / tmB1;
-// stage 2 reads h through tmA1 and W_down through tmB2.
+// Stage 1 reads rows A through tmA0 (or gathers token rows through tmX) and
+// W_gate / W_up through tmB0 / tmB1; stage 2 reads h through tmA1 and W_down
+// through tmB2.
 template <int DT, int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmB1,
                         const __grid_constant__ CUtensorMap tmA1,
-                        const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmB2,
+                        const __grid_constant__ CUtensorMap tmX, const GemmParams p) {
     constexpr bool HAS0 = MODE != MODE_DOWN, HAS1 = MODE != MODE_GATE_UP;
     constexpr uint32_t IDESC = idesc_f16(DT == kBF16, BM, MMA_N);
     using OutT = typename Elem<DT>::T;
@@ -256,8 +266,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * A_BYTES;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4 + 2 * TRING);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *tid_ring = reinterpret_cast<int *>(tmem_slot + 2);
+    static_assert((2 * STAGES + 4 + 2 * TRING) * 8 + 8 + 4 * TRING <= BAR_BYTES, "barrier area");
     int *sched = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(bars) + BAR_BYTES);
     int *blk_g = sched + MAX_SCHED;
     int *blk_m = blk_g + MAX_SCHED;
@@ -275,6 +287,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    auto tidf_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + i); };
+    auto tide_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + TRING + i); };
+    // tiles from the global counter (in order, each CTA taking the next one
+    // when its producer is ready) instead of a fixed round-robin deal
+    const bool dynamic = MODE == MODE_MLP && p.tile_counter != nullptr;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -284,6 +301,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
             mbar_init(tempty_bar(a), 4);  // one arrival per epilogue warp
+        }
+        for (int i = 0; i < TRING; ++i) {
+            mbar_init(tidf_bar(i), 1);
+            mbar_init(tide_bar(i), 1 + EPI_WARPS);  // the MMA warp and every epilogue warp
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -370,7 +391,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             long issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+            int rslot = 0;
+            uint32_t rphase = 0;
+            // dynamic: the first tile of CTA b is tile b; later ones come from
+            // the counter (offset by the grid), fetched one tile ahead so the
+            // atomic's round trip overlaps the current tile
+            int next_tile = dynamic ? static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1) : 0;
+            for (int it = 0; ok; ++it) {
+                int tile = blockIdx.x + it * static_cast<int>(gridDim.x);
+                if (dynamic) {
+                    // pass the tile id on (-1: none left)
+                    if (it > 0) {
+                        tile = next_tile;
+                        next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
+                    }
+                    if (tile >= total) tile = -1;
+                    if (!mbar_wait_bounded(tide_bar(rslot), rphase ^ 1u, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tid_ring[rslot] = tile;
+                    mbar_arrive(tidf_bar(rslot));
+                    if (++rslot == TRING) {
+                        rslot = 0;
+                        rphase ^= 1u;
+                    }
+                    if (tile < 0) break;
+                } else if (tile >= total) {
+                    break;
+                }
                 const TileInfo ti = decode_tile<MODE>(p, sc, tile, n0_tiles);
                 if (ti.rows == 0) continue;
                 // a stage-2 tile reads h rows of its block: wait until every
@@ -381,21 +430,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 const int kblocks = phase_params_of(p, ti.phase).k_blocks;
+                // stage-1 rows gathered from x: the swapped MMA reads np rows
+                const bool gather = MODE == MODE_MLP && ti.phase == 0 && p.gather_idx != nullptr;
+                int np_g = (ti.rows + 15) & ~15;
+                if (gather && np_g > SWAP_MAX_ROWS) {  // the host guarantees rows <= 64
+                    np_g = SWAP_MAX_ROWS;
+                    if (p.err) atomicExch(p.err, kErrDeviceFlag);
+                }
+                const uint32_t stage_tx = gather ? static_cast<uint32_t>(np_g * BK * 2 + B_BYTES) : STAGE_BYTES;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    mbar_arrive_expect_tx(fb, stage_tx);
                     const uint32_t a_dst = smem_u32(sA + stage * A_BYTES);
                     const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
                     // a large expert's rows and weight stripes are reused by the
                     // tiles of its run: keep them; a small expert's weights are
                     // read by one block only: let them leave L2 first
-                    const CUtensorMap *ta = HAS0 && ti.phase == 0 ? &tmA0 : &tmA1;
-                    if (ti.big) tma_load_2d_hint(a_dst, ta, fb, kb * BK, ti.m_start, pol_last);
-                    else tma_load_2d(a_dst, ta, fb, kb * BK, ti.m_start);
+                    if (gather) {
+                        // four rows per copy; rows past the block repeat its first token
+                        const int32_t *ids = p.gather_idx + ti.m_start;
+                        for (int r = 0; r < np_g; r += 4) {
+                            const int i0 = __ldg(ids + (r < ti.rows ? r : 0));
+                            const int i1 = __ldg(ids + (r + 1 < ti.rows ? r + 1 : 0));
+                            const int i2 = __ldg(ids + (r + 2 < ti.rows ? r + 2 : 0));
+                            const int i3 = __ldg(ids + (r + 3 < ti.rows ? r + 3 : 0));
+                            tma_gather4(a_dst + static_cast<uint32_t>(r * BK * 2), &tmX, fb, kb * BK, i0, i1, i2, i3);
+                        }
+                    } else {
+                        const CUtensorMap *ta = HAS0 && ti.phase == 0 ? &tmA0 : &tmA1;
+                        if (ti.big) tma_load_2d_hint(a_dst, ta, fb, kb * BK, ti.m_start, pol_last);
+                        else tma_load_2d(a_dst, ta, fb, kb * BK, ti.m_start);
+                    }
                     const uint64_t polb = ti.big ? pol_last : pol_first;
                     if (HAS0 && ti.phase == 0) {
                         tma_load_3d_hint(b_dst, &tmB0, fb, kb * BK, ti.n0, ti.g, polb);
@@ -428,7 +497,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             uint32_t last_bar = 0, last_parity = 0;
             bool committed = false;
-            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+            int rslot = 0;
+            uint32_t rphase = 0;
+            for (int it = 0; ok; ++it) {
+                int tile = blockIdx.x + it * static_cast<int>(gridDim.x);
+                if (dynamic) {
+                    if (!mbar_wait_bounded(tidf_bar(rslot), rphase, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tile = tid_ring[rslot];
+                    mbar_arrive(tide_bar(rslot));
+                    if (++rslot == TRING) {
+                        rslot = 0;
+                        rphase ^= 1u;
+                    }
+                    if (tile < 0) break;
+                } else if (tile >= total) {
+                    break;
+                }
                 const TileInfo ti = decode_tile<MODE>(p, sc, tile, n0_tiles);
                 if (ti.rows == 0) continue;
                 const int kblocks = phase_params_of(p, ti.phase).k_blocks;
@@ -490,7 +577,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int q = warp & 3;  // TMEM lane quarter this warp may read
         const int row = q * 32 + lane;
         int local = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        int rslot = 0;
+        uint32_t rphase = 0;
+        for (int it = 0;; ++it) {
+            int tile = blockIdx.x + it * static_cast<int>(gridDim.x);
+            if (dynamic) {
+                // lane 0 takes the id (one arrival per warp), the warp follows
+                int got = 1, tl = -1;
+                if (lane == 0) {
+                    got = mbar_wait_bounded(tidf_bar(rslot), rphase, abort_flag, p.err) ? 1 : 0;
+                    if (got) {
+                        tl = tid_ring[rslot];
+                        mbar_arrive(tide_bar(rslot));
+                    }
+                }
+                got = __shfl_sync(0xffffffffu, got, 0);
+                tl = __shfl_sync(0xffffffffu, tl, 0);
+                if (++rslot == TRING) {
+                    rslot = 0;
+                    rphase ^= 1u;
+                }
+                if (!got || tl < 0) break;
+                tile = tl;
+            } else if (tile >= total) {
+                break;
+            }
             const TileInfo ti = decode_tile<MODE>(p, sc, tile, n0_tiles);
             if (ti.rows == 0) continue;
             const bool gu = HAS0 && ti.phase == 0;  // stage 1: silu(gate) * up
@@ -679,7 +790,7 @@ cudaError_t launch_typed(const CUtensorMap *maps, const GemmParams &p, int grid,
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
     return launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, maps[0], maps[1],
-                      maps[2], maps[3], maps[4], p);
+                      maps[2], maps[3], maps[4], maps[5], p);
 }
 
 template <int MODE>
@@ -699,6 +810,8 @@ GemmParams base_params(const int32_t *sizes, const int32_t *offsets, const int32
     p.gidx = gidx;
     p.row_weights = row_weights;
     p.ready = nullptr;
+    p.tile_counter = nullptr;
+    p.gather_idx = nullptr;
     p.m_blocks = static_cast<int>(m_blocks);
     p.err = err;
     return p;
@@ -739,13 +852,14 @@ cudaError_t launch_grouped_gemm(bool gate_up, int dtype, const void *a, const vo
                                 const float *row_weights, int64_t n_rows, int64_t K, int64_t N,
                                 int64_t E, void *out, int32_t *err, cudaStream_t stream) {
     if (n_rows <= 0 || m_blocks <= 0) return cudaSuccess;
-    CUtensorMap maps[5];
+    CUtensorMap maps[6];
     GemmParams p = base_params(sizes, offsets, padded, gidx, m_blocks, row_weights, err);
     if (gate_up) {
         // stage 1: K = d_h, N = d_e
         if (!stage1_maps(maps, dtype, a, w0, w1, n_rows, K, N, E)) return cudaErrorInvalidValue;
         maps[3] = maps[0];
         maps[4] = maps[1];
+        maps[5] = maps[0];
         p.ph[0] = phase_params(out, K, N, 128);
         p.ph[1] = p.ph[0];
         return launch_mode<MODE_GATE_UP>(dtype, maps, p, m_blocks * p.ph[0].n_tiles, stream);
@@ -755,6 +869,7 @@ cudaError_t launch_grouped_gemm(bool gate_up, int dtype, const void *a, const vo
     maps[0] = maps[3];
     maps[1] = maps[4];
     maps[2] = maps[4];
+    maps[5] = maps[3];
     p.ph[1] = phase_params(out, K, N, 256);
     p.ph[0] = p.ph[1];
     return launch_mode<MODE_DOWN>(dtype, maps, p, m_blocks * p.ph[1].n_tiles, stream);
@@ -765,14 +880,26 @@ cudaError_t launch_grouped_mlp(int dtype, const void *a, const void *w_gate, con
                                const int32_t *padded, const int32_t *gidx, int64_t m_blocks,
                                const float *row_weights, int64_t n_rows, int64_t d_h, int64_t d_e,
                                int64_t E, void *h, void *y, int32_t *ready, int32_t *err,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, const void *x, const int32_t *gather_idx,
+                               int64_t T) {
     if (n_rows <= 0 || m_blocks <= 0) return cudaSuccess;
-    CUtensorMap maps[5];
-    if (!stage1_maps(maps, dtype, a, w_gate, w_up, n_rows, d_h, d_e, E) ||
+    CUtensorMap maps[6];
+    // gathering: stage 1 reads token rows of x by index (then `a` is unused)
+    const void *a_map = gather_idx ? x : a;
+    const int64_t a_rows = gather_idx ? T : n_rows;
+    if (!stage1_maps(maps, dtype, a_map, w_gate, w_up, a_rows, d_h, d_e, E) ||
         !stage2_maps(maps, dtype, h, w_down, n_rows, d_h, d_e, E))
         return cudaErrorInvalidValue;
+    if (gather_idx) {
+        if (!make_map_2d(&maps[5], dtype, x, static_cast<uint64_t>(d_h), static_cast<uint64_t>(T), 1u))
+            return cudaErrorInvalidValue;
+    } else {
+        maps[5] = maps[0];
+    }
     GemmParams p = base_params(sizes, offsets, padded, gidx, m_blocks, row_weights, err);
     p.ready = ready;
+    p.tile_counter = ready + m_blocks;
+    p.gather_idx = gather_idx;
     p.ph[0] = phase_params(h, d_h, d_e, 128);
     p.ph[1] = phase_params(y, d_e, d_h, 256);
     return launch_mode<MODE_MLP>(dtype, maps, p, m_blocks * (p.ph[0].n_tiles + p.ph[1].n_tiles), stream);

@@ -44,13 +44,17 @@ cudaError_t launch_grouped_gemm(bool gate_up, int dtype, const void *a, const vo
                                 const int32_t *padded, const int32_t *gidx, int64_t m_blocks,
                                 const float *row_weights, int64_t n_rows, int64_t K, int64_t N,
                                 int64_t E, void *out, int32_t *err, cudaStream_t stream);
-// Stage 1 and stage 2 in one persistent launch; `ready` (m_blocks int32) must
-// be zero when the kernel starts.
+// Stage 1 and stage 2 in one persistent launch; `ready` (m_blocks + 1 int32:
+// the per-block counters, then the tile counter) must be zero when the
+// kernel starts.  With gather_idx (every block at most 64 rows, as when
+// T <= 64), stage 1 gathers its rows from x [T, d_h] by those indices and `a`
+// is not read.
 cudaError_t launch_grouped_mlp(int dtype, const void *a, const void *w_gate, const void *w_up,
                                const void *w_down, const int32_t *sizes, const int32_t *offsets,
                                const int32_t *padded, const int32_t *gidx, int64_t m_blocks,
                                const float *row_weights, int64_t n_rows, int64_t d_h, int64_t d_e,
                                int64_t E, void *h, void *y, int32_t *ready, int32_t *err,
-                               cudaStream_t stream);
+                               cudaStream_t stream, const void *x = nullptr,
+                               const int32_t *gather_idx = nullptr, int64_t T = 0);
 
 }  // namespace moe

@@ -92,9 +92,14 @@ def test_argument_errors_without_launch(lib):
                                 fake, None, None) == MOE_ERR_INVALID_ARG
     # expert MLP in one launch: no counter buffer, misaligned d_expert
     assert lib.moe_grouped_mlp(fake, fake, fake, fake, fake, fake, fake, fake, 3, None, 8, 256, 128, 8, 1,
-                               fake, fake, None, None, None) == MOE_ERR_INVALID_ARG
+                               fake, fake, None, None, None, 0, None, None) == MOE_ERR_INVALID_ARG
     assert lib.moe_grouped_mlp(fake, fake, fake, fake, fake, fake, fake, fake, 3, None, 8, 256, 100, 8, 1,
-                               fake, fake, fake, None, None) == MOE_ERR_INVALID_ARG
+                               fake, fake, fake, None, None, 0, None, None) == MOE_ERR_INVALID_ARG
+    # gathering form: more than 64 tokens, or no tokens given
+    assert lib.moe_grouped_mlp(None, fake, fake, fake, fake, fake, fake, fake, 3, None, 8, 256, 128, 8, 1,
+                               fake, fake, fake, fake, fake, 65, None, None) == MOE_ERR_INVALID_ARG
+    assert lib.moe_grouped_mlp(None, fake, fake, fake, fake, fake, fake, fake, 3, None, 8, 256, 128, 8, 1,
+                               fake, fake, fake, None, fake, 8, None, None) == MOE_ERR_INVALID_ARG
     # forward: workspace too small, misaligned workspace
     assert lib.moe_forward(fake, fake, None, fake, fake, fake, 64, 256, 128, 8, 2, 0, P(0x100000), 16,
                            fake, None, None) == MOE_ERR_WORKSPACE
