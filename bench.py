@@ -54,6 +54,28 @@ def kernels_per_step(cfg) -> int:
     return gate + dispatch + gather + 2
 
 
+# DRAM bytes (read + write) of one expert-MLP launch from one ncu capture
+# (1-pass dram__bytes_read.sum + dram__bytes_write.sum on GB300, the commands
+# in profiles/dram_traffic_full_size.md), valid for the kernel source whose
+# hash is given; any later change to that source reports null.
+MLP_TRAFFIC = {"source_sha256_16": "f85821a92f05df9e",
+               "bytes": {"decode": 604.47e6 + 3.38e6, "prefill": 16.40e9 + 572.05e6}}
+MLP_SOURCES = ["mixture_experts_routed_gate_gb300/csrc/grouped_gemm.cu",
+               "mixture_experts_routed_gate_gb300/csrc/common.cuh"]
+
+
+def mlp_traffic(workload: str):
+    import hashlib
+    h = hashlib.sha256()
+    root = os.path.dirname(os.path.abspath(__file__))
+    for f in MLP_SOURCES:
+        with open(os.path.join(root, f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest()[:16] != MLP_TRAFFIC["source_sha256_16"]:
+        return None
+    return MLP_TRAFFIC["bytes"].get(workload)
+
+
 def forward_stages(T: int) -> list:
     """The entry points of one forward, in order (moe_forward makes the same
     calls; for T <= 64 the expert MLP gathers its rows and there is no gather)."""
@@ -688,13 +710,13 @@ def main():
         achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
         rl = {"kernel": "grouped_gemm_kernel<MLP>", "bound": "hbm", "achieved": round(achieved, 1),
               "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-              "traffic": None, "peak_source": peak_src + " (hbm_gbs)",
+              "traffic": mlp_traffic(cfg.name), "peak_source": peak_src + " (hbm_gbs)",
               "algorithmic_bytes_per_launch": gu_bytes, "launch_us": round(gu_ms * 1e3, 2)}
     else:
         achieved = gu_flops / (gu_ms * 1e-3) / 1e12
         rl = {"kernel": "grouped_gemm_kernel<MLP>", "bound": "tensor", "achieved": round(achieved, 1),
               "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-              "traffic": None, "peak_source": peak_src + " (bf16_tflops)",
+              "traffic": mlp_traffic(cfg.name), "peak_source": peak_src + " (bf16_tflops)",
               "algorithmic_flops_per_launch": gu_flops, "launch_us": round(gu_ms * 1e3, 2)}
     bytes_min = roofline.moe_forward_bytes_min(T, d_h, d_e, E, round(e_act), es)
     step_roof_ms = max(bytes_min / (peaks["hbm_gbs"] * 1e9), flops_step / (peaks["bf16_tflops"] * 1e12)) * 1e3
