@@ -14,7 +14,8 @@
  *           (routing, sort, tables, scatter-reduce), "tilelang kernel stage 1
  *           gate+up" and "tilelang kernel stage 2 down".
  *   [SKEL]  TileLang tutorial ch.18 skeletons.py, moe_routed_kernel (the
- *           dispatch contract and the two kernels).
+ *           dispatch contract and the two kernels), w4a8_dequant_gemm (the
+ *           int4 weight format) and the module notes on quantisation.
  *   [PR55]  TileOPs-Metax PR #55 "[moe_reduce_fused] feat": section 1
  *           (kernel semantics), section 2 (accuracy), section 3 (roofline).
  *   The gate body is not printed on any page; its reading (softmax over fp32
@@ -629,6 +630,139 @@ int oracle_grouped_down(const void *h, const void *w_down, const int32_t *group_
     gemm_ctx c = {h, w_down, NULL, group_sizes, group_offsets, group_padded_offsets,
                   group_idx_for_bx, row_weights, block_m, n_rows, d_h, d_e, E, dtype, y, 2};
     parallel_for(m_blocks, nthreads, gemm_blocks, &c);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* o4q: the expert MLP with int4 weights (weight-only, W4A16).                 */
+/* ------------------------------------------------------------------------- */
+/*
+ * [SKEL w4a8_dequant_gemm]: the weight is int4, two values per uint8 byte;
+ * element j of a row sits in byte j / 2, nibble j % 2 counted from the low
+ * end, and is sign-extended (two's complement, -8 .. 7) when unpacked on
+ * chip; the unpacked value is cast to the compute type and fed to the GEMM.
+ * [SKEL quantisation notes]: weight-only W4A16 is the same kernel with
+ * 16-bit activations.  Reading (the pages print no scale): an optional fp32
+ * scale per output channel multiplies the fp32 sum (NULL = the plain int4
+ * value), i.e. for stage 1
+ *   G = (sum_j a_j * q_gate[g,n,j]) * s_gate[g,n],  U likewise with s_up,
+ *   h = rt(silu(G) * U)
+ * and for stage 2  y = rt((sum_i h_i * q_down[g,o,i]) * s_down[g,o] (* rw)).
+ * Every product a * q is exact in fp32; sums in ascending index.
+ */
+void oracle_unpack_int4(const uint8_t *packed, int64_t n, int8_t *out)
+{
+    for (int64_t j = 0; j < n; ++j) {
+        const int nib = (packed[j / 2] >> (4 * (int)(j % 2))) & 0xF;
+        out[j] = (int8_t)(nib >= 8 ? nib - 16 : nib);
+    }
+}
+
+typedef struct {
+    const void *a; const int8_t *q1, *q2; const float *s1, *s2;
+    const int32_t *sizes, *offsets, *padded, *gidx;
+    const float *row_weights;
+    int64_t block_m, n_rows, d_h, d_e, E; int dtype; void *out;
+    int stage;
+} gemm_q_ctx;
+
+static void stage1_row_q(const gemm_q_ctx *c, int64_t r, int64_t g)
+{
+    for (int64_t n = 0; n < c->d_e; ++n) {
+        const int64_t wrow = (g * c->d_e + n) * c->d_h;
+        float gate = 0.0f, up = 0.0f;
+        for (int64_t j = 0; j < c->d_h; ++j) {
+            float av = load_elem(c->a, r * c->d_h + j, c->dtype);
+            gate = gate + av * (float)c->q1[wrow + j];
+            up = up + av * (float)c->q2[wrow + j];
+        }
+        if (c->s1) gate = gate * c->s1[g * c->d_e + n];
+        if (c->s2) up = up * c->s2[g * c->d_e + n];
+        float sv = (float)silu_d((double)gate);
+        store_elem(c->out, r * c->d_e + n, c->dtype, sv * up);
+    }
+}
+
+static void stage2_row_q(const gemm_q_ctx *c, int64_t r, int64_t g)
+{
+    for (int64_t o = 0; o < c->d_h; ++o) {
+        const int64_t wrow = (g * c->d_h + o) * c->d_e;
+        float acc = 0.0f;
+        for (int64_t j = 0; j < c->d_e; ++j)
+            acc = acc + load_elem(c->a, r * c->d_e + j, c->dtype) * (float)c->q1[wrow + j];
+        if (c->s1) acc = acc * c->s1[g * c->d_h + o];
+        if (c->row_weights) acc = acc * c->row_weights[r];
+        store_elem(c->out, r * c->d_h + o, c->dtype, acc);
+    }
+}
+
+/* the block walk of the CSDN stage kernels (see gemm_blocks), int4 weights */
+static void gemm_q_blocks(int64_t lo, int64_t hi, void *vctx)
+{
+    gemm_q_ctx *c = (gemm_q_ctx *)vctx;
+    const int64_t B = c->block_m;
+    for (int64_t bx = lo; bx < hi; ++bx) {
+        int64_t g = c->gidx[bx];
+        int64_t m_start = bx * B - c->padded[g] + c->offsets[g];
+        int64_t rows = c->sizes[g] - (bx * B - c->padded[g]);
+        if (rows > B) rows = B;
+        if (rows < 0) rows = 0;
+        for (int64_t i = 0; i < rows; ++i) {
+            if (c->stage == 1) stage1_row_q(c, m_start + i, g);
+            else stage2_row_q(c, m_start + i, g);
+        }
+    }
+}
+
+/* q_gate, q_up: [E, d_e, d_h / 2] packed bytes; s_gate, s_up: [E, d_e] or NULL */
+int oracle_grouped_gate_up_silu_w4(const void *a, const uint8_t *q_gate, const uint8_t *q_up,
+                                   const float *s_gate, const float *s_up,
+                                   const int32_t *group_sizes, const int32_t *group_offsets,
+                                   const int32_t *group_padded_offsets,
+                                   const int32_t *group_idx_for_bx, int64_t m_blocks,
+                                   int64_t block_m, int64_t n_rows, int64_t d_h, int64_t d_e,
+                                   int64_t E, int dtype, void *h, int nthreads)
+{
+    oracle_init();
+    if (!a || !q_gate || !q_up || !h || d_h <= 0 || d_h % 2 != 0 || d_e <= 0 ||
+        (dtype != 0 && dtype != 1) ||
+        !check_tables(group_sizes, group_offsets, group_padded_offsets, group_idx_for_bx,
+                      m_blocks, n_rows, E, block_m))
+        return OR_EINVAL;
+    const int64_t n = E * d_e * d_h;
+    int8_t *qg = (int8_t *)malloc((size_t)n), *qu = (int8_t *)malloc((size_t)n);
+    if (!qg || !qu) { free(qg); free(qu); return OR_EINVAL; }
+    oracle_unpack_int4(q_gate, n, qg);
+    oracle_unpack_int4(q_up, n, qu);
+    gemm_q_ctx c = {a, qg, qu, s_gate, s_up, group_sizes, group_offsets, group_padded_offsets,
+                    group_idx_for_bx, NULL, block_m, n_rows, d_h, d_e, E, dtype, h, 1};
+    parallel_for(m_blocks, nthreads, gemm_q_blocks, &c);
+    free(qg);
+    free(qu);
+    return OR_OK;
+}
+
+/* q_down: [E, d_h, d_e / 2] packed bytes; s_down: [E, d_h] or NULL */
+int oracle_grouped_down_w4(const void *h, const uint8_t *q_down, const float *s_down,
+                           const int32_t *group_sizes, const int32_t *group_offsets,
+                           const int32_t *group_padded_offsets, const int32_t *group_idx_for_bx,
+                           int64_t m_blocks, int64_t block_m, const float *row_weights,
+                           int64_t n_rows, int64_t d_h, int64_t d_e, int64_t E, int dtype,
+                           void *y, int nthreads)
+{
+    oracle_init();
+    if (!h || !q_down || !y || d_h <= 0 || d_e <= 0 || d_e % 2 != 0 || (dtype != 0 && dtype != 1) ||
+        !check_tables(group_sizes, group_offsets, group_padded_offsets, group_idx_for_bx,
+                      m_blocks, n_rows, E, block_m))
+        return OR_EINVAL;
+    const int64_t n = E * d_h * d_e;
+    int8_t *qd = (int8_t *)malloc((size_t)n);
+    if (!qd) return OR_EINVAL;
+    oracle_unpack_int4(q_down, n, qd);
+    gemm_q_ctx c = {h, qd, NULL, s_down, NULL, group_sizes, group_offsets, group_padded_offsets,
+                    group_idx_for_bx, row_weights, block_m, n_rows, d_h, d_e, E, dtype, y, 2};
+    parallel_for(m_blocks, nthreads, gemm_q_blocks, &c);
+    free(qd);
     return OR_OK;
 }
 

@@ -65,6 +65,10 @@ def _load():
         "oracle_moe_tokens_dense": (I, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I64, I, P, I]),
         "oracle_rows_gate_up_silu": (I, [P, P, I64, P, P, I64, I64, I64, I, P, I]),
         "oracle_rows_down": (I, [P, P, I64, P, P, I64, I64, I64, I, P, I]),
+        "oracle_unpack_int4": (None, [P, I64, P]),
+        "oracle_grouped_gate_up_silu_w4": (I, [P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I64,
+                                               I, P, I]),
+        "oracle_grouped_down_w4": (I, [P, P, P, P, P, P, P, I64, I64, P, I64, I64, I64, I64, I, P, I]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -213,6 +217,59 @@ def grouped_down(h, w_down, tables: dict, dtype: str, row_weights=None, block_m:
     _check(_load().oracle_grouped_down(
         _ptr(hb), _ptr(wd), _ptr(s), _ptr(o), _ptr(p), _ptr(g), g.size, block_m, _ptr(rw),
         n_rows, d_h, d_e, E, DTYPE_CODES[dtype], _ptr(y), nthreads), "grouped_down")
+    return y
+
+
+def unpack_int4(packed: np.ndarray, n: int) -> np.ndarray:
+    """int8 values of n int4 elements packed two per byte (element j: byte
+    j // 2, nibble j % 2 from the low end, two's complement)."""
+    pk = np.ascontiguousarray(packed, dtype=np.uint8)
+    if pk.size * 2 < n:
+        raise ValueError("not enough packed bytes")
+    out = np.empty(n, dtype=np.int8)
+    _load().oracle_unpack_int4(_ptr(pk), n, _ptr(out))
+    return out
+
+
+def _f32_or_none(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float32)
+
+
+def grouped_gate_up_silu_w4(a, q_gate, q_up, tables: dict, dtype: str, s_gate=None, s_up=None,
+                            block_m: int = 128, nthreads: int = 0) -> np.ndarray:
+    """Stage 1 with int4 weights: q_gate / q_up [E, d_e, d_h // 2] uint8 packed
+    as the pages print it; s_gate / s_up [E, d_e] fp32 or None."""
+    ab = _bits(a, dtype)
+    qg, qu = np.ascontiguousarray(q_gate, np.uint8), np.ascontiguousarray(q_up, np.uint8)
+    n_rows, d_h = ab.shape
+    E, d_e, half = qg.shape
+    if half * 2 != d_h or qu.shape != qg.shape:
+        raise ValueError("q_gate / q_up must be [E, d_e, d_h // 2]")
+    sg, su = _f32_or_none(s_gate), _f32_or_none(s_up)
+    s, o, p, g = _tables(tables)
+    h = _empty((n_rows, d_e), dtype)
+    _check(_load().oracle_grouped_gate_up_silu_w4(
+        _ptr(ab), _ptr(qg), _ptr(qu), _ptr(sg), _ptr(su), _ptr(s), _ptr(o), _ptr(p), _ptr(g), g.size,
+        block_m, n_rows, d_h, d_e, E, DTYPE_CODES[dtype], _ptr(h), nthreads), "grouped_gate_up_silu_w4")
+    return h
+
+
+def grouped_down_w4(h, q_down, tables: dict, dtype: str, s_down=None, row_weights=None,
+                    block_m: int = 128, nthreads: int = 0) -> np.ndarray:
+    """Stage 2 with int4 weights: q_down [E, d_h, d_e // 2] uint8; s_down [E, d_h] or None."""
+    hb = _bits(h, dtype)
+    qd = np.ascontiguousarray(q_down, np.uint8)
+    n_rows, d_e = hb.shape
+    E, d_h, half = qd.shape
+    if half * 2 != d_e:
+        raise ValueError("q_down must be [E, d_h, d_e // 2]")
+    sd = _f32_or_none(s_down)
+    rw = _f32_or_none(row_weights)
+    s, o, p, g = _tables(tables)
+    y = _empty((n_rows, d_h), dtype)
+    _check(_load().oracle_grouped_down_w4(
+        _ptr(hb), _ptr(qd), _ptr(sd), _ptr(s), _ptr(o), _ptr(p), _ptr(g), g.size, block_m, _ptr(rw),
+        n_rows, d_h, d_e, E, DTYPE_CODES[dtype], _ptr(y), nthreads), "grouped_down_w4")
     return y
 
 

@@ -556,3 +556,87 @@ def test_e4m3_output_is_the_rounded_fp32_result(oracle):
     f32, _ = oracle.reduce_fused_scaled(x, pos, w, None, sf, "f32", "f32")
     f8, _ = oracle.reduce_fused_scaled(x, pos, w, None, sf, "f32", "e4m3")
     assert np.array_equal(f8, oracle.encode(f32, "e4m3"))
+
+
+# --------------------------------------------------------------------------- #
+# int4 weights (skeletons.py w4a8_dequant_gemm; weight-only W4A16)
+# --------------------------------------------------------------------------- #
+
+def _pack_int4(q: np.ndarray) -> np.ndarray:
+    """Test-side packer, the inverse of the pages' layout: element 2i in the
+    low nibble of byte i, element 2i + 1 in the high nibble."""
+    u = (q.astype(np.int16) & 0xF).astype(np.uint8)
+    u = u.reshape(*q.shape[:-1], q.shape[-1] // 2, 2)
+    return (u[..., 0] | (u[..., 1] << 4)).astype(np.uint8)
+
+
+def test_unpack_int4_hand_decoded_bytes(oracle):
+    with open(os.path.join(GOLDEN, "int4_unpack_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        got = oracle.unpack_int4(np.array(c["bytes"], np.uint8), len(c["values"]))
+        assert got.tolist() == c["values"], c
+
+
+def test_unpack_int4_inverts_packing_of_every_pair(oracle):
+    vals = np.array([(a, b) for a in range(-8, 8) for b in range(-8, 8)], np.int8).reshape(-1)
+    packed = _pack_int4(vals)
+    assert packed.size == 256 and len(set(packed.tolist())) == 256
+    assert np.array_equal(oracle.unpack_int4(packed, vals.size), vals)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_w4_stages_equal_fp_stages_on_the_same_integers(oracle, dtype):
+    """Unscaled int4 weights are integers -8..7, exact in fp16 and bf16: the
+    int4 stages must give the bits of the plain stages fed those integers."""
+    rng = np.random.default_rng(21)
+    T, k, E, d_h, d_e = 150, 2, 4, 64, 32
+    _, tab = _random_tables(oracle, rng, T, k, E)
+    a = _enc(rng.standard_normal((T * k, d_h)) * 0.5, dtype)
+    qg = rng.integers(-8, 8, (E, d_e, d_h)).astype(np.int8)
+    qu = rng.integers(-8, 8, (E, d_e, d_h)).astype(np.int8)
+    qd = rng.integers(-8, 8, (E, d_h, d_e)).astype(np.int8)
+    h_q = oracle.grouped_gate_up_silu_w4(a, _pack_int4(qg), _pack_int4(qu), tab, dtype)
+    h_f = oracle.grouped_gate_up_silu(a, _enc(qg, dtype), _enc(qu, dtype), tab, dtype)
+    assert np.array_equal(h_q, h_f)
+    y_q = oracle.grouped_down_w4(h_q, _pack_int4(qd), tab, dtype)
+    y_f = oracle.grouped_down(h_q, _enc(qd, dtype), tab, dtype)
+    assert np.array_equal(y_q, y_f)
+    ones_e = np.ones((E, d_e), np.float32)
+    assert np.array_equal(oracle.grouped_gate_up_silu_w4(a, _pack_int4(qg), _pack_int4(qu), tab, dtype,
+                                                         s_gate=ones_e, s_up=ones_e), h_q)
+
+
+def test_w4_stages_integer_closed_form_and_pow2_scales(oracle):
+    """fp16, integer operands, gate logits >= 40 (silu(G) = G in fp32):
+    h = G * U and y = h Q_down^T exactly; a power-of-two scale per output
+    channel scales h (through up) and y exactly."""
+    rng = np.random.default_rng(22)
+    T, k, E, d_h, d_e = 200, 2, 3, 16, 16
+    _, tab = _random_tables(oracle, rng, T, k, E)
+    Tk = T * k
+    a = rng.integers(0, 2, (Tk, d_h)).astype(np.float32)
+    a[:, 0] = 6
+    qg = rng.integers(0, 2, (E, d_e, d_h)).astype(np.int8)
+    qg[:, :, 0] = 7
+    qu = rng.integers(-1, 2, (E, d_e, d_h)).astype(np.int8)
+    qu[:, :, 0] = 0
+    h = oracle.grouped_gate_up_silu_w4(_bits_f16(a), _pack_int4(qg), _pack_int4(qu), tab, "f16")
+    expert_of_row = np.repeat(np.arange(E), tab["group_sizes"])
+    ai = a.astype(np.int64)
+    G = np.einsum("rj,rnj->rn", ai, qg.astype(np.int64)[expert_of_row])
+    U = np.einsum("rj,rnj->rn", ai, qu.astype(np.int64)[expert_of_row])
+    assert G.min() >= 40 and np.abs(G * U).max() < 2048
+    assert np.array_equal(oracle.decode(h, "f16"), (G * U).astype(np.float32))
+    s_up = rng.choice([0.5, 2.0, 4.0], (E, d_e)).astype(np.float32)
+    h2 = oracle.grouped_gate_up_silu_w4(_bits_f16(a), _pack_int4(qg), _pack_int4(qu), tab, "f16", s_up=s_up)
+    assert np.array_equal(oracle.decode(h2, "f16"), (G * U * s_up[expert_of_row]).astype(np.float32))
+    hi = rng.integers(-2, 3, (Tk, d_e)).astype(np.float32)
+    qd = rng.integers(-8, 8, (E, d_h, d_e)).astype(np.int8)
+    y = oracle.grouped_down_w4(_bits_f16(hi), _pack_int4(qd), tab, "f16")
+    Y = np.einsum("rn,ron->ro", hi.astype(np.int64), qd.astype(np.int64)[expert_of_row])
+    assert np.abs(Y).max() <= 2048
+    assert np.array_equal(oracle.decode(y, "f16"), Y.astype(np.float32))
+    s_down = rng.choice([0.25, 1.0, 2.0], (E, d_h)).astype(np.float32)
+    y2 = oracle.grouped_down_w4(_bits_f16(hi), _pack_int4(qd), tab, "f16", s_down=s_down)
+    assert np.array_equal(oracle.decode(y2, "f16"), (Y * s_down[expert_of_row]).astype(np.float32))
