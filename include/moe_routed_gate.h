@@ -222,6 +222,46 @@ MOE_API moe_status_t moe_grouped_mlp(const void *a, const void *w_gate, const vo
                              int32_t *err_flag, moe_stream_t stream);
 
 /*
+ * Weight-only int4 experts (W4A16; TileLang tutorial ch.18 skeletons.py,
+ * w4a8_dequant_gemm and its notes on quantisation: int4 weights two per
+ * byte, element j of a row in byte j/2 at nibble j%2 from the low end, two's
+ * complement, unpacked on chip and cast to the 16-bit compute type).
+ *
+ * moe_pack_int4_weights: rewrites n_bytes of weights in that format (any
+ * [E, N, K/2] stack, K % 8 == 0) into the layout the int4 kernels read
+ * (inside every 4-byte word: elements 2m, 2m+1 in nibbles m, m+4, stored as
+ * value + 8).  Device pointers, 4-byte aligned, n_bytes % 4 == 0; plain and
+ * packed may be the same buffer.  Done once when the weights are loaded.
+ */
+MOE_API moe_status_t moe_pack_int4_weights(const uint8_t *plain, int64_t n_bytes, uint8_t *packed,
+                                   moe_stream_t stream);
+
+/*
+ * Both expert stages in one launch with int4 weights, for 1 <= T <= 64
+ * tokens (every expert then holds at most 64 rows):
+ *   stage 1: G = (A q_gate[g]^T) * s_gate[g], U = (A q_up[g]^T) * s_up[g],
+ *            h = rt(silu(G) * U)       (A: rows of x gathered by sorted_token_idx)
+ *   stage 2: y = rt((h q_down[g]^T) * s_down[g] (* row_weights))
+ * in fp32 accumulators; q_* are moe_pack_int4_weights output: q_gate / q_up
+ * [E, d_e, d_h/2], q_down [E, d_h, d_e/2] bytes; s_* fp32 per output channel
+ * ([E, d_e], [E, d_e], [E, d_h]) or NULL for 1 (the pages print no scale;
+ * reading: a per-channel scale on the fp32 sum).  x [T, d_h] in `dtype`;
+ * h [n_rows, d_e], y [n_rows, d_h]; ready as moe_grouped_mlp (m_blocks + 1
+ * int32, zeroed by this call).  d_h % 64 == 0, d_e % 64 == 0,
+ * m_blocks <= 1088 (else MOE_ERR_UNSUPPORTED).  Waits bounded as
+ * moe_grouped_mlp.
+ */
+MOE_API moe_status_t moe_grouped_mlp_w4a16(const void *x, const int32_t *sorted_token_idx, int64_t T,
+                                   const uint8_t *q_gate, const uint8_t *q_up, const uint8_t *q_down,
+                                   const float *s_gate, const float *s_up, const float *s_down,
+                                   const int32_t *group_sizes, const int32_t *group_offsets,
+                                   const int32_t *group_padded_offsets,
+                                   const int32_t *group_idx_for_bx, int64_t m_blocks,
+                                   const float *row_weights, int64_t n_rows, int64_t d_h, int64_t d_e,
+                                   int64_t E, moe_dtype_t dtype, void *h, void *y, int32_t *ready,
+                                   int32_t *err_flag, moe_stream_t stream);
+
+/*
  * moe_reduce_fused (TileOPs-Metax PR #55, section 1): for every token t and
  * hidden element h,
  *   out[t, h] = cast( sum over k ascending with 0 <= pos[t,k] < n_rows of
@@ -274,6 +314,18 @@ MOE_API moe_status_t moe_forward(const void *x, const void *w_g, const float *bi
                          const void *w_up, const void *w_down, int64_t T, int64_t d_h,
                          int64_t d_e, int64_t E, int64_t k, moe_dtype_t dtype, void *ws,
                          size_t ws_bytes, void *out, int32_t *err_flag, moe_stream_t stream);
+
+/*
+ * moe_forward with int4 experts (moe_grouped_mlp_w4a16 as the expert MLP),
+ * for 1 <= T <= 64 tokens; the gate weight w_g stays in `dtype`.  Same
+ * workspace (moe_forward_workspace_bytes) and outputs as moe_forward.
+ */
+MOE_API moe_status_t moe_forward_w4a16(const void *x, const void *w_g, const float *bias,
+                               const uint8_t *q_gate, const uint8_t *q_up, const uint8_t *q_down,
+                               const float *s_gate, const float *s_up, const float *s_down,
+                               int64_t T, int64_t d_h, int64_t d_e, int64_t E, int64_t k,
+                               moe_dtype_t dtype, void *ws, size_t ws_bytes, void *out,
+                               int32_t *err_flag, moe_stream_t stream);
 
 /*
  * Offsets (bytes from the workspace start) of moe_forward's intermediates, for

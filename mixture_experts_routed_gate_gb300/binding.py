@@ -64,6 +64,10 @@ def lib():
         "moe_reduce_fused": (I, [P, I64, P, P, I64, I64, I64, I, I, P, P, P]),
         "moe_reduce_fused_scaled": (I, [P, I64, P, P, P, P, I64, I64, I64, I, I, P, P, P]),
         "moe_forward": (I, [P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, SZ, P, P, P]),
+        "moe_pack_int4_weights": (I, [P, I64, P, P]),
+        "moe_grouped_mlp_w4a16": (I, [P, P, I64, P, P, P, P, P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I,
+                                      P, P, P, P, P]),
+        "moe_forward_w4a16": (I, [P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, SZ, P, P, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -79,7 +83,8 @@ def exported_symbols():
             "moe_forward_workspace_offset", "moe_gate_topk", "moe_build_dispatch",
             "moe_build_dispatch_noalloc",
             "moe_gather_rows", "moe_grouped_gate_up_silu", "moe_grouped_down",
-            "moe_grouped_mlp", "moe_reduce_fused", "moe_reduce_fused_scaled", "moe_forward"]
+            "moe_grouped_mlp", "moe_pack_int4_weights", "moe_grouped_mlp_w4a16",
+            "moe_forward_w4a16", "moe_reduce_fused", "moe_reduce_fused_scaled", "moe_forward"]
 
 
 # --------------------------------------------------------------------------- helpers
@@ -333,6 +338,105 @@ def moe_grouped_mlp(a, w_gate, w_up, w_down, tables, row_weights=None, h=None, y
             _ptr(sorted_token_idx), x.shape[0] if gathering else 0, _ptr(err), _stream(src.device)),
             "moe_grouped_mlp")
     return h, y
+
+
+def moe_pack_int4_weights(plain, packed=None):
+    """int4 weights as the pages pack them (uint8, two per byte, element j in
+    byte j // 2 at nibble j % 2 from the low end) -> the layout the int4
+    kernels read (same shape)."""
+    _cuda(plain, "plain", dtype=torch.uint8)
+    if plain.numel() % 4 != 0:
+        raise ValueError("the packed weights must hold a multiple of 4 bytes")
+    if packed is None:
+        packed = torch.empty_like(plain)
+    _cuda(packed, "packed", dtype=torch.uint8)
+    if packed.numel() != plain.numel():
+        raise ValueError("packed must have the size of plain")
+    with torch.cuda.device(plain.device):
+        _check(lib().moe_pack_int4_weights(_ptr(plain), plain.numel(), _ptr(packed), _stream(plain.device)),
+               "moe_pack_int4_weights")
+    return packed
+
+
+def _scale(t, name, shape):
+    if t is None:
+        return None
+    _cuda(t, name, dtype=torch.float32)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be {tuple(shape)}")
+    return t
+
+
+def moe_grouped_mlp_w4a16(x, sorted_token_idx, q_gate, q_up, q_down, tables, s_gate=None, s_up=None,
+                          s_down=None, row_weights=None, h=None, y=None, ready=None, err=None):
+    """Both expert stages with int4 weights (moe_pack_int4_weights layout),
+    rows gathered from x [T <= 64, d_h]; returns (h, y)."""
+    _cuda(x, "x", ndim=2)
+    _cuda(sorted_token_idx, "sorted_token_idx", dtype=torch.int32)
+    for n, t in (("q_gate", q_gate), ("q_up", q_up), ("q_down", q_down)):
+        _cuda(t, n, dtype=torch.uint8, ndim=3)
+    T, d_h = x.shape
+    E, d_e, half = q_gate.shape
+    if half * 2 != d_h or q_up.shape != q_gate.shape or tuple(q_down.shape) != (E, d_h, d_e // 2):
+        raise ValueError("q_gate / q_up must be [E, d_e, d_h // 2] and q_down [E, d_h, d_e // 2]")
+    s_gate = _scale(s_gate, "s_gate", (E, d_e))
+    s_up = _scale(s_up, "s_up", (E, d_e))
+    s_down = _scale(s_down, "s_down", (E, d_h))
+    s, o, p, g = _tables(tables)
+    n_rows = sorted_token_idx.numel()
+    if row_weights is not None:
+        _cuda(row_weights, "row_weights", dtype=torch.float32)
+    if h is None:
+        h = torch.empty((n_rows, d_e), dtype=x.dtype, device=x.device)
+    if y is None:
+        y = torch.empty((n_rows, d_h), dtype=x.dtype, device=x.device)
+    if ready is None:
+        ready = torch.empty(g.numel() + 1, dtype=torch.int32, device=x.device)
+    _cuda(h, "h", dtype=x.dtype)
+    _cuda(y, "y", dtype=x.dtype)
+    _cuda(ready, "ready", dtype=torch.int32)
+    if ready.numel() < g.numel() + 1:
+        raise ValueError("ready needs one int32 per M block plus one")
+    if err is not None:
+        _cuda(err, "err", dtype=torch.int32)
+    with torch.cuda.device(x.device):
+        _check(lib().moe_grouped_mlp_w4a16(
+            _ptr(x), _ptr(sorted_token_idx), T, _ptr(q_gate), _ptr(q_up), _ptr(q_down), _ptr(s_gate),
+            _ptr(s_up), _ptr(s_down), _ptr(s), _ptr(o), _ptr(p), _ptr(g), g.numel(), _ptr(row_weights),
+            n_rows, d_h, d_e, E, _dtype_code(x, "x"), _ptr(h), _ptr(y), _ptr(ready), _ptr(err),
+            _stream(x.device)), "moe_grouped_mlp_w4a16")
+    return h, y
+
+
+def moe_forward_w4a16(x, w_g, bias, q_gate, q_up, q_down, k: int, s_gate=None, s_up=None, s_down=None,
+                      ws=None, out=None, err=None):
+    """The routed forward with int4 experts for up to 64 tokens; returns out [T, d_hidden]."""
+    _cuda(x, "x", ndim=2)
+    _cuda(w_g, "w_g", dtype=x.dtype)
+    if bias is not None:
+        _cuda(bias, "bias", dtype=torch.float32, ndim=1)
+    for n, t in (("q_gate", q_gate), ("q_up", q_up), ("q_down", q_down)):
+        _cuda(t, n, dtype=torch.uint8, ndim=3)
+    T, d_h = x.shape
+    E, d_e, _ = q_gate.shape
+    s_gate = _scale(s_gate, "s_gate", (E, d_e))
+    s_up = _scale(s_up, "s_up", (E, d_e))
+    s_down = _scale(s_down, "s_down", (E, d_h))
+    need = forward_workspace_bytes(T, d_h, d_e, E, k, x.dtype)
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _cuda(ws, "ws", dtype=torch.uint8)
+    if out is None:
+        out = torch.empty((T, d_h), dtype=x.dtype, device=x.device)
+    _cuda(out, "out", dtype=x.dtype)
+    if err is not None:
+        _cuda(err, "err", dtype=torch.int32)
+    with torch.cuda.device(x.device):
+        _check(lib().moe_forward_w4a16(
+            _ptr(x), _ptr(w_g), _ptr(bias), _ptr(q_gate), _ptr(q_up), _ptr(q_down), _ptr(s_gate), _ptr(s_up),
+            _ptr(s_down), T, d_h, d_e, E, k, _dtype_code(x, "x"), _ptr(ws), ws.numel(), _ptr(out), _ptr(err),
+            _stream(x.device)), "moe_forward_w4a16")
+    return out
 
 
 def moe_reduce_fused(x, token_topk_to_pos, topk_weights=None, out_dtype=None, out=None, err=None):

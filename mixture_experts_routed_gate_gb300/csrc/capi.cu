@@ -285,6 +285,64 @@ moe_status_t moe_grouped_mlp(const void *a, const void *w_gate, const void *w_up
                        ready, err_flag, stream, true, x, sorted_token_idx, T);
 }
 
+moe_status_t moe_pack_int4_weights(const uint8_t *plain, int64_t n_bytes, uint8_t *packed,
+                                   moe_stream_t stream) {
+    if (n_bytes < 0 || n_bytes % 4 != 0) return MOE_ERR_INVALID_ARG;
+    if (n_bytes == 0) return MOE_OK;
+    if (!plain || !packed || (reinterpret_cast<uintptr_t>(plain) & 3u) ||
+        (reinterpret_cast<uintptr_t>(packed) & 3u))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_status(moe::launch_pack_int4(plain, n_bytes, packed, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// zero_ready as in grouped_mlp
+static moe_status_t grouped_mlp_w4(const void *x, const int32_t *sorted_token_idx, int64_t T,
+                                   const uint8_t *q_gate, const uint8_t *q_up, const uint8_t *q_down,
+                                   const float *s_gate, const float *s_up, const float *s_down,
+                                   const int32_t *group_sizes, const int32_t *group_offsets,
+                                   const int32_t *group_padded_offsets,
+                                   const int32_t *group_idx_for_bx, int64_t m_blocks,
+                                   const float *row_weights, int64_t n_rows, int64_t d_h, int64_t d_e,
+                                   int64_t E, moe_dtype_t dtype, void *h, void *y, int32_t *ready,
+                                   int32_t *err_flag, moe_stream_t stream, bool zero_ready) {
+    if (!is_half_type(dtype)) return MOE_ERR_UNSUPPORTED;
+    if (d_h <= 0 || d_e <= 0 || d_h % 64 != 0 || d_e % 64 != 0) return MOE_ERR_INVALID_ARG;
+    if (T <= 0 || T > 64) return MOE_ERR_INVALID_ARG;
+    if (n_rows == 0) return MOE_OK;
+    moe_status_t st = check_gemm_tables(group_sizes, group_offsets, group_padded_offsets,
+                                        group_idx_for_bx, m_blocks, n_rows, E);
+    if (st != MOE_OK) return st;
+    if (m_blocks > 1088) return MOE_ERR_UNSUPPORTED;
+    if (!x || !sorted_token_idx || !q_gate || !q_up || !q_down || !h || !y || !ready)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q_gate) || !aligned16(q_up) || !aligned16(q_down) ||
+        !aligned16(h) || !aligned16(y))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (zero_ready) {
+        cudaError_t e = cudaMemsetAsync(ready, 0, static_cast<size_t>(m_blocks + 1) * 4, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return cuda_status(moe::launch_grouped_mlp_w4(
+        dtype, x, sorted_token_idx, T, q_gate, q_up, q_down, s_gate, s_up, s_down, group_sizes,
+        group_offsets, group_padded_offsets, group_idx_for_bx, m_blocks, row_weights, n_rows, d_h, d_e,
+        E, h, y, ready, err_flag, s));
+}
+
+moe_status_t moe_grouped_mlp_w4a16(const void *x, const int32_t *sorted_token_idx, int64_t T,
+                                   const uint8_t *q_gate, const uint8_t *q_up, const uint8_t *q_down,
+                                   const float *s_gate, const float *s_up, const float *s_down,
+                                   const int32_t *group_sizes, const int32_t *group_offsets,
+                                   const int32_t *group_padded_offsets,
+                                   const int32_t *group_idx_for_bx, int64_t m_blocks,
+                                   const float *row_weights, int64_t n_rows, int64_t d_h, int64_t d_e,
+                                   int64_t E, moe_dtype_t dtype, void *h, void *y, int32_t *ready,
+                                   int32_t *err_flag, moe_stream_t stream) {
+    return grouped_mlp_w4(x, sorted_token_idx, T, q_gate, q_up, q_down, s_gate, s_up, s_down,
+                          group_sizes, group_offsets, group_padded_offsets, group_idx_for_bx, m_blocks,
+                          row_weights, n_rows, d_h, d_e, E, dtype, h, y, ready, err_flag, stream, true);
+}
+
 static bool reduce_pair_ok(moe_dtype_t in, moe_dtype_t out, bool allow_fp8) {
     const bool in_ok = in == MOE_F16 || in == MOE_BF16 || in == MOE_F32;
     if (!in_ok) return false;
@@ -380,5 +438,53 @@ moe_status_t moe_forward(const void *x, const void *w_g, const float *bias, cons
     if (st != MOE_OK) return st;
     return moe_reduce_fused(ybuf, Tk, pos, topk_w, T, k, d_h, dtype, dtype, out, err_flag, stream);
 }
+
+moe_status_t moe_forward_w4a16(const void *x, const void *w_g, const float *bias,
+                               const uint8_t *q_gate, const uint8_t *q_up, const uint8_t *q_down,
+                               const float *s_gate, const float *s_up, const float *s_down,
+                               int64_t T, int64_t d_h, int64_t d_e, int64_t E, int64_t k,
+                               moe_dtype_t dtype, void *ws, size_t ws_bytes, void *out,
+                               int32_t *err_flag, moe_stream_t stream) {
+    if (!is_half_type(dtype)) return MOE_ERR_UNSUPPORTED;
+    if (T < 0 || T > 64 || d_h <= 0 || d_e <= 0 || E <= 0 || k <= 0 || k > E || k > 32 || E > 1024)
+        return MOE_ERR_INVALID_ARG;
+    if (d_h % 256 != 0 || d_e % 64 != 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !w_g || !q_gate || !q_up || !q_down || !out || !ws) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_g)) return MOE_ERR_INVALID_ARG;
+    FwdLayout L;
+    if (!fwd_layout(T, d_h, d_e, E, k, dtype, &L)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    char *w = static_cast<char *>(ws);
+    float *logits = reinterpret_cast<float *>(w + L.off[0]);
+    int32_t *topk_idx = reinterpret_cast<int32_t *>(w + L.off[1]);
+    float *topk_w = reinterpret_cast<float *>(w + L.off[2]);
+    int32_t *sizes = reinterpret_cast<int32_t *>(w + L.off[3]);
+    int32_t *offsets = reinterpret_cast<int32_t *>(w + L.off[4]);
+    int32_t *padded = reinterpret_cast<int32_t *>(w + L.off[5]);
+    int32_t *gidx = reinterpret_cast<int32_t *>(w + L.off[6]);
+    int32_t *stok = reinterpret_cast<int32_t *>(w + L.off[7]);
+    float *sw = reinterpret_cast<float *>(w + L.off[8]);
+    int32_t *pos = reinterpret_cast<int32_t *>(w + L.off[9]);
+    void *scratch = w + L.off[10];
+    void *hbuf = w + L.off[12];
+    void *ybuf = w + L.off[13];
+    int32_t *ready = reinterpret_cast<int32_t *>(w + L.off[14]);
+    const int64_t Tk = T * k;
+    const int64_t mb = m_blocks_of(T, k, E, MOE_BLOCK_M);
+    moe_status_t st = moe_gate_topk(x, w_g, bias, T, d_h, E, k, dtype, topk_idx, topk_w, logits,
+                                    static_cast<size_t>(T) * E * 4, stream);
+    if (st != MOE_OK) return st;
+    st = build_dispatch(topk_idx, topk_w, T, k, E, MOE_BLOCK_M, sizes, offsets, padded, gidx, stok,
+                        sw, pos, scratch, moe::dispatch_scratch_bytes(Tk, E), ready, stream);
+    if (st != MOE_OK) return st;
+    st = grouped_mlp_w4(x, stok, T, q_gate, q_up, q_down, s_gate, s_up, s_down, sizes, offsets,
+                        padded, gidx, mb, nullptr, Tk, d_h, d_e, E, dtype, hbuf, ybuf, ready, err_flag,
+                        stream, false);
+    if (st != MOE_OK) return st;
+    return moe_reduce_fused(ybuf, Tk, pos, topk_w, T, k, d_h, dtype, dtype, out, err_flag, stream);
+}
+
 
 }  // extern "C"

@@ -727,6 +727,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
+// Any tensor map: dims / strides (bytes, dims 1..rank-1) / box, innermost first.
+bool encode_tma_map(CUtensorMap *m, int data_type, int rank, const void *ptr, const uint64_t *dims,
+                    const uint64_t *strides_bytes, const uint32_t *box, int swizzle_128b) {
+    auto fn = encode_fn();
+    if (!fn || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], e[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        e[i] = 1;
+        if (i + 1 < rank) st[i] = strides_bytes[i];
+    }
+    CUresult r = fn(m, static_cast<CUtensorMapDataType>(data_type), static_cast<cuuint32_t>(rank),
+                    const_cast<void *>(ptr), d, st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle_128b ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Row-major [rows, inner] 16-bit matrix, box = box_inner x box_rows, no swizzle.
 bool encode_tma_2d_plain(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows,
                          uint32_t box_inner, uint32_t box_rows) {

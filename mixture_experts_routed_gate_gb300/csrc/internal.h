@@ -16,6 +16,11 @@ int device_sm_count();
 // box = box_inner x box_rows elements, no swizzle.  False if encoding fails.
 bool encode_tma_2d_plain(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows,
                          uint32_t box_inner, uint32_t box_rows);
+// grouped_gemm.cu: any tensor map (CUtensorMapDataType in data_type); dims,
+// box innermost first; strides in bytes for dims 1..rank-1; 128-byte swizzle
+// or none.  False if encoding fails.
+bool encode_tma_map(CUtensorMap *m, int data_type, int rank, const void *ptr, const uint64_t *dims,
+                    const uint64_t *strides_bytes, const uint32_t *box, int swizzle_128b);
 
 // gate_topk.cu: logits (written to `logits`, [T, E] fp32), top-k ids and weights
 cudaError_t launch_gate_topk(const void *x, const void *wg, const float *bias, int64_t T,
@@ -56,5 +61,22 @@ cudaError_t launch_grouped_mlp(int dtype, const void *a, const void *w_gate, con
                                int64_t E, void *h, void *y, int32_t *ready, int32_t *err,
                                cudaStream_t stream, const void *x = nullptr,
                                const int32_t *gather_idx = nullptr, int64_t T = 0);
+
+// grouped_gemm_w4.cu: int4 weights, two per byte as the pages pack them, into
+// the layout the int4 kernels read (n_bytes % 4 == 0).
+cudaError_t launch_pack_int4(const uint8_t *plain, int64_t n_bytes, uint8_t *packed,
+                             cudaStream_t stream);
+// Both expert stages with int4 weights (packed by launch_pack_int4) and
+// optional fp32 scales per output channel; stage-1 rows gathered from x
+// [T, d_h] by gather_idx (T <= 64, so every block has at most 64 rows);
+// `ready` (m_blocks + 1 int32) zero at kernel start.
+cudaError_t launch_grouped_mlp_w4(int dtype, const void *x, const int32_t *gather_idx, int64_t T,
+                                  const uint8_t *q_gate, const uint8_t *q_up, const uint8_t *q_down,
+                                  const float *s_gate, const float *s_up, const float *s_down,
+                                  const int32_t *sizes, const int32_t *offsets,
+                                  const int32_t *padded, const int32_t *gidx, int64_t m_blocks,
+                                  const float *row_weights, int64_t n_rows, int64_t d_h,
+                                  int64_t d_e, int64_t E, void *h, void *y, int32_t *ready,
+                                  int32_t *err, cudaStream_t stream);
 
 }  // namespace moe
