@@ -384,9 +384,81 @@ def run_native(args, cfg, rank, world, dev):
 
     e2e = measure_e2e(args, cfg, d, dev, flush, world)
     aux = measure_reduce_aux(dev, flush) if rank == 0 else None
-    return dict(per_stage=per_stage, stages=list(step.stages), total_ms=total_ms, act_experts=act_experts,
+    w4 = measure_w4(cfg, d, dev, flush) if rank == 0 and cfg.T <= 64 else None
+    return dict(per_stage=per_stage, stages=list(step.stages), w4=w4, total_ms=total_ms, act_experts=act_experts,
                 sizes_pool=sizes_pool, clocks=clocks, e2e=e2e, aux=aux, mode=mode,
                 eager_ms=float(np.median(eager_ms)), wall_s=t_wall)
+
+
+def quantize_int4(w):
+    """Per-output-channel symmetric int4 of a stacked [E, N, K] weight:
+    s = max|w| / 7 over K, q = clamp(round(w / s), -8, 7), packed two per
+    byte in the pages' order ([E, N, K // 2] uint8).  Setup only."""
+    wf = w.float()
+    s = (wf.abs().amax(dim=2) / 7.0).clamp_min(1e-12)
+    q = torch.clamp(torch.round(wf / s[..., None]), -8, 7).to(torch.int16)
+    plain = ((q[..., 0::2] & 0xF) | ((q[..., 1::2] & 0xF) << 4)).to(torch.uint8).contiguous()
+    return plain, s.contiguous()
+
+
+def measure_w4(cfg, d, dev, flush, steps: int = 200):
+    """The decode forward with int4 experts (moe_forward_w4a16; the same
+    random-init weights quantised per output channel), and its expert MLP
+    alone against the weight-streaming roofline."""
+    from mixture_experts_routed_gate_gb300 import binding
+    T, d_h, d_e, E, k = cfg.T, cfg.d_hidden, cfg.d_expert, cfg.n_experts, cfg.top_k
+    qg, sg = quantize_int4(d["w_gate"])
+    qu, su = quantize_int4(d["w_up"])
+    qd, sd = quantize_int4(d["w_down"])
+    ex = binding.Int4Experts(qg, qu, qd, sg, su, sd)
+    del qg, qu, qd
+    ws = torch.empty(binding.forward_workspace_bytes(T, d_h, d_e, E, k, d["x"].dtype), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty((T, d_h), dtype=d["x"].dtype, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    v = binding.forward_workspace_views(ws, T, d_h, d_e, E, k, d["x"].dtype)
+    tables = {n: v[n] for n in ("group_sizes", "group_offsets", "group_padded_offsets", "group_idx_for_bx")}
+    fwd = lambda: binding.moe_forward_w4a16(d["x"], d["wg"], d["bias"], ex, k, ws=ws, out=out, err=err)
+    ready = torch.empty(tables["group_idx_for_bx"].numel() + 1, dtype=torch.int32, device=dev)
+    mlp = lambda: binding.moe_grouped_mlp_w4a16(d["x"], v["sorted_token_idx"], ex, tables, h=v["h"], y=v["y"],
+                                                ready=ready, err=err)
+    stream = torch.cuda.Stream(dev)
+    res = {}
+    with torch.cuda.stream(stream):
+        fwd()
+        mlp()
+        stream.synchronize()
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error flag {int(err.item())} in the int4 forward")
+        sizes = v["group_sizes"].cpu().numpy()
+        e_act = int((sizes > 0).sum())
+        for name, fn in (("forward", fwd), ("expert_mlp", mlp)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            for _ in range(3):
+                flush()
+                g.replay()
+            ts = []
+            for _ in range(steps):
+                flush()
+                s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s_.record(stream)
+                g.replay()
+                e_.record(stream)
+                e_.synchronize()
+                ts.append(s_.elapsed_time(e_))
+            res[name] = float(np.mean(ts))
+    Tk = T * k
+    w_bytes = 3 * e_act * d_e * d_h // 2 + 4 * e_act * (2 * d_e + d_h)
+    mlp_bytes = w_bytes + Tk * (2 * d_h + 2 * d_e) * 2
+    peaks, _ = load_peaks()
+    gbs = mlp_bytes / (res["expert_mlp"] * 1e-3) / 1e9
+    return {"weights": "int4 per output channel (symmetric, max|w|/7), fp32 scales", "active_experts": e_act,
+            "ms_per_step": round(res["forward"], 5), "tokens_per_s": round(T / (res["forward"] * 1e-3), 1),
+            "expert_mlp_us": round(res["expert_mlp"] * 1e3, 2), "expert_mlp_bytes": mlp_bytes,
+            "expert_mlp_gbs": round(gbs, 1), "expert_mlp_frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "expert_mlp_note": "the standalone call includes the stream memset of its counters"}
 
 
 def measure_e2e(args, cfg, d, dev, flush, world):
@@ -732,6 +804,7 @@ def main():
         "active_experts": e_act,
         "roofline": rl,
         "reduce_fused_bf16_x8_7168": res["aux"],
+        "w4a16": res["w4"],
         "cpu_baseline": {"value": round(cpu["value"], 2), "unit": "tokens/s", "cores": threads,
                          "kind": "oracle", "sample": cpu["sample"]},
         "e2e": {"value": round(aggregate_throughput(T * args.steps, world, e2e["total_ms"]), 1), "unit": "tokens/s",

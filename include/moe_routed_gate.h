@@ -227,14 +227,20 @@ MOE_API moe_status_t moe_grouped_mlp(const void *a, const void *w_gate, const vo
  * byte, element j of a row in byte j/2 at nibble j%2 from the low end, two's
  * complement, unpacked on chip and cast to the 16-bit compute type).
  *
- * moe_pack_int4_weights: rewrites n_bytes of weights in that format (any
- * [E, N, K/2] stack, K % 8 == 0) into the layout the int4 kernels read
- * (inside every 4-byte word: elements 2m, 2m+1 in nibbles m, m+4, stored as
- * value + 8).  Device pointers, 4-byte aligned, n_bytes % 4 == 0; plain and
- * packed may be the same buffer.  Done once when the weights are loaded.
+ * moe_pack_int4_bytes / moe_pack_int4_weights: a stacked weight [E, N, K]
+ * in that format (plain: E*N*K/2 bytes) rewritten into the tiled layout the
+ * int4 kernels read: tiles of tile_rows output channels (128 for W_gate and
+ * W_up, N = d_e, K = d_h; 256 for W_down, N = d_h, K = d_e), stored
+ * [E][ceil(N/tile_rows)][K/64][tile_rows][32 bytes] so that one 64-wide K
+ * step of a tile is one contiguous block; inside each 4-byte word elements
+ * 2m, 2m+1 sit in nibbles m, m+4 as value + 8; rows past N hold zeros.
+ * moe_pack_int4_bytes returns the packed size (-1 for K % 64 != 0, sizes
+ * <= 0 or another tile_rows).  Device pointers, 16-byte aligned, distinct.
+ * Done once when the weights are loaded.
  */
-MOE_API moe_status_t moe_pack_int4_weights(const uint8_t *plain, int64_t n_bytes, uint8_t *packed,
-                                   moe_stream_t stream);
+MOE_API int64_t moe_pack_int4_bytes(int64_t E, int64_t N, int64_t K, int64_t tile_rows);
+MOE_API moe_status_t moe_pack_int4_weights(const uint8_t *plain, int64_t E, int64_t N, int64_t K,
+                                   int64_t tile_rows, uint8_t *packed, moe_stream_t stream);
 
 /*
  * Both expert stages in one launch with int4 weights, for 1 <= T <= 64
@@ -242,8 +248,8 @@ MOE_API moe_status_t moe_pack_int4_weights(const uint8_t *plain, int64_t n_bytes
  *   stage 1: G = (A q_gate[g]^T) * s_gate[g], U = (A q_up[g]^T) * s_up[g],
  *            h = rt(silu(G) * U)       (A: rows of x gathered by sorted_token_idx)
  *   stage 2: y = rt((h q_down[g]^T) * s_down[g] (* row_weights))
- * in fp32 accumulators; q_* are moe_pack_int4_weights output: q_gate / q_up
- * [E, d_e, d_h/2], q_down [E, d_h, d_e/2] bytes; s_* fp32 per output channel
+ * in fp32 accumulators; q_* are moe_pack_int4_weights output (q_gate, q_up
+ * with tile_rows 128, q_down with 256); s_* fp32 per output channel
  * ([E, d_e], [E, d_e], [E, d_h]) or NULL for 1 (the pages print no scale;
  * reading: a per-channel scale on the fp32 sum).  x [T, d_h] in `dtype`;
  * h [n_rows, d_e], y [n_rows, d_h]; ready as moe_grouped_mlp (m_blocks + 1

@@ -64,7 +64,8 @@ def lib():
         "moe_reduce_fused": (I, [P, I64, P, P, I64, I64, I64, I, I, P, P, P]),
         "moe_reduce_fused_scaled": (I, [P, I64, P, P, P, P, I64, I64, I64, I, I, P, P, P]),
         "moe_forward": (I, [P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, SZ, P, P, P]),
-        "moe_pack_int4_weights": (I, [P, I64, P, P]),
+        "moe_pack_int4_bytes": (I64, [I64, I64, I64, I64]),
+        "moe_pack_int4_weights": (I, [P, I64, I64, I64, I64, P, P]),
         "moe_grouped_mlp_w4a16": (I, [P, P, I64, P, P, P, P, P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I,
                                       P, P, P, P, P]),
         "moe_forward_w4a16": (I, [P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, SZ, P, P, P]),
@@ -83,7 +84,7 @@ def exported_symbols():
             "moe_forward_workspace_offset", "moe_gate_topk", "moe_build_dispatch",
             "moe_build_dispatch_noalloc",
             "moe_gather_rows", "moe_grouped_gate_up_silu", "moe_grouped_down",
-            "moe_grouped_mlp", "moe_pack_int4_weights", "moe_grouped_mlp_w4a16",
+            "moe_grouped_mlp", "moe_pack_int4_bytes", "moe_pack_int4_weights", "moe_grouped_mlp_w4a16",
             "moe_forward_w4a16", "moe_reduce_fused", "moe_reduce_fused_scaled", "moe_forward"]
 
 
@@ -340,22 +341,40 @@ def moe_grouped_mlp(a, w_gate, w_up, w_down, tables, row_weights=None, h=None, y
     return h, y
 
 
-def moe_pack_int4_weights(plain, packed=None):
-    """int4 weights as the pages pack them (uint8, two per byte, element j in
-    byte j // 2 at nibble j % 2 from the low end) -> the layout the int4
-    kernels read (same shape)."""
-    _cuda(plain, "plain", dtype=torch.uint8)
-    if plain.numel() % 4 != 0:
-        raise ValueError("the packed weights must hold a multiple of 4 bytes")
-    if packed is None:
-        packed = torch.empty_like(plain)
-    _cuda(packed, "packed", dtype=torch.uint8)
-    if packed.numel() != plain.numel():
-        raise ValueError("packed must have the size of plain")
+def moe_pack_int4_weights(plain, tile_rows: int):
+    """A stacked int4 weight in the pages' format (uint8 [E, N, K // 2]: two
+    per byte, element j in byte j // 2 at nibble j % 2 from the low end) ->
+    the tiled layout the int4 kernels read (tile_rows 128 for W_gate / W_up,
+    256 for W_down); returns a flat uint8 tensor."""
+    _cuda(plain, "plain", dtype=torch.uint8, ndim=3)
+    E, N, half = plain.shape
+    nbytes = int(lib().moe_pack_int4_bytes(E, N, 2 * half, tile_rows))
+    if nbytes < 0:
+        raise ValueError("K must be a multiple of 64 and tile_rows 128 or 256")
+    packed = torch.empty(nbytes, dtype=torch.uint8, device=plain.device)
     with torch.cuda.device(plain.device):
-        _check(lib().moe_pack_int4_weights(_ptr(plain), plain.numel(), _ptr(packed), _stream(plain.device)),
-               "moe_pack_int4_weights")
+        _check(lib().moe_pack_int4_weights(_ptr(plain), E, N, 2 * half, tile_rows, _ptr(packed),
+                                           _stream(plain.device)), "moe_pack_int4_weights")
     return packed
+
+
+class Int4Experts:
+    """The three expert weights of a layer in the int4 kernels' layout, with
+    their per-channel scales (or None)."""
+
+    def __init__(self, q_gate, q_up, q_down, s_gate=None, s_up=None, s_down=None):
+        """q_gate, q_up: uint8 [E, d_e, d_h // 2]; q_down: [E, d_h, d_e // 2] in
+        the pages' int4 format; s_*: fp32 [E, d_e], [E, d_e], [E, d_h] or None."""
+        self.E, self.d_e, half = q_gate.shape
+        self.d_h = 2 * half
+        if tuple(q_up.shape) != tuple(q_gate.shape) or tuple(q_down.shape) != (self.E, self.d_h, self.d_e // 2):
+            raise ValueError("q_gate / q_up must be [E, d_e, d_h // 2] and q_down [E, d_h, d_e // 2]")
+        self.q_gate = moe_pack_int4_weights(q_gate, 128)
+        self.q_up = moe_pack_int4_weights(q_up, 128)
+        self.q_down = moe_pack_int4_weights(q_down, 256)
+        self.s_gate = _scale(s_gate, "s_gate", (self.E, self.d_e))
+        self.s_up = _scale(s_up, "s_up", (self.E, self.d_e))
+        self.s_down = _scale(s_down, "s_down", (self.E, self.d_h))
 
 
 def _scale(t, name, shape):
@@ -367,21 +386,16 @@ def _scale(t, name, shape):
     return t
 
 
-def moe_grouped_mlp_w4a16(x, sorted_token_idx, q_gate, q_up, q_down, tables, s_gate=None, s_up=None,
-                          s_down=None, row_weights=None, h=None, y=None, ready=None, err=None):
-    """Both expert stages with int4 weights (moe_pack_int4_weights layout),
-    rows gathered from x [T <= 64, d_h]; returns (h, y)."""
+def moe_grouped_mlp_w4a16(x, sorted_token_idx, experts: "Int4Experts", tables, row_weights=None, h=None,
+                          y=None, ready=None, err=None):
+    """Both expert stages with int4 weights, rows gathered from x [T <= 64, d_h];
+    returns (h, y)."""
     _cuda(x, "x", ndim=2)
     _cuda(sorted_token_idx, "sorted_token_idx", dtype=torch.int32)
-    for n, t in (("q_gate", q_gate), ("q_up", q_up), ("q_down", q_down)):
-        _cuda(t, n, dtype=torch.uint8, ndim=3)
     T, d_h = x.shape
-    E, d_e, half = q_gate.shape
-    if half * 2 != d_h or q_up.shape != q_gate.shape or tuple(q_down.shape) != (E, d_h, d_e // 2):
-        raise ValueError("q_gate / q_up must be [E, d_e, d_h // 2] and q_down [E, d_h, d_e // 2]")
-    s_gate = _scale(s_gate, "s_gate", (E, d_e))
-    s_up = _scale(s_up, "s_up", (E, d_e))
-    s_down = _scale(s_down, "s_down", (E, d_h))
+    E, d_e = experts.E, experts.d_e
+    if d_h != experts.d_h:
+        raise ValueError("x and the experts disagree on d_hidden")
     s, o, p, g = _tables(tables)
     n_rows = sorted_token_idx.numel()
     if row_weights is not None:
@@ -399,29 +413,26 @@ def moe_grouped_mlp_w4a16(x, sorted_token_idx, q_gate, q_up, q_down, tables, s_g
         raise ValueError("ready needs one int32 per M block plus one")
     if err is not None:
         _cuda(err, "err", dtype=torch.int32)
+    q = experts
     with torch.cuda.device(x.device):
         _check(lib().moe_grouped_mlp_w4a16(
-            _ptr(x), _ptr(sorted_token_idx), T, _ptr(q_gate), _ptr(q_up), _ptr(q_down), _ptr(s_gate),
-            _ptr(s_up), _ptr(s_down), _ptr(s), _ptr(o), _ptr(p), _ptr(g), g.numel(), _ptr(row_weights),
+            _ptr(x), _ptr(sorted_token_idx), T, _ptr(q.q_gate), _ptr(q.q_up), _ptr(q.q_down), _ptr(q.s_gate),
+            _ptr(q.s_up), _ptr(q.s_down), _ptr(s), _ptr(o), _ptr(p), _ptr(g), g.numel(), _ptr(row_weights),
             n_rows, d_h, d_e, E, _dtype_code(x, "x"), _ptr(h), _ptr(y), _ptr(ready), _ptr(err),
             _stream(x.device)), "moe_grouped_mlp_w4a16")
     return h, y
 
 
-def moe_forward_w4a16(x, w_g, bias, q_gate, q_up, q_down, k: int, s_gate=None, s_up=None, s_down=None,
-                      ws=None, out=None, err=None):
+def moe_forward_w4a16(x, w_g, bias, experts: "Int4Experts", k: int, ws=None, out=None, err=None):
     """The routed forward with int4 experts for up to 64 tokens; returns out [T, d_hidden]."""
     _cuda(x, "x", ndim=2)
     _cuda(w_g, "w_g", dtype=x.dtype)
     if bias is not None:
         _cuda(bias, "bias", dtype=torch.float32, ndim=1)
-    for n, t in (("q_gate", q_gate), ("q_up", q_up), ("q_down", q_down)):
-        _cuda(t, n, dtype=torch.uint8, ndim=3)
     T, d_h = x.shape
-    E, d_e, _ = q_gate.shape
-    s_gate = _scale(s_gate, "s_gate", (E, d_e))
-    s_up = _scale(s_up, "s_up", (E, d_e))
-    s_down = _scale(s_down, "s_down", (E, d_h))
+    E, d_e = experts.E, experts.d_e
+    if d_h != experts.d_h:
+        raise ValueError("x and the experts disagree on d_hidden")
     need = forward_workspace_bytes(T, d_h, d_e, E, k, x.dtype)
     if ws is None:
         ws = torch.empty(need, dtype=torch.uint8, device=x.device)
@@ -431,11 +442,12 @@ def moe_forward_w4a16(x, w_g, bias, q_gate, q_up, q_down, k: int, s_gate=None, s
     _cuda(out, "out", dtype=x.dtype)
     if err is not None:
         _cuda(err, "err", dtype=torch.int32)
+    q = experts
     with torch.cuda.device(x.device):
         _check(lib().moe_forward_w4a16(
-            _ptr(x), _ptr(w_g), _ptr(bias), _ptr(q_gate), _ptr(q_up), _ptr(q_down), _ptr(s_gate), _ptr(s_up),
-            _ptr(s_down), T, d_h, d_e, E, k, _dtype_code(x, "x"), _ptr(ws), ws.numel(), _ptr(out), _ptr(err),
-            _stream(x.device)), "moe_forward_w4a16")
+            _ptr(x), _ptr(w_g), _ptr(bias), _ptr(q.q_gate), _ptr(q.q_up), _ptr(q.q_down), _ptr(q.s_gate),
+            _ptr(q.s_up), _ptr(q.s_down), T, d_h, d_e, E, k, _dtype_code(x, "x"), _ptr(ws), ws.numel(),
+            _ptr(out), _ptr(err), _stream(x.device)), "moe_forward_w4a16")
     return out
 
 

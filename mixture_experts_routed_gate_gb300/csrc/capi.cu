@@ -285,14 +285,18 @@ moe_status_t moe_grouped_mlp(const void *a, const void *w_gate, const void *w_up
                        ready, err_flag, stream, true, x, sorted_token_idx, T);
 }
 
-moe_status_t moe_pack_int4_weights(const uint8_t *plain, int64_t n_bytes, uint8_t *packed,
-                                   moe_stream_t stream) {
-    if (n_bytes < 0 || n_bytes % 4 != 0) return MOE_ERR_INVALID_ARG;
-    if (n_bytes == 0) return MOE_OK;
-    if (!plain || !packed || (reinterpret_cast<uintptr_t>(plain) & 3u) ||
-        (reinterpret_cast<uintptr_t>(packed) & 3u))
+int64_t moe_pack_int4_bytes(int64_t E, int64_t N, int64_t K, int64_t tile_rows) {
+    if (tile_rows != 128 && tile_rows != 256) return -1;
+    return moe::pack_int4_bytes(E, N, K, static_cast<int>(tile_rows));
+}
+
+moe_status_t moe_pack_int4_weights(const uint8_t *plain, int64_t E, int64_t N, int64_t K,
+                                   int64_t tile_rows, uint8_t *packed, moe_stream_t stream) {
+    if (moe_pack_int4_bytes(E, N, K, tile_rows) < 0) return MOE_ERR_INVALID_ARG;
+    if (!plain || !packed || plain == packed || !aligned16(plain) || !aligned16(packed))
         return MOE_ERR_INVALID_ARG;
-    return cuda_status(moe::launch_pack_int4(plain, n_bytes, packed, reinterpret_cast<cudaStream_t>(stream)));
+    return cuda_status(moe::launch_pack_int4(plain, E, N, K, static_cast<int>(tile_rows), packed,
+                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // zero_ready as in grouped_mlp

@@ -10,23 +10,30 @@
 // kernel with 16-bit activations is the weight-only W4A16 form).  Reading: an
 // optional fp32 scale per output channel multiplies the fp32 sum.
 //
-// launch_pack_int4 moves each 32-bit word of that format (8 elements) into
-// the order the converter wants -- elements 2m and 2m+1 in nibbles m and
-// m+4 -- stored offset-binary (value + 8), so that one AND-OR with the fp16
-// (or bf16) exponent of 1024 (128) and one packed subtraction of 1032 (136)
-// give two exact values.
+// launch_pack_int4 rewrites a stacked [E, N, K] weight in that format into
+// tiles of R output channels (R = 128 for W_gate / W_up, 256 for W_down):
+// [E][ceil(N/R)][K/64][R rows][32 bytes], so that the 64-wide K step of one
+// tile is one contiguous block (one bulk copy, sequential DRAM reads), rows
+// past N holding zeros.  Inside each 32-bit word (8 elements) elements 2m
+// and 2m+1 move to nibbles m and m+4, stored offset-binary (value + 8), so
+// one AND-OR with the fp16 (or bf16) exponent of 1024 (128) and one packed
+// subtraction of 1032 (136) give two exact values.
 //
-// Kernel (one persistent CTA per SM, 320 threads):
-//   warp 0      producer: per 64-wide K step, one stage of a 9-deep ring:
-//               the block's rows (stage 1: up to 64 token rows gathered from
-//               x by four-row TMA gathers; stage 2: 64 rows of h) and the
-//               packed weights of 256 output channels (8 KB);
-//   warps 6..9  converters: unpack the stage's 256 x 64 weights into one of
-//               two 32 KB tiles in the 128-byte swizzled K-major layout the
-//               tensor cores read (the layout TMA gives 16-bit weights);
-//   warp 1      MMA: tcgen05.mma M=128 N=rows (two per K=16 step: weight
-//               halves as the M operand, the block's rows as N) into a TMEM
-//               accumulator, double buffered;
+// Kernel (one persistent CTA per SM, 448 threads):
+//   warp 0      producer: per 128-wide K step (two 64-wide sub-steps), one
+//               stage of a 6-deep ring: the block's rows (stage 1: up to 64
+//               token rows gathered from x by four-row TMA gathers; stage 2:
+//               64 rows of h) and the packed weights of 256 output channels
+//               (16 KB, bulk copies of contiguous tile blocks);
+//   warps 6..13 converters: unpack the stage's 256 x 64 weights straight into
+//               tensor memory (tcgen05.st; thread = TMEM lane = output
+//               channel), one of two 128-column A buffers;
+//   warp 1      MMA: tcgen05.mma M=128 N=rows with the A operand (the weights,
+//               two 128-channel halves) read from tensor memory and the
+//               block's rows as the shared-memory B operand, into a TMEM
+//               accumulator, double buffered.  Unpacking into tensor memory
+//               keeps the 16-bit weights off shared memory: per step only the
+//               8 KB of packed weights and the rows pass through it;
 //   warps 2..5  epilogue: scales, silu(gate)*up for stage 1, row-masked
 //               stores; a stage-1 warp-tile publishes its h rows on the
 //               block's counter for the stage-2 tiles.
@@ -42,41 +49,41 @@
 namespace moe {
 namespace {
 
-constexpr int W4_BK = 64;                        // K elements per step
+constexpr int W4_BK = 64;                        // K elements per sub-step (one packed block)
+constexpr int W4_SUB = 2;                        // sub-steps per pipeline stage (K = 128)
 constexpr int W4_ROWS = 256;                     // weight rows (output channels) per tile
-constexpr int W4_PACK_ROW = W4_BK / 2;           // 32 packed bytes per row and step
-constexpr int W4_PACK_BYTES = W4_ROWS * W4_PACK_ROW;  // 8 KB
+constexpr int W4_PACK_ROW = W4_BK / 2;           // 32 packed bytes per row and sub-step
+constexpr int W4_PACK_SUB = W4_ROWS * W4_PACK_ROW;      // 8 KB
+constexpr int W4_PACK_BYTES = W4_SUB * W4_PACK_SUB;     // 16 KB
 constexpr int W4_TOK_ROWS = 64;                  // the most rows a block may hold here
-constexpr int W4_TOK_BYTES = W4_TOK_ROWS * W4_BK * 2;  // 8 KB, 128-byte swizzled
+constexpr int W4_TOK_SUB = W4_TOK_ROWS * W4_BK * 2;     // 8 KB, 128-byte swizzled
+constexpr int W4_TOK_BYTES = W4_SUB * W4_TOK_SUB;       // 16 KB
 constexpr int W4_STAGE_BYTES = W4_TOK_BYTES + W4_PACK_BYTES;
-constexpr int W4_STAGES = 9;
-constexpr int W4_CONV_BYTES = W4_ROWS * W4_BK * 2;  // 32 KB, two 16 KB MMA operands
-constexpr int W4_CONVS = 2;
-constexpr int W4_THREADS = 320;
-constexpr int W4_CONV_WARP0 = 6;                 // converter warps 6..9
-constexpr int W4_CONV_WARPS = 4;
+constexpr int W4_STAGES = 6;
+constexpr int W4_CONVS = 2;                      // A buffers in tensor memory
+constexpr int W4_A_SUB = W4_BK;                  // columns per sub-step: 2 halves x 64 x 16-bit / 32-bit
+constexpr int W4_A_COLS = W4_SUB * W4_A_SUB;
+constexpr int W4_A_COL0 = 256;                   // A buffers after the two accumulators
+constexpr int W4_THREADS = 448;
+constexpr int W4_CONV_WARP0 = 6;                 // converter warps 6..13: two per TMEM lane quarter
+constexpr int W4_CONV_WARPS = 8;
 constexpr int W4_EPI_WARPS = 4;
 constexpr int W4_TRING = 4;
 constexpr int W4_ACC_COLS = 128;                 // 2 x up to 64 columns per accumulator
-constexpr int W4_TMEM_COLS = 256;
+constexpr int W4_TMEM_COLS = 512;
+static_assert(W4_A_COL0 + W4_CONVS * W4_A_COLS <= W4_TMEM_COLS && 2 * W4_ACC_COLS <= W4_A_COL0, "tmem");
+static_assert(W4_STAGES > W4_CONVS, "a stage is released W4_CONVS steps after its use");
 constexpr int W4_MAX_BLOCKS = 1088;              // M blocks the schedule lists
 constexpr int W4_BAR_BYTES = 512;
 constexpr int W4_SCHED_BYTES = W4_MAX_BLOCKS * (4 * 3 + 1) + 64 * 4;
-constexpr int W4_SMEM_BYTES = 1024 + W4_CONVS * W4_CONV_BYTES + W4_STAGES * W4_STAGE_BYTES +
-                              W4_BAR_BYTES + W4_SCHED_BYTES;
+constexpr int W4_SMEM_BYTES = 1024 + W4_STAGES * W4_STAGE_BYTES + W4_BAR_BYTES + W4_SCHED_BYTES;
 static_assert(W4_SMEM_BYTES <= 232448, "shared memory per CTA");
-static_assert(W4_STAGE_BYTES % 1024 == 0 && W4_CONV_BYTES % 1024 == 0, "swizzle atoms");
+static_assert(W4_STAGE_BYTES % 1024 == 0, "swizzle atoms");
 
 // ---------------------------------------------------------------------------
-// repack: one thread per 32-bit word (8 elements)
+// repack: one thread per 32-bit output word (8 elements)
 // ---------------------------------------------------------------------------
-__global__ void pack_int4_kernel(const uint32_t *__restrict__ plain, int64_t n_words,
-                                 uint32_t *__restrict__ packed) {
-    griddep_wait();
-    griddep_launch_dependents();
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i >= n_words) return;
-    const uint32_t w = plain[i];
+__device__ __forceinline__ uint32_t w4_reorder(uint32_t w) {
     uint32_t o = 0;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -84,12 +91,34 @@ __global__ void pack_int4_kernel(const uint32_t *__restrict__ plain, int64_t n_w
         const int slot = (e & 1) ? 4 + (e >> 1) : (e >> 1);
         o |= nib << (4 * slot);
     }
-    packed[i] = o ^ 0x88888888u;  // offset-binary: value + 8
+    return o ^ 0x88888888u;  // offset-binary: value + 8
+}
+
+// plain [E, N, K/2] bytes -> [E][NT = ceil(N/R)][S = K/64][R][32 bytes]
+__global__ void pack_int4_kernel(const uint32_t *__restrict__ plain, int64_t E, int64_t N, int64_t K,
+                                 int R, uint32_t *__restrict__ packed) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int64_t NT = (N + R - 1) / R, S = K / W4_BK;
+    const int64_t total = E * NT * S * R * 8;  // output words
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= total) return;
+    const int w = static_cast<int>(i & 7);
+    int64_t rest = i >> 3;
+    const int r = static_cast<int>(rest % R);
+    rest /= R;
+    const int64_t st = rest % S;
+    rest /= S;
+    const int64_t t = rest % NT;
+    const int64_t e = rest / NT;
+    const int64_t n = t * R + r;
+    packed[i] = n < N ? w4_reorder(plain[(e * N + n) * (K / 8) + st * 8 + w]) : 0x88888888u;  // zeros past N
 }
 
 struct W4Params {
     const int32_t *sizes, *offsets, *padded, *gidx;
     const int32_t *gather_idx;  // stage-1 rows: token indices into x
+    const uint8_t *q_gate, *q_up, *q_down;  // tiled packed weights (see launch_pack_int4)
     const float *row_weights;
     const float *s_gate, *s_up, *s_down;
     int *ready;         // per M block: stage-1 epilogue warp-tiles stored
@@ -97,7 +126,7 @@ struct W4Params {
     void *h, *y;
     int m_blocks, d_h, d_e;
     int nt0, nt1;       // output tiles per block: stage 1 (128 columns), stage 2 (256)
-    int kb0, kb1;       // K steps: stage 1 (d_h / 64), stage 2 (d_e / 64)
+    int kb0, kb1;       // 64-wide K sub-steps: stage 1 (d_h / 64), stage 2 (d_e / 64)
     int *err;
 };
 
@@ -133,6 +162,17 @@ __device__ __forceinline__ W4Tile w4_tile(const W4Params &p, const int *list, co
     return ti;
 }
 
+// bulk copy of `bytes` contiguous bytes (16-byte aligned) into shared memory,
+// completing on `bar`, with an L2 policy
+__device__ __forceinline__ void w4_bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                            uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+
 __device__ __forceinline__ void w4_wait_drain(uint32_t bar, uint32_t parity) {
     const unsigned long long start = global_timer_ns();
     while (!mbar_try_wait(bar, parity))
@@ -140,14 +180,35 @@ __device__ __forceinline__ void w4_wait_drain(uint32_t bar, uint32_t parity) {
 }
 
 // Unpack one 32-bit word (8 elements, the repacked layout) into 8 values of
-// the compute type, in element order.
+// the compute type, in element order.  fp16: nibbles at bits 0 and 16 OR-ed
+// into the mantissa of 1024 give 1024 + u (then minus 1032); nibbles at bits
+// 4 and 20 give 1024 + 16 u (then times 1/16 minus 72), so only the pairs
+// of the upper byte need a shift.  bf16 has 7 mantissa bits: every pair is
+// shifted down to bit 0 and 136 subtracted from 128 + u.
 template <int DT>
 __device__ __forceinline__ uint4 w4_unpack8(uint32_t w) {
     constexpr uint32_t MAGIC = DT == kBF16 ? 0x43004300u : 0x64006400u;  // 128 / 1024, twice
+    uint4 r;
+    if (DT == kF16) {
+        const uint32_t w8 = w >> 8;
+        uint32_t q[4];
+        q[0] = (w & 0x000F000Fu) | MAGIC;
+        q[1] = (w & 0x00F000F0u) | MAGIC;
+        q[2] = (w8 & 0x000F000Fu) | MAGIC;
+        q[3] = (w8 & 0x00F000F0u) | MAGIC;
+        const __half2 off = __floats2half2_rn(1032.0f, 1032.0f);
+        const __half2 sixteenth = __floats2half2_rn(0.0625f, 0.0625f), off16 = __floats2half2_rn(-72.0f, -72.0f);
+        const __half2 v0 = __hsub2(*reinterpret_cast<__half2 *>(&q[0]), off);
+        const __half2 v1 = __hfma2(*reinterpret_cast<__half2 *>(&q[1]), sixteenth, off16);
+        const __half2 v2 = __hsub2(*reinterpret_cast<__half2 *>(&q[2]), off);
+        const __half2 v3 = __hfma2(*reinterpret_cast<__half2 *>(&q[3]), sixteenth, off16);
+        r = make_uint4(*reinterpret_cast<const uint32_t *>(&v0), *reinterpret_cast<const uint32_t *>(&v1),
+                       *reinterpret_cast<const uint32_t *>(&v2), *reinterpret_cast<const uint32_t *>(&v3));
+        return r;
+    }
     uint32_t q[4];
 #pragma unroll
     for (int m = 0; m < 4; ++m) q[m] = ((w >> (4 * m)) & 0x000F000Fu) | MAGIC;
-    uint4 r;
     if (DT == kBF16) {
         const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
         __nv_bfloat162 v[4];
@@ -193,23 +254,20 @@ template <int DT>
 __global__ void __launch_bounds__(W4_THREADS, 1)
     grouped_mlp_w4_kernel(const __grid_constant__ CUtensorMap tmX,    // x [T, d_h], box 64 x 1
                           const __grid_constant__ CUtensorMap tmH,    // h [rows, d_e], box 64 x 64
-                          const __grid_constant__ CUtensorMap tmQg,   // [E, d_e, d_h/2] u8, box 32 x 128
-                          const __grid_constant__ CUtensorMap tmQu,
-                          const __grid_constant__ CUtensorMap tmQd,   // [E, d_h, d_e/2] u8, box 32 x 256
                           const W4Params p) {
     using OutT = typename Elem<DT>::T;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
-    uint8_t *conv = smem;                                      // [W4_CONVS][32 KB]
-    uint8_t *stages = conv + W4_CONVS * W4_CONV_BYTES;          // [W4_STAGES][tokens 8 KB | packed 8 KB]
+    uint8_t *stages = smem;                                     // [W4_STAGES][tokens 8 KB | packed 8 KB]
     uint64_t *bars = reinterpret_cast<uint64_t *>(stages + W4_STAGES * W4_STAGE_BYTES);
     // barriers: pfull, pempty [stages]; cfull, cempty [convs]; tfull, tempty [2]; tidf, tide [ring]
     constexpr int NBARS = 2 * W4_STAGES + 2 * W4_CONVS + 4 + 2 * W4_TRING;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *tid_ring = reinterpret_cast<int *>(tmem_slot + 2);
-    volatile int *stage_flag = reinterpret_cast<volatile int *>(tid_ring + W4_TRING);  // 1 = K step, 0 = end
+    // per stage: 16 * gemm stage + sub-steps held (1 or 2); 0 = no more stages
+    volatile int *stage_flag = reinterpret_cast<volatile int *>(tid_ring + W4_TRING);
     static_assert(NBARS * 8 + 8 + 4 * W4_TRING + 4 * W4_STAGES <= W4_BAR_BYTES, "barrier area");
     int *list = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(bars) + W4_BAR_BYTES);
     int *blk_g = list + W4_MAX_BLOCKS;
@@ -232,7 +290,9 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < W4_STAGES; ++s) {
             mbar_init(pfull(s), 1);
-            mbar_init(pempty(s), W4_CONV_WARPS + 1);  // every converter warp and the MMA's commit
+            // every converter warp, once both it and the MMA are done with the
+            // stage (see the converters: one MMA commit per step, not two)
+            mbar_init(pempty(s), W4_CONV_WARPS);
         }
         for (int c = 0; c < W4_CONVS; ++c) {
             mbar_init(cfull(c), W4_CONV_WARPS);
@@ -250,9 +310,6 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmX);
         tma_prefetch_desc(&tmH);
-        tma_prefetch_desc(&tmQg);
-        tma_prefetch_desc(&tmQu);
-        tma_prefetch_desc(&tmQd);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), W4_TMEM_COLS);
@@ -289,80 +346,118 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
-        if (lane == 0) {
-            const uint64_t pol_first = l2_policy_evict_first();  // weights are read once
-            int stage = 0;
-            uint32_t phase = 0;
-            long issued = 0;
-            bool ok = true;
-            int rslot = 0;
-            uint32_t rphase = 0;
-            int next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
-            for (int it = 0; ok; ++it) {
-                int tile = it == 0 ? static_cast<int>(blockIdx.x) : next_tile;
+        // the whole warp: lane 0 takes tiles, arms the stage barriers and
+        // issues the weight copies; lane j (< rows / 4) holds the token ids
+        // of rows 4j .. 4j+3 for the tile and issues their gather every step
+        const uint64_t pol_first = l2_policy_evict_first();  // weights are read once
+        int stage = 0;
+        uint32_t phase = 0;
+        long issued = 0;
+        bool ok = true;
+        int rslot = 0;
+        uint32_t rphase = 0;
+        int next_tile = 0;
+        if (lane == 0) next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
+        for (int it = 0; ok; ++it) {
+            int tile = 0;
+            int go = 1;
+            if (lane == 0) {
+                tile = it == 0 ? static_cast<int>(blockIdx.x) : next_tile;
                 if (it > 0) next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
                 if (tile >= total) tile = -1;
-                if (!mbar_wait_bounded(tide(rslot), rphase ^ 1u, abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                tid_ring[rslot] = tile;
-                mbar_arrive(tidf(rslot));
-                if (++rslot == W4_TRING) {
-                    rslot = 0;
-                    rphase ^= 1u;
-                }
-                if (tile < 0) break;
-                const W4Tile ti = w4_tile(p, list, blk_g, blk_m, blk_rows, n_blocks, tile);
-                // stage 2 reads its block's h rows: all stage-1 warp-tiles stored
-                if (ti.phase == 1 &&
-                    !counter_wait_bounded(p.ready + ti.bx, W4_EPI_WARPS * p.nt0, abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                int np = (ti.rows + 15) & ~15;
-                if (np > W4_TOK_ROWS) {  // the host admits at most 64 tokens
-                    np = W4_TOK_ROWS;
-                    if (p.err) atomicExch(p.err, kErrDeviceFlag);
-                }
-                const int kblocks = ti.phase == 0 ? p.kb0 : p.kb1;
-                const uint32_t tx = static_cast<uint32_t>((ti.phase == 0 ? np * W4_BK * 2 : W4_TOK_BYTES) +
-                                                          W4_PACK_BYTES);
-                const int32_t *ids = p.gather_idx + ti.m_start;
-                for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!mbar_wait_bounded(pempty(stage), phase ^ 1u, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *st = stages + stage * W4_STAGE_BYTES;
-                    const uint32_t tok = smem_u32(st), pk = smem_u32(st + W4_TOK_BYTES);
-                    const uint32_t fb = pfull(stage);
-                    stage_flag[stage] = 1;
-                    mbar_arrive_expect_tx(fb, tx);
-                    if (ti.phase == 0) {
-                        // four token rows per copy; rows past the block repeat its first row
-                        for (int r = 0; r < np; r += 4) {
-                            const int i0 = __ldg(ids + (r < ti.rows ? r : 0));
-                            const int i1 = __ldg(ids + (r + 1 < ti.rows ? r + 1 : 0));
-                            const int i2 = __ldg(ids + (r + 2 < ti.rows ? r + 2 : 0));
-                            const int i3 = __ldg(ids + (r + 3 < ti.rows ? r + 3 : 0));
-                            tma_gather4(tok + static_cast<uint32_t>(r * W4_BK * 2), &tmX, fb, kb * W4_BK, i0, i1,
-                                        i2, i3);
-                        }
-                        tma_load_3d_hint(pk, &tmQg, fb, kb * W4_PACK_ROW, ti.n0, ti.g, pol_first);
-                        tma_load_3d_hint(pk + W4_PACK_BYTES / 2, &tmQu, fb, kb * W4_PACK_ROW, ti.n0, ti.g,
-                                         pol_first);
-                    } else {
-                        tma_load_2d(tok, &tmH, fb, kb * W4_BK, ti.m_start);
-                        tma_load_3d_hint(pk, &tmQd, fb, kb * W4_PACK_ROW, ti.n0, ti.g, pol_first);
-                    }
-                    ++issued;
-                    if (++stage == W4_STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                go = mbar_wait_bounded(tide(rslot), rphase ^ 1u, abort_flag, p.err) ? 1 : 0;
+                if (go) {
+                    tid_ring[rslot] = tile;
+                    mbar_arrive(tidf(rslot));
                 }
             }
+            go = __shfl_sync(0xffffffffu, go, 0);
+            tile = __shfl_sync(0xffffffffu, tile, 0);
+            if (++rslot == W4_TRING) {
+                rslot = 0;
+                rphase ^= 1u;
+            }
+            if (!go) {
+                ok = false;
+                break;
+            }
+            if (tile < 0) break;
+            const W4Tile ti = w4_tile(p, list, blk_g, blk_m, blk_rows, n_blocks, tile);
+            // stage 2 reads its block's h rows: all stage-1 warp-tiles stored
+            if (ti.phase == 1) {
+                if (lane == 0)
+                    go = counter_wait_bounded(p.ready + ti.bx, W4_EPI_WARPS * p.nt0, abort_flag, p.err) ? 1 : 0;
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) {
+                    ok = false;
+                    break;
+                }
+            }
+            int np = (ti.rows + 15) & ~15;
+            if (np > W4_TOK_ROWS) {  // the host admits at most 64 tokens
+                np = W4_TOK_ROWS;
+                if (lane == 0 && p.err) atomicExch(p.err, kErrDeviceFlag);
+            }
+            // this lane's four token ids (rows past the block repeat its first row)
+            int i0 = 0, i1 = 0, i2 = 0, i3 = 0;
+            const bool gatherer = ti.phase == 0 && 4 * lane < np;
+            if (gatherer) {
+                const int32_t *ids = p.gather_idx + ti.m_start;
+                const int r = 4 * lane;
+                i0 = __ldg(ids + (r < ti.rows ? r : 0));
+                i1 = __ldg(ids + (r + 1 < ti.rows ? r + 1 : 0));
+                i2 = __ldg(ids + (r + 2 < ti.rows ? r + 2 : 0));
+                i3 = __ldg(ids + (r + 3 < ti.rows ? r + 3 : 0));
+            }
+            const int ksub = ti.phase == 0 ? p.kb0 : p.kb1;
+            const int kstages = (ksub + W4_SUB - 1) / W4_SUB;
+            for (int kb = 0; kb < kstages; ++kb) {
+                const int nsub = min(W4_SUB, ksub - kb * W4_SUB);
+                const uint32_t tx = static_cast<uint32_t>(nsub * ((ti.phase == 0 ? np * W4_BK * 2 : W4_TOK_SUB) +
+                                                                  W4_PACK_SUB));
+                if (lane == 0) go = mbar_wait_bounded(pempty(stage), phase ^ 1u, abort_flag, p.err) ? 1 : 0;
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *st = stages + stage * W4_STAGE_BYTES;
+                const uint32_t tok = smem_u32(st), pk = smem_u32(st + W4_TOK_BYTES);
+                const uint32_t fb = pfull(stage);
+                if (lane == 0) {
+                    stage_flag[stage] = 16 * ti.phase + nsub;
+                    mbar_arrive_expect_tx(fb, tx);
+                }
+                __syncwarp();  // the stage's byte count is armed before any copy lands
+                const int sub0 = kb * W4_SUB;  // first 64-wide sub-step of the stage
+                if (ti.phase == 0) {
+                    if (gatherer)
+                        for (int u = 0; u < nsub; ++u)
+                            tma_gather4(tok + static_cast<uint32_t>(u * W4_TOK_SUB + 4 * lane * W4_BK * 2), &tmX, fb,
+                                        (sub0 + u) * W4_BK, i0, i1, i2, i3);
+                    if (lane == 0) {
+                        // 128 gate rows for each sub-step, then 128 up rows (consecutive blocks)
+                        const int64_t blk = (static_cast<int64_t>(ti.g) * p.nt0 + ti.n0 / 128) * p.kb0 + sub0;
+                        const uint32_t bytes = static_cast<uint32_t>(nsub * W4_PACK_SUB / 2);
+                        w4_bulk_g2s(pk, p.q_gate + blk * (W4_PACK_SUB / 2), bytes, fb, pol_first);
+                        w4_bulk_g2s(pk + W4_PACK_BYTES / 2, p.q_up + blk * (W4_PACK_SUB / 2), bytes, fb, pol_first);
+                    }
+                } else if (lane == 0) {
+                    for (int u = 0; u < nsub; ++u)
+                        tma_load_2d(tok + static_cast<uint32_t>(u * W4_TOK_SUB), &tmH, fb, (sub0 + u) * W4_BK,
+                                    ti.m_start);
+                    const int64_t blk = (static_cast<int64_t>(ti.g) * p.nt1 + ti.n0 / 256) * p.kb1 + sub0;
+                    w4_bulk_g2s(pk, p.q_down + blk * W4_PACK_SUB, static_cast<uint32_t>(nsub * W4_PACK_SUB), fb,
+                                pol_first);
+                }
+                ++issued;
+                if (++stage == W4_STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (lane == 0) {
             if (ok && mbar_wait_bounded(pempty(stage), phase ^ 1u, abort_flag, p.err)) {
                 stage_flag[stage] = 0;  // the converters stop here
                 mbar_arrive(pfull(stage));
@@ -400,7 +495,8 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
                 }
                 if (tile < 0) break;
                 const W4Tile ti = w4_tile(p, list, blk_g, blk_m, blk_rows, n_blocks, tile);
-                const int kblocks = ti.phase == 0 ? p.kb0 : p.kb1;
+                const int ksub = ti.phase == 0 ? p.kb0 : p.kb1;
+                const int kstages = (ksub + W4_SUB - 1) / W4_SUB;
                 const int acc = local & 1;
                 const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
                 if (!mbar_wait_bounded(tempty(acc), acc_phase ^ 1u, abort_flag, p.err)) {
@@ -412,26 +508,31 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
                 int np = (ti.rows + 15) & ~15;
                 if (np > W4_TOK_ROWS) np = W4_TOK_ROWS;
                 const uint32_t idesc = idesc_f16(DT == kBF16, 128, static_cast<uint32_t>(np));
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int kb = 0; kb < kstages; ++kb) {
+                    const int nsub = min(W4_SUB, ksub - kb * W4_SUB);
                     if (!mbar_wait_bounded(cfull(cb), cph, abort_flag, p.err) ||
                         !mbar_wait_bounded(pfull(stage), phase, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t cvb = smem_u32(conv + cb * W4_CONV_BYTES);
-                    const uint64_t a0 = smem_desc_sw128(cvb);
-                    const uint64_t a1 = smem_desc_sw128(cvb + W4_CONV_BYTES / 2);
-                    const uint64_t bd = smem_desc_sw128(smem_u32(stages + stage * W4_STAGE_BYTES));
+                    for (int u = 0; u < nsub; ++u) {
+                        // A buffer cb, sub-step u: channels 0..127 in 32 columns, 128..255 in the next 32
+                        const uint32_t a0 =
+                            tmem_base + static_cast<uint32_t>(W4_A_COL0 + cb * W4_A_COLS + u * W4_A_SUB);
+                        const uint64_t bd = smem_desc_sw128(smem_u32(stages + stage * W4_STAGE_BYTES + u * W4_TOK_SUB));
 #pragma unroll
-                    for (int k = 0; k < W4_BK / 16; ++k) {
-                        const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-                        // D[channel][row]: first 128 channels into columns [0, np), the rest into [np, 2np)
-                        tc_mma_f16(d_tmem, a0 + 2u * k, bd + 2u * k, idesc, accum);
-                        tc_mma_f16(d_tmem + static_cast<uint32_t>(np), a1 + 2u * k, bd + 2u * k, idesc, accum);
+                        for (int k = 0; k < W4_BK / 16; ++k) {
+                            const uint32_t accum = (kb | u | k) != 0 ? 1u : 0u;
+                            // D[channel][row]: first 128 channels into columns [0, np), the rest into [np, 2np)
+                            tc_mma_f16_ta(d_tmem, a0 + 8u * k, bd + 2u * k, idesc, accum);
+                            tc_mma_f16_ta(d_tmem + static_cast<uint32_t>(np), a0 + W4_A_SUB / 2 + 8u * k,
+                                          bd + 2u * k, idesc, accum);
+                        }
                     }
-                    tc_commit(pempty(stage));  // the rows' stage may be refilled once these finish
-                    tc_commit(cempty(cb));     // and the unpacked weights overwritten
+                    // the unpacked weights may be overwritten once these finish; the
+                    // converters then also release this step's stage for the producer
+                    tc_commit(cempty(cb));
                     last_bar = cempty(cb);
                     last_parity = cph;
                     committed = true;
@@ -452,33 +553,55 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
         }
     } else if (warp >= W4_CONV_WARP0) {
         // ------------------------------ converters ------------------------------
-        // warp cw unpacks rows 16 i + 4 cw + lane / 8 (i = 0..15) of every
-        // stage: lane reads one 32-bit word (8 weights) and writes 16 bytes at
-        // the swizzled position (chunk ^ row % 8) of the row
-        const int cw = warp - W4_CONV_WARP0;
-        const int chunk = lane & 7;
+        // warp w owns TMEM lanes 32 (w % 4) .. +31: its thread t unpacks the
+        // 64 weights of channel 32 (w % 4) + t of half (w - 6) / 4 (channels
+        // 0..127 in columns [0, 32) of the A buffer, 128..255 in [32, 64))
+        const int quarter = warp & 3;
+        const int half = (warp - W4_CONV_WARP0) / 4;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         int stage = 0, cb = 0;
         uint32_t phase = 0, cph = 0;
+        long step = 0;
         for (;;) {
             if (!mbar_wait_bounded(pfull(stage), phase, abort_flag, p.err)) break;
-            if (stage_flag[stage] == 0) break;
+            const int flag = stage_flag[stage];
+            if (flag == 0) break;
+            const int nsub = flag & 15, gphase = flag >> 4;
             if (!mbar_wait_bounded(cempty(cb), cph ^ 1u, abort_flag, p.err)) break;
+            // the buffer is free: the MMA has finished step - W4_CONVS, whose
+            // stage (rows and packed weights, both read) goes back to the producer
+            if (step >= W4_CONVS && lane == 0)
+                mbar_arrive(pempty((stage + W4_STAGES - W4_CONVS) % W4_STAGES));
+            tc_fence_after();
+            // packed rows: stage 1 [gate sub 0 | gate sub 1 | up sub 0 | up sub 1] (4 KB
+            // each), stage 2 [sub 0 | sub 1] (8 KB each, channels 0..255)
             const uint8_t *pk = stages + stage * W4_STAGE_BYTES + W4_TOK_BYTES;
-            uint8_t *cv = conv + cb * W4_CONV_BYTES;
-#pragma unroll 4
-            for (int i = 0; i < W4_ROWS / (4 * W4_CONV_WARPS); ++i) {
-                const int row = i * (4 * W4_CONV_WARPS) + cw * 4 + (lane >> 3);
-                const uint32_t w = *reinterpret_cast<const uint32_t *>(pk + row * W4_PACK_ROW + chunk * 4);
-                *reinterpret_cast<uint4 *>(cv + row * (W4_BK * 2) + ((chunk ^ (row & 7)) << 4)) =
-                    w4_unpack8<DT>(w);
+            const int ch = quarter * 32 + lane;  // channel within the half
+            const uint8_t *prow = gphase == 0 ? pk + half * (W4_PACK_BYTES / 2) + ch * W4_PACK_ROW
+                                              : pk + (half * 128 + ch) * W4_PACK_ROW;
+            const int sub_stride = gphase == 0 ? W4_PACK_SUB / 2 : W4_PACK_SUB;
+            for (int u = 0; u < nsub; ++u) {
+                const uint4 lo = *reinterpret_cast<const uint4 *>(prow + u * sub_stride);
+                const uint4 hi = *reinterpret_cast<const uint4 *>(prow + u * sub_stride + 16);
+                const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                uint32_t cols[32];
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    const uint4 v = w4_unpack8<DT>(wv[w]);
+                    cols[4 * w + 0] = v.x;
+                    cols[4 * w + 1] = v.y;
+                    cols[4 * w + 2] = v.z;
+                    cols[4 * w + 3] = v.w;
+                }
+                tmem_st32(tmem_base + lane_base +
+                              static_cast<uint32_t>(W4_A_COL0 + cb * W4_A_COLS + u * W4_A_SUB + half * 32),
+                          cols);
             }
-            // the tensor cores read the tile through the async proxy
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tmem_st_wait();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(cfull(cb));
-                mbar_arrive(pempty(stage));
-            }
+            if (lane == 0) mbar_arrive(cfull(cb));
+            ++step;
             if (++stage == W4_STAGES) {
                 stage = 0;
                 phase ^= 1u;
@@ -595,19 +718,23 @@ cudaError_t launch_w4_typed(const CUtensorMap *maps, const W4Params &p, int grid
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
-    return launch_pdl(kern, dim3(grid), dim3(W4_THREADS), W4_SMEM_BYTES, stream, maps[0], maps[1],
-                      maps[2], maps[3], maps[4], p);
+    return launch_pdl(kern, dim3(grid), dim3(W4_THREADS), W4_SMEM_BYTES, stream, maps[0], maps[1], p);
 }
 
 }  // namespace
 
-cudaError_t launch_pack_int4(const uint8_t *plain, int64_t n_bytes, uint8_t *packed,
+int64_t pack_int4_bytes(int64_t E, int64_t N, int64_t K, int R) {
+    if (E <= 0 || N <= 0 || K <= 0 || K % W4_BK != 0 || R <= 0) return -1;
+    return E * ((N + R - 1) / R) * R * (K / 2);
+}
+
+cudaError_t launch_pack_int4(const uint8_t *plain, int64_t E, int64_t N, int64_t K, int R, uint8_t *packed,
                              cudaStream_t stream) {
-    if (n_bytes <= 0) return cudaSuccess;
-    const int64_t n_words = n_bytes / 4;
+    const int64_t n_words = pack_int4_bytes(E, N, K, R) / 4;
+    if (n_words <= 0) return cudaSuccess;
     const int64_t blocks = (n_words + 255) / 256;
     return launch_pdl(pack_int4_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
-                      reinterpret_cast<const uint32_t *>(plain), n_words, reinterpret_cast<uint32_t *>(packed));
+                      reinterpret_cast<const uint32_t *>(plain), E, N, K, R, reinterpret_cast<uint32_t *>(packed));
 }
 
 cudaError_t launch_grouped_mlp_w4(int dtype, const void *x, const int32_t *gather_idx, int64_t T,
@@ -622,7 +749,7 @@ cudaError_t launch_grouped_mlp_w4(int dtype, const void *x, const int32_t *gathe
     if (m_blocks > W4_MAX_BLOCKS) return cudaErrorInvalidValue;
     const int t16 = dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const int t8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    CUtensorMap maps[5];
+    CUtensorMap maps[2];
     const uint64_t uh = static_cast<uint64_t>(d_h), ue = static_cast<uint64_t>(d_e);
     {   // x [T, d_h], one row per box (four rows per gather)
         const uint64_t dims[2] = {uh, static_cast<uint64_t>(T)}, st[1] = {uh * 2};
@@ -634,24 +761,15 @@ cudaError_t launch_grouped_mlp_w4(int dtype, const void *x, const int32_t *gathe
         const uint32_t box[2] = {W4_BK, W4_TOK_ROWS};
         if (!encode_tma_map(&maps[1], t16, 2, h, dims, st, box, 1)) return cudaErrorInvalidValue;
     }
-    {   // packed W_gate / W_up [E, d_e, d_h / 2] bytes, 128 channels per box
-        const uint64_t dims[3] = {uh / 2, ue, static_cast<uint64_t>(E)}, st[2] = {uh / 2, ue * uh / 2};
-        const uint32_t box[3] = {W4_PACK_ROW, 128, 1};
-        if (!encode_tma_map(&maps[2], t8, 3, q_gate, dims, st, box, 0) ||
-            !encode_tma_map(&maps[3], t8, 3, q_up, dims, st, box, 0))
-            return cudaErrorInvalidValue;
-    }
-    {   // packed W_down [E, d_h, d_e / 2] bytes, 256 channels per box
-        const uint64_t dims[3] = {ue / 2, uh, static_cast<uint64_t>(E)}, st[2] = {ue / 2, uh * ue / 2};
-        const uint32_t box[3] = {W4_PACK_ROW, 256, 1};
-        if (!encode_tma_map(&maps[4], t8, 3, q_down, dims, st, box, 0)) return cudaErrorInvalidValue;
-    }
     W4Params p{};
     p.sizes = sizes;
     p.offsets = offsets;
     p.padded = padded;
     p.gidx = gidx;
     p.gather_idx = gather_idx;
+    p.q_gate = q_gate;
+    p.q_up = q_up;
+    p.q_down = q_down;
     p.row_weights = row_weights;
     p.s_gate = s_gate;
     p.s_up = s_up;

@@ -62,11 +62,14 @@ cudaError_t launch_grouped_mlp(int dtype, const void *a, const void *w_gate, con
                                cudaStream_t stream, const void *x = nullptr,
                                const int32_t *gather_idx = nullptr, int64_t T = 0);
 
-// grouped_gemm_w4.cu: int4 weights, two per byte as the pages pack them, into
-// the layout the int4 kernels read (n_bytes % 4 == 0).
-cudaError_t launch_pack_int4(const uint8_t *plain, int64_t n_bytes, uint8_t *packed,
+// grouped_gemm_w4.cu: int4 weights [E, N, K], two per byte as the pages pack
+// them, into the tiled layout the int4 kernels read (tiles of R output
+// channels; R = 128 for W_gate / W_up, 256 for W_down); bytes of that layout
+// (-1 for bad sizes; K % 64 == 0).
+int64_t pack_int4_bytes(int64_t E, int64_t N, int64_t K, int R);
+cudaError_t launch_pack_int4(const uint8_t *plain, int64_t E, int64_t N, int64_t K, int R, uint8_t *packed,
                              cudaStream_t stream);
-// Both expert stages with int4 weights (packed by launch_pack_int4) and
+// Both expert stages with int4 weights (tiled by launch_pack_int4) and
 // optional fp32 scales per output channel; stage-1 rows gathered from x
 // [T, d_h] by gather_idx (T <= 64, so every block has at most 64 rows);
 // `ready` (m_blocks + 1 int32) zero at kernel start.

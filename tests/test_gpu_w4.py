@@ -33,20 +33,31 @@ def _tables_to(dev, tab):
     return {n: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for n, v in tab.items()}
 
 
-def test_pack_int4_weights_layout():
-    """Inside each 4-byte word (8 elements) element 2m goes to nibble m and
-    element 2m+1 to nibble m+4, stored as value + 8 (the header's layout)."""
+@pytest.mark.parametrize("N,R", [(40, 128), (300, 256), (128, 128)])
+def test_pack_int4_weights_layout(N, R):
+    """The header's layout: [E][ceil(N/R)][K/64][R rows][32 bytes]; inside each
+    4-byte word element 2m in nibble m and 2m+1 in nibble m+4, as value + 8;
+    rows past N hold zeros (nibbles 8)."""
     dev = require_cuda()
-    rng = np.random.default_rng(1)
-    q = rng.integers(-8, 8, (3, 40, 64)).astype(np.int8)
-    plain = _pack_pages(q)
-    got = binding.moe_pack_int4_weights(torch.from_numpy(plain).to(dev)).cpu().numpy()
-    words = q.reshape(-1, 8).astype(np.int64) + 8
-    want = np.zeros(words.shape[0], np.uint32)
+    rng = np.random.default_rng(N + R)
+    E, K = 3, 128
+    q = rng.integers(-8, 8, (E, N, K)).astype(np.int8)
+    got = binding.moe_pack_int4_weights(torch.from_numpy(_pack_pages(q)).to(dev), R).cpu().numpy()
+    NT, S = -(-N // R), K // 64
+    qp = np.zeros((E, NT * R, K), np.int64)  # padded rows are value 0
+    qp[:, :N] = q
+    words = (qp.reshape(E, NT, R, S, 8, 8) + 8).transpose(0, 1, 3, 2, 4, 5)  # E, NT, S, R, word, element
+    want = np.zeros(words.shape[:-1], np.uint32)
     for e in range(8):
         slot = e // 2 if e % 2 == 0 else 4 + e // 2
-        want |= (words[:, e].astype(np.uint32) << np.uint32(4 * slot))
-    assert np.array_equal(got.reshape(-1).view(np.uint32), want)
+        want |= (words[..., e].astype(np.uint32) << np.uint32(4 * slot))
+    assert got.size == E * NT * R * K // 2
+    assert np.array_equal(got.view(np.uint32), want.reshape(-1))
+
+
+def _experts(dev, qg, qu, qd, sg, su, sd):
+    t = lambda a: None if a is None else torch.from_numpy(a).to(dev)
+    return binding.Int4Experts(t(_pack_pages(qg)), t(_pack_pages(qu)), t(_pack_pages(qd)), t(sg), t(su), t(sd))
 
 
 def _w4_case(dtype, T, k, E, d_h, d_e, skew, seed, scaled):
@@ -86,11 +97,9 @@ def test_w4_mlp_vs_oracle(oracle, dtype, scaled, T, k, E, d_h, d_e, skew):
     tab = oracle.build_dispatch(idx, None, E, 128)
     tabd = _tables_to(dev, tab)
     pg, pu, pd = _pack_pages(qg), _pack_pages(qu), _pack_pages(qd)
-    dq = [binding.moe_pack_int4_weights(torch.from_numpy(a).to(dev)) for a in (pg, pu, pd)]
-    to_dev = (lambda a: None if a is None else torch.from_numpy(a).to(dev))
+    ex = _experts(dev, qg, qu, qd, sg, su, sd)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    h, y = binding.moe_grouped_mlp_w4a16(x.to(dev), tabd["sorted_token_idx"], *dq, tabd,
-                                         s_gate=to_dev(sg), s_up=to_dev(su), s_down=to_dev(sd), err=err)
+    h, y = binding.moe_grouped_mlp_w4a16(x.to(dev), tabd["sorted_token_idx"], ex, tabd, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     a = oracle.gather_rows(bits(x), tab["sorted_token_idx"], dtype)
@@ -124,9 +133,8 @@ def test_w4_mlp_integer_inputs_bit_exact(oracle):
     sd = rng.choice([0.25, 1.0, 2.0], (E, d_h)).astype(np.float32)
     tabd = _tables_to(dev, tab)
     pg, pu, pd = _pack_pages(qg), _pack_pages(qu), _pack_pages(qd)
-    dq = [binding.moe_pack_int4_weights(torch.from_numpy(a).to(dev)) for a in (pg, pu, pd)]
-    h, y = binding.moe_grouped_mlp_w4a16(torch.from_numpy(x).to(dev), tabd["sorted_token_idx"], *dq, tabd,
-                                         s_up=torch.from_numpy(su).to(dev), s_down=torch.from_numpy(sd).to(dev))
+    ex = _experts(dev, qg, qu, qd, None, su, sd)
+    h, y = binding.moe_grouped_mlp_w4a16(torch.from_numpy(x).to(dev), tabd["sorted_token_idx"], ex, tabd)
     torch.cuda.synchronize()
     a = oracle.gather_rows(x.view(np.uint16), tab["sorted_token_idx"], "f16")
     h_ref = oracle.grouped_gate_up_silu_w4(a, pg, pu, tab, "f16", s_up=su)
@@ -151,13 +159,11 @@ def test_w4_forward_decode_size_vs_oracle(oracle):
     su = sg.copy()
     sd = (np.full((E, d_h), 1.0) / (8 * np.sqrt(d_e))).astype(np.float32)
     pg, pu, pd = _pack_pages(qg), _pack_pages(qu), _pack_pages(qd)
-    dq = [binding.moe_pack_int4_weights(torch.from_numpy(a).to(dev)) for a in (pg, pu, pd)]
+    ex = _experts(dev, qg, qu, qd, sg, su, sd)
     ws = torch.empty(binding.forward_workspace_bytes(T, d_h, d_e, E, k, d["x"].dtype), dtype=torch.uint8,
                      device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    out = binding.moe_forward_w4a16(d["x"], d["wg"], d["bias"], *dq, k, s_gate=torch.from_numpy(sg).to(dev),
-                                    s_up=torch.from_numpy(su).to(dev), s_down=torch.from_numpy(sd).to(dev),
-                                    ws=ws, err=err)
+    out = binding.moe_forward_w4a16(d["x"], d["wg"], d["bias"], ex, k, ws=ws, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     v = binding.forward_workspace_views(ws, T, d_h, d_e, E, k, d["x"].dtype)
@@ -182,12 +188,13 @@ def test_w4_argument_errors():
     T, k, E = 65, 2, 4
     tab = _tables_to(dev, oracle.build_dispatch(_routing(rng, T, k, E), None, E, 128))
     x = torch.zeros((T, 256), dtype=torch.float16, device=dev)
-    q = torch.zeros((E, 64, 128), dtype=torch.uint8, device=dev)
-    qd = torch.zeros((E, 256, 32), dtype=torch.uint8, device=dev)
+    z = np.zeros((E, 64, 256), np.int8)
+    ex = _experts(dev, z, z, np.zeros((E, 256, 64), np.int8), None, None, None)
     with pytest.raises(binding.MoEError):  # more than 64 tokens
-        binding.moe_grouped_mlp_w4a16(x, tab["sorted_token_idx"], q, q, qd, tab)
+        binding.moe_grouped_mlp_w4a16(x, tab["sorted_token_idx"], ex, tab)
     with pytest.raises(ValueError):  # wrong scale shape
-        binding.moe_grouped_mlp_w4a16(x[:8], tab["sorted_token_idx"][:16], q, q, qd, tab,
-                                      s_gate=torch.ones((E, 32), device=dev))
-    with pytest.raises(binding.MoEError):
-        binding.moe_pack_int4_weights(torch.zeros(6, dtype=torch.uint8, device=dev)[1:5])
+        binding.Int4Experts(*[torch.zeros((E, 64, 128), dtype=torch.uint8, device=dev)] * 2,
+                            torch.zeros((E, 256, 32), dtype=torch.uint8, device=dev),
+                            s_gate=torch.ones((E, 32), device=dev))
+    with pytest.raises(ValueError):  # K not a multiple of 64
+        binding.moe_pack_int4_weights(torch.zeros((E, 64, 40), dtype=torch.uint8, device=dev), 128)
