@@ -86,7 +86,8 @@ def forward_stages(T: int) -> list:
 
 # stages `--only` can time alone: the forward's, plus the two GEMM stages as
 # separate launches
-ONLY_STAGES = ["gate_topk", "dispatch", "gather", "expert_mlp", "reduce", "gate_up_silu", "down"]
+ONLY_STAGES = ["gate_topk", "dispatch", "gather", "expert_mlp", "reduce", "gate_up_silu", "down",
+               "w4_expert_mlp"]
 
 
 def describe(cfg) -> str:
@@ -618,11 +619,21 @@ def run_only(args):
         with torch.cuda.stream(stream):
             run_calls(calls)  # produce every intermediate once
         stream.synchronize()
-        fnc, fargs = step.calls(d["x"], stream.cuda_stream, names=[args.only])[0]
-        def fn():
-            st = fnc(*fargs)
-            if st != 0:
-                raise RuntimeError(binding.lib().moe_status_string(st).decode())
+        if args.only == "w4_expert_mlp":
+            # the int4 expert MLP on the same routing (weights quantised per channel)
+            ex = binding.Int4Experts(*[quantize_int4(d[n])[0] for n in ("w_gate", "w_up", "w_down")])
+            tables = {n: step.v[n] for n in ("group_sizes", "group_offsets", "group_padded_offsets",
+                                              "group_idx_for_bx")}
+            ready = torch.empty(tables["group_idx_for_bx"].numel() + 1, dtype=torch.int32, device=dev)
+            def fn():
+                binding.moe_grouped_mlp_w4a16(d["x"], step.v["sorted_token_idx"], ex, tables, h=step.v["h"],
+                                              y=step.v["y"], ready=ready)
+        else:
+            fnc, fargs = step.calls(d["x"], stream.cuda_stream, names=[args.only])[0]
+            def fn():
+                st = fnc(*fargs)
+                if st != 0:
+                    raise RuntimeError(binding.lib().moe_status_string(st).decode())
         sizes = step.v["group_sizes"].cpu().numpy()
         info = {"workload": describe(cfg), "active_experts": int((sizes > 0).sum()),
                 "max_rows": int(sizes.max())}
