@@ -204,9 +204,10 @@ MOE_API moe_status_t moe_grouped_down(const void *h, const void *w_down, const i
  * before the launch.
  * Gathering form: with sorted_token_idx non-NULL, stage 1 reads its rows from
  * the tokens x [T, d_h] by those indices (the gather of the CSDN "forward",
- * step 3, done by four-row TMA gathers in the kernel) and `a` is not read; this needs
- * 1 <= T <= 64 (every expert then holds at most 64 rows).  Otherwise x and T
- * are ignored and may be NULL / 0.
+ * step 3, done by four-row TMA gathers in the kernel) and `a` is not read;
+ * T >= 1 is the number of rows of x (every index must be below it).  It pays
+ * when blocks are small (at most 64 rows); a full 128-row tile is read faster
+ * from gathered rows `a`.  Otherwise x and T are ignored and may be NULL / 0.
  * The waits are bounded: after about 2 s *err_flag is set to
  * MOE_ERR_TIMEOUT and the kernel returns (this needs all CTAs of the grid,
  * one per SM, resident at once; a GPU shared with a partitioning runtime can

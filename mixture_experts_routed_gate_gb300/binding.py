@@ -297,8 +297,7 @@ def moe_grouped_down(h, w_down, tables, row_weights=None, y=None, err=None):
 def moe_grouped_mlp(a, w_gate, w_up, w_down, tables, row_weights=None, h=None, y=None,
                     ready=None, err=None, x=None, sorted_token_idx=None):
     """Stage 1 and stage 2 in one launch; returns (h, y).  With x and
-    sorted_token_idx (and a=None), stage 1 gathers its rows from the tokens x
-    (needs at most 64 tokens)."""
+    sorted_token_idx (and a=None), stage 1 gathers its rows from the tokens x."""
     gathering = sorted_token_idx is not None
     if gathering:
         _cuda(x, "x", ndim=2)

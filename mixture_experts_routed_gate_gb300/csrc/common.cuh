@@ -216,6 +216,17 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *desc, uint
         : "memory");
 }
 
+// tma_gather4 with an L2 eviction policy
+__device__ __forceinline__ void tma_gather4_hint(uint32_t dst, const void *desc, uint32_t bar, int c0,
+                                                 int r0, int r1, int r2, int r3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+        "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *desc, uint32_t bar, int c0,
                                             int c1, int c2) {
     asm volatile(

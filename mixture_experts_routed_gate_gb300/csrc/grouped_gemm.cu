@@ -88,9 +88,8 @@ struct GemmParams {
     const float *row_weights;
     int *ready;  // MODE_MLP: per M block, stage-1 epilogue warp-tiles stored
     int *tile_counter;  // MODE_MLP: next tile to take (null: fixed round-robin)
-    // MODE_MLP with every block at most SWAP_MAX_ROWS rows: stage 1 gathers its
-    // rows straight from the tokens x (through tmX) by these indices (null:
-    // stage 1 reads the gathered rows through tmA0)
+    // MODE_MLP: stage 1 gathers its rows straight from the tokens x (through
+    // tmX) by these indices (null: stage 1 reads the gathered rows through tmA0)
     const int32_t *gather_idx;
     PhaseParams ph[2];  // [0] stage 1 (gate/up), [1] stage 2 (down)
     int m_blocks;
@@ -384,87 +383,112 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
-        if (lane == 0) {
-            const uint64_t pol_first = l2_policy_evict_first();
-            const uint64_t pol_last = l2_policy_evict_last();
-            int stage = 0;
-            uint32_t phase = 0;
-            long issued = 0;
-            bool ok = true;
-            int rslot = 0;
-            uint32_t rphase = 0;
-            // dynamic: the first tile of CTA b is tile b; later ones come from
-            // the counter (offset by the grid), fetched one tile ahead so the
-            // atomic's round trip overlaps the current tile
-            int next_tile = dynamic ? static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1) : 0;
-            for (int it = 0; ok; ++it) {
-                int tile = blockIdx.x + it * static_cast<int>(gridDim.x);
-                if (dynamic) {
-                    // pass the tile id on (-1: none left)
+        // the whole warp: lane 0 takes tiles, arms the stage barriers and issues
+        // the weight (and tiled row) copies; when stage-1 rows are gathered from
+        // x, lane j holds the token ids of rows 4j .. 4j+3 for the tile and
+        // issues their gather every K step (128 rows for a full tile)
+        const uint64_t pol_first = l2_policy_evict_first();
+        const uint64_t pol_last = l2_policy_evict_last();
+        int stage = 0;
+        uint32_t phase = 0;
+        long issued = 0;
+        bool ok = true;
+        int rslot = 0;
+        uint32_t rphase = 0;
+        // dynamic: the first tile of CTA b is tile b; later ones come from the
+        // counter (offset by the grid), fetched one tile ahead so the atomic's
+        // round trip overlaps the current tile
+        int next_tile = 0;
+        if (dynamic && lane == 0) next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
+        for (int it = 0; ok; ++it) {
+            int tile = blockIdx.x + it * static_cast<int>(gridDim.x);
+            if (dynamic) {
+                // pass the tile id on (-1: none left)
+                int go = 1;
+                if (lane == 0) {
                     if (it > 0) {
                         tile = next_tile;
                         next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
                     }
                     if (tile >= total) tile = -1;
-                    if (!mbar_wait_bounded(tide_bar(rslot), rphase ^ 1u, abort_flag, p.err)) {
-                        ok = false;
-                        break;
+                    go = mbar_wait_bounded(tide_bar(rslot), rphase ^ 1u, abort_flag, p.err) ? 1 : 0;
+                    if (go) {
+                        tid_ring[rslot] = tile;
+                        mbar_arrive(tidf_bar(rslot));
                     }
-                    tid_ring[rslot] = tile;
-                    mbar_arrive(tidf_bar(rslot));
-                    if (++rslot == TRING) {
-                        rslot = 0;
-                        rphase ^= 1u;
-                    }
-                    if (tile < 0) break;
-                } else if (tile >= total) {
-                    break;
                 }
-                const TileInfo ti = decode_tile<MODE>(p, sc, tile, n0_tiles);
-                if (ti.rows == 0) continue;
-                // a stage-2 tile reads h rows of its block: wait until every
-                // stage-1 epilogue warp-tile of the block has stored them
-                if (MODE == MODE_MLP && ti.phase == 1 &&
-                    !counter_wait_bounded(p.ready + ti.bx, EPI_WARPS * p.ph[0].n_tiles, abort_flag, p.err)) {
+                go = __shfl_sync(0xffffffffu, go, 0);
+                tile = __shfl_sync(0xffffffffu, tile, 0);
+                if (++rslot == TRING) {
+                    rslot = 0;
+                    rphase ^= 1u;
+                }
+                if (!go) {
                     ok = false;
                     break;
                 }
-                const int kblocks = phase_params_of(p, ti.phase).k_blocks;
-                // stage-1 rows gathered from x: the swapped MMA reads np rows
-                const bool gather = MODE == MODE_MLP && ti.phase == 0 && p.gather_idx != nullptr;
-                int np_g = (ti.rows + 15) & ~15;
-                if (gather && np_g > SWAP_MAX_ROWS) {  // the host guarantees rows <= 64
-                    np_g = SWAP_MAX_ROWS;
-                    if (p.err) atomicExch(p.err, kErrDeviceFlag);
+                if (tile < 0) break;
+            } else if (tile >= total) {
+                break;
+            }
+            const TileInfo ti = decode_tile<MODE>(p, sc, tile, n0_tiles);
+            if (ti.rows == 0) continue;
+            // a stage-2 tile reads h rows of its block: wait until every
+            // stage-1 epilogue warp-tile of the block has stored them
+            if (MODE == MODE_MLP && ti.phase == 1) {
+                int go = 1;
+                if (lane == 0)
+                    go = counter_wait_bounded(p.ready + ti.bx, EPI_WARPS * p.ph[0].n_tiles, abort_flag, p.err) ? 1
+                                                                                                                 : 0;
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) {
+                    ok = false;
+                    break;
                 }
-                const uint32_t stage_tx = gather ? static_cast<uint32_t>(np_g * BK * 2 + B_BYTES) : STAGE_BYTES;
-                for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, stage_tx);
-                    const uint32_t a_dst = smem_u32(sA + stage * A_BYTES);
-                    const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
+            }
+            const int kblocks = phase_params_of(p, ti.phase).k_blocks;
+            // stage-1 rows gathered from x: a swapped tile reads np rows, a full one 128
+            const bool gather = MODE == MODE_MLP && ti.phase == 0 && p.gather_idx != nullptr;
+            const int nrow_g = ti.rows <= SWAP_MAX_ROWS ? ((ti.rows + 15) & ~15) : BM;
+            const uint32_t stage_tx = gather ? static_cast<uint32_t>(nrow_g * BK * 2 + B_BYTES) : STAGE_BYTES;
+            // this lane's four token ids (rows past the block repeat its first row)
+            int i0 = 0, i1 = 0, i2 = 0, i3 = 0;
+            const bool gatherer = gather && 4 * lane < nrow_g;
+            if (gatherer) {
+                const int32_t *ids = p.gather_idx + ti.m_start;
+                const int r = 4 * lane;
+                i0 = __ldg(ids + (r < ti.rows ? r : 0));
+                i1 = __ldg(ids + (r + 1 < ti.rows ? r + 1 : 0));
+                i2 = __ldg(ids + (r + 2 < ti.rows ? r + 2 : 0));
+                i3 = __ldg(ids + (r + 3 < ti.rows ? r + 3 : 0));
+            }
+            for (int kb = 0; kb < kblocks; ++kb) {
+                int go = 1;
+                if (lane == 0) go = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err) ? 1 : 0;
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = full_bar(stage);
+                const uint32_t a_dst = smem_u32(sA + stage * A_BYTES);
+                const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
+                if (lane == 0) mbar_arrive_expect_tx(fb, stage_tx);
+                __syncwarp();  // the stage's byte count is armed before any copy lands
+                if (gather) {
+                    // x rows are read by k experts and every N tile of a block: keep them
+                    if (gatherer)
+                        tma_gather4_hint(a_dst + static_cast<uint32_t>(4 * lane * BK * 2), &tmX, fb, kb * BK, i0,
+                                         i1, i2, i3, pol_last);
+                } else if (lane == 0) {
                     // a large expert's rows and weight stripes are reused by the
                     // tiles of its run: keep them; a small expert's weights are
                     // read by one block only: let them leave L2 first
-                    if (gather) {
-                        // four rows per copy; rows past the block repeat its first token
-                        const int32_t *ids = p.gather_idx + ti.m_start;
-                        for (int r = 0; r < np_g; r += 4) {
-                            const int i0 = __ldg(ids + (r < ti.rows ? r : 0));
-                            const int i1 = __ldg(ids + (r + 1 < ti.rows ? r + 1 : 0));
-                            const int i2 = __ldg(ids + (r + 2 < ti.rows ? r + 2 : 0));
-                            const int i3 = __ldg(ids + (r + 3 < ti.rows ? r + 3 : 0));
-                            tma_gather4(a_dst + static_cast<uint32_t>(r * BK * 2), &tmX, fb, kb * BK, i0, i1, i2, i3);
-                        }
-                    } else {
-                        const CUtensorMap *ta = HAS0 && ti.phase == 0 ? &tmA0 : &tmA1;
-                        if (ti.big) tma_load_2d_hint(a_dst, ta, fb, kb * BK, ti.m_start, pol_last);
-                        else tma_load_2d(a_dst, ta, fb, kb * BK, ti.m_start);
-                    }
+                    const CUtensorMap *ta = HAS0 && ti.phase == 0 ? &tmA0 : &tmA1;
+                    if (ti.big) tma_load_2d_hint(a_dst, ta, fb, kb * BK, ti.m_start, pol_last);
+                    else tma_load_2d(a_dst, ta, fb, kb * BK, ti.m_start);
+                }
+                if (lane == 0) {
                     const uint64_t polb = ti.big ? pol_last : pol_first;
                     if (HAS0 && ti.phase == 0) {
                         tma_load_3d_hint(b_dst, &tmB0, fb, kb * BK, ti.n0, ti.g, polb);
@@ -472,20 +496,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     } else {
                         tma_load_3d_hint(b_dst, &tmB2, fb, kb * BK, ti.n0, ti.g, polb);
                     }
-                    ++issued;
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                }
+                ++issued;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
-            if (!ok) {
-                // let every copy still in flight land before shared memory goes away
-                for (long j = 1; j <= STAGES && j <= issued; ++j) {
-                    const long i = issued - j;
-                    mbar_wait_drain(full_bar(static_cast<int>(i % STAGES)),
-                                    static_cast<uint32_t>((i / STAGES) & 1));
-                }
+        }
+        if (!ok && lane == 0) {
+            // let every copy still in flight land before shared memory goes away
+            for (long j = 1; j <= STAGES && j <= issued; ++j) {
+                const long i = issued - j;
+                mbar_wait_drain(full_bar(static_cast<int>(i % STAGES)), static_cast<uint32_t>((i / STAGES) & 1));
             }
         }
     } else if (warp == 1) {

@@ -95,9 +95,11 @@ def test_argument_errors_without_launch(lib):
                                fake, fake, None, None, None, 0, None, None) == MOE_ERR_INVALID_ARG
     assert lib.moe_grouped_mlp(fake, fake, fake, fake, fake, fake, fake, fake, 3, None, 8, 256, 100, 8, 1,
                                fake, fake, fake, None, None, 0, None, None) == MOE_ERR_INVALID_ARG
-    # gathering form: more than 64 tokens, or no tokens given
+    # gathering form: no token rows, more rows than int32 indices reach, or no tokens given
     assert lib.moe_grouped_mlp(None, fake, fake, fake, fake, fake, fake, fake, 3, None, 8, 256, 128, 8, 1,
-                               fake, fake, fake, fake, fake, 65, None, None) == MOE_ERR_INVALID_ARG
+                               fake, fake, fake, fake, fake, 0, None, None) == MOE_ERR_INVALID_ARG
+    assert lib.moe_grouped_mlp(None, fake, fake, fake, fake, fake, fake, fake, 3, None, 8, 256, 128, 8, 1,
+                               fake, fake, fake, fake, fake, 1 << 31, None, None) == MOE_ERR_INVALID_ARG
     assert lib.moe_grouped_mlp(None, fake, fake, fake, fake, fake, fake, fake, 3, None, 8, 256, 128, 8, 1,
                                fake, fake, fake, None, fake, 8, None, None) == MOE_ERR_INVALID_ARG
     # forward: workspace too small, misaligned workspace
