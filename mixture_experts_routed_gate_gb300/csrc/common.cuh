@@ -195,6 +195,14 @@ __device__ __forceinline__ void tma_prefetch_desc(const void *desc) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(desc)) : "memory");
 }
 
+// L2 prefetch of one box of a 3-D tensor map (no shared memory, no barrier)
+__device__ __forceinline__ void tma_prefetch_3d(const void *desc, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(desc)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *desc, uint32_t bar, int c0,
                                             int c1) {
     asm volatile(

@@ -201,8 +201,11 @@ __global__ void __launch_bounds__(SMALL_THREADS)
     const int rounds = (n_pairs + SMALL_THREADS - 1) / SMALL_THREADS;  // <= SMALL_MAX_ROUNDS
     const int wf0 = warp * rounds * 32;
     for (int i = threadIdx.x; i < SMALL_WARPS * E; i += SMALL_THREADS) wcount[i] = 0;
-    griddep_wait();
+    // release the next kernel before waiting: its CTAs become resident while
+    // the gate still runs and start their own independent set-up (every
+    // dependent waits for this grid before it reads the tables)
     griddep_launch_dependents();
+    griddep_wait();
     int ev[SMALL_MAX_ROUNDS];
 #pragma unroll
     for (int r = 0; r < SMALL_MAX_ROUNDS; ++r) {

@@ -61,6 +61,9 @@ constexpr int BAR_BYTES = 256;
 // Tile ids handed from the producer to the MMA and epilogue warps when tiles
 // are taken from a global counter (expert MLP mode).
 constexpr int TRING = 4;
+// K steps of the first tile prefetched into L2 before the dependency wait
+// (few-token launches; 16 x 32 KB per CTA, about 78 MB over the grid)
+constexpr int PREFETCH_STEPS = 16;
 // Blocks with at most this many valid rows run "swapped": the weight tile is
 // the M=128 operand and the block's rows the N operand (N = rows rounded up
 // to 16), so a mostly-padding block costs N/128 of a full MMA.
@@ -94,6 +97,9 @@ struct GemmParams {
     PhaseParams ph[2];  // [0] stage 1 (gate/up), [1] stage 2 (down)
     int m_blocks;
     int *err;
+    // MODE_MLP, every expert at most one block (a few tokens): the expert
+    // count, for the start-up prefetch below (0: none)
+    int prefetch_experts;
 };
 
 struct TileInfo {
@@ -323,6 +329,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     // everything above is independent of the previous kernel; the tables and
     // rows below are not
+    // While the routing kernels still run, pull the first K steps of this
+    // CTA's first tile into L2.  With one block per expert and every expert
+    // routed, stage-1 tile b (CTA b's first) is stripe b % n_tiles of expert
+    // b / n_tiles; when some expert is idle the guess is off by a few stripes,
+    // which other CTAs read soon after.  Weights do not come from the
+    // routing, so this may run before the dependency wait.
+    if (MODE == MODE_MLP && p.prefetch_experts > 0 && warp == 0 && lane == 0) {
+        const int nt = p.ph[0].n_tiles;
+        const int g = static_cast<int>(blockIdx.x) / nt;
+        if (g < p.prefetch_experts) {
+            const int n0 = (static_cast<int>(blockIdx.x) - g * nt) * 128;
+            for (int kb = 0; kb < PREFETCH_STEPS && kb < p.ph[0].k_blocks; ++kb) {
+                tma_prefetch_3d(&tmB0, kb * BK, n0, g);
+                tma_prefetch_3d(&tmB1, kb * BK, n0, g);
+            }
+        }
+    }
     griddep_wait();
     griddep_launch_dependents();
     // ----- schedule: classify the M blocks, list full and partial ones -----
@@ -943,6 +966,7 @@ cudaError_t launch_grouped_mlp(int dtype, const void *a, const void *w_gate, con
     p.ready = ready;
     p.tile_counter = ready + m_blocks;
     p.gather_idx = gather_idx;
+    p.prefetch_experts = gather_idx && T <= SWAP_MAX_ROWS ? static_cast<int>(E) : 0;
     p.ph[0] = phase_params(h, d_h, d_e, 128);
     p.ph[1] = phase_params(y, d_e, d_h, 256);
     return launch_mode<MODE_MLP>(dtype, maps, p, m_blocks * (p.ph[0].n_tiles + p.ph[1].n_tiles), stream);
