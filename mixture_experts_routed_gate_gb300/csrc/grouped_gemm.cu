@@ -56,7 +56,6 @@ constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int B_BYTES = MMA_N * BK * 2;      // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int BAR_BYTES = 256;
 // Tile ids handed from the producer to the MMA and epilogue warps when tiles
 // are taken from a global counter (expert MLP mode).
@@ -72,9 +71,21 @@ constexpr int MAX_SCHED = 1024;  // M blocks the in-kernel schedule can order
 // block list; per block: expert, first row, valid rows, class; per listed
 // full block: run start / length (int16); scan scratch
 constexpr int SCHED_BYTES = MAX_SCHED * 4 * 3 + 2 * MAX_SCHED * 2 + 2 * MAX_SCHED + 64;
-constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES + SCHED_BYTES;
 
-enum { MODE_GATE_UP = 0, MODE_DOWN = 1, MODE_MLP = 2 };
+// MODE_MLP: both stages in one launch.  MODE_MLP_FEW: the same when every
+// block holds at most 64 rows (rows gathered from at most 64 tokens): a ring
+// stage then needs 64 rows of A, so five stages fit and each SM keeps 160 KB
+// of weights in flight instead of 128 KB.
+enum { MODE_GATE_UP = 0, MODE_DOWN = 1, MODE_MLP = 2, MODE_MLP_FEW = 3 };
+
+template <int MODE>
+struct Layout {
+    static constexpr bool MLP = MODE == MODE_MLP || MODE == MODE_MLP_FEW;
+    static constexpr int NST = MODE == MODE_MLP_FEW ? 5 : STAGES;
+    static constexpr int A_SLOT = MODE == MODE_MLP_FEW ? SWAP_MAX_ROWS * BK * 2 : A_BYTES;
+    static constexpr int SMEM = 1024 /*alignment slack*/ + NST * (A_SLOT + B_BYTES) + BAR_BYTES + SCHED_BYTES;
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+};
 
 struct PhaseParams {
     void *out;     // h (stage 1) or y (stage 2), row-major [rows, N]
@@ -197,7 +208,7 @@ template <int MODE>
 __device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, const Schedule &sc, int tile,
                                                 int n0_tiles) {
     int phase = MODE == MODE_DOWN ? 1 : 0;
-    if (MODE == MODE_MLP && tile >= n0_tiles) {
+    if (Layout<MODE>::MLP && tile >= n0_tiles) {
         phase = 1;
         tile -= n0_tiles;
     }
@@ -262,6 +273,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const __grid_constant__ CUtensorMap tmB2,
                         const __grid_constant__ CUtensorMap tmX, const GemmParams p) {
     constexpr bool HAS0 = MODE != MODE_DOWN, HAS1 = MODE != MODE_GATE_UP;
+    constexpr bool IS_MLP = Layout<MODE>::MLP;
+    constexpr int NST = Layout<MODE>::NST, A_SLOT = Layout<MODE>::A_SLOT;
     constexpr uint32_t IDESC = idesc_f16(DT == kBF16, BM, MMA_N);
     using OutT = typename Elem<DT>::T;
 
@@ -269,12 +282,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
     uint8_t *sA = smem;
-    uint8_t *sB = smem + STAGES * A_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4 + 2 * TRING);
+    uint8_t *sB = smem + NST * A_SLOT;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + NST * B_BYTES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * NST + 4 + 2 * TRING);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *tid_ring = reinterpret_cast<int *>(tmem_slot + 2);
-    static_assert((2 * STAGES + 4 + 2 * TRING) * 8 + 8 + 4 * TRING <= BAR_BYTES, "barrier area");
+    static_assert((2 * NST + 4 + 2 * TRING) * 8 + 8 + 4 * TRING <= BAR_BYTES, "barrier area");
     int *sched = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(bars) + BAR_BYTES);
     int *blk_g = sched + MAX_SCHED;
     int *blk_m = blk_g + MAX_SCHED;
@@ -289,17 +302,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int lane = threadIdx.x & 31;
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
-    auto tidf_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + i); };
-    auto tide_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 4 + TRING + i); };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (NST + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * NST + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * NST + 2 + a); };
+    auto tidf_bar = [&](int i) { return bar0 + 8u * (2 * NST + 4 + i); };
+    auto tide_bar = [&](int i) { return bar0 + 8u * (2 * NST + 4 + TRING + i); };
     // tiles from the global counter (in order, each CTA taking the next one
     // when its producer is ready) instead of a fixed round-robin deal
-    const bool dynamic = MODE == MODE_MLP && p.tile_counter != nullptr;
+    const bool dynamic = IS_MLP && p.tile_counter != nullptr;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < NST; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
@@ -335,7 +348,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // b / n_tiles; when some expert is idle the guess is off by a few stripes,
     // which other CTAs read soon after.  Weights do not come from the
     // routing, so this may run before the dependency wait.
-    if (MODE == MODE_MLP && p.prefetch_experts > 0 && warp == 0 && lane == 0) {
+    if (IS_MLP && p.prefetch_experts > 0 && warp == 0 && lane == 0) {
         const int nt = p.ph[0].n_tiles;
         const int g = static_cast<int>(blockIdx.x) / nt;
         if (g < p.prefetch_experts) {
@@ -458,7 +471,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (ti.rows == 0) continue;
             // a stage-2 tile reads h rows of its block: wait until every
             // stage-1 epilogue warp-tile of the block has stored them
-            if (MODE == MODE_MLP && ti.phase == 1) {
+            if (IS_MLP && ti.phase == 1) {
                 int go = 1;
                 if (lane == 0)
                     go = counter_wait_bounded(p.ready + ti.bx, EPI_WARPS * p.ph[0].n_tiles, abort_flag, p.err) ? 1
@@ -471,9 +484,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             const int kblocks = phase_params_of(p, ti.phase).k_blocks;
             // stage-1 rows gathered from x: a swapped tile reads np rows, a full one 128
-            const bool gather = MODE == MODE_MLP && ti.phase == 0 && p.gather_idx != nullptr;
+            const bool gather = IS_MLP && ti.phase == 0 && p.gather_idx != nullptr;
             const int nrow_g = ti.rows <= SWAP_MAX_ROWS ? ((ti.rows + 15) & ~15) : BM;
-            const uint32_t stage_tx = gather ? static_cast<uint32_t>(nrow_g * BK * 2 + B_BYTES) : STAGE_BYTES;
+            const uint32_t stage_tx = static_cast<uint32_t>((gather ? nrow_g * BK * 2 : A_SLOT) + B_BYTES);
             // this lane's four token ids (rows past the block repeat its first row)
             int i0 = 0, i1 = 0, i2 = 0, i3 = 0;
             const bool gatherer = gather && 4 * lane < nrow_g;
@@ -494,7 +507,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 const uint32_t fb = full_bar(stage);
-                const uint32_t a_dst = smem_u32(sA + stage * A_BYTES);
+                const uint32_t a_dst = smem_u32(sA + stage * A_SLOT);
                 const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
                 if (lane == 0) mbar_arrive_expect_tx(fb, stage_tx);
                 __syncwarp();  // the stage's byte count is armed before any copy lands
@@ -521,7 +534,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 ++issued;
-                if (++stage == STAGES) {
+                if (++stage == NST) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -529,9 +542,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!ok && lane == 0) {
             // let every copy still in flight land before shared memory goes away
-            for (long j = 1; j <= STAGES && j <= issued; ++j) {
+            for (long j = 1; j <= NST && j <= issued; ++j) {
                 const long i = issued - j;
-                mbar_wait_drain(full_bar(static_cast<int>(i % STAGES)), static_cast<uint32_t>((i / STAGES) & 1));
+                mbar_wait_drain(full_bar(static_cast<int>(i % NST)), static_cast<uint32_t>((i / NST) & 1));
             }
         }
     } else if (warp == 1) {
@@ -582,7 +595,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t a_desc = smem_desc_sw128(smem_u32(sA + stage * A_BYTES));
+                    const uint64_t a_desc = smem_desc_sw128(smem_u32(sA + stage * A_SLOT));
                     const uint64_t b_desc = smem_desc_sw128(smem_u32(sB + stage * B_BYTES));
                     if (swap) {
                         // D[feature][row]: first 128 weight rows into columns [0, np),
@@ -607,7 +620,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     last_bar = empty_bar(stage);
                     last_parity = phase;
                     committed = true;
-                    if (++stage == STAGES) {
+                    if (++stage == NST) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -698,7 +711,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty_bar(acc));
-                if (MODE == MODE_MLP && gu) publish_h(p.ready + ti.bx, lane);
+                if (IS_MLP && gu) publish_h(p.ready + ti.bx, lane);
                 ++local;
                 continue;
             }
@@ -745,7 +758,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
-            if (MODE == MODE_MLP && gu) publish_h(p.ready + ti.bx, lane);
+            if (IS_MLP && gu) publish_h(p.ready + ti.bx, lane);
             ++local;
         }
     }
@@ -851,11 +864,11 @@ cudaError_t launch_typed(const CUtensorMap *maps, const GemmParams &p, int grid,
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<MODE>::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
-    return launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, maps[0], maps[1],
+    return launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), Layout<MODE>::SMEM, stream, maps[0], maps[1],
                       maps[2], maps[3], maps[4], maps[5], p);
 }
 
@@ -902,10 +915,11 @@ bool stage1_maps(CUtensorMap *maps, int dtype, const void *a, const void *w_gate
                        static_cast<uint64_t>(E), 128u);
 }
 
-// Stage-2 maps into maps[3..4]: h [n_rows, d_e], W_down [E, d_h, d_e].
+// Stage-2 maps into maps[3..4]: h [n_rows, d_e] (boxes of h_rows rows),
+// W_down [E, d_h, d_e].
 bool stage2_maps(CUtensorMap *maps, int dtype, const void *h, const void *w_down, int64_t n_rows,
-                 int64_t d_h, int64_t d_e, int64_t E) {
-    return make_map_2d(&maps[3], dtype, h, static_cast<uint64_t>(d_e), static_cast<uint64_t>(n_rows), BM) &&
+                 int64_t d_h, int64_t d_e, int64_t E, uint32_t h_rows = BM) {
+    return make_map_2d(&maps[3], dtype, h, static_cast<uint64_t>(d_e), static_cast<uint64_t>(n_rows), h_rows) &&
            make_map_3d(&maps[4], dtype, w_down, static_cast<uint64_t>(d_e), static_cast<uint64_t>(d_h),
                        static_cast<uint64_t>(E), 256u);
 }
@@ -949,12 +963,15 @@ cudaError_t launch_grouped_mlp(int dtype, const void *a, const void *w_gate, con
                                cudaStream_t stream, const void *x, const int32_t *gather_idx,
                                int64_t T) {
     if (n_rows <= 0 || m_blocks <= 0) return cudaSuccess;
+    // rows gathered from at most 64 tokens: no expert, so no block, holds
+    // more than 64 rows (MODE_MLP_FEW; its stage 2 copies 64 rows of h)
+    const bool few = gather_idx != nullptr && T <= SWAP_MAX_ROWS;
     CUtensorMap maps[6];
     // gathering: stage 1 reads token rows of x by index (then `a` is unused)
     const void *a_map = gather_idx ? x : a;
     const int64_t a_rows = gather_idx ? T : n_rows;
     if (!stage1_maps(maps, dtype, a_map, w_gate, w_up, a_rows, d_h, d_e, E) ||
-        !stage2_maps(maps, dtype, h, w_down, n_rows, d_h, d_e, E))
+        !stage2_maps(maps, dtype, h, w_down, n_rows, d_h, d_e, E, few ? SWAP_MAX_ROWS : BM))
         return cudaErrorInvalidValue;
     if (gather_idx) {
         if (!make_map_2d(&maps[5], dtype, x, static_cast<uint64_t>(d_h), static_cast<uint64_t>(T), 1u))
@@ -966,10 +983,12 @@ cudaError_t launch_grouped_mlp(int dtype, const void *a, const void *w_gate, con
     p.ready = ready;
     p.tile_counter = ready + m_blocks;
     p.gather_idx = gather_idx;
-    p.prefetch_experts = gather_idx && T <= SWAP_MAX_ROWS ? static_cast<int>(E) : 0;
+    p.prefetch_experts = few ? static_cast<int>(E) : 0;
     p.ph[0] = phase_params(h, d_h, d_e, 128);
     p.ph[1] = phase_params(y, d_e, d_h, 256);
-    return launch_mode<MODE_MLP>(dtype, maps, p, m_blocks * (p.ph[0].n_tiles + p.ph[1].n_tiles), stream);
+    const int64_t tiles = m_blocks * (p.ph[0].n_tiles + p.ph[1].n_tiles);
+    if (few) return launch_mode<MODE_MLP_FEW>(dtype, maps, p, tiles, stream);
+    return launch_mode<MODE_MLP>(dtype, maps, p, tiles, stream);
 }
 
 }  // namespace moe
