@@ -464,8 +464,9 @@ def measure_w4(cfg, d, dev, flush, steps: int = 200):
 
 def measure_e2e(args, cfg, d, dev, flush, world):
     """The public API end to end: binding.ForwardGraph with pinned host input
-    and output buffers; each step copies the tokens host -> device, runs the
-    forward and copies the output device -> host, all inside the events."""
+    and output buffers; each step moves the tokens host -> device (a copy
+    kernel reading the pinned buffer), runs the forward and lands the output
+    in the pinned host buffer (the combine's stores), all inside the events."""
     from mixture_experts_routed_gate_gb300 import binding
     T, d_h = cfg.T, cfg.d_hidden
     n_pool = 4

@@ -148,6 +148,18 @@ MOE_API moe_status_t moe_build_dispatch_noalloc(const int32_t *topk_idx, const f
                                         moe_stream_t stream);
 
 /*
+ * Stream-ordered copy by a kernel: dst[0, bytes) = src[0, bytes).  Either side
+ * may be host memory the device can reach (a pinned allocation's pointer under
+ * unified addressing), so a caller can move its tokens in, inside a captured
+ * CUDA graph, without a memcpy node (a small copy costs one round trip over
+ * the host link; launched with programmatic dependent launch like the
+ * forward's kernels).  Not part of the pages' method: plumbing for the
+ * forward's end-to-end path.  bytes % 16 == 0, both pointers 16-byte aligned,
+ * the ranges must not overlap (MOE_ERR_INVALID_ARG otherwise).
+ */
+MOE_API moe_status_t moe_copy(const void *src, void *dst, int64_t bytes, moe_stream_t stream);
+
+/*
  * Row gather (CSDN "forward", step 3: stacked_expert_tokens[r] = x_flat[token of r]).
  *   a_out[r, :] = x[sorted_token_idx[r], :] for r < n_rows.  x [T, d_h].
  * sorted_token_idx values must lie in [0, T).  d_h * elem_size % 16 == 0.
@@ -312,7 +324,10 @@ MOE_API moe_status_t moe_reduce_fused_scaled(const void *x, int64_t n_rows,
  * for T <= 64 the gather is done inside moe_grouped_mlp (its gathering form)
  * and the gathered-rows section of the workspace is left unwritten.
  * x [T, d_h]; w_g [E, d_h]; bias [E] fp32 or NULL; w_gate/w_up [E, d_e, d_h];
- * w_down [E, d_h, d_e]; out [T, d_h]; all in `dtype` (f16 or bf16).
+ * w_down [E, d_h, d_e]; out [T, d_h]; all in `dtype` (f16 or bf16).  `out`
+ * may also be host memory the device can store to (a pinned allocation's
+ * pointer under unified addressing): the combine writes it with plain
+ * stores, so the result reaches the host without a separate copy.
  * ws: moe_forward_workspace_bytes(...) bytes, 256-byte aligned; it holds every
  * intermediate (routing, tables, gathered rows, h, y) and is not read before
  * being written, so it needs no clearing.  err_flag: optional device int32.

@@ -57,6 +57,7 @@ def lib():
         "moe_gate_topk": (I, [P, P, P, I64, I64, I64, I64, I, P, P, P, SZ, P]),
         "moe_build_dispatch": (I, [P, P, I64, I64, I64, I64, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_build_dispatch_noalloc": (I, [P, P, I64, I64, I64, I64, P, P, P, P, P, P, P, P]),
+        "moe_copy": (I, [P, P, I64, P]),
         "moe_gather_rows": (I, [P, P, I64, I64, I64, I, P, P]),
         "moe_grouped_gate_up_silu": (I, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, P, P]),
         "moe_grouped_down": (I, [P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I, P, P, P]),
@@ -83,7 +84,7 @@ def exported_symbols():
             "moe_build_dispatch_workspace_bytes", "moe_forward_workspace_bytes",
             "moe_forward_workspace_offset", "moe_gate_topk", "moe_build_dispatch",
             "moe_build_dispatch_noalloc",
-            "moe_gather_rows", "moe_grouped_gate_up_silu", "moe_grouped_down",
+            "moe_copy", "moe_gather_rows", "moe_grouped_gate_up_silu", "moe_grouped_down",
             "moe_grouped_mlp", "moe_pack_int4_bytes", "moe_pack_int4_weights", "moe_grouped_mlp_w4a16",
             "moe_forward_w4a16", "moe_reduce_fused", "moe_reduce_fused_scaled", "moe_forward"]
 
@@ -110,6 +111,20 @@ def _cuda(t, name, dtype=None, ndim=None):
     if ndim is not None and t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
     return t
+
+
+def _cuda_or_pinned(t, name, dtype=None):
+    """A CUDA tensor, or a pinned host tensor: with unified addressing its
+    address is valid on the device, which stores to it directly."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda:
+        if not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if dtype is not None and t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        return t
+    return _cuda(t, name, dtype=dtype)
 
 
 def _dtype_code(t, name):
@@ -225,6 +240,22 @@ def moe_build_dispatch_noalloc(topk_idx, topk_w, E: int, block_m: int = BLOCK_M,
             _ptr(out["sorted_row_weight"]), _ptr(out["token_topk_to_pos"]), _stream(dev)),
             "moe_build_dispatch_noalloc")
     return out
+
+
+def moe_copy(src, dst):
+    """dst[:] = src by a kernel on dst's device stream; either may be a pinned
+    host tensor (same number of bytes, 16-byte multiple)."""
+    dev_t = dst if dst.is_cuda else src
+    if not dev_t.is_cuda:
+        raise ValueError("moe_copy: one side must be a CUDA tensor")
+    _cuda_or_pinned(src, "src")
+    _cuda_or_pinned(dst, "dst")
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("moe_copy: src and dst sizes differ")
+    with torch.cuda.device(dev_t.device):
+        _check(lib().moe_copy(_ptr(src), _ptr(dst), nbytes, _stream(dev_t.device)), "moe_copy")
+    return dst
 
 
 def moe_gather_rows(x, sorted_token_idx, out=None):
@@ -546,7 +577,9 @@ def forward_workspace_views(ws, T, d_h, d_e, E, k, dtype) -> dict:
 
 
 def moe_forward(x, w_g, bias, w_gate, w_up, w_down, k: int, ws=None, out=None, err=None):
-    """The whole routed forward; returns out [T, d_hidden]."""
+    """The whole routed forward; returns out [T, d_hidden].  ``out`` may be a
+    pinned host tensor: the combine kernel then stores the result straight
+    into host memory (no separate device-to-host copy)."""
     _cuda(x, "x", ndim=2)
     for n, t in (("w_g", w_g), ("w_gate", w_gate), ("w_up", w_up), ("w_down", w_down)):
         _cuda(t, n, dtype=x.dtype)
@@ -560,7 +593,9 @@ def moe_forward(x, w_g, bias, w_gate, w_up, w_down, k: int, ws=None, out=None, e
     _cuda(ws, "ws", dtype=torch.uint8)
     if out is None:
         out = torch.empty((T, d_h), dtype=x.dtype, device=x.device)
-    _cuda(out, "out", dtype=x.dtype)
+    _cuda_or_pinned(out, "out", dtype=x.dtype)
+    if tuple(out.shape) != (T, d_h):
+        raise ValueError(f"out must be [{T}, {d_h}], got {tuple(out.shape)}")
     if err is not None:
         _cuda(err, "err", dtype=torch.int32)
     with torch.cuda.device(x.device):
@@ -573,8 +608,9 @@ def moe_forward(x, w_g, bias, w_gate, w_up, w_down, k: int, ws=None, out=None, e
 
 class ForwardGraph:
     """``moe_forward`` captured once into a CUDA graph for a fixed token count,
-    with static device buffers (and, with ``host_io``, pinned host buffers whose
-    host-to-device and device-to-host copies are part of the graph).
+    with static device buffers (and, with ``host_io``, pinned host buffers: a
+    copy kernel in the graph reads the tokens from ``x_host``, and the combine
+    kernel stores the output straight into ``out_host``).
 
     Fill ``x`` (or ``x_host``), call :meth:`replay`, and read ``out`` (or
     ``out_host`` after synchronising).  One replay is one launch from the host,
@@ -602,10 +638,9 @@ class ForwardGraph:
     def _body(self):
         w_g, bias, w_gate, w_up, w_down, k = self.params
         if self.x_host is not None:
-            self.x.copy_(self.x_host, non_blocking=True)
-        moe_forward(self.x, w_g, bias, w_gate, w_up, w_down, k, ws=self.ws, out=self.out, err=self.err)
-        if self.out_host is not None:
-            self.out_host.copy_(self.out, non_blocking=True)
+            moe_copy(self.x_host, self.x)  # a kernel, not a memcpy node
+        out = self.out_host if self.out_host is not None else self.out
+        moe_forward(self.x, w_g, bias, w_gate, w_up, w_down, k, ws=self.ws, out=out, err=self.err)
 
     def replay(self):
         self.graph.replay()

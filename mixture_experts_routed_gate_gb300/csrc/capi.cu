@@ -184,6 +184,16 @@ moe_status_t moe_gather_rows(const void *x, const int32_t *sorted_token_idx, int
                                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_copy(const void *src, void *dst, int64_t bytes, moe_stream_t stream) {
+    if (bytes < 0 || bytes % 16 != 0) return MOE_ERR_INVALID_ARG;
+    if (bytes == 0) return MOE_OK;
+    if (!src || !dst || !aligned16(src) || !aligned16(dst)) return MOE_ERR_INVALID_ARG;
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+    if (s0 < d0 + static_cast<uintptr_t>(bytes) && d0 < s0 + static_cast<uintptr_t>(bytes))
+        return MOE_ERR_INVALID_ARG;  // overlapping
+    return cuda_status(moe::launch_copy(src, dst, bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 static moe_status_t check_gemm_tables(const int32_t *s, const int32_t *o, const int32_t *p,
                                       const int32_t *g, int64_t m_blocks, int64_t n_rows, int64_t E) {
     if (!s || !o || !p || !g) return MOE_ERR_INVALID_ARG;

@@ -36,6 +36,7 @@ cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_
                             int32_t *ready, cudaStream_t stream);
 
 // rows.cu
+cudaError_t launch_copy(const void *src, void *dst, int64_t bytes, cudaStream_t stream);
 cudaError_t launch_gather_rows(const void *x, const int32_t *sorted_token_idx, int64_t n_rows,
                                int64_t d_h, int elem_bytes, void *a_out, cudaStream_t stream);
 cudaError_t launch_reduce_fused(const void *x, int64_t n_rows, const int32_t *pos,

@@ -45,6 +45,45 @@ __global__ void __launch_bounds__(GA_WARPS * 32)
 }
 
 // ---------------------------------------------------------------------------
+// copy: dst[i] = src[i] over 16-byte vectors, either side host memory the
+// device can reach (pinned, mapped).  Every thread issues its loads before
+// its stores, so a small copy costs one round trip over the host link.
+// ---------------------------------------------------------------------------
+constexpr int CP_THREADS = 256;
+constexpr int CP_VEC = 4;  // vectors per thread per pass
+
+// a plain (coherent) 16-byte load: the source may be host memory that the
+// host wrote just before the launch, so not the read-only data path
+__device__ __forceinline__ uint4 ld_coherent(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__global__ void __launch_bounds__(CP_THREADS)
+    copy_kernel(const uint4 *src, uint4 *__restrict__ dst, int64_t nvec) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * CP_THREADS;
+    for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * CP_THREADS + threadIdx.x; i0 < nvec;
+         i0 += stride * CP_VEC) {
+        uint4 v[CP_VEC];
+#pragma unroll
+        for (int j = 0; j < CP_VEC; ++j) {
+            const int64_t i = i0 + j * stride;
+            if (i < nvec) v[j] = ld_coherent(src + i);
+        }
+#pragma unroll
+        for (int j = 0; j < CP_VEC; ++j) {
+            const int64_t i = i0 + j * stride;
+            if (i < nvec) dst[i] = v[j];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // moe_reduce_fused (TileOPs-Metax PR #55, section 1): one thread per 8
 // consecutive hidden elements of one token.  The K slot rows are gathered
 // with all loads of a group of 8 slots issued before any is consumed (the
@@ -455,6 +494,17 @@ cudaError_t launch_gather_rows(const void *x, const int32_t *sorted_token_idx, i
     return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(GA_WARPS * 32), 0,
                       stream, static_cast<const uint4 *>(x), sorted_token_idx, n_rows, nvec,
                       static_cast<uint4 *>(a_out));
+}
+
+cudaError_t launch_copy(const void *src, void *dst, int64_t bytes, cudaStream_t stream) {
+    if (bytes <= 0) return cudaSuccess;
+    const int64_t nvec = bytes / 16;
+    // enough threads for one vector each up to 152 x 8 CTAs, then 4 per pass
+    const int64_t want = (nvec + CP_THREADS - 1) / CP_THREADS;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+    const int blocks = static_cast<int>(want < cap ? want : cap);
+    return launch_pdl(copy_kernel, dim3(static_cast<unsigned>(blocks)), dim3(CP_THREADS), 0, stream,
+                      static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), nvec);
 }
 
 cudaError_t launch_reduce_fused(const void *x, int64_t n_rows, const int32_t *pos,

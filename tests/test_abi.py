@@ -110,6 +110,11 @@ def test_argument_errors_without_launch(lib):
     # empty problems are valid no-ops
     assert lib.moe_reduce_fused(fake, 0, fake, None, 0, 2, 256, 1, 1, fake, None, None) == MOE_OK
     assert lib.moe_gather_rows(fake, fake, 0, 4, 256, 1, fake, None) == MOE_OK
+    assert lib.moe_copy(fake, P(0x200000), 0, None) == MOE_OK
+    # copy: size not a 16-byte multiple, misaligned, overlapping ranges
+    assert lib.moe_copy(fake, P(0x200000), 24, None) == MOE_ERR_INVALID_ARG
+    assert lib.moe_copy(P(0x100008), P(0x200000), 32, None) == MOE_ERR_INVALID_ARG
+    assert lib.moe_copy(P(0x100000), P(0x100010), 64, None) == MOE_ERR_INVALID_ARG
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -102,6 +102,43 @@ def test_forward_graph_replay_matches_eager(host_io):
         assert int(fg.err.item()) == 0
 
 
+def test_forward_output_into_pinned_host_memory():
+    """moe_forward with `out` a pinned host tensor: the combine stores the
+    result straight into host memory, the same bits as a device `out`."""
+    dev = require_cuda()
+    cfg = workloads.MOE_CONFIGS["decode"]
+    d = workloads.make_moe_inputs(cfg, device=dev)
+    want = binding.moe_forward(d["x"], d["wg"], d["bias"], d["w_gate"], d["w_up"], d["w_down"], cfg.top_k)
+    host = torch.full((cfg.T, cfg.d_hidden), float("nan"), dtype=want.dtype).pin_memory()
+    got = binding.moe_forward(d["x"], d["wg"], d["bias"], d["w_gate"], d["w_up"], d["w_down"], cfg.top_k,
+                              out=host)
+    torch.cuda.synchronize()
+    assert got is host
+    assert torch.equal(host.view(torch.int16), want.cpu().view(torch.int16))
+    with pytest.raises(ValueError):
+        binding.moe_forward(d["x"], d["wg"], d["bias"], d["w_gate"], d["w_up"], d["w_down"], cfg.top_k,
+                            out=torch.empty((cfg.T, cfg.d_hidden), dtype=want.dtype))  # pageable
+
+
+@pytest.mark.parametrize("nbytes", [16, 4096, 262144, (1 << 22) + 48])
+def test_copy_kernel_host_and_device(nbytes):
+    """moe_copy moves bytes pinned host -> device, device -> pinned host and
+    device -> device, bit for bit, including a size that is not a whole
+    number of passes of the grid."""
+    dev = require_cuda()
+    n = nbytes // 2
+    src_h = torch.randint(-32768, 32767, (n,), dtype=torch.int16).pin_memory()
+    d1 = torch.empty(n, dtype=torch.int16, device=dev)
+    binding.moe_copy(src_h, d1)
+    d2 = torch.empty(n, dtype=torch.int16, device=dev)
+    binding.moe_copy(d1, d2)
+    back = torch.empty(n, dtype=torch.int16).pin_memory()
+    binding.moe_copy(d2, back)
+    torch.cuda.synchronize()
+    assert torch.equal(back, src_h)
+    assert torch.equal(d1.cpu(), src_h)
+
+
 def _compact(w, experts):
     """The listed experts' slices of a stacked weight, on the host."""
     idx = torch.as_tensor(experts, dtype=torch.long, device=w.device)
