@@ -19,7 +19,7 @@
 //   * E <= 64: one CTA holds 1 token (small batches) or 4 tokens x all
 //     experts and also selects the top-k from its logits in shared memory
 //     (one launch for the gate);
-//   * many tokens: CTA = 16 tokens x 32 experts (16 warps of 4 x 8 pairs), then
+//   * many tokens: CTA = 16 tokens x 16 experts (8 warps of 4 x 8 pairs), then
 //     topk_softmax_kernel;
 //   * few tokens: CTA = one warp of 4 tokens x 8 experts (more CTAs in
 //     flight), then topk_softmax_kernel.
@@ -32,10 +32,42 @@ namespace {
 constexpr int SLICE = 256;                // elements per lane round: 32 lanes x 8
 constexpr int ROW_BYTES = SLICE * 2;      // 512 B of one row per slice
 // Ring depth: the small-batch shapes keep up to 8 slices (about 200 KB) in
-// flight, since their time is the latency of the first slices; the 16-warp
-// many-token shape keeps 4 (two CTAs per SM).
+// flight, since their time is the latency of the first slices; the 8-warp
+// many-token shape keeps 4 (two CTAs per SM, each 64 KB of ring).  Measured
+// at 4096 tokens x 256 experts x 7168: 3, 4 or 6 stages and one to three CTAs
+// per SM within 10%, 16 x 16 fastest among 8x16 / 16x16 / 16x32 / 32x16 tiles.
 __host__ __device__ constexpr int gate_stages(int rows, bool many_tokens) {
     return many_tokens ? 4 : ((200 * 1024) / (rows * ROW_BYTES) > 8 ? 8 : (200 * 1024) / (rows * ROW_BYTES));
+}
+
+// c + a*b for one 16-bit element of each packed pair (lo or hi half), the
+// fp32 accumulator updated by the mixed-precision FMA (16-bit sources, fp32
+// addend and result, one rounding).  A product of two fp16 or two bf16 values
+// is exact in fp32, so this is bit for bit fmaf(float(a), float(b), c) with
+// no separate conversion instructions.
+template <int DT, bool HI>
+__device__ __forceinline__ float fma_mixed(uint32_t a, uint32_t b, float c) {
+    float d;
+    if constexpr (DT == kBF16) {
+        if constexpr (HI)
+            asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+                "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}"
+                : "=f"(d) : "r"(a), "r"(b), "f"(c));
+        else
+            asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+                "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}"
+                : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    } else {
+        if constexpr (HI)
+            asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+                "fma.rn.f32.f16 %0, ah, bh, %3;\n\t}"
+                : "=f"(d) : "r"(a), "r"(b), "f"(c));
+        else
+            asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+                "fma.rn.f32.f16 %0, al, bl, %3;\n\t}"
+                : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    }
+    return d;
 }
 
 // Top-k by (logit desc, id asc) and the softmax weights of TOK tokens whose
@@ -161,7 +193,7 @@ __global__ void __launch_bounds__(WT *WE * 32)
                 float *__restrict__ topk_w) {
     constexpr int TOK = WT * TPW, EXP = WE * 8, ROWS = TOK + EXP;
     constexpr int STAGE_BYTES = ROWS * ROW_BYTES;
-    constexpr int GATE_STAGES = gate_stages(ROWS, WT * WE > 8);
+    constexpr int GATE_STAGES = gate_stages(ROWS, WT * WE > 1 && !FUSE_TOPK);
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * TOK, e0 = blockIdx.y * EXP;
@@ -218,27 +250,23 @@ __global__ void __launch_bounds__(WT *WE * 32)
             wv[j] = *reinterpret_cast<const uint4 *>(stage + (TOK + we + j) * ROW_BYTES + lane * 16);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            float2 xf[TPW], wf[8];
+            uint32_t xw[TPW], ww[8];
 #pragma unroll
-            for (int i = 0; i < TPW; ++i) {
-                const uint32_t word = q == 0 ? xv[i].x : q == 1 ? xv[i].y : q == 2 ? xv[i].z : xv[i].w;
-                xf[i] = unpack2<DT>(word);
-            }
+            for (int i = 0; i < TPW; ++i)
+                xw[i] = q == 0 ? xv[i].x : q == 1 ? xv[i].y : q == 2 ? xv[i].z : xv[i].w;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t word = q == 0 ? wv[j].x : q == 1 ? wv[j].y : q == 2 ? wv[j].z : wv[j].w;
-                wf[j] = unpack2<DT>(word);
-            }
+            for (int j = 0; j < 8; ++j)
+                ww[j] = q == 0 ? wv[j].x : q == 1 ? wv[j].y : q == 2 ? wv[j].z : wv[j].w;
             // element 2q of every pair, then element 2q+1: the two updates of
             // one accumulator are TPW*8 independent FMAs apart
 #pragma unroll
             for (int i = 0; i < TPW; ++i)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xf[i].x, wf[j].x, acc[i][j]);
+                for (int j = 0; j < 8; ++j) acc[i][j] = fma_mixed<DT, false>(xw[i], ww[j], acc[i][j]);
 #pragma unroll
             for (int i = 0; i < TPW; ++i)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xf[i].y, wf[j].y, acc[i][j]);
+                for (int j = 0; j < 8; ++j) acc[i][j] = fma_mixed<DT, true>(xw[i], ww[j], acc[i][j]);
         }
         __syncthreads();  // every warp is done with this stage: refill it
         if (threadIdx.x == 0 && s + GATE_STAGES < n_slices && !*abort_flag) load_slice(s + GATE_STAGES);
@@ -325,7 +353,7 @@ cudaError_t launch_gate_shape(const void *x, const void *wg, const float *bias, 
                               int64_t d_h, int64_t E, int64_t k, float *logits, int32_t *idx,
                               float *w, cudaStream_t stream) {
     constexpr int TOK = WT * TPW, EXP = WE * 8;
-    constexpr int GATE_STAGES = gate_stages(TOK + EXP, WT * WE > 8);
+    constexpr int GATE_STAGES = gate_stages(TOK + EXP, WT * WE > 1 && !FUSE);
     const size_t smem = static_cast<size_t>(GATE_STAGES) * (TOK + EXP) * ROW_BYTES + 8 * GATE_STAGES + 16;
     CUtensorMap tm_x, tm_w;
     if (!encode_tma_2d_plain(&tm_x, x, static_cast<uint64_t>(d_h), static_cast<uint64_t>(T), SLICE, TOK) ||
@@ -376,8 +404,8 @@ cudaError_t launch_gate_typed(const void *x, const void *wg, const float *bias, 
         return launch_gate_shape<DT, 4, 1, 8, true>(x, wg, bias, T, d_h, E, k, logits, idx, w, stream);
     }
     cudaError_t e;
-    if (T >= 512)  // 16 tokens x 32 experts per CTA: 16 warps of 4 x 8 pairs
-        e = launch_gate_shape<DT, 4, 4, 4, false>(x, wg, bias, T, d_h, E, k, logits, idx, w, stream);
+    if (T >= 512)  // 16 tokens x 16 experts per CTA: 8 warps of 4 x 8 pairs, two CTAs per SM
+        e = launch_gate_shape<DT, 4, 4, 2, false>(x, wg, bias, T, d_h, E, k, logits, idx, w, stream);
     else           // one warp of 4 x 8 pairs per CTA
         e = launch_gate_shape<DT, 4, 1, 1, false>(x, wg, bias, T, d_h, E, k, logits, idx, w, stream);
     if (e != cudaSuccess) return e;
