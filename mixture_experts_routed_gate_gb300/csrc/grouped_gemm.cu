@@ -60,6 +60,9 @@ constexpr int BAR_BYTES = 256;
 // Tile ids handed from the producer to the MMA and epilogue warps when tiles
 // are taken from a global counter (expert MLP mode).
 constexpr int TRING = 4;
+// The producer takes its next tile from the shared counter this many K steps
+// before the end of the current tile (see the producer)
+constexpr int NEXT_FETCH = 2;
 // K steps of the first tile prefetched into L2 before the dependency wait
 // (few-token launches; 16 x 32 KB per CTA, about 78 MB over the grid)
 constexpr int PREFETCH_STEPS = 16;
@@ -432,10 +435,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int rslot = 0;
         uint32_t rphase = 0;
         // dynamic: the first tile of CTA b is tile b; later ones come from the
-        // counter (offset by the grid), fetched one tile ahead so the atomic's
-        // round trip overlaps the current tile
+        // counter (offset by the grid).  The next tile is taken NEXT_FETCH K
+        // steps before the current tile's last copy is issued: late enough that
+        // at the end of the launch the last tiles go to CTAs that are about to
+        // be free (taking it at the start of the current tile bound them a whole
+        // tile early), early enough that the atomic's round trip is hidden (its
+        // result is first used at the next tile).
         int next_tile = 0;
-        if (dynamic && lane == 0) next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
+        bool have_next = false;
         for (int it = 0; ok; ++it) {
             int tile = blockIdx.x + it * static_cast<int>(gridDim.x);
             if (dynamic) {
@@ -443,8 +450,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 int go = 1;
                 if (lane == 0) {
                     if (it > 0) {
+                        if (!have_next) next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
                         tile = next_tile;
-                        next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
+                        have_next = false;
                     }
                     if (tile >= total) tile = -1;
                     go = mbar_wait_bounded(tide_bar(rslot), rphase ^ 1u, abort_flag, p.err) ? 1 : 0;
@@ -498,7 +506,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 i2 = __ldg(ids + (r + 2 < ti.rows ? r + 2 : 0));
                 i3 = __ldg(ids + (r + 3 < ti.rows ? r + 3 : 0));
             }
+            const int fetch_kb = kblocks > NEXT_FETCH ? kblocks - NEXT_FETCH : 0;
             for (int kb = 0; kb < kblocks; ++kb) {
+                if (dynamic && lane == 0 && kb == fetch_kb) {
+                    next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
+                    have_next = true;
+                }
                 int go = 1;
                 if (lane == 0) go = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err) ? 1 : 0;
                 go = __shfl_sync(0xffffffffu, go, 0);

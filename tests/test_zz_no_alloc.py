@@ -25,10 +25,12 @@ def _routing(seed, T, k, E, dev):
 def test_noalloc_dispatch_matches_workspace_dispatch_twice():
     """Two calls in a row, through the C-ABI, each compared table by table
     (bit for bit, the tolerance the dispatch tests use) with the workspace
-    entry point; the second call has a different size and routing, so stale
-    counters left by the first call would show."""
+    entry point.  Both calls take the multi-kernel path that uses the fixed
+    scratch (32768 pairs; then 300 experts, more than the one-CTA path
+    handles) with a different size and routing, so stale counters left by
+    the first call would show."""
     dev = require_cuda()
-    for seed, (T, k, E) in enumerate([(4096, 8, 256), (300, 6, 64)]):
+    for seed, (T, k, E) in enumerate([(4096, 8, 256), (300, 6, 300)]):
         idx, w = _routing(seed, T, k, E, dev)
         want = binding.moe_build_dispatch(idx, w, E)
         got = binding.moe_build_dispatch_noalloc(idx, w, E)
