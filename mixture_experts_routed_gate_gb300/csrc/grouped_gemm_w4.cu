@@ -69,6 +69,7 @@ constexpr int W4_CONV_WARP0 = 6;                 // converter warps 6..13: two p
 constexpr int W4_CONV_WARPS = 8;
 constexpr int W4_EPI_WARPS = 4;
 constexpr int W4_TRING = 4;
+constexpr int W4_NEXT_FETCH = 1;                 // stages before a tile's end that the next one is taken
 constexpr int W4_ACC_COLS = 128;                 // 2 x up to 64 columns per accumulator
 constexpr int W4_TMEM_COLS = 512;
 static_assert(W4_A_COL0 + W4_CONVS * W4_A_COLS <= W4_TMEM_COLS && 2 * W4_ACC_COLS <= W4_A_COL0, "tmem");
@@ -356,14 +357,19 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
         bool ok = true;
         int rslot = 0;
         uint32_t rphase = 0;
+        // the next tile is taken W4_NEXT_FETCH stages before the current tile's
+        // last copy (at the end of the launch the last tiles then go to CTAs
+        // that are about to be free; the atomic's result is first used at the
+        // next tile, so its round trip stays hidden)
         int next_tile = 0;
-        if (lane == 0) next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
+        bool have_next = false;
         for (int it = 0; ok; ++it) {
             int tile = 0;
             int go = 1;
             if (lane == 0) {
+                if (it > 0 && !have_next) next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
                 tile = it == 0 ? static_cast<int>(blockIdx.x) : next_tile;
-                if (it > 0) next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
+                have_next = false;
                 if (tile >= total) tile = -1;
                 go = mbar_wait_bounded(tide(rslot), rphase ^ 1u, abort_flag, p.err) ? 1 : 0;
                 if (go) {
@@ -411,7 +417,12 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
             }
             const int ksub = ti.phase == 0 ? p.kb0 : p.kb1;
             const int kstages = (ksub + W4_SUB - 1) / W4_SUB;
+            const int fetch_kb = kstages > W4_NEXT_FETCH ? kstages - W4_NEXT_FETCH : 0;
             for (int kb = 0; kb < kstages; ++kb) {
+                if (lane == 0 && kb == fetch_kb) {
+                    next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
+                    have_next = true;
+                }
                 const int nsub = min(W4_SUB, ksub - kb * W4_SUB);
                 const uint32_t tx = static_cast<uint32_t>(nsub * ((ti.phase == 0 ? np * W4_BK * 2 : W4_TOK_SUB) +
                                                                   W4_PACK_SUB));
