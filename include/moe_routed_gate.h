@@ -160,6 +160,25 @@ MOE_API moe_status_t moe_build_dispatch_noalloc(const int32_t *topk_idx, const f
 MOE_API moe_status_t moe_copy(const void *src, void *dst, int64_t bytes, moe_stream_t stream);
 
 /*
+ * Stream-ordered bounded wait on a flag (a doorbell): work queued after this
+ * call on `stream` starts once *flag >= expected, so a pre-launched forward
+ * (a replayed CUDA graph, say) can wait for an upstream producer, such as
+ * the host filling pinned token buffers or another engine's kernel, without
+ * a host synchronisation.  flag: int32 in device memory or in host memory
+ * the device can read (a pinned allocation's pointer under unified
+ * addressing); it is read with system-scope loads and never written.  Not
+ * part of the pages' method: plumbing, like moe_copy.
+ * If the flag has not reached `expected` after timeout_ns (1 ns .. 10 s) the
+ * wait gives up: *err_flag is set to MOE_ERR_TIMEOUT, the kernel returns and
+ * the stream goes on (the CUDA context stays usable; the caller checks
+ * *err_flag).  The forward's own kernels bound every wait the same way.
+ * err_flag: required device int32.  MOE_ERR_INVALID_ARG for a null pointer
+ * or a timeout out of range.
+ */
+MOE_API moe_status_t moe_wait_flag(const int32_t *flag, int32_t expected, int64_t timeout_ns,
+                                   int32_t *err_flag, moe_stream_t stream);
+
+/*
  * Row gather (CSDN "forward", step 3: stacked_expert_tokens[r] = x_flat[token of r]).
  *   a_out[r, :] = x[sorted_token_idx[r], :] for r < n_rows.  x [T, d_h].
  * sorted_token_idx values must lie in [0, T).  d_h * elem_size % 16 == 0.

@@ -58,6 +58,7 @@ def lib():
         "moe_build_dispatch": (I, [P, P, I64, I64, I64, I64, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_build_dispatch_noalloc": (I, [P, P, I64, I64, I64, I64, P, P, P, P, P, P, P, P]),
         "moe_copy": (I, [P, P, I64, P]),
+        "moe_wait_flag": (I, [P, ctypes.c_int32, I64, P, P]),
         "moe_gather_rows": (I, [P, P, I64, I64, I64, I, P, P]),
         "moe_grouped_gate_up_silu": (I, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, P, P]),
         "moe_grouped_down": (I, [P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I, P, P, P]),
@@ -84,7 +85,7 @@ def exported_symbols():
             "moe_build_dispatch_workspace_bytes", "moe_forward_workspace_bytes",
             "moe_forward_workspace_offset", "moe_gate_topk", "moe_build_dispatch",
             "moe_build_dispatch_noalloc",
-            "moe_copy", "moe_gather_rows", "moe_grouped_gate_up_silu", "moe_grouped_down",
+            "moe_copy", "moe_wait_flag", "moe_gather_rows", "moe_grouped_gate_up_silu", "moe_grouped_down",
             "moe_grouped_mlp", "moe_pack_int4_bytes", "moe_pack_int4_weights", "moe_grouped_mlp_w4a16",
             "moe_forward_w4a16", "moe_reduce_fused", "moe_reduce_fused_scaled", "moe_forward"]
 
@@ -256,6 +257,17 @@ def moe_copy(src, dst):
     with torch.cuda.device(dev_t.device):
         _check(lib().moe_copy(_ptr(src), _ptr(dst), nbytes, _stream(dev_t.device)), "moe_copy")
     return dst
+
+
+def moe_wait_flag(flag, expected: int, timeout_s: float, err, device=None):
+    """Stream-ordered bounded wait until flag[0] >= expected (flag: int32 CUDA
+    tensor or pinned host tensor); on a timeout err[0] becomes MOE_ERR_TIMEOUT."""
+    _cuda_or_pinned(flag, "flag", dtype=torch.int32)
+    _cuda(err, "err", dtype=torch.int32)
+    dev = err.device if device is None else device
+    with torch.cuda.device(dev):
+        _check(lib().moe_wait_flag(_ptr(flag), int(expected), int(timeout_s * 1e9), _ptr(err), _stream(dev)),
+               "moe_wait_flag")
 
 
 def moe_gather_rows(x, sorted_token_idx, out=None):

@@ -194,6 +194,13 @@ moe_status_t moe_copy(const void *src, void *dst, int64_t bytes, moe_stream_t st
     return cuda_status(moe::launch_copy(src, dst, bytes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_wait_flag(const int32_t *flag, int32_t expected, int64_t timeout_ns, int32_t *err_flag,
+                           moe_stream_t stream) {
+    if (!flag || !err_flag || timeout_ns < 1 || timeout_ns > 10000000000ll) return MOE_ERR_INVALID_ARG;
+    return cuda_status(moe::launch_wait_flag(flag, expected, timeout_ns, err_flag,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
 static moe_status_t check_gemm_tables(const int32_t *s, const int32_t *o, const int32_t *p,
                                       const int32_t *g, int64_t m_blocks, int64_t n_rows, int64_t E) {
     if (!s || !o || !p || !g) return MOE_ERR_INVALID_ARG;

@@ -37,6 +37,10 @@ cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_
 
 // rows.cu
 cudaError_t launch_copy(const void *src, void *dst, int64_t bytes, cudaStream_t stream);
+// one thread polls *flag (system scope) until >= expected or timeout_ns pass
+// (then *err = kErrTimeout)
+cudaError_t launch_wait_flag(const int32_t *flag, int32_t expected, int64_t timeout_ns, int32_t *err,
+                             cudaStream_t stream);
 cudaError_t launch_gather_rows(const void *x, const int32_t *sorted_token_idx, int64_t n_rows,
                                int64_t d_h, int elem_bytes, void *a_out, cudaStream_t stream);
 cudaError_t launch_reduce_fused(const void *x, int64_t n_rows, const int32_t *pos,

@@ -419,6 +419,29 @@ __global__ void __launch_bounds__(RB_THREADS)
     }
 }
 
+// moe_wait_flag: lane 0 polls the flag with system-scope loads (a flag in
+// pinned host memory written by the host is seen), sleeping between polls;
+// the wait is bounded by the global timer and reports a timeout in *err.
+// Launched without programmatic dependent launch: work after it on the
+// stream starts only once it has returned.
+__global__ void __launch_bounds__(32)
+    wait_flag_kernel(const int32_t *flag, int32_t expected, unsigned long long timeout_ns, int32_t *err) {
+    if (threadIdx.x != 0) return;
+    const unsigned long long start = global_timer_ns();
+    for (;;) {
+        int32_t v;
+        asm volatile("ld.relaxed.sys.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v >= expected) break;
+        if (global_timer_ns() - start > timeout_ns) {
+            atomicExch(err, kErrTimeout);
+            break;
+        }
+        __nanosleep(1000);
+    }
+    // order what the flag's writer stored before the flag ahead of later work
+    __threadfence_system();
+}
+
 template <typename TIn, typename TOut>
 cudaError_t launch_reduce_bulk(const void *x, int64_t n_rows, const int32_t *pos, const float *w,
                                const float *x_sf, const float *sf, int64_t T, int64_t K, int64_t H,
@@ -505,6 +528,12 @@ cudaError_t launch_copy(const void *src, void *dst, int64_t bytes, cudaStream_t 
     const int blocks = static_cast<int>(want < cap ? want : cap);
     return launch_pdl(copy_kernel, dim3(static_cast<unsigned>(blocks)), dim3(CP_THREADS), 0, stream,
                       static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), nvec);
+}
+
+cudaError_t launch_wait_flag(const int32_t *flag, int32_t expected, int64_t timeout_ns, int32_t *err,
+                             cudaStream_t stream) {
+    wait_flag_kernel<<<1, 32, 0, stream>>>(flag, expected, static_cast<unsigned long long>(timeout_ns), err);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_reduce_fused(const void *x, int64_t n_rows, const int32_t *pos,

@@ -115,6 +115,11 @@ def test_argument_errors_without_launch(lib):
     assert lib.moe_copy(fake, P(0x200000), 24, None) == MOE_ERR_INVALID_ARG
     assert lib.moe_copy(P(0x100008), P(0x200000), 32, None) == MOE_ERR_INVALID_ARG
     assert lib.moe_copy(P(0x100000), P(0x100010), 64, None) == MOE_ERR_INVALID_ARG
+    # bounded flag wait: no flag, no error word, timeout out of range
+    assert lib.moe_wait_flag(None, 1, 1000, fake, None) == MOE_ERR_INVALID_ARG
+    assert lib.moe_wait_flag(fake, 1, 1000, None, None) == MOE_ERR_INVALID_ARG
+    assert lib.moe_wait_flag(fake, 1, 0, fake, None) == MOE_ERR_INVALID_ARG
+    assert lib.moe_wait_flag(fake, 1, 10_000_000_001, fake, None) == MOE_ERR_INVALID_ARG
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
