@@ -4,6 +4,8 @@ workload (T=4096, d_hidden 7168, d_expert 2048, 256 experts, top-8, bf16) at
 full size and in the benchmark's launch configuration on its routing and
 tables (all, bit for bit) and on sampled h / y rows and output tokens that
 the oracle computes one by one."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -75,6 +77,46 @@ def test_forward_token_counts(oracle, T):
     for n in TABLES:
         assert_bits_equal(views[n].cpu().numpy().reshape(ref[n].shape), ref[n], n)
     assert_close(bits(out), ref["out"], cfg.dtype, *MOE_TOL[cfg.dtype], "out")
+
+
+@pytest.mark.parametrize("T,E,k,d_e", [(64, 8, 2, 128), (65, 8, 2, 128), (40, 1, 1, 128), (300, 1, 1, 64),
+                                        (33, 8, 8, 128), (130, 4, 4, 192)])
+def test_forward_boundary_and_degenerate_shapes(oracle, T, E, k, d_e):
+    """T = 64 and 65 (the largest launch that gathers its rows inside the
+    expert MLP, and the smallest that runs the gather kernel first); a single
+    expert (every token's only slot on expert 0: 40 rows in one ragged block,
+    or 300 rows in two full blocks and a ragged one, each followed by the
+    trailing block the tables add, with weight exactly 1); every
+    token on every expert (k = E); a d_expert with a partial last stage-1 tile
+    (192).  Routing and tables bit for bit, the output within tolerance."""
+    dev = require_cuda()
+    cfg = dataclasses.replace(workloads.MOE_CONFIGS["tiny"], batch=1, seq=T, n_experts=E, top_k=k,
+                              d_expert=d_e)
+    d = workloads.make_moe_inputs(cfg, device=dev)
+    out, views = _run_forward(d, cfg)
+    nb = {n: (bits(v) if v is not None else None) for n, v in d.items()}
+    ref = oracle.moe_forward(nb["x"], nb["wg"], nb["bias"], nb["w_gate"], nb["w_up"], nb["w_down"],
+                             cfg.top_k, cfg.dtype)
+    assert_bits_equal(views["topk_idx"].cpu().numpy(), ref["topk_idx"], "topk_idx")
+    for n in TABLES:
+        assert_bits_equal(views[n].cpu().numpy().reshape(ref[n].shape), ref[n], n)
+    if k == E:
+        assert (ref["group_sizes"] == T).all()
+    if E == 1:
+        assert np.array_equal(views["topk_w"].cpu().numpy(), np.ones((T, 1), np.float32))
+    rtol, atol = MOE_TOL[cfg.dtype]
+    assert_close(bits(views["y"]), ref["y"], cfg.dtype, rtol, atol, "y")
+    assert_close(bits(out), ref["out"], cfg.dtype, rtol, atol, "out")
+
+
+def test_forward_with_no_tokens_is_a_no_op():
+    dev = require_cuda()
+    cfg = workloads.MOE_CONFIGS["tiny"]
+    d = workloads.make_moe_inputs(cfg, device=dev, T=1)
+    x0 = d["x"][:0]
+    out = binding.moe_forward(x0, d["wg"], d["bias"], d["w_gate"], d["w_up"], d["w_down"], cfg.top_k)
+    torch.cuda.synchronize()
+    assert tuple(out.shape) == (0, cfg.d_hidden)
 
 
 @pytest.mark.parametrize("host_io", [False, True])
