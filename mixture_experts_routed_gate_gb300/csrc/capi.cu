@@ -375,7 +375,7 @@ static moe_status_t reduce_common(const void *x, int64_t n_rows, const int32_t *
                                   const float *w, const float *x_sf, const float *sf, int64_t T,
                                   int64_t K, int64_t H, moe_dtype_t in_dtype,
                                   moe_dtype_t out_dtype, void *out, int32_t *err_flag,
-                                  moe_stream_t stream, bool allow_fp8) {
+                                  moe_stream_t stream, bool allow_fp8, bool pos_early = false) {
     if (T < 0 || K <= 0 || H <= 0 || n_rows < 0) return MOE_ERR_INVALID_ARG;
     if (H % 256 != 0) return MOE_ERR_INVALID_ARG;
     if (!reduce_pair_ok(in_dtype, out_dtype, allow_fp8)) return MOE_ERR_UNSUPPORTED;
@@ -384,7 +384,7 @@ static moe_status_t reduce_common(const void *x, int64_t n_rows, const int32_t *
     if (!aligned16(out) || (x && !aligned16(x))) return MOE_ERR_INVALID_ARG;
     return cuda_status(moe::launch_reduce_fused(x, n_rows, pos, w, x_sf, sf, T, K, H, in_dtype,
                                                 out_dtype, out, err_flag,
-                                                reinterpret_cast<cudaStream_t>(stream)));
+                                                reinterpret_cast<cudaStream_t>(stream), pos_early));
 }
 
 moe_status_t moe_reduce_fused(const void *x, int64_t n_rows, const int32_t *token_topk_to_pos,
@@ -461,7 +461,10 @@ moe_status_t moe_forward(const void *x, const void *w_g, const float *bias, cons
                          d_e, E, dtype, hbuf, ybuf, ready, err_flag, stream, false);
     }
     if (st != MOE_OK) return st;
-    return moe_reduce_fused(ybuf, Tk, pos, topk_w, T, k, d_h, dtype, dtype, out, err_flag, stream);
+    // the combine's positions and weights come from the dispatch, which
+    // completed before the expert MLP passed its own dependency wait
+    return reduce_common(ybuf, Tk, pos, topk_w, nullptr, nullptr, T, k, d_h, dtype, dtype, out, err_flag,
+                         stream, false, true);
 }
 
 moe_status_t moe_forward_w4a16(const void *x, const void *w_g, const float *bias,
@@ -508,7 +511,10 @@ moe_status_t moe_forward_w4a16(const void *x, const void *w_g, const float *bias
                         padded, gidx, mb, nullptr, Tk, d_h, d_e, E, dtype, hbuf, ybuf, ready, err_flag,
                         stream, false);
     if (st != MOE_OK) return st;
-    return moe_reduce_fused(ybuf, Tk, pos, topk_w, T, k, d_h, dtype, dtype, out, err_flag, stream);
+    // the combine's positions and weights come from the dispatch, which
+    // completed before the expert MLP passed its own dependency wait
+    return reduce_common(ybuf, Tk, pos, topk_w, nullptr, nullptr, T, k, d_h, dtype, dtype, out, err_flag,
+                         stream, false, true);
 }
 
 

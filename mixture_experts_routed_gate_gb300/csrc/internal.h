@@ -43,10 +43,13 @@ cudaError_t launch_wait_flag(const int32_t *flag, int32_t expected, int64_t time
                              cudaStream_t stream);
 cudaError_t launch_gather_rows(const void *x, const int32_t *sorted_token_idx, int64_t n_rows,
                                int64_t d_h, int elem_bytes, void *a_out, cudaStream_t stream);
+// pos_early: the positions and weights were complete before the previous
+// kernel started (moe_forward: the dispatch precedes the expert MLP), so the
+// combine may read them before its dependency wait
 cudaError_t launch_reduce_fused(const void *x, int64_t n_rows, const int32_t *pos,
                                 const float *w, const float *x_sf, const float *sf, int64_t T,
                                 int64_t K, int64_t H, int in_dtype, int out_dtype, void *out,
-                                int32_t *err, cudaStream_t stream);
+                                int32_t *err, cudaStream_t stream, bool pos_early = false);
 
 // grouped_gemm.cu
 cudaError_t launch_grouped_gemm(bool gate_up, int dtype, const void *a, const void *w0,

@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(RB_THREADS)
     reduce_bulk_kernel(const TIn *__restrict__ x, int64_t n_rows, const int32_t *__restrict__ pos,
                        const float *__restrict__ w, const float *__restrict__ x_sf,
                        const float *__restrict__ sf, int T, int K, int H, int HT, int stages,
-                       TOut *__restrict__ out, int32_t *__restrict__ err) {
+                       TOut *__restrict__ out, int32_t *__restrict__ err, int pos_early) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row_bytes = HT * static_cast<int>(sizeof(TIn));
@@ -297,8 +297,6 @@ __global__ void __launch_bounds__(RB_THREADS)
         fence_mbar_init();
     }
     __syncthreads();
-    griddep_wait();  // x, positions and weights may come from the previous kernel
-    griddep_launch_dependents();
 
     // Items are dealt round-robin (neighbouring CTAs read neighbouring H tiles
     // of the same rows, which keeps DRAM pages open).  The producer holds the
@@ -326,8 +324,13 @@ __global__ void __launch_bounds__(RB_THREADS)
         bool ok = true;
         int p_cur, p_nxt;
         float w_cur, w_nxt;
+        // x, and unless the caller vouches for them the positions and
+        // weights, may come from the previous kernel: wait for it first
+        if (!pos_early) griddep_wait();
         load_group(0, p_cur, w_cur);
         load_group(G, p_nxt, w_nxt);
+        if (pos_early) griddep_wait();
+        griddep_launch_dependents();
         for (int64_t sidx = 0;; ++sidx) {
             const int64_t item = blockIdx.x + sidx * static_cast<int64_t>(gridDim.x);
             if (item >= n_items) break;
@@ -377,6 +380,8 @@ __global__ void __launch_bounds__(RB_THREADS)
         }
     } else {
         // ------------------------------- consumers ------------------------------
+        griddep_wait();  // out may still be read by the previous kernel
+        griddep_launch_dependents();
         const int ct = threadIdx.x - 32;  // 0 .. 127
         int stage = 0;
         uint32_t phase = 0;
@@ -445,7 +450,7 @@ __global__ void __launch_bounds__(32)
 template <typename TIn, typename TOut>
 cudaError_t launch_reduce_bulk(const void *x, int64_t n_rows, const int32_t *pos, const float *w,
                                const float *x_sf, const float *sf, int64_t T, int64_t K, int64_t H,
-                               void *out, int32_t *err, cudaStream_t stream) {
+                               void *out, int32_t *err, cudaStream_t stream, bool pos_early) {
     // H tile: the largest of 1024 / 512 / 256 that divides H with a slot row <= 2 KB
     int HT = 256;
     for (int cand : {1024, 512}) {
@@ -477,15 +482,16 @@ cudaError_t launch_reduce_bulk(const void *x, int64_t n_rows, const int32_t *pos
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(RB_THREADS), smem, stream,
                       static_cast<const TIn *>(x), n_rows, pos, w, x_sf, sf, static_cast<int>(T),
                       static_cast<int>(K), static_cast<int>(H), HT, stages,
-                      static_cast<TOut *>(out), err);
+                      static_cast<TOut *>(out), err, pos_early ? 1 : 0);
 }
 
 template <typename TIn, typename TOut>
 cudaError_t launch_reduce_typed(const void *x, int64_t n_rows, const int32_t *pos, const float *w,
                                 const float *x_sf, const float *sf, int64_t T, int64_t K,
-                                int64_t H, void *out, int32_t *err, cudaStream_t stream) {
+                                int64_t H, void *out, int32_t *err, cudaStream_t stream, bool pos_early) {
     if (K <= RB_MAX_K)
-        return launch_reduce_bulk<TIn, TOut>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream);
+        return launch_reduce_bulk<TIn, TOut>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream,
+                                             pos_early);
     const int64_t threads = T * (H / 8);
     const int64_t blocks = (threads + RD_THREADS - 1) / RD_THREADS;
     return launch_pdl(reduce_fused_kernel<TIn, TOut>, dim3(static_cast<unsigned>(blocks)),
@@ -497,12 +503,12 @@ cudaError_t launch_reduce_typed(const void *x, int64_t n_rows, const int32_t *po
 template <typename TIn>
 cudaError_t launch_reduce_in(const void *x, int64_t n_rows, const int32_t *pos, const float *w,
                              const float *x_sf, const float *sf, int64_t T, int64_t K, int64_t H,
-                             int out_dtype, void *out, int32_t *err, cudaStream_t stream) {
+                             int out_dtype, void *out, int32_t *err, cudaStream_t stream, bool pe) {
     switch (out_dtype) {
-        case kF16: return launch_reduce_typed<TIn, __half>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream);
-        case kBF16: return launch_reduce_typed<TIn, __nv_bfloat16>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream);
-        case kF32: return launch_reduce_typed<TIn, float>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream);
-        case kE4M3: return launch_reduce_typed<TIn, __nv_fp8_e4m3>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream);
+        case kF16: return launch_reduce_typed<TIn, __half>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream, pe);
+        case kBF16: return launch_reduce_typed<TIn, __nv_bfloat16>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream, pe);
+        case kF32: return launch_reduce_typed<TIn, float>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream, pe);
+        case kE4M3: return launch_reduce_typed<TIn, __nv_fp8_e4m3>(x, n_rows, pos, w, x_sf, sf, T, K, H, out, err, stream, pe);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -539,12 +545,13 @@ cudaError_t launch_wait_flag(const int32_t *flag, int32_t expected, int64_t time
 cudaError_t launch_reduce_fused(const void *x, int64_t n_rows, const int32_t *pos,
                                 const float *w, const float *x_sf, const float *sf, int64_t T,
                                 int64_t K, int64_t H, int in_dtype, int out_dtype, void *out,
-                                int32_t *err, cudaStream_t stream) {
+                                int32_t *err, cudaStream_t stream, bool pos_early) {
     if (T <= 0) return cudaSuccess;
+    const bool pe = pos_early;
     switch (in_dtype) {
-        case kF16: return launch_reduce_in<__half>(x, n_rows, pos, w, x_sf, sf, T, K, H, out_dtype, out, err, stream);
-        case kBF16: return launch_reduce_in<__nv_bfloat16>(x, n_rows, pos, w, x_sf, sf, T, K, H, out_dtype, out, err, stream);
-        case kF32: return launch_reduce_in<float>(x, n_rows, pos, w, x_sf, sf, T, K, H, out_dtype, out, err, stream);
+        case kF16: return launch_reduce_in<__half>(x, n_rows, pos, w, x_sf, sf, T, K, H, out_dtype, out, err, stream, pe);
+        case kBF16: return launch_reduce_in<__nv_bfloat16>(x, n_rows, pos, w, x_sf, sf, T, K, H, out_dtype, out, err, stream, pe);
+        case kF32: return launch_reduce_in<float>(x, n_rows, pos, w, x_sf, sf, T, K, H, out_dtype, out, err, stream, pe);
         default: return cudaErrorInvalidValue;
     }
 }
