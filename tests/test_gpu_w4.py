@@ -88,12 +88,11 @@ def test_w4_mlp_vs_oracle(oracle, dtype, scaled, T, k, E, d_h, d_e, skew):
     kernel's h (isolates stage 2).  Ragged row counts, a partial N tile
     (d_e = 192), a single token, experts with up to 64 rows, empty experts,
     with and without per-channel scales."""
-    if not scaled and dtype == "f16" and d_h > 256:
-        pytest.skip("unscaled int4 sums over 512 inputs exceed the fp16 range of h")
     dev = require_cuda()
     rng, idx, x, qg, qu, qd, sg, su, sd = _w4_case(dtype, T, k, E, d_h, d_e, skew, 50 + T + E, scaled)
     if not scaled:
-        x = (x.float() * 0.05).to(x.dtype)  # keep unscaled int4 sums in range
+        # keep unscaled int4 sums (|q| <= 8 over d_h, then d_e, inputs) inside the fp16 range
+        x = (x.float() * (0.05 if d_h <= 256 else 0.01)).to(x.dtype)
     tab = oracle.build_dispatch(idx, None, E, 128)
     tabd = _tables_to(dev, tab)
     pg, pu, pd = _pack_pages(qg), _pack_pages(qu), _pack_pages(qd)
