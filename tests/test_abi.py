@@ -127,3 +127,11 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_build, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         binding.lib()
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    """A C11 program that includes only the header and the CUDA runtime
+    compiles (-Wall -Werror) and links against the library."""
+    import c_caller
+    exe = c_caller.build(str(tmp_path))
+    assert os.path.exists(exe)
