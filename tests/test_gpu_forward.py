@@ -79,19 +79,21 @@ def test_forward_token_counts(oracle, T):
     assert_close(bits(out), ref["out"], cfg.dtype, *MOE_TOL[cfg.dtype], "out")
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("T,E,k,d_e", [(64, 8, 2, 128), (65, 8, 2, 128), (40, 1, 1, 128), (300, 1, 1, 64),
                                         (33, 8, 8, 128), (130, 4, 4, 192)])
-def test_forward_boundary_and_degenerate_shapes(oracle, T, E, k, d_e):
+def test_forward_boundary_and_degenerate_shapes(oracle, dtype, T, E, k, d_e):
     """T = 64 and 65 (the largest launch that gathers its rows inside the
     expert MLP, and the smallest that runs the gather kernel first); a single
     expert (every token's only slot on expert 0: 40 rows in one ragged block,
     or 300 rows in two full blocks and a ragged one, each followed by the
     trailing block the tables add, with weight exactly 1); every
     token on every expert (k = E); a d_expert with a partial last stage-1 tile
-    (192).  Routing and tables bit for bit, the output within tolerance."""
+    (192); fp16 and bf16.  Routing and tables bit for bit, the output within
+    the dtype's tolerance."""
     dev = require_cuda()
     cfg = dataclasses.replace(workloads.MOE_CONFIGS["tiny"], batch=1, seq=T, n_experts=E, top_k=k,
-                              d_expert=d_e)
+                              d_expert=d_e, dtype=dtype)
     d = workloads.make_moe_inputs(cfg, device=dev)
     out, views = _run_forward(d, cfg)
     nb = {n: (bits(v) if v is not None else None) for n, v in d.items()}
