@@ -3,13 +3,15 @@
 // for the contract of every entry point.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "../../include/moe_routed_gate.h"
 #include "internal.h"
 
 namespace moe {
 
 int device_sm_count() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];  // zero-initialised; several host threads may call
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
     if (dev < 64 && cached[dev] > 0) return cached[dev];

@@ -315,7 +315,7 @@ cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_
                                static_cast<int>(m_blocks), ready);
     if (e != cudaSuccess || n_chunks == 0) return e;
     const size_t smem = static_cast<size_t>(DS_WARPS) * E * 4;
-    static size_t attr_bytes[64] = {0};
+    static std::atomic<size_t> attr_bytes[64];  // zero-initialised; several host threads may launch
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     if (smem > 48 * 1024 && (dev < 0 || dev >= 64 || attr_bytes[dev] < smem)) {

@@ -360,7 +360,7 @@ cudaError_t launch_gate_shape(const void *x, const void *wg, const float *bias, 
         !encode_tma_2d_plain(&tm_w, wg, static_cast<uint64_t>(d_h), static_cast<uint64_t>(E), SLICE, EXP))
         return cudaErrorInvalidValue;
     auto kern = gate_kernel<DT, TPW, WT, WE, FUSE>;
-    static bool attr_done[64] = {false};
+    static std::atomic<bool> attr_done[64];  // zero-initialised; several host threads may launch
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     if (smem > 48 * 1024 && (dev < 0 || dev >= 64 || !attr_done[dev])) {

@@ -785,15 +785,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
+    // looked up once (a function-local static: thread-safe initialisation)
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -873,7 +874,7 @@ cudaError_t launch_typed(const CUtensorMap *maps, const GemmParams &p, int grid,
     auto kern = grouped_gemm_kernel<DT, MODE>;
     // the shared-memory opt-in is set once per device (cheap launches, and no
     // attribute call while a graph is being captured after the first use)
-    static bool attr_done[64] = {false};
+    static std::atomic<bool> attr_done[64];  // zero-initialised; several host threads may launch
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {

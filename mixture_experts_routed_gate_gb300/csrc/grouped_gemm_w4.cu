@@ -721,7 +721,7 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
 template <int DT>
 cudaError_t launch_w4_typed(const CUtensorMap *maps, const W4Params &p, int grid, cudaStream_t stream) {
     auto kern = grouped_mlp_w4_kernel<DT>;
-    static bool attr_done[64] = {false};
+    static std::atomic<bool> attr_done[64];  // zero-initialised; several host threads may launch
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {

@@ -466,7 +466,7 @@ cudaError_t launch_reduce_bulk(const void *x, int64_t n_rows, const int32_t *pos
     stages = stages < 2 ? 2 : (stages > 6 ? 6 : stages);
     const size_t smem = static_cast<size_t>(stages) * stage_bytes + 16 * stages + 16;
     auto kern = reduce_bulk_kernel<TIn, TOut>;
-    static size_t attr_bytes[64] = {0};
+    static std::atomic<size_t> attr_bytes[64];  // zero-initialised; several host threads may launch
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     if (smem > 48 * 1024 && (dev < 0 || dev >= 64 || attr_bytes[dev] < smem)) {
