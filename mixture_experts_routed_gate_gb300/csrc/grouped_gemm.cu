@@ -24,8 +24,10 @@
 //               the activation dtype and store only the block's valid rows.
 // Tiles are (M block, N tile) pairs; the blocks are ordered by the schedule
 // below (full and partial blocks interleaved; blocks with no valid rows, the
-// padding blocks the tables create, left out) and dealt round-robin to the
-// CTAs.
+// padding blocks the tables create, left out).  The single-stage modes deal
+// them round-robin to the CTAs; the expert MLP mode starts CTA b on tile b
+// and hands out the rest from a shared counter, each CTA taking its next tile
+// two K steps before it issues the current one's last copy.
 //
 // The expert MLP mode runs both stages in one launch: the stage-1 tiles come
 // first in the tile order, then the stage-2 tiles in the same block order.
