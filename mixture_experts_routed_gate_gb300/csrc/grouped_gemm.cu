@@ -493,9 +493,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             const int kblocks = phase_params_of(p, ti.phase).k_blocks;
-            // stage-1 rows gathered from x: a swapped tile reads np rows, a full one 128
+            // stage-1 rows gathered from x: the block's rows rounded up to 4, one
+            // four-row gather per producer lane.  The MMA reads np (swapped) or 128
+            // rows of the slot; the ones past the gathered rows hold stale bytes
+            // that only reach accumulator rows / columns nobody stores, and every
+            // copy saved shortens the producer's issue path, which paces a K step
             const bool gather = IS_MLP && ti.phase == 0 && p.gather_idx != nullptr;
-            const int nrow_g = ti.rows <= SWAP_MAX_ROWS ? ((ti.rows + 15) & ~15) : BM;
+            const int nrow_g = (ti.rows + 3) & ~3;
             const uint32_t stage_tx = static_cast<uint32_t>((gather ? nrow_g * BK * 2 : A_SLOT) + B_BYTES);
             // this lane's four token ids (rows past the block repeat its first row)
             int i0 = 0, i1 = 0, i2 = 0, i3 = 0;
