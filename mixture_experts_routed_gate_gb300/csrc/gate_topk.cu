@@ -19,7 +19,7 @@
 //   * E <= 64: one CTA holds 1 token (small batches) or 4 tokens x all
 //     experts and also selects the top-k from its logits in shared memory
 //     (one launch for the gate);
-//   * many tokens: CTA = 16 tokens x 16 experts (8 warps of 4 x 8 pairs), then
+//   * many tokens: CTA = 16 tokens x 16 experts (4 warps of 8 x 8 pairs), then
 //     topk_softmax_kernel;
 //   * few tokens: CTA = one warp of 4 tokens x 8 experts (more CTAs in
 //     flight), then topk_softmax_kernel.
@@ -32,10 +32,12 @@ namespace {
 constexpr int SLICE = 256;                // elements per lane round: 32 lanes x 8
 constexpr int ROW_BYTES = SLICE * 2;      // 512 B of one row per slice
 // Ring depth: the small-batch shapes keep up to 8 slices (about 200 KB) in
-// flight, since their time is the latency of the first slices; the 8-warp
-// many-token shape keeps 4 (two CTAs per SM, each 64 KB of ring).  Measured
+// flight, since their time is the latency of the first slices; the 4-warp
+// many-token shape keeps 4 (three CTAs per SM, each 64 KB of ring).  Measured
 // at 4096 tokens x 256 experts x 7168: 3, 4 or 6 stages and one to three CTAs
-// per SM within 10%, 16 x 16 fastest among 8x16 / 16x16 / 16x32 / 32x16 tiles.
+// per SM within 10%, 16 x 16 fastest among 8x16 / 16x16 / 16x32 / 32x16 tiles;
+// 8 x 8 pairs per warp 2% faster than 4 x 8 (300 vs 306 us; 8x16 and 16x8
+// CTAs of 8 x 8 warps 340-357 us, 32x16 and 16x32 ones 304 us).
 __host__ __device__ constexpr int gate_stages(int rows, bool many_tokens) {
     return many_tokens ? 4 : ((200 * 1024) / (rows * ROW_BYTES) > 8 ? 8 : (200 * 1024) / (rows * ROW_BYTES));
 }
@@ -292,23 +294,33 @@ __global__ void __launch_bounds__(WT *WE * 32)
             acc[i][j] = v;
         }
 
-    // every lane now holds all TPW*8 sums; lane L keeps pair L (TPW*8 <= 32)
-    // and writes it: one select chain and one store, compact one-shot code
-    static_assert(TPW * 8 <= 32, "one pair per lane");
-    float mine = 0.0f;
-#pragma unroll
-    for (int i = 0; i < TPW; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) mine = (i * 8 + j == lane) ? acc[i][j] : mine;
-    const int my_i = lane >> 3, my_j = lane & 7;
-    const int my_t = t0 + wt + my_i, my_e = e0 + we + my_j;
+    // every lane now holds all TPW*8 sums; lane L keeps pairs L, L + 32, ...
+    // and writes them: one select chain and one store per pair
     if constexpr (!FUSE_TOPK) {
-        if (lane < TPW * 8 && my_t < T && my_e < E) {
-            float l = mine;
-            if (bias) l = l + bias[my_e];
-            logits[static_cast<int64_t>(my_t) * E + my_e] = l;
+#pragma unroll
+        for (int r = 0; r < (TPW * 8 + 31) / 32; ++r) {
+            const int pr = r * 32 + lane;
+            float mine = 0.0f;
+#pragma unroll
+            for (int i = 0; i < TPW; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) mine = (i * 8 + j == pr) ? acc[i][j] : mine;
+            const int my_t = t0 + wt + (pr >> 3), my_e = e0 + we + (pr & 7);
+            if (pr < TPW * 8 && my_t < T && my_e < E) {
+                float l = mine;
+                if (bias) l = l + bias[my_e];
+                logits[static_cast<int64_t>(my_t) * E + my_e] = l;
+            }
         }
     } else {
+        static_assert(TPW * 8 <= 32, "one pair per lane");
+        float mine = 0.0f;
+#pragma unroll
+        for (int i = 0; i < TPW; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mine = (i * 8 + j == lane) ? acc[i][j] : mine;
+        const int my_i = lane >> 3, my_j = lane & 7;
+        const int my_t = t0 + wt + my_i, my_e = e0 + we + my_j;
         // one CTA holds every expert of its TOK tokens: logits to shared
         // memory, then warp w selects the top-k of token t0 + w
         static_assert(!FUSE_TOPK || (WT == 1 && EXP == 64 && TPW <= WE), "fused shape");
@@ -404,8 +416,8 @@ cudaError_t launch_gate_typed(const void *x, const void *wg, const float *bias, 
         return launch_gate_shape<DT, 4, 1, 8, true>(x, wg, bias, T, d_h, E, k, logits, idx, w, stream);
     }
     cudaError_t e;
-    if (T >= 512)  // 16 tokens x 16 experts per CTA: 8 warps of 4 x 8 pairs, two CTAs per SM
-        e = launch_gate_shape<DT, 4, 4, 2, false>(x, wg, bias, T, d_h, E, k, logits, idx, w, stream);
+    if (T >= 512)  // 16 tokens x 16 experts per CTA: 4 warps of 8 x 8 pairs, three CTAs per SM
+        e = launch_gate_shape<DT, 8, 2, 2, false>(x, wg, bias, T, d_h, E, k, logits, idx, w, stream);
     else           // one warp of 4 x 8 pairs per CTA
         e = launch_gate_shape<DT, 4, 1, 1, false>(x, wg, bias, T, d_h, E, k, logits, idx, w, stream);
     if (e != cudaSuccess) return e;

@@ -45,7 +45,10 @@ def test_gate_topk_workloads(oracle, name):
 
 
 @pytest.mark.parametrize("T,d_h,E,k,dtype", [(37, 512, 40, 3, "bf16"), (1, 256, 8, 8, "f16"),
-                                             (100, 768, 1, 1, "bf16"), (17, 256, 1000, 32, "f16")])
+                                             (100, 768, 1, 1, "bf16"), (17, 256, 1000, 32, "f16"),
+                                             # the many-token shape (T >= 512, E > 64), ragged in
+                                             # both tokens and experts
+                                             (601, 512, 100, 4, "f16"), (530, 768, 72, 8, "bf16")])
 def test_gate_topk_ragged_shapes(oracle, T, d_h, E, k, dtype):
     dev = require_cuda()
     g = torch.Generator(device=dev).manual_seed(T + E)
