@@ -13,10 +13,10 @@ namespace moe {
 int device_sm_count() {
     static std::atomic<int> cached[64];  // zero-initialised; several host threads may call
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 152;
     if (dev < 64 && cached[dev] > 0) return cached[dev];
     int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
     if (dev < 64) cached[dev] = n;
     return n;
 }
@@ -449,7 +449,8 @@ moe_status_t moe_forward(const void *x, const void *w_g, const float *bias, cons
     if (st != MOE_OK) return st;
     if (T <= 64) {
         // every block holds at most 64 rows (a swapped tile of np <= 64 rows):
-        // stage 1 gathers them from x, np / 4 four-row copies per K step.  A
+        // stage 1 gathers them from x, one four-row copy per four of the
+        // block's rows (rounded up) per K step.  A
         // full 128-row tile would take 32 such copies per step, which the
         // copy engine issues slower than one tiled copy of the gathered rows
         // (prefill: about 1.9x the expert MLP's time), so larger T first
