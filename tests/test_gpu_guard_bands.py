@@ -1,0 +1,188 @@
+"""Writes past the end (or before the start) of an output or a workspace.
+
+Every output and workspace each entry point writes is placed between two
+4 KiB guard bands of a byte pattern; after the call the bands must hold the
+pattern still.  The shapes are ragged (tokens, experts, rows per expert and
+columns that are not multiples of the kernels' tiles) so the edge masks of
+the gate, the dispatch, the gather, both GEMM stages (swapped and full
+tiles), the combine (both kernels) and the forward are the ones exercised.
+No index here is out of range for the buffers themselves: the check is that
+no kernel writes outside them."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import require_cuda
+from mixture_experts_routed_gate_gb300 import binding, workloads
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 4096  # bytes on each side; keeps the view 256-byte aligned
+PATTERN = 0xA5
+
+
+class Guards:
+    """Buffers placed between two guard bands of PATTERN bytes."""
+
+    def __init__(self, dev):
+        self.dev = dev
+        self.items = []
+
+    def empty(self, shape, dtype, name):
+        shape = tuple(int(s) for s in shape)
+        nbytes = torch.empty((), dtype=dtype).element_size()
+        for s in shape:
+            nbytes *= s
+        assert nbytes > 0, name
+        raw = torch.full((GUARD + nbytes + GUARD,), PATTERN, dtype=torch.uint8, device=self.dev)
+        self.items.append((name, raw, nbytes))
+        return raw[GUARD:GUARD + nbytes].view(dtype).view(shape)
+
+    def zeros(self, shape, dtype, name):
+        t = self.empty(shape, dtype, name)
+        t.zero_()
+        return t
+
+    def check(self):
+        torch.cuda.synchronize()
+        for name, raw, nbytes in self.items:
+            head = int((raw[:GUARD] != PATTERN).sum())
+            tail = int((raw[GUARD + nbytes:] != PATTERN).sum())
+            assert head == 0 and tail == 0, (
+                f"{name}: {head} guard bytes before and {tail} after the buffer were overwritten")
+
+
+def _dispatch_out(G, T, k, E):
+    mb = binding.num_m_blocks(T, k, E)
+    i32 = torch.int32
+    return dict(group_sizes=G.empty((E,), i32, "group_sizes"),
+                group_offsets=G.empty((E,), i32, "group_offsets"),
+                group_padded_offsets=G.empty((E,), i32, "group_padded_offsets"),
+                group_idx_for_bx=G.empty((mb,), i32, "group_idx_for_bx"),
+                sorted_token_idx=G.empty((T * k,), i32, "sorted_token_idx"),
+                sorted_row_weight=G.empty((T * k,), torch.float32, "sorted_row_weight"),
+                token_topk_to_pos=G.empty((T, k), i32, "token_topk_to_pos"))
+
+
+@pytest.mark.parametrize("T,d_h,E,k,dtype", [(601, 512, 100, 4, "f16"),   # 16 x 16 CTAs, ragged
+                                             (37, 512, 40, 3, "bf16"),    # top-k fused, E <= 64
+                                             (5, 256, 72, 8, "f16"),      # one-warp CTAs
+                                             (700, 768, 64, 6, "bf16")])  # 4 tokens per fused CTA
+def test_routing_dispatch_gather_stay_inside(T, d_h, E, k, dtype):
+    dev = require_cuda()
+    G = Guards(dev)
+    td = workloads.torch_dtype(dtype)
+    g = torch.Generator(device=dev).manual_seed(T * 7 + E)
+    x = torch.randn((T, d_h), generator=g, device=dev).to(td)
+    wg = (torch.randn((E, d_h), generator=g, device=dev) / d_h ** 0.5).to(td)
+    idx = G.empty((T, k), torch.int32, "topk_idx")
+    w = G.empty((T, k), torch.float32, "topk_w")
+    ws = G.empty((T * E * 4,), torch.uint8, "gate workspace")
+    binding.moe_gate_topk(x, wg, None, k, topk_idx=idx, topk_w=w, ws=ws)
+    need = int(binding.lib().moe_build_dispatch_workspace_bytes(T, k, E))
+    dws = G.empty((max(need, 16),), torch.uint8, "dispatch workspace")
+    tab = binding.moe_build_dispatch(idx, w, E, out=_dispatch_out(G, T, k, E), ws=dws)
+    tab2 = binding.moe_build_dispatch_noalloc(idx, w, E, out=_dispatch_out(G, T, k, E))
+    a = G.empty((T * k, d_h), td, "gathered rows")
+    binding.moe_gather_rows(x, tab["sorted_token_idx"], out=a)
+    G.check()
+    for name in tab:
+        assert torch.equal(tab[name], tab2[name]), name
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("T,E,k,d_h,d_e", [(150, 3, 2, 256, 192),   # full (non-swapped) tiles, partial N
+                                           (61, 5, 3, 512, 128),    # swapped tiles only
+                                           (97, 9, 4, 256, 320)])
+def test_expert_gemms_stay_inside(dtype, T, E, k, d_h, d_e):
+    dev = require_cuda()
+    cfg = workloads.MoEConfig("guard", 1, T, d_h, d_e, E, k, dtype, 21 + T)
+    d = workloads.make_moe_inputs(cfg, device=dev)
+    td = workloads.torch_dtype(dtype)
+    idx, w = binding.moe_gate_topk(d["x"], d["wg"], None, k)
+    tab = binding.moe_build_dispatch(idx, w, E)
+    a = binding.moe_gather_rows(d["x"], tab["sorted_token_idx"])
+    Tk = T * k
+    mb = tab["group_idx_for_bx"].numel()
+    G = Guards(dev)
+    err = G.zeros((1,), torch.int32, "err")
+    h = G.empty((Tk, d_e), td, "h (gate/up)")
+    binding.moe_grouped_gate_up_silu(a, d["w_gate"], d["w_up"], tab, h=h, err=err)
+    y = G.empty((Tk, d_h), td, "y (down)")
+    binding.moe_grouped_down(h, d["w_down"], tab, row_weights=tab["sorted_row_weight"], y=y, err=err)
+    h2 = G.empty((Tk, d_e), td, "h (expert MLP)")
+    y2 = G.empty((Tk, d_h), td, "y (expert MLP)")
+    ready = G.empty((mb + 1,), torch.int32, "ready counters")
+    binding.moe_grouped_mlp(a, d["w_gate"], d["w_up"], d["w_down"], tab, h=h2, y=y2, ready=ready, err=err)
+    h3 = G.empty((Tk, d_e), td, "h (expert MLP, gathering)")
+    y3 = G.empty((Tk, d_h), td, "y (expert MLP, gathering)")
+    ready3 = G.empty((mb + 1,), torch.int32, "ready counters (gathering)")
+    binding.moe_grouped_mlp(None, d["w_gate"], d["w_up"], d["w_down"], tab, h=h3, y=y3, ready=ready3,
+                            err=err, x=d["x"], sorted_token_idx=tab["sorted_token_idx"])
+    G.check()
+    assert int(err.item()) == 0
+    assert torch.equal(h2, h3) and torch.equal(y2, y3)
+
+
+@pytest.mark.parametrize("T,K,H,in_dt,out_dt", [(33, 8, 768, "bf16", "bf16"), (7, 40, 256, "f16", "f16"),
+                                                (19, 3, 512, "f32", "bf16"), (1, 8, 256, "f32", "f32")])
+def test_combine_stays_inside(T, K, H, in_dt, out_dt):
+    dev = require_cuda()
+    r = workloads.make_reduce_inputs(T, K, H, in_dt, 5, device=dev, scales=True)
+    G = Guards(dev)
+    err = G.zeros((1,), torch.int32, "err")
+    out = G.empty((T, H), workloads.torch_dtype(out_dt), "combine out")
+    binding.moe_reduce_fused(r["x"], r["pos"], r["w"], out=out, err=err)
+    out8 = G.empty((T, H), torch.float8_e4m3fn, "scaled combine e4m3 out")
+    binding.moe_reduce_fused_scaled(r["x"], r["pos"], r["w"], x_sf=r["x_sf"], sf=r["sf"], out=out8, err=err)
+    G.check()
+    assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("T,E,k,d_h,d_e", [(150, 3, 2, 256, 192), (61, 5, 3, 512, 128), (65, 8, 2, 256, 128)])
+def test_forward_stays_inside_its_workspace(dtype, T, E, k, d_h, d_e):
+    dev = require_cuda()
+    cfg = workloads.MoEConfig("guard", 1, T, d_h, d_e, E, k, dtype, 40 + T)
+    d = workloads.make_moe_inputs(cfg, device=dev)
+    td = workloads.torch_dtype(dtype)
+    G = Guards(dev)
+    ws = G.empty((binding.forward_workspace_bytes(T, d_h, d_e, E, k, td),), torch.uint8, "forward workspace")
+    out = G.empty((T, d_h), td, "forward out")
+    err = G.zeros((1,), torch.int32, "err")
+    binding.moe_forward(d["x"], d["wg"], None, d["w_gate"], d["w_up"], d["w_down"], k, ws=ws, out=out, err=err)
+    G.check()
+    assert int(err.item()) == 0
+    ref = binding.moe_forward(d["x"], d["wg"], None, d["w_gate"], d["w_up"], d["w_down"], k)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+
+
+def test_int4_forward_and_copy_stay_inside():
+    dev = require_cuda()
+    T, k, E, d_h, d_e = 33, 4, 8, 256, 192
+    rng = np.random.default_rng(3)
+
+    def u8(shape):
+        return torch.from_numpy(rng.integers(0, 256, shape, dtype=np.uint8)).to(dev)
+
+    def scale(shape, fan_in):
+        return torch.from_numpy((rng.uniform(0.5, 1.5, shape) / (8 * np.sqrt(fan_in))).astype(np.float32)).to(dev)
+
+    ex = binding.Int4Experts(u8((E, d_e, d_h // 2)), u8((E, d_e, d_h // 2)), u8((E, d_h, d_e // 2)),
+                             scale((E, d_e), d_h), scale((E, d_e), d_h), scale((E, d_h), d_e))
+    g = torch.Generator(device=dev).manual_seed(9)
+    x = torch.randn((T, d_h), generator=g, device=dev).to(torch.float16)
+    wg = (torch.randn((E, d_h), generator=g, device=dev) / d_h ** 0.5).to(torch.float16)
+    G = Guards(dev)
+    ws = G.empty((binding.forward_workspace_bytes(T, d_h, d_e, E, k, torch.float16),), torch.uint8,
+                 "int4 forward workspace")
+    out = G.empty((T, d_h), torch.float16, "int4 forward out")
+    err = G.zeros((1,), torch.int32, "err")
+    binding.moe_forward_w4a16(x, wg, None, ex, k, ws=ws, out=out, err=err)
+    src = torch.arange(4096 + 48, dtype=torch.int32, device=dev).to(torch.uint8)
+    dst = G.empty((4096 + 48,), torch.uint8, "copy dst")
+    binding.moe_copy(src, dst)
+    G.check()
+    assert int(err.item()) == 0
+    assert torch.equal(dst, src)
