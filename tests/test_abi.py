@@ -135,3 +135,32 @@ def test_header_is_plain_c_and_links(tmp_path):
     import c_caller
     exe = c_caller.build(str(tmp_path))
     assert os.path.exists(exe)
+
+
+@pytest.mark.parametrize("T,d_h,d_e,E,k", [(1, 256, 64, 1, 1), (64, 2048, 768, 64, 6), (65, 256, 192, 8, 2),
+                                           (4096, 7168, 2048, 256, 8), (300, 512, 320, 1000, 32)])
+def test_forward_workspace_sections_are_disjoint(lib, T, d_h, d_e, E, k):
+    """Every intermediate of moe_forward gets its own 256-byte aligned range
+    inside the workspace, large enough for its shape (checked on a host
+    buffer: only the library's sizing functions run)."""
+    import torch
+    for dtype in (torch.float16, torch.bfloat16):
+        need = binding.forward_workspace_bytes(T, d_h, d_e, E, k, dtype)
+        ws = torch.empty(need, dtype=torch.uint8)
+        views = binding.forward_workspace_views(ws, T, d_h, d_e, E, k, dtype)
+        base = ws.data_ptr()
+        ranges = []
+        for name, v in views.items():
+            lo = v.data_ptr() - base
+            hi = lo + v.numel() * v.element_size()
+            assert lo % 256 == 0, name
+            assert 0 <= lo and hi <= need, (name, lo, hi, need)
+            ranges.append((lo, hi, name))
+        ranges.sort()
+        for (lo0, hi0, n0), (lo1, hi1, n1) in zip(ranges, ranges[1:]):
+            assert hi0 <= lo1, f"{n0} [{lo0}, {hi0}) overlaps {n1} [{lo1}, {hi1})"
+        # the dispatch scratch sits between token_topk_to_pos and the rows A
+        off = [lib.moe_forward_workspace_offset(T, d_h, d_e, E, k, 0 if dtype == torch.float16 else 1, i)
+               for i in range(15)]
+        scratch = lib.moe_build_dispatch_workspace_bytes(T, k, E)
+        assert off[11] - off[10] >= scratch
