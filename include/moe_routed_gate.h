@@ -55,7 +55,7 @@ typedef enum { MOE_F16 = 0, MOE_BF16 = 1, MOE_F32 = 2, MOE_E4M3 = 3 } moe_dtype_
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1, /* null pointer, bad size, k > E, misaligned, ... */
-    MOE_ERR_UNSUPPORTED = 2, /* a dtype or shape combination this build does not run */
+    MOE_ERR_UNSUPPORTED = 2, /* a dtype or shape combination the library does not run */
     MOE_ERR_WORKSPACE = 3,   /* workspace smaller than the *_workspace_bytes answer */
     MOE_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
     MOE_ERR_DEVICE_FLAG = 5, /* (err_flag value) a combine position was out of range */

@@ -1,7 +1,7 @@
 // gate_topk.cu -- gate logits, top-k selection and softmax weights.
 //
 // The pages call the gate (CSDN "forward", step 1: expert_indices,
-// expert_scores = gating_network(x)) but do not print it.  This build reads
+// expert_scores = gating_network(x)) but do not print it.  This library reads
 // it as a linear gate with softmax over fp32 logits, top-k with ties to the
 // lower expert id, and the top-k probabilities as the routing weights.
 //
