@@ -109,7 +109,9 @@ MOE_API moe_status_t moe_gate_topk(const void *x, const void *w_g, const float *
  *   expert): row r = group_offsets[e] + rank; sorted_token_idx[r] = t,
  *   sorted_row_weight[r] = topk_w[f] (1 when topk_w is NULL),
  *   token_topk_to_pos[f] = r.
- * topk_idx [T,k] int32 with values in [0, E) (others give undefined tables);
+ * topk_idx [T,k] int32 with values in [0, E); a pair whose id lies outside
+ * that range is dropped (counted nowhere, given no row, its token_topk_to_pos
+ * entry left unwritten; nothing is written out of bounds);
  * outputs sized [E], [E], [E], [M_blk], [Tk], [Tk], [Tk].  block_m must be 128.
  * ws: moe_build_dispatch_workspace_bytes(T, k, E) bytes of scratch.
  */
