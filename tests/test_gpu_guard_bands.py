@@ -186,3 +186,39 @@ def test_int4_forward_and_copy_stay_inside():
     G.check()
     assert int(err.item()) == 0
     assert torch.equal(dst, src)
+
+
+@pytest.mark.parametrize("T,k,E", [(300, 4, 20),    # one-CTA dispatch
+                                   (5000, 8, 64)])  # histogram / scan / scatter kernels
+def test_dispatch_drops_ids_outside_the_experts(oracle, T, k, E):
+    """A pair whose expert id lies outside [0, E) is dropped: counted nowhere,
+    given no row, its token_topk_to_pos entry left as it was.  The valid
+    pairs get the tables the oracle gives when the dropped ones are sent to
+    one extra expert E instead (whose rows come after every other expert's),
+    and nothing is written outside the outputs."""
+    dev = require_cuda()
+    rng = np.random.default_rng(T + E)
+    idx = rng.integers(0, E, (T, k)).astype(np.int32)
+    bad = rng.random((T, k)) < 0.05
+    idx[bad] = np.where(rng.random(int(bad.sum())) < 0.5, -1, E + 3).astype(np.int32)
+    w = rng.random((T, k)).astype(np.float32)
+    G = Guards(dev)
+    out = _dispatch_out(G, T, k, E)
+    out["token_topk_to_pos"].fill_(-7)
+    need = int(binding.lib().moe_build_dispatch_workspace_bytes(T, k, E))
+    dws = G.empty((max(need, 16),), torch.uint8, "dispatch workspace")
+    binding.moe_build_dispatch(torch.from_numpy(idx).to(dev), torch.from_numpy(w).to(dev), E, out=out, ws=dws)
+    G.check()
+    ref = oracle.build_dispatch(np.where(bad, E, idx).astype(np.int32), w, E + 1)
+    got = {n: t.cpu().numpy() for n, t in out.items()}
+    n_valid = int((~bad).sum())
+    for name in ("group_sizes", "group_offsets", "group_padded_offsets"):
+        assert np.array_equal(got[name], ref[name][:E]), name
+    mb = got["group_idx_for_bx"].size
+    assert np.array_equal(got["group_idx_for_bx"], np.minimum(ref["group_idx_for_bx"][:mb], E - 1))
+    assert np.array_equal(got["sorted_token_idx"][:n_valid], ref["sorted_token_idx"][:n_valid])
+    assert np.array_equal(got["sorted_row_weight"][:n_valid].view(np.uint32),
+                          ref["sorted_row_weight"][:n_valid].view(np.uint32))
+    pos = got["token_topk_to_pos"]
+    assert np.array_equal(pos[~bad], ref["token_topk_to_pos"][~bad])
+    assert (pos[bad] == -7).all()
