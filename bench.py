@@ -709,12 +709,19 @@ def oracle_prefill_sample(cfg, budget_s):
 # ----------------------------------------------------------------------------- main
 
 def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=None)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", choices=list(workloads.MOE_CONFIGS), default="decode")
+    ap = argparse.ArgumentParser(
+        description="Routed-expert MoE forward throughput: one JSON line with tokens/s, the dominant "
+                    "kernel's roofline fraction, the end-to-end rate with host buffers and the oracle's rate.")
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs (one rank each under torchrun; independent replicas, weak scaling)")
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 2000 decode / tiny, 60 prefill; 3 for the reference arm)")
+    ap.add_argument("--warmup", type=int, default=5, help="untimed warm-up steps (at least 3)")
+    ap.add_argument("--impl", choices=["native", "reference"], default="native",
+                    help="native: the CUDA library; reference: the CPU oracle on the host cores")
+    ap.add_argument("--workload", choices=list(workloads.MOE_CONFIGS), default="decode",
+                    help="decode: 64 tokens, 2048/768, 64 experts, top-6, fp16; prefill: 4096 tokens, "
+                         "7168/2048, 256 experts, top-8, bf16; tiny: 64 tokens, 256/128, 8 experts, top-2")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time")
     ap.add_argument("--only", default=None,
                     choices=ONLY_STAGES + ["reduce-512", "reduce-4096"],
