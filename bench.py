@@ -12,10 +12,18 @@ is evicted (a 256 MB write, then a 256 MB read of another buffer), outside
 the timed events.  A second timed pass replays graphs of the six entry
 points with event record nodes between them for each kernel's device time.
 
+The headline workload is prefill (4096 tokens, d_hidden 7168, d_expert 2048,
+256 experts, top-8, bf16, Zipf gate bias), the largest one-GPU workload; the
+decode workload (64 tokens) follows as the ``decode`` sub-record with its own
+roofline, oracle rate and end-to-end rate, and moe_reduce_fused alone on the
+bf16 512 / 4096 x 8 x 7168 workloads as ``reduce_fused_bf16_x8_7168``.
+
 Prints ONE JSON line (rank 0).  ``value`` = tokens processed by all ranks /
 max-over-ranks time.  ``e2e`` = the same metric through the public
 ``binding.ForwardGraph`` with pinned host input and output buffers, the
 host-to-device and device-to-host copies inside the timed region.
+``cpu_baseline`` = the oracle's whole forward on the host cores over a
+bounded sample of the same workload (for prefill: tokens of the same batch).
 ``--impl reference`` times the CPU oracle on the host cores instead.
 """
 from __future__ import annotations
@@ -55,9 +63,9 @@ def kernels_per_step(cfg) -> int:
 
 
 # DRAM bytes (read + write) of one expert-MLP launch from one ncu capture
-# (1-pass dram__bytes_read.sum + dram__bytes_write.sum on GB300, the commands
-# in profiles/dram_traffic_full_size.md), valid for the kernel source whose
-# hash is given; any later change to that source reports null.
+# (1-pass dram__bytes_read.sum + dram__bytes_write.sum on GB300), valid for the
+# kernel source whose hash is given; any later change to that source reports
+# null.
 MLP_TRAFFIC = {"source_sha256_16": "507b569f1caa12ad",
                "bytes": {"decode": 604.74e6 + 3.26e6, "prefill": 16.015e9 + 572.22e6}}
 MLP_SOURCES = ["mixture_experts_routed_gate_gb300/csrc/grouped_gemm.cu",
@@ -276,7 +284,7 @@ def timing_events(n):
     return [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)]
 
 
-def run_native(args, cfg, rank, world, dev):
+def run_native(args, cfg, rank, world, dev, with_aux=True):
     from mixture_experts_routed_gate_gb300 import binding
     _build.build()
     binding.lib()
@@ -384,7 +392,7 @@ def run_native(args, cfg, rank, world, dev):
         raise RuntimeError(f"device error flag {int(step.err.item())} in the timed region")
 
     e2e = measure_e2e(args, cfg, d, dev, flush, world)
-    aux = measure_reduce_aux(dev, flush) if rank == 0 else None
+    aux = measure_reduce_aux(dev, flush) if rank == 0 and with_aux else None
     w4 = measure_w4(cfg, d, dev, flush) if rank == 0 and cfg.T <= 64 else None
     return dict(per_stage=per_stage, stages=list(step.stages), w4=w4, total_ms=total_ms, act_experts=act_experts,
                 sizes_pool=sizes_pool, clocks=clocks, e2e=e2e, aux=aux, mode=mode,
@@ -660,69 +668,181 @@ def run_only(args):
 
 # ----------------------------------------------------------------------------- oracle arm
 
-def oracle_sample(cfg, budget_s: float, min_runs: int = 1):
-    """The oracle's forward on the host cores: whole steps on the small
-    workloads, a few tokens of the dense per-token path on prefill."""
-    from oracle import oracle
-    oracle.build()
-    d = workloads.make_moe_inputs(cfg, device="cpu") if cfg.name != "prefill" else None
-    threads = oracle.threads(0)
-    if cfg.name == "prefill":
-        # routing of a 4096-token batch would need the full 22.5 GB of weights on
-        # the host: time the dense per-token path over 8 experts instead
-        return oracle_prefill_sample(cfg, budget_s), threads
-    nb = {n: (workloads.to_numpy_bits(v) if v is not None else None) for n, v in d.items()}
-    runs, t0 = 0, time.perf_counter()
-    while True:
-        oracle.moe_forward(nb["x"], nb["wg"], nb["bias"], nb["w_gate"], nb["w_up"], nb["w_down"],
-                           cfg.top_k, cfg.dtype)
-        runs += 1
-        el = time.perf_counter() - t0
-        if runs >= min_runs and el >= budget_s:
-            break
-    tok_s = cfg.T * runs / el
-    return dict(value=tok_s, seconds=el, sample=f"{runs} whole forward pass(es) of the {cfg.name} "
-                f"workload ({cfg.T} tokens each)"), threads
+class OracleSample:
+    """The oracle's whole forward (gate, top-k, dispatch tables, gather, both
+    expert stages, combine: ``oracle.moe_forward``) on the host cores, over a
+    bounded sample of a workload.
+
+    decode / tiny: whole batches of the workload's shape (drawn on the host).
+    prefill: a seeded sample of tokens of the very batch the GPU arm times
+    (drawn on the GPU with the same generator, so the bits are identical),
+    with the full gate (all 256 experts) and the full expert weights as
+    host arrays; only the experts the sample routes to are ever read, so
+    only those are copied into the (lazily committed) host arrays."""
+
+    PREFILL_TOKENS = 32
+
+    def __init__(self, cfg, device=None):
+        from oracle import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.cfg = cfg
+        if cfg.name != "prefill":
+            d = workloads.make_moe_inputs(cfg, device="cpu")
+            self.nb = {n: (workloads.to_numpy_bits(v) if v is not None else None) for n, v in d.items()}
+            self.tokens = cfg.T
+            self.sample = f"whole forward passes of the {cfg.name} workload ({cfg.T} tokens each)"
+            return
+        dev = device if device is not None else torch.device("cuda", 0)
+        d = workloads.make_moe_inputs(cfg, device=dev)
+        rng = np.random.default_rng(12345)
+        tok = np.sort(rng.choice(cfg.T, self.PREFILL_TOKENS, replace=False))
+        bits = workloads.to_numpy_bits
+        nb = {"x": bits(d["x"][torch.from_numpy(tok).to(dev)]), "wg": bits(d["wg"]),
+              "bias": d["bias"].cpu().numpy()}
+        idx, _ = oracle.gate_topk(nb["x"], nb["wg"], nb["bias"], cfg.top_k, cfg.dtype)
+        used = np.unique(idx)
+        E, d_h, d_e = cfg.n_experts, cfg.d_hidden, cfg.d_expert
+        for name, shape in (("w_gate", (E, d_e, d_h)), ("w_up", (E, d_e, d_h)), ("w_down", (E, d_h, d_e))):
+            host = np.empty(shape, np.uint16)  # pages of unused experts are never touched
+            for e in used:
+                host[e] = bits(d[name][int(e)])
+            nb[name] = host
+        del d
+        torch.cuda.empty_cache()
+        self.nb = nb
+        self.tokens = self.PREFILL_TOKENS
+        self.sample = (f"whole forward passes (gate over all {E} experts, top-{cfg.top_k}, dispatch, both "
+                       f"expert stages, combine) of {self.PREFILL_TOKENS} seeded tokens of the prefill "
+                       f"batch, routed to {used.size} experts")
+
+    def run_once(self):
+        nb, cfg = self.nb, self.cfg
+        self.oracle.moe_forward(nb["x"], nb["wg"], nb["bias"], nb["w_gate"], nb["w_up"], nb["w_down"],
+                                cfg.top_k, cfg.dtype)
+
+    def rate(self, budget_s: float, min_runs: int = 1):
+        """tokens/s over whole forward passes filling about budget_s seconds."""
+        runs, t0 = 0, time.perf_counter()
+        while True:
+            self.run_once()
+            runs += 1
+            el = time.perf_counter() - t0
+            if runs >= min_runs and el >= budget_s:
+                break
+        return dict(value=self.tokens * runs / el, seconds=el, runs=runs,
+                    sample=f"{runs} x {self.sample}"), self.oracle.threads(0)
 
 
-def oracle_prefill_sample(cfg, budget_s):
-    from oracle import oracle
-    small = workloads.MoEConfig("prefill-slice", 1, 8, cfg.d_hidden, cfg.d_expert, 8, cfg.top_k,
-                                cfg.dtype, cfg.seed)
-    d = workloads.make_moe_inputs(small, device="cpu")
-    nb = {n: (workloads.to_numpy_bits(v) if v is not None else None) for n, v in d.items()}
-    idx = np.tile(np.arange(cfg.top_k, dtype=np.int32), (small.T, 1))
-    w = np.full((small.T, cfg.top_k), 1.0 / cfg.top_k, np.float32)
-    toks = np.arange(small.T, dtype=np.int32)
-    runs, t0 = 0, time.perf_counter()
-    while True:
-        oracle.moe_tokens_dense(nb["x"], nb["w_gate"], nb["w_up"], nb["w_down"], idx, w, toks, cfg.dtype)
-        runs += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
-    return dict(value=small.T * runs / el, seconds=el,
-                sample=f"{runs} x {small.T} tokens through the dense per-token expert path "
-                       f"(8 experts of the prefill shape each); gate and dispatch not included")
+# ----------------------------------------------------------------------------- records
+
+def workload_record(args, cfg, res, world, steps, cpu_budget, dev):
+    """The figures of one workload's timed run: tokens/s, per-kernel times,
+    the expert MLP's roofline, the oracle's rate and the end-to-end rate."""
+    peaks, peak_src = load_peaks()
+    T, k, d_h, d_e, E = cfg.T, cfg.top_k, cfg.d_hidden, cfg.d_expert, cfg.n_experts
+    Tk = T * k
+    per_stage = res["per_stage"]
+    ms_step = res["total_ms"] / steps
+    value = aggregate_throughput(T * steps, world, res["total_ms"])
+    e_act = float(np.mean(res["act_experts"]))
+    es = 2
+    flops_step = roofline.moe_forward_flops(T, k, d_h, d_e, E)
+    stages = res["stages"]
+    # dominant kernel: the expert MLP (both grouped GEMM stages in one launch);
+    # its algorithmic bytes averaged over the pooled batches the steps cycle through
+    gu_ms = float(per_stage[:, stages.index("expert_mlp")].mean())
+    gu_bytes = float(np.mean([roofline.expert_mlp_bytes(Tk, d_h, d_e, a, es) for a in res["act_experts"]]))
+    gu_flops = roofline.expert_mlp_flops(Tk, d_h, d_e)
+    # a kernel inside a step of milliseconds runs at the sustained tensor rate
+    tflops_key = "bf16_tflops_sustained" if ms_step > 1.0 else "bf16_tflops"
+    t_bytes = gu_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_flops = gu_flops / (peaks[tflops_key] * 1e12)
+    traffic = mlp_traffic(cfg.name)
+    common = {"kernel": "grouped_gemm_kernel<MLP>", "traffic": traffic,
+              "traffic_source": ("dram__bytes_read.sum + dram__bytes_write.sum of one ncu capture of this "
+                                 "kernel at this workload, stored with the hash of the kernel source it was "
+                                 "taken on; null when the source differs" if traffic is not None else
+                                 "null: the kernel source differs from the one the stored ncu counters "
+                                 "were taken on"),
+              "launch_us": round(gu_ms * 1e3, 2), "algorithmic_bytes_per_launch": round(gu_bytes),
+              "algorithmic_flops_per_launch": gu_flops,
+              "time_at_hbm_peak_us": round(t_bytes * 1e6, 2), "time_at_tensor_peak_us": round(t_flops * 1e6, 2)}
+    if t_bytes >= t_flops:
+        achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+        rl = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+              "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peak_src + " (hbm_gbs)", **common}
+    else:
+        achieved = gu_flops / (gu_ms * 1e-3) / 1e12
+        rl = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks[tflops_key], "unit": "TFLOP/s",
+              "frac": round(achieved / peaks[tflops_key], 4), "peak_source": f"{peak_src} ({tflops_key})",
+              **common}
+    rl["tensor_frac_of_" + tflops_key] = round(gu_flops / (gu_ms * 1e-3) / 1e12 / peaks[tflops_key], 4)
+    bytes_min = float(np.mean([roofline.moe_forward_bytes_min(T, d_h, d_e, E, a, es) for a in res["act_experts"]]))
+    step_roof_ms = max(bytes_min / (peaks["hbm_gbs"] * 1e9), flops_step / (peaks[tflops_key] * 1e12)) * 1e3
+    sampler = OracleSample(cfg, dev)
+    cpu, threads = sampler.rate(cpu_budget)
+    del sampler
+    e2e = res["e2e"]
+    rec = {
+        "value": round(value, 1), "unit": "tokens/s", "ms_per_step": round(ms_step, 5), "steps": steps,
+        "tflops": round(flops_step * steps / (res["total_ms"] / 1e3) / 1e12, 3),
+        "step_roofline_frac": round(step_roof_ms / ms_step, 4),
+        "kernels_us": {s: round(float(per_stage[:, i].mean()) * 1e3, 2) for i, s in enumerate(stages)},
+        "kernels_note": "per-kernel times from replays of the same graphs with event nodes between the kernels",
+        "active_experts": e_act,
+        "expert_rows_max": int(max(int(s_.max()) for s_ in res["sizes_pool"])),
+        "roofline": rl,
+        "cpu_baseline": {"value": round(cpu["value"], 2), "unit": "tokens/s", "cores": threads,
+                         "kind": "oracle", "sample": cpu["sample"]},
+        "e2e": {"value": round(aggregate_throughput(T * steps, world, e2e["total_ms"]), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+        "gpu_launches": kernels_per_step(cfg) * steps,
+        "launch_mode": res["mode"],
+        "eager_ms_per_step": round(res["eager_ms"], 5),
+    }
+    if res.get("aux") is not None:
+        rec["reduce_fused_bf16_x8_7168"] = res["aux"]
+    if res.get("w4") is not None:
+        rec["w4a16"] = res["w4"]
+    rec["clocks"] = res["clocks"]
+    return rec
+
+
+def config_of(cfg, args):
+    return {"workload": describe(cfg), "T": cfg.T, "d_hidden": cfg.d_hidden, "d_expert": cfg.d_expert,
+            "n_experts": cfg.n_experts, "top_k": cfg.top_k,
+            "l2": "evicted before every timed step: 256 MB write, then a 256 MB read of another buffer",
+            "parallelism": f"replicas x{args.gpus}"}
 
 
 # ----------------------------------------------------------------------------- main
 
+DEFAULT_STEPS = {"decode": 2000, "tiny": 2000, "prefill": 60}
+
+
 def main():
     ap = argparse.ArgumentParser(
         description="Routed-expert MoE forward throughput: one JSON line with tokens/s, the dominant "
-                    "kernel's roofline fraction, the end-to-end rate with host buffers and the oracle's rate.")
+                    "kernel's roofline fraction, the end-to-end rate with host buffers and the oracle's rate "
+                    "on the prefill workload (the headline), with the decode workload and the combine alone "
+                    "as sub-records.")
     ap.add_argument("--gpus", type=int, default=1,
                     help="GPUs (one rank each under torchrun; independent replicas, weak scaling)")
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default: 2000 decode / tiny, 60 prefill; 3 for the reference arm)")
+                    help="timed steps of the headline workload (default: 60 prefill, 2000 decode / tiny; "
+                         "3 for the reference arm)")
     ap.add_argument("--warmup", type=int, default=5, help="untimed warm-up steps (at least 3)")
     ap.add_argument("--impl", choices=["native", "reference"], default="native",
                     help="native: the CUDA library; reference: the CPU oracle on the host cores")
-    ap.add_argument("--workload", choices=list(workloads.MOE_CONFIGS), default="decode",
-                    help="decode: 64 tokens, 2048/768, 64 experts, top-6, fp16; prefill: 4096 tokens, "
-                         "7168/2048, 256 experts, top-8, bf16; tiny: 64 tokens, 256/128, 8 experts, top-2")
-    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time")
+    ap.add_argument("--workload", choices=list(workloads.MOE_CONFIGS), default="prefill",
+                    help="headline workload. prefill: 4096 tokens, 7168/2048, 256 experts, top-8, bf16, Zipf "
+                         "gate bias; decode: 64 tokens, 2048/768, 64 experts, top-6, fp16; tiny: 64 tokens, "
+                         "256/128, 8 experts, top-2")
+    ap.add_argument("--sub-steps", type=int, default=500,
+                    help="timed steps of the decode sub-record (recorded with the prefill headline)")
+    ap.add_argument("--no-sub", action="store_true", help="skip the decode sub-record")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time per workload")
     ap.add_argument("--only", default=None,
                     choices=ONLY_STAGES + ["reduce-512", "reduce-4096"],
                     help="time one stage alone (profiling aid; not the benchmark line)")
@@ -735,7 +855,7 @@ def main():
         return
     cfg = workloads.MOE_CONFIGS[args.workload]
     if args.steps is None:
-        args.steps = {"decode": 2000, "tiny": 2000, "prefill": 60}[cfg.name] if args.impl == "native" else 3
+        args.steps = DEFAULT_STEPS[cfg.name] if args.impl == "native" else 3
     args.warmup = max(args.warmup, 3)
 
     rank = int(os.environ.get("RANK", "0"))
@@ -746,26 +866,24 @@ def main():
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": cfg.dtype,
             "data": "synthetic: seeded N(0,1) tokens, N(0,1/fan_in) random-init expert and gate weights",
-            "config": {"workload": describe(cfg), "T": cfg.T, "d_hidden": cfg.d_hidden,
-                       "d_expert": cfg.d_expert, "n_experts": cfg.n_experts, "top_k": cfg.top_k,
-                       "l2": "evicted before every timed step: 256 MB write, then a 256 MB read of another buffer",
-                       "parallelism": f"replicas x{args.gpus}"}}
+            "config": config_of(cfg, args)}
 
     if args.impl == "reference":
         if rank != 0:
             return
-        steps_ms = []
+        dev = torch.device("cuda", local) if torch.cuda.is_available() else None
+        sampler = OracleSample(cfg, dev)
+        steps_ms, info, threads = [], None, 1
         budget = max(1.0, args.cpu_budget / max(1, args.steps))
-        info = None
         for i in range(args.warmup + args.steps):
-            res, threads = oracle_sample(cfg, budget if i >= args.warmup else 0.0)
+            res, threads = sampler.rate(budget if i >= args.warmup else 0.0)
             if i >= args.warmup:
                 steps_ms.append(cfg.T / res["value"] * 1e3)
                 info = res
         tok_s = cfg.T * len(steps_ms) / (sum(steps_ms) / 1e3)
         line = dict(base, impl="reference", value=tok_s, ms_per_step=statistics.mean(steps_ms),
                     cpu_baseline={"value": tok_s, "unit": "tokens/s", "cores": threads,
-                                  "kind": "oracle", "sample": info["sample"]},
+                                  "kind": "oracle", "sample": f"per step: {info['sample']}"},
                     e2e={"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                          "d2h_bytes_per_step": 0})
         print(json.dumps(line))
@@ -775,64 +893,28 @@ def main():
         backend = "nccl" if torch.cuda.is_available() else "gloo"
         torch.distributed.init_process_group(backend=backend)
     dev = torch.device("cuda", local)
-    res = run_native(args, cfg, rank, world, dev)
+    res = run_native(args, cfg, rank, world, dev, with_aux=True)
+    rec = workload_record(args, cfg, res, world, args.steps, args.cpu_budget, dev) if rank == 0 else None
+    del res
+    sub = None
+    if cfg.name == "prefill" and not args.no_sub:
+        # the decode workload, every rank (the replicas stay in step), recorded by rank 0
+        dcfg = workloads.MOE_CONFIGS["decode"]
+        sargs = argparse.Namespace(**vars(args))
+        sargs.steps = max(args.sub_steps, args.steps)
+        torch.cuda.empty_cache()
+        dres = run_native(sargs, dcfg, rank, world, dev, with_aux=False)
+        if rank == 0:
+            sub = workload_record(sargs, dcfg, dres, world, sargs.steps, args.cpu_budget, dev)
+            sub = {"config": config_of(dcfg, args), "dtype": dcfg.dtype, **sub}
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return
-
-    peaks, peak_src = load_peaks()
-    T, k, d_h, d_e, E = cfg.T, cfg.top_k, cfg.d_hidden, cfg.d_expert, cfg.n_experts
-    Tk = T * k
-    per_stage = res["per_stage"]
-    ms_step = res["total_ms"] / args.steps
-    value = aggregate_throughput(T * args.steps, world, res["total_ms"])
-    e_act = float(np.mean(res["act_experts"]))
-    es = 2
-    flops_step = roofline.moe_forward_flops(T, k, d_h, d_e, E)
-    # dominant kernel: the expert MLP (both grouped GEMM stages in one launch)
-    stages = res["stages"]
-    gu_ms = float(per_stage[:, stages.index("expert_mlp")].mean())
-    gu_bytes = roofline.expert_mlp_bytes(Tk, d_h, d_e, round(e_act), es)
-    gu_flops = roofline.expert_mlp_flops(Tk, d_h, d_e)
-    t_bytes = gu_bytes / (peaks["hbm_gbs"] * 1e9)
-    t_flops = gu_flops / (peaks["bf16_tflops"] * 1e12)
-    if t_bytes >= t_flops:
-        achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
-        rl = {"kernel": "grouped_gemm_kernel<MLP>", "bound": "hbm", "achieved": round(achieved, 1),
-              "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-              "traffic": mlp_traffic(cfg.name), "peak_source": peak_src + " (hbm_gbs)",
-              "algorithmic_bytes_per_launch": gu_bytes, "launch_us": round(gu_ms * 1e3, 2)}
-    else:
-        achieved = gu_flops / (gu_ms * 1e-3) / 1e12
-        rl = {"kernel": "grouped_gemm_kernel<MLP>", "bound": "tensor", "achieved": round(achieved, 1),
-              "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-              "traffic": mlp_traffic(cfg.name), "peak_source": peak_src + " (bf16_tflops)",
-              "algorithmic_flops_per_launch": gu_flops, "launch_us": round(gu_ms * 1e3, 2)}
-    bytes_min = roofline.moe_forward_bytes_min(T, d_h, d_e, E, round(e_act), es)
-    step_roof_ms = max(bytes_min / (peaks["hbm_gbs"] * 1e9), flops_step / (peaks["bf16_tflops"] * 1e12)) * 1e3
-    cpu, threads = oracle_sample(cfg, args.cpu_budget)
-    e2e = res["e2e"]
     line = dict(base)
-    line.update({
-        "value": round(value, 1), "ms_per_step": round(ms_step, 5),
-        "tflops": round(flops_step * args.steps / (res["total_ms"] / 1e3) / 1e12, 3),
-        "step_roofline_frac": round(step_roof_ms / ms_step, 4),
-        "kernels_us": {s: round(float(per_stage[:, i].mean()) * 1e3, 2) for i, s in enumerate(stages)},
-        "kernels_note": "per-kernel times from replays of the same graphs with event nodes between the kernels",
-        "active_experts": e_act,
-        "roofline": rl,
-        "reduce_fused_bf16_x8_7168": res["aux"],
-        "w4a16": res["w4"],
-        "cpu_baseline": {"value": round(cpu["value"], 2), "unit": "tokens/s", "cores": threads,
-                         "kind": "oracle", "sample": cpu["sample"]},
-        "e2e": {"value": round(aggregate_throughput(T * args.steps, world, e2e["total_ms"]), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
-        "gpu_launches": kernels_per_step(cfg) * args.steps,
-        "launch_mode": res["mode"],
-        "eager_ms_per_step": round(res["eager_ms"], 5),
-        "clocks": res["clocks"],
-    })
+    line.update(rec)
+    if sub is not None:
+        line["decode"] = sub
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

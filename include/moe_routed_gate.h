@@ -134,8 +134,12 @@ MOE_API moe_status_t moe_build_dispatch(const int32_t *topk_idx, const float *to
  *   - Limit: ceil(T*k / 2048) * E <= 262144 counters (for E = 256 that is up
  *     to 2,097,152 token-expert pairs); larger problems return
  *     MOE_ERR_WORKSPACE without launching.
- *   - The first call on a device looks the array's device address up
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call made outside a stream capture looks the array's device
+ *     address up (cudaGetSymbolAddress, a host-side lookup); a call made
+ *     during a capture reuses the address of the last call outside one on
+ *     that device.  So make the first call on a device before any stream
+ *     capture, and after a cudaDeviceReset (which moves the array) make one
+ *     call outside a capture before capturing again.
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, other threads) race and give undefined tables.  Nothing needs
  *     clearing between calls: the first kernel writes every counter it reads.
@@ -339,7 +343,11 @@ MOE_API moe_status_t moe_reduce_fused_scaled(const void *x, int64_t n_rows,
                                      void *out, int32_t *err_flag, moe_stream_t stream);
 
 /*
- * The whole routed forward, stream ordered, no host round trip:
+ * The whole routed forward (CSDN "tilelang baseline": the custom_kernel entry
+ * that takes the tokens, the gate and the stacked expert weights and returns
+ * the layer output, and the "forward" section that composes routing, the
+ * table build, the two expert kernels and the weighted combine), stream
+ * ordered, no host round trip:
  *   moe_gate_topk -> moe_build_dispatch -> moe_gather_rows ->
  *   moe_grouped_mlp (stage 1 + stage 2 in one launch) -> moe_reduce_fused;
  * for T <= 64 the gather is done inside moe_grouped_mlp (its gathering form)

@@ -141,18 +141,38 @@ moe_status_t moe_gate_topk(const void *x, const void *w_g, const float *bias, in
                                              topk_w, s));
 }
 
-static moe_status_t build_dispatch(const int32_t *topk_idx, const float *topk_w, int64_t T,
-                                   int64_t k, int64_t E, int64_t block_m, int32_t *group_sizes,
-                                   int32_t *group_offsets, int32_t *group_padded_offsets,
-                                   int32_t *group_idx_for_bx, int32_t *sorted_token_idx,
-                                   float *sorted_row_weight, int32_t *token_topk_to_pos, void *ws,
-                                   size_t ws_bytes, int32_t *ready, moe_stream_t stream) {
+}  // extern "C"
+
+namespace moe {
+
+int check_dispatch_args(const int32_t *topk_idx, int64_t T, int64_t k, int64_t E, int64_t block_m,
+                        const int32_t *group_sizes, const int32_t *group_offsets,
+                        const int32_t *group_padded_offsets, const int32_t *group_idx_for_bx,
+                        const int32_t *sorted_token_idx, const float *sorted_row_weight,
+                        const int32_t *token_topk_to_pos) {
     if (T < 0 || k <= 0 || E <= 0 || E > 1024 || block_m != MOE_BLOCK_M) return MOE_ERR_INVALID_ARG;
     if (T * k > (int64_t(1) << 30)) return MOE_ERR_UNSUPPORTED;
     if (!group_sizes || !group_offsets || !group_padded_offsets || !group_idx_for_bx)
         return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!topk_idx || !sorted_token_idx || !sorted_row_weight || !token_topk_to_pos))
         return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+}  // namespace moe
+
+extern "C" {
+
+static moe_status_t build_dispatch(const int32_t *topk_idx, const float *topk_w, int64_t T,
+                                   int64_t k, int64_t E, int64_t block_m, int32_t *group_sizes,
+                                   int32_t *group_offsets, int32_t *group_padded_offsets,
+                                   int32_t *group_idx_for_bx, int32_t *sorted_token_idx,
+                                   float *sorted_row_weight, int32_t *token_topk_to_pos, void *ws,
+                                   size_t ws_bytes, int32_t *ready, moe_stream_t stream) {
+    const int st = moe::check_dispatch_args(topk_idx, T, k, E, block_m, group_sizes, group_offsets,
+                                            group_padded_offsets, group_idx_for_bx,
+                                            sorted_token_idx, sorted_row_weight, token_topk_to_pos);
+    if (st != MOE_OK) return static_cast<moe_status_t>(st);
     const size_t need = moe_build_dispatch_workspace_bytes(T, k, E);
     if (T > 0 && (ws_bytes < need || !ws)) return MOE_ERR_WORKSPACE;
     return cuda_status(moe::launch_dispatch(

@@ -347,31 +347,35 @@ static constexpr int64_t kStaticScratchInts = 262144;  // 1 MiB of int32 counter
 static __device__ __align__(256) int32_t g_dispatch_static_scratch[kStaticScratchInts];
 
 static std::mutex g_static_scratch_mu;
-static void *g_static_scratch_addr[64];  // device address per device id, looked up once
+static void *g_static_scratch_addr[64];  // last address seen per device id
 
 extern "C" MOE_API moe_status_t moe_build_dispatch_noalloc(
     const int32_t *topk_idx, const float *topk_w, int64_t T, int64_t k, int64_t E,
     int64_t block_m, int32_t *group_sizes, int32_t *group_offsets,
     int32_t *group_padded_offsets, int32_t *group_idx_for_bx, int32_t *sorted_token_idx,
     float *sorted_row_weight, int32_t *token_topk_to_pos, moe_stream_t stream) {
-    if (T < 0 || k <= 0 || E <= 0 || E > 1024 || block_m != MOE_BLOCK_M) return MOE_ERR_INVALID_ARG;
-    if (T * k > (int64_t(1) << 30)) return MOE_ERR_UNSUPPORTED;
-    if (!group_sizes || !group_offsets || !group_padded_offsets || !group_idx_for_bx)
-        return MOE_ERR_INVALID_ARG;
-    if (T > 0 && (!topk_idx || !sorted_token_idx || !sorted_row_weight || !token_topk_to_pos))
-        return MOE_ERR_INVALID_ARG;
+    const int st = moe::check_dispatch_args(topk_idx, T, k, E, block_m, group_sizes, group_offsets,
+                                            group_padded_offsets, group_idx_for_bx,
+                                            sorted_token_idx, sorted_row_weight, token_topk_to_pos);
+    if (st != MOE_OK) return static_cast<moe_status_t>(st);
     // the histograms need ceil(T*k / 2048) * E counters
     if (moe::dispatch_scratch_bytes(T * k, E) > sizeof(g_dispatch_static_scratch))
         return MOE_ERR_WORKSPACE;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return MOE_ERR_CUDA;
     void *scratch = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_static_scratch_mu);
-        if (g_static_scratch_addr[dev] == nullptr) {
-            // host code only sees a stand-in symbol: ask the runtime for the
-            // array's address on the current device
+        // Host code only sees a stand-in symbol: ask the runtime for the
+        // array's address in the current context.  Outside a capture the
+        // address is looked up on every call (a host-side table lookup), so a
+        // context re-created by cudaDeviceReset is picked up; during a capture
+        // the address of the last call outside one is used.
+        if (cap == cudaStreamCaptureStatusNone || g_static_scratch_addr[dev] == nullptr) {
             void *addr = nullptr;
             if (cudaGetSymbolAddress(&addr, g_dispatch_static_scratch) != cudaSuccess || !addr)
                 return MOE_ERR_CUDA;
@@ -385,7 +389,6 @@ extern "C" MOE_API moe_status_t moe_build_dispatch_noalloc(
     cudaError_t e = moe::launch_dispatch(topk_idx, topk_w, T, k, E, block_m, group_sizes,
                                          group_offsets, group_padded_offsets, group_idx_for_bx,
                                          m_blocks, sorted_token_idx, sorted_row_weight,
-                                         token_topk_to_pos, scratch, nullptr,
-                                         reinterpret_cast<cudaStream_t>(stream));
+                                         token_topk_to_pos, scratch, nullptr, s);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -27,6 +27,14 @@ cudaError_t launch_gate_topk(const void *x, const void *wg, const float *bias, i
                              int64_t d_h, int64_t E, int64_t k, int dtype, float *logits,
                              int32_t *topk_idx, float *topk_w, cudaStream_t stream);
 
+// capi.cu: the host-side argument checks shared by both dispatch entry
+// points (a moe_status_t value; MOE_OK when the call may go ahead).
+int check_dispatch_args(const int32_t *topk_idx, int64_t T, int64_t k, int64_t E, int64_t block_m,
+                        const int32_t *group_sizes, const int32_t *group_offsets,
+                        const int32_t *group_padded_offsets, const int32_t *group_idx_for_bx,
+                        const int32_t *sorted_token_idx, const float *sorted_row_weight,
+                        const int32_t *token_topk_to_pos);
+
 // dispatch.cu
 size_t dispatch_scratch_bytes(int64_t n_pairs, int64_t E);
 cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_t T, int64_t k,

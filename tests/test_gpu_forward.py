@@ -2,8 +2,9 @@
 workloads.  The small workloads are compared on every output; the prefill
 workload (T=4096, d_hidden 7168, d_expert 2048, 256 experts, top-8, bf16) at
 full size and in the benchmark's launch configuration on its routing and
-tables (all, bit for bit) and on sampled h / y rows and output tokens that
-the oracle computes one by one."""
+tables (all, bit for bit), on every h / y row of three experts (the largest,
+a mid-sized one, a small one) and on 256 output tokens that the oracle
+computes one by one by the dense per-token brute force."""
 import dataclasses
 
 import numpy as np
@@ -208,20 +209,18 @@ def test_forward_prefill_full_size(oracle):
     sizes = tab["group_sizes"]
     assert sizes.max() > 1000 and (sizes == 0).any(), "the Zipf bias should skew the loads"
 
-    # sampled rows of h and y: first and last rows, both ends of the largest
-    # expert and of its ragged last block, and rows of small experts
+    # every h and y row of three experts: the largest (> 1000 rows: many full
+    # 128-row tiles, walked stripe by stripe, and a ragged last block), a
+    # mid-sized one (several blocks and a ragged tail) and a small one whose
+    # single block runs as a swapped tile (<= 64 rows)
     offs = tab["group_offsets"]
     big = int(np.argmax(sizes))
-    small = [int(e) for e in np.argsort(sizes) if 0 < sizes[e] < 8][:2]
-    rows = {0, int(sizes.sum()) - 1, int(offs[big]), int(offs[big] + sizes[big] - 1),
-            int(offs[big] + (sizes[big] // 128) * 128 - 1), int(offs[big] + 127), int(offs[big] + 128)}
-    for e in small:
-        rows |= {int(offs[e]), int(offs[e] + sizes[e] - 1)}
-    rows = np.array(sorted(r for r in rows if 0 <= r < sizes.sum()), dtype=np.int64)
-    row_expert = np.searchsorted(np.cumsum(sizes), rows, side="right").astype(np.int32)
-    experts = np.unique(row_expert)
-    remap = {int(e): i for i, e in enumerate(experts)}
-    re = np.array([remap[int(e)] for e in row_expert], np.int32)
+    mids = [int(e) for e in np.argsort(sizes) if 200 <= sizes[e] <= 900 and sizes[e] % 128 != 0]
+    smalls = [int(e) for e in np.argsort(sizes) if 16 < sizes[e] <= 64]
+    assert mids and smalls, "the Zipf routing should give mid-sized and small experts"
+    experts = [big, mids[len(mids) // 2], smalls[-1]]
+    rows = np.concatenate([np.arange(offs[e], offs[e] + sizes[e]) for e in experts]).astype(np.int64)
+    re = np.concatenate([np.full(sizes[e], i, np.int32) for i, e in enumerate(experts)])
     x_h = bits(d["x"])
     a_rows = x_h[tab["sorted_token_idx"][rows]]
     h_ref = oracle.rows_gate_up_silu(a_rows, re, _compact(d["w_gate"], experts),
@@ -229,15 +228,41 @@ def test_forward_prefill_full_size(oracle):
     y_ref = oracle.rows_down(h_ref, re, _compact(d["w_down"], experts), cfg.dtype)
     rtol, atol = MOE_TOL[cfg.dtype]
     rows_t = torch.from_numpy(rows).to(dev)
-    assert_close(bits(views["h"].index_select(0, rows_t)), h_ref, cfg.dtype, rtol, atol, "sampled h rows")
-    assert_close(bits(views["y"].index_select(0, rows_t)), y_ref, cfg.dtype, rtol, atol, "sampled y rows")
+    assert_close(bits(views["h"].index_select(0, rows_t)), h_ref, cfg.dtype, rtol, atol,
+                 f"h rows of experts {experts} ({[int(sizes[e]) for e in experts]} rows)")
+    assert_close(bits(views["y"].index_select(0, rows_t)), y_ref, cfg.dtype, rtol, atol,
+                 f"y rows of experts {experts}")
 
-    # sampled output tokens, computed by the dense per-token brute force
-    tokens = np.array([0, 1, 1234, 2047, 4095], dtype=np.int32)
-    used = np.unique(ref_idx[tokens])
-    remap = {int(e): i for i, e in enumerate(used)}
-    idx_c = np.vectorize(lambda e: remap.get(int(e), 0))(ref_idx).astype(np.int32)
-    want = oracle.moe_tokens_dense(x_h, _compact(d["w_gate"], used), _compact(d["w_up"], used),
-                                   _compact(d["w_down"], used), idx_c, ref_w, tokens, cfg.dtype)
-    got = bits(out.index_select(0, torch.from_numpy(tokens.astype(np.int64)).to(dev)))
-    assert_close(got, want, cfg.dtype, rtol, atol, "sampled output tokens")
+    # 256 output tokens (the first, the last and a seeded sample), each
+    # computed by the dense per-token brute force from its own top-k; the
+    # host holds at most 64 experts' weights at a time
+    rng = np.random.default_rng(2)
+    tokens = np.unique(np.concatenate([[0, cfg.T - 1],
+                                       rng.choice(np.arange(1, cfg.T - 1), 254, replace=False)]))
+    assert tokens.size == 256
+    got_all = bits(out.index_select(0, torch.from_numpy(tokens.astype(np.int64)).to(dev)))
+    for group in _token_groups(tokens, ref_idx, 64):
+        used = np.unique(ref_idx[group])
+        remap = np.zeros(cfg.n_experts, np.int32)
+        remap[used] = np.arange(used.size, dtype=np.int32)
+        want = oracle.moe_tokens_dense(x_h, _compact(d["w_gate"], used), _compact(d["w_up"], used),
+                                       _compact(d["w_down"], used), remap[ref_idx], ref_w,
+                                       group.astype(np.int32), cfg.dtype)
+        got = got_all[np.searchsorted(tokens, group)]
+        assert_close(got, want, cfg.dtype, rtol, atol, f"output tokens {group[:4]}...")
+
+
+def _token_groups(tokens, topk_idx, max_experts):
+    """Split tokens into groups whose routed experts number at most
+    max_experts together (greedy, in token order)."""
+    groups, cur, cur_set = [], [], set()
+    for t in tokens:
+        e = set(int(v) for v in topk_idx[t])
+        if cur and len(cur_set | e) > max_experts:
+            groups.append(np.array(cur))
+            cur, cur_set = [], set()
+        cur.append(int(t))
+        cur_set |= e
+    if cur:
+        groups.append(np.array(cur))
+    return groups

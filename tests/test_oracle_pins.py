@@ -347,6 +347,65 @@ def test_grouped_gemms_random_vs_float64(oracle, dtype):
         assert np.all(np.abs(yf[r] - ref_y) <= tol_y)
 
 
+def test_row_forms_integer_closed_form(oracle):
+    """rows_gate_up_silu / rows_down (row i uses expert row_expert[i], the
+    forms the full-size tests sample with): fp32 storage, integer operands,
+    gate logits >= 40 so silu(G) rounds to G, a shuffled row -> expert map
+    that is neither sorted nor the identity, and power-of-two row weights.
+    Every sum is an integer below 2^24, so h = G*U and y = (h W_down^T) * rw
+    hold exactly against an int64 einsum."""
+    rng = np.random.default_rng(16)
+    n, E, d_h, d_e = 97, 5, 32, 16
+    row_expert = rng.integers(0, E, n).astype(np.int32)
+    assert not np.all(np.diff(row_expert) >= 0)
+    a = rng.integers(0, 3, (n, d_h)).astype(np.float32)
+    a[:, 0] = 1
+    wg = rng.integers(0, 2, (E, d_e, d_h)).astype(np.float32)
+    wg[:, :, 0] = 40
+    wu = rng.integers(-2, 3, (E, d_e, d_h)).astype(np.float32)
+    wd = rng.integers(-1, 2, (E, d_h, d_e)).astype(np.float32)
+    rw = rng.choice([0.5, 1.0, 2.0, 0.25], n).astype(np.float32)
+    h = oracle.rows_gate_up_silu(a, row_expert, wg, wu, "f32")
+    y = oracle.rows_down(h, row_expert, wd, "f32", row_weights=rw)
+    y1 = oracle.rows_down(h, row_expert, wd, "f32")
+    ai = a.astype(np.int64)
+    G = np.einsum("rj,rnj->rn", ai, wg.astype(np.int64)[row_expert])
+    U = np.einsum("rj,rnj->rn", ai, wu.astype(np.int64)[row_expert])
+    assert G.min() >= 40
+    H = G * U
+    assert np.array_equal(h, H.astype(np.float32))
+    Y = np.einsum("rn,ron->ro", H, wd.astype(np.int64)[row_expert])
+    assert np.abs(Y).max() < 2 ** 24
+    assert np.array_equal(y1, Y.astype(np.float32))
+    assert np.array_equal(y, (Y * rw[:, None]).astype(np.float32))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_row_forms_equal_the_block_walk_on_shuffled_rows(oracle, dtype):
+    """The rows of a dispatch fed to the per-row forms in a shuffled order,
+    each with the expert its block belongs to, give the table-driven
+    stages' rows bit for bit (random 16-bit inputs, rows spanning several
+    128-row blocks and a ragged tail, row weights in stage 2)."""
+    rng = np.random.default_rng(17)
+    T, k, E, d_h, d_e = 300, 2, 3, 64, 32
+    idx, tab = _random_tables(oracle, rng, T, k, E)
+    Tk = T * k
+    assert tab["group_sizes"].max() > 128
+    a = _enc(rng.standard_normal((Tk, d_h)), dtype)
+    wg = _enc(rng.standard_normal((E, d_e, d_h)) / 8, dtype)
+    wu = _enc(rng.standard_normal((E, d_e, d_h)) / 8, dtype)
+    wd = _enc(rng.standard_normal((E, d_h, d_e)) / 6, dtype)
+    rw = rng.random(Tk).astype(np.float32)
+    h = oracle.grouped_gate_up_silu(a, wg, wu, tab, dtype)
+    y = oracle.grouped_down(h, wd, tab, dtype, row_weights=rw)
+    expert_of_row = np.repeat(np.arange(E, dtype=np.int32), tab["group_sizes"])
+    perm = rng.permutation(Tk)
+    h_rows = oracle.rows_gate_up_silu(a[perm], expert_of_row[perm], wg, wu, dtype)
+    assert np.array_equal(h_rows, h[perm])
+    y_rows = oracle.rows_down(h[perm], expert_of_row[perm], wd, dtype, row_weights=rw[perm])
+    assert np.array_equal(y_rows, y[perm])
+
+
 def test_grouped_gemms_zero_weights(oracle):
     rng = np.random.default_rng(8)
     T, k, E, d_h, d_e = 20, 2, 4, 64, 32
