@@ -245,10 +245,12 @@ MOE_API moe_status_t moe_grouped_down(const void *h, const void *w_down, const i
  * T >= 1 is the number of rows of x (every index must be below it).  It pays
  * when blocks are small (at most 64 rows); a full 128-row tile is read faster
  * from gathered rows `a`.  Otherwise x and T are ignored and may be NULL / 0.
- * The waits are bounded: after about 2 s *err_flag is set to
- * MOE_ERR_TIMEOUT and the kernel returns (this needs all CTAs of the grid,
- * one per SM, resident at once; a GPU shared with a partitioning runtime can
- * break that).  Other arguments, layouts and errors as the two calls.
+ * Every tile is taken from the shared counter in order, and all stage-1
+ * tiles come before all stage-2 tiles, so a stage-2 tile only waits on tiles
+ * that running CTAs hold: the launch completes whether or not all its CTAs
+ * (one per SM) are resident at once.  The waits are bounded all the same:
+ * after about 2 s *err_flag is set to MOE_ERR_TIMEOUT and the kernel
+ * returns.  Other arguments, layouts and errors as the two calls.
  */
 MOE_API moe_status_t moe_grouped_mlp(const void *a, const void *w_gate, const void *w_up,
                              const void *w_down, const int32_t *group_sizes,

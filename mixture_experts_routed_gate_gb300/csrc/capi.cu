@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdlib>
 
 #include "../../include/moe_routed_gate.h"
 #include "internal.h"
@@ -19,6 +20,18 @@ int device_sm_count() {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
     if (dev < 64) cached[dev] = n;
     return n;
+}
+
+int mlp_grid(int64_t tiles) {
+    // MOE_MLP_GRID: a CTA count for the persistent expert-MLP launches in place
+    // of one CTA per SM (read at every launch; tests use it to run the kernel
+    // on fewer CTAs, or on more CTAs than fit on the GPU at once)
+    int64_t grid = device_sm_count();
+    if (const char *v = std::getenv("MOE_MLP_GRID")) {
+        const long n = std::strtol(v, nullptr, 10);
+        if (n >= 1 && n <= 65535) grid = n;
+    }
+    return static_cast<int>(tiles < grid ? tiles : grid);
 }
 
 }  // namespace moe

@@ -25,16 +25,19 @@
 // Tiles are (M block, N tile) pairs; the blocks are ordered by the schedule
 // below (full and partial blocks interleaved; blocks with no valid rows, the
 // padding blocks the tables create, left out).  The single-stage modes deal
-// them round-robin to the CTAs; the expert MLP mode starts CTA b on tile b
-// and hands out the rest from a shared counter, each CTA taking its next tile
-// two K steps before it issues the current one's last copy.
+// them round-robin to the CTAs; the expert MLP mode hands out every tile from
+// a shared counter, in order, each CTA taking its next tile two K steps
+// before it issues the current one's last copy.
 //
 // The expert MLP mode runs both stages in one launch: the stage-1 tiles come
 // first in the tile order, then the stage-2 tiles in the same block order.
 // Each epilogue warp that stores part of a block's h publishes it on a
 // per-block counter; the producer starts a stage-2 tile once its block's
-// counter is complete.  A CTA's stage-1 tiles all precede its stage-2 tiles
-// and every CTA of the grid is resident (one per SM), so every wait ends.
+// counter is complete.  Tiles are taken in order and every stage-1 tile
+// precedes every stage-2 tile, so when a stage-2 tile is taken, the stage-1
+// tiles it waits on have all been taken by running CTAs, whose own progress
+// waits on nothing later: every wait ends, whether or not the whole grid is
+// resident at once.
 // Both stages then share one wave tail and no launch gap separates them.
 //
 // Every wait is bounded (see
@@ -366,6 +369,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     griddep_wait();
     griddep_launch_dependents();
+    // dynamic: the first tile comes from the shared counter too (claimed here,
+    // its round trip hidden behind the schedule build), so every tile a CTA
+    // waits on belongs to a CTA that is already running
+    int first_tile = 0;
+    if (dynamic && threadIdx.x == 0) first_tile = atomicAdd(p.tile_counter, 1);
     // ----- schedule: classify the M blocks, list full and partial ones -----
     Schedule sc{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0, p.m_blocks};
     if (p.m_blocks <= MAX_SCHED) {
@@ -436,26 +444,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         int rslot = 0;
         uint32_t rphase = 0;
-        // dynamic: the first tile of CTA b is tile b; later ones come from the
-        // counter (offset by the grid).  The next tile is taken NEXT_FETCH K
-        // steps before the current tile's last copy is issued: late enough that
-        // at the end of the launch the last tiles go to CTAs that are about to
-        // be free (taking it at the start of the current tile bound them a whole
-        // tile early), early enough that the atomic's round trip is hidden (its
-        // result is first used at the next tile).
-        int next_tile = 0;
-        bool have_next = false;
+        // dynamic: every tile, the first included, comes from the shared
+        // counter, in order, so a stage-2 tile is only ever taken after all
+        // stage-1 tiles (which precede it in the order) were taken by running
+        // CTAs: progress does not depend on all CTAs being resident at once.
+        // The next tile is taken NEXT_FETCH K steps before the current tile's
+        // last copy is issued: late enough that at the end of the launch the
+        // last tiles go to CTAs that are about to be free (taking it at the
+        // start of the current tile bound them a whole tile early), early
+        // enough that the atomic's round trip is hidden (its result is first
+        // used at the next tile).
+        int next_tile = first_tile;
+        bool have_next = true;
         for (int it = 0; ok; ++it) {
             int tile = blockIdx.x + it * static_cast<int>(gridDim.x);
             if (dynamic) {
                 // pass the tile id on (-1: none left)
                 int go = 1;
                 if (lane == 0) {
-                    if (it > 0) {
-                        if (!have_next) next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
-                        tile = next_tile;
-                        have_next = false;
-                    }
+                    if (!have_next) next_tile = atomicAdd(p.tile_counter, 1);
+                    tile = next_tile;
+                    have_next = false;
                     if (tile >= total) tile = -1;
                     go = mbar_wait_bounded(tide_bar(rslot), rphase ^ 1u, abort_flag, p.err) ? 1 : 0;
                     if (go) {
@@ -515,7 +524,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int fetch_kb = kblocks > NEXT_FETCH ? kblocks - NEXT_FETCH : 0;
             for (int kb = 0; kb < kblocks; ++kb) {
                 if (dynamic && lane == 0 && kb == fetch_kb) {
-                    next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
+                    next_tile = atomicAdd(p.tile_counter, 1);
                     have_next = true;
                 }
                 int go = 1;
@@ -895,7 +904,8 @@ cudaError_t launch_typed(const CUtensorMap *maps, const GemmParams &p, int grid,
 template <int MODE>
 cudaError_t launch_mode(int dtype, const CUtensorMap *maps, const GemmParams &p, int64_t tiles,
                         cudaStream_t stream) {
-    const int grid = static_cast<int>(tiles < device_sm_count() ? tiles : device_sm_count());
+    const int grid = Layout<MODE>::MLP ? mlp_grid(tiles)
+                                       : static_cast<int>(tiles < device_sm_count() ? tiles : device_sm_count());
     if (dtype == kBF16) return launch_typed<kBF16, MODE>(maps, p, grid, stream);
     return launch_typed<kF16, MODE>(maps, p, grid, stream);
 }

@@ -318,6 +318,10 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
     }
     griddep_wait();  // the tables, x and the counters come from earlier kernels
     griddep_launch_dependents();
+    // every tile, the first included, comes from the shared counter (see the
+    // producer); the first claim's round trip hides behind the schedule build
+    int first_tile = 0;
+    if (threadIdx.x == 0) first_tile = atomicAdd(p.tile_counter, 1);
 
     // ----- schedule: the non-empty M blocks in order, with their lookups -----
     int n_blocks = 0;
@@ -361,14 +365,17 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
         // last copy (at the end of the launch the last tiles then go to CTAs
         // that are about to be free; the atomic's result is first used at the
         // next tile, so its round trip stays hidden)
-        int next_tile = 0;
-        bool have_next = false;
+        // Tiles are taken in order and stage-1 tiles precede stage-2 tiles, so a
+        // stage-2 tile's stage-1 tiles are all held by running CTAs when it is
+        // taken: progress does not need the whole grid resident at once.
+        int next_tile = first_tile;
+        bool have_next = true;
         for (int it = 0; ok; ++it) {
             int tile = 0;
             int go = 1;
             if (lane == 0) {
-                if (it > 0 && !have_next) next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
-                tile = it == 0 ? static_cast<int>(blockIdx.x) : next_tile;
+                if (!have_next) next_tile = atomicAdd(p.tile_counter, 1);
+                tile = next_tile;
                 have_next = false;
                 if (tile >= total) tile = -1;
                 go = mbar_wait_bounded(tide(rslot), rphase ^ 1u, abort_flag, p.err) ? 1 : 0;
@@ -420,7 +427,7 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
             const int fetch_kb = kstages > W4_NEXT_FETCH ? kstages - W4_NEXT_FETCH : 0;
             for (int kb = 0; kb < kstages; ++kb) {
                 if (lane == 0 && kb == fetch_kb) {
-                    next_tile = static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
+                    next_tile = atomicAdd(p.tile_counter, 1);
                     have_next = true;
                 }
                 const int nsub = min(W4_SUB, ksub - kb * W4_SUB);
@@ -798,7 +805,7 @@ cudaError_t launch_grouped_mlp_w4(int dtype, const void *x, const int32_t *gathe
     p.kb1 = static_cast<int>(d_e / W4_BK);
     p.err = err;
     const int64_t tiles = m_blocks * (p.nt0 + p.nt1);
-    const int grid = static_cast<int>(tiles < device_sm_count() ? tiles : device_sm_count());
+    const int grid = mlp_grid(tiles);
     if (dtype == kBF16) return launch_w4_typed<kBF16>(maps, p, grid, stream);
     return launch_w4_typed<kF16>(maps, p, grid, stream);
 }

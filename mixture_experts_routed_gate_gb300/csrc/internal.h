@@ -11,6 +11,9 @@
 namespace moe {
 
 int device_sm_count();
+// capi.cu: CTAs of a persistent expert-MLP launch with `tiles` tiles: one per
+// SM (at most `tiles`), or the MOE_MLP_GRID environment variable's count
+int mlp_grid(int64_t tiles);
 
 // grouped_gemm.cu: tensor map of a row-major [rows, inner] 16-bit matrix,
 // box = box_inner x box_rows elements, no swizzle.  False if encoding fails.

@@ -256,3 +256,44 @@ def test_grouped_mlp_gathering_form_equals_gathered_rows(oracle, dtype, T, k, E,
     assert int(err.item()) == 0
     assert_bits_equal(bits(h2), bits(h1), "gathered h")
     assert_bits_equal(bits(y2), bits(y1), "gathered y")
+
+
+@pytest.mark.parametrize("grid", [1, 7, 76, 304])
+@pytest.mark.parametrize("case", ["decode", "prefill-1024x32"])
+def test_expert_mlp_progress_does_not_need_a_resident_grid(oracle, monkeypatch, case, grid):
+    """The persistent expert MLP takes every tile, its first included, from a
+    shared counter, so a stage-2 tile never waits on a stage-1 tile that no
+    running CTA holds.  Run on 1, 7 or 76 CTAs, and on 304 CTAs (twice the
+    SMs: the second half can only start once CTAs of the first half have
+    exited), the forward completes with no timed-out wait and gives the same
+    bits as the launch with one CTA per SM (tiles are computed whole by one
+    CTA, in a fixed order, so the grid cannot change a result).  Cases: the
+    decode forward (few-token launch, rows gathered inside) and a 1024-token
+    prefill-shaped forward over 32 experts (full 128-row tiles, large experts'
+    stripe runs); the decode output is also checked against the oracle."""
+    import dataclasses
+    dev = require_cuda()
+    if case == "decode":
+        cfg = workloads.MOE_CONFIGS["decode"]
+    else:
+        cfg = dataclasses.replace(workloads.MOE_CONFIGS["prefill"], batch=1, seq=1024, n_experts=32)
+    d = workloads.make_moe_inputs(cfg, device=dev)
+
+    def run():
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        out = binding.moe_forward(d["x"], d["wg"], d["bias"], d["w_gate"], d["w_up"], d["w_down"],
+                                  cfg.top_k, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, f"device error flag {int(err.item())}"
+        return bits(out)
+
+    monkeypatch.delenv("MOE_MLP_GRID", raising=False)
+    want = run()
+    monkeypatch.setenv("MOE_MLP_GRID", str(grid))
+    got = run()
+    assert_bits_equal(got, want, f"{case}, {grid} CTAs vs one per SM")
+    if case == "decode":
+        nb = {n: (bits(v) if v is not None else None) for n, v in d.items()}
+        ref = oracle.moe_forward(nb["x"], nb["wg"], nb["bias"], nb["w_gate"], nb["w_up"], nb["w_down"],
+                                 cfg.top_k, cfg.dtype)
+        assert_close(got, ref["out"], cfg.dtype, *MOE_TOL[cfg.dtype], "decode out")
