@@ -229,7 +229,8 @@ class NativeStep:
         ready = ctypes.c_void_p(self.v["mlp_ready"].data_ptr())
         by_name = {
             "gate_topk": (L.moe_gate_topk, (p(x), p(d["wg"]), p(d["bias"]), T, d_h, E, k, self.code,
-                               p(v["topk_idx"]), p(v["topk_w"]), p(v["logits"]), T * E * 4, sp)),
+                               p(v["topk_idx"]), p(v["topk_w"]), p(v["logits"]),
+                               int(L.moe_gate_topk_workspace_bytes(T, E)), sp)),
             "dispatch": (L.moe_build_dispatch, (p(v["topk_idx"]), p(v["topk_w"]), T, k, E, 128, *tables,
                                     p(v["sorted_token_idx"]), p(v["sorted_row_weight"]),
                                     p(v["token_topk_to_pos"]), ctypes.c_void_p(self.scratch_ptr),
@@ -614,7 +615,7 @@ def run_only(args):
         E, k = cfg.n_experts, cfg.top_k
         idx = torch.empty((T, k), dtype=torch.int32, device=dev)
         w = torch.empty((T, k), dtype=torch.float32, device=dev)
-        ws = torch.empty(T * E * 4, dtype=torch.uint8, device=dev)
+        ws = torch.empty(int(binding.lib().moe_gate_topk_workspace_bytes(T, E)), dtype=torch.uint8, device=dev)
         def fn():
             binding.moe_gate_topk(d["x"], d["wg"], d["bias"], k, topk_idx=idx, topk_w=w, ws=ws)
         info = {"workload": describe(cfg), "flops": roofline.gate_flops(T, cfg.d_hidden, E)}

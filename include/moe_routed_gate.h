@@ -90,7 +90,17 @@ MOE_API size_t moe_forward_workspace_bytes(int64_t T, int64_t d_h, int64_t d_e, 
  *   topk_w[t, j] = softmax over all E logits at topk_idx[t, j] (no renormalisation).
  * x [T, d_h] and w_g [E, d_h] in `dtype` (f16 or bf16); bias [E] fp32 or NULL.
  * Requires d_h % 256 == 0, 1 <= k <= min(E, 32), E <= 1024.
- * ws: moe_gate_topk_workspace_bytes(T, E) bytes of scratch (the fp32 logits).
+ * ws: moe_gate_topk_workspace_bytes(T, E) bytes of scratch, 256-byte aligned;
+ * its first T*E*4 bytes receive the fp32 logits [T, E].
+ * Many tokens (T >= 1024): the products run on the tensor cores in another
+ * summation order, and every expert whose tensor-core logit lies within a
+ * stated error bound of the k-th largest is recomputed in the fixed order
+ * above, so topk_idx and topk_w are what the fixed order gives (an expert
+ * outside the bound cannot be selected).  The logits written then carry the
+ * fixed-order value for every recomputed expert (the selected ones among
+ * them) and the tensor-core value, within the bound, for the others; the
+ * softmax denominator sums those values.  Fewer tokens: every logit is the
+ * fixed-order value.
  */
 MOE_API moe_status_t moe_gate_topk(const void *x, const void *w_g, const float *bias, int64_t T,
                            int64_t d_h, int64_t E, int64_t k, moe_dtype_t dtype,

@@ -67,7 +67,7 @@ bool fwd_layout(int64_t T, int64_t d_h, int64_t d_e, int64_t E, int64_t k, moe_d
     const size_t Tk = static_cast<size_t>(T * k);
     const size_t mb = static_cast<size_t>(m_blocks_of(T, k, E, MOE_BLOCK_M));
     const size_t sz[kFwdSections] = {
-        static_cast<size_t>(T) * E * 4,  // 0 logits
+        moe_gate_topk_workspace_bytes(T, E),  // 0 logits (+ the tensor-core gate's scratch)
         Tk * 4,                          // 1 topk_idx
         Tk * 4,                          // 2 topk_w
         static_cast<size_t>(E) * 4,      // 3 group_sizes
@@ -115,7 +115,7 @@ int64_t moe_num_m_blocks(int64_t T, int64_t k, int64_t E, int64_t block_m) {
 
 size_t moe_gate_topk_workspace_bytes(int64_t T, int64_t E) {
     if (T < 0 || E <= 0) return static_cast<size_t>(-1);
-    return static_cast<size_t>(T) * static_cast<size_t>(E) * 4;
+    return align_up(static_cast<size_t>(T) * static_cast<size_t>(E) * 4) + moe::gate_tc_scratch_bytes(T, E);
 }
 
 size_t moe_build_dispatch_workspace_bytes(int64_t T, int64_t k, int64_t E) {
@@ -137,21 +137,34 @@ int64_t moe_forward_workspace_offset(int64_t T, int64_t d_h, int64_t d_e, int64_
     return static_cast<int64_t>(L.off[index]);
 }
 
-moe_status_t moe_gate_topk(const void *x, const void *w_g, const float *bias, int64_t T,
-                           int64_t d_h, int64_t E, int64_t k, moe_dtype_t dtype,
-                           int32_t *topk_idx, float *topk_w, void *ws, size_t ws_bytes,
-                           moe_stream_t stream) {
+static moe_status_t gate_topk(const void *x, const void *w_g, const float *bias, int64_t T,
+                              int64_t d_h, int64_t E, int64_t k, moe_dtype_t dtype,
+                              int32_t *topk_idx, float *topk_w, void *ws, size_t ws_bytes,
+                              int32_t *err_flag, moe_stream_t stream) {
     if (T < 0 || d_h <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
     if (d_h % 256 != 0 || k > E || k > 32 || E > 1024) return MOE_ERR_INVALID_ARG;
     if (!is_half_type(dtype)) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
     if (!x || !w_g || !topk_idx || !topk_w || !ws) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(w_g) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_g) || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0)
+        return MOE_ERR_INVALID_ARG;
     if (ws_bytes < moe_gate_topk_workspace_bytes(T, E)) return MOE_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     float *logits = static_cast<float *>(ws);
+    // the tensor-core gate's scratch follows the logits (present for many tokens)
+    void *tc_scratch = moe::gate_tc_scratch_bytes(T, E) > 0
+                           ? static_cast<char *>(ws) + align_up(static_cast<size_t>(T) * E * 4)
+                           : nullptr;
     return cuda_status(moe::launch_gate_topk(x, w_g, bias, T, d_h, E, k, dtype, logits, topk_idx,
-                                             topk_w, s));
+                                             topk_w, tc_scratch, err_flag, s));
+}
+
+moe_status_t moe_gate_topk(const void *x, const void *w_g, const float *bias, int64_t T,
+                           int64_t d_h, int64_t E, int64_t k, moe_dtype_t dtype,
+                           int32_t *topk_idx, float *topk_w, void *ws, size_t ws_bytes,
+                           moe_stream_t stream) {
+    return gate_topk(x, w_g, bias, T, d_h, E, k, dtype, topk_idx, topk_w, ws, ws_bytes, nullptr,
+                     stream);
 }
 
 }  // extern "C"
@@ -473,8 +486,8 @@ moe_status_t moe_forward(const void *x, const void *w_g, const float *bias, cons
     const int64_t Tk = T * k;
     const int64_t mb = m_blocks_of(T, k, E, MOE_BLOCK_M);
     moe_status_t st;
-    st = moe_gate_topk(x, w_g, bias, T, d_h, E, k, dtype, topk_idx, topk_w, logits,
-                       static_cast<size_t>(T) * E * 4, stream);
+    st = gate_topk(x, w_g, bias, T, d_h, E, k, dtype, topk_idx, topk_w, logits,
+                   moe_gate_topk_workspace_bytes(T, E), err_flag, stream);
     if (st != MOE_OK) return st;
     // the dispatch also clears the expert MLP's per-block counters
     st = build_dispatch(topk_idx, topk_w, T, k, E, MOE_BLOCK_M, sizes, offsets, padded, gidx, stok,
@@ -537,8 +550,8 @@ moe_status_t moe_forward_w4a16(const void *x, const void *w_g, const float *bias
     int32_t *ready = reinterpret_cast<int32_t *>(w + L.off[14]);
     const int64_t Tk = T * k;
     const int64_t mb = m_blocks_of(T, k, E, MOE_BLOCK_M);
-    moe_status_t st = moe_gate_topk(x, w_g, bias, T, d_h, E, k, dtype, topk_idx, topk_w, logits,
-                                    static_cast<size_t>(T) * E * 4, stream);
+    moe_status_t st = gate_topk(x, w_g, bias, T, d_h, E, k, dtype, topk_idx, topk_w, logits,
+                                moe_gate_topk_workspace_bytes(T, E), err_flag, stream);
     if (st != MOE_OK) return st;
     st = build_dispatch(topk_idx, topk_w, T, k, E, MOE_BLOCK_M, sizes, offsets, padded, gidx, stok,
                         sw, pos, scratch, moe::dispatch_scratch_bytes(Tk, E), ready, stream);

@@ -102,6 +102,39 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 }
 
 // ----------------------------------------------------------------------------
+// Gate arithmetic
+// ----------------------------------------------------------------------------
+// c + a*b for one 16-bit element of each packed pair (lo or hi half), the
+// fp32 accumulator updated by the mixed-precision FMA (16-bit sources, fp32
+// addend and result, one rounding).  A product of two fp16 or two bf16 values
+// is exact in fp32, so this is bit for bit fmaf(float(a), float(b), c) with
+// no separate conversion instructions.
+template <int DT, bool HI>
+__device__ __forceinline__ float fma_mixed(uint32_t a, uint32_t b, float c) {
+    float d;
+    if constexpr (DT == kBF16) {
+        if constexpr (HI)
+            asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+                "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}"
+                : "=f"(d) : "r"(a), "r"(b), "f"(c));
+        else
+            asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+                "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}"
+                : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    } else {
+        if constexpr (HI)
+            asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+                "fma.rn.f32.f16 %0, ah, bh, %3;\n\t}"
+                : "=f"(d) : "r"(a), "r"(b), "f"(c));
+        else
+            asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+                "fma.rn.f32.f16 %0, al, bl, %3;\n\t}"
+                : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    }
+    return d;
+}
+
+// ----------------------------------------------------------------------------
 // mbarrier
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -1,0 +1,664 @@
+// gate_tc.cu -- gate logits on the tensor cores for many tokens, with the
+// routing kept exactly what the fixed summation order gives.
+//
+// The routing (top-k ids, their order, the tables built from them) is defined
+// by logits summed in one fixed order (8-element chunks, chunk c by warp lane
+// c mod 32 in ascending index with fmaf, the 32 partials combined by the xor
+// butterfly 16, 8, 4, 2, 1, then + bias).  A tensor-core product sums in
+// another order, so its logits can differ in the last bits and could swap two
+// experts whose logits nearly tie.  This path therefore:
+//
+//   1. gate_tc_kernel: logits~ = x W_g^T on the tensor cores (tcgen05, fp32
+//      accumulation, operands by TMA), K split over S CTAs per output tile
+//      (partials [S, T, E]); the otherwise idle epilogue warps also compute
+//      |w_e|_2 for every gate row and, from the token tiles in shared memory,
+//      each split's share of |x_t|^2.
+//   2. gate_select_kernel, one CTA per token: sums the partials in a fixed
+//      order, bounds |logit~ - logit| <= delta(t, e) from |x_t|_2 |w_e|_2
+//      (Cauchy-Schwarz on sum |x_j w_j|) and the rounding depth of both
+//      orders, and keeps as candidates every expert whose upper bound reaches
+//      the k-th largest lower bound.  An expert outside that set has a logit
+//      strictly below k others, so it cannot be selected.  Every candidate's
+//      logit is then recomputed in the fixed order (the same bits as the
+//      CUDA-core gate), and the top-k is chosen among the candidates by
+//      (logit desc, id asc).  Weights: softmax at the selected experts, the
+//      denominator over the fixed-order logits of the candidates and the
+//      tensor-core logits of the others (their terms are below the k-th
+//      largest and within delta of exact).
+//
+// Error model behind delta (stated, not measured): one tcgen05 K=16 MMA step
+// returns the fp32 accumulator within 18 * 2^-23 * max(|acc_in|, |products|)
+// of the exact sum (17 addends, each aligned to the largest and truncated to
+// fp32 precision, plus the final rounding; products of two 16-bit values are
+// exact in fp32); a split of G such steps is then within 18 G 2^-23 of its
+// own sum |x_j w_j|, the fixed order within (d_h/32 + 5) 2^-24 of it, and the
+// S partials and the bias add S + 2 more roundings.  delta doubles that sum
+// of bounds and adds 2^-22 |logit~| for the final bias rounding on both sides.
+// If any value is not finite every expert becomes a candidate.
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int GT_BM = 128;       // tokens per tile (MMA M)
+constexpr int GT_BN = 256;       // experts per tile (MMA N)
+constexpr int GT_BK = 64;        // 64 x 2 B = one 128-byte swizzle row
+constexpr int GT_STAGES = 4;
+constexpr int GT_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int GT_A_BYTES = GT_BM * GT_BK * 2;
+constexpr int GT_B_BYTES = GT_BN * GT_BK * 2;
+constexpr int GT_SMEM = 1024 + GT_STAGES * (GT_A_BYTES + GT_B_BYTES) + 256;
+constexpr int GT_MAX_SPLITS = 8;
+constexpr int SEL_WARPS = 4;     // warps of a select CTA (one token)
+
+struct GateTcParams {
+    float *part;           // [S, T, E] fp32 partial logits (no bias)
+    float *wnorm;          // [E] |w_e|_2
+    float *xss;            // [S, T] sum of x_t^2 over each split's columns
+    const uint8_t *wg;     // gate weight [E, d_h], 16-bit elements
+    int T, E, d_h;
+    int nk;                // 64-wide K steps in d_h
+    int ks;                // K steps per split
+    int *err;
+};
+
+// Sum of squares of one row of d_h 16-bit values, by a warp (every lane
+// gets the total).  Eight 16-byte loads in flight per lane.
+template <int DT>
+__device__ __forceinline__ float row_sumsq(const uint8_t *row_bytes, int d_h, int lane) {
+    const uint4 *row = reinterpret_cast<const uint4 *>(row_bytes);
+    const int chunks = d_h / 8;
+    float ss = 0.0f;
+    for (int cb = lane; cb < chunks; cb += 32 * 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (cb + 32 * u < chunks) v[u] = __ldg(row + cb + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (cb + 32 * u < chunks) {
+                const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f = unpack2<DT>(w4[q]);
+                    ss = fmaf(f.x, f.x, ss);
+                    ss = fmaf(f.y, f.y, ss);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int sh = 16; sh >= 1; sh >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, sh);
+    return ss;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(GT_THREADS, 1)
+    gate_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                   const GateTcParams p) {
+    constexpr uint32_t IDESC = idesc_f16(DT == kBF16, GT_BM, GT_BN);
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + GT_STAGES * GT_A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + GT_STAGES * GT_B_BYTES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * GT_STAGES + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (GT_STAGES + s); };
+    const uint32_t acc_bar = bar0 + 8u * (2 * GT_STAGES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * GT_BM, n0 = blockIdx.y * GT_BN, split = blockIdx.z;
+    const int kb0 = split * p.ks;
+    const int kb1 = min(p.nk, kb0 + p.ks);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < GT_STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            // a stage is free once its MMAs completed (commit) and every
+            // epilogue warp has read its token rows' squares from it
+            mbar_init(empty_bar(s), 1 + 4);
+        }
+        mbar_init(acc_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), GT_BN);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    griddep_wait();  // x may come from the previous kernel
+    griddep_launch_dependents();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------ TMA producer ------------------------------
+            int stage = 0;
+            uint32_t phase = 0;
+            long issued = 0;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = full_bar(stage);
+                mbar_arrive_expect_tx(fb, GT_A_BYTES + GT_B_BYTES);
+                // rows past T or E read as zero
+                tma_load_2d(smem_u32(sA + stage * GT_A_BYTES), &tm_x, fb, kb * GT_BK, m0);
+                tma_load_2d(smem_u32(sB + stage * GT_B_BYTES), &tm_w, fb, kb * GT_BK, n0);
+                ++issued;
+                if (++stage == GT_STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) {
+                // let the copies in flight land before shared memory goes away
+                for (long j = 1; j <= GT_STAGES && j <= issued; ++j) {
+                    const long i = issued - j;
+                    const uint32_t bar = full_bar(static_cast<int>(i % GT_STAGES));
+                    const unsigned long long t0 = global_timer_ns();
+                    while (!mbar_try_wait(bar, static_cast<uint32_t>((i / GT_STAGES) & 1)))
+                        if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------- MMA issuer --------------------------------
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t a_desc = smem_desc_sw128(smem_u32(sA + stage * GT_A_BYTES));
+                const uint64_t b_desc = smem_desc_sw128(smem_u32(sB + stage * GT_B_BYTES));
+#pragma unroll
+                for (int k = 0; k < GT_BK / 16; ++k)
+                    tc_mma_f16(tmem_base, a_desc + 2u * k, b_desc + 2u * k, IDESC,
+                               (kb > kb0 || k > 0) ? 1u : 0u);
+                tc_commit(empty_bar(stage));
+                if (++stage == GT_STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            // the accumulator (or, after an abort, the last MMAs) is complete
+            tc_commit(acc_bar);
+            if (!ok) {
+                const unsigned long long t0 = global_timer_ns();
+                while (!mbar_try_wait(acc_bar, 0))
+                    if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
+            }
+        }
+    } else {
+        // -------------------------------- epilogue --------------------------------
+        // while the main loop runs: the sum of squares of this thread's token
+        // row over the split's columns, read from each stage's A tile (the
+        // row's 128 bytes; the swizzle only permutes 16-byte chunks inside
+        // them) before the stage is released
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const int t = m0 + row;
+        {
+            int stage = 0;
+            uint32_t phase = 0;
+            float ss = 0.0f;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                int go = 1;
+                if (lane == 0) go = mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.err) ? 1 : 0;
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) {
+                    ok = false;
+                    break;
+                }
+                const uint4 *r = reinterpret_cast<const uint4 *>(sA + stage * GT_A_BYTES + row * 128);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = r[c];
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const float2 f = unpack2<DT>(w4[h]);
+                        ss = fmaf(f.x, f.x, ss);
+                        ss = fmaf(f.y, f.y, ss);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(stage));
+                if (++stage == GT_STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (ok && blockIdx.y == 0 && t < p.T) p.xss[static_cast<int64_t>(split) * p.T + t] = ss;
+        }
+        // |w_e|_2 of a share of the gate rows (all CTAs together cover every
+        // row once), while the last MMAs run
+        {
+            const int n_cta = gridDim.x * gridDim.y * gridDim.z;
+            const int cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+            const int gw = cta * 4 + (warp - 2);
+            for (int e = gw; e < p.E; e += n_cta * 4) {
+                const float ss = row_sumsq<DT>(p.wg + static_cast<int64_t>(e) * p.d_h * 2, p.d_h, lane);
+                if (lane == 0) p.wnorm[e] = sqrtf(ss);
+            }
+        }
+        // then the partial logits of this tile and split: thread = token row
+        int ready = 1;
+        if (lane == 0) ready = mbar_wait_bounded(acc_bar, 0, abort_flag, p.err) ? 1 : 0;
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        if (ready) {
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+            float *out = p.part + (static_cast<int64_t>(split) * p.T + (t < p.T ? t : 0)) * p.E;
+#pragma unroll 1
+            for (int c = 0; c < GT_BN / 16; ++c) {
+                uint32_t r[16];
+                tmem_ld16(t_row + c * 16, r);
+                tmem_ld_wait();
+                const int e0 = n0 + c * 16;
+                if (t < p.T && e0 < p.E) {
+                    if (e0 + 16 <= p.E && (p.E & 3) == 0) {
+                        float4 *dst = reinterpret_cast<float4 *>(out + e0);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                 __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (e0 + i < p.E) out[e0 + i] = __uint_as_float(r[i]);
+                    }
+                }
+            }
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, GT_BN);
+    }
+}
+
+// One CTA of SEL_WARPS warps per token: warp 0 finds the candidates while the
+// other warps stage the token's row of x in shared memory; then all warps
+// recompute the candidates in the fixed order (two per pass of a warp), and
+// warp 0 selects the top-k and the weights.  Shared memory: the row of x
+// (d_h 16-bit values); per expert its logit (tensor-core value, replaced by
+// the fixed-order value for candidates); the candidate ids and their
+// fixed-order logits; the candidate count.
+template <int DT, int SLOTS>
+__global__ void __launch_bounds__(SEL_WARPS * 32)
+    gate_select_kernel(const uint8_t *__restrict__ x, const uint8_t *__restrict__ wg,
+                       const float *__restrict__ bias, const float *__restrict__ part,
+                       const float *__restrict__ wnorm, const float *__restrict__ xss, int T, int E,
+                       int d_h, int S, int k, float coef, float *__restrict__ logits,
+                       int32_t *__restrict__ topk_idx, float *__restrict__ topk_w) {
+    extern __shared__ __align__(16) uint8_t sel_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint4 *xs = reinterpret_cast<uint4 *>(sel_smem);
+    float *val = reinterpret_cast<float *>(sel_smem + d_h * 2);
+    int *cand_id = reinterpret_cast<int *>(val + E);
+    float *cand_val = reinterpret_cast<float *>(cand_id + E);
+    int *n_cand = reinterpret_cast<int *>(cand_val + E);
+    const int t = blockIdx.x;
+    const int chunks = d_h / 8;
+    griddep_wait();  // partials and norms come from gate_tc_kernel
+    griddep_launch_dependents();
+
+    if (warp != 0) {
+        // the token's row into shared memory, every load issued first
+        const uint4 *xrow = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t) * d_h * 2);
+        const int tid = threadIdx.x - 32, nthr = (SEL_WARPS - 1) * 32;
+        for (int cb = tid; cb < chunks; cb += nthr * 10) {
+            uint4 v[10];
+#pragma unroll
+            for (int u = 0; u < 10; ++u)
+                if (cb + nthr * u < chunks) v[u] = __ldg(xrow + cb + nthr * u);
+#pragma unroll
+            for (int u = 0; u < 10; ++u)
+                if (cb + nthr * u < chunks) xs[cb + nthr * u] = v[u];
+        }
+    } else {
+        float xv[8];
+#pragma unroll
+        for (int sp = 0; sp < 8; ++sp) xv[sp] = sp < S ? xss[static_cast<int64_t>(sp) * T + t] : 0.0f;
+        float xsum = xv[0];
+#pragma unroll
+        for (int sp = 1; sp < 8; ++sp)
+            if (sp < S) xsum = xsum + xv[sp];
+        const float xn = sqrtf(xsum);
+        // tensor-core logits (partials summed in split order, then + bias) and bounds
+        float lo[SLOTS], hi[SLOTS];
+        bool bad = !isfinite(xn);
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) {
+            const int e = s * 32 + lane;
+            lo[s] = -INFINITY;
+            hi[s] = -INFINITY;
+            if (e < E) {
+                float pv[8];
+#pragma unroll
+                for (int sp = 0; sp < 8; ++sp)
+                    pv[sp] = sp < S ? part[(static_cast<int64_t>(sp) * T + t) * E + e] : 0.0f;
+                float l = pv[0];
+#pragma unroll
+                for (int sp = 1; sp < 8; ++sp)
+                    if (sp < S) l = l + pv[sp];
+                const float b = bias ? bias[e] : 0.0f;
+                if (bias) l = l + b;
+                const float d = coef * fmaf(xn, wnorm[e], fabsf(b)) + 0x1.0p-22f * fabsf(l) + 1e-30f;
+                val[e] = l;
+                lo[s] = l - d;
+                hi[s] = l + d;
+                bad |= !isfinite(l) || !isfinite(d);
+            }
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        // theta = k-th largest lower bound (k rounds of a warp max; a removed
+        // value is marked NaN in a copy)
+        float theta = -INFINITY;
+        if (!bad) {
+            float rem[SLOTS];
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s) rem[s] = lo[s];
+            for (int j = 0; j < k; ++j) {
+                float best = -INFINITY;
+                int best_e = 0x7fffffff;
+#pragma unroll
+                for (int s = 0; s < SLOTS; ++s) {
+                    const int e = s * 32 + lane;
+                    if (e < E && !isnan(rem[s]) && (best_e == 0x7fffffff || rem[s] > best)) {
+                        best = rem[s];
+                        best_e = e;
+                    }
+                }
+#pragma unroll
+                for (int sh = 16; sh >= 1; sh >>= 1) {
+                    const float ob = __shfl_xor_sync(0xffffffffu, best, sh);
+                    const int oe = __shfl_xor_sync(0xffffffffu, best_e, sh);
+                    if (oe != 0x7fffffff && (best_e == 0x7fffffff || ob > best || (ob == best && oe < best_e))) {
+                        best = ob;
+                        best_e = oe;
+                    }
+                }
+#pragma unroll
+                for (int s = 0; s < SLOTS; ++s)
+                    if (s * 32 + lane == best_e) rem[s] = NAN;
+                theta = best;
+            }
+        }
+        // candidates, in ascending expert id
+        int n = 0;
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) {
+            const int e = s * 32 + lane;
+            const bool c = e < E && (bad || hi[s] >= theta);
+            const unsigned m = __ballot_sync(0xffffffffu, c);
+            if (c) cand_id[n + __popc(m & ((1u << lane) - 1u))] = e;
+            n += __popc(m);
+        }
+        if (lane == 0) *n_cand = n;
+    }
+    __syncthreads();
+    const int n = *n_cand;
+
+    // fixed-order logits of the candidates, two per pass of a warp: lane L sums
+    // its chunks c = L, L + 32, ... in ascending order (seven chunks' loads in
+    // flight at a time), then the xor butterfly
+    constexpr int U = 7;
+    for (int i0 = 2 * warp; i0 < n; i0 += 2 * SEL_WARPS) {
+        const int ng = min(2, n - i0);
+        const int e0 = cand_id[i0], e1 = cand_id[i0 + (ng > 1 ? 1 : 0)];
+        const uint4 *w0 = reinterpret_cast<const uint4 *>(wg + static_cast<int64_t>(e0) * d_h * 2);
+        const uint4 *w1 = reinterpret_cast<const uint4 *>(wg + static_cast<int64_t>(e1) * d_h * 2);
+        float acc0 = 0.0f, acc1 = 0.0f;
+        for (int cb = lane; cb < chunks; cb += 32 * U) {
+            uint4 a[U], b[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = cb + 32 * u;
+                if (c < chunks) {
+                    a[u] = __ldg(w0 + c);
+                    if (ng > 1) b[u] = __ldg(w1 + c);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = cb + 32 * u;
+                if (c < chunks) {
+                    const uint4 xv = xs[c];
+                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                    const uint32_t aw[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc0 = fma_mixed<DT, false>(xw[q], aw[q], acc0);
+                        acc0 = fma_mixed<DT, true>(xw[q], aw[q], acc0);
+                    }
+                    if (ng > 1) {
+                        const uint32_t bw[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            acc1 = fma_mixed<DT, false>(xw[q], bw[q], acc1);
+                            acc1 = fma_mixed<DT, true>(xw[q], bw[q], acc1);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int sh = 16; sh >= 1; sh >>= 1) {
+            acc0 = acc0 + __shfl_xor_sync(0xffffffffu, acc0, sh);
+            acc1 = acc1 + __shfl_xor_sync(0xffffffffu, acc1, sh);
+        }
+        if (bias) {
+            acc0 = acc0 + bias[e0];
+            acc1 = acc1 + bias[e1];
+        }
+        if (lane == 0) {
+            cand_val[i0] = acc0;
+            val[e0] = acc0;
+            if (ng > 1) {
+                cand_val[i0 + 1] = acc1;
+                val[e1] = acc1;
+            }
+        }
+    }
+    __syncthreads();
+    if (warp != 0) return;
+
+    // top-k among the candidates by (logit desc, id asc); lane j keeps slot j
+    unsigned taken = 0;  // bit i: candidate lane + 32 i already selected
+    float top = 0.0f, my_v = 0.0f;
+    int my_e = 0;
+    for (int j = 0; j < k; ++j) {
+        float best = -INFINITY;
+        int best_e = 0x7fffffff, best_i = -1;
+        for (int i = lane, b = 0; i < n; i += 32, ++b) {
+            if (taken & (1u << b)) continue;
+            const float v = cand_val[i];
+            const int e = cand_id[i];
+            if (best_i < 0 || v > best || (v == best && e < best_e)) {
+                best = v;
+                best_e = e;
+                best_i = i;
+            }
+        }
+#pragma unroll
+        for (int sh = 16; sh >= 1; sh >>= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best, sh);
+            const int oe = __shfl_xor_sync(0xffffffffu, best_e, sh);
+            const int oi = __shfl_xor_sync(0xffffffffu, best_i, sh);
+            if (oi >= 0 && (best_i < 0 || ob > best || (ob == best && oe < best_e))) {
+                best = ob;
+                best_e = oe;
+                best_i = oi;
+            }
+        }
+        if (best_i >= 0 && (best_i & 31) == lane) taken |= 1u << (best_i >> 5);
+        if (j == 0) top = best;
+        if (j == lane) {
+            my_v = best;
+            my_e = best_e;
+        }
+    }
+    // softmax denominator over every expert (per lane in slot order, then the
+    // butterfly), the logits row written once
+    float sum = 0.0f;
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+        const int e = s * 32 + lane;
+        if (e < E) {
+            const float v = val[e];
+            sum += expf(v - top);
+            logits[static_cast<int64_t>(t) * E + e] = v;
+        }
+    }
+#pragma unroll
+    for (int sh = 16; sh >= 1; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
+    if (lane < k) {
+        topk_idx[static_cast<int64_t>(t) * k + lane] = my_e;
+        topk_w[static_cast<int64_t>(t) * k + lane] = expf(my_v - top) / sum;
+    }
+}
+
+size_t select_smem_bytes(int64_t d_h, int64_t E) {
+    return static_cast<size_t>(d_h * 2 + E * 12 + 16);
+}
+
+int splits_for(int64_t T, int64_t E) {
+    const int64_t tiles = ((T + GT_BM - 1) / GT_BM) * ((E + GT_BN - 1) / GT_BN);
+    int64_t s = 128 / (tiles > 0 ? tiles : 1);
+    return static_cast<int>(s < 1 ? 1 : (s > GT_MAX_SPLITS ? GT_MAX_SPLITS : s));
+}
+
+template <int DT>
+cudaError_t launch_typed(const void *x, const void *wg, const float *bias, int64_t T, int64_t d_h,
+                         int64_t E, int64_t k, float *logits, float *part, float *wnorm, float *xss,
+                         int32_t *topk_idx, float *topk_w, int32_t *err, cudaStream_t stream) {
+    const int nk = static_cast<int>(d_h / GT_BK);
+    int S = splits_for(T, E);
+    if (S > nk) S = nk;
+    const int ks = (nk + S - 1) / S;
+    S = (nk + ks - 1) / ks;  // every split non-empty
+    CUtensorMap tm_x, tm_w;
+    const int cu_dt = DT == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint64_t dx[2] = {static_cast<uint64_t>(d_h), static_cast<uint64_t>(T)};
+    const uint64_t dw[2] = {static_cast<uint64_t>(d_h), static_cast<uint64_t>(E)};
+    const uint64_t st[1] = {static_cast<uint64_t>(d_h) * 2};
+    const uint32_t bx[2] = {GT_BK, GT_BM}, bw[2] = {GT_BK, GT_BN};
+    if (!encode_tma_map(&tm_x, cu_dt, 2, x, dx, st, bx, 1) || !encode_tma_map(&tm_w, cu_dt, 2, wg, dw, st, bw, 1))
+        return cudaErrorInvalidValue;
+    GateTcParams p;
+    p.part = part;
+    p.wnorm = wnorm;
+    p.xss = xss;
+    p.wg = static_cast<const uint8_t *>(wg);
+    p.T = static_cast<int>(T);
+    p.E = static_cast<int>(E);
+    p.d_h = static_cast<int>(d_h);
+    p.nk = nk;
+    p.ks = ks;
+    p.err = err;
+
+    static std::atomic<bool> attr_done[64];  // zero-initialised; several host threads may launch
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const size_t sel_smem = select_smem_bytes(d_h, E);
+    const int slots = static_cast<int>((E + 31) / 32);
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gate_tc_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, GT_SMEM);
+        if (e != cudaSuccess) return e;
+#define MOE_SEL_ATTR(SL)                                                                                 \
+        e = cudaFuncSetAttribute(gate_select_kernel<DT, SL>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                 kGateTcMaxSelectSmem);                                                  \
+        if (e != cudaSuccess) return e;
+        MOE_SEL_ATTR(2)
+        MOE_SEL_ATTR(4)
+        MOE_SEL_ATTR(8)
+        MOE_SEL_ATTR(16)
+        MOE_SEL_ATTR(32)
+#undef MOE_SEL_ATTR
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    const dim3 grid(static_cast<unsigned>((T + GT_BM - 1) / GT_BM), static_cast<unsigned>((E + GT_BN - 1) / GT_BN),
+                    static_cast<unsigned>(S));
+    cudaError_t e = launch_pdl(gate_tc_kernel<DT>, grid, dim3(GT_THREADS), GT_SMEM, stream, tm_x, tm_w, p);
+    if (e != cudaSuccess) return e;
+
+    // |logit~ - logit| <= coef * (|x| |w| + |bias|) + 2^-22 |logit~|
+    const double u = std::ldexp(1.0, -24);
+    const double groups = 4.0 * ks;                           // K=16 MMA steps per split
+    const double c_tc = 18.0 * groups * 2.0 * u;              // tensor-core splits
+    const double c_fixed = (static_cast<double>(d_h) / 32.0 + 6.0) * u;  // fixed-order sum
+    const double c_sum = (S + 2.0) * u;                       // partials and bias
+    const double norms = (1.0 + std::ldexp(1.0, -9)) * (1.0 + std::ldexp(1.0, -9));  // fp32 norms
+    const float coef = static_cast<float>(2.0 * (c_tc + c_fixed + c_sum) * norms);
+    const unsigned sel_grid = static_cast<unsigned>(T);
+#define MOE_SEL_CASE(SL)                                                                                     \
+    if (slots <= SL)                                                                                         \
+        return launch_pdl(gate_select_kernel<DT, SL>, dim3(sel_grid), dim3(SEL_WARPS * 32), sel_smem, stream, \
+                          static_cast<const uint8_t *>(x), static_cast<const uint8_t *>(wg), bias,           \
+                          static_cast<const float *>(part), static_cast<const float *>(wnorm),               \
+                          static_cast<const float *>(xss), static_cast<int>(T), static_cast<int>(E),         \
+                          static_cast<int>(d_h), S,                                                          \
+                          static_cast<int>(k), coef, logits, topk_idx, topk_w);
+    MOE_SEL_CASE(2)
+    MOE_SEL_CASE(4)
+    MOE_SEL_CASE(8)
+    MOE_SEL_CASE(16)
+    MOE_SEL_CASE(32)
+#undef MOE_SEL_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool gate_tc_applies(int64_t T, int64_t d_h, int64_t E) {
+    return T >= kGateTcMinTokens && d_h % GT_BK == 0 && E <= 1024 &&
+           select_smem_bytes(d_h, E) <= static_cast<size_t>(kGateTcMaxSelectSmem);
+}
+
+size_t gate_tc_scratch_bytes(int64_t T, int64_t E) {
+    if (T < kGateTcMinTokens) return 0;
+    const size_t part = static_cast<size_t>(splits_for(T, E)) * T * E * 4;
+    return (part + 255) / 256 * 256 + (static_cast<size_t>(E) * 4 + 255) / 256 * 256 +
+           (static_cast<size_t>(splits_for(T, E)) * T * 4 + 255) / 256 * 256;
+}
+
+cudaError_t launch_gate_tc(const void *x, const void *wg, const float *bias, int64_t T, int64_t d_h,
+                           int64_t E, int64_t k, int dtype, float *logits, void *scratch,
+                           int32_t *topk_idx, float *topk_w, int32_t *err, cudaStream_t stream) {
+    float *part = static_cast<float *>(scratch);
+    const size_t part_bytes = static_cast<size_t>(splits_for(T, E)) * T * E * 4;
+    float *wnorm = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) + (part_bytes + 255) / 256 * 256);
+    float *xss = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(wnorm) +
+                                           (static_cast<size_t>(E) * 4 + 255) / 256 * 256);
+    if (dtype == kBF16)
+        return launch_typed<kBF16>(x, wg, bias, T, d_h, E, k, logits, part, wnorm, xss, topk_idx, topk_w, err,
+                                   stream);
+    return launch_typed<kF16>(x, wg, bias, T, d_h, E, k, logits, part, wnorm, xss, topk_idx, topk_w, err,
+                              stream);
+}
+
+}  // namespace moe

@@ -42,36 +42,6 @@ __host__ __device__ constexpr int gate_stages(int rows, bool many_tokens) {
     return many_tokens ? 4 : ((200 * 1024) / (rows * ROW_BYTES) > 8 ? 8 : (200 * 1024) / (rows * ROW_BYTES));
 }
 
-// c + a*b for one 16-bit element of each packed pair (lo or hi half), the
-// fp32 accumulator updated by the mixed-precision FMA (16-bit sources, fp32
-// addend and result, one rounding).  A product of two fp16 or two bf16 values
-// is exact in fp32, so this is bit for bit fmaf(float(a), float(b), c) with
-// no separate conversion instructions.
-template <int DT, bool HI>
-__device__ __forceinline__ float fma_mixed(uint32_t a, uint32_t b, float c) {
-    float d;
-    if constexpr (DT == kBF16) {
-        if constexpr (HI)
-            asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-                "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}"
-                : "=f"(d) : "r"(a), "r"(b), "f"(c));
-        else
-            asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-                "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}"
-                : "=f"(d) : "r"(a), "r"(b), "f"(c));
-    } else {
-        if constexpr (HI)
-            asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-                "fma.rn.f32.f16 %0, ah, bh, %3;\n\t}"
-                : "=f"(d) : "r"(a), "r"(b), "f"(c));
-        else
-            asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-                "fma.rn.f32.f16 %0, al, bl, %3;\n\t}"
-                : "=f"(d) : "r"(a), "r"(b), "f"(c));
-    }
-    return d;
-}
-
 // Top-k by (logit desc, id asc) and the softmax weights of TOK tokens whose
 // 64 logits per token (E <= 64 valid) sit in shared memory, lsm[TOK][64],
 // with every thread of the CTA taking part (the single-token latency case).
@@ -428,8 +398,14 @@ cudaError_t launch_gate_typed(const void *x, const void *wg, const float *bias, 
 
 cudaError_t launch_gate_topk(const void *x, const void *wg, const float *bias, int64_t T,
                              int64_t d_h, int64_t E, int64_t k, int dtype, float *logits,
-                             int32_t *topk_idx, float *topk_w, cudaStream_t stream) {
+                             int32_t *topk_idx, float *topk_w, void *tc_scratch, int32_t *err,
+                             cudaStream_t stream) {
     if (T <= 0) return cudaSuccess;
+    // many tokens: logits on the tensor cores, the routing made exact by the
+    // fixed-order recompute of every candidate (gate_tc.cu)
+    if (tc_scratch != nullptr && gate_tc_applies(T, d_h, E))
+        return launch_gate_tc(x, wg, bias, T, d_h, E, k, dtype, logits, tc_scratch, topk_idx, topk_w, err,
+                              stream);
     if (dtype == kBF16)
         return launch_gate_typed<kBF16>(x, wg, bias, T, d_h, E, k, logits, topk_idx, topk_w, stream);
     return launch_gate_typed<kF16>(x, wg, bias, T, d_h, E, k, logits, topk_idx, topk_w, stream);

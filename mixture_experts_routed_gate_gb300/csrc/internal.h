@@ -25,10 +25,27 @@ bool encode_tma_2d_plain(CUtensorMap *m, const void *ptr, uint64_t inner, uint64
 bool encode_tma_map(CUtensorMap *m, int data_type, int rank, const void *ptr, const uint64_t *dims,
                     const uint64_t *strides_bytes, const uint32_t *box, int swizzle_128b);
 
-// gate_topk.cu: logits (written to `logits`, [T, E] fp32), top-k ids and weights
+// gate_topk.cu: logits (written to `logits`, [T, E] fp32), top-k ids and
+// weights.  tc_scratch (gate_tc_scratch_bytes(T, E) bytes, or null) lets
+// many-token calls run the tensor-core path of gate_tc.cu; err (nullable)
+// receives a timed-out wait of that path.
 cudaError_t launch_gate_topk(const void *x, const void *wg, const float *bias, int64_t T,
                              int64_t d_h, int64_t E, int64_t k, int dtype, float *logits,
-                             int32_t *topk_idx, float *topk_w, cudaStream_t stream);
+                             int32_t *topk_idx, float *topk_w, void *tc_scratch, int32_t *err,
+                             cudaStream_t stream);
+
+// gate_tc.cu: the tensor-core gate (tokens at least kGateTcMinTokens): its
+// scratch (split-K partial logits and the gate rows' norms), whether it
+// applies to a shape, and the launch (logits as launch_gate_topk writes them:
+// the fixed-order value for every expert that could be selected, the
+// tensor-core value for the others).
+constexpr int64_t kGateTcMinTokens = 1024;
+constexpr int kGateTcMaxSelectSmem = 200 * 1024;
+size_t gate_tc_scratch_bytes(int64_t T, int64_t E);
+bool gate_tc_applies(int64_t T, int64_t d_h, int64_t E);
+cudaError_t launch_gate_tc(const void *x, const void *wg, const float *bias, int64_t T, int64_t d_h,
+                           int64_t E, int64_t k, int dtype, float *logits, void *scratch,
+                           int32_t *topk_idx, float *topk_w, int32_t *err, cudaStream_t stream);
 
 // capi.cu: the host-side argument checks shared by both dispatch entry
 // points (a moe_status_t value; MOE_OK when the call may go ahead).

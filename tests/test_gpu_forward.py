@@ -11,7 +11,8 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import MOE_TOL, assert_bits_equal, assert_close, bits, require_cuda
+from gpu_helpers import (MOE_TOL, assert_bits_equal, assert_close, bits, check_gate_logits,
+                         gate_uses_tensor_cores, require_cuda)
 from mixture_experts_routed_gate_gb300 import binding, workloads
 
 pytestmark = pytest.mark.gpu
@@ -197,11 +198,13 @@ def test_forward_prefill_full_size(oracle):
     d = workloads.make_moe_inputs(cfg, device=dev)
     out, views = _run_forward(d, cfg)
     k = cfg.top_k
-    # routing: all tokens, bit for bit (logits too)
+    # routing: all tokens, bit for bit (the logits as check_gate_logits says)
     ref_logits = oracle.gate_logits(bits(d["x"]), bits(d["wg"]), d["bias"].cpu().numpy(), cfg.dtype)
-    assert_bits_equal(views["logits"].cpu().numpy().view(np.uint32), ref_logits.view(np.uint32), "logits")
     ref_idx, ref_w = oracle.topk_softmax(ref_logits, k)
     assert_bits_equal(views["topk_idx"].cpu().numpy(), ref_idx, "topk_idx")
+    check_gate_logits(views["logits"].cpu().numpy(), ref_logits, ref_idx, bits(d["x"]), bits(d["wg"]),
+                      d["bias"].cpu().numpy(), cfg.dtype,
+                      gate_uses_tensor_cores(cfg.T, cfg.d_hidden, cfg.n_experts))
     assert np.allclose(views["topk_w"].cpu().numpy(), ref_w, rtol=1e-5, atol=1e-7)
     tab = oracle.build_dispatch(ref_idx, ref_w, cfg.n_experts, 128)
     for n in TABLES:

@@ -67,7 +67,8 @@ def _dispatch_out(G, T, k, E):
 @pytest.mark.parametrize("T,d_h,E,k,dtype", [(601, 512, 100, 4, "f16"),   # 16 x 16 CTAs, ragged
                                              (37, 512, 40, 3, "bf16"),    # top-k fused, E <= 64
                                              (5, 256, 72, 8, "f16"),      # one-warp CTAs
-                                             (700, 768, 64, 6, "bf16")])  # 4 tokens per fused CTA
+                                             (700, 768, 64, 6, "bf16"),   # 4 tokens per fused CTA
+                                             (1100, 512, 100, 4, "f16")])  # tensor-core gate, ragged
 def test_routing_dispatch_gather_stay_inside(T, d_h, E, k, dtype):
     dev = require_cuda()
     G = Guards(dev)
@@ -77,7 +78,7 @@ def test_routing_dispatch_gather_stay_inside(T, d_h, E, k, dtype):
     wg = (torch.randn((E, d_h), generator=g, device=dev) / d_h ** 0.5).to(td)
     idx = G.empty((T, k), torch.int32, "topk_idx")
     w = G.empty((T, k), torch.float32, "topk_w")
-    ws = G.empty((T * E * 4,), torch.uint8, "gate workspace")
+    ws = G.empty((int(binding.lib().moe_gate_topk_workspace_bytes(T, E)),), torch.uint8, "gate workspace")
     binding.moe_gate_topk(x, wg, None, k, topk_idx=idx, topk_w=w, ws=ws)
     need = int(binding.lib().moe_build_dispatch_workspace_bytes(T, k, E))
     dws = G.empty((max(need, 16),), torch.uint8, "dispatch workspace")

@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import assert_bits_equal, bits, require_cuda
+from gpu_helpers import assert_bits_equal, bits, check_gate_logits, gate_uses_tensor_cores, require_cuda
 from mixture_experts_routed_gate_gb300 import binding, workloads
 
 pytestmark = pytest.mark.gpu
@@ -19,20 +19,25 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 def _gate_gpu(x, wg, bias, k):
     T, E = x.shape[0], wg.shape[0]
-    ws = torch.empty(T * E * 4, dtype=torch.uint8, device=x.device)
+    need = int(binding.lib().moe_gate_topk_workspace_bytes(T, E))
+    ws = torch.empty(need, dtype=torch.uint8, device=x.device)
     idx, w = binding.moe_gate_topk(x, wg, bias, k, ws=ws)
     torch.cuda.synchronize()
-    logits = ws.view(torch.float32).view(T, E)
+    logits = ws[:T * E * 4].view(torch.float32).view(T, E)
     return idx.cpu().numpy(), w.cpu().numpy(), logits.cpu().numpy()
 
 
 def _check_gate(oracle, x, wg, bias, k, dtype):
+    """Ids bit for bit, weights within rtol 1e-5, logits as check_gate_logits
+    says (bit for bit, or on the tensor-core path within its bound)."""
     idx, w, logits = _gate_gpu(x, wg, bias, k)
-    ref_logits = oracle.gate_logits(bits(x), bits(wg), None if bias is None else bias.cpu().numpy(), dtype)
+    b = None if bias is None else bias.cpu().numpy()
+    ref_logits = oracle.gate_logits(bits(x), bits(wg), b, dtype)
     ref_idx, ref_w = oracle.topk_softmax(ref_logits, k)
-    assert_bits_equal(logits.view(np.uint32), ref_logits.view(np.uint32), "gate logits")
     assert_bits_equal(idx, ref_idx, "topk_idx")
     assert np.allclose(w, ref_w, rtol=1e-5, atol=1e-7), float(np.abs(w - ref_w).max())
+    check_gate_logits(logits, ref_logits, idx, bits(x), bits(wg), b, dtype,
+                      gate_uses_tensor_cores(x.shape[0], x.shape[1], wg.shape[0]))
     return idx, w
 
 
@@ -56,6 +61,60 @@ def test_gate_topk_ragged_shapes(oracle, T, d_h, E, k, dtype):
     wg = (torch.randn((E, d_h), generator=g, device=dev) / d_h ** 0.5).to(workloads.torch_dtype(dtype))
     bias = torch.randn(E, generator=g, device=dev) * 0.1
     _check_gate(oracle, x, wg, bias, k, dtype)
+
+
+@pytest.mark.parametrize("T,d_h,E,k,dtype", [(1024, 7168, 256, 8, "bf16"),  # prefill width, one N tile
+                                             (1100, 512, 100, 4, "f16"),    # ragged tokens and experts
+                                             (1031, 768, 72, 8, "bf16"),
+                                             (2048, 2048, 64, 6, "f16"),
+                                             (1024, 256, 1000, 32, "f16"),  # four N tiles, k = 32
+                                             (1200, 256, 8, 2, "bf16")])    # N tile mostly past E
+def test_gate_tensor_core_path_shapes(oracle, T, d_h, E, k, dtype):
+    """Many tokens: logits on the tensor cores, every expert that could be
+    selected recomputed in the fixed order.  Ids bit for bit, weights within
+    rtol 1e-5, selected logits bit for bit, the rest within the bound."""
+    assert gate_uses_tensor_cores(T, d_h, E)
+    dev = require_cuda()
+    g = torch.Generator(device=dev).manual_seed(T + 3 * E)
+    x = torch.randn((T, d_h), generator=g, device=dev).to(workloads.torch_dtype(dtype))
+    wg = (torch.randn((E, d_h), generator=g, device=dev) / d_h ** 0.5).to(workloads.torch_dtype(dtype))
+    rank = torch.randperm(E, generator=g, device=dev).to(torch.float64) + 1.0
+    bias = (-1.1 * torch.log(rank)).to(torch.float32)
+    _check_gate(oracle, x, wg, bias, k, dtype)
+
+
+def test_gate_tensor_core_path_ties_and_near_ties(oracle):
+    """Many tokens on the tensor-core path: (a) experts 3, 4, 5 share one row
+    and a dominant bias, so their logits tie exactly and the order must be
+    3, 4, 5 with equal weights; (b) expert 2j + 1 equals expert 2j but for one
+    element one bf16 step away, so pairs of logits nearly tie and only the
+    fixed-order recompute separates them; (c) zero tokens: every logit equals
+    its bias, all experts tie, the first k ids win with weight 1/E."""
+    dev = require_cuda()
+    T, d_h, E = 1024, 1024, 64
+    g = torch.Generator(device=dev).manual_seed(5)
+    x = torch.randn((T, d_h), generator=g, device=dev).to(torch.bfloat16)
+    wg = (torch.randn((E, d_h), generator=g, device=dev) * 0.05).to(torch.bfloat16)
+    wg[4] = wg[3]
+    wg[5] = wg[3]
+    bias = torch.zeros(E, device=dev)
+    bias[3:6] = 100.0
+    idx, w = _check_gate(oracle, x, wg.contiguous(), bias, 3, "bf16")
+    assert (idx == np.array([3, 4, 5])).all()
+    assert (w[:, 0] == w[:, 1]).all() and (w[:, 1] == w[:, 2]).all()
+
+    wn = wg.clone()
+    wn[1::2] = wn[0::2]
+    j = torch.randint(0, d_h, (E // 2,), generator=g, device=dev)
+    bumped = wn[1::2].view(torch.int16)
+    rows = torch.arange(E // 2, device=dev)
+    bumped[rows, j] = bumped[rows, j] + 1  # one step of the bf16 encoding
+    _check_gate(oracle, x, wn.contiguous(), None, 8, "bf16")
+
+    x0 = torch.zeros((T, d_h), dtype=torch.bfloat16, device=dev)
+    idx, w = _check_gate(oracle, x0, wg.contiguous(), None, 6, "bf16")
+    assert (idx == np.arange(6)).all()
+    assert np.allclose(w, 1.0 / E, rtol=1e-6)
 
 
 def test_gate_hand_computed_order_cases():
