@@ -34,6 +34,13 @@ int mlp_grid(int64_t tiles) {
     return static_cast<int>(tiles < grid ? tiles : grid);
 }
 
+bool mlp_pairs_enabled() {
+    // MOE_MLP_PAIRS=0 keeps the expert MLP on the one-SM kernel (tests compare
+    // the two forms); read at every launch
+    const char *v = std::getenv("MOE_MLP_PAIRS");
+    return !(v && v[0] == '0');
+}
+
 }  // namespace moe
 
 namespace {
@@ -330,6 +337,12 @@ static moe_status_t grouped_mlp(const void *a, const void *w_gate, const void *w
         cudaError_t e = cudaMemsetAsync(ready, 0, static_cast<size_t>(m_blocks + 1) * 4, s);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
+    // many rows, pre-gathered, no row weight: both stages on pairs of SMs
+    if (!gather_idx && !row_weights && moe::mlp_pairs_enabled() &&
+        moe::grouped_mlp2_applies(n_rows, d_h, d_e, E))
+        return cuda_status(moe::launch_grouped_mlp2(dtype, a, w_gate, w_up, w_down, group_sizes,
+                                                    group_offsets, group_padded_offsets, m_blocks, n_rows,
+                                                    d_h, d_e, E, h, y, ready, err_flag, s));
     return cuda_status(moe::launch_grouped_mlp(dtype, a, w_gate, w_up, w_down, group_sizes,
                                                group_offsets, group_padded_offsets, group_idx_for_bx,
                                                m_blocks, row_weights, n_rows, d_h, d_e, E, h, y,

@@ -98,6 +98,19 @@ cudaError_t launch_grouped_mlp(int dtype, const void *a, const void *w_gate, con
                                cudaStream_t stream, const void *x = nullptr,
                                const int32_t *gather_idx = nullptr, int64_t T = 0);
 
+// grouped_mlp2.cu: both stages on CTA pairs (tcgen05 cta_group::2) from
+// pre-gathered rows, no row weight; `ready` as launch_grouped_mlp.  Applies
+// when d_e % 256 == 0, d_h % 512 == 0 and the work units fit the in-kernel
+// schedule (n_rows / 256 + E <= 512).
+bool grouped_mlp2_applies(int64_t n_rows, int64_t d_h, int64_t d_e, int64_t E);
+cudaError_t launch_grouped_mlp2(int dtype, const void *a, const void *w_gate, const void *w_up,
+                                const void *w_down, const int32_t *sizes, const int32_t *offsets,
+                                const int32_t *padded, int64_t m_blocks, int64_t n_rows, int64_t d_h,
+                                int64_t d_e, int64_t E, void *h, void *y, int32_t *ready, int32_t *err,
+                                cudaStream_t stream);
+// capi.cu: false when MOE_MLP_PAIRS=0 (tests compare the one-SM form)
+bool mlp_pairs_enabled();
+
 // grouped_gemm_w4.cu: int4 weights [E, N, K], two per byte as the pages pack
 // them, into the tiled layout the int4 kernels read (tiles of R output
 // channels; R = 128 for W_gate / W_up, 256 for W_down); bytes of that layout

@@ -297,3 +297,48 @@ def test_expert_mlp_progress_does_not_need_a_resident_grid(oracle, monkeypatch, 
         ref = oracle.moe_forward(nb["x"], nb["wg"], nb["bias"], nb["w_gate"], nb["w_up"], nb["w_down"],
                                  cfg.top_k, cfg.dtype)
         assert_close(got, ref["out"], cfg.dtype, *MOE_TOL[cfg.dtype], "decode out")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("d_h,d_e", [(512, 256), (1024, 512)])
+def test_expert_mlp_on_sm_pairs_matches_one_sm_form_and_oracle(oracle, monkeypatch, dtype, d_h, d_e):
+    """The many-row expert MLP runs on pairs of SMs (tcgen05 cta_group::2):
+    experts with more than 64 rows in 256-row units (one or two per pair of
+    M blocks, the last one ragged), smaller experts swapped (their rows the
+    MMA's N, split between the two SMs).  Expert sizes chosen to hit every
+    boundary: 1, 15, 16, 17, 63, 64 rows (swapped), 65, 128, 255, 256, 257,
+    511, 512, 700 rows (units of 256), an empty expert.  The pair launch gives
+    the bits of the one-SM launch, and h and y agree with the oracle."""
+    dev = require_cuda()
+    sizes = [1, 15, 0, 16, 17, 63, 64, 65, 128, 255, 256, 257, 511, 512, 700]
+    E = len(sizes)
+    idx = np.repeat(np.arange(E, dtype=np.int32), sizes)
+    rng = np.random.default_rng(d_h + d_e)
+    idx = idx[rng.permutation(idx.size)].reshape(-1, 1)  # one slot per token, tokens shuffled
+    T = idx.shape[0]
+    td = workloads.torch_dtype(dtype)
+    g = torch.Generator().manual_seed(d_e)
+    x = torch.randn((T, d_h), generator=g).to(td)
+    wg = (torch.randn((E, d_e, d_h), generator=g) / d_h ** 0.5).to(td).to(dev)
+    wu = (torch.randn((E, d_e, d_h), generator=g) / d_h ** 0.5).to(td).to(dev)
+    wd = (torch.randn((E, d_h, d_e), generator=g) / d_e ** 0.5).to(td).to(dev)
+    tab = oracle.build_dispatch(idx, None, E, 128)
+    assert list(tab["group_sizes"]) == sizes
+    a = oracle.gather_rows(bits(x), tab["sorted_token_idx"], dtype)
+    tabd = _tables_to(dev, tab)
+    a_d = _from_bits(a, dtype, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    monkeypatch.setenv("MOE_MLP_PAIRS", "0")
+    h1, y1 = binding.moe_grouped_mlp(a_d, wg, wu, wd, tabd, err=err)
+    torch.cuda.synchronize()
+    monkeypatch.delenv("MOE_MLP_PAIRS")
+    h2, y2 = binding.moe_grouped_mlp(a_d, wg, wu, wd, tabd, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_bits_equal(bits(h2), bits(h1), "pair h vs one-SM h")
+    assert_bits_equal(bits(y2), bits(y1), "pair y vs one-SM y")
+    h_ref = oracle.grouped_gate_up_silu(a, bits(wg.cpu()), bits(wu.cpu()), tab, dtype)
+    y_ref = oracle.grouped_down(h_ref, bits(wd.cpu()), tab, dtype)
+    rtol, atol = MOE_TOL[dtype]
+    assert_close(bits(h2), h_ref, dtype, rtol, atol, "pair h vs oracle")
+    assert_close(bits(y2), y_ref, dtype, rtol, atol, "pair y vs oracle")
