@@ -38,13 +38,19 @@
 // stage-1 epilogue warp of its unit has stored its h (per-unit counters), and
 // since tiles are taken in order, those stage-1 tiles belong to running pairs.
 //
-// Roles per CTA (192 threads): warp 0 TMA producer (both CTAs load their own
-// halves; the copies complete on the even CTA's ring barrier), warp 1 MMA
-// issuer (even CTA only: one thread issues the pair's MMAs and commits them
-// to both CTAs' barriers), warps 2-5 epilogue (each CTA drains its own tensor
-// memory: SiLU(gate) * up or the down output, rounded to the dtype, stores of
-// valid rows only).  Every wait is bounded (2 s): on expiry the kernel records
-// a timeout, winds down and returns.
+// Roles per CTA (224 threads): warp 0 TMA producer (both CTAs load their own
+// halves; the copies complete on the even CTA's ring barrier), warps 1 and 6
+// MMA issuers (even CTA only: one thread each; they commit to both CTAs'
+// barriers), warps 2-5 epilogue (each CTA drains its own tensor memory:
+// SiLU(gate) * up or the down output, rounded to the dtype, stores of valid
+// rows only).  One thread issues a small-N MMA about every 85 cycles, and a
+// swapped tile needs one MMA per 4 KB of weights per SM, so a swapped tile's
+// two accumulators (gate and up, or the two W_down halves) are issued by two
+// threads in parallel, each in the same K order as one thread would (the
+// results do not change); a big tile's MMAs (N = 256, bound by the tensor
+// pipe) all come from warp 1, warp 6 only keeping step.  Every wait is
+// bounded (2 s): on expiry the kernel records a timeout, winds down and
+// returns.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -60,7 +66,8 @@ constexpr int P_R1 = 128 * P_BK * 2;        // 16 KB: weights
 constexpr int P_RT = 32;                    // token rows of a small tile per CTA
 constexpr int P_R2 = P_RT * P_BK * 2;       // 4 KB: rows (small)
 constexpr int P_STAGE = P_R0 + P_R1 + P_R2;  // 36 KB
-constexpr int P_THREADS = 192;
+constexpr int P_THREADS = 224;               // 7 warps (see the roles below)
+constexpr int P_MMA2_WARP = 6;              // the second MMA issuer
 constexpr int P_EPI = 4;
 constexpr int P_TRING = 4;
 constexpr int P_NEXT_FETCH = 2;
@@ -212,16 +219,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < P_ST; ++s) {
             mbar_init(full_bar(s), 1);   // even CTA: its expect_tx arrival (+ both CTAs' bytes)
-            mbar_init(empty_bar(s), 1);  // the pair's MMA commit
+            mbar_init(empty_bar(s), 2);  // the commits of the pair's two MMA threads
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(tfull_bar(a), 1);            // the pair's MMA commit
+            mbar_init(tfull_bar(a), 2);            // the commits of the two MMA threads
             mbar_init(tempty_bar(a), 2 * P_EPI);   // even CTA: every epilogue warp of both CTAs
         }
         for (int i = 0; i < P_TRING; ++i) {
             mbar_init(tidf_bar(i), 1);  // the even CTA's producer
-            // even CTA: its MMA thread and epilogue warps, the odd CTA's producer and epilogue warps
-            mbar_init(tide_bar(i), 2 + 2 * P_EPI);
+            // even CTA: its two MMA threads and epilogue warps, the odd CTA's
+            // producer and epilogue warps
+            mbar_init(tide_bar(i), 3 + 2 * P_EPI);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -417,8 +425,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 p_drain(full_bar(static_cast<int>(i % P_ST)), static_cast<uint32_t>((i / P_ST) & 1));
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------- MMA issuer --------------------------------
+    } else if (warp == 1 || warp == P_MMA2_WARP) {
+        // ------------------------------- MMA issuers --------------------------------
+        // thread A (warp 1): every MMA of a big tile, the first accumulator of a
+        // swapped tile; thread B (warp 6): the second accumulator of a swapped
+        // tile.  Both wait for each stage and commit it, so every barrier phase
+        // sees one commit from each.
+        const bool mma_b = warp == P_MMA2_WARP;
         if (leader && lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
@@ -462,18 +475,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                     const uint64_t d0 = smem_desc_sw128(r0), d1 = smem_desc_sw128(r0 + P_R0),
                                    d2 = smem_desc_sw128(r0 + P_R0 + P_R1);
                     if (t.big) {
+                        if (!mma_b) {
+#pragma unroll
+                            for (int k = 0; k < P_BK / 16; ++k)
+                                tc_mma2_f16(d_tmem, d0 + 2u * k, d1 + 2u * k, IDESC_BIG, (kb | k) != 0 ? 1u : 0u);
+                        }
+                    } else {
+                        // D[feature][row]: the R0 weights into columns [0, np) (thread A),
+                        // R1 into [np, 2 np) (thread B)
+                        const uint32_t d_acc = mma_b ? d_tmem + static_cast<uint32_t>(np) : d_tmem;
+                        const uint64_t da = mma_b ? d1 : d0;
 #pragma unroll
                         for (int k = 0; k < P_BK / 16; ++k)
-                            tc_mma2_f16(d_tmem, d0 + 2u * k, d1 + 2u * k, IDESC_BIG, (kb | k) != 0 ? 1u : 0u);
-                    } else {
-                        // D[feature][row]: the R0 weights into columns [0, np), R1 into [np, 2 np)
-#pragma unroll
-                        for (int k = 0; k < P_BK / 16; ++k) {
-                            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-                            tc_mma2_f16(d_tmem, d0 + 2u * k, d2 + 2u * k, idesc_sw, accum);
-                            tc_mma2_f16(d_tmem + static_cast<uint32_t>(np), d1 + 2u * k, d2 + 2u * k, idesc_sw,
-                                        accum);
-                        }
+                            tc_mma2_f16(d_acc, da + 2u * k, d2 + 2u * k, idesc_sw, (kb | k) != 0 ? 1u : 0u);
                     }
                     tc_commit2_both(empty_bar(stage));  // frees the stage in both CTAs
                     last_bar = empty_bar(stage);
