@@ -8,7 +8,7 @@
 // with the block -> (expert g, first row m_start, valid rows) lookup of the
 // pages' dispatch contract.
 //
-// Design (one persistent CTA per SM, 192 threads):
+// Design (one persistent CTA per SM, 224 threads):
 //   warp 0      TMA producer: per 64-wide K step loads the 128-row A tile and the
 //               256-row B tile (stage 1: 128 W_gate rows + 128 W_up rows of the
 //               same output columns; stage 2: 256 W_down rows) into a 4-deep
@@ -19,6 +19,8 @@
 //               with at most 64 valid rows are computed swapped: two M=128
 //               MMAs with the weight halves as A and the block's rows as B
 //               (N = rows rounded up to 16), a fraction of the tensor work.
+//   warp 6      second MMA issuer: a swapped tile's second MMA of each pair
+//               (one thread issues a small-N MMA only about every 85 cycles).
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (thread = row), stage 1
 //               fuses silu(gate)*up, stage 2 the optional row weight; round to
 //               the activation dtype and store only the block's valid rows.
@@ -55,7 +57,8 @@ constexpr int BM = 128;
 constexpr int BK = 64;  // 64 x 2 B = 128 B: one swizzle span per row
 constexpr int UMMA_K = 16;
 constexpr int STAGES = 4;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 224;  // 7 warps: producer, MMA, 4 epilogue, second MMA issuer
+constexpr int MMA2_WARP = 6;
 constexpr int MMA_N = 256;
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
@@ -322,15 +325,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), 2);  // the commits of the two MMA threads
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(tfull_bar(a), 1);
+            mbar_init(tfull_bar(a), 2);  // the commits of the two MMA threads
             mbar_init(tempty_bar(a), 4);  // one arrival per epilogue warp
         }
         for (int i = 0; i < TRING; ++i) {
             mbar_init(tidf_bar(i), 1);
-            mbar_init(tide_bar(i), 1 + EPI_WARPS);  // the MMA warp and every epilogue warp
+            mbar_init(tide_bar(i), 2 + EPI_WARPS);  // both MMA threads and every epilogue warp
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -575,8 +578,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_wait_drain(full_bar(static_cast<int>(i % NST)), static_cast<uint32_t>((i / NST) & 1));
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------- MMA issuer --------------------------------
+    } else if (warp == 1 || warp == MMA2_WARP) {
+        // ------------------------------- MMA issuers --------------------------------
+        // One thread issues a small-N MMA about every 85 cycles, so a swapped
+        // tile's two accumulators are issued by two threads: warp 1 the first
+        // (and every MMA of an unswapped tile), warp 6 the second, each in the
+        // K order one thread would use (the results do not change).  Both wait
+        // for every stage and commit it.
+        const bool mma_b = warp == MMA2_WARP;
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
@@ -626,17 +635,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint64_t a_desc = smem_desc_sw128(smem_u32(sA + stage * A_SLOT));
                     const uint64_t b_desc = smem_desc_sw128(smem_u32(sB + stage * B_BYTES));
                     if (swap) {
-                        // D[feature][row]: first 128 weight rows into columns [0, np),
-                        // the other 128 into [np, 2np)
-                        const uint64_t b2_desc = smem_desc_sw128(smem_u32(sB + stage * B_BYTES + B_BYTES / 2));
+                        // D[feature][row]: first 128 weight rows into columns [0, np)
+                        // (warp 1), the other 128 into [np, 2np) (warp 6)
+                        const uint64_t wb_desc =
+                            mma_b ? smem_desc_sw128(smem_u32(sB + stage * B_BYTES + B_BYTES / 2)) : b_desc;
+                        const uint32_t d_acc = mma_b ? d_tmem + static_cast<uint32_t>(np) : d_tmem;
 #pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k) {
-                            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-                            tc_mma_f16(d_tmem, b_desc + 2u * k, a_desc + 2u * k, idesc_sw, accum);
-                            tc_mma_f16(d_tmem + static_cast<uint32_t>(np), b2_desc + 2u * k,
-                                       a_desc + 2u * k, idesc_sw, accum);
-                        }
-                    } else {
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            tc_mma_f16(d_acc, wb_desc + 2u * k, a_desc + 2u * k, idesc_sw, (kb | k) != 0 ? 1u : 0u);
+                    } else if (!mma_b) {
 #pragma unroll
                         for (int k = 0; k < BK / UMMA_K; ++k) {
                             // +32 bytes per K=16 step inside the 128-byte swizzled row
