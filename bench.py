@@ -63,25 +63,42 @@ def kernels_per_step(cfg) -> int:
 
 
 # DRAM bytes (read + write) of one expert-MLP launch from one ncu capture
-# (1-pass dram__bytes_read.sum + dram__bytes_write.sum on GB300), valid for the
-# kernel source whose hash is given; any later change to that source reports
-# null.
-MLP_TRAFFIC = {"source_sha256_16": "507b569f1caa12ad",
-               "bytes": {"decode": 604.74e6 + 3.26e6, "prefill": 16.015e9 + 572.22e6}}
-MLP_SOURCES = ["mixture_experts_routed_gate_gb300/csrc/grouped_gemm.cu",
-               "mixture_experts_routed_gate_gb300/csrc/common.cuh"]
+# (1-pass dram__bytes_read.sum + dram__bytes_write.sum on GB300) per
+# workload, valid for the kernel sources whose hash is given; any later change
+# to those sources reports null.
+MLP_TRAFFIC = {
+    "decode": {"sources": ["mixture_experts_routed_gate_gb300/csrc/grouped_gemm.cu",
+                           "mixture_experts_routed_gate_gb300/csrc/common.cuh"],
+               "source_sha256_16": "5d6fd8826b004c65", "bytes": 604787712 + 2955264},
+    "prefill": {"sources": ["mixture_experts_routed_gate_gb300/csrc/grouped_mlp2.cu",
+                            "mixture_experts_routed_gate_gb300/csrc/common.cuh"],
+                "source_sha256_16": "57ababa2a64f2460", "bytes": 15753160704 + 583650816},
+}
+
+
+def sources_hash(files) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def mlp_traffic(workload: str):
-    import hashlib
-    h = hashlib.sha256()
-    root = os.path.dirname(os.path.abspath(__file__))
-    for f in MLP_SOURCES:
-        with open(os.path.join(root, f), "rb") as fh:
-            h.update(fh.read())
-    if h.hexdigest()[:16] != MLP_TRAFFIC["source_sha256_16"]:
+    rec = MLP_TRAFFIC.get(workload)
+    if rec is None or rec["bytes"] is None or sources_hash(rec["sources"]) != rec["source_sha256_16"]:
         return None
-    return MLP_TRAFFIC["bytes"].get(workload)
+    return rec["bytes"]
+
+
+def mlp_kernel_name(cfg) -> str:
+    """The expert-MLP kernel the forward launches for this workload."""
+    if cfg.T <= 64:
+        return "grouped_gemm_kernel<MLP_FEW> (one SM per tile, rows gathered in the kernel)"
+    if cfg.d_expert % 256 == 0 and cfg.d_hidden % 512 == 0 and cfg.T * cfg.top_k // 256 + cfg.n_experts <= 512:
+        return "grouped_mlp2_kernel (SM pairs, tcgen05 cta_group::2)"
+    return "grouped_gemm_kernel<MLP> (one SM per tile)"
 
 
 def forward_stages(T: int) -> list:
@@ -760,7 +777,7 @@ def workload_record(args, cfg, res, world, steps, cpu_budget, dev):
     t_bytes = gu_bytes / (peaks["hbm_gbs"] * 1e9)
     t_flops = gu_flops / (peaks[tflops_key] * 1e12)
     traffic = mlp_traffic(cfg.name)
-    common = {"kernel": "grouped_gemm_kernel<MLP>", "traffic": traffic,
+    common = {"kernel": mlp_kernel_name(cfg), "traffic": traffic,
               "traffic_source": ("dram__bytes_read.sum + dram__bytes_write.sum of one ncu capture of this "
                                  "kernel at this workload, stored with the hash of the kernel source it was "
                                  "taken on; null when the source differs" if traffic is not None else
