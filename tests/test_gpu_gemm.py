@@ -308,7 +308,8 @@ def test_expert_mlp_on_sm_pairs_matches_one_sm_form_and_oracle(oracle, monkeypat
     MMA's N, split between the two SMs).  Expert sizes chosen to hit every
     boundary: 1, 15, 16, 17, 63, 64 rows (swapped), 65, 128, 255, 256, 257,
     511, 512, 700 rows (units of 256), an empty expert.  The pair launch gives
-    the bits of the one-SM launch, and h and y agree with the oracle."""
+    the bits of the one-SM launch (and of its gathering form, rows read from
+    the tokens by index), and h and y agree with the oracle."""
     dev = require_cuda()
     sizes = [1, 15, 0, 16, 17, 63, 64, 65, 128, 255, 256, 257, 511, 512, 700]
     E = len(sizes)
@@ -333,10 +334,15 @@ def test_expert_mlp_on_sm_pairs_matches_one_sm_form_and_oracle(oracle, monkeypat
     torch.cuda.synchronize()
     monkeypatch.delenv("MOE_MLP_PAIRS")
     h2, y2 = binding.moe_grouped_mlp(a_d, wg, wu, wd, tabd, err=err)
+    # the gathering form (rows read from x by index; the one-SM kernel's)
+    h3, y3 = binding.moe_grouped_mlp(None, wg, wu, wd, tabd, err=err, x=x.to(dev),
+                                     sorted_token_idx=tabd["sorted_token_idx"])
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert_bits_equal(bits(h2), bits(h1), "pair h vs one-SM h")
     assert_bits_equal(bits(y2), bits(y1), "pair y vs one-SM y")
+    assert_bits_equal(bits(h3), bits(h1), "gathering-form h vs one-SM h")
+    assert_bits_equal(bits(y3), bits(y1), "gathering-form y vs one-SM y")
     h_ref = oracle.grouped_gate_up_silu(a, bits(wg.cpu()), bits(wu.cpu()), tab, dtype)
     y_ref = oracle.grouped_down(h_ref, bits(wd.cpu()), tab, dtype)
     rtol, atol = MOE_TOL[dtype]

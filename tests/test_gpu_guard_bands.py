@@ -94,7 +94,9 @@ def test_routing_dispatch_gather_stay_inside(T, d_h, E, k, dtype):
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("T,E,k,d_h,d_e", [(150, 3, 2, 256, 192),   # full (non-swapped) tiles, partial N
                                            (61, 5, 3, 512, 128),    # swapped tiles only
-                                           (97, 9, 4, 256, 320)])
+                                           (97, 9, 4, 256, 320),
+                                           (300, 6, 3, 512, 256),   # SM-pair kernel: 256-row units
+                                           (90, 24, 2, 1024, 512)])  # SM-pair kernel: mostly swapped units
 def test_expert_gemms_stay_inside(dtype, T, E, k, d_h, d_e):
     dev = require_cuda()
     cfg = workloads.MoEConfig("guard", 1, T, d_h, d_e, E, k, dtype, 21 + T)
@@ -141,7 +143,8 @@ def test_combine_stays_inside(T, K, H, in_dt, out_dt):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("T,E,k,d_h,d_e", [(150, 3, 2, 256, 192), (61, 5, 3, 512, 128), (65, 8, 2, 256, 128)])
+@pytest.mark.parametrize("T,E,k,d_h,d_e", [(150, 3, 2, 256, 192), (61, 5, 3, 512, 128), (65, 8, 2, 256, 128),
+                                           (1100, 20, 4, 512, 256)])  # tensor-core gate, SM-pair expert MLP
 def test_forward_stays_inside_its_workspace(dtype, T, E, k, d_h, d_e):
     dev = require_cuda()
     cfg = workloads.MoEConfig("guard", 1, T, d_h, d_e, E, k, dtype, 40 + T)
