@@ -19,7 +19,7 @@
 // one AND-OR with the fp16 (or bf16) exponent of 1024 (128) and one packed
 // subtraction of 1032 (136) give two exact values.
 //
-// Kernel (one persistent CTA per SM, 448 threads):
+// Kernel (one persistent CTA per SM, 480 threads):
 //   warp 0      producer: per 128-wide K step (two 64-wide sub-steps), one
 //               stage of a 6-deep ring: the block's rows (stage 1: up to 64
 //               token rows gathered from x by four-row TMA gathers; stage 2:
@@ -28,10 +28,11 @@
 //   warps 6..13 converters: unpack the stage's 256 x 64 weights straight into
 //               tensor memory (tcgen05.st; thread = TMEM lane = output
 //               channel), one of two 128-column A buffers;
-//   warp 1      MMA: tcgen05.mma M=128 N=rows with the A operand (the weights,
-//               two 128-channel halves) read from tensor memory and the
-//               block's rows as the shared-memory B operand, into a TMEM
-//               accumulator, double buffered.  Unpacking into tensor memory
+//   warps 1, 14 MMA: tcgen05.mma M=128 N=rows with the A operand (the
+//               weights, one 128-channel half per warp, the two halves issued
+//               in parallel) read from tensor memory and the block's rows as
+//               the shared-memory B operand, into a TMEM accumulator, double
+//               buffered.  Unpacking into tensor memory
 //               keeps the 16-bit weights off shared memory: per step only the
 //               8 KB of packed weights and the rows pass through it;
 //   warps 2..5  epilogue: scales, silu(gate)*up for stage 1, row-masked
@@ -64,10 +65,12 @@ constexpr int W4_CONVS = 2;                      // A buffers in tensor memory
 constexpr int W4_A_SUB = W4_BK;                  // columns per sub-step: 2 halves x 64 x 16-bit / 32-bit
 constexpr int W4_A_COLS = W4_SUB * W4_A_SUB;
 constexpr int W4_A_COL0 = 256;                   // A buffers after the two accumulators
-constexpr int W4_THREADS = 448;
+constexpr int W4_THREADS = 480;
 constexpr int W4_CONV_WARP0 = 6;                 // converter warps 6..13: two per TMEM lane quarter
 constexpr int W4_CONV_WARPS = 8;
 constexpr int W4_EPI_WARPS = 4;
+constexpr int W4_MMA2_WARP = 14;                 // issues the second 128-channel half's MMAs
+constexpr int W4_MMA_WARPS = 2;
 constexpr int W4_TRING = 4;
 constexpr int W4_NEXT_FETCH = 1;                 // stages before a tile's end that the next one is taken
 constexpr int W4_ACC_COLS = 128;                 // 2 x up to 64 columns per accumulator
@@ -190,7 +193,7 @@ template <int DT>
 __device__ __forceinline__ uint4 w4_unpack8(uint32_t w) {
     constexpr uint32_t MAGIC = DT == kBF16 ? 0x43004300u : 0x64006400u;  // 128 / 1024, twice
     uint4 r;
-    if (DT == kF16) {
+    if constexpr (DT == kF16) {
         const uint32_t w8 = w >> 8;
         uint32_t q[4];
         q[0] = (w & 0x000F000Fu) | MAGIC;
@@ -205,23 +208,14 @@ __device__ __forceinline__ uint4 w4_unpack8(uint32_t w) {
         const __half2 v3 = __hfma2(*reinterpret_cast<__half2 *>(&q[3]), sixteenth, off16);
         r = make_uint4(*reinterpret_cast<const uint32_t *>(&v0), *reinterpret_cast<const uint32_t *>(&v1),
                        *reinterpret_cast<const uint32_t *>(&v2), *reinterpret_cast<const uint32_t *>(&v3));
-        return r;
-    }
-    uint32_t q[4];
+    } else {
+        uint32_t q[4];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) q[m] = ((w >> (4 * m)) & 0x000F000Fu) | MAGIC;
-    if (DT == kBF16) {
+        for (int m = 0; m < 4; ++m) q[m] = ((w >> (4 * m)) & 0x000F000Fu) | MAGIC;
         const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
         __nv_bfloat162 v[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) v[m] = __hsub2(*reinterpret_cast<__nv_bfloat162 *>(&q[m]), off);
-        r = make_uint4(*reinterpret_cast<uint32_t *>(&v[0]), *reinterpret_cast<uint32_t *>(&v[1]),
-                       *reinterpret_cast<uint32_t *>(&v[2]), *reinterpret_cast<uint32_t *>(&v[3]));
-    } else {
-        const __half2 off = __floats2half2_rn(1032.0f, 1032.0f);
-        __half2 v[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) v[m] = __hsub2(*reinterpret_cast<__half2 *>(&q[m]), off);
         r = make_uint4(*reinterpret_cast<uint32_t *>(&v[0]), *reinterpret_cast<uint32_t *>(&v[1]),
                        *reinterpret_cast<uint32_t *>(&v[2]), *reinterpret_cast<uint32_t *>(&v[3]));
     }
@@ -297,15 +291,15 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
         }
         for (int c = 0; c < W4_CONVS; ++c) {
             mbar_init(cfull(c), W4_CONV_WARPS);
-            mbar_init(cempty(c), 1);
+            mbar_init(cempty(c), W4_MMA_WARPS);
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(tfull(a), 1);
+            mbar_init(tfull(a), W4_MMA_WARPS);
             mbar_init(tempty(a), W4_EPI_WARPS);
         }
         for (int i = 0; i < W4_TRING; ++i) {
             mbar_init(tidf(i), 1);
-            mbar_init(tide(i), 1 + W4_EPI_WARPS);
+            mbar_init(tide(i), W4_MMA_WARPS + W4_EPI_WARPS);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -489,8 +483,12 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == W4_MMA2_WARP) {
         // --------------------------------- MMA ---------------------------------
+        // warp 1 issues the MMAs of channels 0..127, warp 14 those of 128..255:
+        // two independent accumulator chains, issued in parallel (one thread
+        // issues an MMA about every 85 cycles, whatever its size)
+        const int half = warp == 1 ? 0 : 1;
         if (lane == 0) {
             int stage = 0, cb = 0;
             uint32_t phase = 0, cph = 0;
@@ -522,9 +520,10 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * W4_ACC_COLS);
                 int np = (ti.rows + 15) & ~15;
                 if (np > W4_TOK_ROWS) np = W4_TOK_ROWS;
+                // D[channel][row]: channels 0..127 into columns [0, np), 128..255 into [np, 2np)
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * W4_ACC_COLS + half * np);
                 const uint32_t idesc = idesc_f16(DT == kBF16, 128, static_cast<uint32_t>(np));
                 for (int kb = 0; kb < kstages; ++kb) {
                     const int nsub = min(W4_SUB, ksub - kb * W4_SUB);
@@ -536,16 +535,13 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
                     tc_fence_after();
                     for (int u = 0; u < nsub; ++u) {
                         // A buffer cb, sub-step u: channels 0..127 in 32 columns, 128..255 in the next 32
-                        const uint32_t a0 =
-                            tmem_base + static_cast<uint32_t>(W4_A_COL0 + cb * W4_A_COLS + u * W4_A_SUB);
+                        const uint32_t a0 = tmem_base + static_cast<uint32_t>(W4_A_COL0 + cb * W4_A_COLS +
+                                                                              u * W4_A_SUB + half * (W4_A_SUB / 2));
                         const uint64_t bd = smem_desc_sw128(smem_u32(stages + stage * W4_STAGE_BYTES + u * W4_TOK_SUB));
 #pragma unroll
                         for (int k = 0; k < W4_BK / 16; ++k) {
                             const uint32_t accum = (kb | u | k) != 0 ? 1u : 0u;
-                            // D[channel][row]: first 128 channels into columns [0, np), the rest into [np, 2np)
                             tc_mma_f16_ta(d_tmem, a0 + 8u * k, bd + 2u * k, idesc, accum);
-                            tc_mma_f16_ta(d_tmem + static_cast<uint32_t>(np), a0 + W4_A_SUB / 2 + 8u * k,
-                                          bd + 2u * k, idesc, accum);
                         }
                     }
                     // the unpacked weights may be overwritten once these finish; the
@@ -569,7 +565,7 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
             }
             if (!ok && committed) w4_wait_drain(last_bar, last_parity);
         }
-    } else if (warp >= W4_CONV_WARP0) {
+    } else if (warp >= W4_CONV_WARP0 && warp < W4_CONV_WARP0 + W4_CONV_WARPS) {
         // ------------------------------ converters ------------------------------
         // warp w owns TMEM lanes 32 (w % 4) .. +31: its thread t unpacks the
         // 64 weights of channel 32 (w % 4) + t of half (w - 6) / 4 (channels
@@ -766,7 +762,6 @@ cudaError_t launch_grouped_mlp_w4(int dtype, const void *x, const int32_t *gathe
     if (n_rows <= 0 || m_blocks <= 0) return cudaSuccess;
     if (m_blocks > W4_MAX_BLOCKS) return cudaErrorInvalidValue;
     const int t16 = dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const int t8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
     CUtensorMap maps[2];
     const uint64_t uh = static_cast<uint64_t>(d_h), ue = static_cast<uint64_t>(d_e);
     {   // x [T, d_h], one row per box (four rows per gather)
