@@ -767,6 +767,100 @@ int oracle_grouped_down_w4(const void *h, const uint8_t *q_down, const float *s_
 }
 
 /* ------------------------------------------------------------------------- */
+/* f3: W4A8 -- int4 weights x int8 activations, int32 sums.                   */
+/* ------------------------------------------------------------------------- */
+/*
+ * [SKEL w4a8_dequant_gemm]: A int8 [M, K]; B uint8 [N, K / 2] in the int4
+ * format above; every int4 value is sign-extended to int8 on chip and the
+ * product summed in an int32 accumulator; the result is written transposed:
+ *   Ct[n, m] = sum_k A[m, k] * int4(B)[n, k]        (Ct int32 [N, M]).
+ * [SKEL quantisation notes]: weight + activation quantisation (W4A8); the
+ * skeleton returns the raw int32 sums (the dequantisation scales are the
+ * caller's).  The sum is formed here in int64: |Ct| <= 8 * 128 * K, so for
+ * K <= 2^20 an int32 accumulator cannot wrap and the two agree (larger K is
+ * refused).
+ */
+#define W4A8_MAX_K (1LL << 20)
+
+static int64_t dot_w4a8(const int8_t *a, const uint8_t *brow, int64_t K)
+{
+    int64_t acc = 0;
+    for (int64_t k = 0; k < K; ++k) {
+        const int nib = (brow[k / 2] >> (4 * (int)(k % 2))) & 0xF;
+        acc += (int64_t)a[k] * (int64_t)(nib >= 8 ? nib - 16 : nib);
+    }
+    return acc;
+}
+
+typedef struct {
+    const int8_t *a; const uint8_t *b; int64_t M, N, K; int32_t *ct;
+} w4a8_ctx;
+
+static void w4a8_cols(int64_t lo, int64_t hi, void *vctx)
+{
+    w4a8_ctx *c = (w4a8_ctx *)vctx;
+    for (int64_t n = lo; n < hi; ++n)
+        for (int64_t m = 0; m < c->M; ++m)
+            c->ct[n * c->M + m] = (int32_t)dot_w4a8(c->a + m * c->K, c->b + n * (c->K / 2), c->K);
+}
+
+int oracle_gemm_w4a8(const int8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K, int32_t *Ct,
+                     int nthreads)
+{
+    if (!A || !B || !Ct || M <= 0 || N <= 0 || K <= 0 || K % 2 != 0 || K > W4A8_MAX_K) return OR_EINVAL;
+    w4a8_ctx c = {A, B, M, N, K, Ct};
+    parallel_for(N, nthreads, w4a8_cols, &c);
+    return OR_OK;
+}
+
+/*
+ * The grouped form for the routed experts: the block walk of [SKEL
+ * moe_routed_kernel] / [CSDN stage 2 down] over the dispatch tables, each
+ * block's rows multiplied by its expert's int4 weight:
+ *   C[r, n] = sum_k a[r, k] * int4(B[g])[n, k]   (a int8 [n_rows, K] in
+ *   expert order, B [E, N, K / 2], C int32 [n_rows, N], g the row's expert).
+ */
+typedef struct {
+    const int8_t *a; const uint8_t *b;
+    const int32_t *sizes, *offsets, *padded, *gidx;
+    int64_t block_m, N, K; int32_t *c;
+} w4a8_grouped_ctx;
+
+static void w4a8_blocks(int64_t lo, int64_t hi, void *vctx)
+{
+    w4a8_grouped_ctx *c = (w4a8_grouped_ctx *)vctx;
+    const int64_t B = c->block_m;
+    for (int64_t bx = lo; bx < hi; ++bx) {
+        const int64_t g = c->gidx[bx];
+        const int64_t m_start = bx * B - c->padded[g] + c->offsets[g];
+        int64_t rows = c->sizes[g] - (bx * B - c->padded[g]);
+        if (rows > B) rows = B;
+        if (rows < 0) rows = 0;
+        for (int64_t i = 0; i < rows; ++i) {
+            const int64_t r = m_start + i;
+            for (int64_t n = 0; n < c->N; ++n)
+                c->c[r * c->N + n] =
+                    (int32_t)dot_w4a8(c->a + r * c->K, c->b + (g * c->N + n) * (c->K / 2), c->K);
+        }
+    }
+}
+
+int oracle_grouped_gemm_w4a8(const int8_t *a, const uint8_t *B, const int32_t *group_sizes,
+                             const int32_t *group_offsets, const int32_t *group_padded_offsets,
+                             const int32_t *group_idx_for_bx, int64_t m_blocks, int64_t block_m,
+                             int64_t n_rows, int64_t N, int64_t K, int64_t E, int32_t *C, int nthreads)
+{
+    if (!a || !B || !C || N <= 0 || K <= 0 || K % 2 != 0 || K > W4A8_MAX_K ||
+        !check_tables(group_sizes, group_offsets, group_padded_offsets, group_idx_for_bx,
+                      m_blocks, n_rows, E, block_m))
+        return OR_EINVAL;
+    w4a8_grouped_ctx c = {a, B, group_sizes, group_offsets, group_padded_offsets, group_idx_for_bx,
+                          block_m, N, K, C};
+    parallel_for(m_blocks, nthreads, w4a8_blocks, &c);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
 /* o5: moe_reduce_fused.                                                       */
 /* ------------------------------------------------------------------------- */
 /*

@@ -69,6 +69,8 @@ def _load():
         "oracle_grouped_gate_up_silu_w4": (I, [P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I64,
                                                I, P, I]),
         "oracle_grouped_down_w4": (I, [P, P, P, P, P, P, P, I64, I64, P, I64, I64, I64, I64, I, P, I]),
+        "oracle_gemm_w4a8": (I, [P, P, I64, I64, I64, P, I]),
+        "oracle_grouped_gemm_w4a8": (I, [P, P, P, P, P, P, I64, I64, I64, I64, I64, I64, P, I]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -271,6 +273,38 @@ def grouped_down_w4(h, q_down, tables: dict, dtype: str, s_down=None, row_weight
         _ptr(hb), _ptr(qd), _ptr(sd), _ptr(s), _ptr(o), _ptr(p), _ptr(g), g.size, block_m, _ptr(rw),
         n_rows, d_h, d_e, E, DTYPE_CODES[dtype], _ptr(y), nthreads), "grouped_down_w4")
     return y
+
+
+def gemm_w4a8(a, b, nthreads: int = 0) -> np.ndarray:
+    """W4A8 GEMM of skeletons.py ``w4a8_dequant_gemm``: a int8 [M, K], b uint8
+    [N, K // 2] (int4 two per byte, element j in byte j // 2 at nibble j % 2
+    from the low end); returns Ct int32 [N, M] = int4(b) @ a.T, summed exactly."""
+    av = np.ascontiguousarray(a, dtype=np.int8)
+    bv = np.ascontiguousarray(b, dtype=np.uint8)
+    M, K = av.shape
+    N, half = bv.shape
+    if half * 2 != K:
+        raise ValueError("b must be [N, K // 2]")
+    ct = np.empty((N, M), dtype=np.int32)
+    _check(_load().oracle_gemm_w4a8(_ptr(av), _ptr(bv), M, N, K, _ptr(ct), nthreads), "gemm_w4a8")
+    return ct
+
+
+def grouped_gemm_w4a8(a, b, tables: dict, block_m: int = 128, nthreads: int = 0) -> np.ndarray:
+    """The grouped W4A8 GEMM over the dispatch tables: a int8 [n_rows, K] in
+    expert order, b uint8 [E, N, K // 2]; returns C int32 [n_rows, N]."""
+    av = np.ascontiguousarray(a, dtype=np.int8)
+    bv = np.ascontiguousarray(b, dtype=np.uint8)
+    n_rows, K = av.shape
+    E, N, half = bv.shape
+    if half * 2 != K:
+        raise ValueError("b must be [E, N, K // 2]")
+    s, o, p, g = _tables(tables)
+    c = np.zeros((n_rows, N), dtype=np.int32)
+    _check(_load().oracle_grouped_gemm_w4a8(
+        _ptr(av), _ptr(bv), _ptr(s), _ptr(o), _ptr(p), _ptr(g), g.size, block_m, n_rows, N, K, E, _ptr(c),
+        nthreads), "grouped_gemm_w4a8")
+    return c
 
 
 def rows_gate_up_silu(a_rows, row_expert, w_gate, w_up, dtype: str, nthreads: int = 0):

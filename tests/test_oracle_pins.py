@@ -699,3 +699,70 @@ def test_w4_stages_integer_closed_form_and_pow2_scales(oracle):
     s_down = rng.choice([0.25, 1.0, 2.0], (E, d_h)).astype(np.float32)
     y2 = oracle.grouped_down_w4(_bits_f16(hi), _pack_int4(qd), tab, "f16", s_down=s_down)
     assert np.array_equal(oracle.decode(y2, "f16"), (Y * s_down[expert_of_row]).astype(np.float32))
+
+
+# --------------------------------------------------------------------------- #
+# W4A8: int4 weights x int8 activations, int32 sums (skeletons.py w4a8_dequant_gemm)
+# --------------------------------------------------------------------------- #
+
+def _int4_by_hand(byte: int, j: int) -> int:
+    """Element j % 2 of one packed byte, decoded with Python integers."""
+    v = (byte >> 4) if j % 2 else (byte & 15)
+    return v - 16 if v & 8 else v
+
+
+def test_w4a8_brute_force_tiny(oracle):
+    """Pure-Python loops over the bytes against the oracle, M != N so that a
+    transposed result or a swapped operand fails."""
+    rng = np.random.default_rng(31)
+    for M, N, K in [(1, 1, 2), (3, 5, 10), (7, 2, 34), (4, 9, 64)]:
+        a = rng.integers(-128, 128, (M, K)).astype(np.int8)
+        b = rng.integers(0, 256, (N, K // 2)).astype(np.uint8)
+        ref = [[sum(int(a[m, k]) * _int4_by_hand(int(b[n, k // 2]), k) for k in range(K))
+                for m in range(M)] for n in range(N)]
+        got = oracle.gemm_w4a8(a, b)
+        assert got.shape == (N, M) and got.dtype == np.int32
+        assert got.tolist() == ref
+
+
+def test_w4a8_extreme_closed_forms(oracle):
+    """Every element at its extreme: the sums are 1024 K, 889 K and -896 K,
+    here up to 2^30 (the int32 accumulator of the pages cannot wrap)."""
+    for K in (64, 4096, 1 << 20):
+        a = np.full((2, K), -128, np.int8)
+        b = np.full((3, K // 2), 0x88, np.uint8)  # every nibble -8
+        assert (oracle.gemm_w4a8(a, b) == 1024 * K).all()
+        assert (oracle.gemm_w4a8(np.full((1, K), 127, np.int8), np.full((1, K // 2), 0x77, np.uint8))
+                == 889 * K).all()
+        assert (oracle.gemm_w4a8(a[:1], np.full((2, K // 2), 0x77, np.uint8)) == -896 * K).all()
+    with pytest.raises(ValueError):
+        oracle.gemm_w4a8(np.zeros((1, (1 << 20) + 2), np.int8), np.zeros((1, (1 << 19) + 1), np.uint8))
+
+
+def test_w4a8_basis_rows_read_the_weights(oracle):
+    """A row that is the unit vector e_k gives column k of the unpacked
+    weight (unpack_int4 is pinned on hand-decoded bytes), for every k."""
+    rng = np.random.default_rng(32)
+    N, K = 6, 32
+    b = rng.integers(0, 256, (N, K // 2)).astype(np.uint8)
+    a = np.eye(K, dtype=np.int8) * np.int8(-1)
+    q = oracle.unpack_int4(b.reshape(-1), N * K).reshape(N, K).astype(np.int32)
+    assert np.array_equal(oracle.gemm_w4a8(a, b), -q)
+
+
+def test_w4a8_grouped_is_the_dense_product_per_expert(oracle):
+    """The grouped form over random dispatch tables equals the dense product
+    of each expert's rows with that expert's weight (transposed back)."""
+    rng = np.random.default_rng(33)
+    T, k, E, N, K = 300, 3, 5, 24, 96
+    _, tab = _random_tables(oracle, rng, T, k, E)
+    n_rows = T * k
+    a = rng.integers(-128, 128, (n_rows, K)).astype(np.int8)
+    b = rng.integers(0, 256, (E, N, K // 2)).astype(np.uint8)
+    c = oracle.grouped_gemm_w4a8(a, b, tab)
+    sizes, offs = tab["group_sizes"], tab["group_offsets"]
+    assert sizes.max() > 128  # several blocks per expert
+    for g in range(E):
+        r0, r1 = int(offs[g]), int(offs[g]) + int(sizes[g])
+        if r1 > r0:
+            assert np.array_equal(c[r0:r1], oracle.gemm_w4a8(a[r0:r1], b[g]).T)
