@@ -412,6 +412,8 @@ def run_native(args, cfg, rank, world, dev, with_aux=True):
     e2e = measure_e2e(args, cfg, d, dev, flush, world)
     aux = measure_reduce_aux(dev, flush) if rank == 0 and with_aux else None
     w4 = measure_w4(cfg, d, dev, flush) if rank == 0 and cfg.T <= 64 else None
+    if w4 is not None:
+        w4["w4a8_gemm"] = measure_w4a8(dev, flush)
     return dict(per_stage=per_stage, stages=list(step.stages), w4=w4, total_ms=total_ms, act_experts=act_experts,
                 sizes_pool=sizes_pool, clocks=clocks, e2e=e2e, aux=aux, mode=mode,
                 eager_ms=float(np.median(eager_ms)), wall_s=t_wall)
@@ -486,6 +488,53 @@ def measure_w4(cfg, d, dev, flush, steps: int = 200):
             "expert_mlp_us": round(res["expert_mlp"] * 1e3, 2), "expert_mlp_bytes": mlp_bytes,
             "expert_mlp_gbs": round(gbs, 1), "expert_mlp_frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
             "expert_mlp_note": "the standalone call includes the stream memset of its counters"}
+
+
+def measure_w4a8(dev, flush, steps: int = 100):
+    """The W4A8 GEMM (moe_gemm_w4a8: int4 weights x int8 activations, exact
+    int32 sums) on the serving shapes beside the pages' w4a8_dequant_gemm,
+    one whole call (counter memset, the K-split output memset, the int8 ->
+    fp16 row kernel and the GEMM) per timed replay, against the bytes the
+    product has to move (packed weights, activations, int32 result)."""
+    from mixture_experts_routed_gate_gb300 import binding
+    peaks, _ = load_peaks()
+    stream = torch.cuda.Stream(dev)
+    out = {}
+    for name, (M, N, K) in workloads.W4A8_SHAPES.items():
+        d = workloads.make_w4a8_inputs(M, N, K, seed=1, device=dev)
+        bp = binding.moe_pack_int4_weights(d["b"], 256)
+        a = d["a"]
+        ct = torch.empty((N, M), dtype=torch.int32, device=dev)
+        ws = torch.empty(int(binding.lib().moe_gemm_w4a8_workspace_bytes(M, K)), dtype=torch.uint8, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        fn = lambda: binding.moe_gemm_w4a8(a, bp, N, out=ct, ws=ws, err=err)
+        with torch.cuda.stream(stream):
+            fn()
+            stream.synchronize()
+            if int(err.item()) != 0:
+                raise RuntimeError(f"device error flag {int(err.item())} in the W4A8 GEMM")
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            for _ in range(3):
+                flush()
+                g.replay()
+            ts = []
+            for _ in range(steps):
+                flush()
+                s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s_.record(stream)
+                g.replay()
+                e_.record(stream)
+                e_.synchronize()
+                ts.append(s_.elapsed_time(e_))
+        us = float(np.mean(ts)) * 1e3
+        nbytes = N * K // 2 + M * K + 4 * N * M
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {"M": M, "N": N, "K": K, "us": round(us, 2), "bytes": nbytes, "gbs": round(gbs, 1),
+                     "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+        del d, bp, a, ct, ws, g
+    return out
 
 
 def measure_e2e(args, cfg, d, dev, flush, world):
@@ -822,7 +871,11 @@ def workload_record(args, cfg, res, world, steps, cpu_budget, dev):
     if res.get("aux") is not None:
         rec["reduce_fused_bf16_x8_7168"] = res["aux"]
     if res.get("w4") is not None:
-        rec["w4a16"] = res["w4"]
+        w4 = dict(res["w4"])
+        w4a8 = w4.pop("w4a8_gemm", None)
+        rec["w4a16"] = w4
+        if w4a8 is not None:
+            rec["w4a8_gemm"] = w4a8
     rec["clocks"] = res["clocks"]
     return rec
 

@@ -318,6 +318,48 @@ MOE_API moe_status_t moe_grouped_mlp_w4a16(const void *x, const int32_t *sorted_
                                    int32_t *err_flag, moe_stream_t stream);
 
 /*
+ * W4A8: int4 weights times int8 activations, summed exactly into int32
+ * (TileLang tutorial ch.18 skeletons.py, w4a8_dequant_gemm: the packed int4
+ * weight is unpacked and sign-extended on chip, the products summed in an
+ * int32 accumulator, the result written transposed; the module notes on
+ * quantisation: weight + activation quantisation, W4A8).  The results are
+ * the exact integer sums (bit-identical to an integer GEMM); the skeleton
+ * applies no scale, so none is taken here.
+ *
+ * moe_gemm_w4a8: Ct[n, m] = sum_k A[m, k] * int4(B)[n, k].  A int8 [M, K]
+ * row-major; B the weight [N, K] in the int4 format, packed by
+ * moe_pack_int4_weights with E = 1 and tile_rows = 256; Ct int32 [N, M]
+ * (transposed, as the skeleton writes it).  1 <= M <= 64 (the decode and
+ * small-batch shapes; M > 64 is MOE_ERR_UNSUPPORTED), N >= 1, K % 64 == 0,
+ * 64 <= K <= 2^20 (|Ct| <= 1024 K cannot overflow int32).  ws: device
+ * scratch of moe_gemm_w4a8_workspace_bytes(M, K) bytes (-1 for bad sizes),
+ * owned by the caller, 16-byte aligned, used only by this call's work.
+ * A, B, ws 16-byte aligned, Ct 4-byte aligned, all distinct.
+ *
+ * moe_grouped_gemm_w4a8: the same per routed row over the dispatch tables
+ * (the block walk of moe_routed_kernel): C[r, n] = sum_k x[i_r, k] *
+ * int4(B[g])[n, k] with g the expert of row r and i_r = sorted_token_idx[r]
+ * (NULL: i_r = r, n_rows <= T).  x int8 [T, K], 1 <= T <= 64 (so an expert
+ * holds at most 64 rows; a block with more is reported on err_flag and its
+ * rows past 64 are not written), B [E, N, K] packed with tile_rows 256,
+ * C int32 [n_rows, N].  A sorted_token_idx entry outside [0, T) is reported
+ * on err_flag (MOE_ERR_DEVICE_FLAG) and its row of C summed from zeros.
+ * ws: moe_grouped_gemm_w4a8_workspace_bytes(n_rows, K, m_blocks) bytes.
+ * m_blocks <= 1088.  Waits bounded as moe_grouped_mlp.
+ */
+MOE_API int64_t moe_gemm_w4a8_workspace_bytes(int64_t M, int64_t K);
+MOE_API moe_status_t moe_gemm_w4a8(const int8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K,
+                                   int32_t *Ct, void *ws, int64_t ws_bytes, int32_t *err_flag,
+                                   moe_stream_t stream);
+MOE_API int64_t moe_grouped_gemm_w4a8_workspace_bytes(int64_t n_rows, int64_t K, int64_t m_blocks);
+MOE_API moe_status_t moe_grouped_gemm_w4a8(const int8_t *x, const int32_t *sorted_token_idx, int64_t T,
+                                           const uint8_t *B, const int32_t *group_sizes,
+                                           const int32_t *group_offsets, const int32_t *group_padded_offsets,
+                                           const int32_t *group_idx_for_bx, int64_t m_blocks, int64_t n_rows,
+                                           int64_t N, int64_t K, int64_t E, int32_t *C, void *ws,
+                                           int64_t ws_bytes, int32_t *err_flag, moe_stream_t stream);
+
+/*
  * moe_reduce_fused (TileOPs-Metax PR #55, section 1): for every token t and
  * hidden element h,
  *   out[t, h] = cast( sum over k ascending with 0 <= pos[t,k] < n_rows of

@@ -71,6 +71,10 @@ def lib():
         "moe_grouped_mlp_w4a16": (I, [P, P, I64, P, P, P, P, P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I,
                                       P, P, P, P, P]),
         "moe_forward_w4a16": (I, [P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, SZ, P, P, P]),
+        "moe_gemm_w4a8_workspace_bytes": (I64, [I64, I64]),
+        "moe_gemm_w4a8": (I, [P, P, I64, I64, I64, P, P, I64, P, P]),
+        "moe_grouped_gemm_w4a8_workspace_bytes": (I64, [I64, I64, I64]),
+        "moe_grouped_gemm_w4a8": (I, [P, P, I64, P, P, P, P, P, I64, I64, I64, I64, I64, P, P, I64, P, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -87,7 +91,9 @@ def exported_symbols():
             "moe_build_dispatch_noalloc",
             "moe_copy", "moe_wait_flag", "moe_gather_rows", "moe_grouped_gate_up_silu", "moe_grouped_down",
             "moe_grouped_mlp", "moe_pack_int4_bytes", "moe_pack_int4_weights", "moe_grouped_mlp_w4a16",
-            "moe_forward_w4a16", "moe_reduce_fused", "moe_reduce_fused_scaled", "moe_forward"]
+            "moe_forward_w4a16", "moe_gemm_w4a8_workspace_bytes", "moe_gemm_w4a8",
+            "moe_grouped_gemm_w4a8_workspace_bytes", "moe_grouped_gemm_w4a8", "moe_reduce_fused",
+            "moe_reduce_fused_scaled", "moe_forward"]
 
 
 # --------------------------------------------------------------------------- helpers
@@ -463,6 +469,64 @@ def moe_grouped_mlp_w4a16(x, sorted_token_idx, experts: "Int4Experts", tables, r
             n_rows, d_h, d_e, E, _dtype_code(x, "x"), _ptr(h), _ptr(y), _ptr(ready), _ptr(err),
             _stream(x.device)), "moe_grouped_mlp_w4a16")
     return h, y
+
+
+def moe_gemm_w4a8(a, b_packed, N: int, out=None, ws=None, err=None):
+    """W4A8 GEMM: a int8 [M <= 64, K], b_packed = moe_pack_int4_weights(b [1, N, K // 2], 256);
+    returns Ct int32 [N, M], the exact sums int4(b) @ a.T."""
+    _cuda(a, "a", dtype=torch.int8, ndim=2)
+    _cuda(b_packed, "b_packed", dtype=torch.uint8)
+    M, K = a.shape
+    nws = int(lib().moe_gemm_w4a8_workspace_bytes(M, K))
+    if nws < 0:
+        raise ValueError("need 1 <= M <= 64, K % 64 == 0, 64 <= K <= 2^20")
+    if out is None:
+        out = torch.empty((N, M), dtype=torch.int32, device=a.device)
+    if ws is None:
+        ws = torch.empty(nws, dtype=torch.uint8, device=a.device)
+    _cuda(out, "out", dtype=torch.int32)
+    _cuda(ws, "ws", dtype=torch.uint8)
+    if tuple(out.shape) != (N, M):
+        raise ValueError("out must be [N, M]")
+    if err is not None:
+        _cuda(err, "err", dtype=torch.int32)
+    with torch.cuda.device(a.device):
+        _check(lib().moe_gemm_w4a8(_ptr(a), _ptr(b_packed), M, N, K, _ptr(out), _ptr(ws), ws.numel(), _ptr(err),
+                                   _stream(a.device)), "moe_gemm_w4a8")
+    return out
+
+
+def moe_grouped_gemm_w4a8(x, sorted_token_idx, b_packed, tables, N: int, E: int, n_rows=None, out=None,
+                          ws=None, err=None):
+    """Grouped W4A8 over the dispatch tables: x int8 [T <= 64, K], rows
+    x[sorted_token_idx[r]] (None: x's own rows), b_packed the [E, N, K] weight
+    packed with tile_rows 256; returns C int32 [n_rows, N]."""
+    _cuda(x, "x", dtype=torch.int8, ndim=2)
+    _cuda(b_packed, "b_packed", dtype=torch.uint8)
+    T, K = x.shape
+    if sorted_token_idx is not None:
+        _cuda(sorted_token_idx, "sorted_token_idx", dtype=torch.int32)
+        n_rows = sorted_token_idx.numel()
+    elif n_rows is None:
+        n_rows = T
+    s, o, p, g = _tables(tables)
+    nws = int(lib().moe_grouped_gemm_w4a8_workspace_bytes(max(n_rows, 1), K, max(g.numel(), 1)))
+    if nws < 0:
+        raise ValueError("need K % 64 == 0, 64 <= K <= 2^20")
+    if out is None:
+        out = torch.empty((n_rows, N), dtype=torch.int32, device=x.device)
+    if ws is None:
+        ws = torch.empty(nws, dtype=torch.uint8, device=x.device)
+    _cuda(out, "out", dtype=torch.int32)
+    _cuda(ws, "ws", dtype=torch.uint8)
+    if err is not None:
+        _cuda(err, "err", dtype=torch.int32)
+    with torch.cuda.device(x.device):
+        _check(lib().moe_grouped_gemm_w4a8(
+            _ptr(x), _ptr(sorted_token_idx), T, _ptr(b_packed), _ptr(s), _ptr(o), _ptr(p), _ptr(g), g.numel(),
+            n_rows, N, K, E, _ptr(out), _ptr(ws), ws.numel(), _ptr(err), _stream(x.device)),
+            "moe_grouped_gemm_w4a8")
+    return out
 
 
 def moe_forward_w4a16(x, w_g, bias, experts: "Int4Experts", k: int, ws=None, out=None, err=None):

@@ -424,6 +424,69 @@ moe_status_t moe_grouped_mlp_w4a16(const void *x, const int32_t *sorted_token_id
                           row_weights, n_rows, d_h, d_e, E, dtype, h, y, ready, err_flag, stream, true);
 }
 
+// ---------------------------------------------------------------------------
+// W4A8: int4 weights x int8 activations, exact int32 sums
+// ---------------------------------------------------------------------------
+static int64_t w4a8_ws_bytes(int64_t n_rows, int64_t K, int64_t blocks) {
+    return static_cast<int64_t>(align_up(static_cast<size_t>(n_rows) * static_cast<size_t>(K) * 2) +
+                                align_up(static_cast<size_t>(blocks + 1) * 4));
+}
+
+static bool w4a8_k_ok(int64_t K) { return K >= 64 && K % 64 == 0 && K <= (int64_t(1) << 20); }
+
+int64_t moe_gemm_w4a8_workspace_bytes(int64_t M, int64_t K) {
+    if (M < 1 || M > 64 || !w4a8_k_ok(K)) return -1;
+    return w4a8_ws_bytes(M, K, 1);
+}
+
+moe_status_t moe_gemm_w4a8(const int8_t *A, const uint8_t *B, int64_t M, int64_t N, int64_t K, int32_t *Ct,
+                           void *ws, int64_t ws_bytes, int32_t *err_flag, moe_stream_t stream) {
+    if (M < 1 || N < 1 || !w4a8_k_ok(K) || N > (int64_t(1) << 24)) return MOE_ERR_INVALID_ARG;
+    if (M > 64) return MOE_ERR_UNSUPPORTED;
+    if (!A || !B || !Ct || !ws || !aligned16(A) || !aligned16(B) || !aligned16(ws) ||
+        (reinterpret_cast<uintptr_t>(Ct) & 3u) != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_gemm_w4a8_workspace_bytes(M, K)) return MOE_ERR_WORKSPACE;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    void *rows = w;
+    int32_t *counters = reinterpret_cast<int32_t *>(w + align_up(static_cast<size_t>(M * K) * 2));
+    return cuda_status(moe::launch_gemm_w4a8(A, nullptr, M, B, nullptr, nullptr, nullptr, nullptr, 0, M, M, N,
+                                             K, rows, counters, Ct, 1, M, N * M, err_flag,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int64_t moe_grouped_gemm_w4a8_workspace_bytes(int64_t n_rows, int64_t K, int64_t m_blocks) {
+    if (n_rows < 1 || m_blocks < 1 || !w4a8_k_ok(K)) return -1;
+    return w4a8_ws_bytes(n_rows, K, m_blocks);
+}
+
+moe_status_t moe_grouped_gemm_w4a8(const int8_t *x, const int32_t *sorted_token_idx, int64_t T,
+                                   const uint8_t *B, const int32_t *group_sizes, const int32_t *group_offsets,
+                                   const int32_t *group_padded_offsets, const int32_t *group_idx_for_bx,
+                                   int64_t m_blocks, int64_t n_rows, int64_t N, int64_t K, int64_t E,
+                                   int32_t *C, void *ws, int64_t ws_bytes, int32_t *err_flag,
+                                   moe_stream_t stream) {
+    if (T < 1 || N < 1 || !w4a8_k_ok(K) || N > (int64_t(1) << 24)) return MOE_ERR_INVALID_ARG;
+    if (T > 64) return MOE_ERR_UNSUPPORTED;
+    if (n_rows == 0) return MOE_OK;
+    if (!sorted_token_idx && n_rows > T) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_gemm_tables(group_sizes, group_offsets, group_padded_offsets, group_idx_for_bx,
+                                        m_blocks, n_rows, E);
+    if (st != MOE_OK) return st;
+    if (m_blocks > 1088) return MOE_ERR_UNSUPPORTED;
+    if (!x || !B || !C || !ws || !aligned16(x) || !aligned16(B) || !aligned16(ws) ||
+        (reinterpret_cast<uintptr_t>(C) & 3u) != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_grouped_gemm_w4a8_workspace_bytes(n_rows, K, m_blocks)) return MOE_ERR_WORKSPACE;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    void *rows = w;
+    int32_t *counters = reinterpret_cast<int32_t *>(w + align_up(static_cast<size_t>(n_rows * K) * 2));
+    return cuda_status(moe::launch_gemm_w4a8(x, sorted_token_idx, T, B, group_sizes, group_offsets,
+                                             group_padded_offsets, group_idx_for_bx, m_blocks, 0, n_rows, N, K,
+                                             rows, counters, C, N, 1, n_rows * N, err_flag,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
 static bool reduce_pair_ok(moe_dtype_t in, moe_dtype_t out, bool allow_fp8) {
     const bool in_ok = in == MOE_F16 || in == MOE_BF16 || in == MOE_F32;
     if (!in_ok) return false;

@@ -132,10 +132,18 @@ struct W4Params {
     int nt0, nt1;       // output tiles per block: stage 1 (128 columns), stage 2 (256)
     int kb0, kb1;       // 64-wide K sub-steps: stage 1 (d_h / 64), stage 2 (d_e / 64)
     int *err;
+    // W4A8 GEMM form (nt0 = 0: stage-2 tiles only, rows from h, int32 out):
+    // a stage-2 tile covers sub-steps [kc * kchunk, (kc + 1) * kchunk) of
+    // kb1; ksplit = 1 and kchunk = kb1 for the expert MLP
+    int ksplit, kchunk;
+    int dense_rows;        // > 0: one block of this many rows, no tables
+    int32_t *out_i32;      // non-null: int32 results at m * ld_row + n * ld_col
+    int64_t ld_row, ld_col;
+    int atomic_out;        // add (the K chunks of a tile) instead of store
 };
 
 struct W4Tile {
-    int g, m_start, rows, n0, bx, phase;
+    int g, m_start, rows, n0, bx, phase, kc;
 };
 
 // Tile t of the launch: the stage-1 tiles of every listed block first, then
@@ -148,14 +156,18 @@ __device__ __forceinline__ W4Tile w4_tile(const W4Params &p, const int *list, co
     int pos, nt;
     if (t < n0_tiles) {
         ti.phase = 0;
+        ti.kc = 0;
         pos = t / p.nt0;
         nt = t - pos * p.nt0;
         ti.n0 = nt * 128;
     } else {
         ti.phase = 1;
         t -= n0_tiles;
-        pos = t / p.nt1;
-        nt = t - pos * p.nt1;
+        const int per_block = p.nt1 * p.ksplit;
+        pos = t / per_block;
+        const int rem = t - pos * per_block;
+        nt = rem / p.ksplit;
+        ti.kc = rem - nt * p.ksplit;
         ti.n0 = nt * 256;
     }
     const int bx = list[pos];
@@ -164,6 +176,13 @@ __device__ __forceinline__ W4Tile w4_tile(const W4Params &p, const int *list, co
     ti.m_start = blk_m[bx];
     ti.rows = blk_rows[bx];
     return ti;
+}
+
+// 64-wide K sub-steps of a tile (its K chunk for a stage-2 tile)
+__device__ __forceinline__ int w4_ksub(const W4Params &p, const W4Tile &ti) {
+    if (ti.phase == 0) return p.kb0;
+    const int left = p.kb1 - ti.kc * p.kchunk;
+    return left < p.kchunk ? left : p.kchunk;
 }
 
 // bulk copy of `bytes` contiguous bytes (16-byte aligned) into shared memory,
@@ -319,7 +338,15 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
 
     // ----- schedule: the non-empty M blocks in order, with their lookups -----
     int n_blocks = 0;
-    {
+    if (p.dense_rows > 0) {  // one block: rows 0 .. dense_rows - 1, weight 0
+        n_blocks = 1;
+        if (threadIdx.x == 0) {
+            list[0] = 0;
+            blk_g[0] = 0;
+            blk_m[0] = 0;
+            blk_rows[0] = static_cast<uint8_t>(p.dense_rows);
+        }
+    } else {
         const int chunk = (p.m_blocks + W4_THREADS - 1) / W4_THREADS;
         const int lo = threadIdx.x * chunk, hi = min(p.m_blocks, lo + chunk);
         int mine = 0;
@@ -341,7 +368,7 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = n_blocks * (p.nt0 + p.nt1);
+    const int total = n_blocks * (p.nt0 + p.nt1 * p.ksplit);
 
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
@@ -391,7 +418,7 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
             if (tile < 0) break;
             const W4Tile ti = w4_tile(p, list, blk_g, blk_m, blk_rows, n_blocks, tile);
             // stage 2 reads its block's h rows: all stage-1 warp-tiles stored
-            if (ti.phase == 1) {
+            if (ti.phase == 1 && p.nt0 > 0) {
                 if (lane == 0)
                     go = counter_wait_bounded(p.ready + ti.bx, W4_EPI_WARPS * p.nt0, abort_flag, p.err) ? 1 : 0;
                 go = __shfl_sync(0xffffffffu, go, 0);
@@ -416,7 +443,8 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
                 i2 = __ldg(ids + (r + 2 < ti.rows ? r + 2 : 0));
                 i3 = __ldg(ids + (r + 3 < ti.rows ? r + 3 : 0));
             }
-            const int ksub = ti.phase == 0 ? p.kb0 : p.kb1;
+            const int ksub = w4_ksub(p, ti);
+            const int kbase = ti.kc * p.kchunk;  // first sub-step of the tile's K chunk
             const int kstages = (ksub + W4_SUB - 1) / W4_SUB;
             const int fetch_kb = kstages > W4_NEXT_FETCH ? kstages - W4_NEXT_FETCH : 0;
             for (int kb = 0; kb < kstages; ++kb) {
@@ -441,7 +469,7 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
                     mbar_arrive_expect_tx(fb, tx);
                 }
                 __syncwarp();  // the stage's byte count is armed before any copy lands
-                const int sub0 = kb * W4_SUB;  // first 64-wide sub-step of the stage
+                const int sub0 = kbase + kb * W4_SUB;  // first 64-wide sub-step of the stage
                 if (ti.phase == 0) {
                     if (gatherer)
                         for (int u = 0; u < nsub; ++u)
@@ -511,7 +539,7 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
                 }
                 if (tile < 0) break;
                 const W4Tile ti = w4_tile(p, list, blk_g, blk_m, blk_rows, n_blocks, tile);
-                const int ksub = ti.phase == 0 ? p.kb0 : p.kb1;
+                const int ksub = w4_ksub(p, ti);
                 const int kstages = (ksub + W4_SUB - 1) / W4_SUB;
                 const int acc = local & 1;
                 const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
@@ -667,6 +695,40 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
             const int rows = ti.rows < np ? ti.rows : np;
             const int f0 = ti.n0 + ch;
             const int f1 = gu ? -1 : ti.n0 + 128 + ch;
+            if (p.out_i32) {
+                // W4A8: the fp32 sums hold integers of magnitude <= 2^24 (a K
+                // chunk is at most 16384 long), so the conversion is exact
+#pragma unroll 1
+                for (int j0 = 0; j0 < np; j0 += 16) {
+                    uint32_t a[16], b[16];
+                    tmem_ld16(t_row + j0, a);
+                    tmem_ld16(t_row + np + j0, b);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int j = j0 + jj;
+                        if (j < rows) {
+                            const int64_t m = ti.m_start + j;
+                            int32_t *o0 = p.out_i32 + m * p.ld_row + static_cast<int64_t>(f0) * p.ld_col;
+                            int32_t *o1 = p.out_i32 + m * p.ld_row + static_cast<int64_t>(f1) * p.ld_col;
+                            const int v0 = __float2int_rn(__uint_as_float(a[jj]));
+                            const int v1 = __float2int_rn(__uint_as_float(b[jj]));
+                            if (p.atomic_out) {
+                                if (f0 < N) atomicAdd(o0, v0);
+                                if (f1 < N) atomicAdd(o1, v1);
+                            } else {
+                                if (f0 < N) *o0 = v0;
+                                if (f1 < N) *o1 = v1;
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty(acc));
+                ++local;
+                continue;
+            }
             // per-channel scales (1 when absent): stage 1 gate / up, stage 2 the two channels
             float sa = 1.0f, sb = 1.0f;
             if (gu) {
@@ -799,9 +861,129 @@ cudaError_t launch_grouped_mlp_w4(int dtype, const void *x, const int32_t *gathe
     p.kb0 = static_cast<int>(d_h / W4_BK);
     p.kb1 = static_cast<int>(d_e / W4_BK);
     p.err = err;
+    p.ksplit = 1;
+    p.kchunk = p.kb1;
     const int64_t tiles = m_blocks * (p.nt0 + p.nt1);
     const int grid = mlp_grid(tiles);
     if (dtype == kBF16) return launch_w4_typed<kBF16>(maps, p, grid, stream);
+    return launch_w4_typed<kF16>(maps, p, grid, stream);
+}
+
+namespace {
+
+// W4A8 activations: int8 rows (row r = x[idx[r]], or x[r] without idx) ->
+// fp16 rows; every int8 value is exact in fp16.  A row index outside
+// [0, T) is reported on err and its row written as zeros.
+__global__ void w4a8_rows_kernel(const int8_t *__restrict__ x, const int32_t *__restrict__ idx, int64_t T,
+                                 int64_t n_rows, int64_t K, __half *__restrict__ out, int32_t *err) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int64_t per_row = K / 16;
+    const int64_t total = n_rows * per_row;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / per_row, c = i - r * per_row;
+        const int64_t src = idx ? __ldg(idx + r) : r;
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+        if (src >= 0 && src < T) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(x + src * K) + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t h[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const __half2 a = __halves2half2(__int2half_rn(static_cast<int8_t>(w[q] & 0xFFu)),
+                                                 __int2half_rn(static_cast<int8_t>((w[q] >> 8) & 0xFFu)));
+                const __half2 b = __halves2half2(__int2half_rn(static_cast<int8_t>((w[q] >> 16) & 0xFFu)),
+                                                 __int2half_rn(static_cast<int8_t>(w[q] >> 24)));
+                h[2 * q] = *reinterpret_cast<const uint32_t *>(&a);
+                h[2 * q + 1] = *reinterpret_cast<const uint32_t *>(&b);
+            }
+            lo = make_uint4(h[0], h[1], h[2], h[3]);
+            hi = make_uint4(h[4], h[5], h[6], h[7]);
+        } else if (err && c == 0) {
+            atomicExch(err, kErrDeviceFlag);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(out + r * K) + 2 * c;
+        dst[0] = lo;
+        dst[1] = hi;
+    }
+}
+
+}  // namespace
+
+W4a8Plan w4a8_plan(int64_t blocks, int64_t N, int64_t K) {
+    W4a8Plan pl;
+    const int64_t kb = K / W4_BK, nt = (N + 255) / 256;
+    // split K until the grid is about one tile per SM, in chunks of at least
+    // four sub-steps, and in any case into chunks of at most 256 sub-steps
+    // (16384 products: the fp32 sums stay integers of magnitude <= 2^24)
+    int64_t ks = device_sm_count() / std::max<int64_t>(1, blocks * nt);
+    ks = std::min<int64_t>(ks, std::max<int64_t>(1, kb / 4));
+    ks = std::max<int64_t>(ks, (kb + kW4a8MaxChunkSub - 1) / kW4a8MaxChunkSub);
+    ks = std::max<int64_t>(ks, 1);
+    pl.kchunk = (kb + ks - 1) / ks;
+    pl.ksplit = (kb + pl.kchunk - 1) / pl.kchunk;
+    return pl;
+}
+
+cudaError_t launch_gemm_w4a8(const int8_t *x, const int32_t *gather_idx, int64_t T, const uint8_t *B,
+                             const int32_t *sizes, const int32_t *offsets, const int32_t *padded,
+                             const int32_t *gidx, int64_t m_blocks, int64_t dense_rows, int64_t n_rows,
+                             int64_t N, int64_t K, void *rows_f16, int32_t *counters, int32_t *out,
+                             int64_t ld_row, int64_t ld_col, int64_t out_elems, int32_t *err,
+                             cudaStream_t stream) {
+    if (n_rows <= 0 || N <= 0) return cudaSuccess;
+    if (dense_rows <= 0 && (m_blocks <= 0 || m_blocks > W4_MAX_BLOCKS)) return cudaErrorInvalidValue;
+    if (dense_rows > W4_TOK_ROWS || K % W4_BK != 0) return cudaErrorInvalidValue;
+    const int64_t blocks = dense_rows > 0 ? 1 : m_blocks;
+    const W4a8Plan pl = w4a8_plan(blocks, N, K);
+    cudaError_t e = cudaMemsetAsync(counters, 0, static_cast<size_t>(blocks + 1) * 4, stream);
+    if (e != cudaSuccess) return e;
+    if (pl.ksplit > 1) {
+        e = cudaMemsetAsync(out, 0, static_cast<size_t>(out_elems) * 4, stream);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        const int64_t work = n_rows * (K / 16);
+        const int64_t nb = std::min<int64_t>((work + 255) / 256, 4LL * device_sm_count());
+        e = launch_pdl(w4a8_rows_kernel, dim3(static_cast<unsigned>(nb)), dim3(256), 0, stream, x, gather_idx,
+                       T, n_rows, K, static_cast<__half *>(rows_f16), err);
+        if (e != cudaSuccess) return e;
+    }
+    CUtensorMap maps[2];
+    {   // the fp16 rows [n_rows, K], 64 rows per box (both map slots: stage-1 rows are unused)
+        const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(n_rows)},
+                       st[1] = {static_cast<uint64_t>(K) * 2};
+        const uint32_t box[2] = {W4_BK, W4_TOK_ROWS};
+        if (!encode_tma_map(&maps[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rows_f16, dims, st, box, 1))
+            return cudaErrorInvalidValue;
+        maps[0] = maps[1];
+    }
+    W4Params p{};
+    p.sizes = sizes;
+    p.offsets = offsets;
+    p.padded = padded;
+    p.gidx = gidx;
+    p.q_down = B;
+    p.ready = counters;
+    p.tile_counter = counters + blocks;
+    p.h = rows_f16;
+    p.m_blocks = static_cast<int>(blocks);
+    p.d_h = static_cast<int>(N);
+    p.d_e = static_cast<int>(K);
+    p.nt0 = 0;
+    p.nt1 = static_cast<int>((N + 255) / 256);
+    p.kb0 = 0;
+    p.kb1 = static_cast<int>(K / W4_BK);
+    p.err = err;
+    p.ksplit = static_cast<int>(pl.ksplit);
+    p.kchunk = static_cast<int>(pl.kchunk);
+    p.dense_rows = static_cast<int>(dense_rows);
+    p.out_i32 = out;
+    p.ld_row = ld_row;
+    p.ld_col = ld_col;
+    p.atomic_out = pl.ksplit > 1 ? 1 : 0;
+    const int grid = mlp_grid(blocks * p.nt1 * pl.ksplit);
     return launch_w4_typed<kF16>(maps, p, grid, stream);
 }
 

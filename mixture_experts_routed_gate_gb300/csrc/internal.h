@@ -131,4 +131,26 @@ cudaError_t launch_grouped_mlp_w4(int dtype, const void *x, const int32_t *gathe
                                   int64_t d_e, int64_t E, void *h, void *y, int32_t *ready,
                                   int32_t *err, cudaStream_t stream);
 
+// W4A8 (int4 weights x int8 activations, int32 sums) on the int4 kernel's
+// stage-2 path: the int8 rows are widened to fp16 (exact) into rows_f16
+// [n_rows, K], then every 256-channel tile sums one K chunk of at most
+// kW4a8MaxChunkSub 64-wide sub-steps in fp32 (exact: every partial sum is an
+// integer of magnitude <= 1024 * 16384 = 2^24) and stores (one chunk) or adds
+// (several, integer atomics) its int32 results at m * ld_row + n * ld_col.
+// dense_rows > 0: one block of that many rows (<= 64) and weight 0, no
+// tables; otherwise the dispatch tables (every block <= 64 rows).
+// counters: (blocks + 1) int32, zeroed here; out (out_elems int32) zeroed
+// here when K is split.  K % 64 == 0.
+constexpr int64_t kW4a8MaxChunkSub = 256;
+struct W4a8Plan {
+    int64_t ksplit = 1, kchunk = 1;  // K chunks per tile and their sub-steps
+};
+W4a8Plan w4a8_plan(int64_t blocks, int64_t N, int64_t K);
+cudaError_t launch_gemm_w4a8(const int8_t *x, const int32_t *gather_idx, int64_t T, const uint8_t *B,
+                             const int32_t *sizes, const int32_t *offsets, const int32_t *padded,
+                             const int32_t *gidx, int64_t m_blocks, int64_t dense_rows, int64_t n_rows,
+                             int64_t N, int64_t K, void *rows_f16, int32_t *counters, int32_t *out,
+                             int64_t ld_row, int64_t ld_col, int64_t out_elems, int32_t *err,
+                             cudaStream_t stream);
+
 }  // namespace moe

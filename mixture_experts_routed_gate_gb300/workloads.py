@@ -75,6 +75,14 @@ REDUCE_CONFIGS = {
     "reduce-4096": ReduceConfig("reduce-4096", 4096, 8, 7168, "bf16", 3),
 }
 
+# The W4A8 GEMM's serving shapes (TileLang tutorial ch.18 skeletons.py,
+# SERVING_SHAPES beside w4a8_dequant_gemm): a decode step (M = 1) and a small
+# batch (M = 32), N x K one weight matrix of that size.
+W4A8_SHAPES = {
+    "gemv_like": (1, 3584, 18944),
+    "small_batch": (32, 3584, 18944),
+}
+
 REDUCE_EDGE_SHAPES = [(4, 2, 256), (1, 8, 256), (8, 1, 256), (32, 8, 3072), (512, 8, 3072)]
 
 
@@ -162,6 +170,16 @@ def make_reduce_inputs(T: int, K: int, H: int, dtype: str, seed: int, device="cp
         s = torch.exp2(u * 4.0 - 2.0)
         out.update(x_sf=s[:n].contiguous(), sf=s[n:].contiguous())
     return out
+
+
+def make_w4a8_inputs(M: int, N: int, K: int, seed: int, device="cpu", E: int = 1) -> dict:
+    """Uniform int8 activations a [M, K] and uniform packed int4 weights b
+    [E, N, K // 2] (every byte value equally likely: both nibbles uniform
+    over -8..7), the layout the pages print."""
+    gen = _gen(device, seed * 104729 + M * 31 + N * 7 + K)
+    a = torch.randint(-128, 128, (M, K), generator=gen, device=device, dtype=torch.int32).to(torch.int8)
+    b = torch.randint(0, 256, (E, N, K // 2), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
+    return dict(a=a, b=b)
 
 
 def to_numpy_bits(t: torch.Tensor):

@@ -192,6 +192,38 @@ def test_int4_forward_and_copy_stay_inside():
     assert torch.equal(dst, src)
 
 
+@pytest.mark.parametrize("M,N,K", [(5, 300, 1984), (1, 3584, 18944), (64, 255, 320)])
+def test_w4a8_stays_inside(oracle, M, N, K):
+    """The W4A8 GEMM (stored and K-split atomic forms) and its grouped form:
+    output and workspace between guard bands."""
+    dev = require_cuda()
+    d = workloads.make_w4a8_inputs(M, N, K, seed=8)
+    bp = binding.moe_pack_int4_weights(d["b"].to(dev), 256)
+    G = Guards(dev)
+    err = G.zeros((1,), torch.int32, "err")
+    ct = G.empty((N, M), torch.int32, "w4a8 Ct")
+    ws = G.empty((binding.lib().moe_gemm_w4a8_workspace_bytes(M, K),), torch.uint8, "w4a8 workspace")
+    binding.moe_gemm_w4a8(d["a"].to(dev), bp, N, out=ct, ws=ws, err=err)
+    E = 3
+    rng = np.random.default_rng(M + N)
+    idx = np.stack([rng.permutation(E)[:2] for _ in range(M)]).astype(np.int32)
+    tab = oracle.build_dispatch(idx, None, E, 128)
+    tabd = {n: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for n, v in tab.items()}
+    dg = workloads.make_w4a8_inputs(M, N, K, seed=9, E=E)
+    bpg = binding.moe_pack_int4_weights(dg["b"].to(dev), 256)
+    n_rows, mb = 2 * M, tab["group_idx_for_bx"].size
+    c = G.empty((n_rows, N), torch.int32, "grouped w4a8 C")
+    wsg = G.empty((binding.lib().moe_grouped_gemm_w4a8_workspace_bytes(n_rows, K, mb),), torch.uint8,
+                  "grouped w4a8 workspace")
+    binding.moe_grouped_gemm_w4a8(dg["a"].to(dev), tabd["sorted_token_idx"], bpg, tabd, N, E, out=c, ws=wsg,
+                                  err=err)
+    G.check()
+    assert int(err.item()) == 0
+    assert np.array_equal(ct.cpu().numpy(), oracle.gemm_w4a8(d["a"].numpy(), d["b"][0].numpy()))
+    rows = dg["a"].numpy()[tab["sorted_token_idx"]]
+    assert np.array_equal(c.cpu().numpy(), oracle.grouped_gemm_w4a8(rows, dg["b"].numpy(), tab))
+
+
 @pytest.mark.parametrize("T,k,E", [(300, 4, 20),    # one-CTA dispatch
                                    (5000, 8, 64)])  # histogram / scan / scatter kernels
 def test_dispatch_drops_ids_outside_the_experts(oracle, T, k, E):
