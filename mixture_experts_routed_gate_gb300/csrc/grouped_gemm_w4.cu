@@ -241,6 +241,23 @@ __device__ __forceinline__ uint4 w4_unpack8(uint32_t w) {
     return r;
 }
 
+// One channel's 64 packed weights of a sub-step (32 bytes of shared memory)
+// unpacked into 32 words of two 16-bit values, in element order.
+template <int DT>
+__device__ __forceinline__ void w4_unpack_row(const uint8_t *prow, uint32_t *cols) {
+    const uint4 lo = *reinterpret_cast<const uint4 *>(prow);
+    const uint4 hi = *reinterpret_cast<const uint4 *>(prow + 16);
+    const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const uint4 v = w4_unpack8<DT>(wv[w]);
+        cols[4 * w + 0] = v.x;
+        cols[4 * w + 1] = v.y;
+        cols[4 * w + 2] = v.z;
+        cols[4 * w + 3] = v.w;
+    }
+}
+
 // Exclusive scan of one int per thread across the CTA; returns the total.
 __device__ __forceinline__ int w4_cta_scan(int v, int *scratch, int *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -562,9 +579,10 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
                     }
                     tc_fence_after();
                     for (int u = 0; u < nsub; ++u) {
-                        // A buffer cb, sub-step u: channels 0..127 in 32 columns, 128..255 in the next 32
+                        // A buffer cb: channels 0..127 in columns [0, 64) (sub-step u at 32 u),
+                        // 128..255 in [64, 128)
                         const uint32_t a0 = tmem_base + static_cast<uint32_t>(W4_A_COL0 + cb * W4_A_COLS +
-                                                                              u * W4_A_SUB + half * (W4_A_SUB / 2));
+                                                                              half * W4_A_SUB + u * (W4_A_SUB / 2));
                         const uint64_t bd = smem_desc_sw128(smem_u32(stages + stage * W4_STAGE_BYTES + u * W4_TOK_SUB));
 #pragma unroll
                         for (int k = 0; k < W4_BK / 16; ++k) {
@@ -622,22 +640,19 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
             const uint8_t *prow = gphase == 0 ? pk + half * (W4_PACK_BYTES / 2) + ch * W4_PACK_ROW
                                               : pk + (half * 128 + ch) * W4_PACK_ROW;
             const int sub_stride = gphase == 0 ? W4_PACK_SUB / 2 : W4_PACK_SUB;
-            for (int u = 0; u < nsub; ++u) {
-                const uint4 lo = *reinterpret_cast<const uint4 *>(prow + u * sub_stride);
-                const uint4 hi = *reinterpret_cast<const uint4 *>(prow + u * sub_stride + 16);
-                const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-                uint32_t cols[32];
+            // the half's columns of both sub-steps are adjacent: one store of 64 columns
+            const uint32_t a_dst =
+                tmem_base + lane_base + static_cast<uint32_t>(W4_A_COL0 + cb * W4_A_COLS + half * W4_A_SUB);
+            if (nsub == W4_SUB) {
+                uint32_t cols[64];
 #pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    const uint4 v = w4_unpack8<DT>(wv[w]);
-                    cols[4 * w + 0] = v.x;
-                    cols[4 * w + 1] = v.y;
-                    cols[4 * w + 2] = v.z;
-                    cols[4 * w + 3] = v.w;
-                }
-                tmem_st32(tmem_base + lane_base +
-                              static_cast<uint32_t>(W4_A_COL0 + cb * W4_A_COLS + u * W4_A_SUB + half * 32),
-                          cols);
+                for (int u = 0; u < W4_SUB; ++u)
+                    w4_unpack_row<DT>(prow + u * sub_stride, cols + 32 * u);
+                tmem_st64(a_dst, cols);
+            } else {
+                uint32_t cols[32];
+                w4_unpack_row<DT>(prow, cols);
+                tmem_st32(a_dst, cols);
             }
             tmem_st_wait();
             tc_fence_before();
