@@ -80,7 +80,8 @@ static_assert(W4_STAGES > W4_CONVS, "a stage is released W4_CONVS steps after it
 constexpr int W4_MAX_BLOCKS = 1088;              // M blocks the schedule lists
 constexpr int W4_BAR_BYTES = 512;
 constexpr int W4_SCHED_BYTES = W4_MAX_BLOCKS * (4 * 3 + 1) + 64 * 4;
-constexpr int W4_SMEM_BYTES = 1024 + W4_STAGES * W4_STAGE_BYTES + W4_BAR_BYTES + W4_SCHED_BYTES;
+constexpr int W4_XPOSE_BYTES = W4_EPI_WARPS * 32 * 17 * 4;  // W4A8 epilogue: a 32 x 16 transpose per warp
+constexpr int W4_SMEM_BYTES = 1024 + W4_STAGES * W4_STAGE_BYTES + W4_BAR_BYTES + W4_SCHED_BYTES + W4_XPOSE_BYTES;
 static_assert(W4_SMEM_BYTES <= 232448, "shared memory per CTA");
 static_assert(W4_STAGE_BYTES % 1024 == 0, "swizzle atoms");
 
@@ -305,6 +306,7 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
     int *blk_m = blk_g + W4_MAX_BLOCKS;
     uint8_t *blk_rows = reinterpret_cast<uint8_t *>(blk_m + W4_MAX_BLOCKS);
     int *scan_scratch = reinterpret_cast<int *>(blk_rows + W4_MAX_BLOCKS);
+    int *xpose = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(bars) + W4_BAR_BYTES + W4_SCHED_BYTES);
     static_assert(W4_MAX_BLOCKS % 4 == 0, "scratch alignment");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -712,13 +714,43 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
             const int f1 = gu ? -1 : ti.n0 + 128 + ch;
             if (p.out_i32) {
                 // W4A8: the fp32 sums hold integers of magnitude <= 2^24 (a K
-                // chunk is at most 16384 long), so the conversion is exact
+                // chunk is at most 16384 long), so the conversion is exact.
+                // Transposed results (Ct[n, m], 8 or more rows) go through a
+                // per-warp shared-memory transpose so that each store or atomic
+                // instruction covers runs of 16 consecutive m.
+                const bool xposed = p.ld_row == 1 && p.ld_col >= 8;
+                int *xt = xpose + (warp - 2) * (32 * 17);
 #pragma unroll 1
                 for (int j0 = 0; j0 < np; j0 += 16) {
                     uint32_t a[16], b[16];
                     tmem_ld16(t_row + j0, a);
                     tmem_ld16(t_row + np + j0, b);
                     tmem_ld_wait();
+                    if (xposed) {
+#pragma unroll
+                        for (int hsel = 0; hsel < 2; ++hsel) {
+                            __syncwarp();
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj)
+                                xt[lane * 17 + jj] = __float2int_rn(__uint_as_float(hsel ? b[jj] : a[jj]));
+                            __syncwarp();
+                            const int jj = lane & 15, j = j0 + jj;
+#pragma unroll 4
+                            for (int i = 0; i < 16; ++i) {
+                                const int c = 2 * i + (lane >> 4);  // channel within the warp's 32
+                                const int n = ti.n0 + hsel * 128 + q * 32 + c;
+                                if (j < rows && n < N) {
+                                    int32_t *o = p.out_i32 + (ti.m_start + j) + static_cast<int64_t>(n) * p.ld_col;
+                                    const int v = xt[c * 17 + jj];
+                                    if (p.atomic_out)
+                                        atomicAdd(o, v);
+                                    else
+                                        *o = v;
+                                }
+                            }
+                        }
+                        continue;
+                    }
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
                         const int j = j0 + jj;
@@ -890,9 +922,15 @@ namespace {
 // fp16 rows; every int8 value is exact in fp16.  A row index outside
 // [0, T) is reported on err and its row written as zeros.
 __global__ void w4a8_rows_kernel(const int8_t *__restrict__ x, const int32_t *__restrict__ idx, int64_t T,
-                                 int64_t n_rows, int64_t K, __half *__restrict__ out, int32_t *err) {
+                                 int64_t n_rows, int64_t K, __half *__restrict__ out, int32_t *err,
+                                 int32_t *zero_a, int64_t n_a, int32_t *zero_b, int64_t n_b) {
     griddep_wait();
     griddep_launch_dependents();
+    // the GEMM's counters and, when it adds K chunks, its output start at zero
+    const int64_t tid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = tid; i < n_a; i += nthr) zero_a[i] = 0;
+    for (int64_t i = tid; i < n_b; i += nthr) zero_b[i] = 0;
     const int64_t per_row = K / 16;
     const int64_t total = n_rows * per_row;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -952,17 +990,12 @@ cudaError_t launch_gemm_w4a8(const int8_t *x, const int32_t *gather_idx, int64_t
     if (dense_rows > W4_TOK_ROWS || K % W4_BK != 0) return cudaErrorInvalidValue;
     const int64_t blocks = dense_rows > 0 ? 1 : m_blocks;
     const W4a8Plan pl = w4a8_plan(blocks, N, K);
-    cudaError_t e = cudaMemsetAsync(counters, 0, static_cast<size_t>(blocks + 1) * 4, stream);
-    if (e != cudaSuccess) return e;
-    if (pl.ksplit > 1) {
-        e = cudaMemsetAsync(out, 0, static_cast<size_t>(out_elems) * 4, stream);
-        if (e != cudaSuccess) return e;
-    }
     {
-        const int64_t work = n_rows * (K / 16);
-        const int64_t nb = std::min<int64_t>((work + 255) / 256, 4LL * device_sm_count());
-        e = launch_pdl(w4a8_rows_kernel, dim3(static_cast<unsigned>(nb)), dim3(256), 0, stream, x, gather_idx,
-                       T, n_rows, K, static_cast<__half *>(rows_f16), err);
+        const int64_t work = std::max<int64_t>(n_rows * (K / 16), pl.ksplit > 1 ? out_elems : 0);
+        const int64_t nb = std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, 4LL * device_sm_count()));
+        const cudaError_t e = launch_pdl(w4a8_rows_kernel, dim3(static_cast<unsigned>(nb)), dim3(256), 0, stream,
+                                         x, gather_idx, T, n_rows, K, static_cast<__half *>(rows_f16), err,
+                                         counters, blocks + 1, out, pl.ksplit > 1 ? out_elems : int64_t(0));
         if (e != cudaSuccess) return e;
     }
     CUtensorMap maps[2];

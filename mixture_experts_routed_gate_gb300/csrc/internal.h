@@ -139,8 +139,8 @@ cudaError_t launch_grouped_mlp_w4(int dtype, const void *x, const int32_t *gathe
 // (several, integer atomics) its int32 results at m * ld_row + n * ld_col.
 // dense_rows > 0: one block of that many rows (<= 64) and weight 0, no
 // tables; otherwise the dispatch tables (every block <= 64 rows).
-// counters: (blocks + 1) int32, zeroed here; out (out_elems int32) zeroed
-// here when K is split.  K % 64 == 0.
+// counters: (blocks + 1) int32 and, when K is split, out (out_elems int32)
+// are zeroed by the row kernel, ahead of the GEMM.  K % 64 == 0.
 constexpr int64_t kW4a8MaxChunkSub = 256;
 struct W4a8Plan {
     int64_t ksplit = 1, kchunk = 1;  // K chunks per tile and their sub-steps
