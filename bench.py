@@ -673,6 +673,15 @@ def run_only(args):
         n_valid = int((r["pos"] >= 0).sum().item())
         info = {"workload": f"{c.name}: T={c.T} K={c.K} H={c.H} bf16",
                 "bytes": roofline.reduce_bytes(n_valid, c.T, c.K, c.H, 2, 2)}
+    elif args.only.startswith("w4a8-"):
+        M, N, K = workloads.W4A8_SHAPES[args.only[len("w4a8-"):]]
+        d = workloads.make_w4a8_inputs(M, N, K, seed=1, device=dev)
+        bp = binding.moe_pack_int4_weights(d["b"], 256)
+        ct = torch.empty((N, M), dtype=torch.int32, device=dev)
+        ws = torch.empty(int(binding.lib().moe_gemm_w4a8_workspace_bytes(M, K)), dtype=torch.uint8, device=dev)
+        def fn():
+            binding.moe_gemm_w4a8(d["a"], bp, N, out=ct, ws=ws)
+        info = {"workload": f"W4A8 GEMM M={M} N={N} K={K}", "bytes": N * K // 2 + M * K + 4 * N * M}
     elif args.only == "gate_topk":
         base = workloads.MOE_CONFIGS[args.workload]
         T = args.tokens or base.T
@@ -915,7 +924,7 @@ def main():
     ap.add_argument("--no-sub", action="store_true", help="skip the decode sub-record")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time per workload")
     ap.add_argument("--only", default=None,
-                    choices=ONLY_STAGES + ["reduce-512", "reduce-4096"],
+                    choices=ONLY_STAGES + ["reduce-512", "reduce-4096"] + ["w4a8-" + n for n in workloads.W4A8_SHAPES],
                     help="time one stage alone (profiling aid; not the benchmark line)")
     ap.add_argument("--experts", type=int, default=None, help="with --only: expert count override")
     ap.add_argument("--tokens", type=int, default=None, help="with --only: token count override")
