@@ -293,8 +293,11 @@ MOE_API moe_status_t moe_pack_int4_weights(const uint8_t *plain, int64_t E, int6
                                    int64_t tile_rows, uint8_t *packed, moe_stream_t stream);
 
 /*
- * Both expert stages in one launch with int4 weights, for 1 <= T <= 64
- * tokens (every expert then holds at most 64 rows):
+ * Both expert stages in one launch with int4 weights, for any T >= 1
+ * (the kernel works on units of at most 64 rows: a 128-row block of the
+ * tables with more rows is two units; it is built for decode-sized T,
+ * where the weight bytes are the cost, and unpacks each weight tile once
+ * per unit, so large T is correct but slow):
  *   stage 1: G = (A q_gate[g]^T) * s_gate[g], U = (A q_up[g]^T) * s_up[g],
  *            h = rt(silu(G) * U)       (A: rows of x gathered by sorted_token_idx)
  *   stage 2: y = rt((h q_down[g]^T) * s_down[g] (* row_weights))
@@ -339,9 +342,8 @@ MOE_API moe_status_t moe_grouped_mlp_w4a16(const void *x, const int32_t *sorted_
  * moe_grouped_gemm_w4a8: the same per routed row over the dispatch tables
  * (the block walk of moe_routed_kernel): C[r, n] = sum_k x[i_r, k] *
  * int4(B[g])[n, k] with g the expert of row r and i_r = sorted_token_idx[r]
- * (NULL: i_r = r, n_rows <= T).  x int8 [T, K], 1 <= T <= 64 (so an expert
- * holds at most 64 rows; a block with more is reported on err_flag and its
- * rows past 64 are not written), B [E, N, K] packed with tile_rows 256,
+ * (NULL: i_r = r, n_rows <= T).  x int8 [T, K], T >= 1 (64-row units as
+ * moe_grouped_mlp_w4a16), B [E, N, K] packed with tile_rows 256,
  * C int32 [n_rows, N].  A sorted_token_idx entry outside [0, T) is reported
  * on err_flag (MOE_ERR_DEVICE_FLAG) and its row of C summed from zeros.
  * ws: moe_grouped_gemm_w4a8_workspace_bytes(n_rows, K, m_blocks) bytes.
@@ -421,9 +423,11 @@ MOE_API moe_status_t moe_forward(const void *x, const void *w_g, const float *bi
                          size_t ws_bytes, void *out, int32_t *err_flag, moe_stream_t stream);
 
 /*
- * moe_forward with int4 experts (moe_grouped_mlp_w4a16 as the expert MLP),
- * for 1 <= T <= 64 tokens; the gate weight w_g stays in `dtype`.  Same
- * workspace (moe_forward_workspace_bytes) and outputs as moe_forward.
+ * moe_forward with int4 experts (moe_grouped_mlp_w4a16 as the expert MLP,
+ * which gathers its rows from x), for T >= 1 tokens with at most 1088
+ * M blocks (else MOE_ERR_UNSUPPORTED); the gate weight w_g stays in
+ * `dtype`.  Same workspace (moe_forward_workspace_bytes) and outputs as
+ * moe_forward.
  */
 MOE_API moe_status_t moe_forward_w4a16(const void *x, const void *w_g, const float *bias,
                                const uint8_t *q_gate, const uint8_t *q_up, const uint8_t *q_down,

@@ -436,7 +436,7 @@ def _scale(t, name, shape):
 
 def moe_grouped_mlp_w4a16(x, sorted_token_idx, experts: "Int4Experts", tables, row_weights=None, h=None,
                           y=None, ready=None, err=None):
-    """Both expert stages with int4 weights, rows gathered from x [T <= 64, d_h];
+    """Both expert stages with int4 weights, rows gathered from x [T, d_h];
     returns (h, y)."""
     _cuda(x, "x", ndim=2)
     _cuda(sorted_token_idx, "sorted_token_idx", dtype=torch.int32)
@@ -498,7 +498,7 @@ def moe_gemm_w4a8(a, b_packed, N: int, out=None, ws=None, err=None):
 
 def moe_grouped_gemm_w4a8(x, sorted_token_idx, b_packed, tables, N: int, E: int, n_rows=None, out=None,
                           ws=None, err=None):
-    """Grouped W4A8 over the dispatch tables: x int8 [T <= 64, K], rows
+    """Grouped W4A8 over the dispatch tables: x int8 [T, K], rows
     x[sorted_token_idx[r]] (None: x's own rows), b_packed the [E, N, K] weight
     packed with tile_rows 256; returns C int32 [n_rows, N]."""
     _cuda(x, "x", dtype=torch.int8, ndim=2)
@@ -530,7 +530,7 @@ def moe_grouped_gemm_w4a8(x, sorted_token_idx, b_packed, tables, N: int, E: int,
 
 
 def moe_forward_w4a16(x, w_g, bias, experts: "Int4Experts", k: int, ws=None, out=None, err=None):
-    """The routed forward with int4 experts for up to 64 tokens; returns out [T, d_hidden]."""
+    """The routed forward with int4 experts; returns out [T, d_hidden]."""
     _cuda(x, "x", ndim=2)
     _cuda(w_g, "w_g", dtype=x.dtype)
     if bias is not None:

@@ -388,7 +388,7 @@ static moe_status_t grouped_mlp_w4(const void *x, const int32_t *sorted_token_id
                                    int32_t *err_flag, moe_stream_t stream, bool zero_ready) {
     if (!is_half_type(dtype)) return MOE_ERR_UNSUPPORTED;
     if (d_h <= 0 || d_e <= 0 || d_h % 64 != 0 || d_e % 64 != 0) return MOE_ERR_INVALID_ARG;
-    if (T <= 0 || T > 64) return MOE_ERR_INVALID_ARG;
+    if (T <= 0) return MOE_ERR_INVALID_ARG;
     if (n_rows == 0) return MOE_OK;
     moe_status_t st = check_gemm_tables(group_sizes, group_offsets, group_padded_offsets,
                                         group_idx_for_bx, m_blocks, n_rows, E);
@@ -467,7 +467,6 @@ moe_status_t moe_grouped_gemm_w4a8(const int8_t *x, const int32_t *sorted_token_
                                    int32_t *C, void *ws, int64_t ws_bytes, int32_t *err_flag,
                                    moe_stream_t stream) {
     if (T < 1 || N < 1 || !w4a8_k_ok(K) || N > (int64_t(1) << 24)) return MOE_ERR_INVALID_ARG;
-    if (T > 64) return MOE_ERR_UNSUPPORTED;
     if (n_rows == 0) return MOE_OK;
     if (!sorted_token_idx && n_rows > T) return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_gemm_tables(group_sizes, group_offsets, group_padded_offsets, group_idx_for_bx,
@@ -599,10 +598,11 @@ moe_status_t moe_forward_w4a16(const void *x, const void *w_g, const float *bias
                                moe_dtype_t dtype, void *ws, size_t ws_bytes, void *out,
                                int32_t *err_flag, moe_stream_t stream) {
     if (!is_half_type(dtype)) return MOE_ERR_UNSUPPORTED;
-    if (T < 0 || T > 64 || d_h <= 0 || d_e <= 0 || E <= 0 || k <= 0 || k > E || k > 32 || E > 1024)
+    if (T < 0 || d_h <= 0 || d_e <= 0 || E <= 0 || k <= 0 || k > E || k > 32 || E > 1024)
         return MOE_ERR_INVALID_ARG;
     if (d_h % 256 != 0 || d_e % 64 != 0) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
+    if (m_blocks_of(T, k, E, MOE_BLOCK_M) > 1088) return MOE_ERR_UNSUPPORTED;
     if (!x || !w_g || !q_gate || !q_up || !q_down || !out || !ws) return MOE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w_g)) return MOE_ERR_INVALID_ARG;

@@ -1,7 +1,8 @@
 // grouped_gemm_w4.cu -- the expert MLP (both GEMM stages in one launch) with
-// int4 weights and 16-bit activations (weight-only W4A16), for up to 64
-// tokens, where the expert weights are read once per step and their bytes
-// are the whole cost.
+// int4 weights and 16-bit activations (weight-only W4A16), built for decode
+// (blocks of up to 64 rows, where the expert weights are read once per step
+// and their bytes are the whole cost; larger blocks are split into 64-row
+// units), and the W4A8 GEMM on the same machinery.
 //
 // Weight format (TileLang tutorial ch.18 skeletons.py, w4a8_dequant_gemm):
 // int4 values two per byte, element j of a row in byte j/2 at nibble j%2
@@ -79,7 +80,9 @@ static_assert(W4_A_COL0 + W4_CONVS * W4_A_COLS <= W4_TMEM_COLS && 2 * W4_ACC_COL
 static_assert(W4_STAGES > W4_CONVS, "a stage is released W4_CONVS steps after its use");
 constexpr int W4_MAX_BLOCKS = 1088;              // M blocks the schedule lists
 constexpr int W4_BAR_BYTES = 512;
-constexpr int W4_SCHED_BYTES = W4_MAX_BLOCKS * (4 * 3 + 1) + 64 * 4;
+// the unit list (up to two 64-row units per block), then per block its
+// expert, first row and row count, then the scan's scratch
+constexpr int W4_SCHED_BYTES = W4_MAX_BLOCKS * (2 * 4 + 4 * 2 + 1) + 64 * 4;
 constexpr int W4_XPOSE_BYTES = W4_EPI_WARPS * 32 * 17 * 4;  // W4A8 epilogue: a 32 x 16 transpose per warp
 constexpr int W4_SMEM_BYTES = 1024 + W4_STAGES * W4_STAGE_BYTES + W4_BAR_BYTES + W4_SCHED_BYTES + W4_XPOSE_BYTES;
 static_assert(W4_SMEM_BYTES <= 232448, "shared memory per CTA");
@@ -147,13 +150,15 @@ struct W4Tile {
     int g, m_start, rows, n0, bx, phase, kc;
 };
 
-// Tile t of the launch: the stage-1 tiles of every listed block first, then
-// the stage-2 tiles in the same block order.
+// Tile t of the launch: the stage-1 tiles of every listed unit first, then
+// the stage-2 tiles in the same unit order.  A unit is up to 64 rows: a
+// 128-row block of the tables with more than 64 rows is two units (list
+// entry 2 bx + half), so the kernel serves any number of tokens.
 __device__ __forceinline__ W4Tile w4_tile(const W4Params &p, const int *list, const int *blk_g,
-                                          const int *blk_m, const uint8_t *blk_rows, int n_blocks,
+                                          const int *blk_m, const uint8_t *blk_rows, int n_units,
                                           int t) {
     W4Tile ti;
-    const int n0_tiles = n_blocks * p.nt0;
+    const int n0_tiles = n_units * p.nt0;
     int pos, nt;
     if (t < n0_tiles) {
         ti.phase = 0;
@@ -171,12 +176,19 @@ __device__ __forceinline__ W4Tile w4_tile(const W4Params &p, const int *list, co
         ti.kc = rem - nt * p.ksplit;
         ti.n0 = nt * 256;
     }
-    const int bx = list[pos];
+    const int e = list[pos];
+    const int bx = e >> 1, half = e & 1;
     ti.bx = bx;
     ti.g = blk_g[bx];
-    ti.m_start = blk_m[bx];
-    ti.rows = blk_rows[bx];
+    ti.m_start = blk_m[bx] + half * W4_TOK_ROWS;
+    ti.rows = min(static_cast<int>(blk_rows[bx]) - half * W4_TOK_ROWS, W4_TOK_ROWS);
     return ti;
+}
+
+// stage-1 epilogue warp-tiles that publish on block bx's counter: every
+// unit of the block, so a stage-2 tile of either unit waits for both
+__device__ __forceinline__ int w4_ready_target(const W4Params &p, const uint8_t *blk_rows, int bx) {
+    return W4_EPI_WARPS * p.nt0 * (blk_rows[bx] > W4_TOK_ROWS ? 2 : 1);
 }
 
 // 64-wide K sub-steps of a tile (its K chunk for a stage-2 tile)
@@ -302,7 +314,7 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
     volatile int *stage_flag = reinterpret_cast<volatile int *>(tid_ring + W4_TRING);
     static_assert(NBARS * 8 + 8 + 4 * W4_TRING + 4 * W4_STAGES <= W4_BAR_BYTES, "barrier area");
     int *list = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(bars) + W4_BAR_BYTES);
-    int *blk_g = list + W4_MAX_BLOCKS;
+    int *blk_g = list + 2 * W4_MAX_BLOCKS;
     int *blk_m = blk_g + W4_MAX_BLOCKS;
     uint8_t *blk_rows = reinterpret_cast<uint8_t *>(blk_m + W4_MAX_BLOCKS);
     int *scan_scratch = reinterpret_cast<int *>(blk_rows + W4_MAX_BLOCKS);
@@ -355,8 +367,8 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
     int first_tile = 0;
     if (threadIdx.x == 0) first_tile = atomicAdd(p.tile_counter, 1);
 
-    // ----- schedule: the non-empty M blocks in order, with their lookups -----
-    int n_blocks = 0;
+    // ----- schedule: the units of the non-empty M blocks in order -----
+    int n_blocks = 0;  // units
     if (p.dense_rows > 0) {  // one block: rows 0 .. dense_rows - 1, weight 0
         n_blocks = 1;
         if (threadIdx.x == 0) {
@@ -377,11 +389,13 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
             blk_g[bx] = g;
             blk_m[bx] = rel + __ldg(p.offsets + g);
             blk_rows[bx] = static_cast<uint8_t>(rows);
-            mine += rows > 0;
+            mine += (rows > 0) + (rows > W4_TOK_ROWS);
         }
         int base = w4_cta_scan(mine, scan_scratch, &n_blocks);
-        for (int bx = lo; bx < hi; ++bx)
-            if (blk_rows[bx] > 0) list[base++] = bx;
+        for (int bx = lo; bx < hi; ++bx) {
+            if (blk_rows[bx] > 0) list[base++] = 2 * bx;
+            if (blk_rows[bx] > W4_TOK_ROWS) list[base++] = 2 * bx + 1;
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -439,7 +453,8 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
             // stage 2 reads its block's h rows: all stage-1 warp-tiles stored
             if (ti.phase == 1 && p.nt0 > 0) {
                 if (lane == 0)
-                    go = counter_wait_bounded(p.ready + ti.bx, W4_EPI_WARPS * p.nt0, abort_flag, p.err) ? 1 : 0;
+                    go = counter_wait_bounded(p.ready + ti.bx, w4_ready_target(p, blk_rows, ti.bx), abort_flag,
+                                              p.err) ? 1 : 0;
                 go = __shfl_sync(0xffffffffu, go, 0);
                 if (!go) {
                     ok = false;
@@ -447,7 +462,7 @@ __global__ void __launch_bounds__(W4_THREADS, 1)
                 }
             }
             int np = (ti.rows + 15) & ~15;
-            if (np > W4_TOK_ROWS) {  // the host admits at most 64 tokens
+            if (np > W4_TOK_ROWS) {  // units hold at most 64 rows
                 np = W4_TOK_ROWS;
                 if (lane == 0 && p.err) atomicExch(p.err, kErrDeviceFlag);
             }

@@ -120,8 +120,9 @@ cudaError_t launch_pack_int4(const uint8_t *plain, int64_t E, int64_t N, int64_t
                              cudaStream_t stream);
 // Both expert stages with int4 weights (tiled by launch_pack_int4) and
 // optional fp32 scales per output channel; stage-1 rows gathered from x
-// [T, d_h] by gather_idx (T <= 64, so every block has at most 64 rows);
-// `ready` (m_blocks + 1 int32) zero at kernel start.
+// [T, d_h] by gather_idx; the kernel works on units of at most 64 rows (a
+// block with more rows is two units); `ready` (m_blocks + 1 int32) zero at
+// kernel start.
 cudaError_t launch_grouped_mlp_w4(int dtype, const void *x, const int32_t *gather_idx, int64_t T,
                                   const uint8_t *q_gate, const uint8_t *q_up, const uint8_t *q_down,
                                   const float *s_gate, const float *s_up, const float *s_down,
@@ -138,7 +139,7 @@ cudaError_t launch_grouped_mlp_w4(int dtype, const void *x, const int32_t *gathe
 // integer of magnitude <= 1024 * 16384 = 2^24) and stores (one chunk) or adds
 // (several, integer atomics) its int32 results at m * ld_row + n * ld_col.
 // dense_rows > 0: one block of that many rows (<= 64) and weight 0, no
-// tables; otherwise the dispatch tables (every block <= 64 rows).
+// tables; otherwise the dispatch tables (64-row units as the expert MLP).
 // counters: (blocks + 1) int32 and, when K is split, out (out_elems int32)
 // are zeroed by the row kernel, ahead of the GEMM.  K % 64 == 0.
 constexpr int64_t kW4a8MaxChunkSub = 256;

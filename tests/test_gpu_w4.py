@@ -82,12 +82,15 @@ def _w4_case(dtype, T, k, E, d_h, d_e, skew, seed, scaled):
 @pytest.mark.parametrize("T,k,E,d_h,d_e,skew", [(64, 6, 64, 512, 256, False),
                                                 (33, 4, 8, 256, 192, True),
                                                 (1, 1, 4, 256, 64, False),
-                                                (64, 8, 16, 256, 128, True)])
+                                                (64, 8, 16, 256, 128, True),
+                                                (300, 2, 3, 512, 128, False),   # 200-row experts
+                                                (200, 4, 8, 256, 192, True)])   # 65..128-row blocks
 def test_w4_mlp_vs_oracle(oracle, dtype, scaled, T, k, E, d_h, d_e, skew):
     """Stage 1 against the oracle; stage 2 against the oracle fed the
     kernel's h (isolates stage 2).  Ragged row counts, a partial N tile
     (d_e = 192), a single token, experts with up to 64 rows, empty experts,
-    with and without per-channel scales."""
+    experts of more than 64 rows (128-row blocks split into two 64-row
+    units, and ragged last blocks), with and without per-channel scales."""
     dev = require_cuda()
     rng, idx, x, qg, qu, qd, sg, su, sd = _w4_case(dtype, T, k, E, d_h, d_e, skew, 50 + T + E, scaled)
     if not scaled:
@@ -180,6 +183,49 @@ def test_w4_forward_decode_size_vs_oracle(oracle):
     assert_close(bits(out), out_ref, "f16", *MOE_TOL["f16"], "int4 forward out")
 
 
+@pytest.mark.parametrize("T,d_h,d_e,E,k", [(300, 256, 128, 8, 2), (1030, 512, 256, 16, 4)])
+def test_w4_forward_beyond_64_tokens_vs_oracle(oracle, T, d_h, d_e, E, k):
+    """The int4 forward past the decode sizes: experts of 75..260 rows, so
+    full 128-row blocks split into two 64-row units and ragged last blocks;
+    at T = 1030 the gate takes its tensor-core path.  Routing and tables
+    bit-exact, the output within the MoE tolerance of the oracle."""
+    dev = require_cuda()
+    cfg = workloads.MoEConfig("w4-big", 1, T, d_h, d_e, E, k, "f16", 60 + T)
+    d = workloads.make_moe_inputs(cfg, device=dev, with_experts=False)
+    rng = np.random.default_rng(T)
+    qg = rng.integers(-8, 8, (E, d_e, d_h)).astype(np.int8)
+    qu = rng.integers(-8, 8, (E, d_e, d_h)).astype(np.int8)
+    qd = rng.integers(-8, 8, (E, d_h, d_e)).astype(np.int8)
+    sg = (rng.uniform(0.5, 1.5, (E, d_e)) / (8 * np.sqrt(d_h))).astype(np.float32)
+    su = (rng.uniform(0.5, 1.5, (E, d_e)) / (8 * np.sqrt(d_h))).astype(np.float32)
+    sd = (rng.uniform(0.5, 1.5, (E, d_h)) / (8 * np.sqrt(d_e))).astype(np.float32)
+    pg, pu, pd = _pack_pages(qg), _pack_pages(qu), _pack_pages(qd)
+    ex = _experts(dev, qg, qu, qd, sg, su, sd)
+    ws = torch.empty(binding.forward_workspace_bytes(T, d_h, d_e, E, k, d["x"].dtype), dtype=torch.uint8,
+                     device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = binding.moe_forward_w4a16(d["x"], d["wg"], d["bias"], ex, k, ws=ws, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    v = binding.forward_workspace_views(ws, T, d_h, d_e, E, k, d["x"].dtype)
+    xb, wgb = bits(d["x"]), bits(d["wg"])
+    idx, w = oracle.gate_topk(xb, wgb, None, k, "f16")
+    assert np.array_equal(v["topk_idx"].cpu().numpy(), idx)
+    tab = oracle.build_dispatch(idx, w, E, 128)
+    assert tab["group_sizes"].max() > 64
+    for name in ("group_sizes", "group_offsets", "group_padded_offsets", "group_idx_for_bx",
+                 "sorted_token_idx"):
+        assert_bits_equal(v[name].cpu().numpy().reshape(-1), tab[name].reshape(-1), name)
+    a = oracle.gather_rows(xb, tab["sorted_token_idx"], "f16")
+    h_ref = oracle.grouped_gate_up_silu_w4(a, pg, pu, tab, "f16", s_gate=sg, s_up=su)
+    assert_close(bits(v["h"]), h_ref, "f16", *MOE_TOL["f16"], "int4 h")
+    y_ref = oracle.grouped_down_w4(bits(v["h"]), pd, tab, "f16", s_down=sd)
+    assert_close(bits(v["y"]), y_ref, "f16", *MOE_TOL["f16"], "int4 y (from the kernel's h)")
+    y_full = oracle.grouped_down_w4(h_ref, pd, tab, "f16", s_down=sd)
+    out_ref, _ = oracle.reduce_fused(y_full, tab["token_topk_to_pos"].reshape(T, k), w, "f16", "f16")
+    assert_close(bits(out), out_ref, "f16", *MOE_TOL["f16"], "int4 forward out")
+
+
 def test_w4_argument_errors():
     dev = require_cuda()
     from oracle import oracle
@@ -189,8 +235,8 @@ def test_w4_argument_errors():
     x = torch.zeros((T, 256), dtype=torch.float16, device=dev)
     z = np.zeros((E, 64, 256), np.int8)
     ex = _experts(dev, z, z, np.zeros((E, 256, 64), np.int8), None, None, None)
-    with pytest.raises(binding.MoEError):  # more than 64 tokens
-        binding.moe_grouped_mlp_w4a16(x, tab["sorted_token_idx"], ex, tab)
+    with pytest.raises(binding.MoEError):  # a dtype the int4 kernel does not run
+        binding.moe_grouped_mlp_w4a16(x.float(), tab["sorted_token_idx"], ex, tab)
     with pytest.raises(ValueError):  # wrong scale shape
         binding.Int4Experts(*[torch.zeros((E, 64, 128), dtype=torch.uint8, device=dev)] * 2,
                             torch.zeros((E, 256, 32), dtype=torch.uint8, device=dev),

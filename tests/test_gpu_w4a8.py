@@ -71,7 +71,8 @@ def _routing(rng, T, k, E, skew):
 @pytest.mark.parametrize("T,k,E,N,K,skew", [(64, 6, 64, 2048, 768, False),   # decode stage-2 shape
                                             (64, 6, 64, 768, 2048, True),    # decode stage-1 shape, skewed
                                             (7, 2, 5, 300, 128, False),      # ragged N, empty experts
-                                            (64, 8, 16, 256, 18944, False)])  # K split into chunks
+                                            (64, 8, 16, 256, 18944, False),  # K split into chunks
+                                            (300, 4, 6, 512, 256, True)])     # 64-row units of larger blocks
 def test_grouped_gemm_w4a8_matches_oracle(oracle, T, k, E, N, K, skew):
     """Rows gathered from x by sorted_token_idx, every routed row against the
     oracle's block walk over the same tables, bit for bit."""
