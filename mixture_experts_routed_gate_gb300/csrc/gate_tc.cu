@@ -13,7 +13,7 @@
 //      (partials [S, T, E]); the otherwise idle epilogue warps also compute
 //      |w_e|_2 for every gate row and, from the token tiles in shared memory,
 //      each split's share of |x_t|^2.
-//   2. gate_select_kernel, one CTA per token: sums the partials in a fixed
+//   2. gate_select_kernel, one warp per token: sums the partials in a fixed
 //      order, bounds |logit~ - logit| <= delta(t, e) from |x_t|_2 |w_e|_2
 //      (Cauchy-Schwarz on sum |x_j w_j|) and the rounding depth of both
 //      orders, and keeps as candidates every expert whose upper bound reaches
@@ -52,7 +52,9 @@ constexpr int GT_A_BYTES = GT_BM * GT_BK * 2;
 constexpr int GT_B_BYTES = GT_BN * GT_BK * 2;
 constexpr int GT_SMEM = 1024 + GT_STAGES * (GT_A_BYTES + GT_B_BYTES) + 256;
 constexpr int GT_MAX_SPLITS = 8;
-constexpr int SEL_WARPS = 4;     // warps of a select CTA (one token)
+constexpr int SEL_WARPS = 4;     // warps (tokens) of a select CTA
+constexpr int SEL_G = 4;         // candidates recomputed together by a warp
+constexpr int SEL_U = 4;         // chunks per lane whose loads are in flight together
 
 struct GateTcParams {
     float *part;           // [S, T, E] fp32 partial logits (no bias)
@@ -300,13 +302,14 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     }
 }
 
-// One CTA of SEL_WARPS warps per token: warp 0 finds the candidates while the
-// other warps stage the token's row of x in shared memory; then all warps
-// recompute the candidates in the fixed order (two per pass of a warp), and
-// warp 0 selects the top-k and the weights.  Shared memory: the row of x
-// (d_h 16-bit values); per expert its logit (tensor-core value, replaced by
-// the fixed-order value for candidates); the candidate ids and their
-// fixed-order logits; the candidate count.
+// One warp per token, SEL_WARPS tokens per CTA.  The warp sums the partials
+// in split order, forms the bounds and the candidate list, recomputes every
+// candidate in the fixed order (SEL_G candidates at a time: lane L runs one
+// accumulator chain per candidate over its chunks c = L, L + 32, ... in
+// ascending order, the chains interleaved, SEL_U chunks' loads in flight),
+// then selects the top-k and forms the weights.  Shared memory per warp: per
+// expert its logit (the tensor-core value, replaced by the fixed-order value
+// for candidates), the candidate ids and their fixed-order logits.
 template <int DT, int SLOTS>
 __global__ void __launch_bounds__(SEL_WARPS * 32)
     gate_select_kernel(const uint8_t *__restrict__ x, const uint8_t *__restrict__ wg,
@@ -316,30 +319,17 @@ __global__ void __launch_bounds__(SEL_WARPS * 32)
                        int32_t *__restrict__ topk_idx, float *__restrict__ topk_w) {
     extern __shared__ __align__(16) uint8_t sel_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint4 *xs = reinterpret_cast<uint4 *>(sel_smem);
-    float *val = reinterpret_cast<float *>(sel_smem + d_h * 2);
+    float *val = reinterpret_cast<float *>(sel_smem) + static_cast<int64_t>(warp) * 3 * E;
     int *cand_id = reinterpret_cast<int *>(val + E);
     float *cand_val = reinterpret_cast<float *>(cand_id + E);
-    int *n_cand = reinterpret_cast<int *>(cand_val + E);
-    const int t = blockIdx.x;
+    const int t = blockIdx.x * SEL_WARPS + warp;
     const int chunks = d_h / 8;
     griddep_wait();  // partials and norms come from gate_tc_kernel
     griddep_launch_dependents();
+    if (t >= T) return;
 
-    if (warp != 0) {
-        // the token's row into shared memory, every load issued first
-        const uint4 *xrow = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t) * d_h * 2);
-        const int tid = threadIdx.x - 32, nthr = (SEL_WARPS - 1) * 32;
-        for (int cb = tid; cb < chunks; cb += nthr * 10) {
-            uint4 v[10];
-#pragma unroll
-            for (int u = 0; u < 10; ++u)
-                if (cb + nthr * u < chunks) v[u] = __ldg(xrow + cb + nthr * u);
-#pragma unroll
-            for (int u = 0; u < 10; ++u)
-                if (cb + nthr * u < chunks) xs[cb + nthr * u] = v[u];
-        }
-    } else {
+    int n = 0;  // candidates (warp-uniform)
+    {
         float xv[8];
 #pragma unroll
         for (int sp = 0; sp < 8; ++sp) xv[sp] = sp < S ? xss[static_cast<int64_t>(sp) * T + t] : 0.0f;
@@ -409,7 +399,6 @@ __global__ void __launch_bounds__(SEL_WARPS * 32)
             }
         }
         // candidates, in ascending expert id
-        int n = 0;
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s) {
             const int e = s * 32 + lane;
@@ -418,74 +407,67 @@ __global__ void __launch_bounds__(SEL_WARPS * 32)
             if (c) cand_id[n + __popc(m & ((1u << lane) - 1u))] = e;
             n += __popc(m);
         }
-        if (lane == 0) *n_cand = n;
     }
-    __syncthreads();
-    const int n = *n_cand;
+    __syncwarp();
 
-    // fixed-order logits of the candidates, two per pass of a warp: lane L sums
-    // its chunks c = L, L + 32, ... in ascending order (seven chunks' loads in
-    // flight at a time), then the xor butterfly
-    constexpr int U = 7;
-    for (int i0 = 2 * warp; i0 < n; i0 += 2 * SEL_WARPS) {
-        const int ng = min(2, n - i0);
-        const int e0 = cand_id[i0], e1 = cand_id[i0 + (ng > 1 ? 1 : 0)];
-        const uint4 *w0 = reinterpret_cast<const uint4 *>(wg + static_cast<int64_t>(e0) * d_h * 2);
-        const uint4 *w1 = reinterpret_cast<const uint4 *>(wg + static_cast<int64_t>(e1) * d_h * 2);
-        float acc0 = 0.0f, acc1 = 0.0f;
-        for (int cb = lane; cb < chunks; cb += 32 * U) {
-            uint4 a[U], b[U];
+    // fixed-order logits of the candidates, SEL_G at a time
+    const uint4 *xrow = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t) * d_h * 2);
+    const uint4 *wbase = reinterpret_cast<const uint4 *>(wg);
+    for (int i0 = 0; i0 < n; i0 += SEL_G) {
+        const int ng = min(SEL_G, n - i0);
+        int off[SEL_G];
+        float acc[SEL_G];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+        for (int g = 0; g < SEL_G; ++g) {
+            off[g] = cand_id[i0 + (g < ng ? g : 0)] * chunks;
+            acc[g] = 0.0f;
+        }
+        for (int cb = lane; cb < chunks; cb += 32 * SEL_U) {
+            uint4 xv[SEL_U], wv[SEL_U][SEL_G];
+#pragma unroll
+            for (int u = 0; u < SEL_U; ++u) {
                 const int c = cb + 32 * u;
                 if (c < chunks) {
-                    a[u] = __ldg(w0 + c);
-                    if (ng > 1) b[u] = __ldg(w1 + c);
+                    xv[u] = __ldg(xrow + c);
+#pragma unroll
+                    for (int g = 0; g < SEL_G; ++g)
+                        if (g < ng) wv[u][g] = __ldg(wbase + off[g] + c);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+            for (int u = 0; u < SEL_U; ++u) {
                 const int c = cb + 32 * u;
                 if (c < chunks) {
-                    const uint4 xv = xs[c];
-                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                    const uint32_t aw[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+                    const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        acc0 = fma_mixed<DT, false>(xw[q], aw[q], acc0);
-                        acc0 = fma_mixed<DT, true>(xw[q], aw[q], acc0);
-                    }
-                    if (ng > 1) {
-                        const uint32_t bw[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+                    for (int g = 0; g < SEL_G; ++g) {
+                        if (g < ng) {
+                            const uint32_t aw[4] = {wv[u][g].x, wv[u][g].y, wv[u][g].z, wv[u][g].w};
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            acc1 = fma_mixed<DT, false>(xw[q], bw[q], acc1);
-                            acc1 = fma_mixed<DT, true>(xw[q], bw[q], acc1);
+                            for (int q = 0; q < 4; ++q) {
+                                acc[g] = fma_mixed<DT, false>(xw[q], aw[q], acc[g]);
+                                acc[g] = fma_mixed<DT, true>(xw[q], aw[q], acc[g]);
+                            }
                         }
                     }
                 }
             }
         }
 #pragma unroll
-        for (int sh = 16; sh >= 1; sh >>= 1) {
-            acc0 = acc0 + __shfl_xor_sync(0xffffffffu, acc0, sh);
-            acc1 = acc1 + __shfl_xor_sync(0xffffffffu, acc1, sh);
-        }
-        if (bias) {
-            acc0 = acc0 + bias[e0];
-            acc1 = acc1 + bias[e1];
-        }
-        if (lane == 0) {
-            cand_val[i0] = acc0;
-            val[e0] = acc0;
-            if (ng > 1) {
-                cand_val[i0 + 1] = acc1;
-                val[e1] = acc1;
+        for (int g = 0; g < SEL_G; ++g) {
+#pragma unroll
+            for (int sh = 16; sh >= 1; sh >>= 1) acc[g] = acc[g] + __shfl_xor_sync(0xffffffffu, acc[g], sh);
+            if (g < ng) {
+                const int e = off[g] / chunks;
+                if (bias) acc[g] = acc[g] + bias[e];
+                if (lane == 0) {
+                    cand_val[i0 + g] = acc[g];
+                    val[e] = acc[g];
+                }
             }
         }
     }
-    __syncthreads();
-    if (warp != 0) return;
+    __syncwarp();
 
     // top-k among the candidates by (logit desc, id asc); lane j keeps slot j
     unsigned taken = 0;  // bit i: candidate lane + 32 i already selected
@@ -543,7 +525,8 @@ __global__ void __launch_bounds__(SEL_WARPS * 32)
 }
 
 size_t select_smem_bytes(int64_t d_h, int64_t E) {
-    return static_cast<size_t>(d_h * 2 + E * 12 + 16);
+    (void)d_h;
+    return static_cast<size_t>(SEL_WARPS * E * 12);
 }
 
 int splits_for(int64_t T, int64_t E) {
@@ -614,7 +597,7 @@ cudaError_t launch_typed(const void *x, const void *wg, const float *bias, int64
     const double c_sum = (S + 2.0) * u;                       // partials and bias
     const double norms = (1.0 + std::ldexp(1.0, -9)) * (1.0 + std::ldexp(1.0, -9));  // fp32 norms
     const float coef = static_cast<float>(2.0 * (c_tc + c_fixed + c_sum) * norms);
-    const unsigned sel_grid = static_cast<unsigned>(T);
+    const unsigned sel_grid = static_cast<unsigned>((T + SEL_WARPS - 1) / SEL_WARPS);
 #define MOE_SEL_CASE(SL)                                                                                     \
     if (slots <= SL)                                                                                         \
         return launch_pdl(gate_select_kernel<DT, SL>, dim3(sel_grid), dim3(SEL_WARPS * 32), sel_smem, stream, \
