@@ -46,7 +46,8 @@ def test_gemm_w4a8_matches_oracle_bit_for_bit(oracle, M, N, K):
 
 @pytest.mark.parametrize("M,N,K", [(3, 38912, 16384),  # one tile per SM: one K chunk of 16384, sums 2^24
                                    (2, 512, 18944),    # sums above 2^24: several chunks added as integers
-                                   (1, 3584, 18944)])
+                                   (1, 3584, 18944),
+                                   (2, 256, 1 << 20)])  # the largest K: 64 chunks, sums up to 2^30
 def test_gemm_w4a8_extremes_are_exact(M, N, K):
     """Rows of -128 and 127 against weight rows of -8, 7 and 0: every product
     at its extreme, Ct = K * a_m * b_n in closed form (up to 1024 K)."""
