@@ -252,7 +252,9 @@ class NativeStep:
                                     p(v["sorted_token_idx"]), p(v["sorted_row_weight"]),
                                     p(v["token_topk_to_pos"]), ctypes.c_void_p(self.scratch_ptr),
                                     self.scratch_bytes, sp)),
-            "gather": (L.moe_gather_rows, (p(x), p(v["sorted_token_idx"]), Tk, T, d_h, self.code, p(v["a"]), sp)),
+            # the token-order gather moe_forward runs
+            "gather": (L.moe_gather_rows_by_token, (p(x), p(v["token_topk_to_pos"]), T, k, Tk, d_h, self.code,
+                                                    p(v["a"]), sp)),
             # the gathering form for T <= 64 (rows from x), as moe_forward does
             "expert_mlp": (L.moe_grouped_mlp, (None if T <= 64 else p(v["a"]), p(d["w_gate"]), p(d["w_up"]),
                                                p(d["w_down"]), *tables, self.mb, None, Tk, d_h, d_e, E,

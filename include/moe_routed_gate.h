@@ -204,6 +204,20 @@ MOE_API moe_status_t moe_gather_rows(const void *x, const int32_t *sorted_token_
                              moe_stream_t stream);
 
 /*
+ * The same gather in token order (what moe_forward runs): for every token t
+ * and slot j < k, a_out[token_topk_to_pos[t, j], :] = x[t, :]; a position
+ * outside [0, n_rows) (a dropped pair, -1) is skipped and rows no position
+ * names are left as they were.  With a dispatch's token_topk_to_pos (every
+ * row named exactly once) the result is moe_gather_rows' with that
+ * dispatch's sorted_token_idx, but each token's row is read from memory once
+ * instead of once per expert it went to.  token_topk_to_pos [T, k] int32,
+ * 1 <= k <= 32.  x [T, d_h]; d_h * elem_size % 16 == 0.
+ */
+MOE_API moe_status_t moe_gather_rows_by_token(const void *x, const int32_t *token_topk_to_pos, int64_t T,
+                                              int64_t k, int64_t n_rows, int64_t d_h, moe_dtype_t dtype,
+                                              void *a_out, moe_stream_t stream);
+
+/*
  * Grouped gate/up GEMM with fused SiLU (CSDN "tilelang kernel stage 1 gate+up";
  * skeletons.py moe_routed_kernel first kernel).  For each M block bx:
  *   g = group_idx_for_bx[bx]; m_start = bx*128 - group_padded_offsets[g] + group_offsets[g];
@@ -404,7 +418,7 @@ MOE_API moe_status_t moe_reduce_fused_scaled(const void *x, int64_t n_rows,
  * the layer output, and the "forward" section that composes routing, the
  * table build, the two expert kernels and the weighted combine), stream
  * ordered, no host round trip:
- *   moe_gate_topk -> moe_build_dispatch -> moe_gather_rows ->
+ *   moe_gate_topk -> moe_build_dispatch -> moe_gather_rows_by_token ->
  *   moe_grouped_mlp (stage 1 + stage 2 in one launch) -> moe_reduce_fused;
  * for T <= 64 the gather is done inside moe_grouped_mlp (its gathering form)
  * and the gathered-rows section of the workspace is left unwritten.

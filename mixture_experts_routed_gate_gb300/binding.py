@@ -60,6 +60,7 @@ def lib():
         "moe_copy": (I, [P, P, I64, P]),
         "moe_wait_flag": (I, [P, ctypes.c_int32, I64, P, P]),
         "moe_gather_rows": (I, [P, P, I64, I64, I64, I, P, P]),
+        "moe_gather_rows_by_token": (I, [P, P, I64, I64, I64, I64, I, P, P]),
         "moe_grouped_gate_up_silu": (I, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, P, P]),
         "moe_grouped_down": (I, [P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I, P, P, P]),
         "moe_grouped_mlp": (I, [P, P, P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I, P, P, P, P, P, I64, P, P]),
@@ -89,7 +90,8 @@ def exported_symbols():
             "moe_build_dispatch_workspace_bytes", "moe_forward_workspace_bytes",
             "moe_forward_workspace_offset", "moe_gate_topk", "moe_build_dispatch",
             "moe_build_dispatch_noalloc",
-            "moe_copy", "moe_wait_flag", "moe_gather_rows", "moe_grouped_gate_up_silu", "moe_grouped_down",
+            "moe_copy", "moe_wait_flag", "moe_gather_rows", "moe_gather_rows_by_token",
+            "moe_grouped_gate_up_silu", "moe_grouped_down",
             "moe_grouped_mlp", "moe_pack_int4_bytes", "moe_pack_int4_weights", "moe_grouped_mlp_w4a16",
             "moe_forward_w4a16", "moe_gemm_w4a8_workspace_bytes", "moe_gemm_w4a8",
             "moe_grouped_gemm_w4a8_workspace_bytes", "moe_grouped_gemm_w4a8", "moe_reduce_fused",
@@ -288,6 +290,26 @@ def moe_gather_rows(x, sorted_token_idx, out=None):
         _check(lib().moe_gather_rows(_ptr(x), _ptr(sorted_token_idx), n, T, d_h,
                                      _dtype_code(x, "x"), _ptr(out), _stream(x.device)),
                "moe_gather_rows")
+    return out
+
+
+def moe_gather_rows_by_token(x, token_topk_to_pos, n_rows: int, out=None):
+    """The gather in token order: out[token_topk_to_pos[t, j]] = x[t] (positions
+    outside [0, n_rows) skipped); with a dispatch's positions, moe_gather_rows'
+    result."""
+    _cuda(x, "x", ndim=2)
+    _cuda(token_topk_to_pos, "token_topk_to_pos", dtype=torch.int32, ndim=2)
+    T, d_h = x.shape
+    k = token_topk_to_pos.shape[1]
+    if token_topk_to_pos.shape[0] != T:
+        raise ValueError("token_topk_to_pos must be [T, k]")
+    if out is None:
+        out = torch.empty((n_rows, d_h), dtype=x.dtype, device=x.device)
+    _cuda(out, "out", dtype=x.dtype)
+    with torch.cuda.device(x.device):
+        _check(lib().moe_gather_rows_by_token(_ptr(x), _ptr(token_topk_to_pos), T, k, n_rows, d_h,
+                                              _dtype_code(x, "x"), _ptr(out), _stream(x.device)),
+               "moe_gather_rows_by_token")
     return out
 
 

@@ -10,7 +10,9 @@ namespace {
 
 // ---------------------------------------------------------------------------
 // gather: a_out[r, :] = x[sorted_token_idx[r], :]  (CSDN "forward", step 3)
-// One warp per row, 16-byte vectors, 4 in flight per lane.
+// One warp per row, 16-byte vectors, 4 in flight per lane; the rows are
+// stored with the evict-first hint, so the stream of output rows does not push
+// the token rows (read up to k times) out of L2.
 // ---------------------------------------------------------------------------
 constexpr int GA_WARPS = 8;
 
@@ -36,12 +38,47 @@ __global__ void __launch_bounds__(GA_WARPS * 32)
     for (; v + 96 < nvec; v += 128) {
         const uint4 a = ld_stream(src + v), b = ld_stream(src + v + 32);
         const uint4 c = ld_stream(src + v + 64), d = ld_stream(src + v + 96);
-        dst[v] = a;
-        dst[v + 32] = b;
-        dst[v + 64] = c;
-        dst[v + 96] = d;
+        __stcs(dst + v, a);
+        __stcs(dst + v + 32, b);
+        __stcs(dst + v + 64, c);
+        __stcs(dst + v + 96, d);
     }
-    for (; v < nvec; v += 32) dst[v] = ld_stream(src + v);
+    for (; v < nvec; v += 32) __stcs(dst + v, ld_stream(src + v));
+}
+
+// The same rows in token order, for the forward: token t's row is read once
+// and written to each of its rows token_topk_to_pos[t, j] (j < k <= 32; a
+// position outside [0, n_rows), a dropped pair, is skipped).  The result is
+// the row-order gather's, but x is read from memory once however many
+// experts a token went to.  One warp per token.
+__global__ void __launch_bounds__(GA_WARPS * 32)
+    scatter_rows_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ pos, int64_t T, int k,
+                        int64_t n_rows, int nvec, uint4 *__restrict__ out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * GA_WARPS + warp;
+    griddep_wait();
+    griddep_launch_dependents();
+    if (t >= T) return;
+    int p = -1;  // lane j < k: the row of slot j
+    if (lane < k) {
+        p = __ldg(pos + t * k + lane);
+        if (p >= n_rows) p = -1;
+    }
+    const uint4 *src = x + t * nvec;
+    for (int v = lane; v < nvec; v += 128) {
+        uint4 a[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (v + 32 * u < nvec) a[u] = ld_stream(src + v + 32 * u);
+        for (int j = 0; j < k; ++j) {
+            const int pj = __shfl_sync(0xffffffffu, p, j);
+            if (pj < 0) continue;
+            uint4 *dst = out + static_cast<int64_t>(pj) * nvec;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (v + 32 * u < nvec) __stcs(dst + v + 32 * u, a[u]);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -522,6 +559,17 @@ cudaError_t launch_gather_rows(const void *x, const int32_t *sorted_token_idx, i
     const int64_t blocks = (n_rows + GA_WARPS - 1) / GA_WARPS;
     return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(GA_WARPS * 32), 0,
                       stream, static_cast<const uint4 *>(x), sorted_token_idx, n_rows, nvec,
+                      static_cast<uint4 *>(a_out));
+}
+
+cudaError_t launch_scatter_rows(const void *x, const int32_t *token_topk_to_pos, int64_t T, int64_t k,
+                                int64_t n_rows, int64_t d_h, int elem_bytes, void *a_out, cudaStream_t stream) {
+    if (T <= 0 || n_rows <= 0) return cudaSuccess;
+    if (k <= 0 || k > 32) return cudaErrorInvalidValue;
+    const int nvec = static_cast<int>(d_h * elem_bytes / 16);
+    const int64_t blocks = (T + GA_WARPS - 1) / GA_WARPS;
+    return launch_pdl(scatter_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(GA_WARPS * 32), 0, stream,
+                      static_cast<const uint4 *>(x), token_topk_to_pos, T, static_cast<int>(k), n_rows, nvec,
                       static_cast<uint4 *>(a_out));
 }
 

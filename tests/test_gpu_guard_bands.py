@@ -86,9 +86,12 @@ def test_routing_dispatch_gather_stay_inside(T, d_h, E, k, dtype):
     tab2 = binding.moe_build_dispatch_noalloc(idx, w, E, out=_dispatch_out(G, T, k, E))
     a = G.empty((T * k, d_h), td, "gathered rows")
     binding.moe_gather_rows(x, tab["sorted_token_idx"], out=a)
+    a2 = G.empty((T * k, d_h), td, "rows gathered in token order")
+    binding.moe_gather_rows_by_token(x, tab["token_topk_to_pos"], T * k, out=a2)
     G.check()
     for name in tab:
         assert torch.equal(tab[name], tab2[name]), name
+    assert torch.equal(a, a2)
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])

@@ -177,6 +177,38 @@ def test_dispatch_tables_bit_exact(oracle, T, k, E, skew):
             assert_bits_equal(got, want, name)
 
 
+@pytest.mark.parametrize("T,k,E,d_h,dtype", [(4096, 8, 256, 7168, "bf16"),  # the prefill shape
+                                             (301, 3, 17, 256, "f16"),
+                                             (70, 32, 40, 512, "f32"),      # k at its limit
+                                             (5, 1, 3, 64, "bf16")])
+def test_gather_rows_by_token_bit_exact(oracle, T, k, E, d_h, dtype):
+    """The token-order gather moe_forward runs gives the row-order gather's
+    rows bit for bit: against the oracle's gather with the same dispatch's
+    sorted_token_idx; a position of -1 (a dropped pair) is skipped and a row
+    no position names keeps its contents."""
+    dev = require_cuda()
+    rng = np.random.default_rng(T + k)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    tab = oracle.build_dispatch(idx, None, E, 128)
+    td = workloads.torch_dtype(dtype)
+    x = torch.randn((T, d_h), generator=torch.Generator().manual_seed(T), dtype=torch.float32).to(td).to(dev)
+    pos = torch.from_numpy(tab["token_topk_to_pos"].reshape(T, k).copy()).to(dev)
+    a = binding.moe_gather_rows_by_token(x, pos, T * k)
+    torch.cuda.synchronize()
+    want = oracle.gather_rows(bits(x), tab["sorted_token_idx"], dtype)
+    assert_bits_equal(bits(a), want, "rows gathered in token order")
+    # drop one pair: its row is not written
+    pos[T // 2, 0] = -1
+    r_dropped = int(tab["token_topk_to_pos"].reshape(T, k)[T // 2, 0])
+    a2 = torch.zeros_like(a)
+    binding.moe_gather_rows_by_token(x, pos, T * k, out=a2)
+    torch.cuda.synchronize()
+    got = bits(a2)
+    keep = np.arange(T * k) != r_dropped
+    assert_bits_equal(got[keep], want[keep], "rows of the kept pairs")
+    assert not got[r_dropped].any()
+
+
 def test_gather_rows_bit_exact(oracle):
     dev = require_cuda()
     x = torch.randn((77, 7168), device=dev).to(torch.bfloat16)
