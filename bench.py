@@ -20,8 +20,10 @@ bf16 512 / 4096 x 8 x 7168 workloads as ``reduce_fused_bf16_x8_7168``.
 
 Prints ONE JSON line (rank 0).  ``value`` = tokens processed by all ranks /
 max-over-ranks time.  ``e2e`` = the same metric through the public
-``binding.ForwardGraph`` with pinned host input and output buffers, the
-host-to-device and device-to-host copies inside the timed region.
+``binding.ForwardPipeline``: batches of tokens in pinned host memory, every
+batch's host-to-device and device-to-host copies inside the timed region
+(overlapping the neighbouring batches' forwards); ``e2e.serial_value`` the
+same through ``binding.ForwardGraph`` one step at a time.
 ``cpu_baseline`` = the oracle's whole forward on the host cores over a
 bounded sample of the same workload (for prefill: tokens of the same batch).
 ``--impl reference`` times the CPU oracle on the host cores instead.
@@ -540,14 +542,43 @@ def measure_w4a8(dev, flush, steps: int = 100):
 
 
 def measure_e2e(args, cfg, d, dev, flush, world):
-    """The public API end to end: binding.ForwardGraph with pinned host input
-    and output buffers; each step moves the tokens host -> device (a copy
-    kernel reading the pinned buffer), runs the forward and lands the output
-    in the pinned host buffer (the combine's stores), all inside the events."""
+    """The public API end to end, two ways, both with every step's tokens
+    copied host -> device from pinned memory and its output copied back
+    inside the timed region:
+
+    * pipelined (the reported ``e2e``): binding.ForwardPipeline over K
+      batches back to back, batch i + 1's copy in and batch i - 1's copy out
+      overlapping batch i's forward (copy engines, two further streams); one
+      timed region from before the first copy in to after the last copy out.
+      No L2 eviction between batches: each batch's tokens arrive over the
+      host link and every forward reads the whole expert weight set, which is
+      larger than L2.
+    * serial: binding.ForwardGraph with host buffers (a copy kernel reading
+      the pinned tokens, the combine storing into the pinned output), one
+      step per timed region after an L2 eviction."""
     from mixture_experts_routed_gate_gb300 import binding
     T, d_h = cfg.T, cfg.d_hidden
     n_pool = 4
-    host_x = [workloads.make_tokens(cfg, T, device="cpu", seed=100 + i) for i in range(n_pool)]
+    host_x = [workloads.make_tokens(cfg, T, device="cpu", seed=100 + i).pin_memory() for i in range(n_pool)]
+    # pipelined
+    pl = binding.ForwardPipeline(d["wg"], d["bias"], d["w_gate"], d["w_up"], d["w_down"], cfg.top_k, T)
+    host_out = [torch.empty((T, d_h), dtype=host_x[0].dtype).pin_memory() for _ in range(2)]
+    for i in range(max(args.warmup, 3)):
+        pl.submit(host_x[i % n_pool], host_out[i % 2])
+    pl.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(pl.copy_in)
+    for i in range(args.steps):
+        last = pl.submit(host_x[i % n_pool], host_out[i % 2])
+    t1.record(pl.copy_out)
+    t1.synchronize()
+    pipe_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    if int(pl.err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(pl.err.item())} in the pipelined e2e region")
+    del pl
+    # serial, one step per timed region
     fg = binding.ForwardGraph(d["wg"], d["bias"], d["w_gate"], d["w_up"], d["w_down"], cfg.top_k, T,
                               host_io=True)
     stream = fg.stream
@@ -574,7 +605,7 @@ def measure_e2e(args, cfg, d, dev, flush, world):
     if int(fg.err.item()) != 0:
         raise RuntimeError(f"device error flag {int(fg.err.item())} in the e2e region")
     es = fg.x.element_size()
-    return dict(total_ms=total_ms, h2d=T * d_h * es, d2h=T * d_h * es)
+    return dict(total_ms=pipe_ms, serial_ms=total_ms, h2d=T * d_h * es, d2h=T * d_h * es)
 
 
 def measure_reduce_aux(dev, flush, reps: int = 20):
@@ -874,7 +905,14 @@ def workload_record(args, cfg, res, world, steps, cpu_budget, dev):
         "cpu_baseline": {"value": round(cpu["value"], 2), "unit": "tokens/s", "cores": threads,
                          "kind": "oracle", "sample": cpu["sample"]},
         "e2e": {"value": round(aggregate_throughput(T * steps, world, e2e["total_ms"]), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "mode": "binding.ForwardPipeline: K batches back to back from pinned host memory, each "
+                        "batch's copy in and copy out (copy engines) overlapping the neighbouring batches' "
+                        "forwards; one timed region; no L2 eviction (every forward reads the whole expert "
+                        "weight set, larger than L2, and its tokens arrive over the host link)",
+                "serial_value": round(aggregate_throughput(T * steps, world, e2e["serial_ms"]), 1),
+                "serial_mode": "binding.ForwardGraph with host buffers, one step per timed region after an "
+                               "L2 eviction"},
         "gpu_launches": kernels_per_step(cfg) * steps,
         "launch_mode": res["mode"],
         "eager_ms_per_step": round(res["eager_ms"], 5),

@@ -704,6 +704,87 @@ def moe_forward(x, w_g, bias, w_gate, w_up, w_down, k: int, ws=None, out=None, e
     return out
 
 
+class ForwardPipeline:
+    """Back-to-back forwards over a sequence of token batches that live in
+    pinned host memory, each result returned to pinned host memory.  Batch
+    i's copy in runs on one copy stream while the forward of batch i - 1 runs
+    on the compute stream, and batch i - 1's copy out on a second copy stream
+    while batch i is computed: two device token buffers and two device
+    outputs, ordered by events, each forward one replay of a CUDA graph of
+    ``moe_forward``.  Every batch crosses the host link once each way; only
+    those copies and the forwards of neighbouring batches overlap.
+
+    :meth:`submit` queues one batch and returns at once; the host must not
+    write that batch's ``x_host`` before its copy in has run, nor read its
+    ``out_host`` before the returned event has completed."""
+
+    def __init__(self, w_g, bias, w_gate, w_up, w_down, k: int, T: int):
+        dev = w_gate.device
+        dt = w_gate.dtype
+        E, d_e, d_h = w_gate.shape
+        self.params = (w_g, bias, w_gate, w_up, w_down, k)
+        self.T, self.d_h = T, d_h
+        self.x = [torch.zeros((T, d_h), dtype=dt, device=dev) for _ in range(2)]
+        self.out = [torch.empty((T, d_h), dtype=dt, device=dev) for _ in range(2)]
+        self.ws = torch.empty(forward_workspace_bytes(T, d_h, d_e, E, k, dt), dtype=torch.uint8, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.compute = torch.cuda.Stream(dev)
+        self.copy_in = torch.cuda.Stream(dev)
+        self.copy_out = torch.cuda.Stream(dev)
+        with torch.cuda.stream(self.compute):
+            for p in range(2):
+                self._body(p)  # first calls on the device outside capture (one-time set-up)
+        self.compute.synchronize()
+        self.graphs = []
+        for p in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.compute):
+                self._body(p)
+            self.graphs.append(g)
+        self.in_done = [torch.cuda.Event() for _ in range(2)]
+        self.fwd_done = [torch.cuda.Event() for _ in range(2)]
+        self.out_done = [torch.cuda.Event() for _ in range(2)]
+        self.issued = 0
+
+    def _body(self, p):
+        w_g, bias, w_gate, w_up, w_down, k = self.params
+        moe_forward(self.x[p], w_g, bias, w_gate, w_up, w_down, k, ws=self.ws, out=self.out[p], err=self.err)
+
+    def submit(self, x_host, out_host):
+        """Queue one batch: x_host and out_host pinned [T, d_hidden] host
+        tensors.  Returns the event that completes when out_host holds the
+        result."""
+        for t, name in ((x_host, "x_host"), (out_host, "out_host")):
+            if t.is_cuda or not t.is_pinned() or tuple(t.shape) != (self.T, self.d_h) or t.dtype != self.x[0].dtype:
+                raise ValueError(f"{name} must be a pinned host tensor [{self.T}, {self.d_h}] of the weights' dtype")
+        p = self.issued % 2
+        again = self.issued >= 2
+        # copy in: the device buffer is free once the forward two batches back is done
+        if again:
+            self.copy_in.wait_event(self.fwd_done[p])
+        with torch.cuda.stream(self.copy_in):
+            self.x[p].copy_(x_host, non_blocking=True)
+        self.in_done[p].record(self.copy_in)
+        # forward: its tokens are in, and its output buffer has been copied out
+        self.compute.wait_event(self.in_done[p])
+        if again:
+            self.compute.wait_event(self.out_done[p])
+        with torch.cuda.stream(self.compute):
+            self.graphs[p].replay()
+        self.fwd_done[p].record(self.compute)
+        # copy out
+        self.copy_out.wait_event(self.fwd_done[p])
+        with torch.cuda.stream(self.copy_out):
+            out_host.copy_(self.out[p], non_blocking=True)
+        self.out_done[p].record(self.copy_out)
+        self.issued += 1
+        return self.out_done[p]
+
+    def synchronize(self):
+        for s in (self.copy_in, self.compute, self.copy_out):
+            s.synchronize()
+
+
 class ForwardGraph:
     """``moe_forward`` captured once into a CUDA graph for a fixed token count,
     with static device buffers (and, with ``host_io``, pinned host buffers: a

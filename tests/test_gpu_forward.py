@@ -269,3 +269,26 @@ def _token_groups(tokens, topk_idx, max_experts):
     if cur:
         groups.append(np.array(cur))
     return groups
+
+
+def test_forward_pipeline_matches_single_forwards():
+    """binding.ForwardPipeline (copies in and out overlapping neighbouring
+    batches' forwards) returns, for every batch, the bits of one moe_forward
+    call on the same tokens; five batches cycle both buffer parities."""
+    dev = require_cuda()
+    cfg = workloads.MOE_CONFIGS["tiny"]
+    d = workloads.make_moe_inputs(cfg, device=dev)
+    T, d_h, k = cfg.T, cfg.d_hidden, cfg.top_k
+    pl = binding.ForwardPipeline(d["wg"], d["bias"], d["w_gate"], d["w_up"], d["w_down"], k, T)
+    xs = [workloads.make_tokens(cfg, T, device="cpu", seed=50 + i).pin_memory() for i in range(5)]
+    outs = [torch.empty((T, d_h), dtype=xs[0].dtype).pin_memory() for _ in range(5)]
+    evs = [pl.submit(xs[i], outs[i]) for i in range(5)]
+    evs[-1].synchronize()
+    pl.synchronize()
+    assert int(pl.err.item()) == 0
+    for i in range(5):
+        ref = binding.moe_forward(xs[i].to(dev), d["wg"], d["bias"], d["w_gate"], d["w_up"], d["w_down"], k)
+        torch.cuda.synchronize()
+        assert torch.equal(outs[i], ref.cpu()), i
+    with pytest.raises(ValueError):
+        pl.submit(xs[0].to(dev), outs[0])  # tokens must be pinned host memory
