@@ -68,12 +68,15 @@ struct GateTcParams {
 };
 
 // Sum of squares of one row of d_h 16-bit values, by a warp (every lane
-// gets the total).  Eight 16-byte loads in flight per lane.
+// gets the total).  Eight 16-byte loads in flight per lane, one partial sum
+// per load (any fp32 order: the sum only enters the error bound).
 template <int DT>
 __device__ __forceinline__ float row_sumsq(const uint8_t *row_bytes, int d_h, int lane) {
     const uint4 *row = reinterpret_cast<const uint4 *>(row_bytes);
     const int chunks = d_h / 8;
-    float ss = 0.0f;
+    float ssu[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) ssu[u] = 0.0f;
     for (int cb = lane; cb < chunks; cb += 32 * 8) {
         uint4 v[8];
 #pragma unroll
@@ -86,12 +89,13 @@ __device__ __forceinline__ float row_sumsq(const uint8_t *row_bytes, int d_h, in
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const float2 f = unpack2<DT>(w4[q]);
-                    ss = fmaf(f.x, f.x, ss);
-                    ss = fmaf(f.y, f.y, ss);
+                    ssu[u] = fmaf(f.x, f.x, ssu[u]);
+                    ssu[u] = fmaf(f.y, f.y, ssu[u]);
                 }
             }
         }
     }
+    float ss = ((ssu[0] + ssu[1]) + (ssu[2] + ssu[3])) + ((ssu[4] + ssu[5]) + (ssu[6] + ssu[7]));
 #pragma unroll
     for (int sh = 16; sh >= 1; sh >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, sh);
     return ss;
@@ -214,14 +218,22 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         // while the main loop runs: the sum of squares of this thread's token
         // row over the split's columns, read from each stage's A tile (the
         // row's 128 bytes; the swizzle only permutes 16-byte chunks inside
-        // them) before the stage is released
+        // them) before the stage is released.  This read releases the stage,
+        // so it paces the main loop: thread `row` reads its chunks starting
+        // at chunk row % 8, so the eight threads of a 16-byte access phase
+        // hit eight different bank groups (reading chunk c in every row put
+        // all of them on the same four banks), and eight partial sums keep
+        // the chain short (the sum only enters the error bound, whose slack
+        // covers any fp32 summation order).
         const int q = warp & 3;
         const int row = q * 32 + lane;
         const int t = m0 + row;
         {
             int stage = 0;
             uint32_t phase = 0;
-            float ss = 0.0f;
+            float ssc[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) ssc[c] = 0.0f;
             bool ok = true;
             for (int kb = kb0; kb < kb1; ++kb) {
                 int go = 1;
@@ -232,15 +244,17 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
                     break;
                 }
                 const uint4 *r = reinterpret_cast<const uint4 *>(sA + stage * GT_A_BYTES + row * 128);
+                uint4 v[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) v[c] = r[(c + row) & 7];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const uint4 v = r[c];
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                    const uint32_t w4[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         const float2 f = unpack2<DT>(w4[h]);
-                        ss = fmaf(f.x, f.x, ss);
-                        ss = fmaf(f.y, f.y, ss);
+                        ssc[c] = fmaf(f.x, f.x, ssc[c]);
+                        ssc[c] = fmaf(f.y, f.y, ssc[c]);
                     }
                 }
                 __syncwarp();
@@ -250,6 +264,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
                     phase ^= 1u;
                 }
             }
+            const float ss = ((ssc[0] + ssc[1]) + (ssc[2] + ssc[3])) + ((ssc[4] + ssc[5]) + (ssc[6] + ssc[7]));
             if (ok && blockIdx.y == 0 && t < p.T) p.xss[static_cast<int64_t>(split) * p.T + t] = ss;
         }
         // |w_e|_2 of a share of the gate rows (all CTAs together cover every
