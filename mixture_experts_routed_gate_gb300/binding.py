@@ -731,6 +731,9 @@ class ForwardPipeline:
         self.compute = torch.cuda.Stream(dev)
         self.copy_in = torch.cuda.Stream(dev)
         self.copy_out = torch.cuda.Stream(dev)
+        # the buffers were filled on the caller's stream
+        for st in (self.compute, self.copy_in, self.copy_out):
+            st.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(self.compute):
             for p in range(2):
                 self._body(p)  # first calls on the device outside capture (one-time set-up)
@@ -807,6 +810,7 @@ class ForwardGraph:
         self.x_host = torch.zeros((T, d_h), dtype=dt).pin_memory() if host_io else None
         self.out_host = torch.empty((T, d_h), dtype=dt).pin_memory() if host_io else None
         self.stream = torch.cuda.Stream(dev)
+        self.stream.wait_stream(torch.cuda.current_stream(dev))  # the buffers were filled on the caller's stream
         with torch.cuda.stream(self.stream):
             self._body()  # first call on the device outside capture (one-time set-up)
         self.stream.synchronize()
