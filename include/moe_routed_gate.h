@@ -350,7 +350,9 @@ MOE_API moe_status_t moe_grouped_mlp_w4a16(const void *x, const int32_t *sorted_
  * small-batch shapes; M > 64 is MOE_ERR_UNSUPPORTED), N >= 1, K % 64 == 0,
  * 64 <= K <= 2^20 (|Ct| <= 1024 K cannot overflow int32).  ws: device
  * scratch of moe_gemm_w4a8_workspace_bytes(M, K) bytes (-1 for bad sizes),
- * owned by the caller, 16-byte aligned, used only by this call's work.
+ * owned by the caller, 16-byte aligned, used only by this call's work (for
+ * M <= 8 the call streams the weights through the CUDA cores, dp4a on the
+ * packed bytes, and leaves ws untouched; larger M use the tensor cores).
  * A, B, ws 16-byte aligned, Ct 4-byte aligned, all distinct.
  *
  * moe_grouped_gemm_w4a8: the same per routed row over the dispatch tables

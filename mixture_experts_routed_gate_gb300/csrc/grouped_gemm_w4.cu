@@ -995,6 +995,187 @@ __global__ void w4a8_rows_kernel(const int8_t *__restrict__ x, const int32_t *__
     }
 }
 
+// ---------------------------------------------------------------------------
+// W4A8 with few rows (the dense form, M <= GV_MAX_M): a weight-streaming GEMV
+// on the CUDA cores.  With so few rows per weight the work is the weight
+// bytes, and unpacking into tensor memory costs more than the MMAs save.  A
+// CTA owns one 256-channel tile and a K range: a producer warp streams the
+// tile's packed sub-steps (8 KB each, contiguous) into a ring of shared
+// memory with bulk copies, so the bytes in flight are bounded by shared
+// memory rather than registers, and each consumer thread owns one output
+// channel.  Each 32-bit word holds 8 weights as value + 8 in the tiled
+// layout's nibble order (elements 0, 2, 4, 6 in nibbles 0-3, 1, 3, 5, 7 in
+// 4-7), so one AND gives the bytes of elements (0, 4, 1, 5) and a shift and
+// AND those of (2, 6, 3, 7); dp4a multiplies them with the activation bytes
+// staged in the same order: sum_k a_k w_k = sum_k a_k (w_k + 8) - 8 sum_k a_k,
+// exact in int32.
+// ---------------------------------------------------------------------------
+constexpr int GV_THREADS = 256;             // consumers: the tile's channels
+constexpr int GV_BLOCK = GV_THREADS + 32;   // + the producer warp
+constexpr int GV_MAX_M = 8;
+constexpr int GV_MAX_SUB = 64;              // 64-wide sub-steps of a CTA's K range
+constexpr int GV_RING = 12;                 // stages of the weight ring
+constexpr int GV_STAGE = GV_THREADS * 32;   // one sub-step of the tile, 8 KB
+
+__host__ __device__ constexpr int gv_smem_bytes(int mt) {
+    return GV_RING * GV_STAGE + 2 * mt * GV_MAX_SUB * 8 * 4 + 2 * GV_RING * 8 + mt * 4 + 16;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(GV_BLOCK)
+    w4a8_gemv_kernel(const int8_t *__restrict__ A, int M, const uint8_t *__restrict__ B, int N, int K,
+                     int kchunk, int32_t *__restrict__ Ct, int atomic_out, int32_t *err) {
+    extern __shared__ __align__(128) uint8_t gv_smem[];
+    uint8_t *ring = gv_smem;
+    uint32_t *a_lo = reinterpret_cast<uint32_t *>(ring + GV_RING * GV_STAGE);  // [MT][GV_MAX_SUB * 8]
+    uint32_t *a_hi = a_lo + MT * GV_MAX_SUB * 8;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(a_hi + MT * GV_MAX_SUB * 8);  // full, empty
+    int *a_sum = reinterpret_cast<int *>(bars + 2 * GV_RING);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(a_sum + MT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int i) { return bar0 + 8u * i; };
+    auto empty_bar = [&](int i) { return bar0 + 8u * (GV_RING + i); };
+    const int kb = K / W4_BK;
+    const int s0 = blockIdx.y * kchunk;
+    const int ns = min(kchunk, kb - s0);
+    if (ns <= 0) return;  // the whole CTA
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < GV_RING; ++i) {
+            mbar_init(full_bar(i), 1);
+            mbar_init(empty_bar(i), GV_THREADS / 32);  // one arrival per consumer warp
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (threadIdx.x < MT) a_sum[threadIdx.x] = 0;
+    __syncthreads();
+    griddep_wait();
+    griddep_launch_dependents();
+
+    if (warp == GV_THREADS / 32) {
+        // ------------------------------ producer ------------------------------
+        const uint8_t *src = B + (static_cast<int64_t>(blockIdx.x) * kb + s0) * GV_STAGE;
+        if (lane == 0) {
+            for (int s = 0; s < ns; ++s) {
+                const int st = s % GV_RING;
+                if (s >= GV_RING &&
+                    !mbar_wait_bounded(empty_bar(st), static_cast<uint32_t>((s / GV_RING) & 1) ^ 1u, abort_flag, err))
+                    break;
+                mbar_arrive_expect_tx(full_bar(st), GV_STAGE);
+                w4_bulk_g2s(smem_u32(ring + st * GV_STAGE), src + static_cast<int64_t>(s) * GV_STAGE, GV_STAGE,
+                            full_bar(st), l2_policy_evict_first());
+            }
+        }
+        return;
+    }
+    // ------------------------------ consumers ------------------------------
+    // the CTA's activations, 8 elements per word pair, in the weight words' byte order
+    const int groups = ns * 8;
+    for (int m = 0; m < M; ++m) {
+        int part = 0;
+        for (int g = threadIdx.x; g < groups; g += GV_THREADS) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(A + static_cast<int64_t>(m) * K +
+                                                                  static_cast<int64_t>(s0) * W4_BK) + g);
+            a_lo[m * GV_MAX_SUB * 8 + g] = __byte_perm(v.x, v.y, 0x5140);  // elements 0, 4, 1, 5
+            a_hi[m * GV_MAX_SUB * 8 + g] = __byte_perm(v.x, v.y, 0x7362);  // elements 2, 6, 3, 7
+            part = __dp4a(static_cast<int>(v.x), 0x01010101, part);
+            part = __dp4a(static_cast<int>(v.y), 0x01010101, part);
+        }
+#pragma unroll
+        for (int sh = 16; sh >= 1; sh >>= 1) part += __shfl_xor_sync(0xffffffffu, part, sh);
+        if (lane == 0) atomicAdd(&a_sum[m], part);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(GV_THREADS) : "memory");  // consumers only
+    const int t = threadIdx.x;
+    // the two 16-byte halves of this channel's 32 bytes, read in a lane-dependent
+    // order so that the eight lanes of an access phase hit eight bank groups
+    const int sel = (lane >> 2) & 1;
+    int acc[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[m] = 0;
+    bool ok = true;
+    for (int s = 0; s < ns; ++s) {
+        const int st = s % GV_RING;
+        if (!mbar_wait_bounded(full_bar(st), static_cast<uint32_t>((s / GV_RING) & 1), abort_flag, err)) {
+            ok = false;
+            break;
+        }
+        const uint4 *r = reinterpret_cast<const uint4 *>(ring + st * GV_STAGE + t * 32);
+        const uint4 x0 = r[sel], x1 = r[sel ^ 1];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(st));
+        const uint4 w0 = sel ? x1 : x0, w1 = sel ? x0 : x1;
+        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int lo = static_cast<int>(wv[q] & 0x0F0F0F0Fu);
+            const int hi = static_cast<int>((wv[q] >> 4) & 0x0F0F0F0Fu);
+            const int g = s * 8 + q;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (m < M) {
+                    acc[m] = __dp4a(lo, static_cast<int>(a_lo[m * GV_MAX_SUB * 8 + g]), acc[m]);
+                    acc[m] = __dp4a(hi, static_cast<int>(a_hi[m * GV_MAX_SUB * 8 + g]), acc[m]);
+                }
+            }
+        }
+    }
+    if (!ok) {
+        // after a timeout, let the copies still in flight land before the CTA exits
+        for (int s = 0; s < ns && s < GV_RING; ++s) {
+            const int last = s + ((ns - 1 - s) / GV_RING) * GV_RING;  // the last use of stage s
+            w4_wait_drain(full_bar(s), static_cast<uint32_t>((last / GV_RING) & 1));
+        }
+        return;
+    }
+    const int n = blockIdx.x * GV_THREADS + t;
+    if (n < N) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+                const int v = acc[m] - 8 * a_sum[m];
+                int32_t *o = Ct + static_cast<int64_t>(n) * M + m;
+                if (atomic_out)
+                    atomicAdd(o, v);
+                else
+                    *o = v;
+            }
+        }
+    }
+}
+
+template <int MT>
+cudaError_t launch_gemv_typed(const int8_t *A, int M, const uint8_t *B, int64_t N, int64_t K, int32_t *Ct,
+                              int32_t *err, cudaStream_t stream) {
+    const int64_t kb = K / W4_BK, nt = (N + GV_THREADS - 1) / GV_THREADS;
+    constexpr int smem = gv_smem_bytes(MT);
+    static_assert(smem <= 232448, "shared memory per CTA");
+    // about one wave at two CTAs per SM (one where two do not fit), at most
+    // GV_MAX_SUB sub-steps each
+    const int per_sm = 2 * smem <= 232448 ? 2 : 1;
+    int64_t ks = std::max<int64_t>(1, per_sm * device_sm_count() / nt);
+    const int64_t kchunk = std::min<int64_t>(GV_MAX_SUB, std::max<int64_t>(1, (kb + ks - 1) / ks));
+    ks = (kb + kchunk - 1) / kchunk;
+    if (ks > 65535 || nt > 0x7fffffff) return cudaErrorInvalidValue;
+    static std::atomic<bool> attr_done[64];  // zero-initialised; several host threads may launch
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(w4a8_gemv_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    if (ks > 1) {
+        const cudaError_t e = cudaMemsetAsync(Ct, 0, static_cast<size_t>(N * M) * 4, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(w4a8_gemv_kernel<MT>, dim3(static_cast<unsigned>(nt), static_cast<unsigned>(ks)),
+                      dim3(GV_BLOCK), smem, stream, A, M, B, static_cast<int>(N), static_cast<int>(K),
+                      static_cast<int>(kchunk), Ct, ks > 1 ? 1 : 0, err);
+}
+
 }  // namespace
 
 W4a8Plan w4a8_plan(int64_t blocks, int64_t N, int64_t K) {
@@ -1021,6 +1202,14 @@ cudaError_t launch_gemm_w4a8(const int8_t *x, const int32_t *gather_idx, int64_t
     if (n_rows <= 0 || N <= 0) return cudaSuccess;
     if (dense_rows <= 0 && (m_blocks <= 0 || m_blocks > W4_MAX_BLOCKS)) return cudaErrorInvalidValue;
     if (dense_rows > W4_TOK_ROWS || K % W4_BK != 0) return cudaErrorInvalidValue;
+    if (dense_rows > 0 && dense_rows <= GV_MAX_M && ld_row == 1 && ld_col == dense_rows) {
+        // few rows: the CUDA-core GEMV (Ct [N, M])
+        const int M = static_cast<int>(dense_rows);
+        if (M == 1) return launch_gemv_typed<1>(x, M, B, N, K, out, err, stream);
+        if (M == 2) return launch_gemv_typed<2>(x, M, B, N, K, out, err, stream);
+        if (M <= 4) return launch_gemv_typed<4>(x, M, B, N, K, out, err, stream);
+        return launch_gemv_typed<8>(x, M, B, N, K, out, err, stream);
+    }
     const int64_t blocks = dense_rows > 0 ? 1 : m_blocks;
     const W4a8Plan pl = w4a8_plan(blocks, N, K);
     {
