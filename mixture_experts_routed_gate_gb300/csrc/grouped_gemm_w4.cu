@@ -39,10 +39,23 @@
 //   warps 2..5  epilogue: scales, silu(gate)*up for stage 1, row-masked
 //               stores; a stage-1 warp-tile publishes its h rows on the
 //               block's counter for the stage-2 tiles.
-// Tiles are taken as in the 16-bit expert MLP: CTA b starts with tile b,
-// the rest come from a shared counter; stage-2 tiles wait (bounded) for
-// their block's h.  Every wait is bounded; on a timeout the kernel records
-// MOE_ERR_TIMEOUT, lets its copies and MMAs land, frees TMEM and returns.
+// Tiles are taken as in the 16-bit expert MLP: every tile, the first
+// included, from a shared counter, stage-1 tiles before stage-2 tiles, over
+// units of at most 64 rows (a dispatch block with more rows is two units);
+// a stage-2 tile waits (bounded) until its block's counter shows every
+// stage-1 warp-tile of the block stored.  Every wait is bounded; on a
+// timeout the kernel records MOE_ERR_TIMEOUT, lets its copies and MMAs land,
+// frees TMEM and returns.
+//
+// W4A8 (int4 weights x int8 activations, exact int32 sums):
+//   * the GEMM form of the same kernel: stage-2 tiles only (256 channels x
+//     one K chunk of at most 16384), rows from an fp16 copy of the int8
+//     activations (w4a8_rows_kernel), an int32 epilogue; every fp32 partial
+//     sum is an integer of magnitude <= 2^24, so it is exact, and the chunks
+//     are added with integer atomics;
+//   * w4a8_gemv_kernel for the dense form with at most 8 rows: the weights
+//     streamed through a shared-memory ring into the CUDA cores, dp4a on the
+//     packed bytes.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
