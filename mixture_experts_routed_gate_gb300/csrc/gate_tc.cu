@@ -54,7 +54,7 @@ constexpr int GT_SMEM = 1024 + GT_STAGES * (GT_A_BYTES + GT_B_BYTES) + 256;
 constexpr int GT_MAX_SPLITS = 8;
 constexpr int SEL_WARPS = 4;     // warps (tokens) of a select CTA
 constexpr int SEL_G = 4;         // candidates recomputed together by a warp
-constexpr int SEL_U = 4;         // chunks per lane whose loads are in flight together
+constexpr int SEL_U = 2;         // chunks per lane whose loads are in flight together
 
 struct GateTcParams {
     float *part;           // [S, T, E] fp32 partial logits (no bias)
