@@ -53,8 +53,8 @@ constexpr int GT_B_BYTES = GT_BN * GT_BK * 2;
 constexpr int GT_SMEM = 1024 + GT_STAGES * (GT_A_BYTES + GT_B_BYTES) + 256;
 constexpr int GT_MAX_SPLITS = 8;
 constexpr int SEL_WARPS = 4;     // warps (tokens) of a select CTA
-constexpr int SEL_G = 4;         // candidates recomputed together by a warp
-constexpr int SEL_U = 2;         // chunks per lane whose loads are in flight together
+constexpr int SEL_G = 3;         // candidates recomputed together by a warp
+constexpr int SEL_U = 4;         // chunks per lane whose loads are in flight together
 
 struct GateTcParams {
     float *part;           // [S, T, E] fp32 partial logits (no bias)
@@ -317,6 +317,77 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     }
 }
 
+// Order-preserving key of a float that is not NaN (-0 taken as +0): a > b
+// as floats exactly when key(a) > key(b); 0 is below every key.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t b = __float_as_uint(f + 0.0f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// One chunk of NG candidates' chains: the 8 elements in ascending order, each
+// a single-rounding fmaf on the exactly widened 16-bit values (the same bits
+// as the mixed-precision FMA of the CUDA-core gate); x is widened once for all
+// NG chains.
+template <int DT, int NG>
+__device__ __forceinline__ void select_chunk(const uint4 &xv, const uint4 *wv, float *acc) {
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 xf = unpack2<DT>(xw[q]);
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            const uint32_t w = q == 0 ? wv[g].x : q == 1 ? wv[g].y : q == 2 ? wv[g].z : wv[g].w;
+            const float2 wf = unpack2<DT>(w);
+            acc[g] = fmaf(xf.x, wf.x, acc[g]);
+            acc[g] = fmaf(xf.y, wf.y, acc[g]);
+        }
+    }
+}
+
+// Lane `lane`'s chains of NG candidates (rows off[g] / chunks of the gate
+// weight): chunks c = lane, lane + 32, ... in ascending order, SEL_U chunks'
+// loads in flight.
+template <int DT, int NG>
+__device__ __forceinline__ void select_chains(const uint4 *__restrict__ xrow, const uint4 *__restrict__ wbase,
+                                              const int *off, int chunks, int lane, float *acc) {
+    int c = lane;
+    for (; c + 32 * (SEL_U - 1) < chunks; c += 32 * SEL_U) {
+        uint4 xv[SEL_U], wv[SEL_U][NG];
+#pragma unroll
+        for (int u = 0; u < SEL_U; ++u) {
+            xv[u] = __ldg(xrow + c + 32 * u);
+#pragma unroll
+            for (int g = 0; g < NG; ++g) wv[u][g] = __ldg(wbase + off[g] + c + 32 * u);
+        }
+#pragma unroll
+        for (int u = 0; u < SEL_U; ++u) select_chunk<DT, NG>(xv[u], wv[u], acc);
+    }
+    for (; c < chunks; c += 32) {
+        uint4 wv[NG];
+        const uint4 xv = __ldg(xrow + c);
+#pragma unroll
+        for (int g = 0; g < NG; ++g) wv[g] = __ldg(wbase + off[g] + c);
+        select_chunk<DT, NG>(xv, wv, acc);
+    }
+}
+
+// select_chains with NG = ng (1 <= ng <= NG), so a short last group runs
+// only its own chains.
+template <int DT, int NG>
+__device__ __forceinline__ void select_group(int ng, const uint4 *xrow, const uint4 *wbase, const int *off,
+                                             int chunks, int lane, float *acc) {
+    if constexpr (NG > 1) {
+        if (ng < NG) {
+            select_group<DT, NG - 1>(ng, xrow, wbase, off, chunks, lane, acc);
+            return;
+        }
+    }
+    select_chains<DT, NG>(xrow, wbase, off, chunks, lane, acc);
+}
+
 // One warp per token, SEL_WARPS tokens per CTA.  The warp sums the partials
 // in split order, forms the bounds and the candidate list, recomputes every
 // candidate in the fixed order (SEL_G candidates at a time: lane L runs one
@@ -380,38 +451,33 @@ __global__ void __launch_bounds__(SEL_WARPS * 32)
             }
         }
         bad = __any_sync(0xffffffffu, bad);
-        // theta = k-th largest lower bound (k rounds of a warp max; a removed
-        // value is marked NaN in a copy)
+        // theta = k-th largest lower bound: k rounds of a warp max (one
+        // integer reduction) over order-preserving keys; each round clears one
+        // holder of the maximum
         float theta = -INFINITY;
         if (!bad) {
-            float rem[SLOTS];
+            uint32_t key[SLOTS];
 #pragma unroll
-            for (int s = 0; s < SLOTS; ++s) rem[s] = lo[s];
+            for (int s = 0; s < SLOTS; ++s) key[s] = s * 32 + lane < E ? order_key(lo[s]) : 0u;
+            uint32_t kth = 0u;
             for (int j = 0; j < k; ++j) {
-                float best = -INFINITY;
-                int best_e = 0x7fffffff;
+                uint32_t m = 0u;
 #pragma unroll
-                for (int s = 0; s < SLOTS; ++s) {
-                    const int e = s * 32 + lane;
-                    if (e < E && !isnan(rem[s]) && (best_e == 0x7fffffff || rem[s] > best)) {
-                        best = rem[s];
-                        best_e = e;
+                for (int s = 0; s < SLOTS; ++s) m = max(m, key[s]);
+                kth = __reduce_max_sync(0xffffffffu, m);
+                const unsigned holders = __ballot_sync(0xffffffffu, m == kth);
+                if (lane == __ffs(holders) - 1) {
+                    bool done = false;
+#pragma unroll
+                    for (int s = 0; s < SLOTS; ++s) {
+                        if (!done && key[s] == kth) {
+                            key[s] = 0u;
+                            done = true;
+                        }
                     }
                 }
-#pragma unroll
-                for (int sh = 16; sh >= 1; sh >>= 1) {
-                    const float ob = __shfl_xor_sync(0xffffffffu, best, sh);
-                    const int oe = __shfl_xor_sync(0xffffffffu, best_e, sh);
-                    if (oe != 0x7fffffff && (best_e == 0x7fffffff || ob > best || (ob == best && oe < best_e))) {
-                        best = ob;
-                        best_e = oe;
-                    }
-                }
-#pragma unroll
-                for (int s = 0; s < SLOTS; ++s)
-                    if (s * 32 + lane == best_e) rem[s] = NAN;
-                theta = best;
             }
+            if (kth != 0u) theta = key_value(kth);
         }
         // candidates, in ascending expert id
 #pragma unroll
@@ -437,37 +503,7 @@ __global__ void __launch_bounds__(SEL_WARPS * 32)
             off[g] = cand_id[i0 + (g < ng ? g : 0)] * chunks;
             acc[g] = 0.0f;
         }
-        for (int cb = lane; cb < chunks; cb += 32 * SEL_U) {
-            uint4 xv[SEL_U], wv[SEL_U][SEL_G];
-#pragma unroll
-            for (int u = 0; u < SEL_U; ++u) {
-                const int c = cb + 32 * u;
-                if (c < chunks) {
-                    xv[u] = __ldg(xrow + c);
-#pragma unroll
-                    for (int g = 0; g < SEL_G; ++g)
-                        if (g < ng) wv[u][g] = __ldg(wbase + off[g] + c);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < SEL_U; ++u) {
-                const int c = cb + 32 * u;
-                if (c < chunks) {
-                    const uint32_t xw[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
-#pragma unroll
-                    for (int g = 0; g < SEL_G; ++g) {
-                        if (g < ng) {
-                            const uint32_t aw[4] = {wv[u][g].x, wv[u][g].y, wv[u][g].z, wv[u][g].w};
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                acc[g] = fma_mixed<DT, false>(xw[q], aw[q], acc[g]);
-                                acc[g] = fma_mixed<DT, true>(xw[q], aw[q], acc[g]);
-                            }
-                        }
-                    }
-                }
-            }
-        }
+        select_group<DT, SEL_G>(ng, xrow, wbase, off, chunks, lane, acc);
 #pragma unroll
         for (int g = 0; g < SEL_G; ++g) {
 #pragma unroll
@@ -484,39 +520,67 @@ __global__ void __launch_bounds__(SEL_WARPS * 32)
     }
     __syncwarp();
 
-    // top-k among the candidates by (logit desc, id asc); lane j keeps slot j
-    unsigned taken = 0;  // bit i: candidate lane + 32 i already selected
+    // top-k among the candidates by (logit desc, id asc); lane j keeps slot j.
+    // At most 32 candidates, none NaN: one per lane, each round a warp max of
+    // the keys and a warp min of the ids holding it.  Otherwise a scan.
     float top = 0.0f, my_v = 0.0f;
     int my_e = 0;
-    for (int j = 0; j < k; ++j) {
-        float best = -INFINITY;
-        int best_e = 0x7fffffff, best_i = -1;
-        for (int i = lane, b = 0; i < n; i += 32, ++b) {
-            if (taken & (1u << b)) continue;
-            const float v = cand_val[i];
-            const int e = cand_id[i];
-            if (best_i < 0 || v > best || (v == best && e < best_e)) {
-                best = v;
-                best_e = e;
-                best_i = i;
+    bool one_each = n <= 32;
+    float cv = 0.0f;
+    int ce = 0;
+    if (one_each) {
+        if (lane < n) {
+            cv = cand_val[lane];
+            ce = cand_id[lane];
+        }
+        one_each = !__any_sync(0xffffffffu, lane < n && isnan(cv));
+    }
+    if (one_each) {
+        uint32_t key = lane < n ? order_key(cv) : 0u;
+        for (int j = 0; j < k; ++j) {
+            const uint32_t m = __reduce_max_sync(0xffffffffu, key);
+            const uint32_t be =
+                __reduce_min_sync(0xffffffffu, key == m && key != 0u ? static_cast<uint32_t>(ce) : 0xffffffffu);
+            if (key == m && static_cast<uint32_t>(ce) == be) key = 0u;
+            const float bv = key_value(m);
+            if (j == 0) top = bv;
+            if (j == lane) {
+                my_v = bv;
+                my_e = static_cast<int>(be);
             }
         }
+    } else {
+        unsigned taken = 0;  // bit i: candidate lane + 32 i already selected
+        for (int j = 0; j < k; ++j) {
+            float best = -INFINITY;
+            int best_e = 0x7fffffff, best_i = -1;
+            for (int i = lane, b = 0; i < n; i += 32, ++b) {
+                if (taken & (1u << b)) continue;
+                const float v = cand_val[i];
+                const int e = cand_id[i];
+                if (best_i < 0 || v > best || (v == best && e < best_e)) {
+                    best = v;
+                    best_e = e;
+                    best_i = i;
+                }
+            }
 #pragma unroll
-        for (int sh = 16; sh >= 1; sh >>= 1) {
-            const float ob = __shfl_xor_sync(0xffffffffu, best, sh);
-            const int oe = __shfl_xor_sync(0xffffffffu, best_e, sh);
-            const int oi = __shfl_xor_sync(0xffffffffu, best_i, sh);
-            if (oi >= 0 && (best_i < 0 || ob > best || (ob == best && oe < best_e))) {
-                best = ob;
-                best_e = oe;
-                best_i = oi;
+            for (int sh = 16; sh >= 1; sh >>= 1) {
+                const float ob = __shfl_xor_sync(0xffffffffu, best, sh);
+                const int oe = __shfl_xor_sync(0xffffffffu, best_e, sh);
+                const int oi = __shfl_xor_sync(0xffffffffu, best_i, sh);
+                if (oi >= 0 && (best_i < 0 || ob > best || (ob == best && oe < best_e))) {
+                    best = ob;
+                    best_e = oe;
+                    best_i = oi;
+                }
             }
-        }
-        if (best_i >= 0 && (best_i & 31) == lane) taken |= 1u << (best_i >> 5);
-        if (j == 0) top = best;
-        if (j == lane) {
-            my_v = best;
-            my_e = best_e;
+            if (best_i >= 0 && (best_i & 31) == lane) taken |= 1u << (best_i >> 5);
+            if (j == 0) top = best;
+            if (j == lane) {
+                my_v = best;
+                my_e = best_e;
+            }
         }
     }
     // softmax denominator over every expert (per lane in slot order, then the
