@@ -256,7 +256,7 @@ class NativeStep:
                                     self.scratch_bytes, sp)),
             # the token-order gather moe_forward runs
             "gather": (L.moe_gather_rows_by_token, (p(x), p(v["token_topk_to_pos"]), T, k, Tk, d_h, self.code,
-                                                    p(v["a"]), sp)),
+                                                    p(v["a"]), None, sp)),
             # the gathering form for T <= 64 (rows from x), as moe_forward does
             "expert_mlp": (L.moe_grouped_mlp, (None if T <= 64 else p(v["a"]), p(d["w_gate"]), p(d["w_up"]),
                                                p(d["w_down"]), *tables, self.mb, None, Tk, d_h, d_e, E,

@@ -211,11 +211,15 @@ MOE_API moe_status_t moe_gather_rows(const void *x, const int32_t *sorted_token_
  * row named exactly once) the result is moe_gather_rows' with that
  * dispatch's sorted_token_idx, but each token's row is read from memory once
  * instead of once per expert it went to.  token_topk_to_pos [T, k] int32,
- * 1 <= k <= 32.  x [T, d_h]; d_h * elem_size % 16 == 0.
+ * 1 <= k <= 32.  x [T, d_h]; d_h * elem_size % 16 == 0.  The rows move by
+ * bulk copies through shared memory (one load per token, one store per
+ * row); err_flag: optional device int32, set to MOE_ERR_TIMEOUT if a copy
+ * wait gives up (the rows of the token that timed out and of the tokens
+ * after it in its stream are then not written).
  */
 MOE_API moe_status_t moe_gather_rows_by_token(const void *x, const int32_t *token_topk_to_pos, int64_t T,
                                               int64_t k, int64_t n_rows, int64_t d_h, moe_dtype_t dtype,
-                                              void *a_out, moe_stream_t stream);
+                                              void *a_out, int32_t *err_flag, moe_stream_t stream);
 
 /*
  * Grouped gate/up GEMM with fused SiLU (CSDN "tilelang kernel stage 1 gate+up";

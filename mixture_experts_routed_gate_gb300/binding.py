@@ -60,7 +60,7 @@ def lib():
         "moe_copy": (I, [P, P, I64, P]),
         "moe_wait_flag": (I, [P, ctypes.c_int32, I64, P, P]),
         "moe_gather_rows": (I, [P, P, I64, I64, I64, I, P, P]),
-        "moe_gather_rows_by_token": (I, [P, P, I64, I64, I64, I64, I, P, P]),
+        "moe_gather_rows_by_token": (I, [P, P, I64, I64, I64, I64, I, P, P, P]),
         "moe_grouped_gate_up_silu": (I, [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I, P, P, P]),
         "moe_grouped_down": (I, [P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I, P, P, P]),
         "moe_grouped_mlp": (I, [P, P, P, P, P, P, P, P, I64, P, I64, I64, I64, I64, I, P, P, P, P, P, I64, P, P]),
@@ -293,7 +293,7 @@ def moe_gather_rows(x, sorted_token_idx, out=None):
     return out
 
 
-def moe_gather_rows_by_token(x, token_topk_to_pos, n_rows: int, out=None):
+def moe_gather_rows_by_token(x, token_topk_to_pos, n_rows: int, out=None, err=None):
     """The gather in token order: out[token_topk_to_pos[t, j]] = x[t] (positions
     outside [0, n_rows) skipped); with a dispatch's positions, moe_gather_rows'
     result."""
@@ -308,7 +308,7 @@ def moe_gather_rows_by_token(x, token_topk_to_pos, n_rows: int, out=None):
     _cuda(out, "out", dtype=x.dtype)
     with torch.cuda.device(x.device):
         _check(lib().moe_gather_rows_by_token(_ptr(x), _ptr(token_topk_to_pos), T, k, n_rows, d_h,
-                                              _dtype_code(x, "x"), _ptr(out), _stream(x.device)),
+                                              _dtype_code(x, "x"), _ptr(out), _ptr(err), _stream(x.device)),
                "moe_gather_rows_by_token")
     return out
 

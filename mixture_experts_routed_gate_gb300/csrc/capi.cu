@@ -241,14 +241,14 @@ moe_status_t moe_gather_rows(const void *x, const int32_t *sorted_token_idx, int
 
 moe_status_t moe_gather_rows_by_token(const void *x, const int32_t *token_topk_to_pos, int64_t T, int64_t k,
                                       int64_t n_rows, int64_t d_h, moe_dtype_t dtype, void *a_out,
-                                      moe_stream_t stream) {
+                                      int32_t *err_flag, moe_stream_t stream) {
     if (n_rows < 0 || T < 0 || d_h <= 0 || k <= 0 || k > 32) return MOE_ERR_INVALID_ARG;
     const int es = dtype == MOE_F32 ? 4 : 2;
     if (dtype != MOE_F16 && dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
     if ((d_h * es) % 16 != 0) return MOE_ERR_INVALID_ARG;
     if (n_rows == 0 || T == 0) return MOE_OK;
     if (!x || !token_topk_to_pos || !a_out || !aligned16(x) || !aligned16(a_out)) return MOE_ERR_INVALID_ARG;
-    return cuda_status(moe::launch_scatter_rows(x, token_topk_to_pos, T, k, n_rows, d_h, es, a_out,
+    return cuda_status(moe::launch_scatter_rows(x, token_topk_to_pos, T, k, n_rows, d_h, es, a_out, err_flag,
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -595,7 +595,7 @@ moe_status_t moe_forward(const void *x, const void *w_g, const float *bias, cons
         // the rows of A in token order: each token's row read once, written to
         // its k rows (the row-order gather re-read token rows from DRAM about
         // seven times at prefill: 409 MB for 58.7 MB of tokens)
-        st = moe_gather_rows_by_token(x, pos, T, k, Tk, d_h, dtype, A, stream);
+        st = moe_gather_rows_by_token(x, pos, T, k, Tk, d_h, dtype, A, err_flag, stream);
         if (st != MOE_OK) return st;
         st = grouped_mlp(A, w_gate, w_up, w_down, sizes, offsets, padded, gidx, mb, nullptr, Tk, d_h,
                          d_e, E, dtype, hbuf, ybuf, ready, err_flag, stream, false);

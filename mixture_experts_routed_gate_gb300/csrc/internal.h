@@ -72,9 +72,12 @@ cudaError_t launch_wait_flag(const int32_t *flag, int32_t expected, int64_t time
 cudaError_t launch_gather_rows(const void *x, const int32_t *sorted_token_idx, int64_t n_rows,
                                int64_t d_h, int elem_bytes, void *a_out, cudaStream_t stream);
 // the same rows written in token order: a_out[token_topk_to_pos[t, j]] = x[t]
-// (k <= 32; positions outside [0, n_rows) skipped); x is read once
+// (k <= 32; positions outside [0, n_rows) skipped); x is read once; bulk
+// copies through shared memory when a row fits (err, nullable, receives a
+// timed-out wait)
 cudaError_t launch_scatter_rows(const void *x, const int32_t *token_topk_to_pos, int64_t T, int64_t k,
-                                int64_t n_rows, int64_t d_h, int elem_bytes, void *a_out, cudaStream_t stream);
+                                int64_t n_rows, int64_t d_h, int elem_bytes, void *a_out, int32_t *err,
+                                cudaStream_t stream);
 // pos_early: the positions and weights were complete before the previous
 // kernel started (moe_forward: the dispatch precedes the expert MLP), so the
 // combine may read them before its dependency wait

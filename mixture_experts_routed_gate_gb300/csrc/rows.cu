@@ -2,6 +2,8 @@
 // token rows into expert order and the moe_reduce_fused combine.
 #include <cuda_fp8.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -78,6 +80,107 @@ __global__ void __launch_bounds__(GA_WARPS * 32)
             for (int u = 0; u < 4; ++u)
                 if (v + 32 * u < nvec) __stcs(dst + v + 32 * u, a[u]);
         }
+    }
+}
+
+// The same scatter with the copy engine: a warp owns the tokens
+// t = w, w + W, ... (W warps in the grid), which pass through two row buffers
+// in shared memory.  Lane 0 loads a token's row with one bulk copy and writes
+// it to each of its k rows with k bulk stores, the next token's load in
+// flight meanwhile; the other lanes only read the positions.  A buffer is
+// reloaded once the stores issued from it have read it.  Every wait is
+// bounded: on expiry the warp records kErrTimeout, waits (bounded) for its
+// loads in flight and stops.
+// bounded wait for a copy still in flight (after a timeout): never hangs
+__device__ __forceinline__ void rb_wait_drain(uint32_t bar, uint32_t parity) {
+    const unsigned long long start = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - start > kWaitTimeoutNs) return;
+}
+
+constexpr int SB_MAX_WARPS = 4;
+constexpr int SB_SMEM_BUDGET = 200 * 1024;
+
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                              uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_s2g_hint(void *dst, uint32_t src, uint32_t bytes, uint64_t pol) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__global__ void __launch_bounds__(SB_MAX_WARPS * 32)
+    scatter_rows_bulk_kernel(const uint8_t *__restrict__ x, const int32_t *__restrict__ pos, int64_t T, int k,
+                             int64_t n_rows, uint32_t row_bytes, uint32_t buf_bytes, uint8_t *__restrict__ out,
+                             int32_t *err) {
+    extern __shared__ __align__(128) uint8_t sb_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warps = blockDim.x >> 5;
+    const uint32_t buf = smem_u32(sb_smem) + static_cast<uint32_t>(warp) * 2u * buf_bytes;
+    const uint32_t bar = smem_u32(sb_smem) + static_cast<uint32_t>(warps) * 2u * buf_bytes + warp * 16u;
+    if (lane == 0) {
+        mbar_init(bar, 1);
+        mbar_init(bar + 8, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    griddep_wait();
+    griddep_launch_dependents();
+    const int64_t W = static_cast<int64_t>(gridDim.x) * warps;
+    int64_t t = static_cast<int64_t>(blockIdx.x) * warps + warp;
+    if (t >= T) return;
+    const uint64_t pol = l2_policy_evict_first();
+    volatile int abort_w = 0;
+    if (lane == 0) {
+        mbar_arrive_expect_tx(bar, row_bytes);
+        bulk_g2s_hint(buf, x + t * row_bytes, row_bytes, bar, pol);
+    }
+    int p_next = lane < k ? __ldg(pos + t * k + lane) : -1;
+    int64_t i = 0;
+    bool ok = true;
+    for (; t < T; t += W, ++i) {
+        const uint32_t b = static_cast<uint32_t>(i & 1);
+        const int p_cur = p_next;
+        const int64_t tn = t + W;
+        if (tn < T) {
+            if (lane == 0) {
+                bulk_wait_read_all();  // the other buffer's stores have read it
+                mbar_arrive_expect_tx(bar + 8u * (b ^ 1u), row_bytes);
+                bulk_g2s_hint(buf + (b ^ 1u) * buf_bytes, x + tn * row_bytes, row_bytes, bar + 8u * (b ^ 1u), pol);
+            }
+            p_next = lane < k ? __ldg(pos + tn * k + lane) : -1;
+        }
+        if (lane == 0) ok = mbar_wait_bounded(bar + 8u * b, static_cast<uint32_t>((i >> 1) & 1), &abort_w, err);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        for (int j = 0; j < k; ++j) {
+            const int pj = __shfl_sync(0xffffffffu, p_cur, j);
+            if (lane == 0 && pj >= 0 && pj < n_rows)
+                bulk_s2g_hint(out + static_cast<int64_t>(pj) * row_bytes, buf + b * buf_bytes, row_bytes, pol);
+        }
+        if (lane == 0) bulk_commit();
+    }
+    if (lane == 0) {
+        if (!ok) {
+            // this token's load and, if issued, the next one's
+            rb_wait_drain(bar + 8u * static_cast<uint32_t>(i & 1), static_cast<uint32_t>((i >> 1) & 1));
+            if (t + W < T)
+                rb_wait_drain(bar + 8u * static_cast<uint32_t>((i + 1) & 1),
+                              static_cast<uint32_t>(((i + 1) >> 1) & 1));
+        }
+        bulk_wait_all();  // every store done before the buffers go away
     }
 }
 
@@ -283,12 +386,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
         : "memory");
-}
-
-__device__ __forceinline__ void rb_wait_drain(uint32_t bar, uint32_t parity) {
-    const unsigned long long start = global_timer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (global_timer_ns() - start > kWaitTimeoutNs) return;
 }
 
 template <typename TIn>
@@ -563,9 +660,45 @@ cudaError_t launch_gather_rows(const void *x, const int32_t *sorted_token_idx, i
 }
 
 cudaError_t launch_scatter_rows(const void *x, const int32_t *token_topk_to_pos, int64_t T, int64_t k,
-                                int64_t n_rows, int64_t d_h, int elem_bytes, void *a_out, cudaStream_t stream) {
+                                int64_t n_rows, int64_t d_h, int elem_bytes, void *a_out, int32_t *err,
+                                cudaStream_t stream) {
     if (T <= 0 || n_rows <= 0) return cudaSuccess;
     if (k <= 0 || k > 32) return cudaErrorInvalidValue;
+    const int64_t row_bytes = d_h * elem_bytes;
+    const int64_t buf_bytes = (row_bytes + 127) / 128 * 128;
+    int64_t wpc = SB_SMEM_BUDGET / (2 * buf_bytes + 16);
+    if (wpc > SB_MAX_WARPS) wpc = SB_MAX_WARPS;
+    if (wpc >= 1 && row_bytes < (1 << 20)) {
+        // bulk form: resident CTAs only (a persistent grid of token streams)
+        static std::atomic<bool> attr_done[64];  // zero-initialised; several host threads may launch
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+        if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(scatter_rows_bulk_kernel,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       SB_SMEM_BUDGET + SB_MAX_WARPS * 16);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) attr_done[dev] = true;
+        }
+        const int64_t smem = wpc * (2 * buf_bytes + 16);
+        int smem_sm = 0, reserved = 0;
+        if (cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+            return cudaErrorInvalidDevice;
+        int64_t per_sm = smem_sm / (smem + reserved);
+        const int64_t by_threads = 2048 / (wpc * 32);
+        if (per_sm > by_threads) per_sm = by_threads;
+        if (per_sm >= 1) {
+            const int64_t want = (T + wpc - 1) / wpc;
+            const int64_t cap = static_cast<int64_t>(device_sm_count()) * per_sm;
+            const int64_t blocks = want < cap ? want : cap;
+            return launch_pdl(scatter_rows_bulk_kernel, dim3(static_cast<unsigned>(blocks)),
+                              dim3(static_cast<unsigned>(wpc * 32)), static_cast<size_t>(smem), stream,
+                              static_cast<const uint8_t *>(x), token_topk_to_pos, T, static_cast<int>(k), n_rows,
+                              static_cast<uint32_t>(row_bytes), static_cast<uint32_t>(buf_bytes),
+                              static_cast<uint8_t *>(a_out), err);
+        }
+    }
     const int nvec = static_cast<int>(d_h * elem_bytes / 16);
     const int64_t blocks = (T + GA_WARPS - 1) / GA_WARPS;
     return launch_pdl(scatter_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(GA_WARPS * 32), 0, stream,
