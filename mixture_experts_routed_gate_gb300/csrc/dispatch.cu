@@ -5,17 +5,17 @@
 // group_idx_for_bx) done on the device with no host round trip:
 //   1. dispatch_hist_kernel: each CTA counts the experts of its chunk of
 //      CHUNK consecutive pairs (f = t*k + j) into hist[chunk][e].
-//   2. dispatch_scan_kernel (one CTA, one thread per expert): per-expert
-//      running sum over chunks -> chunk bases and group_sizes; block scans ->
-//      group_offsets and the padded offsets; a binary search per M block ->
-//      group_idx_for_bx.  Chunk bases are made absolute in place.
-//   3. dispatch_scatter_kernel: each warp owns a contiguous run of pairs;
-//      warp-level counts in shared memory give every warp its start per
-//      expert; the warp then walks its pairs 32 at a time in ascending f and
-//      ranks equal experts with __match_any_sync, so the order inside an
-//      expert is ascending f (a stable sort) with no atomics-order effects.
+//   2. dispatch_scan_scatter_kernel, one CTA per chunk: each CTA sums the
+//      chunk histograms itself (per-expert totals and its chunk's bases), two
+//      block scans give group_offsets and the padded offsets, a binary search
+//      per M block gives group_idx_for_bx (spread over the CTAs; CTA 0 writes
+//      the per-expert tables); then warp-level counts in shared memory give
+//      every warp its start per expert, and the warp walks its pairs 32 at a
+//      time in ascending f, ranking equal experts with __match_any_sync, so
+//      the order inside an expert is ascending f (a stable sort) with no
+//      atomics-order effects.
 // Problems of at most 16384 pairs and 256 experts run all of it in a single
-// CTA (dispatch_small_kernel): one launch instead of three.
+// CTA (dispatch_small_kernel): one launch instead of two.
 #include <mutex>
 
 #include "../../include/moe_routed_gate.h"
@@ -29,7 +29,6 @@ constexpr int DS_WARPS = 8;
 constexpr int DS_THREADS = DS_WARPS * 32;
 constexpr int PAIRS_PER_WARP = 256;
 constexpr int CHUNK = DS_WARPS * PAIRS_PER_WARP;  // 2048 pairs per CTA
-constexpr int SCAN_THREADS = 1024;                // E <= 1024
 
 __global__ void __launch_bounds__(DS_THREADS)
     dispatch_hist_kernel(const int32_t *__restrict__ idx, int64_t n_pairs, int E,
@@ -40,13 +39,17 @@ __global__ void __launch_bounds__(DS_THREADS)
     griddep_launch_dependents();
     __syncthreads();
     const int64_t f0 = static_cast<int64_t>(blockIdx.x) * CHUNK;
-    for (int i = threadIdx.x; i < CHUNK; i += DS_THREADS) {
-        const int64_t f = f0 + i;
-        if (f < n_pairs) {
-            const int e = __ldg(idx + f);
-            if (e >= 0 && e < E) atomicAdd(&counts[e], 1);
-        }
+    // all of the thread's loads first, then the counts
+    constexpr int PER_THREAD = CHUNK / DS_THREADS;
+    int ev[PER_THREAD];
+#pragma unroll
+    for (int i = 0; i < PER_THREAD; ++i) {
+        const int64_t f = f0 + i * DS_THREADS + threadIdx.x;
+        ev[i] = f < n_pairs ? __ldg(idx + f) : -1;
     }
+#pragma unroll
+    for (int i = 0; i < PER_THREAD; ++i)
+        if (ev[i] >= 0 && ev[i] < E) atomicAdd(&counts[ev[i]], 1);
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += DS_THREADS)
         hist[static_cast<int64_t>(blockIdx.x) * E + e] = counts[e];
@@ -80,39 +83,83 @@ __device__ int block_exclusive_scan(int v, int *warp_sums) {
     return out;
 }
 
-__global__ void __launch_bounds__(SCAN_THREADS)
-    dispatch_scan_kernel(int32_t *__restrict__ hist, int n_chunks, int E, int block_m,
-                         int32_t *__restrict__ sizes, int32_t *__restrict__ offsets,
-                         int32_t *__restrict__ padded, int32_t *__restrict__ gidx,
-                         int m_blocks, int32_t *__restrict__ ready) {
+// Steps 2 and 3 in one launch: every CTA sums the raw chunk histograms
+// itself (its chunk's per-expert bases, the group sizes and both block
+// scans), so no separate scan grid runs between the histogram and the
+// scatter.  CTA 0 writes sizes / offsets / padded; the M-block lookup and the
+// expert MLP's counters are spread over the CTAs.
+constexpr int DS_MAX_PER_THREAD = 4;  // E <= 4 * DS_THREADS = 1024
+
+__global__ void __launch_bounds__(DS_THREADS)
+    dispatch_scan_scatter_kernel(const int32_t *__restrict__ idx, const float *__restrict__ w,
+                                 int64_t n_pairs, int k, int E, int block_m, const int32_t *__restrict__ hist,
+                                 int n_chunks, int32_t *__restrict__ sizes, int32_t *__restrict__ offsets,
+                                 int32_t *__restrict__ padded, int32_t *__restrict__ gidx, int m_blocks,
+                                 int32_t *__restrict__ ready, int32_t *__restrict__ sorted_tok,
+                                 float *__restrict__ sorted_w, int32_t *__restrict__ pos) {
+    extern __shared__ int32_t ds_smem[];
+    int32_t *wcount = ds_smem;                  // [DS_WARPS][E]
+    int32_t *po_s = ds_smem + DS_WARPS * E;     // [E] padded offsets
+    int32_t *cbase = po_s + E;                  // [E] this chunk's first row per expert
     __shared__ int warp_sums[32];
-    __shared__ int po_s[SCAN_THREADS];
-    const int e = threadIdx.x;
-    int count = 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < DS_WARPS * E; i += DS_THREADS) wcount[i] = 0;
     griddep_wait();
     griddep_launch_dependents();
-    if (e < E) {
-        for (int c = 0; c < n_chunks; ++c) {
-            int32_t *h = hist + static_cast<int64_t>(c) * E + e;
-            const int v = *h;
-            *h = count;  // chunk base relative to the expert's start
-            count += v;
-        }
-        sizes[e] = count;
+    // this warp's pairs (expert ids and weights) in registers, loaded once
+    // and before the histogram sums so that both latencies overlap
+    constexpr int ROUNDS = PAIRS_PER_WARP / 32;
+    const int64_t wf0 = static_cast<int64_t>(blockIdx.x) * CHUNK + static_cast<int64_t>(warp) * PAIRS_PER_WARP;
+    int ev[ROUNDS];
+    float wv[ROUNDS];
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+        const int64_t f = wf0 + r * 32 + lane;
+        int e = f < n_pairs ? __ldg(idx + f) : -1;
+        ev[r] = (e >= 0 && e < E) ? e : -1;
+        wv[r] = (w && f < n_pairs) ? __ldg(w + f) : 1.0f;
     }
-    const int off = block_exclusive_scan(e < E ? count : 0, warp_sums);
-    // padded size of expert e: ceil((count + 1) / block_m) * block_m
-    const int psize = e < E ? ((count + block_m) / block_m) * block_m : 0;
-    const int poff = block_exclusive_scan(psize, warp_sums);
-    if (e < E) {
-        offsets[e] = off;
-        padded[e] = poff;
-        po_s[e] = poff;
-        for (int c = 0; c < n_chunks; ++c) hist[static_cast<int64_t>(c) * E + e] += off;
+    // totals and this chunk's bases of the experts e = per * tid + i
+    const int per = (E + DS_THREADS - 1) / DS_THREADS;
+    int tot[DS_MAX_PER_THREAD], bas[DS_MAX_PER_THREAD];
+    int my_tot = 0, my_pad = 0;
+#pragma unroll
+    for (int i = 0; i < DS_MAX_PER_THREAD; ++i) {
+        const int e = threadIdx.x * per + i;
+        tot[i] = 0;
+        bas[i] = 0;
+        if (i < per && e < E) {
+#pragma unroll 4
+            for (int c = 0; c < n_chunks; ++c) {
+                const int v = hist[static_cast<int64_t>(c) * E + e];
+                if (c < static_cast<int>(blockIdx.x)) bas[i] += v;
+                tot[i] += v;
+            }
+            my_tot += tot[i];
+            // padded size of expert e: ceil((count + 1) / block_m) * block_m
+            my_pad += ((tot[i] + block_m) / block_m) * block_m;
+        }
+    }
+    int run = block_exclusive_scan(my_tot, warp_sums);
+    int prun = block_exclusive_scan(my_pad, warp_sums);
+#pragma unroll
+    for (int i = 0; i < DS_MAX_PER_THREAD; ++i) {
+        const int e = threadIdx.x * per + i;
+        if (i < per && e < E) {
+            if (blockIdx.x == 0) {
+                sizes[e] = tot[i];
+                offsets[e] = run;
+                padded[e] = prun;
+            }
+            po_s[e] = prun;
+            cbase[e] = run + bas[i];
+            run += tot[i];
+            prun += ((tot[i] + block_m) / block_m) * block_m;
+        }
     }
     __syncthreads();
     // group_idx_for_bx[bx] = last e with bx * block_m >= po[e] (po[0] = 0, increasing)
-    for (int bx = threadIdx.x; bx < m_blocks; bx += SCAN_THREADS) {
+    for (int bx = blockIdx.x * DS_THREADS + threadIdx.x; bx < m_blocks; bx += gridDim.x * DS_THREADS) {
         const long long start = static_cast<long long>(bx) * block_m;
         int lo = 0, hi = E - 1;
         while (lo < hi) {
@@ -123,45 +170,33 @@ __global__ void __launch_bounds__(SCAN_THREADS)
         gidx[bx] = lo;
         if (ready) ready[bx] = 0;
     }
-    if (ready && threadIdx.x == 0) ready[m_blocks] = 0;  // the expert MLP's tile counter
-}
+    if (ready && blockIdx.x == 0 && threadIdx.x == 0) ready[m_blocks] = 0;  // the expert MLP's tile counter
 
-__global__ void __launch_bounds__(DS_THREADS)
-    dispatch_scatter_kernel(const int32_t *__restrict__ idx, const float *__restrict__ w,
-                            int64_t n_pairs, int k, int E, const int32_t *__restrict__ bases,
-                            int32_t *__restrict__ sorted_tok, float *__restrict__ sorted_w,
-                            int32_t *__restrict__ pos) {
-    extern __shared__ int32_t wcount[];  // [DS_WARPS][E]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < DS_WARPS * E; i += DS_THREADS) wcount[i] = 0;
-    griddep_wait();
-    griddep_launch_dependents();
-    __syncthreads();
-    const int64_t wf0 = static_cast<int64_t>(blockIdx.x) * CHUNK + static_cast<int64_t>(warp) * PAIRS_PER_WARP;
     int32_t *mine = wcount + warp * E;
+    const unsigned lt_mask = (1u << lane) - 1u;
     // pass 1: per-warp expert counts
-    for (int r = 0; r < PAIRS_PER_WARP; r += 32) {
-        const int64_t f = wf0 + r + lane;
-        const int e = f < n_pairs ? __ldg(idx + f) : -1;
-        if (e >= 0 && e < E) atomicAdd(&mine[e], 1);
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+        const unsigned peers = __match_any_sync(0xffffffffu, ev[r]);
+        if (ev[r] >= 0 && (peers & lt_mask) == 0) mine[ev[r]] += __popc(peers);
+        __syncwarp();
     }
     __syncthreads();
     // warp starts per expert: chunk base + counts of the earlier warps
     for (int e = threadIdx.x; e < E; e += DS_THREADS) {
-        int run = __ldg(bases + static_cast<int64_t>(blockIdx.x) * E + e);
+        int r0 = cbase[e];
         for (int wv = 0; wv < DS_WARPS; ++wv) {
             const int c = wcount[wv * E + e];
-            wcount[wv * E + e] = run;
-            run += c;
+            wcount[wv * E + e] = r0;
+            r0 += c;
         }
     }
     __syncthreads();
     // pass 2: stable ranks inside the warp, 32 pairs at a time in ascending f
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int r = 0; r < PAIRS_PER_WARP; r += 32) {
-        const int64_t f = wf0 + r + lane;
-        int e = f < n_pairs ? __ldg(idx + f) : -1;
-        if (e >= E) e = -1;
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+        const int64_t f = wf0 + r * 32 + lane;
+        const int e = ev[r];
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         int row = 0;
         if (e >= 0) row = mine[e] + __popc(peers & lt_mask);
@@ -170,7 +205,7 @@ __global__ void __launch_bounds__(DS_THREADS)
         __syncwarp();
         if (e >= 0) {
             sorted_tok[row] = static_cast<int32_t>(f / k);
-            sorted_w[row] = w ? __ldg(w + f) : 1.0f;
+            sorted_w[row] = wv[r];
             pos[f] = row;
         }
     }
@@ -309,25 +344,22 @@ cudaError_t launch_dispatch(const int32_t *topk_idx, const float *topk_w, int64_
                                    n_pairs, static_cast<int>(E), hist);
         if (e != cudaSuccess) return e;
     }
-    cudaError_t e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(SCAN_THREADS), 0, stream, hist,
-                               static_cast<int>(n_chunks), static_cast<int>(E),
-                               static_cast<int>(block_m), sizes, offsets, padded, gidx,
-                               static_cast<int>(m_blocks), ready);
-    if (e != cudaSuccess || n_chunks == 0) return e;
-    const size_t smem = static_cast<size_t>(DS_WARPS) * E * 4;
+    const size_t smem = static_cast<size_t>(DS_WARPS + 2) * E * 4;
     static std::atomic<size_t> attr_bytes[64];  // zero-initialised; several host threads may launch
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     if (smem > 48 * 1024 && (dev < 0 || dev >= 64 || attr_bytes[dev] < smem)) {
-        e = cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
+        cudaError_t e = cudaFuncSetAttribute(dispatch_scan_scatter_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_bytes[dev] = smem;
     }
-    return launch_pdl(dispatch_scatter_kernel, dim3(static_cast<unsigned>(n_chunks)), dim3(DS_THREADS),
-                      smem, stream, topk_idx, topk_w, n_pairs, static_cast<int>(k),
-                      static_cast<int>(E), static_cast<const int32_t *>(hist), sorted_token_idx,
-                      sorted_row_weight, pos);
+    // one CTA per chunk (one CTA writes the tables when there are no pairs)
+    const unsigned grid = static_cast<unsigned>(n_chunks > 0 ? n_chunks : 1);
+    return launch_pdl(dispatch_scan_scatter_kernel, dim3(grid), dim3(DS_THREADS), smem, stream, topk_idx, topk_w,
+                      n_pairs, static_cast<int>(k), static_cast<int>(E), static_cast<int>(block_m),
+                      static_cast<const int32_t *>(hist), static_cast<int>(n_chunks), sizes, offsets, padded,
+                      gidx, static_cast<int>(m_blocks), ready, sorted_token_idx, sorted_row_weight, pos);
 }
 
 }  // namespace moe
