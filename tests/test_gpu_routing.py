@@ -180,7 +180,10 @@ def test_dispatch_tables_bit_exact(oracle, T, k, E, skew):
 @pytest.mark.parametrize("T,k,E,d_h,dtype", [(4096, 8, 256, 7168, "bf16"),  # the prefill shape
                                              (301, 3, 17, 256, "f16"),
                                              (70, 32, 40, 512, "f32"),      # k at its limit
-                                             (5, 1, 3, 64, "bf16")])
+                                             (5, 1, 3, 64, "bf16"),
+                                             (20000, 2, 9, 64, "bf16"),     # two tokens per warp, both buffers
+                                             (3, 2, 4, 24576, "f32"),       # 96 KB rows: one warp per CTA
+                                             (9, 2, 5, 26624, "f32")])      # 104 KB rows: the register form
 def test_gather_rows_by_token_bit_exact(oracle, T, k, E, d_h, dtype):
     """The token-order gather moe_forward runs gives the row-order gather's
     rows bit for bit: against the oracle's gather with the same dispatch's
@@ -193,8 +196,10 @@ def test_gather_rows_by_token_bit_exact(oracle, T, k, E, d_h, dtype):
     td = workloads.torch_dtype(dtype)
     x = torch.randn((T, d_h), generator=torch.Generator().manual_seed(T), dtype=torch.float32).to(td).to(dev)
     pos = torch.from_numpy(tab["token_topk_to_pos"].reshape(T, k).copy()).to(dev)
-    a = binding.moe_gather_rows_by_token(x, pos, T * k)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    a = binding.moe_gather_rows_by_token(x, pos, T * k, err=err)
     torch.cuda.synchronize()
+    assert int(err.item()) == 0
     want = oracle.gather_rows(bits(x), tab["sorted_token_idx"], dtype)
     assert_bits_equal(bits(a), want, "rows gathered in token order")
     # drop one pair: its row is not written
