@@ -54,12 +54,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 def kernels_per_step(cfg) -> int:
-    """Kernels of one forward: gate (+ a top-k kernel when E > 64), dispatch
-    (one kernel up to 16384 pairs and 256 experts, else three), gather (none
-    when T <= 64: the expert MLP gathers its rows itself), the expert MLP
-    (both GEMM stages in one launch) and the combine."""
-    gate = 1 if cfg.n_experts <= 64 else 2
-    dispatch = 1 if cfg.T * cfg.top_k <= 16384 and cfg.n_experts <= 256 else 3
+    """Kernels of one forward: gate (from 1024 tokens the tensor-core logits
+    and the selection; below, the CUDA-core gate plus a top-k kernel when
+    E > 64), dispatch (one kernel up to 16384 pairs and 256 experts, else
+    two), gather (none when T <= 64: the expert MLP gathers its rows itself),
+    the expert MLP (both GEMM stages in one launch) and the combine."""
+    gate = 2 if cfg.T >= 1024 and cfg.d_hidden % 64 == 0 else (1 if cfg.n_experts <= 64 else 2)
+    dispatch = 1 if cfg.T * cfg.top_k <= 16384 and cfg.n_experts <= 256 else 2
     gather = 0 if cfg.T <= 64 else 1
     return gate + dispatch + gather + 2
 
