@@ -46,11 +46,15 @@ namespace {
 constexpr int GT_BM = 128;       // tokens per tile (MMA M)
 constexpr int GT_BN = 256;       // experts per tile (MMA N)
 constexpr int GT_BK = 64;        // 64 x 2 B = one 128-byte swizzle row
-constexpr int GT_STAGES = 4;
-constexpr int GT_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+// Two rings: token rows come from DRAM (read once), gate rows from L2 (every
+// token tile reads them), so the token ring is the deeper one.
+constexpr int GT_XS = 6;         // token-row stages (16 KB each)
+constexpr int GT_WS = 3;         // gate-row stages (32 KB each)
+constexpr int GT_THREADS = 192;  // warp 0 TMA (lane 0 token rows, lane 1 gate rows), warp 1 MMA, warps 2-5 epilogue
 constexpr int GT_A_BYTES = GT_BM * GT_BK * 2;
 constexpr int GT_B_BYTES = GT_BN * GT_BK * 2;
-constexpr int GT_SMEM = 1024 + GT_STAGES * (GT_A_BYTES + GT_B_BYTES) + 256;
+constexpr int GT_SMEM = 1024 + GT_XS * GT_A_BYTES + GT_WS * GT_B_BYTES + 256;
+static_assert(GT_SMEM <= 227 * 1024, "shared memory per CTA");
 constexpr int GT_MAX_SPLITS = 8;
 constexpr int SEL_WARPS = 4;     // warps (tokens) of a select CTA
 constexpr int SEL_G = 3;         // candidates recomputed together by a warp
@@ -110,25 +114,33 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     const uint32_t raw_u32 = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);
     uint8_t *sA = smem;
-    uint8_t *sB = smem + GT_STAGES * GT_A_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + GT_STAGES * GT_B_BYTES);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * GT_STAGES + 1);
+    uint8_t *sB = smem + GT_XS * GT_A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + GT_WS * GT_B_BYTES);
+    constexpr int NBARS = 2 * GT_XS + 2 * GT_WS + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    static_assert(NBARS * 8 + 8 <= 256, "barrier area");
     const uint32_t bar0 = smem_u32(bars);
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (GT_STAGES + s); };
-    const uint32_t acc_bar = bar0 + 8u * (2 * GT_STAGES);
+    auto xfull_bar = [&](int s) { return bar0 + 8u * s; };
+    auto xempty_bar = [&](int s) { return bar0 + 8u * (GT_XS + s); };
+    auto wfull_bar = [&](int s) { return bar0 + 8u * (2 * GT_XS + s); };
+    auto wempty_bar = [&](int s) { return bar0 + 8u * (2 * GT_XS + GT_WS + s); };
+    const uint32_t acc_bar = bar0 + 8u * (2 * GT_XS + 2 * GT_WS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * GT_BM, n0 = blockIdx.y * GT_BN, split = blockIdx.z;
     const int kb0 = split * p.ks;
     const int kb1 = min(p.nk, kb0 + p.ks);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < GT_STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
-            // a stage is free once its MMAs completed (commit) and every
-            // epilogue warp has read its token rows' squares from it
-            mbar_init(empty_bar(s), 1 + 4);
+        for (int s = 0; s < GT_XS; ++s) {
+            mbar_init(xfull_bar(s), 1);
+            // a token stage is free once its MMAs completed (commit) and
+            // every epilogue warp has read its token rows' squares from it
+            mbar_init(xempty_bar(s), 1 + 4);
+        }
+        for (int s = 0; s < GT_WS; ++s) {
+            mbar_init(wfull_bar(s), 1);
+            mbar_init(wempty_bar(s), 1);  // its MMAs completed
         }
         mbar_init(acc_bar, 1);
         *abort_flag = 0;
@@ -148,35 +160,42 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     griddep_launch_dependents();
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------ TMA producer ------------------------------
+        if (lane < 2) {
+            // ------------------------------ TMA producers -----------------------------
+            // lane 0: the token rows (ring of GT_XS); lane 1: the gate rows (GT_WS)
+            const bool xr = lane == 0;
+            const int nst = xr ? GT_XS : GT_WS;
+            const uint32_t bytes = xr ? GT_A_BYTES : GT_B_BYTES;
             int stage = 0;
             uint32_t phase = 0;
             long issued = 0;
             bool ok = true;
             for (int kb = kb0; kb < kb1; ++kb) {
-                if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+                if (!mbar_wait_bounded(xr ? xempty_bar(stage) : wempty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
-                const uint32_t fb = full_bar(stage);
-                mbar_arrive_expect_tx(fb, GT_A_BYTES + GT_B_BYTES);
+                const uint32_t fb = xr ? xfull_bar(stage) : wfull_bar(stage);
+                mbar_arrive_expect_tx(fb, bytes);
                 // rows past T or E read as zero
-                tma_load_2d(smem_u32(sA + stage * GT_A_BYTES), &tm_x, fb, kb * GT_BK, m0);
-                tma_load_2d(smem_u32(sB + stage * GT_B_BYTES), &tm_w, fb, kb * GT_BK, n0);
+                if (xr)
+                    tma_load_2d(smem_u32(sA + stage * GT_A_BYTES), &tm_x, fb, kb * GT_BK, m0);
+                else
+                    tma_load_2d(smem_u32(sB + stage * GT_B_BYTES), &tm_w, fb, kb * GT_BK, n0);
                 ++issued;
-                if (++stage == GT_STAGES) {
+                if (++stage == nst) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) {
                 // let the copies in flight land before shared memory goes away
-                for (long j = 1; j <= GT_STAGES && j <= issued; ++j) {
+                for (long j = 1; j <= nst && j <= issued; ++j) {
                     const long i = issued - j;
-                    const uint32_t bar = full_bar(static_cast<int>(i % GT_STAGES));
+                    const int st = static_cast<int>(i % nst);
+                    const uint32_t bar = xr ? xfull_bar(st) : wfull_bar(st);
                     const unsigned long long t0 = global_timer_ns();
-                    while (!mbar_try_wait(bar, static_cast<uint32_t>((i / GT_STAGES) & 1)))
+                    while (!mbar_try_wait(bar, static_cast<uint32_t>((i / nst) & 1)))
                         if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
                 }
             }
@@ -184,25 +203,31 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------- MMA issuer --------------------------------
-            int stage = 0;
-            uint32_t phase = 0;
+            int xs = 0, ws = 0;
+            uint32_t xphase = 0, wphase = 0;
             bool ok = true;
             for (int kb = kb0; kb < kb1; ++kb) {
-                if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.err)) {
+                if (!mbar_wait_bounded(xfull_bar(xs), xphase, abort_flag, p.err) ||
+                    !mbar_wait_bounded(wfull_bar(ws), wphase, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t a_desc = smem_desc_sw128(smem_u32(sA + stage * GT_A_BYTES));
-                const uint64_t b_desc = smem_desc_sw128(smem_u32(sB + stage * GT_B_BYTES));
+                const uint64_t a_desc = smem_desc_sw128(smem_u32(sA + xs * GT_A_BYTES));
+                const uint64_t b_desc = smem_desc_sw128(smem_u32(sB + ws * GT_B_BYTES));
 #pragma unroll
                 for (int k = 0; k < GT_BK / 16; ++k)
                     tc_mma_f16(tmem_base, a_desc + 2u * k, b_desc + 2u * k, IDESC,
                                (kb > kb0 || k > 0) ? 1u : 0u);
-                tc_commit(empty_bar(stage));
-                if (++stage == GT_STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
+                tc_commit(xempty_bar(xs));
+                tc_commit(wempty_bar(ws));
+                if (++xs == GT_XS) {
+                    xs = 0;
+                    xphase ^= 1u;
+                }
+                if (++ws == GT_WS) {
+                    ws = 0;
+                    wphase ^= 1u;
                 }
             }
             // the accumulator (or, after an abort, the last MMAs) is complete
@@ -237,7 +262,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
             bool ok = true;
             for (int kb = kb0; kb < kb1; ++kb) {
                 int go = 1;
-                if (lane == 0) go = mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.err) ? 1 : 0;
+                if (lane == 0) go = mbar_wait_bounded(xfull_bar(stage), phase, abort_flag, p.err) ? 1 : 0;
                 go = __shfl_sync(0xffffffffu, go, 0);
                 if (!go) {
                     ok = false;
@@ -258,8 +283,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(stage));
-                if (++stage == GT_STAGES) {
+                if (lane == 0) mbar_arrive(xempty_bar(stage));
+                if (++stage == GT_XS) {
                     stage = 0;
                     phase ^= 1u;
                 }
