@@ -62,6 +62,7 @@ constexpr int SEL_U = 4;         // chunks per lane whose loads are in flight to
 
 struct GateTcParams {
     float *part;           // [S, T, E] fp32 partial logits (no bias)
+    int tma_store;         // 1: the partials leave through tm_p (E % 4 == 0)
     float *wnorm;          // [E] |w_e|_2
     float *xss;            // [S, T] sum of x_t^2 over each split's columns
     const uint8_t *wg;     // gate weight [E, d_h], 16-bit elements
@@ -105,10 +106,18 @@ __device__ __forceinline__ float row_sumsq(const uint8_t *row_bytes, int d_h, in
     return ss;
 }
 
+// shared -> global tensor store of one box (3-D map), in the CTA's bulk group
+__device__ __forceinline__ void tma_store_3d(const void *desc, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(desc)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 template <int DT>
 __global__ void __launch_bounds__(GT_THREADS, 1)
     gate_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                   const GateTcParams p) {
+                   const __grid_constant__ CUtensorMap tm_p, const GateTcParams p) {
     constexpr uint32_t IDESC = idesc_f16(DT == kBF16, GT_BM, GT_BN);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -307,29 +316,57 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         int ready = 1;
         if (lane == 0) ready = mbar_wait_bounded(acc_bar, 0, abort_flag, p.err) ? 1 : 0;
         ready = __shfl_sync(0xffffffffu, ready, 0);
+        // every epilogue warp is past its reads of the token stages before
+        // the ring is reused for the staged tile
+        asm volatile("bar.sync 1, 128;" ::: "memory");
         if (ready) {
             tc_fence_after();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-            float *out = p.part + (static_cast<int64_t>(split) * p.T + (t < p.T ? t : 0)) * p.E;
+            if (p.tma_store) {
+                // the tile in the idle ring as GT_BN / 32 boxes of 128 token rows x 32
+                // experts (128-byte rows, 16-byte chunks swizzled by row % 8, as the
+                // store's tensor map reads them; eight rows of a warp's store fill
+                // all banks once)
 #pragma unroll 1
-            for (int c = 0; c < GT_BN / 16; ++c) {
-                uint32_t r[16];
-                tmem_ld16(t_row + c * 16, r);
-                tmem_ld_wait();
-                const int e0 = n0 + c * 16;
-                if (t < p.T && e0 < p.E) {
-                    if (e0 + 16 <= p.E && (p.E & 3) == 0) {
-                        float4 *dst = reinterpret_cast<float4 *>(out + e0);
+                for (int b = 0; b < GT_BN / 32; ++b) {
+                    uint32_t r0[16], r1[16];
+                    tmem_ld16(t_row + b * 32, r0);
+                    tmem_ld16(t_row + b * 32 + 16, r1);
+                    tmem_ld_wait();
+                    uint8_t *rowp = smem + b * (GT_BM * 128) + row * 128;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                                 __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-                    } else {
+                    for (int c = 0; c < 4; ++c) {
+                        *reinterpret_cast<uint4 *>(rowp + ((c ^ (row & 7)) * 16)) =
+                            make_uint4(r0[4 * c], r0[4 * c + 1], r0[4 * c + 2], r0[4 * c + 3]);
+                        *reinterpret_cast<uint4 *>(rowp + (((c + 4) ^ (row & 7)) * 16)) =
+                            make_uint4(r1[4 * c], r1[4 * c + 1], r1[4 * c + 2], r1[4 * c + 3]);
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            } else {
+                float *out = p.part + (static_cast<int64_t>(split) * p.T + (t < p.T ? t : 0)) * p.E;
+#pragma unroll 1
+                for (int c = 0; c < GT_BN / 16; ++c) {
+                    uint32_t r[16];
+                    tmem_ld16(t_row + c * 16, r);
+                    tmem_ld_wait();
+                    const int e0 = n0 + c * 16;
+                    if (t < p.T && e0 < p.E) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             if (e0 + i < p.E) out[e0 + i] = __uint_as_float(r[i]);
                     }
                 }
+            }
+        }
+        if (p.tma_store) {
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // every row staged
+            if (warp == 2 && lane == 0 && ready) {
+                // rows past T (per split) and experts past E are clipped by the map
+                for (int b = 0; b < GT_BN / 32; ++b)
+                    if (n0 + 32 * b < p.E) tma_store_3d(&tm_p, smem_u32(smem + b * (GT_BM * 128)), n0 + 32 * b, m0, split);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
             }
         }
     }
@@ -690,7 +727,19 @@ cudaError_t launch_typed(const void *x, const void *wg, const float *bias, int64
     }
     const dim3 grid(static_cast<unsigned>((T + GT_BM - 1) / GT_BM), static_cast<unsigned>((E + GT_BN - 1) / GT_BN),
                     static_cast<unsigned>(S));
-    cudaError_t e = launch_pdl(gate_tc_kernel<DT>, grid, dim3(GT_THREADS), GT_SMEM, stream, tm_x, tm_w, p);
+    // the partials leave by tensor stores when each token row of them is a
+    // whole number of 16-byte units (E % 4 == 0); [E, T, S] so that the rows
+    // of a tile past T are clipped in every split
+    CUtensorMap tm_p = tm_x;
+    p.tma_store = 0;
+    if (E % 4 == 0) {
+        const uint64_t dp[3] = {static_cast<uint64_t>(E), static_cast<uint64_t>(T), static_cast<uint64_t>(S)};
+        const uint64_t sp[2] = {static_cast<uint64_t>(E) * 4, static_cast<uint64_t>(T) * E * 4};
+        const uint32_t bp[3] = {32, GT_BM, 1};
+        if (encode_tma_map(&tm_p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, part, dp, sp, bp, 1)) p.tma_store = 1;
+        else tm_p = tm_x;
+    }
+    cudaError_t e = launch_pdl(gate_tc_kernel<DT>, grid, dim3(GT_THREADS), GT_SMEM, stream, tm_x, tm_w, tm_p, p);
     if (e != cudaSuccess) return e;
 
     // |logit~ - logit| <= coef * (|x| |w| + |bias|) + 2^-22 |logit~|
