@@ -9,10 +9,13 @@
 // experts whose logits nearly tie.  This path therefore:
 //
 //   1. gate_tc_kernel: logits~ = x W_g^T on the tensor cores (tcgen05, fp32
-//      accumulation, operands by TMA), K split over S CTAs per output tile
-//      (partials [S, T, E]); the otherwise idle epilogue warps also compute
-//      |w_e|_2 for every gate row and, from the token tiles in shared memory,
-//      each split's share of |x_t|^2.
+//      accumulation, operands by TMA through two rings: token rows, read
+//      once from DRAM, in the deeper one; gate rows, re-read from L2 by
+//      every token tile, in the other), K split over S CTAs per output tile
+//      (partials [S, T, E], written by tensor stores from the idle ring);
+//      the otherwise idle epilogue warps also compute |w_e|_2 for every gate
+//      row and, from the token tiles in shared memory, each split's share of
+//      |x_t|^2.
 //   2. gate_select_kernel, one warp per token: sums the partials in a fixed
 //      order, bounds |logit~ - logit| <= delta(t, e) from |x_t|_2 |w_e|_2
 //      (Cauchy-Schwarz on sum |x_j w_j|) and the rounding depth of both
@@ -21,7 +24,8 @@
 //      strictly below k others, so it cannot be selected.  Every candidate's
 //      logit is then recomputed in the fixed order (the same bits as the
 //      CUDA-core gate), and the top-k is chosen among the candidates by
-//      (logit desc, id asc).  Weights: softmax at the selected experts, the
+//      (logit desc, id asc); the k-th lower bound and the top-k are integer
+//      warp reductions on order-preserving keys of the floats.  Weights: softmax at the selected experts, the
 //      denominator over the fixed-order logits of the candidates and the
 //      tensor-core logits of the others (their terms are below the k-th
 //      largest and within delta of exact).
