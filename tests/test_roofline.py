@@ -49,3 +49,19 @@ def test_forward_counts():
     assert f == 2 * 64 * 64 * 2048 + 3_623_878_656 + 2 * 64 * 6 * 2048
     assert roofline.moe_forward_bytes_min(64, 2048, 768, 64, 64, 2) == \
         3 * 64 * 768 * 2048 * 2 + 64 * 2048 * 2 + 2 * 64 * 2048 * 2
+
+
+def test_kernels_per_step_follow_the_launch_structure():
+    """The launch count the bench line claims: prefill (T=4096, 256 experts,
+    top-8) runs the tensor-core logits and the selection, the histogram and
+    the scan-and-scatter dispatch, the gather, the expert MLP and the combine
+    (7); decode (T=64, 64 experts) the fused CUDA-core gate, the one-CTA
+    dispatch, the gathering expert MLP and the combine (4)."""
+    import dataclasses
+    import bench
+    from mixture_experts_routed_gate_gb300 import workloads
+    assert bench.kernels_per_step(workloads.MOE_CONFIGS["prefill"]) == 7
+    assert bench.kernels_per_step(workloads.MOE_CONFIGS["decode"]) == 4
+    # below the tensor-core gate's token count with more than 64 experts: gate + top-k
+    mid = dataclasses.replace(workloads.MOE_CONFIGS["prefill"], batch=1, seq=512)
+    assert bench.kernels_per_step(mid) == 2 + 1 + 1 + 2
